@@ -1,0 +1,96 @@
+"""Load-time requantisation NVFP4 -> sign-symmetric 2-bit planes, and the NVFP4 delta.
+
+README "Frontier MoE on consumer Blackwell (SM120)", §"GLM-5.2 (753B)" ¶1 and
+§"How it fits -- 2-bit experts at FP4 quality" (bullets 1-2, last ¶): the
+loader dequantises modelopt NVFP4 experts exactly and requantises them to a
+sign-symmetric 2-bit codebook; an FP4 "delta" restores NVFP4 precision for
+experts held in the delta cache.  The pages print the levels {-4,-1,1,4};
+this library fixes the codebook q in {-3,-1,+1,+3} (no zero level).
+
+Everything is in units of the tensor's scale_2, where an NVFP4 weight is the
+exact number v = e2m1(code) * e4m3(s4).  Per block b of 16 along K:
+
+  s16[b]  = e4m3 satfinite RNE( max_{k in b} |v_k| / 3 )
+  sign_k  = sign bit of the NVFP4 code (so -0 maps to the negative side)
+  mag_k   = |v_k| >= 2 * s16[b]        (|q| = 3; the tie goes to 3)
+  W2_k    = (sign ? -1 : +1) * (mag ? 3 : 1) * s16[b]          (x scale_2)
+
+Delta (the residual on the same scale_2):
+
+  d_k     = v_k - W2_k                                     (exact in fp64)
+  s4d[b]  = e4m3 satfinite RNE( max_{k in b} |d_k| / 6 )
+  dcode_k = sign(d_k) | e2m1 satfinite RNE(|d_k| / s4d[b]);  a zero
+            magnitude is written as +0, and s4d = 0 gives all +0.
+
+Plane layout: row-major [N, K/32] uint32, bit j of word w holds weight
+k = 32 w + j (least significant bit first); sign bit 1 = negative, mag bit 1 =
+|q| = 3.  Delta codes pack two per byte, low nibble = even k.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .formats import E4M3_POS, e2m1_rne_ratio, e4m3_rne_ratio, e4m3_decode
+from .nvfp4 import dequantize_units, unpack_codes
+
+
+def pack_bits(bits: np.ndarray) -> np.ndarray:
+    """[N, K] of 0/1 -> [N, K/32] uint32, bit j of word w = element 32w + j."""
+    bits = np.asarray(bits, dtype=np.uint64)
+    N, K = bits.shape
+    assert K % 32 == 0
+    b = bits.reshape(N, K // 32, 32)
+    weights = np.uint64(1) << np.arange(32, dtype=np.uint64)
+    return (b * weights).sum(axis=2).astype(np.uint32)
+
+
+def unpack_bits(words: np.ndarray) -> np.ndarray:
+    """[N, K/32] uint32 -> [N, K] uint8 of 0/1."""
+    words = np.asarray(words, dtype=np.uint32)
+    shifts = np.arange(32, dtype=np.uint32)
+    b = (words[..., None] >> shifts) & np.uint32(1)
+    return b.reshape(words.shape[:-1] + (words.shape[-1] * 32,)).astype(np.uint8)
+
+
+def requant_2bit(codes: np.ndarray, s4: np.ndarray, want_delta: bool = True):
+    """One [N, K] NVFP4 matrix (codes [N, K/2], s4 [N, K/16]) -> planes (+ delta).
+
+    Returns dict(sign [N,K/32] u32, mag [N,K/32] u32, s16 [N,K/16] u8) and, if
+    ``want_delta``, also dcodes [N, K/2] u8 and ds4 [N, K/16] u8.
+    """
+    v = dequantize_units(codes, s4)                    # exact fp64, units of scale_2
+    N, K = v.shape
+    av = np.abs(v)
+    bmax = av.reshape(N, K // 16, 16).max(axis=2)
+    s16 = e4m3_rne_ratio(bmax, 3.0)
+    s16v = np.repeat(E4M3_POS[s16.astype(np.int64)], 16, axis=1)
+    sign = (unpack_codes(codes) >> 3).astype(np.uint8)
+    mag = (av >= 2.0 * s16v).astype(np.uint8)
+    out = dict(sign=pack_bits(sign), mag=pack_bits(mag), s16=s16.astype(np.uint8))
+    if want_delta:
+        w2 = np.where(sign == 1, -1.0, 1.0) * np.where(mag == 1, 3.0, 1.0) * s16v
+        d = v - w2                                      # exact: both are short dyadics
+        ad = np.abs(d)
+        dmax = ad.reshape(N, K // 16, 16).max(axis=2)
+        ds4 = e4m3_rne_ratio(dmax, 6.0)
+        step = np.repeat(E4M3_POS[ds4.astype(np.int64)], 16, axis=1)
+        dmag = np.zeros((N, K), dtype=np.uint8)
+        nz = step > 0
+        dmag[nz] = e2m1_rne_ratio(ad[nz], step[nz])
+        dsign = ((d < 0) & (dmag > 0)).astype(np.uint8)
+        dcode = (dsign << 3) | dmag
+        out["dcodes"] = (dcode[:, 0::2] | (dcode[:, 1::2] << 4)).astype(np.uint8)
+        out["ds4"] = ds4.astype(np.uint8)
+    return out
+
+
+def dequant_2bit_units(sign: np.ndarray, mag: np.ndarray, s16: np.ndarray) -> np.ndarray:
+    """2-bit planes -> fp64 weights in units of scale_2."""
+    sb = unpack_bits(sign)
+    mb = unpack_bits(mag)
+    q = np.where(sb == 1, -1.0, 1.0) * np.where(mb == 1, 3.0, 1.0)
+    return q * np.repeat(e4m3_decode(s16), 16, axis=-1)
+
+
+def dequant_2bit(sign, mag, s16, scale_2) -> np.ndarray:
+    return dequant_2bit_units(sign, mag, s16) * np.float64(scale_2)

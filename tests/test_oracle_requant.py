@@ -1,0 +1,199 @@
+"""Pins for oracle.nvfp4 (input quantiser) and oracle.requant (2-bit planes + delta).
+
+Independent references: hand-worked examples under tests/golden/, exhaustive
+nearest-level search with exact rationals, and the invariants the method
+states (never-zero code, sign symmetry, delta reconstruction bound).
+"""
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from oracle import formats as F
+from oracle import nvfp4, requant
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _pack_codes(codes):
+    codes = np.asarray(codes, dtype=np.uint8).reshape(1, -1)
+    return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+
+
+# ------------------------------------------------------------------ NVFP4
+def test_nvfp4_worked_example():
+    g = _load("nvfp4_worked_example.json")
+    w = np.array(g["w"], dtype=np.float32).reshape(1, -1)
+    packed, s4, scale_2 = nvfp4.quantize(w)
+    assert float(scale_2) == g["expect_scale_2"]
+    assert s4.reshape(-1).tolist() == g["expect_s4_codes"]
+    assert nvfp4.unpack_codes(packed).reshape(-1).tolist() == g["expect_codes"]
+
+
+def _brute_nearest(r: Fraction, levels):
+    """Index of the level nearest r; ties -> even index; saturate at the top."""
+    if r >= levels[-1]:
+        return len(levels) - 1
+    best = None
+    for i, v in enumerate(levels):
+        d = abs(r - v)
+        if best is None or d < best[0] or (d == best[0] and i % 2 == 0):
+            best = (d, i)
+    return best[1]
+
+
+def test_nvfp4_bruteforce_small():
+    rng = np.random.default_rng(3)
+    w = (rng.standard_normal((3, 32)) * np.exp2(rng.integers(-8, 4, (3, 1)))).astype(np.float32)
+    packed, s4, scale_2 = nvfp4.quantize(w)
+    amax = Fraction(float(np.max(np.abs(w))))
+    assert Fraction(float(scale_2)) == Fraction(float(np.float32(float(amax) / 2688.0)))
+    sc2 = Fraction(float(scale_2))
+    codes = nvfp4.unpack_codes(packed)
+    for n in range(3):
+        for b in range(2):
+            blk = [Fraction(float(v)) for v in w[n, 16 * b:16 * b + 16]]
+            bm = max(abs(v) for v in blk)
+            s4_ref = _brute_nearest(bm / (6 * sc2), F.E4M3_VALUE_FRAC[:127])
+            assert s4[n, b] == s4_ref
+            step = F.E4M3_VALUE_FRAC[s4_ref] * sc2
+            for j, v in enumerate(blk):
+                m = _brute_nearest(abs(v) / step, F.E2M1_MAG_FRAC) if step > 0 else 0
+                sgn = 8 if np.signbit(w[n, 16 * b + j]) else 0
+                assert codes[n, 16 * b + j] == (sgn | m)
+
+
+def test_nvfp4_error_bound():
+    rng = np.random.default_rng(4)
+    w = (rng.standard_normal((64, 256)) * 0.02).astype(np.float32)
+    packed, s4, scale_2 = nvfp4.quantize(w)
+    deq = nvfp4.dequantize(packed, s4, scale_2)
+    step = np.repeat(F.e4m3_decode(s4), 16, axis=1) * float(scale_2)
+    # half the widest e2m1 gap (between 4 and 6) is 1 step; saturation at 6 adds
+    # at most 6*(RNE excess of s4), also below 1 step for normal s4
+    assert np.all(np.abs(w - deq) <= step + 1e-30)
+
+
+# ------------------------------------------------------------------ requant
+def test_requant_worked_example():
+    g = _load("requant_worked_example.json")
+    codes = _pack_codes(g["codes"])
+    s4 = np.array([[g["s4_code"]]], dtype=np.uint8)
+    assert nvfp4.dequantize_units(codes, s4).reshape(-1).tolist() == g["v"]
+    codes32 = np.concatenate([codes, codes], axis=1)          # planes need K % 32 == 0
+    s4_32 = np.concatenate([s4, s4], axis=1)
+    out = requant.requant_2bit(codes32, s4_32)
+    assert out["s16"].reshape(-1).tolist() == [g["expect_s16_code"]] * 2
+    w2 = requant.dequant_2bit_units(out["sign"], out["mag"], out["s16"]).reshape(-1)[:16]
+    assert (w2 / g["expect_s16"]).tolist() == g["expect_q"]
+    v = np.array(g["v"], dtype=np.float64)
+    assert (v - w2).tolist() == g["expect_delta"]
+    assert out["ds4"].reshape(-1).tolist() == [g["expect_ds4_code"]] * 2
+    dcodes = nvfp4.unpack_codes(out["dcodes"]).reshape(-1)[:16]
+    assert dcodes.tolist() == g["expect_dcodes"]
+    assert (F.e2m1_decode(dcodes)).tolist() == g["expect_dcode_values"]
+
+
+def _random_nvfp4(rng, N, K, zero_frac=0.05):
+    codes = rng.integers(0, 16, (N, K), dtype=np.uint8)
+    codes[rng.random((N, K)) < zero_frac] = 0
+    s4 = rng.integers(0, 127, (N, K // 16), dtype=np.uint8)     # finite, non-negative
+    s4[rng.random((N, K // 16)) < 0.05] = 0
+    return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8), s4
+
+
+def test_requant_bruteforce_levels():
+    """s16 is the nearest e4m3 to max|v|/3 and q the nearest of {s16, 3 s16} (ties -> 3)."""
+    rng = np.random.default_rng(5)
+    codes, s4 = _random_nvfp4(rng, 6, 64)
+    out = requant.requant_2bit(codes, s4)
+    c4 = nvfp4.unpack_codes(codes)
+    sign = requant.unpack_bits(out["sign"])
+    mag = requant.unpack_bits(out["mag"])
+    for n in range(6):
+        for b in range(4):
+            vals = [F.E2M1_MAG_FRAC[c & 7] * (-1 if c & 8 else 1) * F.E4M3_VALUE_FRAC[s4[n, b]]
+                    for c in c4[n, 16 * b:16 * b + 16]]
+            bm = max(abs(v) for v in vals)
+            s16_ref = _brute_nearest(bm / 3, F.E4M3_VALUE_FRAC[:127])
+            assert out["s16"][n, b] == s16_ref
+            s = F.E4M3_VALUE_FRAC[s16_ref]
+            for j, v in enumerate(vals):
+                k = 16 * b + j
+                to1, to3 = abs(abs(v) - s), abs(abs(v) - 3 * s)
+                assert mag[n, k] == (1 if to3 <= to1 else 0)
+                assert sign[n, k] == (c4[n, k] >> 3)
+
+
+def test_requant_never_zero_and_error_bound():
+    rng = np.random.default_rng(6)
+    codes, s4 = _random_nvfp4(rng, 32, 128)
+    out = requant.requant_2bit(codes, s4)
+    s16v = np.repeat(F.e4m3_decode(out["s16"]), 16, axis=1)
+    w2 = requant.dequant_2bit_units(out["sign"], out["mag"], out["s16"])
+    ok = s16v > 0
+    q = w2[ok] / s16v[ok]
+    assert set(np.unique(q).tolist()) <= {-3.0, -1.0, 1.0, 3.0}
+    v = nvfp4.dequantize_units(codes, s4)
+    bmax = np.repeat(np.abs(v).reshape(32, -1, 16).max(axis=2), 16, axis=1)
+    unclipped = bmax / 3 <= 448
+    assert np.all(np.abs(v - w2)[unclipped] <= s16v[unclipped])
+
+
+def test_requant_sign_symmetry():
+    rng = np.random.default_rng(7)
+    codes, s4 = _random_nvfp4(rng, 16, 96)
+    neg = codes ^ np.uint8(0x88)                       # flip both nibbles' sign bits
+    a = requant.requant_2bit(codes, s4)
+    b = requant.requant_2bit(neg, s4)
+    assert np.array_equal(b["sign"], ~a["sign"])
+    assert np.array_equal(b["mag"], a["mag"])
+    assert np.array_equal(b["s16"], a["s16"])
+    assert np.array_equal(b["ds4"], a["ds4"])
+    ca, cb = nvfp4.unpack_codes(a["dcodes"]), nvfp4.unpack_codes(b["dcodes"])
+    nz = (ca & 7) > 0
+    assert np.array_equal(cb[nz], ca[nz] ^ 8)
+    assert np.all(cb[~nz] == 0) and np.all(ca[~nz] == 0)
+
+
+def test_delta_reconstruction_bound():
+    """W_2bit + deq(delta) reproduces W_nvfp4 to NVFP4 rounding of the residual."""
+    rng = np.random.default_rng(8)
+    codes, s4 = _random_nvfp4(rng, 32, 128)
+    out = requant.requant_2bit(codes, s4)
+    v = nvfp4.dequantize_units(codes, s4)
+    w2 = requant.dequant_2bit_units(out["sign"], out["mag"], out["s16"])
+    dq = nvfp4.dequantize_units(out["dcodes"], out["ds4"])
+    d = v - w2
+    err = np.abs(d - dq)
+    step = np.repeat(F.e4m3_decode(out["ds4"]), 16, axis=1)
+    dmax = np.repeat(np.abs(d).reshape(32, -1, 16).max(axis=2), 16, axis=1)
+    bound = np.maximum(step, dmax - 6 * step)
+    assert np.all(err <= bound)
+    normal = step >= 2.0 ** -6
+    assert np.all(err[normal] <= step[normal])
+    # exact where the residual is itself on the delta grid
+    on_grid = np.isin(np.abs(d) / np.where(step > 0, step, 1), F.E2M1_MAG) & (step > 0)
+    assert np.all(err[on_grid] == 0)
+
+
+def test_requant_realistic_weights_roundtrip():
+    """NVFP4-quantised N(0, 0.02) weights: the delta restores them almost exactly."""
+    rng = np.random.default_rng(9)
+    w = (rng.standard_normal((64, 256)) * 0.02).astype(np.float32)
+    codes, s4, scale_2 = nvfp4.quantize(w)
+    out = requant.requant_2bit(codes, s4)
+    v = nvfp4.dequantize(codes, s4, scale_2)
+    w2 = requant.dequant_2bit(out["sign"], out["mag"], out["s16"], scale_2)
+    dq = nvfp4.dequantize(out["dcodes"], out["ds4"], scale_2)
+    rel2 = np.linalg.norm(v - w2) / np.linalg.norm(v)
+    relf = np.linalg.norm(v - w2 - dq) / np.linalg.norm(v)
+    assert 0.2 < rel2 < 0.6          # 2-bit alone is coarse
+    assert relf < 0.1 * rel2         # the FP4 residual recovers >90% of it
