@@ -1,0 +1,28 @@
+"""GB300 (sm_103a) MoE expert layer over sign-symmetric 2-bit experts with an NVFP4 delta.
+
+Thin Python binding of the C ABI in ``include/moet.h`` (libmoet.so).  Every
+function here only checks and marshals arguments; all computation runs in the
+library's CUDA kernels.  PyTorch is used for device memory and streams only.
+There is no CPU fallback: importing this package without the built library,
+or calling it on tensors that are not on a CUDA device, raises.
+
+Entry points (same names as the C ABI without the ``moet_`` prefix):
+  quantize_nvfp4   fp32 weights -> NVFP4 (codes, s4, scale_2)
+  requant_2bit     NVFP4 -> 2-bit sign/magnitude planes + s16 (+ delta)
+  route_topk       logits -> top-k ids/weights, expert offsets, permutation
+  moe_forward      the MoE layer y = sum_j w_j FFN_e(x) on the 2-bit planes
+"""
+from ._lib import (  # noqa: F401
+    MoetError,
+    Planes,
+    DeltaPool,
+    lib,
+    lib_path,
+    status_string,
+    last_device_error,
+    quantize_nvfp4,
+    requant_2bit,
+    route_topk,
+    forward_workspace_size,
+    moe_forward,
+)

@@ -1,0 +1,534 @@
+// MoE expert-layer forward over 2-bit sign/magnitude planes with the NVFP4 delta.
+//
+// README "Frontier MoE on consumer Blackwell (SM120)", "How it fits -- 2-bit
+// experts at FP4 quality", bullet 2: decode streams the 2-bit experts (an FP4
+// read is twice the bytes); experts in the delta cache add the FP4 residual
+// for tokens the confidence gate flags.
+//
+// Launch chain on the caller's stream (no host synchronisation):
+//   1. prologue   chunk list (expert, first pair, count<=64) from the expert
+//                 offsets; per-token power-of-two activation scales; zeroes
+//                 the per-pair |h| maxima.
+//   2. fc<FC1>    h = SiLU(x Wg^T) * (x Wu^T) per routed pair (+ delta on gated
+//                 pairs of cached experts), fp32, bucketed order.
+//   3. fc<FC2>    o_p = w_p * h_p W2^T (+ delta), fp32, in pair order t*k+j.
+//   4. combine    y_t = sum_j o_{t*k+j} in a fixed order, rounded to bf16.
+//
+// Inner product engine (fc kernels).  A warp owns a 16-row MMA tile of one
+// expert's weight matrix (FC1: 8 gate rows + the 8 matching up rows, so
+// SiLU*mul happens in registers; FC2: 16 output rows) and streams its 2-bit
+// planes with 128-bit read-only loads, 128 weights per row per step.  The
+// codes are expanded in registers to f16 A fragments of mma.sync.m16n8k16:
+// f16 +-1 and +-3 have a zero low byte, so one PRMT over a 4-entry byte
+// table turns two 2-bit codes into one f16x2 register.  K is permuted inside
+// each 16-block so that every lane's codes sit at a fixed stride in the
+// plane word; the activations (B operand, staged once per CTA in shared
+// memory as f16) carry the same permutation.  One MMA covers exactly one
+// 16-weight scale block, and its fp32 result is scaled by that block's s16
+// and accumulated in fp32.  Activations reach f16 through a power-of-two
+// scale per row (token or pair) so that the conversion from bf16 is exact
+// except for values 2^31 below the row maximum.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+
+namespace moet {
+
+constexpr int kChunk = 64;          // pairs per work item
+constexpr int kThreads = 256;       // 8 warps
+constexpr int kSmemBudget = 96 * 1024;
+constexpr uint32_t kCodeLut = 0xC242BC3Cu;  // f16 high bytes of +1, -1, +3, -3
+
+struct WsLayout {
+  size_t hdr, tok_scale, hmax, chunks, h, o, total;
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+__host__ __device__ inline int max_chunks(int T, int E, int k) {
+  const long long pairs = (long long)T * k;
+  return (int)((pairs < E ? pairs : E) + (pairs + kChunk - 1) / kChunk);
+}
+
+inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
+  WsLayout L;
+  const size_t pairs = (size_t)T * k;
+  size_t off = 0;
+  L.hdr = off;       off += align256(16);
+  L.tok_scale = off; off += align256(sizeof(float) * T);
+  L.hmax = off;      off += align256(sizeof(unsigned) * pairs);
+  L.chunks = off;    off += align256(sizeof(int4) * (size_t)max_chunks(T, E, k));
+  L.h = off;         off += align256(sizeof(float) * pairs * I);
+  L.o = off;         off += align256(sizeof(float) * pairs * H);
+  L.total = off;
+  return L;
+}
+
+// power-of-two multiplier that brings max|row| into [2^14, 2^15)
+__device__ __forceinline__ float pow2_scale_for(float amax) {
+  if (!(amax > 0.0f) || !isfinite(amax)) return 1.0f;
+  int e;
+  frexpf(amax, &e);          // amax = f * 2^e, f in [0.5, 1)
+  int s = 15 - e;            // amax * 2^s in [2^14, 2^15)
+  s = s > 100 ? 100 : (s < -100 ? -100 : s);
+  return ldexpf(1.0f, s);
+}
+
+// ---------------------------------------------------------------- prologue
+__global__ void __launch_bounds__(kThreads) prologue_kernel(
+    int T, int H, int E, int k, const uint16_t* __restrict__ x, const int32_t* __restrict__ offsets,
+    int* __restrict__ hdr, float* __restrict__ tok_scale, unsigned* __restrict__ hmax,
+    int4* __restrict__ chunks) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (blockIdx.x == 0) {
+    if (warp != 0) return;
+    bool ok = __ldg(offsets) == 0 && __ldg(offsets + E) == T * k;
+    int running = 0;
+    for (int c0 = 0; c0 < E; c0 += 32) {
+      const int e = c0 + lane;
+      int n = 0;
+      if (e < E) {
+        n = __ldg(offsets + e + 1) - __ldg(offsets + e);
+        if (n < 0) { ok = false; n = 0; }
+      }
+      const int nch = (n + kChunk - 1) / kChunk;
+      int incl = nch;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int first = running + incl - nch;
+      for (int c = 0; c < nch; ++c) {
+        const int cnt = min(kChunk, n - c * kChunk);
+        chunks[first + c] = make_int4(e, c * kChunk, cnt, 0);
+      }
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    if (lane == 0) {
+      if (!ok) record_error(MOET_ERR_DEVICE_INDEX);
+      hdr[0] = ok ? running : 0;
+      hdr[1] = ok ? 1 : 0;
+    }
+    return;
+  }
+  // blocks >= 1: one warp per token, plus zeroing of hmax
+  const int gw = (blockIdx.x - 1) * (kThreads / 32) + warp;
+  const int nthreads = (gridDim.x - 1) * kThreads;
+  for (int i = (blockIdx.x - 1) * kThreads + tid; i < T * k; i += nthreads) hmax[i] = 0u;
+  if (gw >= T) return;
+  const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)gw * H);
+  float m = 0.0f;
+  for (int i = lane; i < H / 8; i += 32) {
+    const uint4 v = __ldg(row + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      m = fmaxf(m, fabsf(__uint_as_float(w[q] << 16)));
+      m = fmaxf(m, fabsf(__uint_as_float(w[q] & 0xFFFF0000u)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) tok_scale[gw] = pow2_scale_for(m);
+}
+
+// ---------------------------------------------------------------- fc kernels
+// Staged layout of one 16-element K-block of an activation row: the lane with
+// c = lane & 3 reads halves 4c..4c+3 = (x_c, x_{c+8}, x_{c+4}, x_{c+12}),
+// which are the B-fragment rows 2c, 2c+1, 2c+8, 2c+9 of mma.m16n8k16; the
+// A fragments built from the planes use the same order.
+
+struct FcArgs {
+  int T, H, I, E, k, K, N;
+  const uint16_t* x;
+  const float* h_in;
+  const int32_t* offsets;
+  const int32_t* perm;
+  const float* topk_w;
+  const uint32_t* sign;
+  const uint32_t* mag;
+  const uint8_t* s16;
+  const float* scale_2;
+  const int32_t* delta_slot;
+  int n_slots;
+  const uint8_t* dcodes;
+  const uint8_t* ds4;
+  const uint8_t* gate;
+  const int* hdr;
+  const int4* chunks;
+  const float* tok_scale;
+  unsigned* hmax;
+  float* out;        // FC1: h [pairs, I] bucketed; FC2: o [pairs, H] by pair id
+  int ks;            // K slice staged per pass (multiple of 128)
+};
+
+template <bool FC1, int NT>
+__global__ void __launch_bounds__(kThreads, 2) fc_kernel(const FcArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, c = lane & 3;
+  if ((int)blockIdx.y >= a.hdr[0]) return;
+  const int4 ch = a.chunks[blockIdx.y];
+  const int e = ch.x, count = ch.z;
+  const int pos0 = __ldg(a.offsets + e) + ch.y;
+  const int K = a.K;
+  const int pitch = a.ks + 16;                           // halves per staged row
+  __half* xs = reinterpret_cast<__half*>(smem_raw);      // [NT*8][pitch]
+  float* rscale = reinterpret_cast<float*>(smem_raw + sizeof(__half) * NT * 8 * pitch);  // [NT*8]
+  float* gatef = rscale + NT * 8;                        // [NT*8]
+  int* rsrc = reinterpret_cast<int*>(gatef + NT * 8);    // [NT*8] token (FC1) or pair id (FC2)
+  __shared__ int any_gated;
+
+  int slot = -1;
+  if (a.delta_slot != nullptr && a.gate != nullptr) {
+    slot = __ldg(a.delta_slot + e);
+    if (slot >= a.n_slots) { record_error(MOET_ERR_DEVICE_INDEX); slot = -1; }
+  }
+  if (tid == 0) any_gated = 0;
+  __syncthreads();
+  if (tid < NT * 8) {
+    float sc = 0.0f, gf = 0.0f;
+    int src = -1;
+    if (tid < count) {
+      const int p = __ldg(a.perm + pos0 + tid);
+      const int tok = p / a.k;
+      if (p < 0 || p >= a.T * a.k) {
+        record_error(MOET_ERR_DEVICE_INDEX);
+      } else {
+        src = FC1 ? tok : p;
+        if (FC1) {
+          sc = __ldg(a.tok_scale + tok);
+        } else {
+          sc = pow2_scale_for(__uint_as_float(a.hmax[pos0 + tid]));
+        }
+        if (slot >= 0 && __ldg(a.gate + tok)) { gf = 1.0f; any_gated = 1; }
+      }
+    }
+    rscale[tid] = sc;
+    gatef[tid] = gf;
+    rsrc[tid] = src;
+  }
+  __syncthreads();
+  const bool do_delta = slot >= 0 && any_gated;
+  const int ntiles = (count + 7) >> 3;
+
+  // rows of this warp
+  int row_g, row_u;
+  if (FC1) {
+    const int i0 = blockIdx.x * 64 + warp * 8;
+    row_g = i0 + g;
+    row_u = a.I + i0 + g;
+  } else {
+    const int r0 = blockIdx.x * 128 + warp * 16;
+    row_g = r0 + g;
+    row_u = r0 + g + 8;
+  }
+  const size_t wpr = (size_t)K / 32, bpr = (size_t)K / 16;
+  const uint32_t* Sg = a.sign + ((size_t)e * a.N + row_g) * wpr;
+  const uint32_t* Mg = a.mag + ((size_t)e * a.N + row_g) * wpr;
+  const uint32_t* Su = a.sign + ((size_t)e * a.N + row_u) * wpr;
+  const uint32_t* Mu = a.mag + ((size_t)e * a.N + row_u) * wpr;
+  const uint8_t* Qg = a.s16 + ((size_t)e * a.N + row_g) * bpr;
+  const uint8_t* Qu = a.s16 + ((size_t)e * a.N + row_u) * bpr;
+  const uint8_t* Dg = nullptr; const uint8_t* Du = nullptr;
+  const uint8_t* DQg = nullptr; const uint8_t* DQu = nullptr;
+  if (do_delta) {
+    Dg = a.dcodes + ((size_t)slot * a.N + row_g) * (K / 2);
+    Du = a.dcodes + ((size_t)slot * a.N + row_u) * (K / 2);
+    DQg = a.ds4 + ((size_t)slot * a.N + row_g) * bpr;
+    DQu = a.ds4 + ((size_t)slot * a.N + row_u) * bpr;
+  }
+
+  float acc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
+
+  for (int k0 = 0; k0 < K; k0 += a.ks) {
+    const int k1 = min(K, k0 + a.ks);
+    const int nblk = (k1 - k0) / 16;
+    __syncthreads();                                     // previous slice fully consumed
+    // ---- stage activations of this slice: one 16-block per item
+    for (int it = tid; it < NT * 8 * nblk; it += kThreads) {
+      const int r = it / nblk, b = it - r * nblk;
+      float v[16];
+      const int src = rsrc[r];
+      if (src >= 0) {
+        const float sc = rscale[r];
+        if (FC1) {
+          const uint4* p = reinterpret_cast<const uint4*>(a.x + (size_t)src * a.H + k0 + 16 * b);
+          const uint4 u0 = __ldg(p), u1 = __ldg(p + 1);
+          const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            v[2 * q] = __uint_as_float(w[q] << 16) * sc;
+            v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u) * sc;
+          }
+        } else {
+          const float4* p = reinterpret_cast<const float4*>(a.h_in + (size_t)(pos0 + r) * a.I + k0 + 16 * b);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 f = p[q];
+            v[4 * q] = f.x * sc; v[4 * q + 1] = f.y * sc; v[4 * q + 2] = f.z * sc; v[4 * q + 3] = f.w * sc;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+      }
+      // staged order: (x0,x8) (x4,x12) (x1,x9) (x5,x13) (x2,x10) (x6,x14) (x3,x11) (x7,x15)
+      uint32_t wv[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int j = (q >> 1) + 4 * (q & 1);
+        const __half2 hp = __floats2half2_rn(v[j], v[j + 8]);
+        wv[q] = *reinterpret_cast<const uint32_t*>(&hp);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)r * pitch + 16 * b);
+      dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+    }
+    __syncthreads();
+
+    // ---- 2-bit pass over the slice, 128 weights per row per step
+    const __half* xrow = xs + (size_t)g * pitch + 4 * c;
+    for (int kk = k0; kk < k1; kk += 128) {
+      const uint4 sg = ldg_nc_v4(Sg + kk / 32), mg = ldg_nc_v4(Mg + kk / 32);
+      const uint4 su = ldg_nc_v4(Su + kk / 32), mu = ldg_nc_v4(Mu + kk / 32);
+      const uint2 qg = ldg_nc_v2(Qg + kk / 16), qu = ldg_nc_v2(Qu + kk / 16);
+      const uint32_t SG[4] = {sg.x, sg.y, sg.z, sg.w}, MG[4] = {mg.x, mg.y, mg.z, mg.w};
+      const uint32_t SU[4] = {su.x, su.y, su.z, su.w}, MU[4] = {mu.x, mu.y, mu.z, mu.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t cg = ((SG[q] >> c) & 0x11111111u) | (((MG[q] >> c) & 0x11111111u) << 1);
+        const uint32_t cu = ((SU[q] >> c) & 0x11111111u) | (((MU[q] >> c) & 0x11111111u) << 1);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const uint32_t xg = hh ? (cg >> 16) : cg, xu = hh ? (cu >> 16) : cu;
+          const uint32_t a0 = prmt(kCodeLut, 0u, (xg << 4) + 0x0404u);
+          const uint32_t a2 = prmt(kCodeLut, 0u, xg + 0x0404u);
+          const uint32_t a1 = prmt(kCodeLut, 0u, (xu << 4) + 0x0404u);
+          const uint32_t a3 = prmt(kCodeLut, 0u, xu + 0x0404u);
+          const int bi = 2 * q + hh;                       // block inside the 128-step
+          const uint32_t qgw = bi < 4 ? qg.x : qg.y, quw = bi < 4 ? qu.x : qu.y;
+          const float sgf = e4m3_to_f32(qgw >> (8 * (bi & 3)));
+          const float suf = e4m3_to_f32(quw >> (8 * (bi & 3)));
+          const int lb = (kk - k0) / 16 + bi;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            if (nt < ntiles) {
+              const uint2 bv = *reinterpret_cast<const uint2*>(xrow + (size_t)nt * 8 * pitch + 16 * lb);
+              float d[4];
+              mma_f16_16816(d, a0, a1, a2, a3, bv.x, bv.y);
+              acc[nt][0] = fmaf(sgf, d[0], acc[nt][0]);
+              acc[nt][1] = fmaf(sgf, d[1], acc[nt][1]);
+              acc[nt][2] = fmaf(suf, d[2], acc[nt][2]);
+              acc[nt][3] = fmaf(suf, d[3], acc[nt][3]);
+            }
+          }
+        }
+      }
+    }
+
+    // ---- delta pass (gated pairs of a cached expert), 32 weights per row per step
+    if (do_delta) {
+      for (int kk = k0; kk < k1; kk += 32) {
+        const uint4 dg = ldg_nc_v4(Dg + kk / 2), du = ldg_nc_v4(Du + kk / 2);
+        const uint32_t sq_g = *reinterpret_cast<const uint16_t*>(DQg + kk / 16);
+        const uint32_t sq_u = *reinterpret_cast<const uint16_t*>(DQu + kk / 16);
+        const uint32_t DG[4] = {dg.x, dg.y, dg.z, dg.w}, DU[4] = {du.x, du.y, du.z, du.w};
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          // weights c, c+8 -> a0/a1 ; c+4, c+12 -> a2/a3 (same permutation as above)
+          const uint32_t lg = DG[2 * hh] >> (4 * c), hg = DG[2 * hh + 1] >> (4 * c);
+          const uint32_t lu = DU[2 * hh] >> (4 * c), hu = DU[2 * hh + 1] >> (4 * c);
+          const uint32_t tg = (lg & 0x000F000Fu) | ((hg & 0x000F000Fu) << 4);
+          const uint32_t tu = (lu & 0x000F000Fu) | ((hu & 0x000F000Fu) << 4);
+          const uint32_t a0 = e2m1x2_to_f16x2(tg & 0xFFu), a2 = e2m1x2_to_f16x2((tg >> 16) & 0xFFu);
+          const uint32_t a1 = e2m1x2_to_f16x2(tu & 0xFFu), a3 = e2m1x2_to_f16x2((tu >> 16) & 0xFFu);
+          const float sgf = e4m3_to_f32(sq_g >> (8 * hh));
+          const float suf = e4m3_to_f32(sq_u >> (8 * hh));
+          const int lb = (kk - k0) / 16 + hh;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            if (nt < ntiles) {
+              const uint2 bv = *reinterpret_cast<const uint2*>(xrow + (size_t)nt * 8 * pitch + 16 * lb);
+              float d[4];
+              mma_f16_16816(d, a0, a1, a2, a3, bv.x, bv.y);
+              const float g0 = gatef[nt * 8 + 2 * c], g1 = gatef[nt * 8 + 2 * c + 1];
+              acc[nt][0] = fmaf(sgf * g0, d[0], acc[nt][0]);
+              acc[nt][1] = fmaf(sgf * g1, d[1], acc[nt][1]);
+              acc[nt][2] = fmaf(suf * g0, d[2], acc[nt][2]);
+              acc[nt][3] = fmaf(suf * g1, d[3], acc[nt][3]);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // ---- epilogue
+  const float sc2 = __ldg(a.scale_2 + e);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int col = 0; col < 2; ++col) {
+      const int n = nt * 8 + 2 * c + col;
+      const bool valid = nt < ntiles && n < count && rsrc[min(n, NT * 8 - 1)] >= 0;
+      const float inv = valid ? sc2 / rscale[n] : 0.0f;
+      if (FC1) {
+        const float gv = acc[nt][col] * inv, uv = acc[nt][2 + col] * inv;
+        const float hv = valid ? gv / (1.0f + expf(-gv)) * uv : 0.0f;
+        if (valid) a.out[(size_t)(pos0 + n) * a.I + row_g] = hv;
+        float m = fabsf(hv);
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+        if (valid && g == 0) atomicMax(a.hmax + pos0 + n, __float_as_uint(m));
+      } else if (valid) {
+        const int p = rsrc[n];
+        const float wp = __ldg(a.topk_w + p) * inv;
+        a.out[(size_t)p * a.H + row_g] = acc[nt][col] * wp;
+        a.out[(size_t)p * a.H + row_u] = acc[nt][2 + col] * wp;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- combine
+__global__ void __launch_bounds__(kThreads) combine_kernel(int T, int H, int k, const int* __restrict__ hdr,
+                                                           const float* __restrict__ o,
+                                                           uint16_t* __restrict__ y) {
+  const long long n4 = (long long)T * H / 4;
+  const bool ok = hdr[1] != 0;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long t = (i * 4) / H, r = (i * 4) % H;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (ok) {
+      for (int j = 0; j < k; ++j) {
+        const float4 v = *reinterpret_cast<const float4*>(o + ((size_t)t * k + j) * H + r);
+        s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+      }
+    }
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(s.x, s.y), hi = __floats2bfloat162_rn(s.z, s.w);
+    uint2 outv;
+    outv.x = *reinterpret_cast<const uint32_t*>(&lo);
+    outv.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(y + (size_t)t * H + r) = outv;
+  }
+}
+
+template <bool FC1, int NT>
+static moet_status launch_fc(const FcArgs& a, int row_tiles, int grid_y, cudaStream_t st) {
+  const size_t smem = sizeof(__half) * NT * 8 * (a.ks + 16) + 3 * sizeof(float) * NT * 8;
+  auto kern = fc_kernel<FC1, NT>;
+  MOET_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  kern<<<dim3(row_tiles, grid_y), kThreads, smem, st>>>(a);
+  MOET_CUDA_TRY(cudaGetLastError());
+  return MOET_OK;
+}
+
+template <bool FC1>
+static moet_status dispatch_fc(FcArgs a, int nt, int row_tiles, int grid_y, cudaStream_t st) {
+  const int rows = nt * 8;
+  int ks = (kSmemBudget / (rows * 2) - 16) / 128 * 128;
+  if (ks > a.K) ks = a.K;
+  a.ks = ks;
+  switch (nt) {
+    case 1: return launch_fc<FC1, 1>(a, row_tiles, grid_y, st);
+    case 2: return launch_fc<FC1, 2>(a, row_tiles, grid_y, st);
+    case 4: return launch_fc<FC1, 4>(a, row_tiles, grid_y, st);
+    default: return launch_fc<FC1, 8>(a, row_tiles, grid_y, st);
+  }
+}
+
+}  // namespace moet
+
+using namespace moet;
+
+MOET_ERROR_ACCESSOR(moet_internal_error_moe)
+
+extern "C" size_t moet_forward_workspace_size(int T, int H, int I, int E, int k) {
+  if (T < 1 || H < 1 || I < 1 || E < 1 || k < 1) return 0;
+  return ws_layout(T, H, I, E, k).total;
+}
+
+extern "C" moet_status moet_moe_forward(int T, int H, int I, int E, int k, const uint16_t* x,
+                                        const int32_t* topk_idx, const float* topk_w,
+                                        const int32_t* expert_offsets, const int32_t* perm,
+                                        const moet_planes* fc1, const moet_planes* fc2,
+                                        const int32_t* delta_slot, int n_slots, const moet_nvfp4* dfc1,
+                                        const moet_nvfp4* dfc2, const uint8_t* gate_mask, uint16_t* y,
+                                        void* workspace, size_t ws_bytes, moet_stream stream) {
+  if (T < 1 || H < 128 || I < 128 || H % 128 || I % 128 || E < 1 || E > 1024 || k < 1 || k > 16 ||
+      k > E)
+    return MOET_ERR_SHAPE;
+  if ((long long)T * k > (1LL << 30) || (long long)T * k * H > (1LL << 40)) return MOET_ERR_UNSUPPORTED;
+  if (!x || !topk_idx || !topk_w || !expert_offsets || !perm || !fc1 || !fc2 || !y) return MOET_ERR_INVALID_ARG;
+  if (!fc1->sign || !fc1->mag || !fc1->s16 || !fc1->scale_2 || !fc2->sign || !fc2->mag || !fc2->s16 ||
+      !fc2->scale_2)
+    return MOET_ERR_INVALID_ARG;
+  const bool with_delta = delta_slot != nullptr && gate_mask != nullptr;
+  if (with_delta) {
+    if (n_slots < 1 || !dfc1 || !dfc2 || !dfc1->codes || !dfc1->s4 || !dfc2->codes || !dfc2->s4)
+      return MOET_ERR_INVALID_ARG;
+    if (((uintptr_t)dfc1->codes & 15) || ((uintptr_t)dfc2->codes & 15) || ((uintptr_t)dfc1->s4 & 1) ||
+        ((uintptr_t)dfc2->s4 & 1))
+      return MOET_ERR_ALIGN;
+  }
+  if (((uintptr_t)x & 15) || ((uintptr_t)y & 15) || ((uintptr_t)fc1->sign & 15) ||
+      ((uintptr_t)fc1->mag & 15) || ((uintptr_t)fc2->sign & 15) || ((uintptr_t)fc2->mag & 15) ||
+      ((uintptr_t)fc1->s16 & 7) || ((uintptr_t)fc2->s16 & 7) || ((uintptr_t)workspace & 255))
+    return MOET_ERR_ALIGN;
+  const WsLayout L = ws_layout(T, H, I, E, k);
+  if (!workspace || ws_bytes < L.total) return MOET_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  char* ws = static_cast<char*>(workspace);
+  int* hdr = reinterpret_cast<int*>(ws + L.hdr);
+  float* tok_scale = reinterpret_cast<float*>(ws + L.tok_scale);
+  unsigned* hmax = reinterpret_cast<unsigned*>(ws + L.hmax);
+  int4* chunks = reinterpret_cast<int4*>(ws + L.chunks);
+  float* h = reinterpret_cast<float*>(ws + L.h);
+  float* o = reinterpret_cast<float*>(ws + L.o);
+
+  prologue_kernel<<<1 + (T + 7) / 8, kThreads, 0, st>>>(T, H, E, k, x, expert_offsets, hdr, tok_scale,
+                                                         hmax, chunks);
+  MOET_CUDA_TRY(cudaGetLastError());
+
+  const int mc = max_chunks(T, E, k);
+  const int maxn = T < kChunk ? T : kChunk;
+  const int nt = maxn <= 8 ? 1 : maxn <= 16 ? 2 : maxn <= 32 ? 4 : 8;
+  FcArgs a{};
+  a.T = T; a.H = H; a.I = I; a.E = E; a.k = k;
+  a.x = x; a.h_in = h; a.offsets = expert_offsets; a.perm = perm; a.topk_w = topk_w;
+  a.delta_slot = with_delta ? delta_slot : nullptr;
+  a.gate = with_delta ? gate_mask : nullptr;
+  a.n_slots = n_slots;
+  a.hdr = hdr; a.chunks = chunks; a.tok_scale = tok_scale; a.hmax = hmax;
+
+  FcArgs a1 = a;
+  a1.K = H; a1.N = 2 * I;
+  a1.sign = fc1->sign; a1.mag = fc1->mag; a1.s16 = fc1->s16; a1.scale_2 = fc1->scale_2;
+  if (with_delta) { a1.dcodes = dfc1->codes; a1.ds4 = dfc1->s4; }
+  a1.out = h;
+  moet_status s = dispatch_fc<true>(a1, nt, I / 64, mc, st);
+  if (s != MOET_OK) return s;
+
+  FcArgs a2 = a;
+  a2.K = I; a2.N = H;
+  a2.sign = fc2->sign; a2.mag = fc2->mag; a2.s16 = fc2->s16; a2.scale_2 = fc2->scale_2;
+  if (with_delta) { a2.dcodes = dfc2->codes; a2.ds4 = dfc2->s4; }
+  a2.out = o;
+  s = dispatch_fc<false>(a2, nt, H / 128, mc, st);
+  if (s != MOET_OK) return s;
+
+  long long n4 = (long long)T * H / 4;
+  int gc = (int)((n4 + kThreads - 1) / kThreads);
+  if (gc > 152 * 8) gc = 152 * 8;
+  combine_kernel<<<gc, kThreads, 0, st>>>(T, H, k, hdr, o, y);
+  MOET_CUDA_TRY(cudaGetLastError());
+  return MOET_OK;
+}

@@ -1,0 +1,211 @@
+// Router top-k + renormalised softmax + token bucketing by expert.
+//
+// Routing step of the MoE layer (README "Frontier MoE on consumer Blackwell
+// (SM120)", "How it fits"; the airanks page's DeepSeek-V4.1 table, row "MoE at
+// decode", counts seven launches from router to FC1 in stock vLLM -- here it is
+// one launch for up to 512 tokens and two beyond).
+//
+// Top-k: one warp per token; each lane holds ceil(E/32) logits in registers
+// and a 64-bit key (order-preserving logit bits, then the complement of the
+// expert id) so that one warp-wide max per round picks the largest logit with
+// the lower id on ties.  NaN maps below -inf, -0 equals +0.
+// Bucketing: one CTA of 1024 threads counts pairs per expert in shared
+// memory, scans, and scatters pair ids stably in chunks of 1024 pairs: the
+// rank inside a warp comes from __match_any_sync, the rank across warps of
+// the chunk from a [32 warps][E] byte table of per-warp counts.
+#include "common.cuh"
+
+namespace moet {
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+  if (f != f) return 0u;                         // NaN: below everything
+  uint32_t u = __float_as_uint(f == 0.0f ? 0.0f : f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+template <int VPL>
+__device__ __forceinline__ void topk_one_token(int t, int E, int k, const float* __restrict__ logits,
+                                               int32_t* __restrict__ topk_idx,
+                                               float* __restrict__ topk_w) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long key[VPL];
+  float val[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      val[i] = __ldg(logits + (long long)t * E + e);
+      key[i] = ((unsigned long long)order_key(val[i]) << 32) | (0xFFFFu - (uint32_t)e);
+    } else {
+      val[i] = 0.0f;
+      key[i] = 0ull;                              // below every real entry
+    }
+  }
+  float my_logit = 0.0f;
+  int my_idx = 0;
+  for (int j = 0; j < k; ++j) {
+    unsigned long long best = 0ull;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) best = key[i] > best ? key[i] : best;
+    unsigned long long wbest = best;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long other = __shfl_xor_sync(0xffffffffu, wbest, o);
+      wbest = other > wbest ? other : wbest;
+    }
+    const int e = 0xFFFF - (int)(wbest & 0xFFFFull);
+    const int owner = e & 31;
+    float lv = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      if (key[i] == wbest) {
+        lv = val[i];
+        key[i] = 0ull;
+      }
+    }
+    lv = __shfl_sync(0xffffffffu, lv, owner);
+    if (lane == j) {
+      my_logit = lv;
+      my_idx = e;
+    }
+  }
+  const float lmax = __shfl_sync(0xffffffffu, my_logit, 0);
+  float ex = lane < k ? expf(my_logit - lmax) : 0.0f;
+  float sum = ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane < k) {
+    topk_idx[(long long)t * k + lane] = my_idx;
+    topk_w[(long long)t * k + lane] = ex / sum;
+  }
+}
+
+template <int VPL>
+__global__ void __launch_bounds__(256) topk_kernel(int T, int E, int k, const float* __restrict__ logits,
+                                                   int32_t* __restrict__ topk_idx,
+                                                   float* __restrict__ topk_w) {
+  const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (t < T) topk_one_token<VPL>(t, E, k, logits, topk_idx, topk_w);
+}
+
+// One CTA of 1024 threads.  If FUSED, it first computes the top-k of all T
+// tokens (32 warps, a token per warp per step), then buckets.
+template <int VPL, bool FUSED>
+__global__ void __launch_bounds__(1024) bucket_kernel(int T, int E, int k, const float* __restrict__ logits,
+                                                      int32_t* __restrict__ topk_idx,
+                                                      float* __restrict__ topk_w,
+                                                      int32_t* __restrict__ offsets,
+                                                      int32_t* __restrict__ perm) {
+  extern __shared__ int smem[];
+  int* counts = smem;                               // [E]
+  int* base = smem + E;                             // [E]
+  unsigned char* wc = (unsigned char*)(smem + 2 * E);  // [32][E]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (FUSED) {
+    for (int t = warp; t < T; t += 32) topk_one_token<VPL>(t, E, k, logits, topk_idx, topk_w);
+  }
+  for (int i = tid; i < E; i += 1024) counts[i] = 0;
+  for (int i = tid; i < 32 * E; i += 1024) wc[i] = 0;
+  __syncthreads();
+  const int n = T * k;
+  for (int p = tid; p < n; p += 1024) {
+    const int e = topk_idx[p];
+    if (e < 0 || e >= E) {
+      record_error(MOET_ERR_DEVICE_INDEX);
+      continue;
+    }
+    atomicAdd(counts + e, 1);
+  }
+  __syncthreads();
+  // exclusive scan of counts[0..E) by warp 0 (E <= 1024: 32 values per lane)
+  if (warp == 0) {
+    int running = 0;
+    for (int c0 = 0; c0 < E; c0 += 32) {
+      const int e = c0 + lane;
+      const int v = e < E ? counts[e] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (e < E) {
+        base[e] = running + incl - v;
+        offsets[e] = running + incl - v;
+      }
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) offsets[E] = running;
+  }
+  __syncthreads();
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int c0 = 0; c0 < n; c0 += 1024) {
+    const int p = c0 + tid;
+    int e = -1;
+    if (p < n) {
+      e = topk_idx[p];
+      if (e < 0 || e >= E) e = -1;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & lt_mask);
+    const int cnt = __popc(peers);
+    if (e >= 0 && rank == 0) wc[warp * E + e] = (unsigned char)cnt;
+    __syncthreads();
+    if (e >= 0) {
+      int pre = 0;
+      for (int w = 0; w < warp; ++w) pre += wc[w * E + e];
+      perm[base[e] + pre + rank] = p;
+    }
+    __syncthreads();
+    if (e >= 0 && rank == 0) {
+      atomicAdd(base + e, cnt);
+      wc[warp * E + e] = 0;
+    }
+    __syncthreads();
+  }
+}
+
+template <int VPL>
+static moet_status launch_route(int T, int E, int k, const float* logits, int32_t* idx, float* w,
+                                int32_t* offsets, int32_t* perm, cudaStream_t st) {
+  const size_t smem = (size_t)E * 8 + (size_t)E * 32;
+  if (T <= 512) {
+    auto kern = bucket_kernel<VPL, true>;
+    if (smem > 48 * 1024) MOET_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    kern<<<1, 1024, smem, st>>>(T, E, k, logits, idx, w, offsets, perm);
+  } else {
+    topk_kernel<VPL><<<(T + 7) / 8, 256, 0, st>>>(T, E, k, logits, idx, w);
+    MOET_CUDA_TRY(cudaGetLastError());
+    auto kern = bucket_kernel<VPL, false>;
+    if (smem > 48 * 1024) MOET_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    kern<<<1, 1024, smem, st>>>(T, E, k, logits, idx, w, offsets, perm);
+  }
+  MOET_CUDA_TRY(cudaGetLastError());
+  return MOET_OK;
+}
+
+}  // namespace moet
+
+using namespace moet;
+
+MOET_ERROR_ACCESSOR(moet_internal_error_route)
+
+extern "C" moet_status moet_route_topk(int T, int E, int k, const float* logits, int32_t* topk_idx,
+                                       float* topk_w, int32_t* expert_offsets, int32_t* perm,
+                                       moet_stream stream) {
+  if (T < 1 || E < 1 || E > 1024 || k < 1 || k > 16 || k > E) return MOET_ERR_SHAPE;
+  if ((long long)T * k > (1LL << 30)) return MOET_ERR_UNSUPPORTED;
+  if (!logits || !topk_idx || !topk_w || !expert_offsets || !perm) return MOET_ERR_INVALID_ARG;
+  if (((uintptr_t)logits & 3) || ((uintptr_t)topk_idx & 3) || ((uintptr_t)topk_w & 3) ||
+      ((uintptr_t)expert_offsets & 3) || ((uintptr_t)perm & 3))
+    return MOET_ERR_ALIGN;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int vpl = (E + 31) / 32;
+  if (vpl <= 2) return launch_route<2>(T, E, k, logits, topk_idx, topk_w, expert_offsets, perm, st);
+  if (vpl <= 4) return launch_route<4>(T, E, k, logits, topk_idx, topk_w, expert_offsets, perm, st);
+  if (vpl <= 8) return launch_route<8>(T, E, k, logits, topk_idx, topk_w, expert_offsets, perm, st);
+  if (vpl <= 12) return launch_route<12>(T, E, k, logits, topk_idx, topk_w, expert_offsets, perm, st);
+  if (vpl <= 16) return launch_route<16>(T, E, k, logits, topk_idx, topk_w, expert_offsets, perm, st);
+  return launch_route<32>(T, E, k, logits, topk_idx, topk_w, expert_offsets, perm, st);
+}

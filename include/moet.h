@@ -1,0 +1,164 @@
+/*
+ * moet.h -- C ABI of the GB300 (sm_103a) library for MoE expert layers over
+ * sign-symmetric 2-bit expert weights with an NVFP4 delta.
+ *
+ * Method: vLLM-Moet README ("Frontier MoE on consumer Blackwell (SM120)"),
+ * sections "GLM-5.2 (753B) -- the headline model" (modelopt NVFP4 experts,
+ * load-time requantisation) and "How it fits -- 2-bit experts at FP4 quality"
+ * (sign-symmetric 2-bit codebook, FP4 delta cache, confidence gate).  The
+ * pages leave the 2-bit levels open; this library fixes q in {-3,-1,+1,+3}
+ * with an e4m3 scale s16 per block of 16 along K.
+ *
+ * Conventions shared by every entry point
+ *  - All array pointers are DEVICE pointers owned by the caller; the library
+ *    never allocates or frees memory (except the one-time 1 KB error flag
+ *    that is part of the library image).  Shapes are given in elements.
+ *  - Every call is asynchronous on `stream` and returns after enqueueing.
+ *    Host-side argument checks run first and nothing is enqueued when one
+ *    fails.  No entry point synchronises, except moet_last_device_error.
+ *  - Problems that only the device can see (an index out of range, a
+ *    bounded wait that expired) never trap: the kernel records the first
+ *    such problem in a device flag and skips the offending access; read it
+ *    with moet_last_device_error.
+ *  - Matrices are row-major.  "Units of scale_2" means a value divided by
+ *    the matrix's fp32 per-tensor scale_2.
+ *
+ * Data formats
+ *  NVFP4 matrix [N, K]: codes u8 [N, K/2] (two e2m1 codes per byte, LOW
+ *    nibble = even k; code bit 3 = sign, bits 0..2 index {0,.5,1,1.5,2,3,4,6}),
+ *    s4 u8 [N, K/16] (e4m3fn scale per 16 along K), scale_2 fp32.
+ *  2-bit planes [N, K]: sign u32 [N, K/32], mag u32 [N, K/32] (bit j of word
+ *    w holds k = 32 w + j; sign 1 = negative; mag 1 = |q| = 3), s16 u8
+ *    [N, K/16] (e4m3fn).  Weight = (sign ? -1 : 1) * (mag ? 3 : 1) * s16 *
+ *    scale_2.  The code is never zero.
+ *  Delta: an NVFP4 matrix on the SAME scale_2 holding W_nvfp4 - W_2bit.
+ */
+#ifndef MOET_H
+#define MOET_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moet_stream; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  MOET_OK = 0,
+  MOET_ERR_INVALID_ARG = 1, /* null pointer where one is required, bad enum/size      */
+  MOET_ERR_SHAPE = 2,       /* a dimension violates the stated divisibility or range  */
+  MOET_ERR_ALIGN = 3,       /* a pointer is not aligned as the entry point requires   */
+  MOET_ERR_UNSUPPORTED = 4, /* shape valid in principle but not handled by this build */
+  MOET_ERR_WORKSPACE = 5,   /* workspace missing or smaller than the size query       */
+  MOET_ERR_CUDA = 6,        /* a CUDA runtime call or kernel launch failed            */
+  MOET_ERR_TIMEOUT = 7,     /* a bounded device wait expired (device flag)            */
+  MOET_ERR_DEVICE_INDEX = 8 /* device saw an index out of range (device flag)         */
+} moet_status;
+
+/* Human-readable name of a status.  Never returns NULL. */
+const char* moet_status_string(moet_status s);
+
+/* Synchronises `stream`, then returns and clears the first device-side
+ * problem recorded by any kernel of this library on the current device
+ * (MOET_OK if none).  Returns MOET_ERR_CUDA if the synchronisation fails. */
+moet_status moet_last_device_error(moet_stream stream);
+
+/* ------------------------------------------------------------------------
+ * moet_quantize_nvfp4 -- fp32 weights -> NVFP4 (the experts' input format).
+ * README "Frontier MoE on consumer Blackwell (SM120)", "GLM-5.2 (753B)" par. 1
+ * (e2m1 x e4m3 block-16 x fp32 scale_2), read as: scale_2 = fp32(amax/2688);
+ * s4 = e4m3 RNE(block amax / (6 scale_2)); code = e2m1 RNE(w / (s4 scale_2)),
+ * ties to even, saturating, sign of w kept (-0 stays -0); amax = 0 or s4 = 0
+ * give +-0 codes.
+ *   M matrices of [N, K] each, K % 32 == 0, M,N >= 1.
+ *   w        [M, N, K] fp32, 16-byte aligned
+ *   scale_2  [M] fp32 (written)
+ *   codes    [M, N, K/2] u8 (written), 16-byte aligned
+ *   s4       [M, N, K/16] u8 (written), 2-byte aligned
+ * Enqueues a zero-fill of scale_2 and three kernels.  */
+moet_status moet_quantize_nvfp4(int M, int N, int K, const float* w, float* scale_2,
+                                uint8_t* codes, uint8_t* s4, moet_stream stream);
+
+/* ------------------------------------------------------------------------
+ * moet_requant_2bit -- load-time NVFP4 -> 2-bit planes (+ optional delta).
+ * README "GLM-5.2 (753B)" par. 1 (exact dequant then sign-symmetric 2-bit
+ * requantisation) and "How it fits" bullets 1-2.  In units of scale_2, with
+ * v = e2m1(code) * e4m3(s4) exact, per block of 16 along K:
+ *   s16 = e4m3 satfinite RNE(max|v| / 3); sign = sign bit of the code;
+ *   mag = (|v| >= 2 s16)   (the nearest level of w's sign, ties to |q| = 3).
+ * Delta (when dcodes and ds4 are both non-NULL): d = v - q s16 (exact),
+ *   ds4 = e4m3 RNE(max|d| / 6), dcode = sign(d) | e2m1 RNE(|d| / ds4),
+ *   a zero magnitude written as +0.  The result does not depend on scale_2,
+ *   which the delta shares with the planes, so scale_2 is not an argument.
+ *   M matrices of [N, K], K % 32 == 0.
+ *   codes [M,N,K/2] u8, s4 [M,N,K/16] u8            (read; 16 B / 2 B aligned)
+ *   sign, mag [M,N,K/32] u32, s16 [M,N,K/16] u8      (written; 4 B / 2 B aligned)
+ *   dcodes [M,N,K/2] u8, ds4 [M,N,K/16] u8            (written if non-NULL)
+ * All outputs are bit-exact functions of the inputs.  */
+moet_status moet_requant_2bit(int M, int N, int K, const uint8_t* codes, const uint8_t* s4,
+                              uint32_t* sign, uint32_t* mag, uint8_t* s16,
+                              uint8_t* dcodes, uint8_t* ds4, moet_stream stream);
+
+/* ------------------------------------------------------------------------
+ * moet_route_topk -- router top-k, renormalised softmax, bucketing by expert.
+ * Per token: the k largest logits (ties -> lower expert id; NaN below -inf),
+ * ordered by decreasing logit; w_j = exp(l_j - l_max) / sum over the k.
+ * counts[e] = pairs routed to e; expert_offsets = exclusive scan [E+1]
+ * (offsets[E] = T k); perm lists pair ids p = t k + j grouped by increasing
+ * expert and by increasing p inside an expert (a stable sort).
+ *   1 <= T, 1 <= E <= 1024, 1 <= k <= min(16, E).
+ *   logits [T, E] fp32 (read); topk_idx [T, k] i32, topk_w [T, k] fp32,
+ *   expert_offsets [E+1] i32, perm [T k] i32 (written).
+ * Indices, offsets and perm are bit-exact; weights are fp32 (|err| < 1e-6).  */
+moet_status moet_route_topk(int T, int E, int k, const float* logits, int32_t* topk_idx,
+                            float* topk_w, int32_t* expert_offsets, int32_t* perm,
+                            moet_stream stream);
+
+/* ------------------------------------------------------------------------
+ * moet_moe_forward -- the MoE expert layer on 2-bit planes with the delta.
+ * README "How it fits" bullet 2: y_t = sum_j w_tj FFN_{e_tj}(x_t), with
+ * FFN_e(x) = W2_e (SiLU(Wg_e x) * (Wu_e x)) and SiLU(z) = z / (1 + e^-z).
+ * FC1 planes hold [2I, H] per expert (gate rows 0..I-1, up rows I..2I-1),
+ * FC2 planes hold [H, I].  For a pair whose token has gate_mask[t] != 0 and
+ * whose expert has delta_slot[e] >= 0, both matrices become W_2bit + delta
+ * (delta pool slot delta_slot[e], same scale_2 as the expert's planes).
+ * No SwiGLU clamp.  bf16 activations in and out, fp32 accumulation.
+ *   T >= 1, H % 128 == 0, I % 128 == 0, 1 <= E <= 1024, 1 <= k <= min(16,E).
+ *   x [T, H] bf16 bits (u16, 16 B aligned); y [T, H] bf16 bits (written).
+ *   topk_idx, topk_w, expert_offsets, perm: as written by moet_route_topk.
+ *   fc1/fc2: planes of all E experts, scale_2 [E] fp32.
+ *   delta_slot [E] i32 (-1 = not cached) and gate_mask [T] u8 may be NULL
+ *   (no delta); n_slots bounds the slot values; dfc1/dfc2 hold the pool as
+ *   [n_slots, 2I, H/2] / [n_slots, H, I/2] codes with matching s4.
+ *   workspace: device buffer of at least moet_forward_workspace_size bytes,
+ *   256-byte aligned; its contents on entry do not matter.
+ * Output tolerance vs the fp64 definition: relative Frobenius error
+ * <= 5e-3 and max abs error <= 2e-2 rms(y).  */
+typedef struct {
+  const uint32_t* sign; /* [E, N, K/32] */
+  const uint32_t* mag;  /* [E, N, K/32] */
+  const uint8_t* s16;   /* [E, N, K/16] */
+  const float* scale_2; /* [E]          */
+} moet_planes;
+
+typedef struct {
+  const uint8_t* codes; /* [S, N, K/2]  */
+  const uint8_t* s4;    /* [S, N, K/16] */
+} moet_nvfp4;
+
+size_t moet_forward_workspace_size(int T, int H, int I, int E, int k);
+
+moet_status moet_moe_forward(int T, int H, int I, int E, int k, const uint16_t* x,
+                             const int32_t* topk_idx, const float* topk_w,
+                             const int32_t* expert_offsets, const int32_t* perm,
+                             const moet_planes* fc1, const moet_planes* fc2,
+                             const int32_t* delta_slot, int n_slots, const moet_nvfp4* dfc1,
+                             const moet_nvfp4* dfc2, const uint8_t* gate_mask, uint16_t* y,
+                             void* workspace, size_t ws_bytes, moet_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOET_H */

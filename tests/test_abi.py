@@ -1,0 +1,71 @@
+"""The C ABI library loads, exports every symbol include/moet.h declares, and its
+host-side argument checks reject bad calls before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__ as g
+    g.build()
+    from bit_moe_expert_moet_gb300 import _lib
+    return _lib.lib
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "moet.h")) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moet_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for required in ("moet_requant_2bit", "moet_route_topk", "moet_moe_forward",
+                     "moet_forward_workspace_size", "moet_status_string", "moet_last_device_error",
+                     "moet_quantize_nvfp4"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        assert lib.moet_status_string(code).decode().startswith("MOET_")
+    assert lib.moet_status_string(99).decode() == "MOET_ERR_UNKNOWN"
+
+
+def test_host_side_rejections(lib):
+    # shape checks come first and return before any CUDA call
+    assert lib.moet_route_topk(0, 8, 2, None, None, None, None, None, None) == 2          # SHAPE
+    assert lib.moet_route_topk(4, 2048, 2, None, None, None, None, None, None) == 2       # E > 1024
+    assert lib.moet_route_topk(4, 8, 17, None, None, None, None, None, None) == 2         # k > 16
+    assert lib.moet_route_topk(4, 8, 2, None, None, None, None, None, None) == 1          # null -> INVALID_ARG
+    assert lib.moet_requant_2bit(1, 1, 48, None, None, None, None, None, None, None, None) == 2   # K % 32
+    assert lib.moet_requant_2bit(1, 1, 64, None, None, None, None, None, None, None, None) == 1
+    p = ctypes.c_void_p(16)                                                               # aligned dummy
+    q = ctypes.c_void_p(17)                                                               # misaligned
+    assert lib.moet_requant_2bit(1, 1, 64, q, p, p, p, p, None, None, None) == 3          # ALIGN
+    assert lib.moet_requant_2bit(1, 1, 64, p, p, p, p, p, p, None, None) == 1             # half a delta
+    assert lib.moet_quantize_nvfp4(1, 1, 40, p, p, p, p, None) == 2
+    fwd_null = [None] * 8 + [0] + [None] * 5 + [0, None]
+    assert lib.moet_moe_forward(1, 100, 128, 8, 2, *fwd_null) == 2                         # H % 128
+    assert lib.moet_moe_forward(1, 128, 128, 8, 2, *fwd_null) == 1                         # nulls
+
+
+def test_workspace_size_is_monotone(lib):
+    ws = lib.moet_forward_workspace_size
+    a = ws(1, 7168, 2048, 256, 8)
+    b = ws(64, 7168, 2048, 256, 8)
+    assert 0 < a < b
+    assert ws(0, 7168, 2048, 256, 8) == 0
+    # fp32 h [T k, I] and o [T k, H] dominate
+    assert b >= 64 * 8 * (7168 + 2048) * 4

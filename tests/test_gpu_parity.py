@@ -1,0 +1,318 @@
+"""GPU parity: the CUDA library (through the C ABI) against the CPU oracle.
+
+Integer outputs (NVFP4 codes/scales, planes, s16, delta, top-k ids, offsets,
+permutation) must match bit for bit; routing weights within 1e-6; the layer
+output within relative Frobenius 5e-3 and max-abs 2e-2 rms(y*).
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import moe as omoe, nvfp4 as onv, requant as orq, route as oroute
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+REL_FROB, MAX_ABS = 5e-3, 2e-2
+
+
+@pytest.fixture(scope="module")
+def moet():
+    import __graft_entry__ as g
+    g.build()
+    import bit_moe_expert_moet_gb300 as m
+    return m
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def host(t):
+    return t.cpu().numpy()
+
+
+def check_y(yg, yo):
+    yg = np.asarray(yg, np.float64)
+    rel = np.linalg.norm(yg - yo) / np.linalg.norm(yo)
+    mx = np.abs(yg - yo).max() / np.sqrt(np.mean(yo ** 2))
+    assert rel <= REL_FROB and mx <= MAX_ABS, (rel, mx)
+    return rel, mx
+
+
+# ------------------------------------------------------------------ quantiser / requant
+def _gpu_quantize(moet, w):
+    M, N, K = w.shape
+    codes = torch.empty((M, N, K // 2), dtype=torch.uint8, device=DEV)
+    s4 = torch.empty((M, N, K // 16), dtype=torch.uint8, device=DEV)
+    sc2 = torch.empty(M, dtype=torch.float32, device=DEV)
+    moet.quantize_nvfp4(dev(w), codes, s4, sc2)
+    return host(codes), host(s4), host(sc2)
+
+
+def _gpu_requant(moet, codes, s4, delta=True):
+    M, N, K2 = codes.shape
+    K = 2 * K2
+    sign = torch.empty((M, N, K // 32), dtype=torch.int32, device=DEV)
+    mag = torch.empty_like(sign)
+    s16 = torch.empty((M, N, K // 16), dtype=torch.uint8, device=DEV)
+    dc = torch.empty((M, N, K // 2), dtype=torch.uint8, device=DEV) if delta else None
+    ds = torch.empty((M, N, K // 16), dtype=torch.uint8, device=DEV) if delta else None
+    moet.requant_2bit(dev(codes), dev(s4), sign, mag, s16, dc, ds)
+    out = dict(sign=host(sign).view(np.uint32), mag=host(mag).view(np.uint32), s16=host(s16))
+    if delta:
+        out["dcodes"], out["ds4"] = host(dc), host(ds)
+    return out
+
+
+def test_quantize_nvfp4_bit_exact(moet):
+    rng = np.random.default_rng(20)
+    ws = [
+        (rng.standard_normal((64, 256)) * 0.02).astype(np.float32),
+        (rng.standard_t(4, (64, 256)) * 0.014).astype(np.float32),
+        (rng.standard_normal((64, 256)) * np.exp2(rng.integers(-40, 40, (64, 1)))).astype(np.float32),
+        np.zeros((64, 256), np.float32),
+    ]
+    ws[0][3, 16:32] = 0.0
+    ws[0][5, :16] = -0.0
+    ws[1][7, 40] = 1e-30
+    w = np.stack(ws)
+    codes, s4, sc2 = _gpu_quantize(moet, w)
+    for m in range(w.shape[0]):
+        oc, os4, osc = onv.quantize(w[m])
+        assert np.float32(osc) == sc2[m]
+        assert np.array_equal(os4, s4[m])
+        assert np.array_equal(oc, codes[m])
+
+
+def _random_nvfp4(rng, M, N, K):
+    codes = rng.integers(0, 256, (M, N, K // 2), dtype=np.uint8)
+    codes[rng.random(codes.shape) < 0.05] = 0
+    s4 = rng.integers(0, 127, (M, N, K // 16), dtype=np.uint8)
+    s4[rng.random(s4.shape) < 0.03] = 0
+    return codes, s4
+
+
+def _check_requant(got, codes, s4):
+    for m in range(codes.shape[0]):
+        ref = orq.requant_2bit(codes[m], s4[m])
+        for key in ("sign", "mag", "s16", "dcodes", "ds4"):
+            assert np.array_equal(ref[key], got[key][m]), (m, key)
+
+
+def test_requant_bit_exact_random(moet):
+    rng = np.random.default_rng(21)
+    codes, s4 = _random_nvfp4(rng, 3, 64, 512)
+    _check_requant(_gpu_requant(moet, codes, s4), codes, s4)
+
+
+def test_requant_exhaustive_scale_and_max_code(moet):
+    """Every (s4, max code) pair, including all s16 ties in the e4m3 subnormal range."""
+    rows = []
+    rng = np.random.default_rng(22)
+    for s in range(127):
+        for mx in range(8):
+            c = rng.integers(0, mx + 1, 32).astype(np.uint8) | (rng.integers(0, 2, 32).astype(np.uint8) << 3)
+            c[0] = mx | (8 if s & 1 else 0)
+            c[17] = mx
+            rows.append((c, s))
+    codes = np.stack([(c[0::2] | (c[1::2] << 4)).astype(np.uint8) for c, _ in rows])[None]
+    s4 = np.array([[s, (s * 7 + 3) % 127] for _, s in rows], dtype=np.uint8)[None]
+    _check_requant(_gpu_requant(moet, codes, s4), codes, s4)
+
+
+def test_requant_without_delta_matches_planes(moet):
+    rng = np.random.default_rng(23)
+    codes, s4 = _random_nvfp4(rng, 2, 32, 256)
+    a = _gpu_requant(moet, codes, s4, delta=True)
+    b = _gpu_requant(moet, codes, s4, delta=False)
+    for key in ("sign", "mag", "s16"):
+        assert np.array_equal(a[key], b[key])
+
+
+# ------------------------------------------------------------------ routing
+def _gpu_route(moet, logits, k):
+    T, E = logits.shape
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    off = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    perm = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    moet.route_topk(dev(logits), k, idx, w, off, perm)
+    return host(idx), host(w), host(off), host(perm)
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 256, 8), (4, 8, 2), (37, 64, 6), (64, 256, 8), (512, 384, 8),
+                                   (513, 256, 8), (4096, 256, 8), (256, 1024, 16), (100, 16, 1), (9, 33, 5)])
+def test_route_bit_exact(moet, T, E, k):
+    rng = np.random.default_rng(T * 1000 + E)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    logits[:, 1] = logits[:, 2]                   # ties -> lower id
+    if T > 3:
+        logits[2, :] = 0.25                        # all equal
+        logits[3, ::3] = -np.inf
+    idx, w, off, perm = _gpu_route(moet, logits, k)
+    oi, ow = oroute.route_topk(logits, k)
+    assert np.array_equal(idx, oi)
+    assert np.abs(w - ow).max() <= 1e-6
+    _, ooff, operm = oroute.bucket(oi, E)
+    assert np.array_equal(off, ooff)
+    assert np.array_equal(perm, operm)
+
+
+def test_route_nan_ranks_below_minus_inf(moet):
+    logits = np.array([[np.nan, -np.inf, 1.0, 2.0, np.nan, -0.0, 0.0, -1.0]], dtype=np.float32)
+    idx, w, _, _ = _gpu_route(moet, logits, 7)
+    oi, _ = oroute.route_topk(logits, 7)
+    assert np.array_equal(idx, oi)
+    assert idx[0].tolist() == [3, 2, 5, 6, 7, 1, 0]
+
+
+# ------------------------------------------------------------------ forward
+def _make_layer(moet, H, I, E, dset, rng=None, cfg=None):
+    """GPU planes + delta pool from fp32 weights via the oracle quantiser (host)."""
+    ref, gp = {}, {}
+    for f, (N, K) in ((1, (2 * I, H)), (2, (H, I))):
+        if cfg is not None:
+            w = np.stack([W.draw_weight(cfg, e, f) for e in range(E)])
+        else:
+            w = (rng.standard_normal((E, N, K)) * 0.02).astype(np.float32)
+        q = [onv.quantize(w[e]) for e in range(E)]
+        codes = np.stack([a[0] for a in q])
+        s4 = np.stack([a[1] for a in q])
+        sc2 = np.array([a[2] for a in q], np.float32)
+        got = _gpu_requant(moet, codes, s4, delta=True)
+        rq = [orq.requant_2bit(codes[e], s4[e]) for e in range(E)]
+        for key in ("sign", "mag", "s16", "dcodes", "ds4"):
+            assert np.array_equal(np.stack([r[key] for r in rq]), got[key])
+        ref[f] = dict(sign=got["sign"], mag=got["mag"], s16=got["s16"], scale_2=sc2)
+        ref[f, "d"] = dict(codes=got["dcodes"][dset], s4=got["ds4"][dset])
+        gp[f] = moet.Planes(dev(got["sign"].view(np.int32)), dev(got["mag"].view(np.int32)), dev(got["s16"]), dev(sc2))
+        gp[f, "d"] = moet.DeltaPool(dev(got["dcodes"][dset]), dev(got["ds4"][dset]))
+    return ref, gp
+
+
+def _run_forward(moet, logits, xb, k, gp, E, H, dset=None, gate=None, slot=None):
+    T = logits.shape[0]
+    ld = dev(logits)
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    off = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    perm = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    moet.route_topk(ld, k, idx, w, off, perm)
+    x = dev(xb.view(np.int16)).view(torch.bfloat16)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    I = gp[2].sign.shape[2] * 32
+    ws = torch.empty(moet.forward_workspace_size(T, H, I, E, k), dtype=torch.uint8, device=DEV)
+    kw = {}
+    if dset is not None:
+        if slot is None:
+            slot = W.delta_slot_table(E, dset)
+        kw = dict(delta_slot=dev(slot), dfc1=gp[1, "d"], dfc2=gp[2, "d"], gate_mask=dev(gate))
+    moet.moe_forward(x, idx, w, off, perm, gp[1], gp[2], y, ws, **kw)
+    err = moet.last_device_error()
+    return y.float().cpu().numpy(), err
+
+
+def _oracle_forward(logits, xb, k, ref, dset=None, gate=None, E=None, tokens=None, slot=None):
+    oi, ow = oroute.route_topk(logits, k)
+    x = W.bf16_bits_to_f32(xb).astype(np.float64)
+    if dset is None:
+        return omoe.moe_forward(x, oi, ow, ref[1], ref[2], tokens=tokens)
+    if slot is None:
+        slot = W.delta_slot_table(E, dset)
+    return omoe.moe_forward(x, oi, ow, ref[1], ref[2], slot, ref[1, "d"], ref[2, "d"], gate, tokens=tokens)
+
+
+@pytest.mark.parametrize("gate_mode", ["config", "all"])
+def test_forward_tiny_layer(moet, gate_mode):
+    cfg = W.CONFIGS["tiny"]
+    logits, xb, dset, gate = W.draw_layer_inputs(cfg)
+    if gate_mode == "all":
+        gate = np.ones(cfg.T, np.uint8)
+    ref, gp = _make_layer(moet, cfg.H, cfg.I, cfg.E, dset, cfg=cfg)
+    yg, err = _run_forward(moet, logits, xb, cfg.k, gp, cfg.E, cfg.H, dset, gate)
+    assert err == 0
+    yo = _oracle_forward(logits, xb, cfg.k, ref, dset, gate, cfg.E)
+    check_y(yg, yo)
+
+
+@pytest.mark.parametrize("T", [1, 9, 33, 100, 300])
+def test_forward_mid_size(moet, T):
+    """Several row tiles, K slices, N-tiles and chunks (T=300 gives > 64 pairs per expert)."""
+    H, I, E, k = 1024, 256, 16, 4
+    rng = np.random.default_rng(30 + T)
+    dset = np.array([1, 4, 5, 11], dtype=np.int32)
+    ref, gp = _make_layer(moet, H, I, E, dset, rng=rng)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    xb = W.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    gate = (rng.random(T) < 0.5).astype(np.uint8)
+    yg, err = _run_forward(moet, logits, xb, k, gp, E, H, dset, gate)
+    assert err == 0
+    check_y(yg, _oracle_forward(logits, xb, k, ref, dset, gate, E))
+    # no delta arguments at all
+    yg2, _ = _run_forward(moet, logits, xb, k, gp, E, H)
+    check_y(yg2, _oracle_forward(logits, xb, k, ref))
+
+
+def test_forward_is_deterministic(moet):
+    H, I, E, k, T = 1024, 256, 16, 4, 100
+    rng = np.random.default_rng(40)
+    dset = np.array([0, 2], dtype=np.int32)
+    _, gp = _make_layer(moet, H, I, E, dset, rng=rng)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    xb = W.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    gate = np.ones(T, np.uint8)
+    a, _ = _run_forward(moet, logits, xb, k, gp, E, H, dset, gate)
+    b, _ = _run_forward(moet, logits, xb, k, gp, E, H, dset, gate)
+    assert np.array_equal(a, b)
+
+
+def test_forward_bad_slot_sets_device_flag(moet):
+    H, I, E, k, T = 256, 128, 8, 2, 8
+    rng = np.random.default_rng(41)
+    dset = np.array([0, 1], dtype=np.int32)
+    _, gp = _make_layer(moet, H, I, E, dset, rng=rng)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    xb = W.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    slot = np.full(E, 7, np.int32)                 # pool has 2 slots
+    yg, err = _run_forward(moet, logits, xb, k, gp, E, H, dset, np.ones(T, np.uint8), slot=slot)
+    assert err == 8                                # MOET_ERR_DEVICE_INDEX
+    assert np.all(np.isfinite(yg))
+    assert moet.last_device_error() == 0           # cleared by the read
+
+
+# ------------------------------------------------------------------ full-size layers, sampled tokens
+def _random_planes(rng, E, N, K):
+    sign = rng.integers(0, 2 ** 32, (E, N, K // 32), dtype=np.uint32)
+    mag = rng.integers(0, 2 ** 32, (E, N, K // 32), dtype=np.uint32)
+    s16 = rng.integers(40, 57, (E, N, K // 16), dtype=np.uint8)
+    sc2 = (rng.random(E) * 0.004 + 0.004).astype(np.float32)
+    return dict(sign=sign, mag=mag, s16=s16, scale_2=sc2)
+
+
+def _full_layer(moet, cfg, dset, rng):
+    ref, gp = {}, {}
+    for f, (N, K) in ((1, (2 * cfg.I, cfg.H)), (2, (cfg.H, cfg.I))):
+        p = _random_planes(rng, cfg.E, N, K)
+        ref[f] = p
+        gp[f] = moet.Planes(dev(p["sign"].view(np.int32)), dev(p["mag"].view(np.int32)), dev(p["s16"]),
+                            dev(p["scale_2"]))
+        S = max(len(dset), 1)
+        d = dict(codes=rng.integers(0, 256, (S, N, K // 2), dtype=np.uint8),
+                 s4=rng.integers(16, 41, (S, N, K // 16), dtype=np.uint8))
+        ref[f, "d"] = d
+        gp[f, "d"] = moet.DeltaPool(dev(d["codes"]), dev(d["s4"]))
+    return ref, gp
+
+
+@pytest.mark.parametrize("name,tokens", [("dsv3_decode_t64", [0, 37]), ("glm_decode", [3])])
+def test_forward_full_size_sampled(moet, name, tokens):
+    cfg = W.CONFIGS[name]
+    logits, xb, dset, gate = W.draw_layer_inputs(cfg)
+    rng = np.random.default_rng(50)
+    ref, gp = _full_layer(moet, cfg, dset, rng)
+    yg, err = _run_forward(moet, logits, xb, cfg.k, gp, cfg.E, cfg.H, dset, gate)
+    assert err == 0
+    assert np.all(np.isfinite(yg))
+    yo = _oracle_forward(logits, xb, cfg.k, ref, dset, gate, cfg.E, tokens=tokens)
+    check_y(yg[tokens], yo[tokens])
