@@ -20,6 +20,9 @@ from ._lib import (  # noqa: F401
     lib_path,
     status_string,
     last_device_error,
+    profile_enable,
+    profile_read,
+    KERNEL_KINDS,
     quantize_nvfp4,
     requant_2bit,
     route_topk,

@@ -43,6 +43,10 @@ lib.moet_route_topk.restype = _i
 lib.moet_route_topk.argtypes = [_i, _i, _i, _p, _p, _p, _p, _p, _p]
 lib.moet_forward_workspace_size.restype = _sz
 lib.moet_forward_workspace_size.argtypes = [_i, _i, _i, _i, _i]
+lib.moet_profile_enable.restype = _i
+lib.moet_profile_enable.argtypes = [_i]
+lib.moet_profile_read.restype = _i
+lib.moet_profile_read.argtypes = [ctypes.POINTER(_i), ctypes.POINTER(_i), ctypes.POINTER(ctypes.c_float)]
 lib.moet_moe_forward.restype = _i
 lib.moet_moe_forward.argtypes = [_i, _i, _i, _i, _i, _p, _p, _p, _p, _p,
                                  ctypes.POINTER(_Planes), ctypes.POINTER(_Planes),
@@ -80,6 +84,21 @@ def _ptr(t: Optional[torch.Tensor], dtype=None, name: str = "") -> Optional[int]
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
     return t.data_ptr()
+
+
+KERNEL_KINDS = ("requant", "quantize", "route", "prologue", "fc1", "fc2", "combine")
+
+
+def profile_enable(on: bool = True):
+    _check("moet_profile_enable", lib.moet_profile_enable(1 if on else 0))
+
+
+def profile_read() -> dict:
+    """{kind: (launches, timed launches, summed ms)} since the previous read."""
+    n = len(KERNEL_KINDS)
+    la, ti, ms = (_i * n)(), (_i * n)(), (ctypes.c_float * n)()
+    _check("moet_profile_read", lib.moet_profile_read(la, ti, ms))
+    return {KERNEL_KINDS[i]: (la[i], ti[i], ms[i]) for i in range(n)}
 
 
 def last_device_error(stream: Optional[torch.cuda.Stream] = None) -> int:

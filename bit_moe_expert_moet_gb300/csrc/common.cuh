@@ -120,6 +120,18 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
   return r;
 }
 
+// Opt-in launch timing (moet_profile_enable): host-side event pairs around
+// each launch of kind `kind` on `st`.  No-ops while profiling is off.
+void prof_begin(int kind, cudaStream_t st);
+void prof_end(int kind, cudaStream_t st);
+
+struct ProfScope {
+  int kind;
+  cudaStream_t st;
+  ProfScope(int k, cudaStream_t s) : kind(k), st(s) { prof_begin(k, s); }
+  ~ProfScope() { prof_end(kind, st); }
+};
+
 }  // namespace moet
 
 // Defines `int name(void)`: reads and clears this unit's device error flag

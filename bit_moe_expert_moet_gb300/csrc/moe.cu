@@ -426,7 +426,10 @@ static moet_status launch_fc(const FcArgs& a, int row_tiles, int grid_y, cudaStr
   const size_t smem = sizeof(__half) * NT * 8 * (a.ks + 16) + 3 * sizeof(float) * NT * 8;
   auto kern = fc_kernel<FC1, NT>;
   MOET_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-  kern<<<dim3(row_tiles, grid_y), kThreads, smem, st>>>(a);
+  {
+    ProfScope ps(FC1 ? MOET_K_FC1 : MOET_K_FC2, st);
+    kern<<<dim3(row_tiles, grid_y), kThreads, smem, st>>>(a);
+  }
   MOET_CUDA_TRY(cudaGetLastError());
   return MOET_OK;
 }
@@ -494,8 +497,11 @@ extern "C" moet_status moet_moe_forward(int T, int H, int I, int E, int k, const
   float* h = reinterpret_cast<float*>(ws + L.h);
   float* o = reinterpret_cast<float*>(ws + L.o);
 
-  prologue_kernel<<<1 + (T + 7) / 8, kThreads, 0, st>>>(T, H, E, k, x, expert_offsets, hdr, tok_scale,
-                                                         hmax, chunks);
+  {
+    ProfScope ps(MOET_K_PROLOGUE, st);
+    prologue_kernel<<<1 + (T + 7) / 8, kThreads, 0, st>>>(T, H, E, k, x, expert_offsets, hdr, tok_scale,
+                                                           hmax, chunks);
+  }
   MOET_CUDA_TRY(cudaGetLastError());
 
   const int mc = max_chunks(T, E, k);
@@ -528,7 +534,10 @@ extern "C" moet_status moet_moe_forward(int T, int H, int I, int E, int k, const
   long long n4 = (long long)T * H / 4;
   int gc = (int)((n4 + kThreads - 1) / kThreads);
   if (gc > 152 * 8) gc = 152 * 8;
-  combine_kernel<<<gc, kThreads, 0, st>>>(T, H, k, hdr, o, y);
+  {
+    ProfScope ps(MOET_K_COMBINE, st);
+    combine_kernel<<<gc, kThreads, 0, st>>>(T, H, k, hdr, o, y);
+  }
   MOET_CUDA_TRY(cudaGetLastError());
   return MOET_OK;
 }

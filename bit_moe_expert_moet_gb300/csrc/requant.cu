@@ -187,9 +187,12 @@ extern "C" moet_status moet_requant_2bit(int M, int N, int K, const uint8_t* cod
     return MOET_ERR_ALIGN;
   if (dcodes && (((uintptr_t)dcodes & 15) || ((uintptr_t)ds4 & 1))) return MOET_ERR_ALIGN;
   const long long n_groups = (long long)M * N * (K / 32);
-  requant_2bit_kernel<<<grid_for(n_groups, 256), 256, 0, (cudaStream_t)stream>>>(
-      n_groups, (const uint4*)codes, (const uint16_t*)s4, sign, mag, (uint16_t*)s16,
-      (uint4*)dcodes, (uint16_t*)ds4);
+  {
+    ProfScope ps(MOET_K_REQUANT, (cudaStream_t)stream);
+    requant_2bit_kernel<<<grid_for(n_groups, 256), 256, 0, (cudaStream_t)stream>>>(
+        n_groups, (const uint4*)codes, (const uint16_t*)s4, sign, mag, (uint16_t*)s16,
+        (uint4*)dcodes, (uint16_t*)ds4);
+  }
   MOET_CUDA_TRY(cudaGetLastError());
   return MOET_OK;
 }
@@ -207,14 +210,23 @@ extern "C" moet_status moet_quantize_nvfp4(int M, int N, int K, const float* w, 
   MOET_CUDA_TRY(cudaMemsetAsync(scale_2, 0, sizeof(float) * M, st));
   int gx = (int)((per4 + 255) / 256);
   if (gx > 512) gx = 512;
-  amax_kernel<<<dim3(gx, M), 256, 0, st>>>(per4, (const float4*)w, (unsigned int*)scale_2);
+  {
+    ProfScope ps(MOET_K_QUANTIZE, st);
+    amax_kernel<<<dim3(gx, M), 256, 0, st>>>(per4, (const float4*)w, (unsigned int*)scale_2);
+  }
   MOET_CUDA_TRY(cudaGetLastError());
-  scale2_kernel<<<(M + 255) / 256, 256, 0, st>>>(M, scale_2);
+  {
+    ProfScope ps(MOET_K_QUANTIZE, st);
+    scale2_kernel<<<(M + 255) / 256, 256, 0, st>>>(M, scale_2);
+  }
   MOET_CUDA_TRY(cudaGetLastError());
   const long long gpm = (long long)N * (K / 32);
   const long long n_groups = gpm * M;
-  quantize_nvfp4_kernel<<<grid_for(n_groups, 256), 256, 0, st>>>(
-      n_groups, gpm, (const float4*)w, scale_2, (uint4*)codes, (uint16_t*)s4);
+  {
+    ProfScope ps(MOET_K_QUANTIZE, st);
+    quantize_nvfp4_kernel<<<grid_for(n_groups, 256), 256, 0, st>>>(
+        n_groups, gpm, (const float4*)w, scale_2, (uint4*)codes, (uint16_t*)s4);
+  }
   MOET_CUDA_TRY(cudaGetLastError());
   return MOET_OK;
 }

@@ -173,12 +173,17 @@ static moet_status launch_route(int T, int E, int k, const float* logits, int32_
   if (T <= 512) {
     auto kern = bucket_kernel<VPL, true>;
     if (smem > 48 * 1024) MOET_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    ProfScope ps(MOET_K_ROUTE, st);
     kern<<<1, 1024, smem, st>>>(T, E, k, logits, idx, w, offsets, perm);
   } else {
-    topk_kernel<VPL><<<(T + 7) / 8, 256, 0, st>>>(T, E, k, logits, idx, w);
+    {
+      ProfScope ps(MOET_K_ROUTE, st);
+      topk_kernel<VPL><<<(T + 7) / 8, 256, 0, st>>>(T, E, k, logits, idx, w);
+    }
     MOET_CUDA_TRY(cudaGetLastError());
     auto kern = bucket_kernel<VPL, false>;
     if (smem > 48 * 1024) MOET_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    ProfScope ps(MOET_K_ROUTE, st);
     kern<<<1, 1024, smem, st>>>(T, E, k, logits, idx, w, offsets, perm);
   }
   MOET_CUDA_TRY(cudaGetLastError());

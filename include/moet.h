@@ -158,6 +158,30 @@ moet_status moet_moe_forward(int T, int H, int I, int E, int k, const uint16_t* 
                              const moet_nvfp4* dfc2, const uint8_t* gate_mask, uint16_t* y,
                              void* workspace, size_t ws_bytes, moet_stream stream);
 
+/* ------------------------------------------------------------------------
+ * Kernel timing (tracing aid, off by default).  While enabled, the library
+ * records a CUDA event before and after each of its kernel launches on the
+ * launching stream (so timings are on-device and per launch; leave it off
+ * during CUDA-graph capture).  moet_profile_read synchronises on the
+ * recorded events and returns, per kernel kind, the number of launches and
+ * their summed duration in milliseconds since the previous read, then
+ * clears the record.  At most 8192 launches are kept between reads; later
+ * ones are counted in launches[] but not timed (check `timed`).
+ *   launches, timed: int[MOET_KERNEL_KINDS]; total_ms: float[MOET_KERNEL_KINDS]. */
+typedef enum {
+  MOET_K_REQUANT = 0,
+  MOET_K_QUANTIZE = 1,
+  MOET_K_ROUTE = 2,
+  MOET_K_PROLOGUE = 3,
+  MOET_K_FC1 = 4,
+  MOET_K_FC2 = 5,
+  MOET_K_COMBINE = 6,
+  MOET_KERNEL_KINDS = 7
+} moet_kernel_kind;
+
+moet_status moet_profile_enable(int on);
+moet_status moet_profile_read(int* launches, int* timed, float* total_ms);
+
 #ifdef __cplusplus
 }
 #endif
