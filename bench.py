@@ -205,7 +205,9 @@ def build_layer(moet, torch, cfg, dset, dev, seed=0, chunk=16):
                     ds4[slot_of[e]].copy_(ds_tmp[e - e0])
         planes[f] = moet.Planes(sign, mag, s16, sc2)
         pools[f] = moet.DeltaPool(dcodes, ds4)
+        del codes, s4, dc_tmp, ds_tmp
     torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
     return planes, pools
 
 

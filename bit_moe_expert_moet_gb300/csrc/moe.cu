@@ -176,8 +176,8 @@ __global__ void __launch_bounds__(kThreads, 2) fc_kernel(const FcArgs a) {
   const int pos0 = __ldg(a.offsets + e) + ch.y;
   const int K = a.K;
   const int pitch = a.ks + 16;                           // halves per staged row
-  __half* xs = reinterpret_cast<__half*>(smem_raw);      // [NT*8][pitch]
-  float* rscale = reinterpret_cast<float*>(smem_raw + sizeof(__half) * NT * 8 * pitch);  // [NT*8]
+  __half* xs = reinterpret_cast<__half*>(smem_raw);      // [NT*8 + 1][pitch], last row = zeros
+  float* rscale = reinterpret_cast<float*>(smem_raw + sizeof(__half) * (NT * 8 + 1) * pitch);  // [NT*8]
   float* gatef = rscale + NT * 8;                        // [NT*8]
   int* rsrc = reinterpret_cast<int*>(gatef + NT * 8);    // [NT*8] token (FC1) or pair id (FC2)
   __shared__ int any_gated;
@@ -250,8 +250,12 @@ __global__ void __launch_bounds__(kThreads, 2) fc_kernel(const FcArgs a) {
     const int k1 = min(K, k0 + a.ks);
     const int nblk = (k1 - k0) / 16;
     __syncthreads();                                     // previous slice fully consumed
-    // ---- stage activations of this slice: one 16-block per item
-    for (int it = tid; it < NT * 8 * nblk; it += kThreads) {
+    if (k0 == 0) {                                       // zero row read by padding columns
+      for (int i = tid; i < pitch / 8; i += kThreads)
+        reinterpret_cast<uint4*>(xs + (size_t)NT * 8 * pitch)[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    // ---- stage the chunk's activation rows of this slice: one 16-block per item
+    for (int it = tid; it < count * nblk; it += kThreads) {
       const int r = it / nblk, b = it - r * nblk;
       float v[16];
       const int src = rsrc[r];
@@ -292,12 +296,22 @@ __global__ void __launch_bounds__(kThreads, 2) fc_kernel(const FcArgs a) {
     }
     __syncthreads();
 
-    // ---- 2-bit pass over the slice, 128 weights per row per step
-    const __half* xrow = xs + (size_t)g * pitch + 4 * c;
+    // ---- 2-bit pass over the slice, 128 weights per row per step; the next
+    // step's plane loads are issued before the current step is expanded
+    const __half* xrow[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int r = nt * 8 + g;
+      xrow[nt] = xs + (size_t)(r < count ? r : NT * 8) * pitch + 4 * c;
+    }
+    uint4 sg = ldg_nc_v4(Sg + k0 / 32), mg = ldg_nc_v4(Mg + k0 / 32);
+    uint4 su = ldg_nc_v4(Su + k0 / 32), mu = ldg_nc_v4(Mu + k0 / 32);
+    uint2 qg = ldg_nc_v2(Qg + k0 / 16), qu = ldg_nc_v2(Qu + k0 / 16);
     for (int kk = k0; kk < k1; kk += 128) {
-      const uint4 sg = ldg_nc_v4(Sg + kk / 32), mg = ldg_nc_v4(Mg + kk / 32);
-      const uint4 su = ldg_nc_v4(Su + kk / 32), mu = ldg_nc_v4(Mu + kk / 32);
-      const uint2 qg = ldg_nc_v2(Qg + kk / 16), qu = ldg_nc_v2(Qu + kk / 16);
+      const int kn = kk + 128 < k1 ? kk + 128 : kk;
+      const uint4 nsg = ldg_nc_v4(Sg + kn / 32), nmg = ldg_nc_v4(Mg + kn / 32);
+      const uint4 nsu = ldg_nc_v4(Su + kn / 32), nmu = ldg_nc_v4(Mu + kn / 32);
+      const uint2 nqg = ldg_nc_v2(Qg + kn / 16), nqu = ldg_nc_v2(Qu + kn / 16);
       const uint32_t SG[4] = {sg.x, sg.y, sg.z, sg.w}, MG[4] = {mg.x, mg.y, mg.z, mg.w};
       const uint32_t SU[4] = {su.x, su.y, su.z, su.w}, MU[4] = {mu.x, mu.y, mu.z, mu.w};
 #pragma unroll
@@ -319,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 2) fc_kernel(const FcArgs a) {
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             if (nt < ntiles) {
-              const uint2 bv = *reinterpret_cast<const uint2*>(xrow + (size_t)nt * 8 * pitch + 16 * lb);
+              const uint2 bv = *reinterpret_cast<const uint2*>(xrow[nt] + 16 * lb);
               float d[4];
               mma_f16_16816(d, a0, a1, a2, a3, bv.x, bv.y);
               acc[nt][0] = fmaf(sgf, d[0], acc[nt][0]);
@@ -330,6 +344,7 @@ __global__ void __launch_bounds__(kThreads, 2) fc_kernel(const FcArgs a) {
           }
         }
       }
+      sg = nsg; mg = nmg; su = nsu; mu = nmu; qg = nqg; qu = nqu;
     }
 
     // ---- delta pass (gated pairs of a cached expert), 32 weights per row per step
@@ -354,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 2) fc_kernel(const FcArgs a) {
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             if (nt < ntiles) {
-              const uint2 bv = *reinterpret_cast<const uint2*>(xrow + (size_t)nt * 8 * pitch + 16 * lb);
+              const uint2 bv = *reinterpret_cast<const uint2*>(xrow[nt] + 16 * lb);
               float d[4];
               mma_f16_16816(d, a0, a1, a2, a3, bv.x, bv.y);
               const float g0 = gatef[nt * 8 + 2 * c], g1 = gatef[nt * 8 + 2 * c + 1];
@@ -423,7 +438,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(int T, int H, int k, 
 
 template <bool FC1, int NT>
 static moet_status launch_fc(const FcArgs& a, int row_tiles, int grid_y, cudaStream_t st) {
-  const size_t smem = sizeof(__half) * NT * 8 * (a.ks + 16) + 3 * sizeof(float) * NT * 8;
+  const size_t smem = sizeof(__half) * (NT * 8 + 1) * (a.ks + 16) + 3 * sizeof(float) * NT * 8;
   auto kern = fc_kernel<FC1, NT>;
   MOET_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   {
@@ -437,7 +452,7 @@ static moet_status launch_fc(const FcArgs& a, int row_tiles, int grid_y, cudaStr
 template <bool FC1>
 static moet_status dispatch_fc(FcArgs a, int nt, int row_tiles, int grid_y, cudaStream_t st) {
   const int rows = nt * 8;
-  int ks = (kSmemBudget / (rows * 2) - 16) / 128 * 128;
+  int ks = (kSmemBudget / ((rows + 1) * 2) - 16) / 128 * 128;
   if (ks > a.K) ks = a.K;
   a.ks = ks;
   switch (nt) {

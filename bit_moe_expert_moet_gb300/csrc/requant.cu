@@ -4,7 +4,7 @@
 // (modelopt NVFP4 = e2m1 x e4m3 block-16 x fp32 scale_2, requantised at load)
 // and "How it fits -- 2-bit experts at FP4 quality" bullets 1-2.
 //
-// Both kernels are HBM-bound streams: one thread owns one 32-weight group of
+// Both kernels are HBM-bound streams: one thread owns 32-weight groups of
 // one row (16 bytes of NVFP4 codes + 2 scale bytes in, one sign word + one
 // magnitude word + 2 scale bytes (+16 + 2 delta bytes) out), so consecutive
 // threads touch consecutive 16-byte chunks and every access is a coalesced
@@ -72,6 +72,85 @@ __global__ void __launch_bounds__(256) requant_2bit_kernel(
     if (dcodes_out != nullptr) {
       dcodes_out[gi] = make_uint4(dwords[0], dwords[1], dwords[2], dwords[3]);
       ds4_out[gi] = (uint16_t)ds4pair;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- requant, planes only
+// Fast path without the delta.  All 16 weights of a block share s4, so
+// v = e2m1(code) * s4 is monotone in the magnitude code: max|v| is the value of
+// the largest magnitude code, and |v| >= 2 s16 holds exactly for the codes at
+// or above a threshold code.  Both s16 and that threshold depend only on
+// (largest code, s4); every CTA tabulates them once in shared memory with the
+// exact rounding above, and the per-weight work is integer arithmetic on
+// eight nibbles at a time.
+__device__ __forceinline__ uint32_t gather_nibble_bit3(uint32_t x) {
+  // bit 3 of nibble i -> bit i (i = 0..7)
+  uint32_t t = (x >> 3) & 0x11111111u;
+  t = (t | (t >> 3)) & 0x03030303u;
+  t = (t | (t >> 6)) & 0x000F000Fu;
+  return (t | (t >> 12)) & 0xFFu;
+}
+
+__device__ __forceinline__ uint32_t max_mag_code(uint32_t w0, uint32_t w1) {
+  uint32_t m = __vmaxu4(__vmaxu4(w0 & 0x07070707u, (w0 >> 4) & 0x07070707u),
+                        __vmaxu4(w1 & 0x07070707u, (w1 >> 4) & 0x07070707u));
+  m = __vmaxu4(m, m >> 16);
+  m = __vmaxu4(m, m >> 8);
+  return m & 0xFFu;
+}
+
+// mag bits (|q| = 3) of the 8 nibbles of w, given the block's threshold code
+__device__ __forceinline__ uint32_t mag_bits(uint32_t w, uint32_t add) {
+  return gather_nibble_bit3(((w & 0x77777777u) + add) & 0x88888888u);
+}
+
+constexpr int kGroupsPerIter = 2;
+
+__global__ void __launch_bounds__(256) requant_planes_kernel(
+    long long n_groups, const uint4* __restrict__ codes, const uint16_t* __restrict__ s4,
+    uint32_t* __restrict__ sign_out, uint32_t* __restrict__ mag_out, uint16_t* __restrict__ s16_out) {
+  // lut[s4 * 8 + maxcode] = s16 | (threshold code << 8)
+  __shared__ uint16_t lut[128 * 8];
+  for (int i = threadIdx.x; i < 127 * 8; i += blockDim.x) {
+    const uint32_t sc = i >> 3, mc = i & 7;
+    const float s4f = e4m3_to_f32(sc);
+    const uint32_t s16 = e4m3_rne_ratio_small(e2m1_mag_value(mc) * s4f, 3.0f);
+    const float two_s16 = 2.0f * e4m3_to_f32(s16);
+    uint32_t thr = 0;
+#pragma unroll
+    for (uint32_t c = 0; c < 8; ++c) thr += (e2m1_mag_value(c) * s4f < two_s16);
+    lut[i] = (uint16_t)(s16 | (thr << 8));
+  }
+  __syncthreads();
+  const long long stride = (long long)gridDim.x * blockDim.x * kGroupsPerIter;
+  for (long long g0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * kGroupsPerIter; g0 < n_groups;
+       g0 += stride) {
+    uint4 cw[kGroupsPerIter];
+    uint32_t sc[kGroupsPerIter];
+#pragma unroll
+    for (int u = 0; u < kGroupsPerIter; ++u) {
+      if (g0 + u < n_groups) {
+        cw[u] = __ldg(codes + g0 + u);
+        sc[u] = __ldg(s4 + g0 + u);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kGroupsPerIter; ++u) {
+      if (g0 + u >= n_groups) break;
+      const uint32_t w[4] = {cw[u].x, cw[u].y, cw[u].z, cw[u].w};
+      uint32_t sign = 0, mag = 0, s16pair = 0;
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        const uint32_t e = lut[((sc[u] >> (8 * b)) & 0x7Fu) * 8 + max_mag_code(w[2 * b], w[2 * b + 1])];
+        s16pair |= (e & 0xFFu) << (8 * b);
+        const uint32_t add = (8u - (e >> 8)) * 0x11111111u;
+        sign |= (gather_nibble_bit3(w[2 * b]) | (gather_nibble_bit3(w[2 * b + 1]) << 8)) << (16 * b);
+        mag |= (mag_bits(w[2 * b], add) | (mag_bits(w[2 * b + 1], add) << 8)) << (16 * b);
+      }
+      sign_out[g0 + u] = sign;
+      mag_out[g0 + u] = mag;
+      s16_out[g0 + u] = (uint16_t)s16pair;
     }
   }
 }
@@ -189,9 +268,16 @@ extern "C" moet_status moet_requant_2bit(int M, int N, int K, const uint8_t* cod
   const long long n_groups = (long long)M * N * (K / 32);
   {
     ProfScope ps(MOET_K_REQUANT, (cudaStream_t)stream);
-    requant_2bit_kernel<<<grid_for(n_groups, 256), 256, 0, (cudaStream_t)stream>>>(
-        n_groups, (const uint4*)codes, (const uint16_t*)s4, sign, mag, (uint16_t*)s16,
-        (uint4*)dcodes, (uint16_t*)ds4);
+    if (dcodes == nullptr) {
+      long long g = (n_groups + 256LL * kGroupsPerIter - 1) / (256LL * kGroupsPerIter);
+      if (g > 152LL * 8) g = 152LL * 8;
+      requant_planes_kernel<<<(int)g, 256, 0, (cudaStream_t)stream>>>(
+          n_groups, (const uint4*)codes, (const uint16_t*)s4, sign, mag, (uint16_t*)s16);
+    } else {
+      requant_2bit_kernel<<<grid_for(n_groups, 256), 256, 0, (cudaStream_t)stream>>>(
+          n_groups, (const uint4*)codes, (const uint16_t*)s4, sign, mag, (uint16_t*)s16,
+          (uint4*)dcodes, (uint16_t*)ds4);
+    }
   }
   MOET_CUDA_TRY(cudaGetLastError());
   return MOET_OK;
