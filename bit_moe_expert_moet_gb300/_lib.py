@@ -86,7 +86,7 @@ def _ptr(t: Optional[torch.Tensor], dtype=None, name: str = "") -> Optional[int]
     return t.data_ptr()
 
 
-KERNEL_KINDS = ("requant", "quantize", "route", "prologue", "fc1", "fc2", "combine")
+KERNEL_KINDS = ("requant", "quantize", "route", "prologue", "fc1", "fc2", "combine", "terms")
 
 
 def profile_enable(on: bool = True):
@@ -191,3 +191,4 @@ def moe_forward(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
         _ptr(gate_mask, torch.uint8, "gate_mask"), _ptr(y, None, "y"),
         _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+

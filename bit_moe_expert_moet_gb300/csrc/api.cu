@@ -86,9 +86,10 @@ extern "C" moet_status moet_profile_read(int* launches, int* timed, float* total
   return st;
 }
 
-extern "C" int moet_internal_error_requant(void);
-extern "C" int moet_internal_error_route(void);
-extern "C" int moet_internal_error_moe(void);
+extern "C" __attribute__((visibility("hidden"))) int moet_internal_error_requant(void);
+extern "C" __attribute__((visibility("hidden"))) int moet_internal_error_route(void);
+extern "C" __attribute__((visibility("hidden"))) int moet_internal_error_moe(void);
+extern "C" __attribute__((visibility("hidden"))) int moet_internal_error_moe_tc(void);
 
 extern "C" const char* moet_status_string(moet_status s) {
   switch (s) {
@@ -108,8 +109,8 @@ extern "C" const char* moet_status_string(moet_status s) {
 extern "C" moet_status moet_last_device_error(moet_stream stream) {
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MOET_ERR_CUDA;
   int first = 0;
-  const int codes[3] = {moet_internal_error_requant(), moet_internal_error_route(),
-                        moet_internal_error_moe()};
+  const int codes[4] = {moet_internal_error_requant(), moet_internal_error_route(),
+                        moet_internal_error_moe(), moet_internal_error_moe_tc()};
   for (int c : codes) {
     if (c < 0) return MOET_ERR_CUDA;
     if (first == 0 && c != 0) first = c;

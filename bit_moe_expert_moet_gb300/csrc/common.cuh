@@ -138,7 +138,7 @@ struct ProfScope {
 // (blocking copy; the caller has synchronised the stream).  Returns -1 if the
 // copy fails.
 #define MOET_ERROR_ACCESSOR(name)                                                   \
-  extern "C" int name(void) {                                                       \
+  extern "C" __attribute__((visibility("hidden"))) int name(void) {                                                       \
     int v = 0;                                                                      \
     if (cudaMemcpyFromSymbol(&v, moet::g_device_error, sizeof(int)) != cudaSuccess) \
       return -1;                                                                    \

@@ -32,6 +32,7 @@
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "moe_tc.cuh"
 
 namespace moet {
 
@@ -41,14 +42,17 @@ constexpr int kSmemBudget = 96 * 1024;
 constexpr uint32_t kCodeLut = 0xC242BC3Cu;  // f16 high bytes of +1, -1, +3, -3
 
 struct WsLayout {
-  size_t hdr, tok_scale, hmax, chunks, h, o, total;
+  size_t hdr, tok_scale, hmax, chunks, h, o, xt, ht, total;
 };
+
+// Largest T routed through the tcgen05 engine (small tokens-per-expert regime).
+constexpr int kTcMaxT = 512;
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-__host__ __device__ inline int max_chunks(int T, int E, int k) {
+__host__ __device__ inline int max_chunks(int T, int E, int k, int chunk) {
   const long long pairs = (long long)T * k;
-  return (int)((pairs < E ? pairs : E) + (pairs + kChunk - 1) / kChunk);
+  return (int)((pairs < E ? pairs : E) + (pairs + chunk - 1) / chunk);
 }
 
 inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
@@ -58,9 +62,14 @@ inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   L.hdr = off;       off += align256(16);
   L.tok_scale = off; off += align256(sizeof(float) * T);
   L.hmax = off;      off += align256(sizeof(unsigned) * pairs);
-  L.chunks = off;    off += align256(sizeof(int4) * (size_t)max_chunks(T, E, k));
+  L.chunks = off;    off += align256(sizeof(int4) * (size_t)max_chunks(T, E, k, kTcTok));
   L.h = off;         off += align256(sizeof(float) * pairs * I);
   L.o = off;         off += align256(sizeof(float) * pairs * H);
+  L.xt = off; L.ht = off;
+  if (T <= kTcMaxT && tc_supported(H, I)) {
+    L.xt = off;      off += align256(tc_terms_bytes((size_t)T, (size_t)H));
+    L.ht = off;      off += align256(tc_terms_bytes(pairs, (size_t)I));
+  }
   L.total = off;
   return L;
 }
@@ -77,7 +86,7 @@ __device__ __forceinline__ float pow2_scale_for(float amax) {
 
 // ---------------------------------------------------------------- prologue
 __global__ void __launch_bounds__(kThreads) prologue_kernel(
-    int T, int H, int E, int k, const uint16_t* __restrict__ x, const int32_t* __restrict__ offsets,
+    int T, int H, int E, int k, int chunk, const uint16_t* __restrict__ x, const int32_t* __restrict__ offsets,
     int* __restrict__ hdr, float* __restrict__ tok_scale, unsigned* __restrict__ hmax,
     int4* __restrict__ chunks) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -92,7 +101,7 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(
         n = __ldg(offsets + e + 1) - __ldg(offsets + e);
         if (n < 0) { ok = false; n = 0; }
       }
-      const int nch = (n + kChunk - 1) / kChunk;
+      const int nch = (n + chunk - 1) / chunk;
       int incl = nch;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -101,8 +110,8 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(
       }
       const int first = running + incl - nch;
       for (int c = 0; c < nch; ++c) {
-        const int cnt = min(kChunk, n - c * kChunk);
-        chunks[first + c] = make_int4(e, c * kChunk, cnt, 0);
+        const int cnt = min(chunk, n - c * chunk);
+        chunks[first + c] = make_int4(e, c * chunk, cnt, 0);
       }
       running += __shfl_sync(0xffffffffu, incl, 31);
     }
@@ -512,14 +521,38 @@ extern "C" moet_status moet_moe_forward(int T, int H, int I, int E, int k, const
   float* h = reinterpret_cast<float*>(ws + L.h);
   float* o = reinterpret_cast<float*>(ws + L.o);
 
+  const bool use_tc = T <= kTcMaxT && tc_supported(H, I);
+  const int chunk = use_tc ? kTcTok : kChunk;
   {
     ProfScope ps(MOET_K_PROLOGUE, st);
-    prologue_kernel<<<1 + (T + 7) / 8, kThreads, 0, st>>>(T, H, E, k, x, expert_offsets, hdr, tok_scale,
-                                                           hmax, chunks);
+    prologue_kernel<<<1 + (T + 7) / 8, kThreads, 0, st>>>(T, H, E, k, chunk, x, expert_offsets, hdr,
+                                                           tok_scale, hmax, chunks);
   }
   MOET_CUDA_TRY(cudaGetLastError());
 
-  const int mc = max_chunks(T, E, k);
+  const int mc = max_chunks(T, E, k, chunk);
+  if (use_tc) {
+    TcForwardArgs f{};
+    f.T = T; f.H = H; f.I = I; f.E = E; f.k = k;
+    f.x = x; f.offsets = expert_offsets; f.perm = perm; f.topk_w = topk_w;
+    f.fc1 = fc1; f.fc2 = fc2;
+    f.delta_slot = with_delta ? delta_slot : nullptr;
+    f.n_slots = n_slots; f.dfc1 = dfc1; f.dfc2 = dfc2;
+    f.gate = with_delta ? gate_mask : nullptr;
+    f.hdr = hdr; f.chunks = chunks; f.h = h; f.o = o; f.max_items = mc;
+    const size_t pairs = (size_t)T * k;
+    auto carve = [](char* base, size_t rows, size_t K, uint8_t** cperm, uint8_t** cnat, uint8_t** sf, float** g) {
+      size_t off = 0;
+      *cperm = reinterpret_cast<uint8_t*>(base + off); off += align256(rows * kTcTerms * (K / 2));
+      *cnat = reinterpret_cast<uint8_t*>(base + off);  off += align256(rows * kTcTerms * (K / 2));
+      *sf = reinterpret_cast<uint8_t*>(base + off);    off += align256(rows * kTcTerms * (K / 16));
+      *g = reinterpret_cast<float*>(base + off);
+    };
+    carve(ws + L.xt, (size_t)T, (size_t)H, &f.buf.x_cperm, &f.buf.x_cnat, &f.buf.x_sf, &f.buf.x_g);
+    carve(ws + L.ht, pairs, (size_t)I, &f.buf.h_cperm, &f.buf.h_cnat, &f.buf.h_sf, &f.buf.h_g);
+    moet_status s = tc_forward(f, st);
+    if (s != MOET_OK) return s;
+  } else {
   const int maxn = T < kChunk ? T : kChunk;
   const int nt = maxn <= 8 ? 1 : maxn <= 16 ? 2 : maxn <= 32 ? 4 : 8;
   FcArgs a{};
@@ -545,6 +578,7 @@ extern "C" moet_status moet_moe_forward(int T, int H, int I, int E, int k, const
   a2.out = o;
   s = dispatch_fc<false>(a2, nt, H / 128, mc, st);
   if (s != MOET_OK) return s;
+  }
 
   long long n4 = (long long)T * H / 4;
   int gc = (int)((n4 + kThreads - 1) / kThreads);

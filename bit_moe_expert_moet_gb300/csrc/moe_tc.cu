@@ -1,0 +1,548 @@
+// tcgen05 block-scaled FC engine for the decode regime (sm_103a).
+//
+// README "Frontier MoE on consumer Blackwell (SM120)", "How it fits -- 2-bit
+// experts at FP4 quality": decode is HBM-bound, so the 2-bit planes must stream
+// at memory speed.  The pages' SM120 kernels feed block-scaled MMAs from a
+// PRMT-LUT decode; on sm_103a the block-scaled MMA is tcgen05.mma
+// kind::mxf4nvf4 (e2m1 operands, ue4m3 scale per 16 elements, fp32 in TMEM).
+//
+// Weights.  The 2-bit level set {+-1, +-3} is, halved, exactly the e2m1 values
+// {+-0.5, +-1.5}, and s16 is exactly a ue4m3 block-16 scale.  So the planes
+// become an exact NVFP4 A operand: each thread expands one weight row of the
+// 128-row tile (sign and magnitude words -> e2m1 nibbles s|0|m|1) with a
+// handful of integer ops per 8 weights, stores it to shared memory in the
+// 128-byte-swizzled K-major layout, and writes the row scales to TMEM; the
+// tensor core applies the block scale.  The factor 2 of the halved levels is
+// applied in the epilogue.
+//
+// Activations.  Each activation row (bf16 token for FC1, fp32 h for FC2) is
+// expanded into kTcTerms NVFP4 terms r = sum_t g_t * e2m1 * ue4m3, each term
+// quantising the residual of the previous ones (the residual shrinks about
+// 6x per term, so 4 terms leave ~1e-3 of the row's block maxima, well inside
+// the 5e-3 output tolerance).  The MMA's N dimension holds (token, term)
+// pairs; the epilogue sums the terms with their fp32 scales g_t.
+//
+// K order.  Inside each 16-element block the MMA sees the weights in the
+// order produced by the expansion (position 8r + n holds element
+// r + 4 (n & 3) + 2 (n >> 2)); the activation terms are stored in the same
+// order ("cperm").  The delta (already NVFP4) is used in its natural order
+// against a naturally ordered copy of the terms ("cnat") and accumulates in
+// a second TMEM region.
+//
+// Pipeline per CTA (128 threads = 4 warps; thread t owns tile row t):
+// 4 stages of {A 16 KB, B 8 KB, SFA 16 TMEM columns, SFB 16 TMEM columns}
+// per 256-weight K chunk; all threads fill a stage, one thread issues the 4
+// MMAs (K = 64 each) and commits them to the stage's mbarrier, which the
+// producers wait on (bounded) before refilling the stage.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "moe_tc.cuh"
+
+namespace moet {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kStages = 4;
+constexpr int kKC = 256;                      // weights per K chunk (one SW128 atom)
+constexpr int kMaxN = kTcTerms * kTcTok;      // 64 columns of D
+constexpr int kTmemCols = 256;
+constexpr int kColD = 0, kColD2 = 64, kColSFA = 128, kColSFB = 192;
+constexpr int kABytes = 128 * 128;            // one stage of A: 128 rows x 128 B
+constexpr int kBBytes = kMaxN * 128;          // one stage of B: 64 rows x 128 B
+constexpr long long kWaitLimit = 1LL << 22;   // polls before a wait is declared stuck
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// SW128 K-major shared-memory matrix descriptor: 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;                 // leading byte offset (unused with this swizzle)
+  d |= (uint64_t)(1024 >> 4) << 32;       // stride byte offset
+  d |= (uint64_t)1 << 46;                 // descriptor version
+  d |= (uint64_t)2 << 61;                 // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: kind::mxf4nvf4, A and B e2m1, K-major, ue4m3 scales, M = 128.
+__device__ __forceinline__ uint32_t mxf4_idesc(int n) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
+}
+
+// Bounded wait for the mbarrier phase with the given parity; false if it gave up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_addr(bar);
+  for (long long it = 0; it < kWaitLimit; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(done)
+        : "r"(a), "r"(parity));
+    if (done) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t sfa,
+                                       uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p; }"
+      ::"r"(d), "l"(ad), "l"(bd), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc));
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar)));
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t v[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]));
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Sign word S and magnitude word M of 32 weights (LSB first) -> 4 words of e2m1
+// nibbles (s | 0 | m | 1) = +-0.5 / +-1.5, in the permuted K order.
+__device__ __forceinline__ uint4 planes_to_e2m1(uint32_t S, uint32_t M) {
+  const uint32_t xs = (S & 0x0000FFFFu) | ((S << 14) & 0xFFFF0000u);
+  const uint32_t ys = (S >> 16) | ((S >> 2) & 0xFFFF0000u);
+  const uint32_t xm = (M & 0x0000FFFFu) | ((M << 14) & 0xFFFF0000u);
+  const uint32_t ym = (M >> 16) | ((M >> 2) & 0xFFFF0000u);
+  uint4 o;
+  o.x = 0x11111111u | ((xm << 1) & 0x22222222u) | ((xs << 3) & 0x88888888u);
+  o.y = 0x11111111u | (xm & 0x22222222u) | ((xs << 2) & 0x88888888u);
+  o.z = 0x11111111u | ((ym << 1) & 0x22222222u) | ((ys << 3) & 0x88888888u);
+  o.w = 0x11111111u | (ym & 0x22222222u) | ((ys << 2) & 0x88888888u);
+  return o;
+}
+
+// ---------------------------------------------------------------- activation terms
+// One CTA per row.  Writes kTcTerms terms: codes in permuted and natural K
+// order, one ue4m3 scale per 16, and one fp32 scale per term.
+template <bool BF16_IN>
+__global__ void __launch_bounds__(kThreads) act_terms_kernel(int K, const void* __restrict__ src,
+                                                            const int32_t* __restrict__ row_src,
+                                                            int src_div, uint8_t* __restrict__ cperm,
+                                                            uint8_t* __restrict__ cnat, uint8_t* __restrict__ sfb,
+                                                            float* __restrict__ gsc) {
+  extern __shared__ float res[];              // [K] residual
+  __shared__ float red[kThreads / 32];
+  const int row = blockIdx.x, tid = threadIdx.x;
+  // row_src (optional) maps the output row to a source row: src_row = row_src[row] / src_div
+  const long long srow = row_src ? (long long)(__ldg(row_src + row) / src_div) : (long long)row;
+  if (BF16_IN) {
+    const uint16_t* s = static_cast<const uint16_t*>(src) + srow * K;
+    for (int i = tid; i < K; i += kThreads) res[i] = __uint_as_float((uint32_t)__ldg(s + i) << 16);
+  } else {
+    const float* s = static_cast<const float*>(src) + srow * K;
+    for (int i = tid; i < K; i += kThreads) res[i] = s[i];
+  }
+  __syncthreads();
+  const int nblk = K / 16;
+  for (int t = 0; t < kTcTerms; ++t) {
+    float m = 0.0f;
+    for (int i = tid; i < K; i += kThreads) m = fmaxf(m, fabsf(res[i]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((tid & 31) == 0) red[tid >> 5] = m;
+    __syncthreads();
+    m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    const float g = m / (6.0f * 448.0f);
+    const size_t term_row = (size_t)row * kTcTerms + t;
+    if (tid == 0) gsc[term_row] = g;
+    for (int b = tid; b < nblk; b += kThreads) {
+      float* r = res + 16 * b;
+      float bm = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) bm = fmaxf(bm, fabsf(r[j]));
+      uint32_t sf = 0;
+      float s = 0.0f;
+      if (g > 0.0f) {
+        sf = f32_to_e4m3_rn(bm / (6.0f * g));
+        s = e4m3_to_f32(sf) * g;
+      }
+      uint32_t code[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        uint32_t c = 0;
+        if (s > 0.0f) {
+          const uint32_t mg = e2m1_rne_mag(fabsf(r[j]), s);
+          const bool neg = r[j] < 0.0f && mg != 0u;
+          const float q = e2m1_mag_value(mg) * s;
+          r[j] -= neg ? -q : q;
+          c = mg | (neg ? 8u : 0u);
+        }
+        code[j] = c;
+      }
+      uint32_t nat0 = 0, nat1 = 0, per0 = 0, per1 = 0;
+#pragma unroll
+      for (int p = 0; p < 16; ++p) {
+        const int j = (p >> 3) + 4 * (p & 3) + 2 * ((p >> 2) & 1);
+        if (p < 8) {
+          nat0 |= code[p] << (4 * p);
+          per0 |= code[j] << (4 * p);
+        } else {
+          nat1 |= code[p] << (4 * (p - 8));
+          per1 |= code[j] << (4 * (p - 8));
+        }
+      }
+      *reinterpret_cast<uint2*>(cnat + term_row * (K / 2) + 8 * b) = make_uint2(nat0, nat1);
+      *reinterpret_cast<uint2*>(cperm + term_row * (K / 2) + 8 * b) = make_uint2(per0, per1);
+      sfb[term_row * (K / 16) + b] = (uint8_t)sf;
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------- FC kernel
+struct FcTcArgs {
+  int T, H, I, k, K, N;          // N = rows of one expert matrix
+  const int32_t* offsets;
+  const int32_t* perm;
+  const float* topk_w;
+  const uint32_t* sign;
+  const uint32_t* mag;
+  const uint8_t* s16;
+  const float* scale_2;
+  const int32_t* delta_slot;
+  int n_slots;
+  const uint8_t* dcodes;
+  const uint8_t* ds4;
+  const uint8_t* gate;
+  const int* hdr;
+  const int4* chunks;
+  const uint8_t* cperm;          // activation terms (rows: FC1 tokens, FC2 bucketed pairs)
+  const uint8_t* cnat;
+  const uint8_t* sfb;
+  const float* gsc;
+  float* out;
+};
+
+struct TcSmem {
+  uint64_t bar[kStages];
+  uint32_t tmem_base;
+  int stuck;
+  int any_gated;
+  int slot;
+  int src_row[kTcTok];           // activation-term row per token of the work item
+  float gate_f[kTcTok];
+  float gsc[kMaxN];              // term scales, column order
+  float wts[kTcTok];             // FC2: routing weight per pair
+  int pair[kTcTok];              // FC2: pair id per column token
+  float xchg[64][kTcTok];        // FC1: up values handed to the gate warps
+};
+
+template <bool FC1>
+__global__ void __launch_bounds__(kThreads, 2) fc_tc_kernel(const FcTcArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_dyn[];
+  // 1024-aligned operand stages, then the small shared state
+  unsigned char* base = smem_dyn + ((1024 - (smem_addr(smem_dyn) & 1023)) & 1023);
+  unsigned char* sA = base;                                    // [kStages][128][128]
+  unsigned char* sB = base + kStages * kABytes;                // [kStages][64][128]
+  TcSmem& sm = *reinterpret_cast<TcSmem*>(sB + kStages * kBBytes);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if ((int)blockIdx.y >= a.hdr[0]) return;
+  const int4 ch = a.chunks[blockIdx.y];
+  const int e = ch.x, ntok = ch.z;
+  const int pos0 = __ldg(a.offsets + e) + ch.y;
+  const int K = a.K, nkc = K / kKC;
+  const int ncols = ((kTcTerms * ntok + 15) / 16) * 16;        // MMA N (multiple of 16, <= 64)
+
+  if (tid == 0) {
+    sm.stuck = 0;
+    sm.any_gated = 0;
+    int slot = -1;
+    if (a.delta_slot != nullptr && a.gate != nullptr) {
+      slot = __ldg(a.delta_slot + e);
+      if (slot >= a.n_slots) { record_error(MOET_ERR_DEVICE_INDEX); slot = -1; }
+    }
+    sm.slot = slot;
+    for (int s = 0; s < kStages; ++s) mbar_init(&sm.bar[s], 1);
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&sm.tmem_base)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  __syncthreads();
+  if (tid < kTcTok) {
+    int srow = -1, pr = -1;
+    float gf = 0.0f, wv = 0.0f;
+    if (tid < ntok) {
+      const int p = __ldg(a.perm + pos0 + tid);
+      if (p < 0 || p >= a.T * a.k) {
+        record_error(MOET_ERR_DEVICE_INDEX);
+      } else {
+        const int tok = p / a.k;
+        srow = FC1 ? tok : pos0 + tid;
+        pr = p;
+        wv = __ldg(a.topk_w + p);
+        if (sm.slot >= 0 && __ldg(a.gate + tok)) { gf = 1.0f; sm.any_gated = 1; }
+      }
+    }
+    sm.src_row[tid] = srow;
+    sm.gate_f[tid] = gf;
+    sm.pair[tid] = pr;
+    sm.wts[tid] = wv;
+  }
+  __syncthreads();
+  if (tid < kMaxN) {
+    const int tk = tid / kTcTerms, term = tid % kTcTerms;
+    const int srow = tk < kTcTok ? sm.src_row[tk] : -1;
+    sm.gsc[tid] = srow >= 0 ? __ldg(a.gsc + (size_t)srow * kTcTerms + term) : 0.0f;
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;");
+  const uint32_t tmem = sm.tmem_base;
+  const bool do_delta = sm.slot >= 0 && sm.any_gated;
+  const uint32_t idesc = mxf4_idesc(ncols);
+
+  // the weight row owned by this thread
+  int wrow;
+  if (FC1) {
+    wrow = tid < 64 ? blockIdx.x * 64 + tid : a.I + blockIdx.x * 64 + (tid - 64);
+  } else {
+    wrow = blockIdx.x * 128 + tid;
+  }
+  // weight rows whose scales this thread writes to TMEM (replicated layout: rows lane + 32 j)
+  int srows[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int tr = lane + 32 * j;
+    srows[j] = FC1 ? (tr < 64 ? blockIdx.x * 64 + tr : a.I + blockIdx.x * 64 + (tr - 64)) : blockIdx.x * 128 + tr;
+  }
+  const size_t wpr = (size_t)K / 32, bpr = (size_t)K / 16;
+  const uint32_t lane_q = (uint32_t)(warp * 32) << 16;      // this warp's TMEM lane quarter
+
+  const int npass = do_delta ? 2 : 1;
+  int cglob = 0;                                             // chunk counter across passes
+  for (int pass = 0; pass < npass; ++pass) {
+    const bool dp = pass == 1;
+    const uint32_t* Sp = a.sign + ((size_t)e * a.N + wrow) * wpr;
+    const uint32_t* Mp = a.mag + ((size_t)e * a.N + wrow) * wpr;
+    const uint8_t* Dp = dp ? a.dcodes + ((size_t)sm.slot * a.N + wrow) * (K / 2) : nullptr;
+    const uint8_t* Q = dp ? a.ds4 : a.s16;
+    const size_t qbase = dp ? (size_t)sm.slot * a.N : (size_t)e * a.N;
+    const uint8_t* act = dp ? a.cnat : a.cperm;
+    const uint32_t dcol = dp ? kColD2 : kColD;
+
+    for (int c = 0; c < nkc; ++c, ++cglob) {
+      const int s = cglob % kStages;
+      if (cglob >= kStages) {
+        if (!mbar_wait(&sm.bar[s], ((cglob / kStages) - 1) & 1)) atomicExch(&sm.stuck, 1);
+      }
+      __syncthreads();
+      if (sm.stuck) break;
+      // ---- A: this thread's weight row, 256 weights = 128 bytes, 128B-swizzled
+      unsigned char* arow = sA + s * kABytes + tid * 128;
+      if (!dp) {
+        const uint4* sp = reinterpret_cast<const uint4*>(Sp + (size_t)c * 8);
+        const uint4* mp = reinterpret_cast<const uint4*>(Mp + (size_t)c * 8);
+        const uint4 s0 = ldg_nc_v4(sp), s1 = ldg_nc_v4(sp + 1), m0 = ldg_nc_v4(mp), m1 = ldg_nc_v4(mp + 1);
+        const uint32_t SW[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+        const uint32_t MW[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+        for (int w = 0; w < 8; ++w)
+          *reinterpret_cast<uint4*>(arow + ((w ^ (tid & 7)) << 4)) = planes_to_e2m1(SW[w], MW[w]);
+      } else {
+        const uint4* dp4 = reinterpret_cast<const uint4*>(Dp + (size_t)c * 128);
+#pragma unroll
+        for (int w = 0; w < 8; ++w) *reinterpret_cast<uint4*>(arow + ((w ^ (tid & 7)) << 4)) = ldg_nc_v4(dp4 + w);
+      }
+      // ---- SFA: rows lane + 32 j, 16 block scales of this chunk -> columns 4 i + j
+      {
+        uint32_t v[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 q = ldg_nc_v4(Q + (qbase + srows[j]) * bpr + (size_t)c * 16);
+          v[0 * 4 + j] = q.x; v[1 * 4 + j] = q.y; v[2 * 4 + j] = q.z; v[3 * 4 + j] = q.w;
+        }
+        tmem_st16(tmem + lane_q + kColSFA + 16 * s, v);
+      }
+      // ---- B: activation-term rows n = token * kTcTerms + term
+      unsigned char* bst = sB + s * kBBytes;
+      for (int it = tid; it < ncols * 8; it += kThreads) {
+        const int n = it >> 3, u = it & 7;
+        const int tk = n / kTcTerms, term = n % kTcTerms;
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        const int srow = tk < ntok ? sm.src_row[tk] : -1;
+        if (srow >= 0 && (!dp || sm.gate_f[tk] != 0.0f)) {
+          const uint8_t* src = act + ((size_t)srow * kTcTerms + term) * (K / 2) + (size_t)c * 128;
+          val = ldg_nc_v4(src + 16 * u);
+        }
+        *reinterpret_cast<uint4*>(bst + n * 128 + ((u ^ (n & 7)) << 4)) = val;
+      }
+      // ---- SFB: B rows lane + 32 j (j < 2 since N <= 64)
+      {
+        uint32_t v[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int n = lane + 32 * j;
+          uint4 q = make_uint4(0u, 0u, 0u, 0u);
+          if (n < ncols) {
+            const int tk = n / kTcTerms, term = n % kTcTerms;
+            const int srow = tk < ntok ? sm.src_row[tk] : -1;
+            if (srow >= 0) q = ldg_nc_v4(a.sfb + ((size_t)srow * kTcTerms + term) * bpr + (size_t)c * 16);
+          }
+          v[0 * 4 + j] = q.x; v[1 * 4 + j] = q.y; v[2 * 4 + j] = q.z; v[3 * 4 + j] = q.w;
+        }
+        tmem_st16(tmem + lane_q + kColSFB + 16 * s, v);
+      }
+      asm volatile("fence.proxy.async.shared::cta;");
+      asm volatile("tcgen05.wait::st.sync.aligned;");
+      asm volatile("tcgen05.fence::before_thread_sync;");
+      __syncthreads();
+      if (tid == 0) {
+        asm volatile("tcgen05.fence::after_thread_sync;");
+        const uint32_t a0 = smem_addr(sA + s * kABytes), b0 = smem_addr(sB + s * kBBytes);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          tc_mma(tmem + dcol, sw128_desc(a0 + 32 * i), sw128_desc(b0 + 32 * i), idesc,
+                 tmem + kColSFA + 16 * s + 4 * i, tmem + kColSFB + 16 * s + 4 * i, (c > 0 || i > 0) ? 1u : 0u);
+        }
+        tc_commit(&sm.bar[s]);
+      }
+    }
+    if (sm.stuck) break;
+  }
+  // ---- drain: every stage's last commit (bounded), then read the accumulators
+  const int issued = cglob;
+  for (int s = 0; s < kStages && s < issued; ++s) {
+    const int last = issued - 1 - ((issued - 1 - s) % kStages);   // last chunk that used stage s
+    if (!mbar_wait(&sm.bar[s], (last / kStages) & 1)) atomicExch(&sm.stuck, 1);
+  }
+  asm volatile("tcgen05.fence::after_thread_sync;");
+  __syncthreads();
+  if (sm.stuck) {
+    if (tid == 0) record_error(MOET_ERR_TIMEOUT);
+  } else {
+    const float sc2 = 2.0f * __ldg(a.scale_2 + e);           // 2: the halved e2m1 levels
+    const float sc2d = __ldg(a.scale_2 + e);
+    for (int c0 = 0; c0 < ncols; c0 += 16) {
+      float v[16], v2[16];
+      tmem_ld16(tmem + lane_q + kColD + c0, v);
+      if (do_delta) tmem_ld16(tmem + lane_q + kColD2 + c0, v2);
+      float acc[16 / kTcTerms];
+#pragma unroll
+      for (int q = 0; q < 16 / kTcTerms; ++q) {
+        float sacc = 0.0f;
+#pragma unroll
+        for (int t = 0; t < kTcTerms; ++t) {
+          const int col = q * kTcTerms + t;
+          float d = sc2 * v[col];
+          if (do_delta) d = fmaf(sc2d, v2[col], d);
+          sacc = fmaf(sm.gsc[c0 + col], d, sacc);
+        }
+        acc[q] = sacc;
+      }
+      if (!FC1) {
+#pragma unroll
+        for (int q = 0; q < 16 / kTcTerms; ++q) {
+          const int tk = c0 / kTcTerms + q;
+          if (tk < ntok && sm.src_row[tk] >= 0) a.out[(size_t)sm.pair[tk] * a.H + wrow] = acc[q] * sm.wts[tk];
+        }
+      } else {
+        // up rows (threads 64..127) hand their values to the gate rows (threads 0..63)
+        if (tid >= 64) {
+#pragma unroll
+          for (int q = 0; q < 16 / kTcTerms; ++q) sm.xchg[tid - 64][c0 / kTcTerms + q] = acc[q];
+        }
+        __syncthreads();
+        if (tid < 64) {
+#pragma unroll
+          for (int q = 0; q < 16 / kTcTerms; ++q) {
+            const int tk = c0 / kTcTerms + q;
+            if (tk < ntok && sm.src_row[tk] >= 0) {
+              const float gv = acc[q], uv = sm.xchg[tid][tk];
+              a.out[(size_t)(pos0 + tk) * a.I + wrow] = gv / (1.0f + expf(-gv)) * uv;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;");
+  __syncthreads();
+  if (warp == 0) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+  }
+}
+
+template <bool FC1>
+moet_status launch_fc_tc(const FcTcArgs& a, int row_tiles, int grid_y, cudaStream_t st) {
+  const size_t smem = 1024 + kStages * (kABytes + kBBytes) + sizeof(TcSmem);
+  auto kern = fc_tc_kernel<FC1>;
+  MOET_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  {
+    ProfScope ps(FC1 ? MOET_K_FC1 : MOET_K_FC2, st);
+    kern<<<dim3(row_tiles, grid_y), kThreads, smem, st>>>(a);
+  }
+  MOET_CUDA_TRY(cudaGetLastError());
+  return MOET_OK;
+}
+
+}  // namespace
+
+moet_status tc_forward(const TcForwardArgs& f, cudaStream_t st) {
+  const int pairs = f.T * f.k;
+  // FC1 input terms: one row per token
+  {
+    ProfScope ps(MOET_K_TERMS, st);
+    act_terms_kernel<true><<<f.T, kThreads, sizeof(float) * f.H, st>>>(
+        f.H, f.x, nullptr, 1, f.buf.x_cperm, f.buf.x_cnat, f.buf.x_sf, f.buf.x_g);
+  }
+  MOET_CUDA_TRY(cudaGetLastError());
+  FcTcArgs a{};
+  a.T = f.T; a.H = f.H; a.I = f.I; a.k = f.k;
+  a.offsets = f.offsets; a.perm = f.perm; a.topk_w = f.topk_w;
+  a.delta_slot = f.delta_slot; a.n_slots = f.n_slots; a.gate = f.gate;
+  a.hdr = f.hdr; a.chunks = f.chunks;
+  FcTcArgs a1 = a;
+  a1.K = f.H; a1.N = 2 * f.I;
+  a1.sign = f.fc1->sign; a1.mag = f.fc1->mag; a1.s16 = f.fc1->s16; a1.scale_2 = f.fc1->scale_2;
+  if (f.delta_slot) { a1.dcodes = f.dfc1->codes; a1.ds4 = f.dfc1->s4; }
+  a1.cperm = f.buf.x_cperm; a1.cnat = f.buf.x_cnat; a1.sfb = f.buf.x_sf; a1.gsc = f.buf.x_g;
+  a1.out = f.h;
+  moet_status s = launch_fc_tc<true>(a1, f.I / 64, f.max_items, st);
+  if (s != MOET_OK) return s;
+  // FC2 input terms: one row per bucketed pair (h rows are in bucketed order)
+  {
+    ProfScope ps(MOET_K_TERMS, st);
+    act_terms_kernel<false><<<pairs, kThreads, sizeof(float) * f.I, st>>>(
+        f.I, f.h, nullptr, 1, f.buf.h_cperm, f.buf.h_cnat, f.buf.h_sf, f.buf.h_g);
+  }
+  MOET_CUDA_TRY(cudaGetLastError());
+  FcTcArgs a2 = a;
+  a2.K = f.I; a2.N = f.H;
+  a2.sign = f.fc2->sign; a2.mag = f.fc2->mag; a2.s16 = f.fc2->s16; a2.scale_2 = f.fc2->scale_2;
+  if (f.delta_slot) { a2.dcodes = f.dfc2->codes; a2.ds4 = f.dfc2->s4; }
+  a2.cperm = f.buf.h_cperm; a2.cnat = f.buf.h_cnat; a2.sfb = f.buf.h_sf; a2.gsc = f.buf.h_g;
+  a2.out = f.o;
+  return launch_fc_tc<false>(a2, f.H / 128, f.max_items, st);
+}
+
+}  // namespace moet
+
+MOET_ERROR_ACCESSOR(moet_internal_error_moe_tc)

@@ -176,7 +176,8 @@ typedef enum {
   MOET_K_FC1 = 4,
   MOET_K_FC2 = 5,
   MOET_K_COMBINE = 6,
-  MOET_KERNEL_KINDS = 7
+  MOET_K_TERMS = 7, /* activation -> NVFP4 term expansion of the tensor-core path */
+  MOET_KERNEL_KINDS = 8
 } moet_kernel_kind;
 
 moet_status moet_profile_enable(int on);

@@ -184,8 +184,11 @@ def _make_layer(moet, H, I, E, dset, rng=None, cfg=None):
         rq = [orq.requant_2bit(codes[e], s4[e]) for e in range(E)]
         for key in ("sign", "mag", "s16", "dcodes", "ds4"):
             assert np.array_equal(np.stack([r[key] for r in rq]), got[key])
-        ref[f] = dict(sign=got["sign"], mag=got["mag"], s16=got["s16"], scale_2=sc2)
-        ref[f, "d"] = dict(codes=got["dcodes"][dset], s4=got["ds4"][dset])
+        # the oracle runs on its own requant output (identical to the GPU's, checked above)
+        ref[f] = dict(sign=np.stack([r["sign"] for r in rq]), mag=np.stack([r["mag"] for r in rq]),
+                      s16=np.stack([r["s16"] for r in rq]), scale_2=sc2)
+        ref[f, "d"] = dict(codes=np.stack([r["dcodes"] for r in rq])[dset],
+                           s4=np.stack([r["ds4"] for r in rq])[dset])
         gp[f] = moet.Planes(dev(got["sign"].view(np.int32)), dev(got["mag"].view(np.int32)), dev(got["s16"]), dev(sc2))
         gp[f, "d"] = moet.DeltaPool(dev(got["dcodes"][dset]), dev(got["ds4"][dset]))
     return ref, gp
@@ -236,9 +239,10 @@ def test_forward_tiny_layer(moet, gate_mode):
     check_y(yg, yo)
 
 
-@pytest.mark.parametrize("T", [1, 9, 33, 100, 300])
+@pytest.mark.parametrize("T", [1, 9, 33, 100, 300, 600])
 def test_forward_mid_size(moet, T):
-    """Several row tiles, K slices, N-tiles and chunks (T=300 gives > 64 pairs per expert)."""
+    """Several row tiles, K chunks, N-tiles and work items (T=300 gives > 64 pairs per
+    expert; T <= 512 runs the tcgen05 engine, T=600 the mma.sync engine)."""
     H, I, E, k = 1024, 256, 16, 4
     rng = np.random.default_rng(30 + T)
     dset = np.array([1, 4, 5, 11], dtype=np.int32)
