@@ -28,4 +28,6 @@ from ._lib import (  # noqa: F401
     route_topk,
     forward_workspace_size,
     moe_forward,
+    moe_forward_static,
+    FORWARD_STATIC_SCRATCH_BYTES,
 )

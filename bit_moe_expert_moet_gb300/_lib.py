@@ -43,6 +43,12 @@ lib.moet_route_topk.restype = _i
 lib.moet_route_topk.argtypes = [_i, _i, _i, _p, _p, _p, _p, _p, _p]
 lib.moet_forward_workspace_size.restype = _sz
 lib.moet_forward_workspace_size.argtypes = [_i, _i, _i, _i, _i]
+lib.moet_moe_forward_static.restype = _i
+lib.moet_moe_forward_static.argtypes = [_i, _i, _i, _i, _i, _p, _p, _p, _p, _p,
+                                        ctypes.POINTER(_Planes), ctypes.POINTER(_Planes),
+                                        _p, _i, ctypes.POINTER(_Nvfp4), ctypes.POINTER(_Nvfp4),
+                                        _p, _p, _p]
+FORWARD_STATIC_SCRATCH_BYTES = 8 << 20
 lib.moet_profile_enable.restype = _i
 lib.moet_profile_enable.argtypes = [_i]
 lib.moet_profile_read.restype = _i
@@ -192,3 +198,33 @@ def moe_forward(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
         _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
         _stream(stream)))
 
+
+def moe_forward_static(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
+                       expert_offsets: torch.Tensor, perm: torch.Tensor, fc1: Planes, fc2: Planes,
+                       y: torch.Tensor, delta_slot: Optional[torch.Tensor] = None,
+                       dfc1: Optional[DeltaPool] = None, dfc2: Optional[DeltaPool] = None,
+                       gate_mask: Optional[torch.Tensor] = None, stream=None):
+    """moe_forward without a workspace, for callers that cannot allocate device
+    memory: the scratch is a fixed 8 MiB array inside the library's device image
+    (shared by all calls; overlapping calls must be serialised by the caller)."""
+    T, H = x.shape
+    E = fc1.scale_2.shape[0]
+    I = fc2.sign.shape[2] * 32
+    k = topk_idx.shape[1]
+    if x.dtype != torch.bfloat16 or y.dtype != torch.bfloat16:
+        raise TypeError("x and y must be bfloat16")
+    c1, c2 = fc1._c("fc1"), fc2._c("fc2")
+    n_slots = 0
+    d1 = d2 = None
+    if delta_slot is not None:
+        if dfc1 is None or dfc2 is None or gate_mask is None:
+            raise ValueError("delta_slot needs dfc1, dfc2 and gate_mask")
+        n_slots = dfc1.codes.shape[0]
+        d1, d2 = dfc1._c("dfc1"), dfc2._c("dfc2")
+    _check("moet_moe_forward_static", lib.moet_moe_forward_static(
+        T, H, I, E, k, _ptr(x, None, "x"), _ptr(topk_idx, torch.int32, "topk_idx"),
+        _ptr(topk_w, torch.float32, "topk_w"), _ptr(expert_offsets, torch.int32, "expert_offsets"),
+        _ptr(perm, torch.int32, "perm"), ctypes.byref(c1), ctypes.byref(c2),
+        _ptr(delta_slot, torch.int32, "delta_slot"), n_slots,
+        ctypes.byref(d1) if d1 is not None else None, ctypes.byref(d2) if d2 is not None else None,
+        _ptr(gate_mask, torch.uint8, "gate_mask"), _ptr(y, None, "y"), _stream(stream)))

@@ -159,6 +159,36 @@ moet_status moet_moe_forward(int T, int H, int I, int E, int k, const uint16_t* 
                              void* workspace, size_t ws_bytes, moet_stream stream);
 
 /* ------------------------------------------------------------------------
+ * moet_moe_forward_static -- moet_moe_forward for callers that cannot
+ * allocate device memory (a plug-in given only its input and output buffers,
+ * code inside a runtime whose device allocator belongs to someone else, a C
+ * caller with no allocator).  The pages describe no such entry point; it is
+ * an addition of this library.  Same arguments and results as
+ * moet_moe_forward, without `workspace`/`ws_bytes`: the scratch is a fixed
+ * array of MOET_FORWARD_STATIC_SCRATCH_BYTES in the library's device image,
+ * present on every GPU that loads the library until the process exits.
+ * Nothing is allocated or freed.
+ *  - Returns MOET_ERR_WORKSPACE, enqueueing nothing, when the layer needs
+ *    more scratch than that (moet_forward_workspace_size(T,H,I,E,k) >
+ *    MOET_FORWARD_STATIC_SCRATCH_BYTES); e.g. H=7168, I=2048, E=256, k=8 fits
+ *    up to T=21 tokens.
+ *  - The first call on a device (with that device current) looks the array's
+ *    device address up with cudaGetSymbolAddress; make it before any stream
+ *    capture.
+ *  - Every call uses the same array and leaves its contents behind; calls
+ *    that overlap on the GPU race on it, so the caller must serialise them.
+ *    No scratch contents need to start at zero. */
+#define MOET_FORWARD_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
+
+moet_status moet_moe_forward_static(int T, int H, int I, int E, int k, const uint16_t* x,
+                                    const int32_t* topk_idx, const float* topk_w,
+                                    const int32_t* expert_offsets, const int32_t* perm,
+                                    const moet_planes* fc1, const moet_planes* fc2,
+                                    const int32_t* delta_slot, int n_slots, const moet_nvfp4* dfc1,
+                                    const moet_nvfp4* dfc2, const uint8_t* gate_mask, uint16_t* y,
+                                    moet_stream stream);
+
+/* ------------------------------------------------------------------------
  * Kernel timing (tracing aid, off by default).  While enabled, the library
  * records a CUDA event before and after each of its kernel launches on the
  * launching stream (so timings are on-device and per launch; leave it off
