@@ -474,25 +474,40 @@ def run_ours(args, rank, world, local):
     extras = {}
     if not args.no_extras and rank == 0:
         sweep = {}
-        for name in ("dsv3_decode_t1", "dsv3_decode_t8"):
-            c2 = W.CONFIGS[name]
-            if name == cfg.name or (c2.H, c2.I, c2.E) != (cfg.H, cfg.I, cfg.E):
-                continue
-            l2 = layer.rebatch(c2)
+
+        def timed(l2, steps, warmup):
             moet.profile_read()
             moet.profile_enable(True)
-            t2 = time_steps(torch, l2.step, args.steps, args.warmup, flush)
+            t2 = time_steps(torch, l2.step, steps, warmup, flush)
             moet.profile_enable(False)
             p2 = moet.profile_read()
             med = statistics.median(t2)
             f2 = p2["fc1"][2] / max(p2["fc1"][1], 1)
-            sweep[name] = {"T": c2.T, "tokens_per_s": c2.T / (med * 1e-3), "ms_per_step_median": med,
-                           "step_gbs": l2.bytes_total / (med * 1e-3) / 1e9,
-                           "step_frac_of_hbm": l2.bytes_total / (med * 1e-3) / 1e9 / peak,
-                           "fc1_gbs": l2.bytes_fc1 / (f2 * 1e-3) / 1e9,
-                           "fc1_frac_of_hbm": l2.bytes_fc1 / (f2 * 1e-3) / 1e9 / peak,
-                           "fc1_launch_ms": f2, "experts_touched": l2.n_used,
-                           "kernel_ms_per_launch": {k: v[2] / max(v[1], 1) for k, v in p2.items() if v[0]}}
+            return {"T": l2.cfg.T, "tokens_per_s": l2.cfg.T / (med * 1e-3), "ms_per_step_median": med,
+                    "step_gbs": l2.bytes_total / (med * 1e-3) / 1e9,
+                    "step_frac_of_hbm": l2.bytes_total / (med * 1e-3) / 1e9 / peak,
+                    "fc1_gbs": l2.bytes_fc1 / (f2 * 1e-3) / 1e9,
+                    "fc1_frac_of_hbm": l2.bytes_fc1 / (f2 * 1e-3) / 1e9 / peak,
+                    "fc1_launch_ms": f2, "experts_touched": l2.n_used, "delta_experts_touched": l2.n_delta,
+                    "kernel_ms_per_launch": {k: v[2] / max(v[1], 1) for k, v in p2.items() if v[0]}}
+
+        for name in ("dsv3_decode_t1", "dsv3_decode_t8", "dsv3_prefill"):
+            c2 = W.CONFIGS[name]
+            if name == cfg.name or (c2.H, c2.I, c2.E) != (cfg.H, cfg.I, cfg.E):
+                continue
+            l2 = layer.rebatch(c2)
+            r = timed(l2, args.steps if c2.T <= 512 else 3, args.warmup if c2.T <= 512 else 1)
+            if c2.T > 512:   # prefill: tensor work 6 H I flops per routed pair
+                flops = 6.0 * c2.H * c2.I * c2.T * c2.k
+                r["tflops"] = flops / (r["ms_per_step_median"] * 1e-3) / 1e12
+            sweep[name] = r
+            del l2
+        for name in ("glm_decode", "kimi_layer"):
+            c3 = W.CONFIGS[name]
+            l3 = Layer(moet, torch, c3, dev)
+            sweep[name] = timed(l3, args.steps, args.warmup)
+            del l3
+            torch.cuda.empty_cache()
         extras["decode_sweep"] = sweep
         extras["requant"] = time_requant(moet, torch, dev)
         extras["requant"]["frac_of_hbm_peak"] = extras["requant"]["gbs"] / peak

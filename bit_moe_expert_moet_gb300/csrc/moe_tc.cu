@@ -17,8 +17,8 @@
 //
 // Activations.  Each activation row (bf16 token for FC1, fp32 h for FC2) is
 // expanded into kTcTerms NVFP4 terms r = sum_t g_t * e2m1 * ue4m3, each term
-// quantising the residual of the previous ones (the residual shrinks about
-// 6x per term, so 4 terms leave ~1e-3 of the row's block maxima, well inside
+// quantising the residual of the previous ones (a block's residual shrinks at
+// least ~6x per term, so 4 terms leave ~1e-3 of the block maxima, well inside
 // the 5e-3 output tolerance).  The MMA's N dimension holds (token, term)
 // pairs; the epilogue sums the terms with their fp32 scales g_t.
 //
@@ -29,11 +29,13 @@
 // against a naturally ordered copy of the terms ("cnat") and accumulates in
 // a second TMEM region.
 //
-// Pipeline per CTA (128 threads = 4 warps; thread t owns tile row t):
-// 4 stages of {A 16 KB, B 8 KB, SFA 16 TMEM columns, SFB 16 TMEM columns}
-// per 256-weight K chunk; all threads fill a stage, one thread issues the 4
-// MMAs (K = 64 each) and commits them to the stage's mbarrier, which the
-// producers wait on (bounded) before refilling the stage.
+// Pipeline per CTA (128 threads = 4 warps; thread t owns tile row t): a ring
+// of kRing slots per 256-weight K chunk, each {A 16 KB, B 8 KB, raw planes
+// 8 KB, raw scales 3 KB, SFA 16 + SFB 16 TMEM columns}.  Chunks are fetched
+// kRing - 1 ahead with cp.async; for the current chunk every thread expands
+// its row into the swizzled A tile and writes scale factors to TMEM, one
+// thread issues the 4 MMAs (K = 64 each) and commits them to the slot's
+// mbarrier, and a slot is refilled only after (bounded wait) its MMAs are done.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -43,18 +45,28 @@ namespace moet {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kStages = 4;
+constexpr int kRing = 3;                      // chunks in flight (async copy + MMA)
 constexpr int kKC = 256;                      // weights per K chunk (one SW128 atom)
 constexpr int kMaxN = kTcTerms * kTcTok;      // 64 columns of D
 constexpr int kTmemCols = 256;
-constexpr int kColD = 0, kColD2 = 64, kColSFA = 128, kColSFB = 192;
-constexpr int kABytes = 128 * 128;            // one stage of A: 128 rows x 128 B
-constexpr int kBBytes = kMaxN * 128;          // one stage of B: 64 rows x 128 B
+constexpr int kColD = 0, kColD2 = 64, kColSFA = 128, kColSFB = 128 + 16 * kRing;
+// one ring slot: converted A (128 rows x 128 B, swizzled), B (64 rows x 128 B, swizzled),
+// raw planes (128 rows x 64 B), raw row scales (128 x 16 B), raw B scales (64 x 16 B)
+constexpr int kOffA = 0, kOffB = 16384, kOffRawA = 24576, kOffRawQ = 32768, kOffRawSfb = 34816;
+constexpr int kSlotBytes = 35840;
 constexpr long long kWaitLimit = 1LL << 22;   // polls before a wait is declared stuck
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
+
+// 16-byte asynchronous global->shared copy; src_bytes = 0 writes zeros and reads nothing.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes = 16) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N)); }
 
 // SW128 K-major shared-memory matrix descriptor: 8-row groups 1024 B apart.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
@@ -136,80 +148,107 @@ __device__ __forceinline__ uint4 planes_to_e2m1(uint32_t S, uint32_t M) {
 }
 
 // ---------------------------------------------------------------- activation terms
-// One CTA per row.  Writes kTcTerms terms: codes in permuted and natural K
-// order, one ue4m3 scale per 16, and one fp32 scale per term.
+// Grid (rows, ceil(K/16 / 128)): every CTA reads its row once for the row
+// maximum m, then each thread expands one 16-element block into kTcTerms
+// NVFP4 terms.  Term t has the fp32 scale g_t = m / (6 * 448) / 4^t and a
+// ue4m3 scale per block chosen from the block's current residual, so each
+// term quantises what the previous ones left (the residual of a block shrinks
+// at least ~6x per term while g_t shrinks 4x, keeping the block scales in the
+// normal e4m3 range).  Outputs per (row, term): codes in permuted and natural
+// K order, one ue4m3 scale per 16, and g_t.
 template <bool BF16_IN>
 __global__ void __launch_bounds__(kThreads) act_terms_kernel(int K, const void* __restrict__ src,
-                                                            const int32_t* __restrict__ row_src,
-                                                            int src_div, uint8_t* __restrict__ cperm,
-                                                            uint8_t* __restrict__ cnat, uint8_t* __restrict__ sfb,
-                                                            float* __restrict__ gsc) {
-  extern __shared__ float res[];              // [K] residual
+                                                            uint8_t* __restrict__ cperm, uint8_t* __restrict__ cnat,
+                                                            uint8_t* __restrict__ sfb, float* __restrict__ gsc) {
   __shared__ float red[kThreads / 32];
   const int row = blockIdx.x, tid = threadIdx.x;
-  // row_src (optional) maps the output row to a source row: src_row = row_src[row] / src_div
-  const long long srow = row_src ? (long long)(__ldg(row_src + row) / src_div) : (long long)row;
+  const uint16_t* sb = static_cast<const uint16_t*>(src) + (size_t)row * K;
+  const float* sf32 = static_cast<const float*>(src) + (size_t)row * K;
+  float m = 0.0f;
   if (BF16_IN) {
-    const uint16_t* s = static_cast<const uint16_t*>(src) + srow * K;
-    for (int i = tid; i < K; i += kThreads) res[i] = __uint_as_float((uint32_t)__ldg(s + i) << 16);
-  } else {
-    const float* s = static_cast<const float*>(src) + srow * K;
-    for (int i = tid; i < K; i += kThreads) res[i] = s[i];
-  }
-  __syncthreads();
-  const int nblk = K / 16;
-  for (int t = 0; t < kTcTerms; ++t) {
-    float m = 0.0f;
-    for (int i = tid; i < K; i += kThreads) m = fmaxf(m, fabsf(res[i]));
+    const uint4* p = reinterpret_cast<const uint4*>(sb);
+    for (int i = tid; i < K / 8; i += kThreads) {
+      const uint4 v = __ldg(p + i);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if ((tid & 31) == 0) red[tid >> 5] = m;
-    __syncthreads();
-    m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-    const float g = m / (6.0f * 448.0f);
-    const size_t term_row = (size_t)row * kTcTerms + t;
-    if (tid == 0) gsc[term_row] = g;
-    for (int b = tid; b < nblk; b += kThreads) {
-      float* r = res + 16 * b;
-      float bm = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) bm = fmaxf(bm, fabsf(r[j]));
-      uint32_t sf = 0;
-      float s = 0.0f;
-      if (g > 0.0f) {
-        sf = f32_to_e4m3_rn(bm / (6.0f * g));
-        s = e4m3_to_f32(sf) * g;
-      }
-      uint32_t code[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        uint32_t c = 0;
-        if (s > 0.0f) {
-          const uint32_t mg = e2m1_rne_mag(fabsf(r[j]), s);
-          const bool neg = r[j] < 0.0f && mg != 0u;
-          const float q = e2m1_mag_value(mg) * s;
-          r[j] -= neg ? -q : q;
-          c = mg | (neg ? 8u : 0u);
-        }
-        code[j] = c;
-      }
-      uint32_t nat0 = 0, nat1 = 0, per0 = 0, per1 = 0;
-#pragma unroll
-      for (int p = 0; p < 16; ++p) {
-        const int j = (p >> 3) + 4 * (p & 3) + 2 * ((p >> 2) & 1);
-        if (p < 8) {
-          nat0 |= code[p] << (4 * p);
-          per0 |= code[j] << (4 * p);
-        } else {
-          nat1 |= code[p] << (4 * (p - 8));
-          per1 |= code[j] << (4 * (p - 8));
-        }
-      }
-      *reinterpret_cast<uint2*>(cnat + term_row * (K / 2) + 8 * b) = make_uint2(nat0, nat1);
-      *reinterpret_cast<uint2*>(cperm + term_row * (K / 2) + 8 * b) = make_uint2(per0, per1);
-      sfb[term_row * (K / 16) + b] = (uint8_t)sf;
+      for (int q = 0; q < 4; ++q)
+        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[q] << 16)), fabsf(__uint_as_float(w[q] & 0xFFFF0000u))));
     }
-    __syncthreads();
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(sf32);
+    for (int i = tid; i < K / 4; i += kThreads) {
+      const float4 v = p[i];
+      m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((tid & 31) == 0) red[tid >> 5] = m;
+  __syncthreads();
+  m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  const float g0 = m / (6.0f * 448.0f);
+  const int b = blockIdx.y * kThreads + tid;
+  if (blockIdx.y == 0 && tid < kTcTerms) gsc[(size_t)row * kTcTerms + tid] = ldexpf(g0, -2 * tid);
+  if (b >= K / 16) return;
+  float r[16];
+  if (BF16_IN) {
+    const uint4* p = reinterpret_cast<const uint4*>(sb + 16 * b);
+    const uint4 u0 = __ldg(p), u1 = __ldg(p + 1);
+    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      r[2 * q] = __uint_as_float(w[q] << 16);
+      r[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+    }
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(sf32 + 16 * b);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 v = p[q];
+      r[4 * q] = v.x; r[4 * q + 1] = v.y; r[4 * q + 2] = v.z; r[4 * q + 3] = v.w;
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < kTcTerms; ++t) {
+    const float g = ldexpf(g0, -2 * t);
+    float bm = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) bm = fmaxf(bm, fabsf(r[j]));
+    uint32_t sf = 0;
+    float sc = 0.0f;
+    if (g > 0.0f) {
+      sf = f32_to_e4m3_rn(bm / (6.0f * g));
+      sc = e4m3_to_f32(sf) * g;
+    }
+    uint32_t code[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      uint32_t cd = 0;
+      if (sc > 0.0f) {
+        const uint32_t mg = e2m1_rne_mag(fabsf(r[j]), sc);
+        const bool neg = r[j] < 0.0f && mg != 0u;
+        const float q = e2m1_mag_value(mg) * sc;
+        r[j] -= neg ? -q : q;
+        cd = mg | (neg ? 8u : 0u);
+      }
+      code[j] = cd;
+    }
+    uint32_t nat0 = 0, nat1 = 0, per0 = 0, per1 = 0;
+#pragma unroll
+    for (int p = 0; p < 16; ++p) {
+      const int j = (p >> 3) + 4 * (p & 3) + 2 * ((p >> 2) & 1);
+      if (p < 8) {
+        nat0 |= code[p] << (4 * p);
+        per0 |= code[j] << (4 * p);
+      } else {
+        nat1 |= code[p] << (4 * (p - 8));
+        per1 |= code[j] << (4 * (p - 8));
+      }
+    }
+    const size_t term_row = (size_t)row * kTcTerms + t;
+    *reinterpret_cast<uint2*>(cnat + term_row * (K / 2) + 8 * b) = make_uint2(nat0, nat1);
+    *reinterpret_cast<uint2*>(cperm + term_row * (K / 2) + 8 * b) = make_uint2(per0, per1);
+    sfb[term_row * (K / 16) + b] = (uint8_t)sf;
   }
 }
 
@@ -238,7 +277,7 @@ struct FcTcArgs {
 };
 
 struct TcSmem {
-  uint64_t bar[kStages];
+  uint64_t bar[kRing];
   uint32_t tmem_base;
   int stuck;
   int any_gated;
@@ -248,7 +287,6 @@ struct TcSmem {
   float gsc[kMaxN];              // term scales, column order
   float wts[kTcTok];             // FC2: routing weight per pair
   int pair[kTcTok];              // FC2: pair id per column token
-  float xchg[64][kTcTok];        // FC1: up values handed to the gate warps
 };
 
 template <bool FC1>
@@ -256,9 +294,7 @@ __global__ void __launch_bounds__(kThreads, 2) fc_tc_kernel(const FcTcArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_dyn[];
   // 1024-aligned operand stages, then the small shared state
   unsigned char* base = smem_dyn + ((1024 - (smem_addr(smem_dyn) & 1023)) & 1023);
-  unsigned char* sA = base;                                    // [kStages][128][128]
-  unsigned char* sB = base + kStages * kABytes;                // [kStages][64][128]
-  TcSmem& sm = *reinterpret_cast<TcSmem*>(sB + kStages * kBBytes);
+  TcSmem& sm = *reinterpret_cast<TcSmem*>(base + kRing * kSlotBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if ((int)blockIdx.y >= a.hdr[0]) return;
@@ -277,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 2) fc_tc_kernel(const FcTcArgs a) {
       if (slot >= a.n_slots) { record_error(MOET_ERR_DEVICE_INDEX); slot = -1; }
     }
     sm.slot = slot;
-    for (int s = 0; s < kStages; ++s) mbar_init(&sm.bar[s], 1);
+    for (int s = 0; s < kRing; ++s) mbar_init(&sm.bar[s], 1);
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&sm.tmem_base)),
@@ -336,107 +372,126 @@ __global__ void __launch_bounds__(kThreads, 2) fc_tc_kernel(const FcTcArgs a) {
   const uint32_t lane_q = (uint32_t)(warp * 32) << 16;      // this warp's TMEM lane quarter
 
   const int npass = do_delta ? 2 : 1;
-  int cglob = 0;                                             // chunk counter across passes
-  for (int pass = 0; pass < npass; ++pass) {
-    const bool dp = pass == 1;
-    const uint32_t* Sp = a.sign + ((size_t)e * a.N + wrow) * wpr;
-    const uint32_t* Mp = a.mag + ((size_t)e * a.N + wrow) * wpr;
-    const uint8_t* Dp = dp ? a.dcodes + ((size_t)sm.slot * a.N + wrow) * (K / 2) : nullptr;
-    const uint8_t* Q = dp ? a.ds4 : a.s16;
-    const size_t qbase = dp ? (size_t)sm.slot * a.N : (size_t)e * a.N;
-    const uint8_t* act = dp ? a.cnat : a.cperm;
-    const uint32_t dcol = dp ? kColD2 : kColD;
+  const int total = nkc * npass;                 // chunks over both passes
 
-    for (int c = 0; c < nkc; ++c, ++cglob) {
-      const int s = cglob % kStages;
-      if (cglob >= kStages) {
-        if (!mbar_wait(&sm.bar[s], ((cglob / kStages) - 1) & 1)) atomicExch(&sm.stuck, 1);
-      }
-      __syncthreads();
-      if (sm.stuck) break;
-      // ---- A: this thread's weight row, 256 weights = 128 bytes, 128B-swizzled
-      unsigned char* arow = sA + s * kABytes + tid * 128;
+  // Issue the asynchronous copies of chunk cg into its ring slot: this thread's
+  // weight row (raw planes, or the delta codes straight into the swizzled A
+  // tile), its row scale, a share of the B rows (straight into the swizzled B
+  // tile; gated tokens only in the delta pass) and one B row scale.
+  auto prefetch = [&](int cg) {
+    if (cg < total) {
+      const bool dp = cg >= nkc;
+      const int c = dp ? cg - nkc : cg;
+      unsigned char* slot = base + (cg % kRing) * kSlotBytes;
       if (!dp) {
-        const uint4* sp = reinterpret_cast<const uint4*>(Sp + (size_t)c * 8);
-        const uint4* mp = reinterpret_cast<const uint4*>(Mp + (size_t)c * 8);
-        const uint4 s0 = ldg_nc_v4(sp), s1 = ldg_nc_v4(sp + 1), m0 = ldg_nc_v4(mp), m1 = ldg_nc_v4(mp + 1);
-        const uint32_t SW[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-        const uint32_t MW[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-#pragma unroll
-        for (int w = 0; w < 8; ++w)
-          *reinterpret_cast<uint4*>(arow + ((w ^ (tid & 7)) << 4)) = planes_to_e2m1(SW[w], MW[w]);
+        const uint32_t* sp = a.sign + ((size_t)e * a.N + wrow) * wpr + (size_t)c * 8;
+        const uint32_t* mp = a.mag + ((size_t)e * a.N + wrow) * wpr + (size_t)c * 8;
+        unsigned char* ra = slot + kOffRawA + tid * 64;
+        cp_async16(ra, sp);
+        cp_async16(ra + 16, sp + 4);
+        cp_async16(ra + 32, mp);
+        cp_async16(ra + 48, mp + 4);
+        cp_async16(slot + kOffRawQ + tid * 16, a.s16 + ((size_t)e * a.N + wrow) * bpr + (size_t)c * 16);
       } else {
-        const uint4* dp4 = reinterpret_cast<const uint4*>(Dp + (size_t)c * 128);
+        const uint8_t* dsrc = a.dcodes + ((size_t)sm.slot * a.N + wrow) * (K / 2) + (size_t)c * 128;
+        unsigned char* arow = slot + kOffA + tid * 128;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) *reinterpret_cast<uint4*>(arow + ((w ^ (tid & 7)) << 4)) = ldg_nc_v4(dp4 + w);
+        for (int u = 0; u < 8; ++u) cp_async16(arow + ((u ^ (tid & 7)) << 4), dsrc + 16 * u);
+        cp_async16(slot + kOffRawQ + tid * 16, a.ds4 + ((size_t)sm.slot * a.N + wrow) * bpr + (size_t)c * 16);
       }
-      // ---- SFA: rows lane + 32 j, 16 block scales of this chunk -> columns 4 i + j
-      {
-        uint32_t v[16];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 q = ldg_nc_v4(Q + (qbase + srows[j]) * bpr + (size_t)c * 16);
-          v[0 * 4 + j] = q.x; v[1 * 4 + j] = q.y; v[2 * 4 + j] = q.z; v[3 * 4 + j] = q.w;
-        }
-        tmem_st16(tmem + lane_q + kColSFA + 16 * s, v);
-      }
-      // ---- B: activation-term rows n = token * kTcTerms + term
-      unsigned char* bst = sB + s * kBBytes;
+      const uint8_t* act = dp ? a.cnat : a.cperm;
       for (int it = tid; it < ncols * 8; it += kThreads) {
         const int n = it >> 3, u = it & 7;
         const int tk = n / kTcTerms, term = n % kTcTerms;
-        uint4 val = make_uint4(0u, 0u, 0u, 0u);
         const int srow = tk < ntok ? sm.src_row[tk] : -1;
-        if (srow >= 0 && (!dp || sm.gate_f[tk] != 0.0f)) {
-          const uint8_t* src = act + ((size_t)srow * kTcTerms + term) * (K / 2) + (size_t)c * 128;
-          val = ldg_nc_v4(src + 16 * u);
-        }
-        *reinterpret_cast<uint4*>(bst + n * 128 + ((u ^ (n & 7)) << 4)) = val;
+        const bool ok = srow >= 0 && (!dp || sm.gate_f[tk] != 0.0f);
+        const uint8_t* src = ok ? act + ((size_t)srow * kTcTerms + term) * (K / 2) + (size_t)c * 128 + 16 * u : act;
+        cp_async16(slot + kOffB + n * 128 + ((u ^ (n & 7)) << 4), src, ok ? 16u : 0u);
       }
-      // ---- SFB: B rows lane + 32 j (j < 2 since N <= 64)
-      {
-        uint32_t v[16];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int n = lane + 32 * j;
-          uint4 q = make_uint4(0u, 0u, 0u, 0u);
-          if (n < ncols) {
-            const int tk = n / kTcTerms, term = n % kTcTerms;
-            const int srow = tk < ntok ? sm.src_row[tk] : -1;
-            if (srow >= 0) q = ldg_nc_v4(a.sfb + ((size_t)srow * kTcTerms + term) * bpr + (size_t)c * 16);
-          }
-          v[0 * 4 + j] = q.x; v[1 * 4 + j] = q.y; v[2 * 4 + j] = q.z; v[3 * 4 + j] = q.w;
-        }
-        tmem_st16(tmem + lane_q + kColSFB + 16 * s, v);
-      }
-      asm volatile("fence.proxy.async.shared::cta;");
-      asm volatile("tcgen05.wait::st.sync.aligned;");
-      asm volatile("tcgen05.fence::before_thread_sync;");
-      __syncthreads();
-      if (tid == 0) {
-        asm volatile("tcgen05.fence::after_thread_sync;");
-        const uint32_t a0 = smem_addr(sA + s * kABytes), b0 = smem_addr(sB + s * kBBytes);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          tc_mma(tmem + dcol, sw128_desc(a0 + 32 * i), sw128_desc(b0 + 32 * i), idesc,
-                 tmem + kColSFA + 16 * s + 4 * i, tmem + kColSFB + 16 * s + 4 * i, (c > 0 || i > 0) ? 1u : 0u);
-        }
-        tc_commit(&sm.bar[s]);
+      if (tid < ncols) {
+        const int tk = tid / kTcTerms, term = tid % kTcTerms;
+        const int srow = tk < ntok ? sm.src_row[tk] : -1;
+        const uint8_t* src = srow >= 0 ? a.sfb + ((size_t)srow * kTcTerms + term) * bpr + (size_t)c * 16 : a.sfb;
+        cp_async16(slot + kOffRawSfb + tid * 16, src, srow >= 0 ? 16u : 0u);
       }
     }
+    cp_async_commit();                           // one group per chunk, possibly empty
+  };
+
+#pragma unroll 1
+  for (int cg = 0; cg < kRing - 1; ++cg) prefetch(cg);
+
+  int cg = 0;
+#pragma unroll 1
+  for (; cg < total; ++cg) {
+    const bool dp = cg >= nkc;
+    const int c = dp ? cg - nkc : cg;
+    const int si = cg % kRing;
+    unsigned char* slot = base + si * kSlotBytes;
+    cp_async_wait<kRing - 2>();                  // this thread's copies of chunk cg have landed
+    __syncthreads();                             // ... and everyone else's
+    if (!dp) {
+      // expand this thread's 256 weights: raw sign/magnitude words -> e2m1 nibbles
+      const uint4* ra = reinterpret_cast<const uint4*>(slot + kOffRawA + tid * 64);
+      const uint4 s0 = ra[0], s1 = ra[1], m0 = ra[2], m1 = ra[3];
+      const uint32_t SW[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+      const uint32_t MW[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+      unsigned char* arow = slot + kOffA + tid * 128;
+#pragma unroll
+      for (int w = 0; w < 8; ++w)
+        *reinterpret_cast<uint4*>(arow + ((w ^ (tid & 7)) << 4)) = planes_to_e2m1(SW[w], MW[w]);
+    }
+    {
+      // scale factors to TMEM, replicated layout: rows lane + 32 j -> columns 4 i + j
+      uint32_t va[16], vb[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 q = *reinterpret_cast<const uint4*>(slot + kOffRawQ + (lane + 32 * j) * 16);
+        va[0 * 4 + j] = q.x; va[1 * 4 + j] = q.y; va[2 * 4 + j] = q.z; va[3 * 4 + j] = q.w;
+        const int n = lane + 32 * j;
+        uint4 r = make_uint4(0u, 0u, 0u, 0u);
+        if (n < ncols) r = *reinterpret_cast<const uint4*>(slot + kOffRawSfb + n * 16);
+        vb[0 * 4 + j] = r.x; vb[1 * 4 + j] = r.y; vb[2 * 4 + j] = r.z; vb[3 * 4 + j] = r.w;
+      }
+      tmem_st16(tmem + lane_q + kColSFA + 16 * si, va);
+      tmem_st16(tmem + lane_q + kColSFB + 16 * si, vb);
+    }
+    asm volatile("fence.proxy.async.shared::cta;");
+    asm volatile("tcgen05.wait::st.sync.aligned;");
+    asm volatile("tcgen05.fence::before_thread_sync;");
+    __syncthreads();
     if (sm.stuck) break;
+    if (tid == 0) {
+      asm volatile("tcgen05.fence::after_thread_sync;");
+      const uint32_t a0 = smem_addr(slot + kOffA), b0 = smem_addr(slot + kOffB);
+      const uint32_t dcol = dp ? kColD2 : kColD;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        tc_mma(tmem + dcol, sw128_desc(a0 + 32 * i), sw128_desc(b0 + 32 * i), idesc,
+               tmem + kColSFA + 16 * si + 4 * i, tmem + kColSFB + 16 * si + 4 * i, (c > 0 || i > 0) ? 1u : 0u);
+      }
+      tc_commit(&sm.bar[si]);
+    }
+    // refill the slot of chunk cg - 1 with chunk cg + kRing - 1 once its MMAs are done
+    if (cg >= 1) {
+      if (!mbar_wait(&sm.bar[(cg - 1) % kRing], ((cg - 1) / kRing) & 1)) atomicExch(&sm.stuck, 1);
+    }
+    prefetch(cg + kRing - 1);
   }
-  // ---- drain: every stage's last commit (bounded), then read the accumulators
-  const int issued = cglob;
-  for (int s = 0; s < kStages && s < issued; ++s) {
-    const int last = issued - 1 - ((issued - 1 - s) % kStages);   // last chunk that used stage s
-    if (!mbar_wait(&sm.bar[s], (last / kStages) & 1)) atomicExch(&sm.stuck, 1);
+  cp_async_wait<0>();
+  // ---- drain: the last use of every slot (bounded), then read the accumulators
+  const int issued = cg;
+  for (int s2 = 0; s2 < kRing && s2 < issued; ++s2) {
+    const int last = issued - 1 - ((issued - 1 - s2) % kRing);   // last chunk that used slot s2
+    if (!mbar_wait(&sm.bar[s2], (last / kRing) & 1)) atomicExch(&sm.stuck, 1);
   }
   asm volatile("tcgen05.fence::after_thread_sync;");
   __syncthreads();
   if (sm.stuck) {
     if (tid == 0) record_error(MOET_ERR_TIMEOUT);
   } else {
+    // FC1: up rows hand their values to the gate rows through the (now idle) ring memory
+    float (*xchg)[kTcTok] = reinterpret_cast<float (*)[kTcTok]>(base);
     const float sc2 = 2.0f * __ldg(a.scale_2 + e);           // 2: the halved e2m1 levels
     const float sc2d = __ldg(a.scale_2 + e);
     for (int c0 = 0; c0 < ncols; c0 += 16) {
@@ -466,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 2) fc_tc_kernel(const FcTcArgs a) {
         // up rows (threads 64..127) hand their values to the gate rows (threads 0..63)
         if (tid >= 64) {
 #pragma unroll
-          for (int q = 0; q < 16 / kTcTerms; ++q) sm.xchg[tid - 64][c0 / kTcTerms + q] = acc[q];
+          for (int q = 0; q < 16 / kTcTerms; ++q) xchg[tid - 64][c0 / kTcTerms + q] = acc[q];
         }
         __syncthreads();
         if (tid < 64) {
@@ -474,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 2) fc_tc_kernel(const FcTcArgs a) {
           for (int q = 0; q < 16 / kTcTerms; ++q) {
             const int tk = c0 / kTcTerms + q;
             if (tk < ntok && sm.src_row[tk] >= 0) {
-              const float gv = acc[q], uv = sm.xchg[tid][tk];
+              const float gv = acc[q], uv = xchg[tid][tk];
               a.out[(size_t)(pos0 + tk) * a.I + wrow] = gv / (1.0f + expf(-gv)) * uv;
             }
           }
@@ -492,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 2) fc_tc_kernel(const FcTcArgs a) {
 
 template <bool FC1>
 moet_status launch_fc_tc(const FcTcArgs& a, int row_tiles, int grid_y, cudaStream_t st) {
-  const size_t smem = 1024 + kStages * (kABytes + kBBytes) + sizeof(TcSmem);
+  const size_t smem = 1024 + kRing * kSlotBytes + sizeof(TcSmem);
   auto kern = fc_tc_kernel<FC1>;
   MOET_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   {
@@ -510,8 +565,9 @@ moet_status tc_forward(const TcForwardArgs& f, cudaStream_t st) {
   // FC1 input terms: one row per token
   {
     ProfScope ps(MOET_K_TERMS, st);
-    act_terms_kernel<true><<<f.T, kThreads, sizeof(float) * f.H, st>>>(
-        f.H, f.x, nullptr, 1, f.buf.x_cperm, f.buf.x_cnat, f.buf.x_sf, f.buf.x_g);
+    const dim3 grid(f.T, (f.H / 16 + kThreads - 1) / kThreads);
+    act_terms_kernel<true><<<grid, kThreads, 0, st>>>(f.H, f.x, f.buf.x_cperm, f.buf.x_cnat, f.buf.x_sf,
+                                                      f.buf.x_g);
   }
   MOET_CUDA_TRY(cudaGetLastError());
   FcTcArgs a{};
@@ -530,8 +586,9 @@ moet_status tc_forward(const TcForwardArgs& f, cudaStream_t st) {
   // FC2 input terms: one row per bucketed pair (h rows are in bucketed order)
   {
     ProfScope ps(MOET_K_TERMS, st);
-    act_terms_kernel<false><<<pairs, kThreads, sizeof(float) * f.I, st>>>(
-        f.I, f.h, nullptr, 1, f.buf.h_cperm, f.buf.h_cnat, f.buf.h_sf, f.buf.h_g);
+    const dim3 grid(pairs, (f.I / 16 + kThreads - 1) / kThreads);
+    act_terms_kernel<false><<<grid, kThreads, 0, st>>>(f.I, f.h, f.buf.h_cperm, f.buf.h_cnat, f.buf.h_sf,
+                                                       f.buf.h_g);
   }
   MOET_CUDA_TRY(cudaGetLastError());
   FcTcArgs a2 = a;
