@@ -44,7 +44,7 @@
 namespace moet {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kFcThreads = 256;               // FC kernel: two threads per weight row
 constexpr int kRing = 3;                      // chunks in flight (async copy + MMA)
 constexpr int kKC = 256;                      // weights per K chunk (one SW128 atom)
 constexpr int kMaxN = kTcTerms * kTcTok;      // 64 columns of D
@@ -148,26 +148,29 @@ __device__ __forceinline__ uint4 planes_to_e2m1(uint32_t S, uint32_t M) {
 }
 
 // ---------------------------------------------------------------- activation terms
-// Grid (rows, ceil(K/16 / 128)): every CTA reads its row once for the row
-// maximum m, then each thread expands one 16-element block into kTcTerms
-// NVFP4 terms.  Term t has the fp32 scale g_t = m / (6 * 448) / 4^t and a
-// ue4m3 scale per block chosen from the block's current residual, so each
-// term quantises what the previous ones left (the residual of a block shrinks
-// at least ~6x per term while g_t shrinks 4x, keeping the block scales in the
-// normal e4m3 range).  Outputs per (row, term): codes in permuted and natural
-// K order, one ue4m3 scale per 16, and g_t.
+// Grid (rows, K / 256): each CTA of 256 threads reads its row once for the
+// row maximum m, then 16 threads expand one 16-element block (one element
+// each) into kTcTerms NVFP4 terms.  Term t has the fp32 scale
+// g_t = m / (6 * 448) / 4^t and a ue4m3 scale per block chosen from the
+// block's current residual, so each term quantises what the previous ones
+// left (a block's residual shrinks at least ~6x per term while g_t shrinks
+// 4x, keeping the block scales in the normal e4m3 range).  Outputs per
+// (row, term): codes in permuted and natural K order, one ue4m3 scale per
+// 16 elements, and g_t.
+constexpr int kTermThreads = 256;
+
 template <bool BF16_IN>
-__global__ void __launch_bounds__(kThreads) act_terms_kernel(int K, const void* __restrict__ src,
-                                                            uint8_t* __restrict__ cperm, uint8_t* __restrict__ cnat,
-                                                            uint8_t* __restrict__ sfb, float* __restrict__ gsc) {
-  __shared__ float red[kThreads / 32];
-  const int row = blockIdx.x, tid = threadIdx.x;
+__global__ void __launch_bounds__(kTermThreads) act_terms_kernel(int K, const void* __restrict__ src,
+                                                                uint8_t* __restrict__ cperm, uint8_t* __restrict__ cnat,
+                                                                uint8_t* __restrict__ sfb, float* __restrict__ gsc) {
+  __shared__ float red[kTermThreads / 32];
+  const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
   const uint16_t* sb = static_cast<const uint16_t*>(src) + (size_t)row * K;
   const float* sf32 = static_cast<const float*>(src) + (size_t)row * K;
   float m = 0.0f;
   if (BF16_IN) {
     const uint4* p = reinterpret_cast<const uint4*>(sb);
-    for (int i = tid; i < K / 8; i += kThreads) {
+    for (int i = tid; i < K / 8; i += kTermThreads) {
       const uint4 v = __ldg(p + i);
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -176,79 +179,58 @@ __global__ void __launch_bounds__(kThreads) act_terms_kernel(int K, const void* 
     }
   } else {
     const float4* p = reinterpret_cast<const float4*>(sf32);
-    for (int i = tid; i < K / 4; i += kThreads) {
+    for (int i = tid; i < K / 4; i += kTermThreads) {
       const float4 v = p[i];
       m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
     }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if ((tid & 31) == 0) red[tid >> 5] = m;
+  if (lane == 0) red[tid >> 5] = m;
   __syncthreads();
-  m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  m = red[0];
+#pragma unroll
+  for (int w = 1; w < kTermThreads / 32; ++w) m = fmaxf(m, red[w]);
   const float g0 = m / (6.0f * 448.0f);
-  const int b = blockIdx.y * kThreads + tid;
   if (blockIdx.y == 0 && tid < kTcTerms) gsc[(size_t)row * kTcTerms + tid] = ldexpf(g0, -2 * tid);
-  if (b >= K / 16) return;
-  float r[16];
-  if (BF16_IN) {
-    const uint4* p = reinterpret_cast<const uint4*>(sb + 16 * b);
-    const uint4 u0 = __ldg(p), u1 = __ldg(p + 1);
-    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      r[2 * q] = __uint_as_float(w[q] << 16);
-      r[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
-    }
-  } else {
-    const float4* p = reinterpret_cast<const float4*>(sf32 + 16 * b);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float4 v = p[q];
-      r[4 * q] = v.x; r[4 * q + 1] = v.y; r[4 * q + 2] = v.z; r[4 * q + 3] = v.w;
-    }
-  }
+  const int idx = blockIdx.y * kTermThreads + tid;         // element index in the row
+  const int b = idx >> 4, j = idx & 15, lbase = lane & 16;
+  const bool live = idx < K;                                // K % 256 == 0: all live
+  float r = 0.0f;
+  if (live) r = BF16_IN ? __uint_as_float((uint32_t)__ldg(sb + idx) << 16) : sf32[idx];
+  // the element whose code lands at permuted position p = 8 rr + n is rr + 4 (n & 3) + 2 (n >> 2)
+  const int p0 = 2 * (j & 7), p1 = p0 + 1;
+  const int src0 = (p0 >> 3) + 4 * (p0 & 3) + 2 * ((p0 >> 2) & 1);
+  const int src1 = (p1 >> 3) + 4 * (p1 & 3) + 2 * ((p1 >> 2) & 1);
 #pragma unroll
   for (int t = 0; t < kTcTerms; ++t) {
     const float g = ldexpf(g0, -2 * t);
-    float bm = 0.0f;
+    float bm = fabsf(r);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) bm = fmaxf(bm, fabsf(r[j]));
+    for (int o = 8; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
     uint32_t sf = 0;
     float sc = 0.0f;
     if (g > 0.0f) {
       sf = f32_to_e4m3_rn(bm / (6.0f * g));
       sc = e4m3_to_f32(sf) * g;
     }
-    uint32_t code[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      uint32_t cd = 0;
-      if (sc > 0.0f) {
-        const uint32_t mg = e2m1_rne_mag(fabsf(r[j]), sc);
-        const bool neg = r[j] < 0.0f && mg != 0u;
-        const float q = e2m1_mag_value(mg) * sc;
-        r[j] -= neg ? -q : q;
-        cd = mg | (neg ? 8u : 0u);
-      }
-      code[j] = cd;
+    uint32_t code = 0;
+    if (sc > 0.0f) {
+      const uint32_t mg = e2m1_rne_mag(fabsf(r), sc);
+      const bool neg = r < 0.0f && mg != 0u;
+      const float q = e2m1_mag_value(mg) * sc;
+      r -= neg ? -q : q;
+      code = mg | (neg ? 8u : 0u);
     }
-    uint32_t nat0 = 0, nat1 = 0, per0 = 0, per1 = 0;
-#pragma unroll
-    for (int p = 0; p < 16; ++p) {
-      const int j = (p >> 3) + 4 * (p & 3) + 2 * ((p >> 2) & 1);
-      if (p < 8) {
-        nat0 |= code[p] << (4 * p);
-        per0 |= code[j] << (4 * p);
-      } else {
-        nat1 |= code[p] << (4 * (p - 8));
-        per1 |= code[j] << (4 * (p - 8));
-      }
+    const uint32_t nat_hi = __shfl_down_sync(0xffffffffu, code, 1);
+    const uint32_t per_lo = __shfl_sync(0xffffffffu, code, lbase + src0);
+    const uint32_t per_hi = __shfl_sync(0xffffffffu, code, lbase + src1);
+    if (live) {
+      const size_t term_row = (size_t)row * kTcTerms + t;
+      if ((j & 1) == 0) cnat[term_row * (K / 2) + 8 * b + (j >> 1)] = (uint8_t)(code | (nat_hi << 4));
+      if (j < 8) cperm[term_row * (K / 2) + 8 * b + j] = (uint8_t)(per_lo | (per_hi << 4));
+      if (j == 0) sfb[term_row * (K / 16) + b] = (uint8_t)sf;
     }
-    const size_t term_row = (size_t)row * kTcTerms + t;
-    *reinterpret_cast<uint2*>(cnat + term_row * (K / 2) + 8 * b) = make_uint2(nat0, nat1);
-    *reinterpret_cast<uint2*>(cperm + term_row * (K / 2) + 8 * b) = make_uint2(per0, per1);
-    sfb[term_row * (K / 16) + b] = (uint8_t)sf;
   }
 }
 
@@ -290,13 +272,14 @@ struct TcSmem {
 };
 
 template <bool FC1>
-__global__ void __launch_bounds__(kThreads, 2) fc_tc_kernel(const FcTcArgs a) {
+__global__ void __launch_bounds__(kFcThreads, 2) fc_tc_kernel(const FcTcArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_dyn[];
   // 1024-aligned operand stages, then the small shared state
   unsigned char* base = smem_dyn + ((1024 - (smem_addr(smem_dyn) & 1023)) & 1023);
   TcSmem& sm = *reinterpret_cast<TcSmem*>(base + kRing * kSlotBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int trow = tid & 127, half = tid >> 7;   // tile row of this thread, and which 128 weights
   if ((int)blockIdx.y >= a.hdr[0]) return;
   const int4 ch = a.chunks[blockIdx.y];
   const int e = ch.x, ntok = ch.z;
@@ -357,9 +340,9 @@ __global__ void __launch_bounds__(kThreads, 2) fc_tc_kernel(const FcTcArgs a) {
   // the weight row owned by this thread
   int wrow;
   if (FC1) {
-    wrow = tid < 64 ? blockIdx.x * 64 + tid : a.I + blockIdx.x * 64 + (tid - 64);
+    wrow = trow < 64 ? blockIdx.x * 64 + trow : a.I + blockIdx.x * 64 + (trow - 64);
   } else {
-    wrow = blockIdx.x * 128 + tid;
+    wrow = blockIdx.x * 128 + trow;
   }
   // weight rows whose scales this thread writes to TMEM (replicated layout: rows lane + 32 j)
   int srows[4];
@@ -369,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 2) fc_tc_kernel(const FcTcArgs a) {
     srows[j] = FC1 ? (tr < 64 ? blockIdx.x * 64 + tr : a.I + blockIdx.x * 64 + (tr - 64)) : blockIdx.x * 128 + tr;
   }
   const size_t wpr = (size_t)K / 32, bpr = (size_t)K / 16;
-  const uint32_t lane_q = (uint32_t)(warp * 32) << 16;      // this warp's TMEM lane quarter
+  const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lane quarter
 
   const int npass = do_delta ? 2 : 1;
   const int total = nkc * npass;                 // chunks over both passes
@@ -384,23 +367,24 @@ __global__ void __launch_bounds__(kThreads, 2) fc_tc_kernel(const FcTcArgs a) {
       const int c = dp ? cg - nkc : cg;
       unsigned char* slot = base + (cg % kRing) * kSlotBytes;
       if (!dp) {
-        const uint32_t* sp = a.sign + ((size_t)e * a.N + wrow) * wpr + (size_t)c * 8;
-        const uint32_t* mp = a.mag + ((size_t)e * a.N + wrow) * wpr + (size_t)c * 8;
-        unsigned char* ra = slot + kOffRawA + tid * 64;
+        // half 0 copies words 0..3 of the chunk's sign and magnitude rows, half 1 words 4..7
+        const uint32_t* sp = a.sign + ((size_t)e * a.N + wrow) * wpr + (size_t)c * 8 + 4 * half;
+        const uint32_t* mp = a.mag + ((size_t)e * a.N + wrow) * wpr + (size_t)c * 8 + 4 * half;
+        unsigned char* ra = slot + kOffRawA + trow * 64 + 16 * half;
         cp_async16(ra, sp);
-        cp_async16(ra + 16, sp + 4);
         cp_async16(ra + 32, mp);
-        cp_async16(ra + 48, mp + 4);
-        cp_async16(slot + kOffRawQ + tid * 16, a.s16 + ((size_t)e * a.N + wrow) * bpr + (size_t)c * 16);
+        if (half == 0)
+          cp_async16(slot + kOffRawQ + trow * 16, a.s16 + ((size_t)e * a.N + wrow) * bpr + (size_t)c * 16);
       } else {
-        const uint8_t* dsrc = a.dcodes + ((size_t)sm.slot * a.N + wrow) * (K / 2) + (size_t)c * 128;
-        unsigned char* arow = slot + kOffA + tid * 128;
+        const uint8_t* dsrc = a.dcodes + ((size_t)sm.slot * a.N + wrow) * (K / 2) + (size_t)c * 128 + 64 * half;
+        unsigned char* arow = slot + kOffA + trow * 128;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) cp_async16(arow + ((u ^ (tid & 7)) << 4), dsrc + 16 * u);
-        cp_async16(slot + kOffRawQ + tid * 16, a.ds4 + ((size_t)sm.slot * a.N + wrow) * bpr + (size_t)c * 16);
+        for (int u = 0; u < 4; ++u) cp_async16(arow + (((4 * half + u) ^ (trow & 7)) << 4), dsrc + 16 * u);
+        if (half == 0)
+          cp_async16(slot + kOffRawQ + trow * 16, a.ds4 + ((size_t)sm.slot * a.N + wrow) * bpr + (size_t)c * 16);
       }
       const uint8_t* act = dp ? a.cnat : a.cperm;
-      for (int it = tid; it < ncols * 8; it += kThreads) {
+      for (int it = tid; it < ncols * 8; it += kFcThreads) {
         const int n = it >> 3, u = it & 7;
         const int tk = n / kTcTerms, term = n % kTcTerms;
         const int srow = tk < ntok ? sm.src_row[tk] : -1;
@@ -431,30 +415,29 @@ __global__ void __launch_bounds__(kThreads, 2) fc_tc_kernel(const FcTcArgs a) {
     cp_async_wait<kRing - 2>();                  // this thread's copies of chunk cg have landed
     __syncthreads();                             // ... and everyone else's
     if (!dp) {
-      // expand this thread's 256 weights: raw sign/magnitude words -> e2m1 nibbles
-      const uint4* ra = reinterpret_cast<const uint4*>(slot + kOffRawA + tid * 64);
-      const uint4 s0 = ra[0], s1 = ra[1], m0 = ra[2], m1 = ra[3];
-      const uint32_t SW[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-      const uint32_t MW[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-      unsigned char* arow = slot + kOffA + tid * 128;
+      // expand this thread's 128 weights: raw sign/magnitude words -> e2m1 nibbles
+      const uint4 sw = *reinterpret_cast<const uint4*>(slot + kOffRawA + trow * 64 + 16 * half);
+      const uint4 mw = *reinterpret_cast<const uint4*>(slot + kOffRawA + trow * 64 + 32 + 16 * half);
+      const uint32_t SW[4] = {sw.x, sw.y, sw.z, sw.w};
+      const uint32_t MW[4] = {mw.x, mw.y, mw.z, mw.w};
+      unsigned char* arow = slot + kOffA + trow * 128;
 #pragma unroll
-      for (int w = 0; w < 8; ++w)
-        *reinterpret_cast<uint4*>(arow + ((w ^ (tid & 7)) << 4)) = planes_to_e2m1(SW[w], MW[w]);
+      for (int w = 0; w < 4; ++w)
+        *reinterpret_cast<uint4*>(arow + (((4 * half + w) ^ (trow & 7)) << 4)) = planes_to_e2m1(SW[w], MW[w]);
     }
     {
-      // scale factors to TMEM, replicated layout: rows lane + 32 j -> columns 4 i + j
-      uint32_t va[16], vb[16];
+      // scale factors to TMEM, replicated layout: rows lane + 32 j -> columns 4 i + j;
+      // warps 0-3 write the weight-row scales, warps 4-7 the activation-term scales
+      uint32_t v[16];
+      const int src = half ? kOffRawSfb : kOffRawQ;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const uint4 q = *reinterpret_cast<const uint4*>(slot + kOffRawQ + (lane + 32 * j) * 16);
-        va[0 * 4 + j] = q.x; va[1 * 4 + j] = q.y; va[2 * 4 + j] = q.z; va[3 * 4 + j] = q.w;
         const int n = lane + 32 * j;
-        uint4 r = make_uint4(0u, 0u, 0u, 0u);
-        if (n < ncols) r = *reinterpret_cast<const uint4*>(slot + kOffRawSfb + n * 16);
-        vb[0 * 4 + j] = r.x; vb[1 * 4 + j] = r.y; vb[2 * 4 + j] = r.z; vb[3 * 4 + j] = r.w;
+        uint4 q = make_uint4(0u, 0u, 0u, 0u);
+        if (!half || n < ncols) q = *reinterpret_cast<const uint4*>(slot + src + n * 16);
+        v[0 * 4 + j] = q.x; v[1 * 4 + j] = q.y; v[2 * 4 + j] = q.z; v[3 * 4 + j] = q.w;
       }
-      tmem_st16(tmem + lane_q + kColSFA + 16 * si, va);
-      tmem_st16(tmem + lane_q + kColSFB + 16 * si, vb);
+      tmem_st16(tmem + lane_q + (half ? kColSFB : kColSFA) + 16 * si, v);
     }
     asm volatile("fence.proxy.async.shared::cta;");
     asm volatile("tcgen05.wait::st.sync.aligned;");
@@ -489,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 2) fc_tc_kernel(const FcTcArgs a) {
   __syncthreads();
   if (sm.stuck) {
     if (tid == 0) record_error(MOET_ERR_TIMEOUT);
-  } else {
+  } else if (half == 0) {
     // FC1: up rows hand their values to the gate rows through the (now idle) ring memory
     float (*xchg)[kTcTok] = reinterpret_cast<float (*)[kTcTok]>(base);
     const float sc2 = 2.0f * __ldg(a.scale_2 + e);           // 2: the halved e2m1 levels
@@ -523,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 2) fc_tc_kernel(const FcTcArgs a) {
 #pragma unroll
           for (int q = 0; q < 16 / kTcTerms; ++q) xchg[tid - 64][c0 / kTcTerms + q] = acc[q];
         }
-        __syncthreads();
+        asm volatile("bar.sync 1, 128;");        // warps 0-3 only
         if (tid < 64) {
 #pragma unroll
           for (int q = 0; q < 16 / kTcTerms; ++q) {
@@ -534,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 2) fc_tc_kernel(const FcTcArgs a) {
             }
           }
         }
-        __syncthreads();
+        asm volatile("bar.sync 1, 128;");
       }
     }
   }
@@ -552,7 +535,7 @@ moet_status launch_fc_tc(const FcTcArgs& a, int row_tiles, int grid_y, cudaStrea
   MOET_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   {
     ProfScope ps(FC1 ? MOET_K_FC1 : MOET_K_FC2, st);
-    kern<<<dim3(row_tiles, grid_y), kThreads, smem, st>>>(a);
+    kern<<<dim3(row_tiles, grid_y), kFcThreads, smem, st>>>(a);
   }
   MOET_CUDA_TRY(cudaGetLastError());
   return MOET_OK;
@@ -565,8 +548,8 @@ moet_status tc_forward(const TcForwardArgs& f, cudaStream_t st) {
   // FC1 input terms: one row per token
   {
     ProfScope ps(MOET_K_TERMS, st);
-    const dim3 grid(f.T, (f.H / 16 + kThreads - 1) / kThreads);
-    act_terms_kernel<true><<<grid, kThreads, 0, st>>>(f.H, f.x, f.buf.x_cperm, f.buf.x_cnat, f.buf.x_sf,
+    const dim3 grid(f.T, (f.H + kTermThreads - 1) / kTermThreads);
+    act_terms_kernel<true><<<grid, kTermThreads, 0, st>>>(f.H, f.x, f.buf.x_cperm, f.buf.x_cnat, f.buf.x_sf,
                                                       f.buf.x_g);
   }
   MOET_CUDA_TRY(cudaGetLastError());
@@ -586,8 +569,8 @@ moet_status tc_forward(const TcForwardArgs& f, cudaStream_t st) {
   // FC2 input terms: one row per bucketed pair (h rows are in bucketed order)
   {
     ProfScope ps(MOET_K_TERMS, st);
-    const dim3 grid(pairs, (f.I / 16 + kThreads - 1) / kThreads);
-    act_terms_kernel<false><<<grid, kThreads, 0, st>>>(f.I, f.h, f.buf.h_cperm, f.buf.h_cnat, f.buf.h_sf,
+    const dim3 grid(pairs, (f.I + kTermThreads - 1) / kTermThreads);
+    act_terms_kernel<false><<<grid, kTermThreads, 0, st>>>(f.I, f.h, f.buf.h_cperm, f.buf.h_cnat, f.buf.h_sf,
                                                        f.buf.h_g);
   }
   MOET_CUDA_TRY(cudaGetLastError());
