@@ -29,13 +29,15 @@
 // against a naturally ordered copy of the terms ("cnat") and accumulates in
 // a second TMEM region.
 //
-// Pipeline per CTA (128 threads = 4 warps; thread t owns tile row t): a ring
-// of kRing slots per 256-weight K chunk, each {A 16 KB, B 8 KB, raw planes
-// 8 KB, raw scales 3 KB, SFA 16 + SFB 16 TMEM columns}.  Chunks are fetched
-// kRing - 1 ahead with cp.async; for the current chunk every thread expands
-// its row into the swizzled A tile and writes scale factors to TMEM, one
-// thread issues the 4 MMAs (K = 64 each) and commits them to the slot's
-// mbarrier, and a slot is refilled only after (bounded wait) its MMAs are done.
+// Pipeline per CTA (256 threads; threads t and t + 128 share tile row t):
+// raw chunks of 256 weights stream into a kRawRing-deep cp.async ring (planes,
+// scales and activation terms, ~19 KB per chunk), refilled as soon as they
+// are staged; staging expands a raw chunk into a kOpRing-deep operand ring
+// (swizzled A and B tiles in shared memory, scale factors in TMEM).  Each
+// iteration has one CTA barrier: thread 0 issues the 4 MMAs (K = 64) of the
+// chunk staged in the previous iteration and commits them to that operand
+// slot's mbarrier, while everyone stages the next chunk into the other slot
+// after a bounded wait for the MMAs that last read it.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -45,15 +47,21 @@ namespace moet {
 namespace {
 
 constexpr int kFcThreads = 256;               // FC kernel: two threads per weight row
-constexpr int kRing = 3;                      // chunks in flight (async copy + MMA)
-constexpr int kKC = 256;                      // weights per K chunk (one SW128 atom)
+constexpr int kRawRing = 3;                   // raw chunks in flight (cp.async)
+constexpr int kOpRing = 2;                    // operand slots (A, B, scales) in use by the tensor core
+constexpr int kKC = 256;                      // weights per main-pass K chunk (one SW128 atom)
+constexpr int kKD = 128;                      // weights per delta-pass K chunk
 constexpr int kMaxN = kTcTerms * kTcTok;      // 64 columns of D
 constexpr int kTmemCols = 256;
-constexpr int kColD = 0, kColD2 = 64, kColSFA = 128, kColSFB = 128 + 16 * kRing;
-// one ring slot: converted A (128 rows x 128 B, swizzled), B (64 rows x 128 B, swizzled),
-// raw planes (128 rows x 64 B), raw row scales (128 x 16 B), raw B scales (64 x 16 B)
-constexpr int kOffA = 0, kOffB = 16384, kOffRawA = 24576, kOffRawQ = 32768, kOffRawSfb = 34816;
-constexpr int kSlotBytes = 35840;
+constexpr int kColD = 0, kColD2 = 64, kColSFA = 128, kColSFB = 128 + 16 * kOpRing;
+// raw slot: planes [half][row][16 B] (sign, then magnitude; the delta pass puts its
+// 32 bytes per half-row in the same two arrays), row scales [row][16 B], B-term
+// scales [n][16 B], B-term codes [n][128 B]
+constexpr int kRawSign = 0, kRawMag = 4096, kRawQ = 8192, kRawSfb = 10240, kRawB = 11264;
+constexpr int kRawBytes = 19456;
+// operand slot: A (128 rows x 128 B, swizzled), B (64 rows x 128 B, swizzled)
+constexpr int kOpA = 0, kOpB = 16384;
+constexpr int kOpBytes = 24576;
 constexpr long long kWaitLimit = 1LL << 22;   // polls before a wait is declared stuck
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -63,6 +71,10 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
 // 16-byte asynchronous global->shared copy; src_bytes = 0 writes zeros and reads nothing.
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes = 16) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes));
+}
+// 8-byte form (8-byte aligned addresses); src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async8(void* dst, const void* src, uint32_t src_bytes = 8) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes));
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
 template <int N>
@@ -259,7 +271,7 @@ struct FcTcArgs {
 };
 
 struct TcSmem {
-  uint64_t bar[kRing];
+  uint64_t bar[kOpRing];
   uint32_t tmem_base;
   int stuck;
   int any_gated;
@@ -276,7 +288,9 @@ __global__ void __launch_bounds__(kFcThreads, 2) fc_tc_kernel(const FcTcArgs a) 
   extern __shared__ __align__(1024) unsigned char smem_dyn[];
   // 1024-aligned operand stages, then the small shared state
   unsigned char* base = smem_dyn + ((1024 - (smem_addr(smem_dyn) & 1023)) & 1023);
-  TcSmem& sm = *reinterpret_cast<TcSmem*>(base + kRing * kSlotBytes);
+  unsigned char* ops = base;                                   // [kOpRing][kOpBytes]
+  unsigned char* raws = base + kOpRing * kOpBytes;             // [kRawRing][kRawBytes]
+  TcSmem& sm = *reinterpret_cast<TcSmem*>(raws + kRawRing * kRawBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int trow = tid & 127, half = tid >> 7;   // tile row of this thread, and which 128 weights
@@ -296,7 +310,7 @@ __global__ void __launch_bounds__(kFcThreads, 2) fc_tc_kernel(const FcTcArgs a) 
       if (slot >= a.n_slots) { record_error(MOET_ERR_DEVICE_INDEX); slot = -1; }
     }
     sm.slot = slot;
-    for (int s = 0; s < kRing; ++s) mbar_init(&sm.bar[s], 1);
+    for (int s = 0; s < kOpRing; ++s) mbar_init(&sm.bar[s], 1);
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&sm.tmem_base)),
@@ -354,119 +368,139 @@ __global__ void __launch_bounds__(kFcThreads, 2) fc_tc_kernel(const FcTcArgs a) 
   const size_t wpr = (size_t)K / 32, bpr = (size_t)K / 16;
   const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lane quarter
 
-  const int npass = do_delta ? 2 : 1;
-  const int total = nkc * npass;                 // chunks over both passes
+  // chunk sequence: nkc main-pass chunks of 256 weights, then (with the delta)
+  // nkd delta-pass chunks of 128 weights
+  const int nkd = do_delta ? K / kKD : 0;
+  const int total = nkc + nkd;
 
-  // Issue the asynchronous copies of chunk cg into its ring slot: this thread's
-  // weight row (raw planes, or the delta codes straight into the swizzled A
-  // tile), its row scale, a share of the B rows (straight into the swizzled B
-  // tile; gated tokens only in the delta pass) and one B row scale.
+  // Asynchronous copies of chunk cg into raw slot cg % kRawRing: this thread's
+  // half row of planes (or of delta codes), the row scales, a share of the
+  // B-term rows and one B-term scale row.  One commit group per chunk.
   auto prefetch = [&](int cg) {
     if (cg < total) {
       const bool dp = cg >= nkc;
       const int c = dp ? cg - nkc : cg;
-      unsigned char* slot = base + (cg % kRing) * kSlotBytes;
+      unsigned char* raw = raws + (cg % kRawRing) * kRawBytes;
       if (!dp) {
-        // half 0 copies words 0..3 of the chunk's sign and magnitude rows, half 1 words 4..7
         const uint32_t* sp = a.sign + ((size_t)e * a.N + wrow) * wpr + (size_t)c * 8 + 4 * half;
         const uint32_t* mp = a.mag + ((size_t)e * a.N + wrow) * wpr + (size_t)c * 8 + 4 * half;
-        unsigned char* ra = slot + kOffRawA + trow * 64 + 16 * half;
-        cp_async16(ra, sp);
-        cp_async16(ra + 32, mp);
-        if (half == 0)
-          cp_async16(slot + kOffRawQ + trow * 16, a.s16 + ((size_t)e * a.N + wrow) * bpr + (size_t)c * 16);
+        cp_async16(raw + kRawSign + (half * 128 + trow) * 16, sp);
+        cp_async16(raw + kRawMag + (half * 128 + trow) * 16, mp);
+        if (half == 0) cp_async16(raw + kRawQ + trow * 16, a.s16 + ((size_t)e * a.N + wrow) * bpr + (size_t)c * 16);
       } else {
-        const uint8_t* dsrc = a.dcodes + ((size_t)sm.slot * a.N + wrow) * (K / 2) + (size_t)c * 128 + 64 * half;
-        unsigned char* arow = slot + kOffA + trow * 128;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) cp_async16(arow + (((4 * half + u) ^ (trow & 7)) << 4), dsrc + 16 * u);
-        if (half == 0)
-          cp_async16(slot + kOffRawQ + trow * 16, a.ds4 + ((size_t)sm.slot * a.N + wrow) * bpr + (size_t)c * 16);
+        const uint8_t* dsrc = a.dcodes + ((size_t)sm.slot * a.N + wrow) * (K / 2) + (size_t)c * 64 + 32 * half;
+        cp_async16(raw + kRawSign + (half * 128 + trow) * 16, dsrc);
+        cp_async16(raw + kRawMag + (half * 128 + trow) * 16, dsrc + 16);
+        if (half == 0) cp_async8(raw + kRawQ + trow * 16, a.ds4 + ((size_t)sm.slot * a.N + wrow) * bpr + (size_t)c * 8);
       }
+      const int bytes_row = dp ? 64 : 128;               // B-term bytes of this chunk per row
       const uint8_t* act = dp ? a.cnat : a.cperm;
-      for (int it = tid; it < ncols * 8; it += kFcThreads) {
-        const int n = it >> 3, u = it & 7;
+      for (int it = tid; it < ncols * (bytes_row / 16); it += kFcThreads) {
+        const int n = it / (bytes_row / 16), u = it % (bytes_row / 16);
         const int tk = n / kTcTerms, term = n % kTcTerms;
         const int srow = tk < ntok ? sm.src_row[tk] : -1;
         const bool ok = srow >= 0 && (!dp || sm.gate_f[tk] != 0.0f);
-        const uint8_t* src = ok ? act + ((size_t)srow * kTcTerms + term) * (K / 2) + (size_t)c * 128 + 16 * u : act;
-        cp_async16(slot + kOffB + n * 128 + ((u ^ (n & 7)) << 4), src, ok ? 16u : 0u);
+        const uint8_t* src = ok ? act + ((size_t)srow * kTcTerms + term) * (K / 2) + (size_t)c * bytes_row + 16 * u : act;
+        cp_async16(raw + kRawB + n * 128 + 16 * u, src, ok ? 16u : 0u);
       }
       if (tid < ncols) {
         const int tk = tid / kTcTerms, term = tid % kTcTerms;
         const int srow = tk < ntok ? sm.src_row[tk] : -1;
-        const uint8_t* src = srow >= 0 ? a.sfb + ((size_t)srow * kTcTerms + term) * bpr + (size_t)c * 16 : a.sfb;
-        cp_async16(slot + kOffRawSfb + tid * 16, src, srow >= 0 ? 16u : 0u);
+        const uint8_t* src = srow >= 0 ? a.sfb + ((size_t)srow * kTcTerms + term) * bpr + (size_t)c * (dp ? 8 : 16) : a.sfb;
+        if (dp) cp_async8(raw + kRawSfb + tid * 16, src, srow >= 0 ? 8u : 0u);   // 8-byte aligned only
+        else cp_async16(raw + kRawSfb + tid * 16, src, srow >= 0 ? 16u : 0u);
       }
     }
-    cp_async_commit();                           // one group per chunk, possibly empty
+    cp_async_commit();
+  };
+
+  // Turn raw chunk cg into the operands of operand slot cg % kOpRing: expand (or
+  // copy) A into the swizzled tile, copy B into its swizzled tile, write the
+  // scale factors to TMEM.  The caller has made the slot free.
+  auto stage = [&](int cg) {
+    const bool dp = cg >= nkc;
+    const int oi = cg % kOpRing;
+    const unsigned char* raw = raws + (cg % kRawRing) * kRawBytes;
+    unsigned char* op = ops + oi * kOpBytes;
+    unsigned char* arow = op + kOpA + trow * 128;
+    const uint4 sw = *reinterpret_cast<const uint4*>(raw + kRawSign + (half * 128 + trow) * 16);
+    const uint4 mw = *reinterpret_cast<const uint4*>(raw + kRawMag + (half * 128 + trow) * 16);
+    if (!dp) {
+      const uint32_t SW[4] = {sw.x, sw.y, sw.z, sw.w};
+      const uint32_t MW[4] = {mw.x, mw.y, mw.z, mw.w};
+#pragma unroll
+      for (int w = 0; w < 4; ++w)
+        *reinterpret_cast<uint4*>(arow + (((4 * half + w) ^ (trow & 7)) << 4)) = planes_to_e2m1(SW[w], MW[w]);
+    } else {
+      *reinterpret_cast<uint4*>(arow + (((2 * half) ^ (trow & 7)) << 4)) = sw;
+      *reinterpret_cast<uint4*>(arow + (((2 * half + 1) ^ (trow & 7)) << 4)) = mw;
+    }
+    const int upr = dp ? 4 : 8;                          // 16-byte pieces per B row
+    for (int it = tid; it < ncols * upr; it += kFcThreads) {
+      const int n = it / upr, u = it % upr;
+      *reinterpret_cast<uint4*>(op + kOpB + n * 128 + ((u ^ (n & 7)) << 4)) =
+          *reinterpret_cast<const uint4*>(raw + kRawB + n * 128 + 16 * u);
+    }
+    // scale factors, replicated TMEM layout (rows lane + 32 j -> columns 4 i + j);
+    // warps 0-3 write the weight-row scales, warps 4-7 the B-term scales
+    uint32_t v[16];
+    const int src = half ? kRawSfb : kRawQ;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = lane + 32 * j;
+      uint4 q = make_uint4(0u, 0u, 0u, 0u);
+      if (!half || n < ncols) q = *reinterpret_cast<const uint4*>(raw + src + n * 16);
+      if (dp) { q.z = 0u; q.w = 0u; }                  // 128-weight chunk: two MMAs' worth
+      v[0 * 4 + j] = q.x; v[1 * 4 + j] = q.y; v[2 * 4 + j] = q.z; v[3 * 4 + j] = q.w;
+    }
+    tmem_st16(tmem + lane_q + (half ? kColSFB : kColSFA) + 16 * oi, v);
+    asm volatile("fence.proxy.async.shared::cta;");
+    asm volatile("tcgen05.wait::st.sync.aligned;");
+    asm volatile("tcgen05.fence::before_thread_sync;");
   };
 
 #pragma unroll 1
-  for (int cg = 0; cg < kRing - 1; ++cg) prefetch(cg);
+  for (int cg = 0; cg < kRawRing; ++cg) prefetch(cg);
+  cp_async_wait<kRawRing - 1>();
+  __syncthreads();
+  stage(0);
 
   int cg = 0;
 #pragma unroll 1
   for (; cg < total; ++cg) {
-    const bool dp = cg >= nkc;
-    const int c = dp ? cg - nkc : cg;
-    const int si = cg % kRing;
-    unsigned char* slot = base + si * kSlotBytes;
-    cp_async_wait<kRing - 2>();                  // this thread's copies of chunk cg have landed
-    __syncthreads();                             // ... and everyone else's
-    if (!dp) {
-      // expand this thread's 128 weights: raw sign/magnitude words -> e2m1 nibbles
-      const uint4 sw = *reinterpret_cast<const uint4*>(slot + kOffRawA + trow * 64 + 16 * half);
-      const uint4 mw = *reinterpret_cast<const uint4*>(slot + kOffRawA + trow * 64 + 32 + 16 * half);
-      const uint32_t SW[4] = {sw.x, sw.y, sw.z, sw.w};
-      const uint32_t MW[4] = {mw.x, mw.y, mw.z, mw.w};
-      unsigned char* arow = slot + kOffA + trow * 128;
-#pragma unroll
-      for (int w = 0; w < 4; ++w)
-        *reinterpret_cast<uint4*>(arow + (((4 * half + w) ^ (trow & 7)) << 4)) = planes_to_e2m1(SW[w], MW[w]);
-    }
-    {
-      // scale factors to TMEM, replicated layout: rows lane + 32 j -> columns 4 i + j;
-      // warps 0-3 write the weight-row scales, warps 4-7 the activation-term scales
-      uint32_t v[16];
-      const int src = half ? kOffRawSfb : kOffRawQ;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int n = lane + 32 * j;
-        uint4 q = make_uint4(0u, 0u, 0u, 0u);
-        if (!half || n < ncols) q = *reinterpret_cast<const uint4*>(slot + src + n * 16);
-        v[0 * 4 + j] = q.x; v[1 * 4 + j] = q.y; v[2 * 4 + j] = q.z; v[3 * 4 + j] = q.w;
-      }
-      tmem_st16(tmem + lane_q + (half ? kColSFB : kColSFA) + 16 * si, v);
-    }
-    asm volatile("fence.proxy.async.shared::cta;");
-    asm volatile("tcgen05.wait::st.sync.aligned;");
-    asm volatile("tcgen05.fence::before_thread_sync;");
-    __syncthreads();
+    cp_async_wait<kRawRing - 2>();               // this thread's copies of chunk cg + 1 landed
+    __syncthreads();                             // operands of cg staged; raw cg + 1 visible
     if (sm.stuck) break;
+    const bool dp = cg >= nkc;
+    const int oi = cg % kOpRing;
     if (tid == 0) {
       asm volatile("tcgen05.fence::after_thread_sync;");
-      const uint32_t a0 = smem_addr(slot + kOffA), b0 = smem_addr(slot + kOffB);
+      const uint32_t a0 = smem_addr(ops + oi * kOpBytes + kOpA), b0 = smem_addr(ops + oi * kOpBytes + kOpB);
       const uint32_t dcol = dp ? kColD2 : kColD;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      const int nmma = dp ? kKD / 64 : kKC / 64;
+      const int c = dp ? cg - nkc : cg;
+      for (int i = 0; i < nmma; ++i) {
         tc_mma(tmem + dcol, sw128_desc(a0 + 32 * i), sw128_desc(b0 + 32 * i), idesc,
-               tmem + kColSFA + 16 * si + 4 * i, tmem + kColSFB + 16 * si + 4 * i, (c > 0 || i > 0) ? 1u : 0u);
+               tmem + kColSFA + 16 * oi + 4 * i, tmem + kColSFB + 16 * oi + 4 * i, (c > 0 || i > 0) ? 1u : 0u);
       }
-      tc_commit(&sm.bar[si]);
+      tc_commit(&sm.bar[oi]);
     }
-    // refill the slot of chunk cg - 1 with chunk cg + kRing - 1 once its MMAs are done
-    if (cg >= 1) {
-      if (!mbar_wait(&sm.bar[(cg - 1) % kRing], ((cg - 1) / kRing) & 1)) atomicExch(&sm.stuck, 1);
+    if (cg + 1 < total) {
+      // the next operand slot was last read by the MMAs of chunk cg + 1 - kOpRing
+      if (cg + 1 >= kOpRing) {
+        const int prev = cg + 1 - kOpRing;
+        if (!mbar_wait(&sm.bar[prev % kOpRing], (prev / kOpRing) & 1)) atomicExch(&sm.stuck, 1);
+      }
+      stage(cg + 1);
     }
-    prefetch(cg + kRing - 1);
+    prefetch(cg + kRawRing);                     // raw slot of chunk cg is free since the barrier
   }
   cp_async_wait<0>();
-  // ---- drain: the last use of every slot (bounded), then read the accumulators
+  // ---- drain: the last use of every operand slot (bounded), then read the accumulators
   const int issued = cg;
-  for (int s2 = 0; s2 < kRing && s2 < issued; ++s2) {
-    const int last = issued - 1 - ((issued - 1 - s2) % kRing);   // last chunk that used slot s2
-    if (!mbar_wait(&sm.bar[s2], (last / kRing) & 1)) atomicExch(&sm.stuck, 1);
+  for (int s2 = 0; s2 < kOpRing && s2 < issued; ++s2) {
+    const int last = issued - 1 - ((issued - 1 - s2) % kOpRing);
+    if (!mbar_wait(&sm.bar[s2], (last / kOpRing) & 1)) atomicExch(&sm.stuck, 1);
   }
   asm volatile("tcgen05.fence::after_thread_sync;");
   __syncthreads();
@@ -530,7 +564,7 @@ __global__ void __launch_bounds__(kFcThreads, 2) fc_tc_kernel(const FcTcArgs a) 
 
 template <bool FC1>
 moet_status launch_fc_tc(const FcTcArgs& a, int row_tiles, int grid_y, cudaStream_t st) {
-  const size_t smem = 1024 + kRing * kSlotBytes + sizeof(TcSmem);
+  const size_t smem = 1024 + kOpRing * kOpBytes + kRawRing * kRawBytes + sizeof(TcSmem);
   auto kern = fc_tc_kernel<FC1>;
   MOET_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   {
