@@ -23,9 +23,8 @@
 // pairs; the epilogue sums the terms with their fp32 scales g_t.
 //
 // K order.  Inside each 16-element block the MMA sees the weights in the
-// order produced by the expansion (position 8r + n holds element
-// r + 4 (n & 3) + 2 (n >> 2)); the activation terms are stored in the same
-// order ("cperm").  The delta (already NVFP4) is used in its natural order
+// order produced by the expansion (position 4 r + n holds element r + 4 n);
+// the activation terms are stored in the same order ("cperm").  The delta (already NVFP4) is used in its natural order
 // against a naturally ordered copy of the terms ("cnat") and accumulates in
 // a second TMEM region.
 //
@@ -145,17 +144,20 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
 }
 
 // Sign word S and magnitude word M of 32 weights (LSB first) -> 4 words of e2m1
-// nibbles (s | 0 | m | 1) = +-0.5 / +-1.5, in the permuted K order.
+// nibbles (s | 0 | m | 1) = +-0.5 / +-1.5.  W_r collects the weights r + 4 n
+// (n = 0..7) with the sign moved to nibble bit 3 and the magnitude to bit 1;
+// its low half holds block 0 (bits 0..15), its high half block 1.  Two byte
+// permutes per block then give 16 MMA positions p = 4 r + n <- weight r + 4 n.
 __device__ __forceinline__ uint4 planes_to_e2m1(uint32_t S, uint32_t M) {
-  const uint32_t xs = (S & 0x0000FFFFu) | ((S << 14) & 0xFFFF0000u);
-  const uint32_t ys = (S >> 16) | ((S >> 2) & 0xFFFF0000u);
-  const uint32_t xm = (M & 0x0000FFFFu) | ((M << 14) & 0xFFFF0000u);
-  const uint32_t ym = (M >> 16) | ((M >> 2) & 0xFFFF0000u);
+  const uint32_t w0 = 0x11111111u | ((S << 3) & 0x88888888u) | ((M << 1) & 0x22222222u);
+  const uint32_t w1 = 0x11111111u | ((S << 2) & 0x88888888u) | (M & 0x22222222u);
+  const uint32_t w2 = 0x11111111u | ((S << 1) & 0x88888888u) | ((M >> 1) & 0x22222222u);
+  const uint32_t w3 = 0x11111111u | (S & 0x88888888u) | ((M >> 2) & 0x22222222u);
   uint4 o;
-  o.x = 0x11111111u | ((xm << 1) & 0x22222222u) | ((xs << 3) & 0x88888888u);
-  o.y = 0x11111111u | (xm & 0x22222222u) | ((xs << 2) & 0x88888888u);
-  o.z = 0x11111111u | ((ym << 1) & 0x22222222u) | ((ys << 3) & 0x88888888u);
-  o.w = 0x11111111u | (ym & 0x22222222u) | ((ys << 2) & 0x88888888u);
+  o.x = prmt(w0, w1, 0x5410u);   // block 0: weights 0,4,8,12, 1,5,9,13
+  o.y = prmt(w2, w3, 0x5410u);   // block 0: weights 2,6,10,14, 3,7,11,15
+  o.z = prmt(w0, w1, 0x7632u);   // block 1
+  o.w = prmt(w2, w3, 0x7632u);
   return o;
 }
 
@@ -210,10 +212,10 @@ __global__ void __launch_bounds__(kTermThreads) act_terms_kernel(int K, const vo
   const bool live = idx < K;                                // K % 256 == 0: all live
   float r = 0.0f;
   if (live) r = BF16_IN ? __uint_as_float((uint32_t)__ldg(sb + idx) << 16) : sf32[idx];
-  // the element whose code lands at permuted position p = 8 rr + n is rr + 4 (n & 3) + 2 (n >> 2)
+  // the element whose code lands at permuted position p = 4 r + n is r + 4 n
   const int p0 = 2 * (j & 7), p1 = p0 + 1;
-  const int src0 = (p0 >> 3) + 4 * (p0 & 3) + 2 * ((p0 >> 2) & 1);
-  const int src1 = (p1 >> 3) + 4 * (p1 & 3) + 2 * ((p1 >> 2) & 1);
+  const int src0 = (p0 >> 2) + 4 * (p0 & 3);
+  const int src1 = (p1 >> 2) + 4 * (p1 & 3);
 #pragma unroll
   for (int t = 0; t < kTcTerms; ++t) {
     const float g = ldexpf(g0, -2 * t);
@@ -373,42 +375,78 @@ __global__ void __launch_bounds__(kFcThreads, 2) fc_tc_kernel(const FcTcArgs a) 
   const int nkd = do_delta ? K / kKD : 0;
   const int total = nkc + nkd;
 
-  // Asynchronous copies of chunk cg into raw slot cg % kRawRing: this thread's
-  // half row of planes (or of delta codes), the row scales, a share of the
-  // B-term rows and one B-term scale row.  One commit group per chunk.
+  // Per-thread sources, fixed for the whole K loop.  Warps 0-3 (half 0) copy
+  // the row scales and write the weight-row scale factors; warps 4-7 (half 1)
+  // copy and stage the B-term tiles and write the B-term scale factors.
+  const size_t wrow_base = (size_t)e * a.N + wrow;
+  const uint4* sign_src = reinterpret_cast<const uint4*>(a.sign + wrow_base * wpr) + half;   // + 2 c
+  const uint4* mag_src = reinterpret_cast<const uint4*>(a.mag + wrow_base * wpr) + half;
+  const uint4* q_src = reinterpret_cast<const uint4*>(a.s16 + wrow_base * bpr);               // + c
+  const int rawp = (half * 128 + trow) * 16;                    // this thread's raw plane offset
+  int aoff[4];                                                  // swizzled A offsets of its 4 pieces
+#pragma unroll
+  for (int w = 0; w < 4; ++w) aoff[w] = kOpA + trow * 128 + (((4 * half + w) ^ (trow & 7)) << 4);
+  const int bt = tid - 128;                                     // B-side thread index (half 1)
+  // main-pass B items of this thread: it = bt + 128 m, row n = it / 8, piece u = it % 8
+  const uint8_t* bsrc[4];
+  int bdst[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const int it = bt + 128 * m;
+    const int n = it >> 3, u = it & 7;
+    bsrc[m] = nullptr;
+    bdst[m] = -1;
+    if (half == 1 && n < ncols) {
+      const int tk = n / kTcTerms, term = n % kTcTerms;
+      const int srow = tk < ntok ? sm.src_row[tk] : -1;
+      bdst[m] = n * 128 + 16 * u;
+      if (srow >= 0) bsrc[m] = a.cperm + ((size_t)srow * kTcTerms + term) * (K / 2) + 16 * u;
+    }
+  }
+  const uint8_t* sfb_src = nullptr;                             // B-term scale row (bt < ncols)
+  if (half == 1 && bt < ncols) {
+    const int tk = bt / kTcTerms, term = bt % kTcTerms;
+    const int srow = tk < ntok ? sm.src_row[tk] : -1;
+    if (srow >= 0) sfb_src = a.sfb + ((size_t)srow * kTcTerms + term) * bpr;
+  }
+
+  // Asynchronous copies of chunk cg into raw slot cg % kRawRing.  One commit
+  // group per chunk (possibly empty) keeps the group count uniform.
   auto prefetch = [&](int cg) {
     if (cg < total) {
       const bool dp = cg >= nkc;
       const int c = dp ? cg - nkc : cg;
       unsigned char* raw = raws + (cg % kRawRing) * kRawBytes;
       if (!dp) {
-        const uint32_t* sp = a.sign + ((size_t)e * a.N + wrow) * wpr + (size_t)c * 8 + 4 * half;
-        const uint32_t* mp = a.mag + ((size_t)e * a.N + wrow) * wpr + (size_t)c * 8 + 4 * half;
-        cp_async16(raw + kRawSign + (half * 128 + trow) * 16, sp);
-        cp_async16(raw + kRawMag + (half * 128 + trow) * 16, mp);
-        if (half == 0) cp_async16(raw + kRawQ + trow * 16, a.s16 + ((size_t)e * a.N + wrow) * bpr + (size_t)c * 16);
+        cp_async16(raw + kRawSign + rawp, sign_src + 2 * c);
+        cp_async16(raw + kRawMag + rawp, mag_src + 2 * c);
+        if (half == 0) cp_async16(raw + kRawQ + trow * 16, q_src + c);
+        else {
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            if (bdst[m] >= 0)
+              cp_async16(raw + kRawB + bdst[m], bsrc[m] ? bsrc[m] + (size_t)c * 128 : a.cperm, bsrc[m] ? 16u : 0u);
+          }
+          if (bt < ncols) cp_async16(raw + kRawSfb + bt * 16, sfb_src ? sfb_src + (size_t)c * 16 : a.sfb, sfb_src ? 16u : 0u);
+        }
       } else {
         const uint8_t* dsrc = a.dcodes + ((size_t)sm.slot * a.N + wrow) * (K / 2) + (size_t)c * 64 + 32 * half;
-        cp_async16(raw + kRawSign + (half * 128 + trow) * 16, dsrc);
-        cp_async16(raw + kRawMag + (half * 128 + trow) * 16, dsrc + 16);
-        if (half == 0) cp_async8(raw + kRawQ + trow * 16, a.ds4 + ((size_t)sm.slot * a.N + wrow) * bpr + (size_t)c * 8);
-      }
-      const int bytes_row = dp ? 64 : 128;               // B-term bytes of this chunk per row
-      const uint8_t* act = dp ? a.cnat : a.cperm;
-      for (int it = tid; it < ncols * (bytes_row / 16); it += kFcThreads) {
-        const int n = it / (bytes_row / 16), u = it % (bytes_row / 16);
-        const int tk = n / kTcTerms, term = n % kTcTerms;
-        const int srow = tk < ntok ? sm.src_row[tk] : -1;
-        const bool ok = srow >= 0 && (!dp || sm.gate_f[tk] != 0.0f);
-        const uint8_t* src = ok ? act + ((size_t)srow * kTcTerms + term) * (K / 2) + (size_t)c * bytes_row + 16 * u : act;
-        cp_async16(raw + kRawB + n * 128 + 16 * u, src, ok ? 16u : 0u);
-      }
-      if (tid < ncols) {
-        const int tk = tid / kTcTerms, term = tid % kTcTerms;
-        const int srow = tk < ntok ? sm.src_row[tk] : -1;
-        const uint8_t* src = srow >= 0 ? a.sfb + ((size_t)srow * kTcTerms + term) * bpr + (size_t)c * (dp ? 8 : 16) : a.sfb;
-        if (dp) cp_async8(raw + kRawSfb + tid * 16, src, srow >= 0 ? 8u : 0u);   // 8-byte aligned only
-        else cp_async16(raw + kRawSfb + tid * 16, src, srow >= 0 ? 16u : 0u);
+        cp_async16(raw + kRawSign + rawp, dsrc);
+        cp_async16(raw + kRawMag + rawp, dsrc + 16);
+        if (half == 0) {
+          cp_async8(raw + kRawQ + trow * 16, a.ds4 + ((size_t)sm.slot * a.N + wrow) * bpr + (size_t)c * 8);
+        } else {
+          for (int it = bt; it < ncols * 4; it += 128) {              // 64 bytes per B row
+            const int n = it >> 2, u = it & 3;
+            const int tk = n / kTcTerms, term = n % kTcTerms;
+            const int srow = tk < ntok ? sm.src_row[tk] : -1;
+            const bool ok = srow >= 0 && sm.gate_f[tk] != 0.0f;
+            const uint8_t* src = ok ? a.cnat + ((size_t)srow * kTcTerms + term) * (K / 2) + (size_t)c * 64 + 16 * u : a.cnat;
+            cp_async16(raw + kRawB + n * 128 + 16 * u, src, ok ? 16u : 0u);
+          }
+          if (bt < ncols)
+            cp_async8(raw + kRawSfb + bt * 16, sfb_src ? sfb_src + (size_t)c * 8 : a.sfb, sfb_src ? 8u : 0u);
+        }
       }
     }
     cp_async_commit();
@@ -422,24 +460,25 @@ __global__ void __launch_bounds__(kFcThreads, 2) fc_tc_kernel(const FcTcArgs a) 
     const int oi = cg % kOpRing;
     const unsigned char* raw = raws + (cg % kRawRing) * kRawBytes;
     unsigned char* op = ops + oi * kOpBytes;
-    unsigned char* arow = op + kOpA + trow * 128;
-    const uint4 sw = *reinterpret_cast<const uint4*>(raw + kRawSign + (half * 128 + trow) * 16);
-    const uint4 mw = *reinterpret_cast<const uint4*>(raw + kRawMag + (half * 128 + trow) * 16);
+    const uint4 sw = *reinterpret_cast<const uint4*>(raw + kRawSign + rawp);
+    const uint4 mw = *reinterpret_cast<const uint4*>(raw + kRawMag + rawp);
     if (!dp) {
       const uint32_t SW[4] = {sw.x, sw.y, sw.z, sw.w};
       const uint32_t MW[4] = {mw.x, mw.y, mw.z, mw.w};
 #pragma unroll
-      for (int w = 0; w < 4; ++w)
-        *reinterpret_cast<uint4*>(arow + (((4 * half + w) ^ (trow & 7)) << 4)) = planes_to_e2m1(SW[w], MW[w]);
+      for (int w = 0; w < 4; ++w) *reinterpret_cast<uint4*>(op + aoff[w]) = planes_to_e2m1(SW[w], MW[w]);
     } else {
+      unsigned char* arow = op + kOpA + trow * 128;
       *reinterpret_cast<uint4*>(arow + (((2 * half) ^ (trow & 7)) << 4)) = sw;
       *reinterpret_cast<uint4*>(arow + (((2 * half + 1) ^ (trow & 7)) << 4)) = mw;
     }
-    const int upr = dp ? 4 : 8;                          // 16-byte pieces per B row
-    for (int it = tid; it < ncols * upr; it += kFcThreads) {
-      const int n = it / upr, u = it % upr;
-      *reinterpret_cast<uint4*>(op + kOpB + n * 128 + ((u ^ (n & 7)) << 4)) =
-          *reinterpret_cast<const uint4*>(raw + kRawB + n * 128 + 16 * u);
+    if (half == 1) {
+      const int upr = dp ? 4 : 8;                        // 16-byte pieces per B row
+      for (int it = bt; it < ncols * upr; it += 128) {
+        const int n = it / upr, u = it % upr;
+        *reinterpret_cast<uint4*>(op + kOpB + n * 128 + ((u ^ (n & 7)) << 4)) =
+            *reinterpret_cast<const uint4*>(raw + kRawB + n * 128 + 16 * u);
+      }
     }
     // scale factors, replicated TMEM layout (rows lane + 32 j -> columns 4 i + j);
     // warps 0-3 write the weight-row scales, warps 4-7 the B-term scales
