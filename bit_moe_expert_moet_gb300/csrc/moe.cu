@@ -67,7 +67,7 @@ inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   L.o = off;         off += align256(sizeof(float) * pairs * H);
   L.xt = off; L.ht = off;
   if (T <= kTcMaxT && tc_supported(H, I)) {
-    L.xt = off;      off += align256(tc_terms_bytes((size_t)T, (size_t)H));
+    L.xt = off;      off += align256(tc_terms_bytes(pairs, (size_t)H));
     L.ht = off;      off += align256(tc_terms_bytes(pairs, (size_t)I));
   }
   L.total = off;
@@ -548,7 +548,7 @@ extern "C" moet_status moet_moe_forward(int T, int H, int I, int E, int k, const
       *sf = reinterpret_cast<uint8_t*>(base + off);    off += align256(rows * kTcTerms * (K / 16));
       *g = reinterpret_cast<float*>(base + off);
     };
-    carve(ws + L.xt, (size_t)T, (size_t)H, &f.buf.x_cperm, &f.buf.x_cnat, &f.buf.x_sf, &f.buf.x_g);
+    carve(ws + L.xt, pairs, (size_t)H, &f.buf.x_cperm, &f.buf.x_cnat, &f.buf.x_sf, &f.buf.x_g);
     carve(ws + L.ht, pairs, (size_t)I, &f.buf.h_cperm, &f.buf.h_cnat, &f.buf.h_sf, &f.buf.h_g);
     moet_status s = tc_forward(f, st);
     if (s != MOET_OK) return s;

@@ -28,16 +28,19 @@
 // against a naturally ordered copy of the terms ("cnat") and accumulates in
 // a second TMEM region.
 //
-// Pipeline per CTA (256 threads; threads t and t + 128 share tile row t):
-// raw chunks of 256 weights stream into a kRawRing-deep cp.async ring (planes,
-// scales and activation terms, ~19 KB per chunk), refilled as soon as they
-// are staged; staging expands a raw chunk into a kOpRing-deep operand ring
-// (swizzled A and B tiles in shared memory, scale factors in TMEM).  Each
-// iteration has one CTA barrier: thread 0 issues the 4 MMAs (K = 64) of the
-// chunk staged in the previous iteration and commits them to that operand
-// slot's mbarrier, while everyone stages the next chunk into the other slot
-// after a bounded wait for the MMAs that last read it.
+// Pipeline per CTA (6 warps, warp-specialised, no CTA-wide barrier in the K
+// loop): warp 0 (one thread) streams each 256-weight K chunk into one of
+// kSlots shared-memory slots with TMA (sign and magnitude planes, row scales,
+// the work item's 64 activation-term rows and their scales); warps 2-5 (one
+// thread per weight row = TMEM lane) expand the planes into the swizzled A
+// tile and write the scale factors to TMEM; warp 1 (one thread) issues the 4
+// MMAs (K = 64) per chunk and commits them to the slot's "empty" mbarrier.
+// Hand-offs: full (TMA bytes landed) -> staged (128 converter arrivals) ->
+// empty (MMA commit); every wait is bounded.
+#include <cuda.h>
 #include <cuda_bf16.h>
+
+#include <cstring>
 
 #include "common.cuh"
 #include "moe_tc.cuh"
@@ -45,39 +48,22 @@
 namespace moet {
 namespace {
 
-constexpr int kFcThreads = 256;               // FC kernel: two threads per weight row
-constexpr int kRawRing = 3;                   // raw chunks in flight (cp.async)
-constexpr int kOpRing = 2;                    // operand slots (A, B, scales) in use by the tensor core
-constexpr int kKC = 256;                      // weights per main-pass K chunk (one SW128 atom)
-constexpr int kKD = 128;                      // weights per delta-pass K chunk
+constexpr int kWsThreads = 192;              // warp 0: TMA producer, warp 1: MMA, warps 2-5: converters
+constexpr int kSlots = 3;                     // K chunks in flight
+constexpr int kKC = 256;                      // weights per K chunk (one SW128 atom)
 constexpr int kMaxN = kTcTerms * kTcTok;      // 64 columns of D
 constexpr int kTmemCols = 256;
-constexpr int kColD = 0, kColD2 = 64, kColSFA = 128, kColSFB = 128 + 16 * kOpRing;
-// raw slot: planes [half][row][16 B] (sign, then magnitude; the delta pass puts its
-// 32 bytes per half-row in the same two arrays), row scales [row][16 B], B-term
-// scales [n][16 B], B-term codes [n][128 B]
-constexpr int kRawSign = 0, kRawMag = 4096, kRawQ = 8192, kRawSfb = 10240, kRawB = 11264;
-constexpr int kRawBytes = 19456;
-// operand slot: A (128 rows x 128 B, swizzled), B (64 rows x 128 B, swizzled)
-constexpr int kOpA = 0, kOpB = 16384;
-constexpr int kOpBytes = 24576;
+constexpr int kColD = 0, kColD2 = 64, kColSFA = 128, kColSFB = 128 + 16 * kSlots;
+// slot layout (1024-aligned): A operand (128 rows x 128 B, SW128), B operand (64 rows x 128 B,
+// SW128), raw sign and magnitude planes [128 rows][32 B], raw row scales [128][16 B], raw B-term
+// scales [64 rows][16 B]
+constexpr int kSA = 0, kSB = 16384, kSSign = 24576, kSMag = 28672, kSQ = 32768, kSF = 34816;
+constexpr int kSlotBytes = 36864;
 constexpr long long kWaitLimit = 1LL << 22;   // polls before a wait is declared stuck
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
-
-// 16-byte asynchronous global->shared copy; src_bytes = 0 writes zeros and reads nothing.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes = 16) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes));
-}
-// 8-byte form (8-byte aligned addresses); src_bytes = 0 writes zeros.
-__device__ __forceinline__ void cp_async8(void* dst, const void* src, uint32_t src_bytes = 8) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N)); }
 
 // SW128 K-major shared-memory matrix descriptor: 8-row groups 1024 B apart.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
@@ -175,12 +161,15 @@ constexpr int kTermThreads = 256;
 
 template <bool BF16_IN>
 __global__ void __launch_bounds__(kTermThreads) act_terms_kernel(int K, const void* __restrict__ src,
+                                                                const int32_t* __restrict__ row_map, int map_div,
                                                                 uint8_t* __restrict__ cperm, uint8_t* __restrict__ cnat,
                                                                 uint8_t* __restrict__ sfb, float* __restrict__ gsc) {
   __shared__ float red[kTermThreads / 32];
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
-  const uint16_t* sb = static_cast<const uint16_t*>(src) + (size_t)row * K;
-  const float* sf32 = static_cast<const float*>(src) + (size_t)row * K;
+  // output row `row` expands source row row_map[row] / map_div (or `row` itself)
+  const size_t srow = row_map ? (size_t)(__ldg(row_map + row) / map_div) : (size_t)row;
+  const uint16_t* sb = static_cast<const uint16_t*>(src) + srow * K;
+  const float* sf32 = static_cast<const float*>(src) + srow * K;
   float m = 0.0f;
   if (BF16_IN) {
     const uint4* p = reinterpret_cast<const uint4*>(sb);
@@ -249,33 +238,35 @@ __global__ void __launch_bounds__(kTermThreads) act_terms_kernel(int K, const vo
 }
 
 // ---------------------------------------------------------------- FC kernel
+struct TmaMaps {
+  CUtensorMap sign, mag, q;        // planes u32 [E N, K/32] box {8, 64}; s16 u8 [E N, K/16] box {16, 64}
+  CUtensorMap act, actn, sfb;      // terms u8 [pairs 4, K/2] box {128, 64} SW128 (perm / natural); scales box {16, 64}
+  CUtensorMap dcodes, ds4;         // delta u8 [S N, K/2] box {128, 64} SW128; scales box {16, 64}
+};
+
 struct FcTcArgs {
   int T, H, I, k, K, N;          // N = rows of one expert matrix
+  int brows;                     // rows of the activation-term box: min(64, 4 * term rows)
   const int32_t* offsets;
   const int32_t* perm;
   const float* topk_w;
-  const uint32_t* sign;
-  const uint32_t* mag;
-  const uint8_t* s16;
   const float* scale_2;
   const int32_t* delta_slot;
   int n_slots;
-  const uint8_t* dcodes;
-  const uint8_t* ds4;
   const uint8_t* gate;
   const int* hdr;
   const int4* chunks;
-  const uint8_t* cperm;          // activation terms (rows: FC1 tokens, FC2 bucketed pairs)
-  const uint8_t* cnat;
-  const uint8_t* sfb;
   const float* gsc;
   float* out;
 };
 
 struct TcSmem {
-  uint64_t bar[kOpRing];
+  uint64_t full[kSlots];         // TMA bytes landed
+  uint64_t staged[kSlots];       // converters done (A expanded, scales in TMEM)
+  uint64_t empty[kSlots];        // MMAs of the slot done
   uint32_t tmem_base;
   int stuck;
+  int issued;                    // MMA chunks issued
   int any_gated;
   int slot;
   int src_row[kTcTok];           // activation-term row per token of the work item
@@ -285,17 +276,35 @@ struct TcSmem {
   int pair[kTcTok];              // FC2: pair id per column token
 };
 
-template <bool FC1>
-__global__ void __launch_bounds__(kFcThreads, 2) fc_tc_kernel(const FcTcArgs a) {
-  extern __shared__ __align__(1024) unsigned char smem_dyn[];
-  // 1024-aligned operand stages, then the small shared state
-  unsigned char* base = smem_dyn + ((1024 - (smem_addr(smem_dyn) & 1023)) & 1023);
-  unsigned char* ops = base;                                   // [kOpRing][kOpBytes]
-  unsigned char* raws = base + kOpRing * kOpBytes;             // [kRawRing][kRawBytes]
-  TcSmem& sm = *reinterpret_cast<TcSmem*>(raws + kRawRing * kRawBytes);
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
 
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool is_stuck(const TcSmem& sm) {
+  return *reinterpret_cast<const volatile int*>(&sm.stuck) != 0;
+}
+
+// Warp-specialised FC over one 128-row weight tile of one expert and one work
+// item of <= kTcTok routed pairs.  Main pass: K chunks of 256 weights from the
+// 2-bit planes; delta pass (cached expert with gated pairs): the same chunks
+// of the NVFP4 delta into a second accumulator.
+template <bool FC1>
+__global__ void __launch_bounds__(kWsThreads, 2) fc_tc_kernel(const FcTcArgs a, const __grid_constant__ TmaMaps maps) {
+  extern __shared__ __align__(1024) unsigned char smem_dyn[];
+  unsigned char* base = smem_dyn + ((1024 - (smem_addr(smem_dyn) & 1023)) & 1023);
+  TcSmem& sm = *reinterpret_cast<TcSmem*>(base + kSlots * kSlotBytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int trow = tid & 127, half = tid >> 7;   // tile row of this thread, and which 128 weights
   if ((int)blockIdx.y >= a.hdr[0]) return;
   const int4 ch = a.chunks[blockIdx.y];
   const int e = ch.x, ntok = ch.z;
@@ -305,6 +314,7 @@ __global__ void __launch_bounds__(kFcThreads, 2) fc_tc_kernel(const FcTcArgs a) 
 
   if (tid == 0) {
     sm.stuck = 0;
+    sm.issued = 0;
     sm.any_gated = 0;
     int slot = -1;
     if (a.delta_slot != nullptr && a.gate != nullptr) {
@@ -312,9 +322,14 @@ __global__ void __launch_bounds__(kFcThreads, 2) fc_tc_kernel(const FcTcArgs a) 
       if (slot >= a.n_slots) { record_error(MOET_ERR_DEVICE_INDEX); slot = -1; }
     }
     sm.slot = slot;
-    for (int s = 0; s < kOpRing; ++s) mbar_init(&sm.bar[s], 1);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.staged[s], 128);
+      mbar_init(&sm.empty[s], 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;");
   }
-  if (warp == 0) {
+  if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&sm.tmem_base)),
                  "r"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -343,272 +358,251 @@ __global__ void __launch_bounds__(kFcThreads, 2) fc_tc_kernel(const FcTcArgs a) 
   __syncthreads();
   if (tid < kMaxN) {
     const int tk = tid / kTcTerms, term = tid % kTcTerms;
-    const int srow = tk < kTcTok ? sm.src_row[tk] : -1;
-    sm.gsc[tid] = srow >= 0 ? __ldg(a.gsc + (size_t)srow * kTcTerms + term) : 0.0f;
+    sm.gsc[tid] = tk < ntok && sm.src_row[tk] >= 0 ? __ldg(a.gsc + (size_t)(pos0 + tk) * kTcTerms + term) : 0.0f;
   }
   asm volatile("tcgen05.fence::before_thread_sync;");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;");
   const uint32_t tmem = sm.tmem_base;
   const bool do_delta = sm.slot >= 0 && sm.any_gated;
-  const uint32_t idesc = mxf4_idesc(ncols);
+  const int total = do_delta ? 2 * nkc : nkc;
+  // the two 64-row halves of the tile in the expert's matrix (FC1: gate rows, then up rows)
+  const int r0 = FC1 ? blockIdx.x * 64 : blockIdx.x * 128;
+  const int r1 = FC1 ? a.I + blockIdx.x * 64 : blockIdx.x * 128 + 64;
 
-  // the weight row owned by this thread
-  int wrow;
-  if (FC1) {
-    wrow = trow < 64 ? blockIdx.x * 64 + trow : a.I + blockIdx.x * 64 + (trow - 64);
-  } else {
-    wrow = blockIdx.x * 128 + trow;
-  }
-  // weight rows whose scales this thread writes to TMEM (replicated layout: rows lane + 32 j)
-  int srows[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int tr = lane + 32 * j;
-    srows[j] = FC1 ? (tr < 64 ? blockIdx.x * 64 + tr : a.I + blockIdx.x * 64 + (tr - 64)) : blockIdx.x * 128 + tr;
-  }
-  const size_t wpr = (size_t)K / 32, bpr = (size_t)K / 16;
-  const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lane quarter
-
-  // chunk sequence: nkc main-pass chunks of 256 weights, then (with the delta)
-  // nkd delta-pass chunks of 128 weights
-  const int nkd = do_delta ? K / kKD : 0;
-  const int total = nkc + nkd;
-
-  // Per-thread sources, fixed for the whole K loop.  Warps 0-3 (half 0) copy
-  // the row scales and write the weight-row scale factors; warps 4-7 (half 1)
-  // copy and stage the B-term tiles and write the B-term scale factors.
-  const size_t wrow_base = (size_t)e * a.N + wrow;
-  const uint4* sign_src = reinterpret_cast<const uint4*>(a.sign + wrow_base * wpr) + half;   // + 2 c
-  const uint4* mag_src = reinterpret_cast<const uint4*>(a.mag + wrow_base * wpr) + half;
-  const uint4* q_src = reinterpret_cast<const uint4*>(a.s16 + wrow_base * bpr);               // + c
-  const int rawp = (half * 128 + trow) * 16;                    // this thread's raw plane offset
-  int aoff[4];                                                  // swizzled A offsets of its 4 pieces
-#pragma unroll
-  for (int w = 0; w < 4; ++w) aoff[w] = kOpA + trow * 128 + (((4 * half + w) ^ (trow & 7)) << 4);
-  const int bt = tid - 128;                                     // B-side thread index (half 1)
-  // main-pass B items of this thread: it = bt + 128 m, row n = it / 8, piece u = it % 8
-  const uint8_t* bsrc[4];
-  int bdst[4];
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    const int it = bt + 128 * m;
-    const int n = it >> 3, u = it & 7;
-    bsrc[m] = nullptr;
-    bdst[m] = -1;
-    if (half == 1 && n < ncols) {
-      const int tk = n / kTcTerms, term = n % kTcTerms;
-      const int srow = tk < ntok ? sm.src_row[tk] : -1;
-      bdst[m] = n * 128 + 16 * u;
-      if (srow >= 0) bsrc[m] = a.cperm + ((size_t)srow * kTcTerms + term) * (K / 2) + 16 * u;
-    }
-  }
-  const uint8_t* sfb_src = nullptr;                             // B-term scale row (bt < ncols)
-  if (half == 1 && bt < ncols) {
-    const int tk = bt / kTcTerms, term = bt % kTcTerms;
-    const int srow = tk < ntok ? sm.src_row[tk] : -1;
-    if (srow >= 0) sfb_src = a.sfb + ((size_t)srow * kTcTerms + term) * bpr;
-  }
-
-  // Asynchronous copies of chunk cg into raw slot cg % kRawRing.  One commit
-  // group per chunk (possibly empty) keeps the group count uniform.
-  auto prefetch = [&](int cg) {
-    if (cg < total) {
-      const bool dp = cg >= nkc;
-      const int c = dp ? cg - nkc : cg;
-      unsigned char* raw = raws + (cg % kRawRing) * kRawBytes;
-      if (!dp) {
-        cp_async16(raw + kRawSign + rawp, sign_src + 2 * c);
-        cp_async16(raw + kRawMag + rawp, mag_src + 2 * c);
-        if (half == 0) cp_async16(raw + kRawQ + trow * 16, q_src + c);
-        else {
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            if (bdst[m] >= 0)
-              cp_async16(raw + kRawB + bdst[m], bsrc[m] ? bsrc[m] + (size_t)c * 128 : a.cperm, bsrc[m] ? 16u : 0u);
-          }
-          if (bt < ncols) cp_async16(raw + kRawSfb + bt * 16, sfb_src ? sfb_src + (size_t)c * 16 : a.sfb, sfb_src ? 16u : 0u);
-        }
-      } else {
-        const uint8_t* dsrc = a.dcodes + ((size_t)sm.slot * a.N + wrow) * (K / 2) + (size_t)c * 64 + 32 * half;
-        cp_async16(raw + kRawSign + rawp, dsrc);
-        cp_async16(raw + kRawMag + rawp, dsrc + 16);
-        if (half == 0) {
-          cp_async8(raw + kRawQ + trow * 16, a.ds4 + ((size_t)sm.slot * a.N + wrow) * bpr + (size_t)c * 8);
+  if (warp == 0) {
+    // ---------------- producer: one thread issues every TMA copy
+    if (lane == 0) {
+      for (int cg = 0; cg < total; ++cg) {
+        const int s = cg % kSlots, u = cg / kSlots;
+        if (u > 0 && !mbar_wait(&sm.empty[s], (u - 1) & 1)) { atomicExch(&sm.stuck, 1); break; }
+        if (is_stuck(sm)) break;
+        const bool dp = cg >= nkc;
+        const int c = dp ? cg - nkc : cg;
+        unsigned char* sl = base + s * kSlotBytes;
+        const uint32_t bytes = (dp ? 16384u + 2048u : 4096u + 4096u + 2048u) + (uint32_t)a.brows * (128u + 16u);
+        mbar_expect_tx(&sm.full[s], bytes);
+        if (!dp) {
+          const int y0 = e * a.N + r0, y1 = e * a.N + r1;
+          tma_load_2d(smem_addr(sl + kSSign), &maps.sign, c * 8, y0, &sm.full[s]);
+          tma_load_2d(smem_addr(sl + kSSign + 2048), &maps.sign, c * 8, y1, &sm.full[s]);
+          tma_load_2d(smem_addr(sl + kSMag), &maps.mag, c * 8, y0, &sm.full[s]);
+          tma_load_2d(smem_addr(sl + kSMag + 2048), &maps.mag, c * 8, y1, &sm.full[s]);
+          tma_load_2d(smem_addr(sl + kSQ), &maps.q, c * 16, y0, &sm.full[s]);
+          tma_load_2d(smem_addr(sl + kSQ + 1024), &maps.q, c * 16, y1, &sm.full[s]);
         } else {
-          for (int it = bt; it < ncols * 4; it += 128) {              // 64 bytes per B row
-            const int n = it >> 2, u = it & 3;
-            const int tk = n / kTcTerms, term = n % kTcTerms;
-            const int srow = tk < ntok ? sm.src_row[tk] : -1;
-            const bool ok = srow >= 0 && sm.gate_f[tk] != 0.0f;
-            const uint8_t* src = ok ? a.cnat + ((size_t)srow * kTcTerms + term) * (K / 2) + (size_t)c * 64 + 16 * u : a.cnat;
-            cp_async16(raw + kRawB + n * 128 + 16 * u, src, ok ? 16u : 0u);
-          }
-          if (bt < ncols)
-            cp_async8(raw + kRawSfb + bt * 16, sfb_src ? sfb_src + (size_t)c * 8 : a.sfb, sfb_src ? 8u : 0u);
+          const int y0 = sm.slot * a.N + r0, y1 = sm.slot * a.N + r1;
+          tma_load_2d(smem_addr(sl + kSA), &maps.dcodes, c * 128, y0, &sm.full[s]);
+          tma_load_2d(smem_addr(sl + kSA + 8192), &maps.dcodes, c * 128, y1, &sm.full[s]);
+          tma_load_2d(smem_addr(sl + kSQ), &maps.ds4, c * 16, y0, &sm.full[s]);
+          tma_load_2d(smem_addr(sl + kSQ + 1024), &maps.ds4, c * 16, y1, &sm.full[s]);
         }
+        // the work item's pairs are consecutive bucketed rows: one 64-row box of terms
+        tma_load_2d(smem_addr(sl + kSB), dp ? &maps.actn : &maps.act, c * 128, pos0 * kTcTerms, &sm.full[s]);
+        tma_load_2d(smem_addr(sl + kSF), &maps.sfb, c * 16, pos0 * kTcTerms, &sm.full[s]);
       }
     }
-    cp_async_commit();
-  };
-
-  // Turn raw chunk cg into the operands of operand slot cg % kOpRing: expand (or
-  // copy) A into the swizzled tile, copy B into its swizzled tile, write the
-  // scale factors to TMEM.  The caller has made the slot free.
-  auto stage = [&](int cg) {
-    const bool dp = cg >= nkc;
-    const int oi = cg % kOpRing;
-    const unsigned char* raw = raws + (cg % kRawRing) * kRawBytes;
-    unsigned char* op = ops + oi * kOpBytes;
-    const uint4 sw = *reinterpret_cast<const uint4*>(raw + kRawSign + rawp);
-    const uint4 mw = *reinterpret_cast<const uint4*>(raw + kRawMag + rawp);
-    if (!dp) {
-      const uint32_t SW[4] = {sw.x, sw.y, sw.z, sw.w};
-      const uint32_t MW[4] = {mw.x, mw.y, mw.z, mw.w};
+  } else if (warp == 1) {
+    // ---------------- MMA issue: one thread
+    if (lane == 0) {
+      const uint32_t idesc = mxf4_idesc(ncols);
+      int cg = 0;
+      for (; cg < total; ++cg) {
+        const int s = cg % kSlots, u = cg / kSlots;
+        if (!mbar_wait(&sm.staged[s], u & 1)) { atomicExch(&sm.stuck, 1); break; }
+        if (is_stuck(sm)) break;
+        asm volatile("tcgen05.fence::after_thread_sync;");
+        const bool dp = cg >= nkc;
+        const int c = dp ? cg - nkc : cg;
+        unsigned char* sl = base + s * kSlotBytes;
+        const uint32_t a0 = smem_addr(sl + kSA), b0 = smem_addr(sl + kSB);
 #pragma unroll
-      for (int w = 0; w < 4; ++w) *reinterpret_cast<uint4*>(op + aoff[w]) = planes_to_e2m1(SW[w], MW[w]);
-    } else {
-      unsigned char* arow = op + kOpA + trow * 128;
-      *reinterpret_cast<uint4*>(arow + (((2 * half) ^ (trow & 7)) << 4)) = sw;
-      *reinterpret_cast<uint4*>(arow + (((2 * half + 1) ^ (trow & 7)) << 4)) = mw;
-    }
-    if (half == 1) {
-      const int upr = dp ? 4 : 8;                        // 16-byte pieces per B row
-      for (int it = bt; it < ncols * upr; it += 128) {
-        const int n = it / upr, u = it % upr;
-        *reinterpret_cast<uint4*>(op + kOpB + n * 128 + ((u ^ (n & 7)) << 4)) =
-            *reinterpret_cast<const uint4*>(raw + kRawB + n * 128 + 16 * u);
-      }
-    }
-    // scale factors, replicated TMEM layout (rows lane + 32 j -> columns 4 i + j);
-    // warps 0-3 write the weight-row scales, warps 4-7 the B-term scales
-    uint32_t v[16];
-    const int src = half ? kRawSfb : kRawQ;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int n = lane + 32 * j;
-      uint4 q = make_uint4(0u, 0u, 0u, 0u);
-      if (!half || n < ncols) q = *reinterpret_cast<const uint4*>(raw + src + n * 16);
-      if (dp) { q.z = 0u; q.w = 0u; }                  // 128-weight chunk: two MMAs' worth
-      v[0 * 4 + j] = q.x; v[1 * 4 + j] = q.y; v[2 * 4 + j] = q.z; v[3 * 4 + j] = q.w;
-    }
-    tmem_st16(tmem + lane_q + (half ? kColSFB : kColSFA) + 16 * oi, v);
-    asm volatile("fence.proxy.async.shared::cta;");
-    asm volatile("tcgen05.wait::st.sync.aligned;");
-    asm volatile("tcgen05.fence::before_thread_sync;");
-  };
-
-#pragma unroll 1
-  for (int cg = 0; cg < kRawRing; ++cg) prefetch(cg);
-  cp_async_wait<kRawRing - 1>();
-  __syncthreads();
-  stage(0);
-
-  int cg = 0;
-#pragma unroll 1
-  for (; cg < total; ++cg) {
-    cp_async_wait<kRawRing - 2>();               // this thread's copies of chunk cg + 1 landed
-    __syncthreads();                             // operands of cg staged; raw cg + 1 visible
-    if (sm.stuck) break;
-    const bool dp = cg >= nkc;
-    const int oi = cg % kOpRing;
-    if (tid == 0) {
-      asm volatile("tcgen05.fence::after_thread_sync;");
-      const uint32_t a0 = smem_addr(ops + oi * kOpBytes + kOpA), b0 = smem_addr(ops + oi * kOpBytes + kOpB);
-      const uint32_t dcol = dp ? kColD2 : kColD;
-      const int nmma = dp ? kKD / 64 : kKC / 64;
-      const int c = dp ? cg - nkc : cg;
-      for (int i = 0; i < nmma; ++i) {
-        tc_mma(tmem + dcol, sw128_desc(a0 + 32 * i), sw128_desc(b0 + 32 * i), idesc,
-               tmem + kColSFA + 16 * oi + 4 * i, tmem + kColSFB + 16 * oi + 4 * i, (c > 0 || i > 0) ? 1u : 0u);
-      }
-      tc_commit(&sm.bar[oi]);
-    }
-    if (cg + 1 < total) {
-      // the next operand slot was last read by the MMAs of chunk cg + 1 - kOpRing
-      if (cg + 1 >= kOpRing) {
-        const int prev = cg + 1 - kOpRing;
-        if (!mbar_wait(&sm.bar[prev % kOpRing], (prev / kOpRing) & 1)) atomicExch(&sm.stuck, 1);
-      }
-      stage(cg + 1);
-    }
-    prefetch(cg + kRawRing);                     // raw slot of chunk cg is free since the barrier
-  }
-  cp_async_wait<0>();
-  // ---- drain: the last use of every operand slot (bounded), then read the accumulators
-  const int issued = cg;
-  for (int s2 = 0; s2 < kOpRing && s2 < issued; ++s2) {
-    const int last = issued - 1 - ((issued - 1 - s2) % kOpRing);
-    if (!mbar_wait(&sm.bar[s2], (last / kOpRing) & 1)) atomicExch(&sm.stuck, 1);
-  }
-  asm volatile("tcgen05.fence::after_thread_sync;");
-  __syncthreads();
-  if (sm.stuck) {
-    if (tid == 0) record_error(MOET_ERR_TIMEOUT);
-  } else if (half == 0) {
-    // FC1: up rows hand their values to the gate rows through the (now idle) ring memory
-    float (*xchg)[kTcTok] = reinterpret_cast<float (*)[kTcTok]>(base);
-    const float sc2 = 2.0f * __ldg(a.scale_2 + e);           // 2: the halved e2m1 levels
-    const float sc2d = __ldg(a.scale_2 + e);
-    for (int c0 = 0; c0 < ncols; c0 += 16) {
-      float v[16], v2[16];
-      tmem_ld16(tmem + lane_q + kColD + c0, v);
-      if (do_delta) tmem_ld16(tmem + lane_q + kColD2 + c0, v2);
-      float acc[16 / kTcTerms];
-#pragma unroll
-      for (int q = 0; q < 16 / kTcTerms; ++q) {
-        float sacc = 0.0f;
-#pragma unroll
-        for (int t = 0; t < kTcTerms; ++t) {
-          const int col = q * kTcTerms + t;
-          float d = sc2 * v[col];
-          if (do_delta) d = fmaf(sc2d, v2[col], d);
-          sacc = fmaf(sm.gsc[c0 + col], d, sacc);
+        for (int i = 0; i < 4; ++i) {
+          tc_mma(tmem + (dp ? kColD2 : kColD), sw128_desc(a0 + 32 * i), sw128_desc(b0 + 32 * i), idesc,
+                 tmem + kColSFA + 16 * s + 4 * i, tmem + kColSFB + 16 * s + 4 * i, (c > 0 || i > 0) ? 1u : 0u);
         }
-        acc[q] = sacc;
+        tc_commit(&sm.empty[s]);
       }
-      if (!FC1) {
+      sm.issued = cg;
+    }
+  } else {
+    // ---------------- converters: thread = tile row = TMEM lane
+    const int trow = 32 * (warp & 3) + lane;
+    const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;
+    for (int cg = 0; cg < total; ++cg) {
+      const int s = cg % kSlots, u = cg / kSlots;
+      if (!mbar_wait(&sm.full[s], u & 1)) { atomicExch(&sm.stuck, 1); break; }
+      if (is_stuck(sm)) break;
+      const bool dp = cg >= nkc;
+      unsigned char* sl = base + s * kSlotBytes;
+      if (!dp) {
+        const uint4 s0 = *reinterpret_cast<const uint4*>(sl + kSSign + trow * 32);
+        const uint4 s1 = *reinterpret_cast<const uint4*>(sl + kSSign + trow * 32 + 16);
+        const uint4 m0 = *reinterpret_cast<const uint4*>(sl + kSMag + trow * 32);
+        const uint4 m1 = *reinterpret_cast<const uint4*>(sl + kSMag + trow * 32 + 16);
+        const uint32_t SW[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+        const uint32_t MW[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+        unsigned char* arow = sl + kSA + trow * 128;
+#pragma unroll
+        for (int w = 0; w < 8; ++w)
+          *reinterpret_cast<uint4*>(arow + ((w ^ (trow & 7)) << 4)) = planes_to_e2m1(SW[w], MW[w]);
+      }
+      // scale factors to TMEM, replicated layout: rows lane + 32 j -> columns 4 i + j
+      uint32_t va[16], vb[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 q = *reinterpret_cast<const uint4*>(sl + kSQ + (lane + 32 * j) * 16);
+        va[0 * 4 + j] = q.x; va[1 * 4 + j] = q.y; va[2 * 4 + j] = q.z; va[3 * 4 + j] = q.w;
+        const int n = lane + 32 * j;
+        uint4 r = make_uint4(0u, 0u, 0u, 0u);
+        if (n < kMaxN) r = *reinterpret_cast<const uint4*>(sl + kSF + n * 16);
+        vb[0 * 4 + j] = r.x; vb[1 * 4 + j] = r.y; vb[2 * 4 + j] = r.z; vb[3 * 4 + j] = r.w;
+      }
+      tmem_st16(tmem + lane_q + kColSFA + 16 * s, va);
+      tmem_st16(tmem + lane_q + kColSFB + 16 * s, vb);
+      asm volatile("fence.proxy.async.shared::cta;");
+      asm volatile("tcgen05.wait::st.sync.aligned;");
+      asm volatile("tcgen05.fence::before_thread_sync;");
+      mbar_arrive(&sm.staged[s]);
+    }
+    // ---------------- epilogue: wait for the last MMA chunk, then read the accumulators
+    if (!is_stuck(sm) && total > 0) {
+      const int last = total - 1;
+      if (!mbar_wait(&sm.empty[last % kSlots], (last / kSlots) & 1)) atomicExch(&sm.stuck, 1);
+    }
+    asm volatile("tcgen05.fence::after_thread_sync;");
+    asm volatile("bar.sync 1, 128;");
+    if (!is_stuck(sm)) {
+      // FC1: up rows hand their values to the gate rows through slot 0's raw B-scale area
+      float (*xchg)[kTcTok] = reinterpret_cast<float (*)[kTcTok]>(base + kSSign);
+      const float sc2 = 2.0f * __ldg(a.scale_2 + e);         // 2: the halved e2m1 levels
+      const float sc2d = __ldg(a.scale_2 + e);
+      const int wrow = trow < 64 ? r0 + trow : r1 + trow - 64;
+      for (int c0 = 0; c0 < ncols; c0 += 16) {
+        float v[16], v2[16];
+        tmem_ld16(tmem + lane_q + kColD + c0, v);
+        if (do_delta) tmem_ld16(tmem + lane_q + kColD2 + c0, v2);
+        float acc[16 / kTcTerms];
 #pragma unroll
         for (int q = 0; q < 16 / kTcTerms; ++q) {
           const int tk = c0 / kTcTerms + q;
-          if (tk < ntok && sm.src_row[tk] >= 0) a.out[(size_t)sm.pair[tk] * a.H + wrow] = acc[q] * sm.wts[tk];
-        }
-      } else {
-        // up rows (threads 64..127) hand their values to the gate rows (threads 0..63)
-        if (tid >= 64) {
+          // delta columns count only for gated pairs (the B box also holds other pairs' rows)
+          const bool gated = do_delta && tk < kTcTok && sm.gate_f[tk] != 0.0f;
+          float sacc = 0.0f;
 #pragma unroll
-          for (int q = 0; q < 16 / kTcTerms; ++q) xchg[tid - 64][c0 / kTcTerms + q] = acc[q];
+          for (int t = 0; t < kTcTerms; ++t) {
+            const int col = q * kTcTerms + t;
+            float d = sc2 * v[col];
+            if (gated) d = fmaf(sc2d, v2[col], d);
+            sacc = fmaf(sm.gsc[c0 + col], d, sacc);
+          }
+          acc[q] = sacc;
         }
-        asm volatile("bar.sync 1, 128;");        // warps 0-3 only
-        if (tid < 64) {
+        if (!FC1) {
 #pragma unroll
           for (int q = 0; q < 16 / kTcTerms; ++q) {
             const int tk = c0 / kTcTerms + q;
-            if (tk < ntok && sm.src_row[tk] >= 0) {
-              const float gv = acc[q], uv = xchg[tid][tk];
-              a.out[(size_t)(pos0 + tk) * a.I + wrow] = gv / (1.0f + expf(-gv)) * uv;
+            if (tk < ntok && sm.src_row[tk] >= 0) a.out[(size_t)sm.pair[tk] * a.H + wrow] = acc[q] * sm.wts[tk];
+          }
+        } else {
+          if (trow >= 64) {
+#pragma unroll
+            for (int q = 0; q < 16 / kTcTerms; ++q) xchg[trow - 64][c0 / kTcTerms + q] = acc[q];
+          }
+          asm volatile("bar.sync 1, 128;");
+          if (trow < 64) {
+#pragma unroll
+            for (int q = 0; q < 16 / kTcTerms; ++q) {
+              const int tk = c0 / kTcTerms + q;
+              if (tk < ntok && sm.src_row[tk] >= 0) {
+                const float gv = acc[q], uv = xchg[trow][tk];
+                a.out[(size_t)(pos0 + tk) * a.I + wrow] = gv / (1.0f + expf(-gv)) * uv;
+              }
             }
           }
+          asm volatile("bar.sync 1, 128;");
         }
-        asm volatile("bar.sync 1, 128;");
       }
     }
   }
-  asm volatile("tcgen05.fence::before_thread_sync;");
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
+    // every MMA this CTA issued must be complete before TMEM is released
+    const int issued = sm.issued;
+    if (lane == 0 && is_stuck(sm) && issued > 0) {
+      const int last = issued - 1;
+      mbar_wait(&sm.empty[last % kSlots], (last / kSlots) & 1);
+    }
+    __syncwarp();
+    asm volatile("tcgen05.fence::after_thread_sync;");
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
   }
+  if (tid == 0 && is_stuck(sm)) record_error(MOET_ERR_TIMEOUT);
+}
+
+// ---------------------------------------------------------------- host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D row-major tensor of `rows` x `cols` elements; box = box_cols x box_rows.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* ptr, uint64_t rows, uint64_t cols,
+              uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || ptr == nullptr) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * esize};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <bool FC1>
-moet_status launch_fc_tc(const FcTcArgs& a, int row_tiles, int grid_y, cudaStream_t st) {
-  const size_t smem = 1024 + kOpRing * kOpBytes + kRawRing * kRawBytes + sizeof(TcSmem);
+moet_status launch_fc_tc(const FcTcArgs& a, const moet_planes* pl, const moet_nvfp4* dl, const uint8_t* cperm,
+                         const uint8_t* cnat, const uint8_t* sfb, int act_rows, int E, int row_tiles, int grid_y,
+                         cudaStream_t st) {
+  TmaMaps m;
+  std::memset(&m, 0, sizeof(m));
+  const uint32_t brows = (uint32_t)(act_rows * kTcTerms < kMaxN ? act_rows * kTcTerms : kMaxN);
+  const uint64_t rowsW = (uint64_t)E * a.N, K = (uint64_t)a.K;
+  bool ok = make_map(&m.sign, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, pl->sign, rowsW, K / 32, 8, 64, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+            make_map(&m.mag, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, pl->mag, rowsW, K / 32, 8, 64, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+            make_map(&m.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pl->s16, rowsW, K / 16, 16, 64, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+            make_map(&m.act, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, cperm, (uint64_t)act_rows * kTcTerms, K / 2, 128,
+                     brows, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_map(&m.actn, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, cnat, (uint64_t)act_rows * kTcTerms, K / 2, 128,
+                     brows, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_map(&m.sfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, sfb, (uint64_t)act_rows * kTcTerms, K / 16, 16,
+                     brows, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (ok && a.delta_slot != nullptr) {
+    const uint64_t rowsD = (uint64_t)a.n_slots * a.N;
+    ok = make_map(&m.dcodes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dl->codes, rowsD, K / 2, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_map(&m.ds4, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dl->s4, rowsD, K / 16, 16, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+  if (!ok) return MOET_ERR_CUDA;
+  FcTcArgs ab = a;
+  ab.brows = (int)brows;
+  const size_t smem = 1024 + kSlots * kSlotBytes + sizeof(TcSmem);
   auto kern = fc_tc_kernel<FC1>;
   MOET_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   {
     ProfScope ps(FC1 ? MOET_K_FC1 : MOET_K_FC2, st);
-    kern<<<dim3(row_tiles, grid_y), kFcThreads, smem, st>>>(a);
+    kern<<<dim3(row_tiles, grid_y), kWsThreads, smem, st>>>(ab, m);
   }
   MOET_CUDA_TRY(cudaGetLastError());
   return MOET_OK;
@@ -621,9 +615,10 @@ moet_status tc_forward(const TcForwardArgs& f, cudaStream_t st) {
   // FC1 input terms: one row per token
   {
     ProfScope ps(MOET_K_TERMS, st);
-    const dim3 grid(f.T, (f.H + kTermThreads - 1) / kTermThreads);
-    act_terms_kernel<true><<<grid, kTermThreads, 0, st>>>(f.H, f.x, f.buf.x_cperm, f.buf.x_cnat, f.buf.x_sf,
-                                                      f.buf.x_g);
+    // one row per bucketed pair (the pair's token), so a work item's rows are consecutive
+    const dim3 grid(pairs, (f.H + kTermThreads - 1) / kTermThreads);
+    act_terms_kernel<true><<<grid, kTermThreads, 0, st>>>(f.H, f.x, f.perm, f.k, f.buf.x_cperm, f.buf.x_cnat,
+                                                          f.buf.x_sf, f.buf.x_g);
   }
   MOET_CUDA_TRY(cudaGetLastError());
   FcTcArgs a{};
@@ -633,27 +628,27 @@ moet_status tc_forward(const TcForwardArgs& f, cudaStream_t st) {
   a.hdr = f.hdr; a.chunks = f.chunks;
   FcTcArgs a1 = a;
   a1.K = f.H; a1.N = 2 * f.I;
-  a1.sign = f.fc1->sign; a1.mag = f.fc1->mag; a1.s16 = f.fc1->s16; a1.scale_2 = f.fc1->scale_2;
-  if (f.delta_slot) { a1.dcodes = f.dfc1->codes; a1.ds4 = f.dfc1->s4; }
-  a1.cperm = f.buf.x_cperm; a1.cnat = f.buf.x_cnat; a1.sfb = f.buf.x_sf; a1.gsc = f.buf.x_g;
+  a1.scale_2 = f.fc1->scale_2;
+  a1.gsc = f.buf.x_g;
   a1.out = f.h;
-  moet_status s = launch_fc_tc<true>(a1, f.I / 64, f.max_items, st);
+  moet_status s = launch_fc_tc<true>(a1, f.fc1, f.dfc1, f.buf.x_cperm, f.buf.x_cnat, f.buf.x_sf, pairs, f.E,
+                                     f.I / 64, f.max_items, st);
   if (s != MOET_OK) return s;
   // FC2 input terms: one row per bucketed pair (h rows are in bucketed order)
   {
     ProfScope ps(MOET_K_TERMS, st);
     const dim3 grid(pairs, (f.I + kTermThreads - 1) / kTermThreads);
-    act_terms_kernel<false><<<grid, kTermThreads, 0, st>>>(f.I, f.h, f.buf.h_cperm, f.buf.h_cnat, f.buf.h_sf,
-                                                       f.buf.h_g);
+    act_terms_kernel<false><<<grid, kTermThreads, 0, st>>>(f.I, f.h, nullptr, 1, f.buf.h_cperm, f.buf.h_cnat,
+                                                           f.buf.h_sf, f.buf.h_g);
   }
   MOET_CUDA_TRY(cudaGetLastError());
   FcTcArgs a2 = a;
   a2.K = f.I; a2.N = f.H;
-  a2.sign = f.fc2->sign; a2.mag = f.fc2->mag; a2.s16 = f.fc2->s16; a2.scale_2 = f.fc2->scale_2;
-  if (f.delta_slot) { a2.dcodes = f.dfc2->codes; a2.ds4 = f.dfc2->s4; }
-  a2.cperm = f.buf.h_cperm; a2.cnat = f.buf.h_cnat; a2.sfb = f.buf.h_sf; a2.gsc = f.buf.h_g;
+  a2.scale_2 = f.fc2->scale_2;
+  a2.gsc = f.buf.h_g;
   a2.out = f.o;
-  return launch_fc_tc<false>(a2, f.H / 128, f.max_items, st);
+  return launch_fc_tc<false>(a2, f.fc2, f.dfc2, f.buf.h_cperm, f.buf.h_cnat, f.buf.h_sf, pairs, f.E, f.H / 128,
+                             f.max_items, st);
 }
 
 }  // namespace moet
