@@ -28,15 +28,15 @@
 // against a naturally ordered copy of the terms ("cnat") and accumulates in
 // a second TMEM region.
 //
-// Pipeline per CTA (6 warps, warp-specialised, no CTA-wide barrier in the K
+// Pipeline per CTA (10 warps, warp-specialised, no CTA-wide barrier in the K
 // loop): warp 0 (one thread) streams each 256-weight K chunk into one of
 // kSlots shared-memory slots with TMA (sign and magnitude planes, row scales,
-// the work item's 64 activation-term rows and their scales); warps 2-5 (one
-// thread per weight row = TMEM lane) expand the planes into the swizzled A
-// tile and write the scale factors to TMEM; warp 1 (one thread) issues the 4
-// MMAs (K = 64) per chunk and commits them to the slot's "empty" mbarrier.
-// Hand-offs: full (TMA bytes landed) -> staged (128 converter arrivals) ->
-// empty (MMA commit); every wait is bounded.
+// the work item's 64 activation-term rows and their scales); warps 2-9 (two
+// threads per weight row; rows = TMEM lanes) expand the planes into the
+// swizzled A tile and write the scale factors to TMEM; warp 1 (one thread)
+// issues the 4 MMAs (K = 64) per chunk and commits them to the slot's
+// "empty" mbarrier.  Hand-offs: full (TMA bytes landed) -> staged (256
+// converter arrivals) -> empty (MMA commit); every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -48,7 +48,8 @@
 namespace moet {
 namespace {
 
-constexpr int kWsThreads = 192;              // warp 0: TMA producer, warp 1: MMA, warps 2-5: converters
+constexpr int kWsThreads = 320;              // warp 0: TMA producer, warp 1: MMA, warps 2-9: converters
+constexpr int kConvThreads = 256;             // two converter threads per weight row
 constexpr int kSlots = 3;                     // K chunks in flight
 constexpr int kKC = 256;                      // weights per K chunk (one SW128 atom)
 constexpr int kMaxN = kTcTerms * kTcTok;      // 64 columns of D
@@ -148,9 +149,9 @@ __device__ __forceinline__ uint4 planes_to_e2m1(uint32_t S, uint32_t M) {
 }
 
 // ---------------------------------------------------------------- activation terms
-// Grid (rows, K / 256): each CTA of 256 threads reads its row once for the
-// row maximum m, then 16 threads expand one 16-element block (one element
-// each) into kTcTerms NVFP4 terms.  Term t has the fp32 scale
+// One CTA of 256 threads per output row: it reads the row once for the row
+// maximum m, then groups of 16 threads expand 16-element blocks (one element
+// per thread, striding over the row) into kTcTerms NVFP4 terms.  Term t has the fp32 scale
 // g_t = m / (6 * 448) / 4^t and a ue4m3 scale per block chosen from the
 // block's current residual, so each term quantises what the previous ones
 // left (a block's residual shrinks at least ~6x per term while g_t shrinks
@@ -195,16 +196,16 @@ __global__ void __launch_bounds__(kTermThreads) act_terms_kernel(int K, const vo
 #pragma unroll
   for (int w = 1; w < kTermThreads / 32; ++w) m = fmaxf(m, red[w]);
   const float g0 = m / (6.0f * 448.0f);
-  if (blockIdx.y == 0 && tid < kTcTerms) gsc[(size_t)row * kTcTerms + tid] = ldexpf(g0, -2 * tid);
-  const int idx = blockIdx.y * kTermThreads + tid;         // element index in the row
-  const int b = idx >> 4, j = idx & 15, lbase = lane & 16;
-  const bool live = idx < K;                                // K % 256 == 0: all live
-  float r = 0.0f;
-  if (live) r = BF16_IN ? __uint_as_float((uint32_t)__ldg(sb + idx) << 16) : sf32[idx];
+  if (tid < kTcTerms) gsc[(size_t)row * kTcTerms + tid] = ldexpf(g0, -2 * tid);
+  const int j = tid & 15, lbase = lane & 16;
   // the element whose code lands at permuted position p = 4 r + n is r + 4 n
   const int p0 = 2 * (j & 7), p1 = p0 + 1;
   const int src0 = (p0 >> 2) + 4 * (p0 & 3);
   const int src1 = (p1 >> 2) + 4 * (p1 & 3);
+  for (int idx = tid; idx < K; idx += kTermThreads) {        // K % 256 == 0
+  const int b = idx >> 4;
+  const bool live = true;
+  float r = BF16_IN ? __uint_as_float((uint32_t)__ldg(sb + idx) << 16) : sf32[idx];
 #pragma unroll
   for (int t = 0; t < kTcTerms; ++t) {
     const float g = ldexpf(g0, -2 * t);
@@ -235,11 +236,12 @@ __global__ void __launch_bounds__(kTermThreads) act_terms_kernel(int K, const vo
       if (j == 0) sfb[term_row * (K / 16) + b] = (uint8_t)sf;
     }
   }
+  }
 }
 
 // ---------------------------------------------------------------- FC kernel
 struct TmaMaps {
-  CUtensorMap sign, mag, q;        // planes u32 [E N, K/32] box {8, 64}; s16 u8 [E N, K/16] box {16, 64}
+  CUtensorMap sign, mag, q;        // planes u32 [E N, K/32] box {8, 64} SW32; s16 u8 [E N, K/16] box {16, 64}
   CUtensorMap act, actn, sfb;      // terms u8 [pairs 4, K/2] box {128, 64} SW128 (perm / natural); scales box {16, 64}
   CUtensorMap dcodes, ds4;         // delta u8 [S N, K/2] box {128, 64} SW128; scales box {16, 64}
 };
@@ -324,7 +326,7 @@ __global__ void __launch_bounds__(kWsThreads, 2) fc_tc_kernel(const FcTcArgs a, 
     sm.slot = slot;
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.staged[s], 128);
+      mbar_init(&sm.staged[s], kConvThreads);
       mbar_init(&sm.empty[s], 1);
     }
     asm volatile("fence.mbarrier_init.release.cluster;");
@@ -426,9 +428,17 @@ __global__ void __launch_bounds__(kWsThreads, 2) fc_tc_kernel(const FcTcArgs a, 
       sm.issued = cg;
     }
   } else {
-    // ---------------- converters: thread = tile row = TMEM lane
+    // ---------------- converters: two threads per tile row (= TMEM lane); half h
+    // expands weight words 4h..4h+3 of the chunk; half 0 writes the row scales to
+    // TMEM, half 1 the activation-term scales
+    const int half = (warp - 2) >> 2;
     const int trow = 32 * (warp & 3) + lane;
     const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;
+    // 32-byte-swizzled raw plane rows: 16-byte piece h of row r sits at piece h ^ ((r >> 2) & 1)
+    const int praw = trow * 32 + ((half ^ ((trow >> 2) & 1)) << 4);
+    int aoff[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) aoff[w] = kSA + trow * 128 + (((4 * half + w) ^ (trow & 7)) << 4);
     for (int cg = 0; cg < total; ++cg) {
       const int s = cg % kSlots, u = cg / kSlots;
       if (!mbar_wait(&sm.full[s], u & 1)) { atomicExch(&sm.stuck, 1); break; }
@@ -436,36 +446,31 @@ __global__ void __launch_bounds__(kWsThreads, 2) fc_tc_kernel(const FcTcArgs a, 
       const bool dp = cg >= nkc;
       unsigned char* sl = base + s * kSlotBytes;
       if (!dp) {
-        const uint4 s0 = *reinterpret_cast<const uint4*>(sl + kSSign + trow * 32);
-        const uint4 s1 = *reinterpret_cast<const uint4*>(sl + kSSign + trow * 32 + 16);
-        const uint4 m0 = *reinterpret_cast<const uint4*>(sl + kSMag + trow * 32);
-        const uint4 m1 = *reinterpret_cast<const uint4*>(sl + kSMag + trow * 32 + 16);
-        const uint32_t SW[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-        const uint32_t MW[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-        unsigned char* arow = sl + kSA + trow * 128;
-#pragma unroll
-        for (int w = 0; w < 8; ++w)
-          *reinterpret_cast<uint4*>(arow + ((w ^ (trow & 7)) << 4)) = planes_to_e2m1(SW[w], MW[w]);
+        const uint4 sw = *reinterpret_cast<const uint4*>(sl + kSSign + praw);
+        const uint4 mw = *reinterpret_cast<const uint4*>(sl + kSMag + praw);
+        *reinterpret_cast<uint4*>(sl + aoff[0]) = planes_to_e2m1(sw.x, mw.x);
+        *reinterpret_cast<uint4*>(sl + aoff[1]) = planes_to_e2m1(sw.y, mw.y);
+        *reinterpret_cast<uint4*>(sl + aoff[2]) = planes_to_e2m1(sw.z, mw.z);
+        *reinterpret_cast<uint4*>(sl + aoff[3]) = planes_to_e2m1(sw.w, mw.w);
       }
       // scale factors to TMEM, replicated layout: rows lane + 32 j -> columns 4 i + j
-      uint32_t va[16], vb[16];
+      uint32_t v[16];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const uint4 q = *reinterpret_cast<const uint4*>(sl + kSQ + (lane + 32 * j) * 16);
-        va[0 * 4 + j] = q.x; va[1 * 4 + j] = q.y; va[2 * 4 + j] = q.z; va[3 * 4 + j] = q.w;
         const int n = lane + 32 * j;
-        uint4 r = make_uint4(0u, 0u, 0u, 0u);
-        if (n < kMaxN) r = *reinterpret_cast<const uint4*>(sl + kSF + n * 16);
-        vb[0 * 4 + j] = r.x; vb[1 * 4 + j] = r.y; vb[2 * 4 + j] = r.z; vb[3 * 4 + j] = r.w;
+        uint4 q = make_uint4(0u, 0u, 0u, 0u);
+        if (half == 0) q = *reinterpret_cast<const uint4*>(sl + kSQ + n * 16);
+        else if (n < kMaxN) q = *reinterpret_cast<const uint4*>(sl + kSF + n * 16);
+        v[0 * 4 + j] = q.x; v[1 * 4 + j] = q.y; v[2 * 4 + j] = q.z; v[3 * 4 + j] = q.w;
       }
-      tmem_st16(tmem + lane_q + kColSFA + 16 * s, va);
-      tmem_st16(tmem + lane_q + kColSFB + 16 * s, vb);
+      tmem_st16(tmem + lane_q + (half ? kColSFB : kColSFA) + 16 * s, v);
       asm volatile("fence.proxy.async.shared::cta;");
       asm volatile("tcgen05.wait::st.sync.aligned;");
       asm volatile("tcgen05.fence::before_thread_sync;");
       mbar_arrive(&sm.staged[s]);
     }
-    // ---------------- epilogue: wait for the last MMA chunk, then read the accumulators
+    // ---------------- epilogue (warps 2-5): wait for the last MMA chunk, read the accumulators
+    if (half == 0) {
     if (!is_stuck(sm) && total > 0) {
       const int last = total - 1;
       if (!mbar_wait(&sm.empty[last % kSlots], (last / kSlots) & 1)) atomicExch(&sm.stuck, 1);
@@ -524,6 +529,7 @@ __global__ void __launch_bounds__(kWsThreads, 2) fc_tc_kernel(const FcTcArgs a, 
         }
       }
     }
+    }
   }
   __syncthreads();
   if (warp == 1) {
@@ -580,8 +586,8 @@ moet_status launch_fc_tc(const FcTcArgs& a, const moet_planes* pl, const moet_nv
   std::memset(&m, 0, sizeof(m));
   const uint32_t brows = (uint32_t)(act_rows * kTcTerms < kMaxN ? act_rows * kTcTerms : kMaxN);
   const uint64_t rowsW = (uint64_t)E * a.N, K = (uint64_t)a.K;
-  bool ok = make_map(&m.sign, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, pl->sign, rowsW, K / 32, 8, 64, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-            make_map(&m.mag, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, pl->mag, rowsW, K / 32, 8, 64, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+  bool ok = make_map(&m.sign, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, pl->sign, rowsW, K / 32, 8, 64, CU_TENSOR_MAP_SWIZZLE_32B) &&
+            make_map(&m.mag, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, pl->mag, rowsW, K / 32, 8, 64, CU_TENSOR_MAP_SWIZZLE_32B) &&
             make_map(&m.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pl->s16, rowsW, K / 16, 16, 64, CU_TENSOR_MAP_SWIZZLE_NONE) &&
             make_map(&m.act, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, cperm, (uint64_t)act_rows * kTcTerms, K / 2, 128,
                      brows, CU_TENSOR_MAP_SWIZZLE_128B) &&
@@ -616,8 +622,7 @@ moet_status tc_forward(const TcForwardArgs& f, cudaStream_t st) {
   {
     ProfScope ps(MOET_K_TERMS, st);
     // one row per bucketed pair (the pair's token), so a work item's rows are consecutive
-    const dim3 grid(pairs, (f.H + kTermThreads - 1) / kTermThreads);
-    act_terms_kernel<true><<<grid, kTermThreads, 0, st>>>(f.H, f.x, f.perm, f.k, f.buf.x_cperm, f.buf.x_cnat,
+    act_terms_kernel<true><<<pairs, kTermThreads, 0, st>>>(f.H, f.x, f.perm, f.k, f.buf.x_cperm, f.buf.x_cnat,
                                                           f.buf.x_sf, f.buf.x_g);
   }
   MOET_CUDA_TRY(cudaGetLastError());
@@ -637,8 +642,7 @@ moet_status tc_forward(const TcForwardArgs& f, cudaStream_t st) {
   // FC2 input terms: one row per bucketed pair (h rows are in bucketed order)
   {
     ProfScope ps(MOET_K_TERMS, st);
-    const dim3 grid(pairs, (f.I + kTermThreads - 1) / kTermThreads);
-    act_terms_kernel<false><<<grid, kTermThreads, 0, st>>>(f.I, f.h, nullptr, 1, f.buf.h_cperm, f.buf.h_cnat,
+    act_terms_kernel<false><<<pairs, kTermThreads, 0, st>>>(f.I, f.h, nullptr, 1, f.buf.h_cperm, f.buf.h_cnat,
                                                            f.buf.h_sf, f.buf.h_g);
   }
   MOET_CUDA_TRY(cudaGetLastError());
