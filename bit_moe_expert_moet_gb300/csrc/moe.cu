@@ -42,7 +42,7 @@ constexpr int kSmemBudget = 96 * 1024;
 constexpr uint32_t kCodeLut = 0xC242BC3Cu;  // f16 high bytes of +1, -1, +3, -3
 
 struct WsLayout {
-  size_t hdr, tok_scale, hmax, chunks, h, o, xt, ht, total;
+  size_t hdr, tok_scale, tok_max, hmax, chunks, h, o, xt, ht, total;
 };
 
 // Largest T routed through the tcgen05 engine (small tokens-per-expert regime).
@@ -61,6 +61,7 @@ inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   size_t off = 0;
   L.hdr = off;       off += align256(16);
   L.tok_scale = off; off += align256(sizeof(float) * T);
+  L.tok_max = off;   off += align256(sizeof(float) * T);
   L.hmax = off;      off += align256(sizeof(unsigned) * pairs);
   L.chunks = off;    off += align256(sizeof(int4) * (size_t)max_chunks(T, E, k, kTcTok));
   L.h = off;         off += align256(sizeof(float) * pairs * I);
@@ -87,8 +88,8 @@ __device__ __forceinline__ float pow2_scale_for(float amax) {
 // ---------------------------------------------------------------- prologue
 __global__ void __launch_bounds__(kThreads) prologue_kernel(
     int T, int H, int E, int k, int chunk, const uint16_t* __restrict__ x, const int32_t* __restrict__ offsets,
-    int* __restrict__ hdr, float* __restrict__ tok_scale, unsigned* __restrict__ hmax,
-    int4* __restrict__ chunks) {
+    int* __restrict__ hdr, float* __restrict__ tok_scale, float* __restrict__ tok_max,
+    unsigned* __restrict__ hmax, int4* __restrict__ chunks) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (blockIdx.x == 0) {
     if (warp != 0) return;
@@ -141,7 +142,10 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if (lane == 0) tok_scale[gw] = pow2_scale_for(m);
+  if (lane == 0) {
+    tok_scale[gw] = pow2_scale_for(m);
+    tok_max[gw] = m;
+  }
 }
 
 // ---------------------------------------------------------------- fc kernels
@@ -516,6 +520,7 @@ extern "C" moet_status moet_moe_forward(int T, int H, int I, int E, int k, const
   char* ws = static_cast<char*>(workspace);
   int* hdr = reinterpret_cast<int*>(ws + L.hdr);
   float* tok_scale = reinterpret_cast<float*>(ws + L.tok_scale);
+  float* tok_max = reinterpret_cast<float*>(ws + L.tok_max);
   unsigned* hmax = reinterpret_cast<unsigned*>(ws + L.hmax);
   int4* chunks = reinterpret_cast<int4*>(ws + L.chunks);
   float* h = reinterpret_cast<float*>(ws + L.h);
@@ -526,7 +531,7 @@ extern "C" moet_status moet_moe_forward(int T, int H, int I, int E, int k, const
   {
     ProfScope ps(MOET_K_PROLOGUE, st);
     prologue_kernel<<<1 + (T + 7) / 8, kThreads, 0, st>>>(T, H, E, k, chunk, x, expert_offsets, hdr,
-                                                           tok_scale, hmax, chunks);
+                                                           tok_scale, tok_max, hmax, chunks);
   }
   MOET_CUDA_TRY(cudaGetLastError());
 
@@ -540,6 +545,7 @@ extern "C" moet_status moet_moe_forward(int T, int H, int I, int E, int k, const
     f.n_slots = n_slots; f.dfc1 = dfc1; f.dfc2 = dfc2;
     f.gate = with_delta ? gate_mask : nullptr;
     f.hdr = hdr; f.chunks = chunks; f.h = h; f.o = o; f.max_items = mc;
+    f.tokmax = tok_max; f.hmax = hmax;
     const size_t pairs = (size_t)T * k;
     auto carve = [](char* base, size_t rows, size_t K, uint8_t** cperm, uint8_t** cnat, uint8_t** sf, float** g) {
       size_t off = 0;

@@ -149,63 +149,37 @@ __device__ __forceinline__ uint4 planes_to_e2m1(uint32_t S, uint32_t M) {
 }
 
 // ---------------------------------------------------------------- activation terms
-// One CTA of 256 threads per output row: it reads the row once for the row
-// maximum m, then groups of 16 threads expand 16-element blocks (one element
-// per thread, striding over the row) into kTcTerms NVFP4 terms.  Term t has the fp32 scale
-// g_t = m / (6 * 448) / 4^t and a ue4m3 scale per block chosen from the
-// block's current residual, so each term quantises what the previous ones
-// left (a block's residual shrinks at least ~6x per term while g_t shrinks
-// 4x, keeping the block scales in the normal e4m3 range).  Outputs per
-// (row, term): codes in permuted and natural K order, one ue4m3 scale per
+// Grid (rows, K / 256), 256 threads: 16 threads expand one 16-element block
+// (one element each) into kTcTerms NVFP4 terms.  Term t has the fp32 scale
+// g_t = m / (6 * 448) / 4^t, m = the row maximum (given: per token for FC1,
+// per pair from FC1's epilogue for FC2), and a ue4m3 scale per block chosen
+// from the block's current residual, so each term quantises what the previous
+// ones left (a block's residual shrinks at least ~6x per term while g_t
+// shrinks 4x, keeping the block scales in the normal e4m3 range).  Outputs
+// per (row, term): codes in permuted and natural K order, one ue4m3 scale per
 // 16 elements, and g_t.
 constexpr int kTermThreads = 256;
 
 template <bool BF16_IN>
 __global__ void __launch_bounds__(kTermThreads) act_terms_kernel(int K, const void* __restrict__ src,
                                                                 const int32_t* __restrict__ row_map, int map_div,
+                                                                const float* __restrict__ rowmax,
                                                                 uint8_t* __restrict__ cperm, uint8_t* __restrict__ cnat,
                                                                 uint8_t* __restrict__ sfb, float* __restrict__ gsc) {
-  __shared__ float red[kTermThreads / 32];
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
   // output row `row` expands source row row_map[row] / map_div (or `row` itself)
   const size_t srow = row_map ? (size_t)(__ldg(row_map + row) / map_div) : (size_t)row;
-  const uint16_t* sb = static_cast<const uint16_t*>(src) + srow * K;
-  const float* sf32 = static_cast<const float*>(src) + srow * K;
-  float m = 0.0f;
-  if (BF16_IN) {
-    const uint4* p = reinterpret_cast<const uint4*>(sb);
-    for (int i = tid; i < K / 8; i += kTermThreads) {
-      const uint4 v = __ldg(p + i);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[q] << 16)), fabsf(__uint_as_float(w[q] & 0xFFFF0000u))));
-    }
-  } else {
-    const float4* p = reinterpret_cast<const float4*>(sf32);
-    for (int i = tid; i < K / 4; i += kTermThreads) {
-      const float4 v = p[i];
-      m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if (lane == 0) red[tid >> 5] = m;
-  __syncthreads();
-  m = red[0];
-#pragma unroll
-  for (int w = 1; w < kTermThreads / 32; ++w) m = fmaxf(m, red[w]);
+  const float m = __ldg(rowmax + srow);
   const float g0 = m / (6.0f * 448.0f);
-  if (tid < kTcTerms) gsc[(size_t)row * kTcTerms + tid] = ldexpf(g0, -2 * tid);
-  const int j = tid & 15, lbase = lane & 16;
+  if (blockIdx.y == 0 && tid < kTcTerms) gsc[(size_t)row * kTcTerms + tid] = ldexpf(g0, -2 * tid);
+  const int idx = blockIdx.y * kTermThreads + tid;          // element of the row (K % 256 == 0)
+  const int b = idx >> 4, j = idx & 15, lbase = lane & 16;
+  float r = BF16_IN ? __uint_as_float((uint32_t)__ldg(static_cast<const uint16_t*>(src) + srow * K + idx) << 16)
+                    : static_cast<const float*>(src)[srow * K + idx];
   // the element whose code lands at permuted position p = 4 r + n is r + 4 n
   const int p0 = 2 * (j & 7), p1 = p0 + 1;
   const int src0 = (p0 >> 2) + 4 * (p0 & 3);
   const int src1 = (p1 >> 2) + 4 * (p1 & 3);
-  for (int idx = tid; idx < K; idx += kTermThreads) {        // K % 256 == 0
-  const int b = idx >> 4;
-  const bool live = true;
-  float r = BF16_IN ? __uint_as_float((uint32_t)__ldg(sb + idx) << 16) : sf32[idx];
 #pragma unroll
   for (int t = 0; t < kTcTerms; ++t) {
     const float g = ldexpf(g0, -2 * t);
@@ -229,26 +203,23 @@ __global__ void __launch_bounds__(kTermThreads) act_terms_kernel(int K, const vo
     const uint32_t nat_hi = __shfl_down_sync(0xffffffffu, code, 1);
     const uint32_t per_lo = __shfl_sync(0xffffffffu, code, lbase + src0);
     const uint32_t per_hi = __shfl_sync(0xffffffffu, code, lbase + src1);
-    if (live) {
-      const size_t term_row = (size_t)row * kTcTerms + t;
-      if ((j & 1) == 0) cnat[term_row * (K / 2) + 8 * b + (j >> 1)] = (uint8_t)(code | (nat_hi << 4));
-      if (j < 8) cperm[term_row * (K / 2) + 8 * b + j] = (uint8_t)(per_lo | (per_hi << 4));
-      if (j == 0) sfb[term_row * (K / 16) + b] = (uint8_t)sf;
-    }
-  }
+    const size_t term_row = (size_t)row * kTcTerms + t;
+    if ((j & 1) == 0) cnat[term_row * (K / 2) + 8 * b + (j >> 1)] = (uint8_t)(code | (nat_hi << 4));
+    if (j < 8) cperm[term_row * (K / 2) + 8 * b + j] = (uint8_t)(per_lo | (per_hi << 4));
+    if (j == 0) sfb[term_row * (K / 16) + b] = (uint8_t)sf;
   }
 }
 
 // ---------------------------------------------------------------- FC kernel
 struct TmaMaps {
   CUtensorMap sign, mag, q;        // planes u32 [E N, K/32] box {8, 64} SW32; s16 u8 [E N, K/16] box {16, 64}
-  CUtensorMap act, actn, sfb;      // terms u8 [pairs 4, K/2] box {128, 64} SW128 (perm / natural); scales box {16, 64}
+  CUtensorMap act, actn, sfb;      // terms u8 [pairs 4, K/2] box {128, 16} SW128 (perm / natural); scales box {16, 16}
   CUtensorMap dcodes, ds4;         // delta u8 [S N, K/2] box {128, 64} SW128; scales box {16, 64}
 };
 
 struct FcTcArgs {
   int T, H, I, k, K, N;          // N = rows of one expert matrix
-  int brows;                     // rows of the activation-term box: min(64, 4 * term rows)
+  int brows;                     // rows of one activation-term box: min(16, 4 * term rows)
   const int32_t* offsets;
   const int32_t* perm;
   const float* topk_w;
@@ -260,6 +231,7 @@ struct FcTcArgs {
   const int4* chunks;
   const float* gsc;
   float* out;
+  unsigned* hmax;                // FC1: max |h| per bucketed pair (fp32 bits), for the FC2 terms
 };
 
 struct TcSmem {
@@ -382,7 +354,8 @@ __global__ void __launch_bounds__(kWsThreads, 2) fc_tc_kernel(const FcTcArgs a, 
         const bool dp = cg >= nkc;
         const int c = dp ? cg - nkc : cg;
         unsigned char* sl = base + s * kSlotBytes;
-        const uint32_t bytes = (dp ? 16384u + 2048u : 4096u + 4096u + 2048u) + (uint32_t)a.brows * (128u + 16u);
+        const int nbox = (ncols + 15) / 16;         // 16-row boxes of activation terms
+        const uint32_t bytes = (dp ? 16384u + 2048u : 4096u + 4096u + 2048u) + (uint32_t)(nbox * a.brows) * (128u + 16u);
         mbar_expect_tx(&sm.full[s], bytes);
         if (!dp) {
           const int y0 = e * a.N + r0, y1 = e * a.N + r1;
@@ -399,9 +372,12 @@ __global__ void __launch_bounds__(kWsThreads, 2) fc_tc_kernel(const FcTcArgs a, 
           tma_load_2d(smem_addr(sl + kSQ), &maps.ds4, c * 16, y0, &sm.full[s]);
           tma_load_2d(smem_addr(sl + kSQ + 1024), &maps.ds4, c * 16, y1, &sm.full[s]);
         }
-        // the work item's pairs are consecutive bucketed rows: one 64-row box of terms
-        tma_load_2d(smem_addr(sl + kSB), dp ? &maps.actn : &maps.act, c * 128, pos0 * kTcTerms, &sm.full[s]);
-        tma_load_2d(smem_addr(sl + kSF), &maps.sfb, c * 16, pos0 * kTcTerms, &sm.full[s]);
+        // the work item's pairs are consecutive bucketed rows: ncols / 16 boxes of 16 term rows
+        for (int bx = 0; bx < nbox; ++bx) {
+          tma_load_2d(smem_addr(sl + kSB + bx * 2048), dp ? &maps.actn : &maps.act, c * 128, pos0 * kTcTerms + 16 * bx,
+                      &sm.full[s]);
+          tma_load_2d(smem_addr(sl + kSF + bx * 256), &maps.sfb, c * 16, pos0 * kTcTerms + 16 * bx, &sm.full[s]);
+        }
       }
     }
   } else if (warp == 1) {
@@ -460,7 +436,7 @@ __global__ void __launch_bounds__(kWsThreads, 2) fc_tc_kernel(const FcTcArgs a, 
         const int n = lane + 32 * j;
         uint4 q = make_uint4(0u, 0u, 0u, 0u);
         if (half == 0) q = *reinterpret_cast<const uint4*>(sl + kSQ + n * 16);
-        else if (n < kMaxN) q = *reinterpret_cast<const uint4*>(sl + kSF + n * 16);
+        else if (n < ncols) q = *reinterpret_cast<const uint4*>(sl + kSF + n * 16);
         v[0 * 4 + j] = q.x; v[1 * 4 + j] = q.y; v[2 * 4 + j] = q.z; v[3 * 4 + j] = q.w;
       }
       tmem_st16(tmem + lane_q + (half ? kColSFB : kColSFA) + 16 * s, v);
@@ -519,10 +495,16 @@ __global__ void __launch_bounds__(kWsThreads, 2) fc_tc_kernel(const FcTcArgs a, 
 #pragma unroll
             for (int q = 0; q < 16 / kTcTerms; ++q) {
               const int tk = c0 / kTcTerms + q;
+              float hv = 0.0f;
               if (tk < ntok && sm.src_row[tk] >= 0) {
                 const float gv = acc[q], uv = xchg[trow][tk];
-                a.out[(size_t)(pos0 + tk) * a.I + wrow] = gv / (1.0f + expf(-gv)) * uv;
+                hv = gv / (1.0f + expf(-gv)) * uv;
+                a.out[(size_t)(pos0 + tk) * a.I + wrow] = hv;
               }
+              float mx = fabsf(hv);
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+              if (lane == 0 && tk < ntok && sm.src_row[tk] >= 0) atomicMax(a.hmax + pos0 + tk, __float_as_uint(mx));
             }
           }
           asm volatile("bar.sync 1, 128;");
@@ -584,7 +566,7 @@ moet_status launch_fc_tc(const FcTcArgs& a, const moet_planes* pl, const moet_nv
                          cudaStream_t st) {
   TmaMaps m;
   std::memset(&m, 0, sizeof(m));
-  const uint32_t brows = (uint32_t)(act_rows * kTcTerms < kMaxN ? act_rows * kTcTerms : kMaxN);
+  const uint32_t brows = (uint32_t)(act_rows * kTcTerms < 16 ? act_rows * kTcTerms : 16);
   const uint64_t rowsW = (uint64_t)E * a.N, K = (uint64_t)a.K;
   bool ok = make_map(&m.sign, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, pl->sign, rowsW, K / 32, 8, 64, CU_TENSOR_MAP_SWIZZLE_32B) &&
             make_map(&m.mag, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, pl->mag, rowsW, K / 32, 8, 64, CU_TENSOR_MAP_SWIZZLE_32B) &&
@@ -622,8 +604,9 @@ moet_status tc_forward(const TcForwardArgs& f, cudaStream_t st) {
   {
     ProfScope ps(MOET_K_TERMS, st);
     // one row per bucketed pair (the pair's token), so a work item's rows are consecutive
-    act_terms_kernel<true><<<pairs, kTermThreads, 0, st>>>(f.H, f.x, f.perm, f.k, f.buf.x_cperm, f.buf.x_cnat,
-                                                          f.buf.x_sf, f.buf.x_g);
+    const dim3 grid(pairs, f.H / kTermThreads);
+    act_terms_kernel<true><<<grid, kTermThreads, 0, st>>>(f.H, f.x, f.perm, f.k, f.tokmax, f.buf.x_cperm,
+                                                          f.buf.x_cnat, f.buf.x_sf, f.buf.x_g);
   }
   MOET_CUDA_TRY(cudaGetLastError());
   FcTcArgs a{};
@@ -636,14 +619,17 @@ moet_status tc_forward(const TcForwardArgs& f, cudaStream_t st) {
   a1.scale_2 = f.fc1->scale_2;
   a1.gsc = f.buf.x_g;
   a1.out = f.h;
+  a1.hmax = f.hmax;
   moet_status s = launch_fc_tc<true>(a1, f.fc1, f.dfc1, f.buf.x_cperm, f.buf.x_cnat, f.buf.x_sf, pairs, f.E,
                                      f.I / 64, f.max_items, st);
   if (s != MOET_OK) return s;
   // FC2 input terms: one row per bucketed pair (h rows are in bucketed order)
   {
     ProfScope ps(MOET_K_TERMS, st);
-    act_terms_kernel<false><<<pairs, kTermThreads, 0, st>>>(f.I, f.h, nullptr, 1, f.buf.h_cperm, f.buf.h_cnat,
-                                                           f.buf.h_sf, f.buf.h_g);
+    const dim3 grid(pairs, f.I / kTermThreads);
+    act_terms_kernel<false><<<grid, kTermThreads, 0, st>>>(f.I, f.h, nullptr, 1,
+                                                           reinterpret_cast<const float*>(f.hmax), f.buf.h_cperm,
+                                                           f.buf.h_cnat, f.buf.h_sf, f.buf.h_g);
   }
   MOET_CUDA_TRY(cudaGetLastError());
   FcTcArgs a2 = a;

@@ -43,6 +43,8 @@ struct TcForwardArgs {
   const int4* chunks;          // (expert, first pair, count <= kTcTok)
   float* h;                    // [T k, I] bucketed
   float* o;                    // [T k, H] pair order
+  const float* tokmax;         // [T] max |x_t| (written by the prologue)
+  unsigned* hmax;              // [T k] max |h| per bucketed pair, zeroed by the prologue
   TcBuffers buf;
   int max_items;
 };
