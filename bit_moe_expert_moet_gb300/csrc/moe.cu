@@ -42,7 +42,7 @@ constexpr int kSmemBudget = 96 * 1024;
 constexpr uint32_t kCodeLut = 0xC242BC3Cu;  // f16 high bytes of +1, -1, +3, -3
 
 struct WsLayout {
-  size_t hdr, tok_scale, tok_max, hmax, chunks, h, o, xt, ht, total;
+  size_t hdr, tok_scale, tok_max, hmax, inv, chunks, h, o, xt, ht, total;
 };
 
 // Largest T routed through the tcgen05 engine (small tokens-per-expert regime).
@@ -63,6 +63,7 @@ inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   L.tok_scale = off; off += align256(sizeof(float) * T);
   L.tok_max = off;   off += align256(sizeof(float) * T);
   L.hmax = off;      off += align256(sizeof(unsigned) * pairs);
+  L.inv = off;       off += align256(sizeof(int32_t) * pairs);
   L.chunks = off;    off += align256(sizeof(int4) * (size_t)max_chunks(T, E, k, kTcTok));
   L.h = off;         off += align256(sizeof(float) * pairs * I);
   L.o = off;         off += align256(sizeof(float) * pairs * H);
@@ -88,8 +89,8 @@ __device__ __forceinline__ float pow2_scale_for(float amax) {
 // ---------------------------------------------------------------- prologue
 __global__ void __launch_bounds__(kThreads) prologue_kernel(
     int T, int H, int E, int k, int chunk, const uint16_t* __restrict__ x, const int32_t* __restrict__ offsets,
-    int* __restrict__ hdr, float* __restrict__ tok_scale, float* __restrict__ tok_max,
-    unsigned* __restrict__ hmax, int4* __restrict__ chunks) {
+    const int32_t* __restrict__ perm, int* __restrict__ hdr, float* __restrict__ tok_scale,
+    float* __restrict__ tok_max, unsigned* __restrict__ hmax, int32_t* __restrict__ inv, int4* __restrict__ chunks) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (blockIdx.x == 0) {
     if (warp != 0) return;
@@ -124,10 +125,17 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(
     }
     return;
   }
-  // blocks >= 1: one warp per token, plus zeroing of hmax
+  // blocks >= 1: one warp per token, zeroing of hmax and (when asked) the
+  // inverse of the bucketing permutation, pair -> bucketed position
   const int gw = (blockIdx.x - 1) * (kThreads / 32) + warp;
   const int nthreads = (gridDim.x - 1) * kThreads;
-  for (int i = (blockIdx.x - 1) * kThreads + tid; i < T * k; i += nthreads) hmax[i] = 0u;
+  for (int i = (blockIdx.x - 1) * kThreads + tid; i < T * k; i += nthreads) {
+    hmax[i] = 0u;
+    if (inv != nullptr) {
+      const int p = __ldg(perm + i);
+      if (p >= 0 && p < T * k) inv[p] = i;
+    }
+  }
   if (gw >= T) return;
   const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)gw * H);
   float m = 0.0f;
@@ -522,6 +530,7 @@ extern "C" moet_status moet_moe_forward(int T, int H, int I, int E, int k, const
   float* tok_scale = reinterpret_cast<float*>(ws + L.tok_scale);
   float* tok_max = reinterpret_cast<float*>(ws + L.tok_max);
   unsigned* hmax = reinterpret_cast<unsigned*>(ws + L.hmax);
+  int32_t* inv = reinterpret_cast<int32_t*>(ws + L.inv);
   int4* chunks = reinterpret_cast<int4*>(ws + L.chunks);
   float* h = reinterpret_cast<float*>(ws + L.h);
   float* o = reinterpret_cast<float*>(ws + L.o);
@@ -530,8 +539,9 @@ extern "C" moet_status moet_moe_forward(int T, int H, int I, int E, int k, const
   const int chunk = use_tc ? kTcTok : kChunk;
   {
     ProfScope ps(MOET_K_PROLOGUE, st);
-    prologue_kernel<<<1 + (T + 7) / 8, kThreads, 0, st>>>(T, H, E, k, chunk, x, expert_offsets, hdr,
-                                                           tok_scale, tok_max, hmax, chunks);
+    prologue_kernel<<<1 + (T + 7) / 8, kThreads, 0, st>>>(T, H, E, k, chunk, x, expert_offsets, perm, hdr,
+                                                           tok_scale, tok_max, hmax, use_tc ? inv : nullptr,
+                                                           chunks);
   }
   MOET_CUDA_TRY(cudaGetLastError());
 
@@ -545,7 +555,7 @@ extern "C" moet_status moet_moe_forward(int T, int H, int I, int E, int k, const
     f.n_slots = n_slots; f.dfc1 = dfc1; f.dfc2 = dfc2;
     f.gate = with_delta ? gate_mask : nullptr;
     f.hdr = hdr; f.chunks = chunks; f.h = h; f.o = o; f.max_items = mc;
-    f.tokmax = tok_max; f.hmax = hmax;
+    f.tokmax = tok_max; f.hmax = hmax; f.inv = inv;
     const size_t pairs = (size_t)T * k;
     auto carve = [](char* base, size_t rows, size_t K, uint8_t** cperm, uint8_t** cnat, uint8_t** sf, float** g) {
       size_t off = 0;

@@ -28,15 +28,18 @@
 // against a naturally ordered copy of the terms ("cnat") and accumulates in
 // a second TMEM region.
 //
-// Pipeline per CTA (10 warps, warp-specialised, no CTA-wide barrier in the K
-// loop): warp 0 (one thread) streams each 256-weight K chunk into one of
-// kSlots shared-memory slots with TMA (sign and magnitude planes, row scales,
-// the work item's 64 activation-term rows and their scales); warps 2-9 (two
-// threads per weight row; rows = TMEM lanes) expand the planes into the
-// swizzled A tile and write the scale factors to TMEM; warp 1 (one thread)
-// issues the 4 MMAs (K = 64) per chunk and commits them to the slot's
-// "empty" mbarrier.  Hand-offs: full (TMA bytes landed) -> staged (256
-// converter arrivals) -> empty (MMA commit); every wait is bounded.
+// Pipeline: a persistent CTA per SM (16 warps, warp-specialised, no CTA-wide
+// barrier in the loop) walks (work item, 128-row weight tile) units.  One
+// thread streams each unit's K chunks into a ring of raw shared-memory stages
+// with TMA (sign and magnitude planes, row scales, the item's activation-term
+// rows and their scales); converter warps expand the planes into a ring of
+// swizzled A stages and write the scale factors to TMEM; one thread issues the
+// MMAs (K = 64 each) and commits them to the stages' "empty" barriers and, at
+// the end of a unit, to one of two TMEM accumulator buffers that the epilogue
+// warps drain while the next unit accumulates.  A scheduler warp prepares
+// each unit's record (pairs, routing weights, gate flags, term scales) ahead
+// of use.  Every wait is bounded; a stuck CTA records an error, waits for its
+// copies and MMAs in flight and releases TMEM.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -48,18 +51,25 @@
 namespace moet {
 namespace {
 
-constexpr int kWsThreads = 320;              // warp 0: TMA producer, warp 1: MMA, warps 2-9: converters
-constexpr int kConvThreads = 256;             // two converter threads per weight row
-constexpr int kSlots = 3;                     // K chunks in flight
+constexpr int kWsThreads = 768;              // 24 warps, roles in fc_tc_kernel
+constexpr int kConvGroups = 2;                // converter groups, taking K chunks in turn
+constexpr int kConvWarps = 8;                 // per group: two converter warps per 32-row quarter
+constexpr int kRaw = 10;                      // raw TMA stages in flight
+constexpr int kAst = 4;                       // expanded-A stages (in TMEM)
+constexpr int kMeta = 4;                      // unit records in flight
 constexpr int kKC = 256;                      // weights per K chunk (one SW128 atom)
 constexpr int kMaxN = kTcTerms * kTcTok;      // 64 columns of D
-constexpr int kTmemCols = 256;
-constexpr int kColD = 0, kColD2 = 64, kColSFA = 128, kColSFB = 128 + 16 * kSlots;
-// slot layout (1024-aligned): A operand (128 rows x 128 B, SW128), B operand (64 rows x 128 B,
-// SW128), raw sign and magnitude planes [128 rows][32 B], raw row scales [128][16 B], raw B-term
-// scales [64 rows][16 B]
-constexpr int kSA = 0, kSB = 16384, kSSign = 24576, kSMag = 28672, kSQ = 32768, kSF = 34816;
-constexpr int kSlotBytes = 36864;
+constexpr int kTmemCols = 512;
+// TMEM columns: accumulator buffer b holds D at 128 b and the delta's D2 at 128 b + 64;
+// A stage s (128 rows x 256 e2m1 = 32 columns) at kColA + 32 s; scale factors per A stage
+// at kColSFA + 16 s (weights) and kColSFB + 16 s (activations)
+constexpr int kColA = 256, kColSFA = kColA + 32 * kAst, kColSFB = kColSFA + 16 * kAst;
+static_assert(kColSFB + 16 * kAst <= kTmemCols, "TMEM columns");
+// raw stage (1024-aligned): sign and magnitude planes [128 rows][32 B] (SW32), row scales
+// [128][16 B]; a delta half chunk puts its codes [128][64 B] (SW64) over the planes and its
+// scales over the row scales.  Then the activation terms [<= 64 rows][128 B] (SW128; natural
+// order [64 B] SW64 for delta half chunks) and their scales [<= 64][16 B].
+constexpr int kRSign = 0, kRMag = 4096, kRQ = 8192, kRB = 10240, kRSF = 18432, kRawBytes = 19456;
 constexpr long long kWaitLimit = 1LL << 22;   // polls before a wait is declared stuck
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -73,6 +83,16 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   d |= (uint64_t)(1024 >> 4) << 32;       // stride byte offset
   d |= (uint64_t)1 << 46;                 // descriptor version
   d |= (uint64_t)2 << 61;                 // 128-byte swizzle
+  return d;
+}
+
+// SW64 K-major descriptor: 8-row groups 512 B apart.
+__device__ __forceinline__ uint64_t sw64_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(512 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)4 << 61;                 // 64-byte swizzle
   return d;
 }
 
@@ -105,6 +125,15 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t ad, uint64_t bd, uin
       "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n"
       "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p; }"
       ::"r"(d), "l"(ad), "l"(bd), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc));
+}
+
+// Same MMA with the A operand in TMEM (row = lane, K along the columns, 8 e2m1 per column).
+__device__ __forceinline__ void tc_mma_ta(uint32_t d, uint32_t a_tmem, uint64_t bd, uint32_t idesc, uint32_t sfa,
+                                          uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], [%1], %2, %3, [%4], [%5], p; }"
+      ::"r"(d), "r"(a_tmem), "l"(bd), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc));
 }
 
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
@@ -149,29 +178,40 @@ __device__ __forceinline__ uint4 planes_to_e2m1(uint32_t S, uint32_t M) {
 }
 
 // ---------------------------------------------------------------- activation terms
-// Grid (rows, K / 256), 256 threads: 16 threads expand one 16-element block
-// (one element each) into kTcTerms NVFP4 terms.  Term t has the fp32 scale
-// g_t = m / (6 * 448) / 4^t, m = the row maximum (given: per token for FC1,
-// per pair from FC1's epilogue for FC2), and a ue4m3 scale per block chosen
-// from the block's current residual, so each term quantises what the previous
-// ones left (a block's residual shrinks at least ~6x per term while g_t
-// shrinks 4x, keeping the block scales in the normal e4m3 range).  Outputs
-// per (row, term): codes in permuted and natural K order, one ue4m3 scale per
-// 16 elements, and g_t.
+// Grid (source rows, K / 256), 256 threads: 16 threads expand one 16-element
+// block (one element each) into kTcTerms NVFP4 terms.  Term t has the fp32
+// scale g_t = m / (6 * 448) / 4^t, m = the row maximum (given: per token for
+// FC1, per pair from FC1's epilogue for FC2), and a ue4m3 scale per block
+// chosen from the block's current residual, so each term quantises what the
+// previous ones left (a block's residual shrinks at least ~6x per term while
+// g_t shrinks 4x, keeping the block scales in the normal e4m3 range).  Outputs
+// per (output row, term): codes in permuted and natural K order, one ue4m3
+// scale per 16 elements, and g_t.  FC1 expands each token once and writes it
+// to the bucketed rows of its k pairs (inv = pair -> bucketed position); FC2
+// expands each bucketed pair row in place (inv = null, ncopy = 1).
 constexpr int kTermThreads = 256;
 
 template <bool BF16_IN>
 __global__ void __launch_bounds__(kTermThreads) act_terms_kernel(int K, const void* __restrict__ src,
-                                                                const int32_t* __restrict__ row_map, int map_div,
-                                                                const float* __restrict__ rowmax,
+                                                                const int32_t* __restrict__ inv, int ncopy,
+                                                                int out_rows, const float* __restrict__ rowmax,
                                                                 uint8_t* __restrict__ cperm, uint8_t* __restrict__ cnat,
                                                                 uint8_t* __restrict__ sfb, float* __restrict__ gsc) {
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
-  // output row `row` expands source row row_map[row] / map_div (or `row` itself)
-  const size_t srow = row_map ? (size_t)(__ldg(row_map + row) / map_div) : (size_t)row;
+  const size_t srow = (size_t)row;
   const float m = __ldg(rowmax + srow);
   const float g0 = m / (6.0f * 448.0f);
-  if (blockIdx.y == 0 && tid < kTcTerms) gsc[(size_t)row * kTcTerms + tid] = ldexpf(g0, -2 * tid);
+  // output rows of this source row (out of range entries are skipped)
+  auto out_row = [&](int cp) -> int {
+    const int r = inv ? __ldg(inv + (size_t)row * ncopy + cp) : row;
+    return r >= 0 && r < out_rows ? r : -1;
+  };
+  if (blockIdx.y == 0 && tid < kTcTerms) {
+    for (int cp = 0; cp < ncopy; ++cp) {
+      const int orow = out_row(cp);
+      if (orow >= 0) gsc[(size_t)orow * kTcTerms + tid] = ldexpf(g0, -2 * tid);
+    }
+  }
   const int idx = blockIdx.y * kTermThreads + tid;          // element of the row (K % 256 == 0)
   const int b = idx >> 4, j = idx & 15, lbase = lane & 16;
   float r = BF16_IN ? __uint_as_float((uint32_t)__ldg(static_cast<const uint16_t*>(src) + srow * K + idx) << 16)
@@ -203,22 +243,28 @@ __global__ void __launch_bounds__(kTermThreads) act_terms_kernel(int K, const vo
     const uint32_t nat_hi = __shfl_down_sync(0xffffffffu, code, 1);
     const uint32_t per_lo = __shfl_sync(0xffffffffu, code, lbase + src0);
     const uint32_t per_hi = __shfl_sync(0xffffffffu, code, lbase + src1);
-    const size_t term_row = (size_t)row * kTcTerms + t;
-    if ((j & 1) == 0) cnat[term_row * (K / 2) + 8 * b + (j >> 1)] = (uint8_t)(code | (nat_hi << 4));
-    if (j < 8) cperm[term_row * (K / 2) + 8 * b + j] = (uint8_t)(per_lo | (per_hi << 4));
-    if (j == 0) sfb[term_row * (K / 16) + b] = (uint8_t)sf;
+    for (int cp = 0; cp < ncopy; ++cp) {
+      const int orow = out_row(cp);
+      if (orow < 0) continue;
+      const size_t term_row = (size_t)orow * kTcTerms + t;
+      if ((j & 1) == 0) cnat[term_row * (K / 2) + 8 * b + (j >> 1)] = (uint8_t)(code | (nat_hi << 4));
+      if (j < 8) cperm[term_row * (K / 2) + 8 * b + j] = (uint8_t)(per_lo | (per_hi << 4));
+      if (j == 0) sfb[term_row * (K / 16) + b] = (uint8_t)sf;
+    }
   }
 }
 
 // ---------------------------------------------------------------- FC kernel
 struct TmaMaps {
   CUtensorMap sign, mag, q;        // planes u32 [E N, K/32] box {8, 64} SW32; s16 u8 [E N, K/16] box {16, 64}
-  CUtensorMap act, actn, sfb;      // terms u8 [pairs 4, K/2] box {128, 16} SW128 (perm / natural); scales box {16, 16}
-  CUtensorMap dcodes, ds4;         // delta u8 [S N, K/2] box {128, 64} SW128; scales box {16, 64}
+  CUtensorMap act, actn, sfb;      // terms u8 [pairs 4, K/2]: box {128, brows} SW128 (permuted order),
+                                   // box {64, brows} SW64 (natural order); scales box {16, brows}
+  CUtensorMap dcodes, ds4;         // delta u8 [S N, K/2] box {64, 64} SW64; scales box {16, 64}
 };
 
 struct FcTcArgs {
   int T, H, I, k, K, N;          // N = rows of one expert matrix
+  int tiles;                     // 128-row weight tiles per expert matrix
   int brows;                     // rows of one activation-term box: min(16, 4 * term rows)
   const int32_t* offsets;
   const int32_t* perm;
@@ -234,21 +280,38 @@ struct FcTcArgs {
   unsigned* hmax;                // FC1: max |h| per bucketed pair (fp32 bits), for the FC2 terms
 };
 
+// One unit of work = (work item, 128-row weight tile), written by the scheduler warp.
+struct UnitMeta {
+  int e, pos0, ntok, ncols;
+  int dslot;                     // delta slot when the unit runs the delta pass, else -1
+  int nch;                       // K steps: K/256 plane chunks (+ 2 K/256 delta half chunks)
+  int r0, r1;                    // first weight rows of the tile's two 64-row halves
+  float sc2;                     // the expert's scale_2
+  int pad[7];
+  int pair[kTcTok];              // pair id t k + j per token column (-1 = none)
+  float wts[kTcTok];             // routing weight per token column
+  float gate_f[kTcTok];          // 1 = the delta counts for this column
+  float gsc[kMaxN];              // term scales g_t, column order
+};
+static_assert(sizeof(UnitMeta) == 512, "UnitMeta layout");
+
 struct TcSmem {
-  uint64_t full[kSlots];         // TMA bytes landed
-  uint64_t staged[kSlots];       // converters done (A expanded, scales in TMEM)
-  uint64_t empty[kSlots];        // MMAs of the slot done
+  uint64_t full[kRaw];           // TMA bytes of the raw stage landed
+  uint64_t raw_empty[kRaw];      // MMAs reading the raw stage done
+  uint64_t staged[kAst];         // converters done (A expanded, scales in TMEM)
+  uint64_t a_empty[kAst];        // MMAs reading the A stage and its TMEM scales done
+  uint64_t acc_full[2];          // unit's accumulation complete
+  uint64_t acc_empty[2];         // epilogue has read the accumulators
+  uint64_t meta_full[kMeta];
+  uint64_t meta_empty[kMeta];
   uint32_t tmem_base;
   int stuck;
-  int issued;                    // MMA chunks issued
-  int any_gated;
-  int slot;
-  int src_row[kTcTok];           // activation-term row per token of the work item
-  float gate_f[kTcTok];
-  float gsc[kMaxN];              // term scales, column order
-  float wts[kTcTok];             // FC2: routing weight per pair
-  int pair[kTcTok];              // FC2: pair id per column token
 };
+
+constexpr size_t kXchgBytes = 64 * kTcTok * sizeof(float);
+constexpr size_t kSmemBytes =
+    1024 + (size_t)kRaw * kRawBytes + kXchgBytes + kMeta * sizeof(UnitMeta) + sizeof(TcSmem);
+static_assert(kSmemBytes <= 232448, "shared memory over the per-CTA limit");
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
   asm volatile(
@@ -269,38 +332,72 @@ __device__ __forceinline__ bool is_stuck(const TcSmem& sm) {
   return *reinterpret_cast<const volatile int*>(&sm.stuck) != 0;
 }
 
-// Warp-specialised FC over one 128-row weight tile of one expert and one work
-// item of <= kTcTok routed pairs.  Main pass: K chunks of 256 weights from the
-// 2-bit planes; delta pass (cached expert with gated pairs): the same chunks
-// of the NVFP4 delta into a second accumulator.
+__device__ __forceinline__ void set_stuck(TcSmem& sm) { atomicExch(&sm.stuck, 1); }
+
+// Warp-uniform bounded wait: true once every lane has seen the phase complete.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_addr(bar);
+  for (long long it = 0; it < kWaitLimit; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(done)
+        : "r"(a), "r"(parity));
+    if (__all_sync(0xffffffffu, done != 0u)) return true;
+  }
+  return false;
+}
+
+// OR of `flag` over the 128 epilogue threads (named barrier 1); every epilogue
+// thread gets the same answer, so their later barriers stay matched.
+__device__ __forceinline__ bool epi_any(bool flag) {
+  uint32_t out;
+  asm volatile("{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.or.pred q, 1, 128, p; selp.u32 %0, 1, 0, q; }"
+               : "=r"(out)
+               : "r"(flag ? 1u : 0u));
+  return out != 0u;
+}
+
+// Persistent warp-specialised FC: one CTA per SM walks the units u = blockIdx.x
+// + j gridDim.x of the (work item x weight tile) grid.  Warp roles:
+//   0, 3   producers, alternate K chunks: each TMA box of a chunk is issued by
+//          its own lane (one instruction), into a ring of kRaw raw stages
+//   1      TMEM owner; one thread issues the MMAs and their commits
+//   2      scheduler: per unit, the item's pairs, weights, gate flags and term
+//          scales into a ring of kMeta unit records
+//   4-7    epilogue (TMEM lane quarters 0-3): term sums, SiLU * up / routing
+//          weight, stores; the accumulators are double-buffered in TMEM so the
+//          next unit's MMAs run while the epilogue reads this one's
+//   8-23   converters in two groups of eight warps (two per 32-row quarter)
+//          that take the K chunks in turn: planes -> e2m1 A operand and scale
+//          factors, both stored straight into TMEM (each thread owns the TMEM
+//          lane of its weight row), so the expanded A never touches shared
+//          memory; a chunk's chain of dependent steps thus has two chunk times
+// Main pass per unit: K chunks of 256 weights from the 2-bit planes.  Delta
+// pass (cached expert with a gated pair): the NVFP4 delta in half chunks of
+// 128 weights (64-byte swizzled rows), so that a raw stage of the planes and
+// one of the delta have the same 10 KB size; it accumulates into a second
+// TMEM region.
 template <bool FC1>
-__global__ void __launch_bounds__(kWsThreads, 2) fc_tc_kernel(const FcTcArgs a, const __grid_constant__ TmaMaps maps) {
+__global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, const __grid_constant__ TmaMaps maps) {
   extern __shared__ __align__(1024) unsigned char smem_dyn[];
   unsigned char* base = smem_dyn + ((1024 - (smem_addr(smem_dyn) & 1023)) & 1023);
-  TcSmem& sm = *reinterpret_cast<TcSmem*>(base + kSlots * kSlotBytes);
+  unsigned char* raw = base;
+  float (*xchg)[kTcTok] = reinterpret_cast<float (*)[kTcTok]>(base + kRaw * kRawBytes);
+  UnitMeta* meta = reinterpret_cast<UnitMeta*>(base + kRaw * kRawBytes + kXchgBytes);
+  TcSmem& sm = *reinterpret_cast<TcSmem*>(meta + kMeta);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if ((int)blockIdx.y >= a.hdr[0]) return;
-  const int4 ch = a.chunks[blockIdx.y];
-  const int e = ch.x, ntok = ch.z;
-  const int pos0 = __ldg(a.offsets + e) + ch.y;
-  const int K = a.K, nkc = K / kKC;
-  const int ncols = ((kTcTerms * ntok + 15) / 16) * 16;        // MMA N (multiple of 16, <= 64)
+  const int total_units = a.hdr[0] * a.tiles;
+  const int nunits = (int)blockIdx.x < total_units ? (total_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  if (nunits == 0) return;
+  const int nkc = a.K / kKC;
 
   if (tid == 0) {
     sm.stuck = 0;
-    sm.issued = 0;
-    sm.any_gated = 0;
-    int slot = -1;
-    if (a.delta_slot != nullptr && a.gate != nullptr) {
-      slot = __ldg(a.delta_slot + e);
-      if (slot >= a.n_slots) { record_error(MOET_ERR_DEVICE_INDEX); slot = -1; }
-    }
-    sm.slot = slot;
-    for (int s = 0; s < kSlots; ++s) {
-      mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.staged[s], kConvThreads);
-      mbar_init(&sm.empty[s], 1);
-    }
+    for (int s = 0; s < kRaw; ++s) { mbar_init(&sm.full[s], 1); mbar_init(&sm.raw_empty[s], 1); }
+    for (int s = 0; s < kAst; ++s) { mbar_init(&sm.staged[s], kConvWarps); mbar_init(&sm.a_empty[s], 1); }
+    for (int s = 0; s < 2; ++s) { mbar_init(&sm.acc_full[s], 1); mbar_init(&sm.acc_empty[s], 4); }
+    for (int s = 0; s < kMeta; ++s) { mbar_init(&sm.meta_full[s], 1); mbar_init(&sm.meta_empty[s], 4); }
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
   if (warp == 1) {
@@ -308,174 +405,216 @@ __global__ void __launch_bounds__(kWsThreads, 2) fc_tc_kernel(const FcTcArgs a, 
                  "r"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-  __syncthreads();
-  if (tid < kTcTok) {
-    int srow = -1, pr = -1;
-    float gf = 0.0f, wv = 0.0f;
-    if (tid < ntok) {
-      const int p = __ldg(a.perm + pos0 + tid);
-      if (p < 0 || p >= a.T * a.k) {
-        record_error(MOET_ERR_DEVICE_INDEX);
-      } else {
-        const int tok = p / a.k;
-        srow = FC1 ? tok : pos0 + tid;
-        pr = p;
-        wv = __ldg(a.topk_w + p);
-        if (sm.slot >= 0 && __ldg(a.gate + tok)) { gf = 1.0f; sm.any_gated = 1; }
-      }
-    }
-    sm.src_row[tid] = srow;
-    sm.gate_f[tid] = gf;
-    sm.pair[tid] = pr;
-    sm.wts[tid] = wv;
-  }
-  __syncthreads();
-  if (tid < kMaxN) {
-    const int tk = tid / kTcTerms, term = tid % kTcTerms;
-    sm.gsc[tid] = tk < ntok && sm.src_row[tk] >= 0 ? __ldg(a.gsc + (size_t)(pos0 + tk) * kTcTerms + term) : 0.0f;
-  }
   asm volatile("tcgen05.fence::before_thread_sync;");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;");
   const uint32_t tmem = sm.tmem_base;
-  const bool do_delta = sm.slot >= 0 && sm.any_gated;
-  const int total = do_delta ? 2 * nkc : nkc;
-  // the two 64-row halves of the tile in the expert's matrix (FC1: gate rows, then up rows)
-  const int r0 = FC1 ? blockIdx.x * 64 : blockIdx.x * 128;
-  const int r1 = FC1 ? a.I + blockIdx.x * 64 : blockIdx.x * 128 + 64;
 
-  if (warp == 0) {
-    // ---------------- producer: one thread issues every TMA copy
-    if (lane == 0) {
-      for (int cg = 0; cg < total; ++cg) {
-        const int s = cg % kSlots, u = cg / kSlots;
-        if (u > 0 && !mbar_wait(&sm.empty[s], (u - 1) & 1)) { atomicExch(&sm.stuck, 1); break; }
-        if (is_stuck(sm)) break;
-        const bool dp = cg >= nkc;
-        const int c = dp ? cg - nkc : cg;
-        unsigned char* sl = base + s * kSlotBytes;
-        const int nbox = (ncols + 15) / 16;         // 16-row boxes of activation terms
-        const uint32_t bytes = (dp ? 16384u + 2048u : 4096u + 4096u + 2048u) + (uint32_t)(nbox * a.brows) * (128u + 16u);
-        mbar_expect_tx(&sm.full[s], bytes);
+  if (warp == 0 || warp == 3) {
+    // ---------------- producers: warp pw takes the chunks g with g % 2 == pw; the
+    // chunk's boxes are issued by one lane each in the same instruction
+    const int pw = warp == 0 ? 0 : 1;
+    int g = 0;
+    bool bad = false;
+    for (int j = 0; j < nunits && !bad; ++j) {
+      const int m = j % kMeta;
+      if (!mbar_wait_warp(&sm.meta_full[m], (j / kMeta) & 1)) { bad = true; break; }
+      const UnitMeta& um = meta[m];
+      const int pos0 = um.pos0, nch = um.nch, dslot = um.dslot;
+      const int nbox = um.ncols / 16;
+      const int y0 = (dslot >= 0 ? dslot : um.e) * a.N;      // delta rows only used by delta chunks
+      const int w0 = um.e * a.N + um.r0, w1 = um.e * a.N + um.r1;
+      for (int c = 0; c < nch; ++c, ++g) {
+        if ((g & 1) != pw) continue;
+        const int rs = g % kRaw, ru = g / kRaw;
+        if (ru > 0 && !mbar_wait_warp(&sm.raw_empty[rs], (ru - 1) & 1)) { bad = true; break; }
+        unsigned char* st = raw + rs * kRawBytes;
+        uint64_t* fb = &sm.full[rs];
+        const bool dp = c >= nkc;
+        if (lane == 0)
+          mbar_expect_tx(fb, 10240u + (uint32_t)(nbox * a.brows) * ((dp ? 64u : 128u) + 16u));
+        __syncwarp();
+        // lane -> box: 0-5 weight boxes (two 64-row halves each), then pairs (terms, scales) per 16 rows
+        const CUtensorMap* map = nullptr;
+        uint32_t dst = 0;
+        int x = 0, y = 0;
         if (!dp) {
-          const int y0 = e * a.N + r0, y1 = e * a.N + r1;
-          tma_load_2d(smem_addr(sl + kSSign), &maps.sign, c * 8, y0, &sm.full[s]);
-          tma_load_2d(smem_addr(sl + kSSign + 2048), &maps.sign, c * 8, y1, &sm.full[s]);
-          tma_load_2d(smem_addr(sl + kSMag), &maps.mag, c * 8, y0, &sm.full[s]);
-          tma_load_2d(smem_addr(sl + kSMag + 2048), &maps.mag, c * 8, y1, &sm.full[s]);
-          tma_load_2d(smem_addr(sl + kSQ), &maps.q, c * 16, y0, &sm.full[s]);
-          tma_load_2d(smem_addr(sl + kSQ + 1024), &maps.q, c * 16, y1, &sm.full[s]);
+          if (lane < 6) {
+            const int hv = lane & 1;
+            map = lane < 2 ? &maps.sign : lane < 4 ? &maps.mag : &maps.q;
+            dst = smem_addr(st + (lane < 2 ? kRSign + 2048 * hv : lane < 4 ? kRMag + 2048 * hv : kRQ + 1024 * hv));
+            x = lane < 4 ? c * 8 : c * 16;
+            y = hv ? w1 : w0;
+          } else if (lane < 6 + 2 * nbox) {
+            const int bx = (lane - 6) >> 1;
+            const bool sf = ((lane - 6) & 1) != 0;
+            map = sf ? &maps.sfb : &maps.act;
+            dst = smem_addr(st + (sf ? kRSF + bx * 256 : kRB + bx * 2048));
+            x = sf ? c * 16 : c * 128;
+            y = pos0 * kTcTerms + 16 * bx;
+          }
         } else {
-          const int y0 = sm.slot * a.N + r0, y1 = sm.slot * a.N + r1;
-          tma_load_2d(smem_addr(sl + kSA), &maps.dcodes, c * 128, y0, &sm.full[s]);
-          tma_load_2d(smem_addr(sl + kSA + 8192), &maps.dcodes, c * 128, y1, &sm.full[s]);
-          tma_load_2d(smem_addr(sl + kSQ), &maps.ds4, c * 16, y0, &sm.full[s]);
-          tma_load_2d(smem_addr(sl + kSQ + 1024), &maps.ds4, c * 16, y1, &sm.full[s]);
+          const int dc = c - nkc, kc = dc >> 1, hf = dc & 1;
+          if (lane < 4) {
+            const int hv = lane & 1;
+            map = lane < 2 ? &maps.dcodes : &maps.ds4;
+            dst = smem_addr(st + (lane < 2 ? 4096 * hv : kRQ + 1024 * hv));
+            x = lane < 2 ? kc * 128 + 64 * hf : kc * 16;
+            y = y0 + (hv ? um.r1 : um.r0);
+          } else if (lane < 4 + 2 * nbox) {
+            const int bx = (lane - 4) >> 1;
+            const bool sf = ((lane - 4) & 1) != 0;
+            map = sf ? &maps.sfb : &maps.actn;
+            dst = smem_addr(st + (sf ? kRSF + bx * 256 : kRB + bx * 1024));
+            x = sf ? kc * 16 : kc * 128 + 64 * hf;
+            y = pos0 * kTcTerms + 16 * bx;
+          }
         }
-        // the work item's pairs are consecutive bucketed rows: ncols / 16 boxes of 16 term rows
-        for (int bx = 0; bx < nbox; ++bx) {
-          tma_load_2d(smem_addr(sl + kSB + bx * 2048), dp ? &maps.actn : &maps.act, c * 128, pos0 * kTcTerms + 16 * bx,
-                      &sm.full[s]);
-          tma_load_2d(smem_addr(sl + kSF + bx * 256), &maps.sfb, c * 16, pos0 * kTcTerms + 16 * bx, &sm.full[s]);
-        }
+        if (map != nullptr) tma_load_2d(dst, map, x, y, fb);
       }
     }
+    if (bad && lane == 0) set_stuck(sm);
+    // every copy this warp issued has landed before the CTA may exit
+    if (lane == 0)
+      for (int i = g > kRaw ? g - kRaw : 0; i < g; ++i)
+        if ((i & 1) == pw) mbar_wait(&sm.full[i % kRaw], (i / kRaw) & 1);
   } else if (warp == 1) {
-    // ---------------- MMA issue: one thread
+    // ---------------- MMA issue
     if (lane == 0) {
-      const uint32_t idesc = mxf4_idesc(ncols);
-      int cg = 0;
-      for (; cg < total; ++cg) {
-        const int s = cg % kSlots, u = cg / kSlots;
-        if (!mbar_wait(&sm.staged[s], u & 1)) { atomicExch(&sm.stuck, 1); break; }
-        if (is_stuck(sm)) break;
+      int g = 0, last = -1;
+      bool bad = false;
+      for (int j = 0; j < nunits && !bad; ++j) {
+        const int m = j % kMeta, ab = j & 1;
+        if (!mbar_wait(&sm.meta_full[m], (j / kMeta) & 1)) { bad = true; break; }
+        if (j >= 2 && !mbar_wait(&sm.acc_empty[ab], ((j >> 1) - 1) & 1)) { bad = true; break; }
+        if (is_stuck(sm)) { bad = true; break; }
         asm volatile("tcgen05.fence::after_thread_sync;");
-        const bool dp = cg >= nkc;
-        const int c = dp ? cg - nkc : cg;
-        unsigned char* sl = base + s * kSlotBytes;
-        const uint32_t a0 = smem_addr(sl + kSA), b0 = smem_addr(sl + kSB);
+        const int nch = meta[m].nch;
+        const uint32_t idesc = mxf4_idesc(meta[m].ncols);
+        const uint32_t dcol = tmem + 128 * ab;
+        for (int c = 0; c < nch; ++c, ++g) {
+          const int as = g % kAst, au = g / kAst, rs = g % kRaw;
+          if (!mbar_wait(&sm.staged[as], au & 1)) { bad = true; break; }
+          asm volatile("tcgen05.fence::after_thread_sync;");
+          const uint32_t bsm = smem_addr(raw + rs * kRawBytes + kRB);
+          const uint32_t sfa = tmem + kColSFA + 16 * as, sfb = tmem + kColSFB + 16 * as;
+          if (c < nkc) {
+            const uint32_t ata = tmem + kColA + 32 * as;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          tc_mma(tmem + (dp ? kColD2 : kColD), sw128_desc(a0 + 32 * i), sw128_desc(b0 + 32 * i), idesc,
-                 tmem + kColSFA + 16 * s + 4 * i, tmem + kColSFB + 16 * s + 4 * i, (c > 0 || i > 0) ? 1u : 0u);
+            for (int i = 0; i < 4; ++i)
+              tc_mma_ta(dcol, ata + 8 * i, sw128_desc(bsm + 32 * i), idesc, sfa + 4 * i, sfb + 4 * i,
+                        (c > 0 || i > 0) ? 1u : 0u);
+          } else {
+            const int dc = c - nkc, hf = dc & 1;
+            const uint32_t asm_ = smem_addr(raw + rs * kRawBytes);
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+              tc_mma(dcol + 64, sw64_desc(asm_ + 32 * i), sw64_desc(bsm + 32 * i), idesc, sfa + 8 * hf + 4 * i,
+                     sfb + 8 * hf + 4 * i, (dc > 0 || i > 0) ? 1u : 0u);
+          }
+          tc_commit(&sm.a_empty[as]);
+          tc_commit(&sm.raw_empty[rs]);
+          last = g;
         }
-        tc_commit(&sm.empty[s]);
+        if (bad) break;
+        tc_commit(&sm.acc_full[ab]);
       }
-      sm.issued = cg;
+      if (bad) set_stuck(sm);
+      // every MMA this thread issued is complete before TMEM is released
+      if (last >= 0) mbar_wait(&sm.a_empty[last % kAst], (last / kAst) & 1);
     }
-  } else {
-    // ---------------- converters: two threads per tile row (= TMEM lane); half h
-    // expands weight words 4h..4h+3 of the chunk; half 0 writes the row scales to
-    // TMEM, half 1 the activation-term scales
-    const int half = (warp - 2) >> 2;
+  } else if (warp == 2) {
+    // ---------------- scheduler
+    for (int j = 0; j < nunits; ++j) {
+      const int m = j % kMeta;
+      if (j >= kMeta && !mbar_wait_warp(&sm.meta_empty[m], ((j / kMeta) - 1) & 1)) {
+        if (lane == 0) set_stuck(sm);
+        break;
+      }
+      if (__any_sync(0xffffffffu, is_stuck(sm))) break;
+      const int u = (int)blockIdx.x + j * (int)gridDim.x;
+      const int item = u / a.tiles, tile = u - item * a.tiles;
+      const int4 ch = a.chunks[item];
+      const int e = ch.x, ntok = ch.z;
+      const int pos0 = __ldg(a.offsets + e) + ch.y;
+      int dslot = -1;
+      if (a.delta_slot != nullptr && a.gate != nullptr) {
+        dslot = __ldg(a.delta_slot + e);
+        if (dslot >= a.n_slots) {
+          if (lane == 0) record_error(MOET_ERR_DEVICE_INDEX);
+          dslot = -1;
+        }
+      }
+      int pr = -1;
+      float wv = 0.0f, gf = 0.0f;
+      if (lane < ntok && lane < kTcTok) {
+        const int p = __ldg(a.perm + pos0 + lane);
+        if (p < 0 || p >= a.T * a.k) {
+          record_error(MOET_ERR_DEVICE_INDEX);
+        } else {
+          pr = p;
+          wv = __ldg(a.topk_w + p);
+          if (dslot >= 0 && __ldg(a.gate + p / a.k)) gf = 1.0f;
+        }
+      }
+      if (!__any_sync(0xffffffffu, gf != 0.0f)) dslot = -1;
+      UnitMeta& um = meta[m];
+      if (lane < kTcTok) { um.pair[lane] = pr; um.wts[lane] = wv; um.gate_f[lane] = gf; }
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int col = lane + 32 * h2, tk = col / kTcTerms;
+        const int ptk = __shfl_sync(0xffffffffu, pr, tk);
+        um.gsc[col] = tk < ntok && ptk >= 0 ? __ldg(a.gsc + (size_t)(pos0 + tk) * kTcTerms + col % kTcTerms) : 0.0f;
+      }
+      if (lane == 0) {
+        um.e = e; um.pos0 = pos0; um.ntok = ntok;
+        um.ncols = ((kTcTerms * ntok + 15) / 16) * 16;
+        um.dslot = dslot;
+        um.nch = dslot >= 0 ? 3 * nkc : nkc;
+        um.r0 = FC1 ? tile * 64 : tile * 128;
+        um.r1 = FC1 ? a.I + tile * 64 : tile * 128 + 64;
+        um.sc2 = __ldg(a.scale_2 + e);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.meta_full[m]);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------- epilogue: TMEM lane quarter warp & 3
     const int trow = 32 * (warp & 3) + lane;
     const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;
-    // 32-byte-swizzled raw plane rows: 16-byte piece h of row r sits at piece h ^ ((r >> 2) & 1)
-    const int praw = trow * 32 + ((half ^ ((trow >> 2) & 1)) << 4);
-    int aoff[4];
-#pragma unroll
-    for (int w = 0; w < 4; ++w) aoff[w] = kSA + trow * 128 + (((4 * half + w) ^ (trow & 7)) << 4);
-    for (int cg = 0; cg < total; ++cg) {
-      const int s = cg % kSlots, u = cg / kSlots;
-      if (!mbar_wait(&sm.full[s], u & 1)) { atomicExch(&sm.stuck, 1); break; }
-      if (is_stuck(sm)) break;
-      const bool dp = cg >= nkc;
-      unsigned char* sl = base + s * kSlotBytes;
-      if (!dp) {
-        const uint4 sw = *reinterpret_cast<const uint4*>(sl + kSSign + praw);
-        const uint4 mw = *reinterpret_cast<const uint4*>(sl + kSMag + praw);
-        *reinterpret_cast<uint4*>(sl + aoff[0]) = planes_to_e2m1(sw.x, mw.x);
-        *reinterpret_cast<uint4*>(sl + aoff[1]) = planes_to_e2m1(sw.y, mw.y);
-        *reinterpret_cast<uint4*>(sl + aoff[2]) = planes_to_e2m1(sw.z, mw.z);
-        *reinterpret_cast<uint4*>(sl + aoff[3]) = planes_to_e2m1(sw.w, mw.w);
+    for (int j = 0; j < nunits; ++j) {
+      const int m = j % kMeta, ab = j & 1;
+      bool ok = mbar_wait_warp(&sm.meta_full[m], (j / kMeta) & 1);
+      ok = ok && mbar_wait_warp(&sm.acc_full[ab], (j >> 1) & 1);
+      asm volatile("tcgen05.fence::after_thread_sync;");
+      if (epi_any(!ok || is_stuck(sm))) {
+        if (!ok && lane == 0) set_stuck(sm);
+        break;
       }
-      // scale factors to TMEM, replicated layout: rows lane + 32 j -> columns 4 i + j
-      uint32_t v[16];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int n = lane + 32 * j;
-        uint4 q = make_uint4(0u, 0u, 0u, 0u);
-        if (half == 0) q = *reinterpret_cast<const uint4*>(sl + kSQ + n * 16);
-        else if (n < ncols) q = *reinterpret_cast<const uint4*>(sl + kSF + n * 16);
-        v[0 * 4 + j] = q.x; v[1 * 4 + j] = q.y; v[2 * 4 + j] = q.z; v[3 * 4 + j] = q.w;
-      }
-      tmem_st16(tmem + lane_q + (half ? kColSFB : kColSFA) + 16 * s, v);
-      asm volatile("fence.proxy.async.shared::cta;");
-      asm volatile("tcgen05.wait::st.sync.aligned;");
-      asm volatile("tcgen05.fence::before_thread_sync;");
-      mbar_arrive(&sm.staged[s]);
-    }
-    // ---------------- epilogue (warps 2-5): wait for the last MMA chunk, read the accumulators
-    if (half == 0) {
-    if (!is_stuck(sm) && total > 0) {
-      const int last = total - 1;
-      if (!mbar_wait(&sm.empty[last % kSlots], (last / kSlots) & 1)) atomicExch(&sm.stuck, 1);
-    }
-    asm volatile("tcgen05.fence::after_thread_sync;");
-    asm volatile("bar.sync 1, 128;");
-    if (!is_stuck(sm)) {
-      // FC1: up rows hand their values to the gate rows through slot 0's raw B-scale area
-      float (*xchg)[kTcTok] = reinterpret_cast<float (*)[kTcTok]>(base + kSSign);
-      const float sc2 = 2.0f * __ldg(a.scale_2 + e);         // 2: the halved e2m1 levels
-      const float sc2d = __ldg(a.scale_2 + e);
-      const int wrow = trow < 64 ? r0 + trow : r1 + trow - 64;
+      const UnitMeta& um = meta[m];
+      const int ncols = um.ncols, ntok = um.ntok, pos0 = um.pos0;
+      const bool do_delta = um.dslot >= 0;
+      const float sc2 = 2.0f * um.sc2;          // 2: the halved e2m1 levels
+      const float sc2d = um.sc2;
+      const int wrow = trow < 64 ? um.r0 + trow : um.r1 + trow - 64;
+      const uint32_t dcol = tmem + lane_q + 128 * ab;
       for (int c0 = 0; c0 < ncols; c0 += 16) {
         float v[16], v2[16];
-        tmem_ld16(tmem + lane_q + kColD + c0, v);
-        if (do_delta) tmem_ld16(tmem + lane_q + kColD2 + c0, v2);
+        tmem_ld16(dcol + c0, v);
+        if (do_delta) tmem_ld16(dcol + 64 + c0, v2);
         float acc[16 / kTcTerms];
 #pragma unroll
         for (int q = 0; q < 16 / kTcTerms; ++q) {
           const int tk = c0 / kTcTerms + q;
           // delta columns count only for gated pairs (the B box also holds other pairs' rows)
-          const bool gated = do_delta && tk < kTcTok && sm.gate_f[tk] != 0.0f;
+          const bool gated = do_delta && um.gate_f[tk] != 0.0f;
           float sacc = 0.0f;
 #pragma unroll
           for (int t = 0; t < kTcTerms; ++t) {
             const int col = q * kTcTerms + t;
             float d = sc2 * v[col];
             if (gated) d = fmaf(sc2d, v2[col], d);
-            sacc = fmaf(sm.gsc[c0 + col], d, sacc);
+            sacc = fmaf(um.gsc[c0 + col], d, sacc);
           }
           acc[q] = sacc;
         }
@@ -483,7 +622,8 @@ __global__ void __launch_bounds__(kWsThreads, 2) fc_tc_kernel(const FcTcArgs a, 
 #pragma unroll
           for (int q = 0; q < 16 / kTcTerms; ++q) {
             const int tk = c0 / kTcTerms + q;
-            if (tk < ntok && sm.src_row[tk] >= 0) a.out[(size_t)sm.pair[tk] * a.H + wrow] = acc[q] * sm.wts[tk];
+            const int pr = um.pair[tk];
+            if (tk < ntok && pr >= 0) a.out[(size_t)pr * a.H + wrow] = acc[q] * um.wts[tk];
           }
         } else {
           if (trow >= 64) {
@@ -495,8 +635,9 @@ __global__ void __launch_bounds__(kWsThreads, 2) fc_tc_kernel(const FcTcArgs a, 
 #pragma unroll
             for (int q = 0; q < 16 / kTcTerms; ++q) {
               const int tk = c0 / kTcTerms + q;
+              const bool valid = tk < ntok && um.pair[tk] >= 0;
               float hv = 0.0f;
-              if (tk < ntok && sm.src_row[tk] >= 0) {
+              if (valid) {
                 const float gv = acc[q], uv = xchg[trow][tk];
                 hv = gv / (1.0f + expf(-gv)) * uv;
                 a.out[(size_t)(pos0 + tk) * a.I + wrow] = hv;
@@ -504,23 +645,77 @@ __global__ void __launch_bounds__(kWsThreads, 2) fc_tc_kernel(const FcTcArgs a, 
               float mx = fabsf(hv);
 #pragma unroll
               for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-              if (lane == 0 && tk < ntok && sm.src_row[tk] >= 0) atomicMax(a.hmax + pos0 + tk, __float_as_uint(mx));
+              if (lane == 0 && valid) atomicMax(a.hmax + pos0 + tk, __float_as_uint(mx));
             }
           }
           asm volatile("bar.sync 1, 128;");
         }
       }
+      asm volatile("tcgen05.fence::before_thread_sync;");
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&sm.acc_empty[ab]);
+        mbar_arrive(&sm.meta_empty[m]);
+      }
     }
+  } else if (warp >= 8) {
+    // ---------------- converters: group grp takes the chunks g with g % 2 == grp;
+    // in a group, two warps per 32-row quarter; half h expands weight words
+    // 4h..4h+3 of the chunk; half 0 writes the row scales to TMEM, half 1 the
+    // activation-term scales
+    const int grp = (warp - 8) >> 3;
+    const int half = ((warp - 8) >> 2) & 1;
+    const int trow = 32 * (warp & 3) + lane;
+    const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;
+    // 32-byte-swizzled raw plane rows: 16-byte piece h of row r sits at piece h ^ ((r >> 2) & 1)
+    const int praw = trow * 32 + ((half ^ ((trow >> 2) & 1)) << 4);
+    int g = 0;
+    bool bad = false;
+    for (int j = 0; j < nunits && !bad; ++j) {
+      const int m = j % kMeta;
+      if (!mbar_wait_warp(&sm.meta_full[m], (j / kMeta) & 1)) { bad = true; break; }
+      if (__any_sync(0xffffffffu, is_stuck(sm))) { bad = true; break; }
+      const int nch = meta[m].nch, ncols = meta[m].ncols;
+      for (int c = 0; c < nch; ++c, ++g) {
+        if ((g % kConvGroups) != grp) continue;
+        const int rs = g % kRaw, ru = g / kRaw, as = g % kAst, au = g / kAst;
+        if (!mbar_wait_warp(&sm.full[rs], ru & 1)) { bad = true; break; }
+        if (au > 0 && !mbar_wait_warp(&sm.a_empty[as], (au - 1) & 1)) { bad = true; break; }
+        const unsigned char* st = raw + rs * kRawBytes;
+        if (c < nkc) {
+          // this thread's 128 weights of the row -> 16 TMEM columns of its lane (K order)
+          const uint4 sw = *reinterpret_cast<const uint4*>(st + kRSign + praw);
+          const uint4 mw = *reinterpret_cast<const uint4*>(st + kRMag + praw);
+          uint32_t av[16];
+          const uint4 e0 = planes_to_e2m1(sw.x, mw.x), e1 = planes_to_e2m1(sw.y, mw.y);
+          const uint4 e2 = planes_to_e2m1(sw.z, mw.z), e3 = planes_to_e2m1(sw.w, mw.w);
+          av[0] = e0.x; av[1] = e0.y; av[2] = e0.z; av[3] = e0.w;
+          av[4] = e1.x; av[5] = e1.y; av[6] = e1.z; av[7] = e1.w;
+          av[8] = e2.x; av[9] = e2.y; av[10] = e2.z; av[11] = e2.w;
+          av[12] = e3.x; av[13] = e3.y; av[14] = e3.z; av[15] = e3.w;
+          tmem_st16(tmem + lane_q + kColA + 32 * as + 16 * half, av);
+        }
+        // scale factors to TMEM, replicated layout: rows lane + 32 j -> columns 4 i + j
+        uint32_t v[16];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int n = lane + 32 * jj;
+          uint4 q = make_uint4(0u, 0u, 0u, 0u);
+          if (half == 0) q = *reinterpret_cast<const uint4*>(st + kRQ + n * 16);
+          else if (n < ncols) q = *reinterpret_cast<const uint4*>(st + kRSF + n * 16);
+          v[0 * 4 + jj] = q.x; v[1 * 4 + jj] = q.y; v[2 * 4 + jj] = q.z; v[3 * 4 + jj] = q.w;
+        }
+        tmem_st16(tmem + lane_q + (half ? kColSFB : kColSFA) + 16 * as, v);
+        asm volatile("tcgen05.wait::st.sync.aligned;");
+        asm volatile("tcgen05.fence::before_thread_sync;");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.staged[as]);
+      }
     }
+    if (bad && lane == 0) set_stuck(sm);
   }
   __syncthreads();
   if (warp == 1) {
-    // every MMA this CTA issued must be complete before TMEM is released
-    const int issued = sm.issued;
-    if (lane == 0 && is_stuck(sm) && issued > 0) {
-      const int last = issued - 1;
-      mbar_wait(&sm.empty[last % kSlots], (last / kSlots) & 1);
-    }
     __syncwarp();
     asm volatile("tcgen05.fence::after_thread_sync;");
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
@@ -560,9 +755,22 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Streaming multiprocessors of the current device (one persistent CTA each).
+int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
 template <bool FC1>
 moet_status launch_fc_tc(const FcTcArgs& a, const moet_planes* pl, const moet_nvfp4* dl, const uint8_t* cperm,
-                         const uint8_t* cnat, const uint8_t* sfb, int act_rows, int E, int row_tiles, int grid_y,
+                         const uint8_t* cnat, const uint8_t* sfb, int act_rows, int E, int row_tiles,
                          cudaStream_t st) {
   TmaMaps m;
   std::memset(&m, 0, sizeof(m));
@@ -573,24 +781,26 @@ moet_status launch_fc_tc(const FcTcArgs& a, const moet_planes* pl, const moet_nv
             make_map(&m.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pl->s16, rowsW, K / 16, 16, 64, CU_TENSOR_MAP_SWIZZLE_NONE) &&
             make_map(&m.act, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, cperm, (uint64_t)act_rows * kTcTerms, K / 2, 128,
                      brows, CU_TENSOR_MAP_SWIZZLE_128B) &&
-            make_map(&m.actn, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, cnat, (uint64_t)act_rows * kTcTerms, K / 2, 128,
-                     brows, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_map(&m.actn, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, cnat, (uint64_t)act_rows * kTcTerms, K / 2, 64,
+                     brows, CU_TENSOR_MAP_SWIZZLE_64B) &&
             make_map(&m.sfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, sfb, (uint64_t)act_rows * kTcTerms, K / 16, 16,
                      brows, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (ok && a.delta_slot != nullptr) {
     const uint64_t rowsD = (uint64_t)a.n_slots * a.N;
-    ok = make_map(&m.dcodes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dl->codes, rowsD, K / 2, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+    ok = make_map(&m.dcodes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dl->codes, rowsD, K / 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_64B) &&
          make_map(&m.ds4, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dl->s4, rowsD, K / 16, 16, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
   }
   if (!ok) return MOET_ERR_CUDA;
   FcTcArgs ab = a;
   ab.brows = (int)brows;
-  const size_t smem = 1024 + kSlots * kSlotBytes + sizeof(TcSmem);
+  ab.tiles = row_tiles;
+  const int grid = sm_count();
+  if (grid <= 0) return MOET_ERR_CUDA;
   auto kern = fc_tc_kernel<FC1>;
-  MOET_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  MOET_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes));
   {
     ProfScope ps(FC1 ? MOET_K_FC1 : MOET_K_FC2, st);
-    kern<<<dim3(row_tiles, grid_y), kWsThreads, smem, st>>>(ab, m);
+    kern<<<grid, kWsThreads, kSmemBytes, st>>>(ab, m);
   }
   MOET_CUDA_TRY(cudaGetLastError());
   return MOET_OK;
@@ -600,12 +810,12 @@ moet_status launch_fc_tc(const FcTcArgs& a, const moet_planes* pl, const moet_nv
 
 moet_status tc_forward(const TcForwardArgs& f, cudaStream_t st) {
   const int pairs = f.T * f.k;
-  // FC1 input terms: one row per token
+  // FC1 input terms: each token once, written to the bucketed rows of its k pairs so that a
+  // work item's term rows are consecutive
   {
     ProfScope ps(MOET_K_TERMS, st);
-    // one row per bucketed pair (the pair's token), so a work item's rows are consecutive
-    const dim3 grid(pairs, f.H / kTermThreads);
-    act_terms_kernel<true><<<grid, kTermThreads, 0, st>>>(f.H, f.x, f.perm, f.k, f.tokmax, f.buf.x_cperm,
+    const dim3 grid(f.T, f.H / kTermThreads);
+    act_terms_kernel<true><<<grid, kTermThreads, 0, st>>>(f.H, f.x, f.inv, f.k, pairs, f.tokmax, f.buf.x_cperm,
                                                           f.buf.x_cnat, f.buf.x_sf, f.buf.x_g);
   }
   MOET_CUDA_TRY(cudaGetLastError());
@@ -621,13 +831,13 @@ moet_status tc_forward(const TcForwardArgs& f, cudaStream_t st) {
   a1.out = f.h;
   a1.hmax = f.hmax;
   moet_status s = launch_fc_tc<true>(a1, f.fc1, f.dfc1, f.buf.x_cperm, f.buf.x_cnat, f.buf.x_sf, pairs, f.E,
-                                     f.I / 64, f.max_items, st);
+                                     f.I / 64, st);
   if (s != MOET_OK) return s;
   // FC2 input terms: one row per bucketed pair (h rows are in bucketed order)
   {
     ProfScope ps(MOET_K_TERMS, st);
     const dim3 grid(pairs, f.I / kTermThreads);
-    act_terms_kernel<false><<<grid, kTermThreads, 0, st>>>(f.I, f.h, nullptr, 1,
+    act_terms_kernel<false><<<grid, kTermThreads, 0, st>>>(f.I, f.h, nullptr, 1, pairs,
                                                            reinterpret_cast<const float*>(f.hmax), f.buf.h_cperm,
                                                            f.buf.h_cnat, f.buf.h_sf, f.buf.h_g);
   }
@@ -637,8 +847,7 @@ moet_status tc_forward(const TcForwardArgs& f, cudaStream_t st) {
   a2.scale_2 = f.fc2->scale_2;
   a2.gsc = f.buf.h_g;
   a2.out = f.o;
-  return launch_fc_tc<false>(a2, f.fc2, f.dfc2, f.buf.h_cperm, f.buf.h_cnat, f.buf.h_sf, pairs, f.E, f.H / 128,
-                             f.max_items, st);
+  return launch_fc_tc<false>(a2, f.fc2, f.dfc2, f.buf.h_cperm, f.buf.h_cnat, f.buf.h_sf, pairs, f.E, f.H / 128, st);
 }
 
 }  // namespace moet

@@ -45,6 +45,7 @@ struct TcForwardArgs {
   float* o;                    // [T k, H] pair order
   const float* tokmax;         // [T] max |x_t| (written by the prologue)
   unsigned* hmax;              // [T k] max |h| per bucketed pair, zeroed by the prologue
+  const int32_t* inv;          // [T k] pair -> bucketed position (written by the prologue)
   TcBuffers buf;
   int max_items;
 };
