@@ -52,24 +52,26 @@ namespace moet {
 namespace {
 
 constexpr int kWsThreads = 768;              // 24 warps, roles in fc_tc_kernel
-constexpr int kConvGroups = 2;                // converter groups, taking K chunks in turn
-constexpr int kConvWarps = 8;                 // per group: two converter warps per 32-row quarter
-constexpr int kRaw = 10;                      // raw TMA stages in flight
-constexpr int kAst = 4;                       // expanded-A stages (in TMEM)
+constexpr int kConvGroups = 2;                // converter groups, one per MMA sub-step of a stage
+constexpr int kConvWarps = 8;                 // per group: two warps per 32-row quarter
+constexpr int kRaw = 5;                       // raw TMA stages in flight
+constexpr int kAst = 2;                       // expanded-A stages (in TMEM)
 constexpr int kMeta = 4;                      // unit records in flight
-constexpr int kKC = 256;                      // weights per K chunk (one SW128 atom)
+constexpr int kKC = 512;                      // weights per plane stage: two MMA sub-steps of 256
+constexpr int kKD = 256;                      // weights per delta stage: one sub-step
 constexpr int kMaxN = kTcTerms * kTcTok;      // 64 columns of D
 constexpr int kTmemCols = 512;
 // TMEM columns: accumulator buffer b holds D at 128 b and the delta's D2 at 128 b + 64;
-// A stage s (128 rows x 256 e2m1 = 32 columns) at kColA + 32 s; scale factors per A stage
-// at kColSFA + 16 s (weights) and kColSFB + 16 s (activations)
-constexpr int kColA = 256, kColSFA = kColA + 32 * kAst, kColSFB = kColSFA + 16 * kAst;
-static_assert(kColSFB + 16 * kAst <= kTmemCols, "TMEM columns");
-// raw stage (1024-aligned): sign and magnitude planes [128 rows][32 B] (SW32), row scales
-// [128][16 B]; a delta half chunk puts its codes [128][64 B] (SW64) over the planes and its
-// scales over the row scales.  Then the activation terms [<= 64 rows][128 B] (SW128; natural
-// order [64 B] SW64 for delta half chunks) and their scales [<= 64][16 B].
-constexpr int kRSign = 0, kRMag = 4096, kRQ = 8192, kRB = 10240, kRSF = 18432, kRawBytes = 19456;
+// A stage s (128 rows x 512 e2m1 = 64 columns; sub-step h at +32 h) at kColA + 64 s;
+// scale factors of A stage s at kColSFA + 32 s and kColSFB + 32 s (sub-step h at +16 h)
+constexpr int kColA = 256, kColSFA = kColA + 64 * kAst, kColSFB = kColSFA + 32 * kAst;
+static_assert(kColSFB + 32 * kAst <= kTmemCols, "TMEM columns");
+// raw stage (1024-aligned).  Plane stage: sign and magnitude planes [128 rows][64 B] (SW64),
+// row scales [128][32 B] (SW32), activation terms [2 sub-steps][<= 64 rows][128 B] (SW128),
+// term scales [<= 64 rows][32 B].  Delta stage: codes [128][128 B] (SW128) at 0, scales
+// [128][16 B] at kRDS, terms in natural order [<= 64][128 B] at kRB, term scales [<= 64][16 B].
+constexpr int kRSign = 0, kRMag = 8192, kRQ = 16384, kRB = 20480, kRSF = 36864, kRawBytes = 38912;
+constexpr int kRDS = 16384;
 constexpr long long kWaitLimit = 1LL << 22;   // polls before a wait is declared stuck
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -256,10 +258,10 @@ __global__ void __launch_bounds__(kTermThreads) act_terms_kernel(int K, const vo
 
 // ---------------------------------------------------------------- FC kernel
 struct TmaMaps {
-  CUtensorMap sign, mag, q;        // planes u32 [E N, K/32] box {8, 64} SW32; s16 u8 [E N, K/16] box {16, 64}
-  CUtensorMap act, actn, sfb;      // terms u8 [pairs 4, K/2]: box {128, brows} SW128 (permuted order),
-                                   // box {64, brows} SW64 (natural order); scales box {16, brows}
-  CUtensorMap dcodes, ds4;         // delta u8 [S N, K/2] box {64, 64} SW64; scales box {16, 64}
+  CUtensorMap sign, mag, q;        // planes u32 [E N, K/32] box {16, 64} SW64; s16 u8 [E N, K/16] box {32, 64} SW32
+  CUtensorMap act, actn;           // terms u8 [pairs 4, K/2] box {128, brows} SW128 (permuted / natural order)
+  CUtensorMap sfb2, sfb1;          // term scales u8 [pairs 4, K/16] box {32, brows} / {16, brows}
+  CUtensorMap dcodes, ds4;         // delta u8 [S N, K/2] box {128, 64} SW128; scales box {16, 64}
 };
 
 struct FcTcArgs {
@@ -284,7 +286,7 @@ struct FcTcArgs {
 struct UnitMeta {
   int e, pos0, ntok, ncols;
   int dslot;                     // delta slot when the unit runs the delta pass, else -1
-  int nch;                       // K steps: K/256 plane chunks (+ 2 K/256 delta half chunks)
+  int nch;                       // stages: ceil(K/512) plane stages (+ K/256 delta stages)
   int r0, r1;                    // first weight rows of the tile's two 64-row halves
   float sc2;                     // the expert's scale_2
   int pad[7];
@@ -360,7 +362,7 @@ __device__ __forceinline__ bool epi_any(bool flag) {
 
 // Persistent warp-specialised FC: one CTA per SM walks the units u = blockIdx.x
 // + j gridDim.x of the (work item x weight tile) grid.  Warp roles:
-//   0, 3   producers, alternate K chunks: each TMA box of a chunk is issued by
+//   0, 3   producers, alternate stages: each TMA box of a stage is issued by
 //          its own lane (one instruction), into a ring of kRaw raw stages
 //   1      TMEM owner; one thread issues the MMAs and their commits
 //   2      scheduler: per unit, the item's pairs, weights, gate flags and term
@@ -368,16 +370,16 @@ __device__ __forceinline__ bool epi_any(bool flag) {
 //   4-7    epilogue (TMEM lane quarters 0-3): term sums, SiLU * up / routing
 //          weight, stores; the accumulators are double-buffered in TMEM so the
 //          next unit's MMAs run while the epilogue reads this one's
-//   8-23   converters in two groups of eight warps (two per 32-row quarter)
-//          that take the K chunks in turn: planes -> e2m1 A operand and scale
-//          factors, both stored straight into TMEM (each thread owns the TMEM
-//          lane of its weight row), so the expanded A never touches shared
-//          memory; a chunk's chain of dependent steps thus has two chunk times
-// Main pass per unit: K chunks of 256 weights from the 2-bit planes.  Delta
-// pass (cached expert with a gated pair): the NVFP4 delta in half chunks of
-// 128 weights (64-byte swizzled rows), so that a raw stage of the planes and
-// one of the delta have the same 10 KB size; it accumulates into a second
-// TMEM region.
+//   8-23   converters in two groups of eight warps (two per 32-row quarter);
+//          group h takes sub-step h of every stage: planes -> e2m1 A operand
+//          and scale factors, both stored straight into TMEM (each thread owns
+//          the TMEM lane of its weight row), so the expanded A never touches
+//          shared memory
+// Main pass per unit: stages of 512 weights from the 2-bit planes (two MMA
+// sub-steps of 256; converter group h expands sub-step h).  Delta pass (cached
+// expert with a gated pair): the NVFP4 delta in stages of 256 weights, its
+// codes used as the A operand straight from shared memory; it accumulates
+// into a second TMEM region.
 template <bool FC1>
 __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, const __grid_constant__ TmaMaps maps) {
   extern __shared__ __align__(1024) unsigned char smem_dyn[];
@@ -390,12 +392,12 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
   const int total_units = a.hdr[0] * a.tiles;
   const int nunits = (int)blockIdx.x < total_units ? (total_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
   if (nunits == 0) return;
-  const int nkc = a.K / kKC;
+  const int nps = (a.K + kKC - 1) / kKC;        // plane stages per unit
 
   if (tid == 0) {
     sm.stuck = 0;
     for (int s = 0; s < kRaw; ++s) { mbar_init(&sm.full[s], 1); mbar_init(&sm.raw_empty[s], 1); }
-    for (int s = 0; s < kAst; ++s) { mbar_init(&sm.staged[s], kConvWarps); mbar_init(&sm.a_empty[s], 1); }
+    for (int s = 0; s < kAst; ++s) { mbar_init(&sm.staged[s], kConvGroups * kConvWarps); mbar_init(&sm.a_empty[s], 1); }
     for (int s = 0; s < 2; ++s) { mbar_init(&sm.acc_full[s], 1); mbar_init(&sm.acc_empty[s], 4); }
     for (int s = 0; s < kMeta; ++s) { mbar_init(&sm.meta_full[s], 1); mbar_init(&sm.meta_empty[s], 4); }
     asm volatile("fence.mbarrier_init.release.cluster;");
@@ -411,8 +413,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
   const uint32_t tmem = sm.tmem_base;
 
   if (warp == 0 || warp == 3) {
-    // ---------------- producers: warp pw takes the chunks g with g % 2 == pw; the
-    // chunk's boxes are issued by one lane each in the same instruction
+    // ---------------- producers: warp pw takes the stages g with g % 2 == pw; the
+    // stage's boxes are issued by one lane each in the same instruction
     const int pw = warp == 0 ? 0 : 1;
     int g = 0;
     bool bad = false;
@@ -422,19 +424,23 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
       const UnitMeta& um = meta[m];
       const int pos0 = um.pos0, nch = um.nch, dslot = um.dslot;
       const int nbox = um.ncols / 16;
-      const int y0 = (dslot >= 0 ? dslot : um.e) * a.N;      // delta rows only used by delta chunks
+      const int y0 = (dslot >= 0 ? dslot : um.e) * a.N;      // delta rows only used by delta stages
       const int w0 = um.e * a.N + um.r0, w1 = um.e * a.N + um.r1;
+      const int trow0 = pos0 * kTcTerms;                    // first activation-term row of the item
       for (int c = 0; c < nch; ++c, ++g) {
         if ((g & 1) != pw) continue;
         const int rs = g % kRaw, ru = g / kRaw;
         if (ru > 0 && !mbar_wait_warp(&sm.raw_empty[rs], (ru - 1) & 1)) { bad = true; break; }
         unsigned char* st = raw + rs * kRawBytes;
         uint64_t* fb = &sm.full[rs];
-        const bool dp = c >= nkc;
-        if (lane == 0)
-          mbar_expect_tx(fb, 10240u + (uint32_t)(nbox * a.brows) * ((dp ? 64u : 128u) + 16u));
+        const bool dp = c >= nps;
+        const int nsub = dp ? 1 : min(2, (a.K - kKC * c) / kKD);
+        if (lane == 0) {
+          const uint32_t bx_bytes = (uint32_t)a.brows * (dp ? 128u + 16u : 128u * nsub + 32u);
+          mbar_expect_tx(fb, (dp ? 16384u + 2048u : 20480u) + (uint32_t)nbox * bx_bytes);
+        }
         __syncwarp();
-        // lane -> box: 0-5 weight boxes (two 64-row halves each), then pairs (terms, scales) per 16 rows
+        // lane -> box: weight boxes (two 64-row halves each), then the item's term boxes (16 rows each)
         const CUtensorMap* map = nullptr;
         uint32_t dst = 0;
         int x = 0, y = 0;
@@ -442,32 +448,42 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
           if (lane < 6) {
             const int hv = lane & 1;
             map = lane < 2 ? &maps.sign : lane < 4 ? &maps.mag : &maps.q;
-            dst = smem_addr(st + (lane < 2 ? kRSign + 2048 * hv : lane < 4 ? kRMag + 2048 * hv : kRQ + 1024 * hv));
-            x = lane < 4 ? c * 8 : c * 16;
+            dst = smem_addr(st + (lane < 2 ? kRSign + 4096 * hv : lane < 4 ? kRMag + 4096 * hv : kRQ + 2048 * hv));
+            x = lane < 4 ? c * 16 : c * 32;
             y = hv ? w1 : w0;
-          } else if (lane < 6 + 2 * nbox) {
-            const int bx = (lane - 6) >> 1;
-            const bool sf = ((lane - 6) & 1) != 0;
-            map = sf ? &maps.sfb : &maps.act;
-            dst = smem_addr(st + (sf ? kRSF + bx * 256 : kRB + bx * 2048));
-            x = sf ? c * 16 : c * 128;
-            y = pos0 * kTcTerms + 16 * bx;
+          } else if (lane < 6 + nsub * nbox) {
+            const int q = lane - 6, sub = q / nbox, bx = q - sub * nbox;
+            map = &maps.act;
+            dst = smem_addr(st + kRB + 8192 * sub + 2048 * bx);
+            x = (2 * c + sub) * 128;
+            y = trow0 + 16 * bx;
+          } else if (lane < 6 + (nsub + 1) * nbox) {
+            const int bx = lane - 6 - nsub * nbox;
+            map = &maps.sfb2;
+            dst = smem_addr(st + kRSF + 512 * bx);
+            x = c * 32;
+            y = trow0 + 16 * bx;
           }
         } else {
-          const int dc = c - nkc, kc = dc >> 1, hf = dc & 1;
+          const int dc = c - nps;
           if (lane < 4) {
             const int hv = lane & 1;
             map = lane < 2 ? &maps.dcodes : &maps.ds4;
-            dst = smem_addr(st + (lane < 2 ? 4096 * hv : kRQ + 1024 * hv));
-            x = lane < 2 ? kc * 128 + 64 * hf : kc * 16;
+            dst = smem_addr(st + (lane < 2 ? 8192 * hv : kRDS + 1024 * hv));
+            x = lane < 2 ? dc * 128 : dc * 16;
             y = y0 + (hv ? um.r1 : um.r0);
+          } else if (lane < 4 + nbox) {
+            const int bx = lane - 4;
+            map = &maps.actn;
+            dst = smem_addr(st + kRB + 2048 * bx);
+            x = dc * 128;
+            y = trow0 + 16 * bx;
           } else if (lane < 4 + 2 * nbox) {
-            const int bx = (lane - 4) >> 1;
-            const bool sf = ((lane - 4) & 1) != 0;
-            map = sf ? &maps.sfb : &maps.actn;
-            dst = smem_addr(st + (sf ? kRSF + bx * 256 : kRB + bx * 1024));
-            x = sf ? kc * 16 : kc * 128 + 64 * hf;
-            y = pos0 * kTcTerms + 16 * bx;
+            const int bx = lane - 4 - nbox;
+            map = &maps.sfb1;
+            dst = smem_addr(st + kRSF + 256 * bx);
+            x = dc * 16;
+            y = trow0 + 16 * bx;
           }
         }
         if (map != nullptr) tma_load_2d(dst, map, x, y, fb);
@@ -496,21 +512,23 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
           const int as = g % kAst, au = g / kAst, rs = g % kRaw;
           if (!mbar_wait(&sm.staged[as], au & 1)) { bad = true; break; }
           asm volatile("tcgen05.fence::after_thread_sync;");
-          const uint32_t bsm = smem_addr(raw + rs * kRawBytes + kRB);
-          const uint32_t sfa = tmem + kColSFA + 16 * as, sfb = tmem + kColSFB + 16 * as;
-          if (c < nkc) {
-            const uint32_t ata = tmem + kColA + 32 * as;
+          const uint32_t rsm = smem_addr(raw + rs * kRawBytes);
+          const uint32_t sfa = tmem + kColSFA + 32 * as, sfb = tmem + kColSFB + 32 * as;
+          if (c < nps) {
+            const int nsub = min(2, (a.K - kKC * c) / kKD);
+            const uint32_t ata = tmem + kColA + 64 * as;
+            for (int h = 0; h < nsub; ++h) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                tc_mma_ta(dcol, ata + 32 * h + 8 * i, sw128_desc(rsm + kRB + 8192 * h + 32 * i), idesc,
+                          sfa + 16 * h + 4 * i, sfb + 16 * h + 4 * i, (c > 0 || h > 0 || i > 0) ? 1u : 0u);
+            }
+          } else {
+            const int dc = c - nps;
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-              tc_mma_ta(dcol, ata + 8 * i, sw128_desc(bsm + 32 * i), idesc, sfa + 4 * i, sfb + 4 * i,
-                        (c > 0 || i > 0) ? 1u : 0u);
-          } else {
-            const int dc = c - nkc, hf = dc & 1;
-            const uint32_t asm_ = smem_addr(raw + rs * kRawBytes);
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-              tc_mma(dcol + 64, sw64_desc(asm_ + 32 * i), sw64_desc(bsm + 32 * i), idesc, sfa + 8 * hf + 4 * i,
-                     sfb + 8 * hf + 4 * i, (dc > 0 || i > 0) ? 1u : 0u);
+              tc_mma(dcol + 64, sw128_desc(rsm + 32 * i), sw128_desc(rsm + kRB + 32 * i), idesc, sfa + 4 * i,
+                     sfb + 4 * i, (dc > 0 || i > 0) ? 1u : 0u);
           }
           tc_commit(&sm.a_empty[as]);
           tc_commit(&sm.raw_empty[rs]);
@@ -570,7 +588,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
         um.e = e; um.pos0 = pos0; um.ntok = ntok;
         um.ncols = ((kTcTerms * ntok + 15) / 16) * 16;
         um.dslot = dslot;
-        um.nch = dslot >= 0 ? 3 * nkc : nkc;
+        um.nch = dslot >= 0 ? nps + a.K / kKD : nps;
         um.r0 = FC1 ? tile * 64 : tile * 128;
         um.r1 = FC1 ? a.I + tile * 64 : tile * 128 + 64;
         um.sc2 = __ldg(a.scale_2 + e);
@@ -659,16 +677,16 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
       }
     }
   } else if (warp >= 8) {
-    // ---------------- converters: group grp takes the chunks g with g % 2 == grp;
-    // in a group, two warps per 32-row quarter; half h expands weight words
-    // 4h..4h+3 of the chunk; half 0 writes the row scales to TMEM, half 1 the
-    // activation-term scales
+    // ---------------- converters: group grp expands sub-step grp (256 weights) of
+    // every plane stage (group 0 handles the delta stages); in a group, two warps
+    // per 32-row quarter; half h expands weight words 4h..4h+3 of the sub-step;
+    // half 0 writes the row scales to TMEM, half 1 the activation-term scales
     const int grp = (warp - 8) >> 3;
     const int half = ((warp - 8) >> 2) & 1;
     const int trow = 32 * (warp & 3) + lane;
     const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;
-    // 32-byte-swizzled raw plane rows: 16-byte piece h of row r sits at piece h ^ ((r >> 2) & 1)
-    const int praw = trow * 32 + ((half ^ ((trow >> 2) & 1)) << 4);
+    // 64-byte-swizzled plane rows: 16-byte piece p of row r sits at piece p ^ ((r >> 1) & 3)
+    const int praw = trow * 64 + (((2 * grp + half) ^ ((trow >> 1) & 3)) << 4);
     int g = 0;
     bool bad = false;
     for (int j = 0; j < nunits && !bad; ++j) {
@@ -677,37 +695,45 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
       if (__any_sync(0xffffffffu, is_stuck(sm))) { bad = true; break; }
       const int nch = meta[m].nch, ncols = meta[m].ncols;
       for (int c = 0; c < nch; ++c, ++g) {
-        if ((g % kConvGroups) != grp) continue;
         const int rs = g % kRaw, ru = g / kRaw, as = g % kAst, au = g / kAst;
         if (!mbar_wait_warp(&sm.full[rs], ru & 1)) { bad = true; break; }
         if (au > 0 && !mbar_wait_warp(&sm.a_empty[as], (au - 1) & 1)) { bad = true; break; }
-        const unsigned char* st = raw + rs * kRawBytes;
-        if (c < nkc) {
-          // this thread's 128 weights of the row -> 16 TMEM columns of its lane (K order)
-          const uint4 sw = *reinterpret_cast<const uint4*>(st + kRSign + praw);
-          const uint4 mw = *reinterpret_cast<const uint4*>(st + kRMag + praw);
-          uint32_t av[16];
-          const uint4 e0 = planes_to_e2m1(sw.x, mw.x), e1 = planes_to_e2m1(sw.y, mw.y);
-          const uint4 e2 = planes_to_e2m1(sw.z, mw.z), e3 = planes_to_e2m1(sw.w, mw.w);
-          av[0] = e0.x; av[1] = e0.y; av[2] = e0.z; av[3] = e0.w;
-          av[4] = e1.x; av[5] = e1.y; av[6] = e1.z; av[7] = e1.w;
-          av[8] = e2.x; av[9] = e2.y; av[10] = e2.z; av[11] = e2.w;
-          av[12] = e3.x; av[13] = e3.y; av[14] = e3.z; av[15] = e3.w;
-          tmem_st16(tmem + lane_q + kColA + 32 * as + 16 * half, av);
-        }
-        // scale factors to TMEM, replicated layout: rows lane + 32 j -> columns 4 i + j
-        uint32_t v[16];
+        const bool dp = c >= nps;
+        const int nsub = dp ? 1 : min(2, (a.K - kKC * c) / kKD);
+        if (grp < nsub) {
+          const unsigned char* st = raw + rs * kRawBytes;
+          if (!dp) {
+            // this thread's 128 weights of the row -> 16 TMEM columns of its lane (K order)
+            const uint4 sw = *reinterpret_cast<const uint4*>(st + kRSign + praw);
+            const uint4 mw = *reinterpret_cast<const uint4*>(st + kRMag + praw);
+            uint32_t av[16];
+            const uint4 e0 = planes_to_e2m1(sw.x, mw.x), e1 = planes_to_e2m1(sw.y, mw.y);
+            const uint4 e2 = planes_to_e2m1(sw.z, mw.z), e3 = planes_to_e2m1(sw.w, mw.w);
+            av[0] = e0.x; av[1] = e0.y; av[2] = e0.z; av[3] = e0.w;
+            av[4] = e1.x; av[5] = e1.y; av[6] = e1.z; av[7] = e1.w;
+            av[8] = e2.x; av[9] = e2.y; av[10] = e2.z; av[11] = e2.w;
+            av[12] = e3.x; av[13] = e3.y; av[14] = e3.z; av[15] = e3.w;
+            tmem_st16(tmem + lane_q + kColA + 64 * as + 32 * grp + 16 * half, av);
+          }
+          // scale factors to TMEM, replicated layout: rows lane + 32 j -> columns 4 i + j
+          uint32_t v[16];
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int n = lane + 32 * jj;
-          uint4 q = make_uint4(0u, 0u, 0u, 0u);
-          if (half == 0) q = *reinterpret_cast<const uint4*>(st + kRQ + n * 16);
-          else if (n < ncols) q = *reinterpret_cast<const uint4*>(st + kRSF + n * 16);
-          v[0 * 4 + jj] = q.x; v[1 * 4 + jj] = q.y; v[2 * 4 + jj] = q.z; v[3 * 4 + jj] = q.w;
+          for (int jj = 0; jj < 4; ++jj) {
+            const int n = lane + 32 * jj;
+            uint4 q = make_uint4(0u, 0u, 0u, 0u);
+            if (half == 0) {
+              // plane row scales: 32-byte-swizzled rows, piece h of row n at h ^ ((n >> 2) & 1)
+              const int off = dp ? kRDS + n * 16 : kRQ + n * 32 + ((grp ^ ((n >> 2) & 1)) << 4);
+              q = *reinterpret_cast<const uint4*>(st + off);
+            } else if (n < ncols) {
+              q = *reinterpret_cast<const uint4*>(st + kRSF + (dp ? n * 16 : n * 32 + 16 * grp));
+            }
+            v[0 * 4 + jj] = q.x; v[1 * 4 + jj] = q.y; v[2 * 4 + jj] = q.z; v[3 * 4 + jj] = q.w;
+          }
+          tmem_st16(tmem + lane_q + (half ? kColSFB : kColSFA) + 32 * as + 16 * grp, v);
+          asm volatile("tcgen05.wait::st.sync.aligned;");
+          asm volatile("tcgen05.fence::before_thread_sync;");
         }
-        tmem_st16(tmem + lane_q + (half ? kColSFB : kColSFA) + 16 * as, v);
-        asm volatile("tcgen05.wait::st.sync.aligned;");
-        asm volatile("tcgen05.fence::before_thread_sync;");
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.staged[as]);
       }
@@ -776,18 +802,17 @@ moet_status launch_fc_tc(const FcTcArgs& a, const moet_planes* pl, const moet_nv
   std::memset(&m, 0, sizeof(m));
   const uint32_t brows = (uint32_t)(act_rows * kTcTerms < 16 ? act_rows * kTcTerms : 16);
   const uint64_t rowsW = (uint64_t)E * a.N, K = (uint64_t)a.K;
-  bool ok = make_map(&m.sign, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, pl->sign, rowsW, K / 32, 8, 64, CU_TENSOR_MAP_SWIZZLE_32B) &&
-            make_map(&m.mag, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, pl->mag, rowsW, K / 32, 8, 64, CU_TENSOR_MAP_SWIZZLE_32B) &&
-            make_map(&m.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pl->s16, rowsW, K / 16, 16, 64, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-            make_map(&m.act, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, cperm, (uint64_t)act_rows * kTcTerms, K / 2, 128,
-                     brows, CU_TENSOR_MAP_SWIZZLE_128B) &&
-            make_map(&m.actn, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, cnat, (uint64_t)act_rows * kTcTerms, K / 2, 64,
-                     brows, CU_TENSOR_MAP_SWIZZLE_64B) &&
-            make_map(&m.sfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, sfb, (uint64_t)act_rows * kTcTerms, K / 16, 16,
-                     brows, CU_TENSOR_MAP_SWIZZLE_NONE);
+  const uint64_t trows = (uint64_t)act_rows * kTcTerms;
+  bool ok = make_map(&m.sign, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, pl->sign, rowsW, K / 32, 16, 64, CU_TENSOR_MAP_SWIZZLE_64B) &&
+            make_map(&m.mag, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, pl->mag, rowsW, K / 32, 16, 64, CU_TENSOR_MAP_SWIZZLE_64B) &&
+            make_map(&m.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pl->s16, rowsW, K / 16, 32, 64, CU_TENSOR_MAP_SWIZZLE_32B) &&
+            make_map(&m.act, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, cperm, trows, K / 2, 128, brows, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_map(&m.actn, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, cnat, trows, K / 2, 128, brows, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_map(&m.sfb2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, sfb, trows, K / 16, 32, brows, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+            make_map(&m.sfb1, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, sfb, trows, K / 16, 16, brows, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (ok && a.delta_slot != nullptr) {
     const uint64_t rowsD = (uint64_t)a.n_slots * a.N;
-    ok = make_map(&m.dcodes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dl->codes, rowsD, K / 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_64B) &&
+    ok = make_map(&m.dcodes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dl->codes, rowsD, K / 2, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
          make_map(&m.ds4, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dl->s4, rowsD, K / 16, 16, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
   }
   if (!ok) return MOET_ERR_CUDA;
