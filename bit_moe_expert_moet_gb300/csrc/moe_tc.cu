@@ -34,7 +34,7 @@
 // with TMA (sign and magnitude planes, row scales, the item's activation-term
 // rows and their scales); converter warps expand the planes into a ring of
 // swizzled A stages and write the scale factors to TMEM; one thread issues the
-// MMAs (K = 64 each) and commits them to the stages' "empty" barriers and, at
+// MMAs (K = 64 each) and commits them to the stage's "done" barrier and, at
 // the end of a unit, to one of two TMEM accumulator buffers that the epilogue
 // warps drain while the next unit accumulates.  A scheduler warp prepares
 // each unit's record (pairs, routing weights, gate flags, term scales) ahead
@@ -66,6 +66,7 @@ constexpr int kTmemCols = 512;
 // scale factors of A stage s at kColSFA + 32 s and kColSFB + 32 s (sub-step h at +16 h)
 constexpr int kColA = 256, kColSFA = kColA + 64 * kAst, kColSFB = kColSFA + 32 * kAst;
 static_assert(kColSFB + 32 * kAst <= kTmemCols, "TMEM columns");
+static_assert(kAst <= kRaw, "an A stage is released by the done barrier of its raw stage");
 // raw stage (1024-aligned).  Plane stage: sign and magnitude planes [128 rows][64 B] (SW64),
 // row scales [128][32 B] (SW32), activation terms [2 sub-steps][<= 64 rows][128 B] (SW128),
 // term scales [<= 64 rows][32 B].  Delta stage: codes [128][128 B] (SW128) at 0, scales
@@ -180,18 +181,18 @@ __device__ __forceinline__ uint4 planes_to_e2m1(uint32_t S, uint32_t M) {
 }
 
 // ---------------------------------------------------------------- activation terms
-// Grid (source rows, K / 256), 256 threads: 16 threads expand one 16-element
-// block (one element each) into kTcTerms NVFP4 terms.  Term t has the fp32
-// scale g_t = m / (6 * 448) / 4^t, m = the row maximum (given: per token for
-// FC1, per pair from FC1's epilogue for FC2), and a ue4m3 scale per block
-// chosen from the block's current residual, so each term quantises what the
-// previous ones left (a block's residual shrinks at least ~6x per term while
-// g_t shrinks 4x, keeping the block scales in the normal e4m3 range).  Outputs
-// per (output row, term): codes in permuted and natural K order, one ue4m3
-// scale per 16 elements, and g_t.  FC1 expands each token once and writes it
-// to the bucketed rows of its k pairs (inv = pair -> bucketed position); FC2
-// expands each bucketed pair row in place (inv = null, ncopy = 1).
-constexpr int kTermThreads = 256;
+// Grid (source rows, ceil(K / 16 / 128)), 128 threads: one thread expands one
+// 16-element block into kTcTerms NVFP4 terms.  Term t has the fp32 scale
+// g_t = m / (6 * 448) / 4^t, m = the row maximum (given: per token for FC1,
+// per pair from FC1's epilogue for FC2), and a ue4m3 scale per block chosen
+// from the block's current residual, so each term quantises what the previous
+// ones left (a block's residual shrinks at least ~6x per term while g_t
+// shrinks 4x, keeping the block scales in the normal e4m3 range).  Outputs per
+// (output row, term): codes in permuted and natural K order (8 bytes each per
+// block), one ue4m3 scale per block, and g_t.  FC1 expands each token once and
+// writes it to the bucketed rows of its k pairs (inv = pair -> bucketed
+// position); FC2 expands each bucketed pair row in place (inv = null, ncopy = 1).
+constexpr int kTermThreads = 128;
 
 template <bool BF16_IN>
 __global__ void __launch_bounds__(kTermThreads) act_terms_kernel(int K, const void* __restrict__ src,
@@ -199,7 +200,7 @@ __global__ void __launch_bounds__(kTermThreads) act_terms_kernel(int K, const vo
                                                                 int out_rows, const float* __restrict__ rowmax,
                                                                 uint8_t* __restrict__ cperm, uint8_t* __restrict__ cnat,
                                                                 uint8_t* __restrict__ sfb, float* __restrict__ gsc) {
-  const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+  const int row = blockIdx.x, tid = threadIdx.x;
   const size_t srow = (size_t)row;
   const float m = __ldg(rowmax + srow);
   const float g0 = m / (6.0f * 448.0f);
@@ -214,44 +215,65 @@ __global__ void __launch_bounds__(kTermThreads) act_terms_kernel(int K, const vo
       if (orow >= 0) gsc[(size_t)orow * kTcTerms + tid] = ldexpf(g0, -2 * tid);
     }
   }
-  const int idx = blockIdx.y * kTermThreads + tid;          // element of the row (K % 256 == 0)
-  const int b = idx >> 4, j = idx & 15, lbase = lane & 16;
-  float r = BF16_IN ? __uint_as_float((uint32_t)__ldg(static_cast<const uint16_t*>(src) + srow * K + idx) << 16)
-                    : static_cast<const float*>(src)[srow * K + idx];
-  // the element whose code lands at permuted position p = 4 r + n is r + 4 n
-  const int p0 = 2 * (j & 7), p1 = p0 + 1;
-  const int src0 = (p0 >> 2) + 4 * (p0 & 3);
-  const int src1 = (p1 >> 2) + 4 * (p1 & 3);
+  const int b = blockIdx.y * kTermThreads + tid;            // 16-element block of the row
+  if (b >= K / 16) return;
+  float r[16];
+  if (BF16_IN) {
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) + srow * K + 16 * b);
+    const uint4 u0 = __ldg(p), u1 = __ldg(p + 1);
+    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      r[2 * i] = __uint_as_float(w[i] << 16);
+      r[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(src) + srow * K + 16 * b);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 v = p[i];
+      r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
+    }
+  }
 #pragma unroll
   for (int t = 0; t < kTcTerms; ++t) {
     const float g = ldexpf(g0, -2 * t);
-    float bm = fabsf(r);
+    float bm = 0.0f;
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+    for (int i = 0; i < 16; ++i) bm = fmaxf(bm, fabsf(r[i]));
     uint32_t sf = 0;
     float sc = 0.0f;
     if (g > 0.0f) {
       sf = f32_to_e4m3_rn(bm / (6.0f * g));
       sc = e4m3_to_f32(sf) * g;
     }
-    uint32_t code = 0;
-    if (sc > 0.0f) {
-      const uint32_t mg = e2m1_rne_mag(fabsf(r), sc);
-      const bool neg = r < 0.0f && mg != 0u;
-      const float q = e2m1_mag_value(mg) * sc;
-      r -= neg ? -q : q;
-      code = mg | (neg ? 8u : 0u);
+    uint32_t code[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      code[i] = 0;
+      if (sc > 0.0f) {
+        const uint32_t mg = e2m1_rne_mag(fabsf(r[i]), sc);
+        const bool neg = r[i] < 0.0f && mg != 0u;
+        const float q = e2m1_mag_value(mg) * sc;
+        r[i] -= neg ? -q : q;
+        code[i] = mg | (neg ? 8u : 0u);
+      }
     }
-    const uint32_t nat_hi = __shfl_down_sync(0xffffffffu, code, 1);
-    const uint32_t per_lo = __shfl_sync(0xffffffffu, code, lbase + src0);
-    const uint32_t per_hi = __shfl_sync(0xffffffffu, code, lbase + src1);
+    // natural order: byte i holds elements 2i, 2i+1; permuted order: position p = 4 r + n
+    // holds element r + 4 n
+    uint32_t nat[2] = {0u, 0u}, per[2] = {0u, 0u};
+#pragma unroll
+    for (int p = 0; p < 16; ++p) {
+      nat[p >> 3] |= code[p] << (4 * (p & 7));
+      per[p >> 3] |= code[(p >> 2) + 4 * (p & 3)] << (4 * (p & 7));
+    }
     for (int cp = 0; cp < ncopy; ++cp) {
       const int orow = out_row(cp);
       if (orow < 0) continue;
       const size_t term_row = (size_t)orow * kTcTerms + t;
-      if ((j & 1) == 0) cnat[term_row * (K / 2) + 8 * b + (j >> 1)] = (uint8_t)(code | (nat_hi << 4));
-      if (j < 8) cperm[term_row * (K / 2) + 8 * b + j] = (uint8_t)(per_lo | (per_hi << 4));
-      if (j == 0) sfb[term_row * (K / 16) + b] = (uint8_t)sf;
+      *reinterpret_cast<uint2*>(cnat + term_row * (K / 2) + 8 * b) = make_uint2(nat[0], nat[1]);
+      *reinterpret_cast<uint2*>(cperm + term_row * (K / 2) + 8 * b) = make_uint2(per[0], per[1]);
+      sfb[term_row * (K / 16) + b] = (uint8_t)sf;
     }
   }
 }
@@ -299,9 +321,8 @@ static_assert(sizeof(UnitMeta) == 512, "UnitMeta layout");
 
 struct TcSmem {
   uint64_t full[kRaw];           // TMA bytes of the raw stage landed
-  uint64_t raw_empty[kRaw];      // MMAs reading the raw stage done
+  uint64_t done[kRaw];           // MMAs of the stage done (raw stage and its A stage free)
   uint64_t staged[kAst];         // converters done (A expanded, scales in TMEM)
-  uint64_t a_empty[kAst];        // MMAs reading the A stage and its TMEM scales done
   uint64_t acc_full[2];          // unit's accumulation complete
   uint64_t acc_empty[2];         // epilogue has read the accumulators
   uint64_t meta_full[kMeta];
@@ -396,8 +417,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
 
   if (tid == 0) {
     sm.stuck = 0;
-    for (int s = 0; s < kRaw; ++s) { mbar_init(&sm.full[s], 1); mbar_init(&sm.raw_empty[s], 1); }
-    for (int s = 0; s < kAst; ++s) { mbar_init(&sm.staged[s], kConvGroups * kConvWarps); mbar_init(&sm.a_empty[s], 1); }
+    for (int s = 0; s < kRaw; ++s) { mbar_init(&sm.full[s], 1); mbar_init(&sm.done[s], 1); }
+    for (int s = 0; s < kAst; ++s) mbar_init(&sm.staged[s], kConvGroups * kConvWarps);
     for (int s = 0; s < 2; ++s) { mbar_init(&sm.acc_full[s], 1); mbar_init(&sm.acc_empty[s], 4); }
     for (int s = 0; s < kMeta; ++s) { mbar_init(&sm.meta_full[s], 1); mbar_init(&sm.meta_empty[s], 4); }
     asm volatile("fence.mbarrier_init.release.cluster;");
@@ -430,7 +451,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
       for (int c = 0; c < nch; ++c, ++g) {
         if ((g & 1) != pw) continue;
         const int rs = g % kRaw, ru = g / kRaw;
-        if (ru > 0 && !mbar_wait_warp(&sm.raw_empty[rs], (ru - 1) & 1)) { bad = true; break; }
+        if (ru > 0 && !mbar_wait_warp(&sm.done[rs], (ru - 1) & 1)) { bad = true; break; }
         unsigned char* st = raw + rs * kRawBytes;
         uint64_t* fb = &sm.full[rs];
         const bool dp = c >= nps;
@@ -530,8 +551,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
               tc_mma(dcol + 64, sw128_desc(rsm + 32 * i), sw128_desc(rsm + kRB + 32 * i), idesc, sfa + 4 * i,
                      sfb + 4 * i, (dc > 0 || i > 0) ? 1u : 0u);
           }
-          tc_commit(&sm.a_empty[as]);
-          tc_commit(&sm.raw_empty[rs]);
+          tc_commit(&sm.done[rs]);
           last = g;
         }
         if (bad) break;
@@ -539,7 +559,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
       }
       if (bad) set_stuck(sm);
       // every MMA this thread issued is complete before TMEM is released
-      if (last >= 0) mbar_wait(&sm.a_empty[last % kAst], (last / kAst) & 1);
+      if (last >= 0) mbar_wait(&sm.done[last % kRaw], (last / kRaw) & 1);
     }
   } else if (warp == 2) {
     // ---------------- scheduler
@@ -695,9 +715,10 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
       if (__any_sync(0xffffffffu, is_stuck(sm))) { bad = true; break; }
       const int nch = meta[m].nch, ncols = meta[m].ncols;
       for (int c = 0; c < nch; ++c, ++g) {
-        const int rs = g % kRaw, ru = g / kRaw, as = g % kAst, au = g / kAst;
+        const int rs = g % kRaw, ru = g / kRaw, as = g % kAst;
         if (!mbar_wait_warp(&sm.full[rs], ru & 1)) { bad = true; break; }
-        if (au > 0 && !mbar_wait_warp(&sm.a_empty[as], (au - 1) & 1)) { bad = true; break; }
+        // the A stage is free once the MMAs of stage g - kAst are done
+        if (g >= kAst && !mbar_wait_warp(&sm.done[(g - kAst) % kRaw], ((g - kAst) / kRaw) & 1)) { bad = true; break; }
         const bool dp = c >= nps;
         const int nsub = dp ? 1 : min(2, (a.K - kKC * c) / kKD);
         if (grp < nsub) {
@@ -839,7 +860,7 @@ moet_status tc_forward(const TcForwardArgs& f, cudaStream_t st) {
   // work item's term rows are consecutive
   {
     ProfScope ps(MOET_K_TERMS, st);
-    const dim3 grid(f.T, f.H / kTermThreads);
+    const dim3 grid(f.T, (f.H / 16 + kTermThreads - 1) / kTermThreads);
     act_terms_kernel<true><<<grid, kTermThreads, 0, st>>>(f.H, f.x, f.inv, f.k, pairs, f.tokmax, f.buf.x_cperm,
                                                           f.buf.x_cnat, f.buf.x_sf, f.buf.x_g);
   }
@@ -861,7 +882,7 @@ moet_status tc_forward(const TcForwardArgs& f, cudaStream_t st) {
   // FC2 input terms: one row per bucketed pair (h rows are in bucketed order)
   {
     ProfScope ps(MOET_K_TERMS, st);
-    const dim3 grid(pairs, f.I / kTermThreads);
+    const dim3 grid(pairs, (f.I / 16 + kTermThreads - 1) / kTermThreads);
     act_terms_kernel<false><<<grid, kTermThreads, 0, st>>>(f.I, f.h, nullptr, 1, pairs,
                                                            reinterpret_cast<const float*>(f.hmax), f.buf.h_cperm,
                                                            f.buf.h_cnat, f.buf.h_sf, f.buf.h_g);

@@ -3,7 +3,7 @@
 // Routing step of the MoE layer (README "Frontier MoE on consumer Blackwell
 // (SM120)", "How it fits"; the airanks page's DeepSeek-V4.1 table, row "MoE at
 // decode", counts seven launches from router to FC1 in stock vLLM -- here it is
-// one launch for up to 512 tokens and two beyond).
+// one launch for up to 16 tokens and two beyond).
 //
 // Top-k: one warp per token; each lane holds ceil(E/32) logits in registers
 // and a 64-bit key (order-preserving logit bits, then the complement of the
@@ -166,11 +166,16 @@ __global__ void __launch_bounds__(1024) bucket_kernel(int T, int E, int k, const
   }
 }
 
+// Largest T routed by the single-CTA fused kernel: beyond it the top-k work
+// (about k warp-wide arg-max rounds per token) is spread over one warp per
+// token on many SMs, and one CTA buckets the result.
+constexpr int kFusedMaxT = 16;
+
 template <int VPL>
 static moet_status launch_route(int T, int E, int k, const float* logits, int32_t* idx, float* w,
                                 int32_t* offsets, int32_t* perm, cudaStream_t st) {
   const size_t smem = (size_t)E * 8 + (size_t)E * 32;
-  if (T <= 512) {
+  if (T <= kFusedMaxT) {
     auto kern = bucket_kernel<VPL, true>;
     if (smem > 48 * 1024) MOET_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     ProfScope ps(MOET_K_ROUTE, st);
