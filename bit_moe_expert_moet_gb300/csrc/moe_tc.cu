@@ -73,7 +73,9 @@ static_assert(kAst <= kRaw, "an A stage is released by the done barrier of its r
 // [128][16 B] at kRDS, terms in natural order [<= 64][128 B] at kRB, term scales [<= 64][16 B].
 constexpr int kRSign = 0, kRMag = 8192, kRQ = 16384, kRB = 20480, kRSF = 36864, kRawBytes = 38912;
 constexpr int kRDS = 16384;
-constexpr long long kWaitLimit = 1LL << 22;   // polls before a wait is declared stuck
+constexpr int kWaitLimit = 1 << 20;           // polls before a wait is declared stuck
+constexpr uint32_t kSuspendNs = 2000;         // suspend-time hint of one poll (the warp sleeps
+                                              // until the phase completes or the hint expires)
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -111,12 +113,13 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 // Bounded wait for the mbarrier phase with the given parity; false if it gave up.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_addr(bar);
-  for (long long it = 0; it < kWaitLimit; ++it) {
+  for (int it = 0; it < kWaitLimit; ++it) {
     uint32_t done;
     asm volatile(
-        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
         : "=r"(done)
-        : "r"(a), "r"(parity));
+        : "r"(a), "r"(parity), "r"(kSuspendNs)
+        : "memory");
     if (done) return true;
   }
   return false;
@@ -360,12 +363,13 @@ __device__ __forceinline__ void set_stuck(TcSmem& sm) { atomicExch(&sm.stuck, 1)
 // Warp-uniform bounded wait: true once every lane has seen the phase complete.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_addr(bar);
-  for (long long it = 0; it < kWaitLimit; ++it) {
+  for (int it = 0; it < kWaitLimit; ++it) {
     uint32_t done;
     asm volatile(
-        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
         : "=r"(done)
-        : "r"(a), "r"(parity));
+        : "r"(a), "r"(parity), "r"(kSuspendNs)
+        : "memory");
     if (__all_sync(0xffffffffu, done != 0u)) return true;
   }
   return false;
