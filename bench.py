@@ -104,6 +104,27 @@ def hbm_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def fc1_traffic(workload):
+    """FC1 DRAM bytes per launch from the committed ncu summary, or None when the summary was
+    taken on another workload or another FC kernel source (the counters no longer apply)."""
+    p = os.path.join(ROOT, "profiles", "fc1_traffic.txt")
+    src = os.path.join(ROOT, "bit_moe_expert_moet_gb300", "csrc", "moe_tc.cu")
+    if workload != "dsv3_decode_t64" or not (os.path.exists(p) and os.path.exists(src)):
+        return None
+    import hashlib
+    with open(src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    rec = {}
+    with open(p) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) == 2 and not line.startswith("#"):
+                rec[parts[0]] = parts[1]
+    if rec.get("source_sha256") != sha:
+        return None
+    return int(rec["fc1_traffic_bytes"])
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms while active."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
@@ -534,7 +555,7 @@ def run_ours(args, rank, world, local):
         "step_frac_of_hbm": layer.bytes_total / (ms_step * 1e-3) / 1e9 / peak,
         "roofline": {"bound": "hbm", "kernel": "fc_kernel<FC1>", "achieved": achieved, "peak": peak,
                      "peak_source": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "algorithmic_bytes_per_launch": layer.bytes_fc1,
+                     "traffic": fc1_traffic(cfg.name), "algorithmic_bytes_per_launch": layer.bytes_fc1,
                      "launch_ms": fc1_ms},
         "kernel_ms_per_launch": kernel_ms,
         "cpu_baseline": cpu,
