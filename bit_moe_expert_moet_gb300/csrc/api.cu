@@ -90,6 +90,7 @@ extern "C" __attribute__((visibility("hidden"))) int moet_internal_error_requant
 extern "C" __attribute__((visibility("hidden"))) int moet_internal_error_route(void);
 extern "C" __attribute__((visibility("hidden"))) int moet_internal_error_moe(void);
 extern "C" __attribute__((visibility("hidden"))) int moet_internal_error_moe_tc(void);
+extern "C" __attribute__((visibility("hidden"))) int moet_internal_error_moe_pf(void);
 
 extern "C" const char* moet_status_string(moet_status s) {
   switch (s) {
@@ -109,8 +110,8 @@ extern "C" const char* moet_status_string(moet_status s) {
 extern "C" moet_status moet_last_device_error(moet_stream stream) {
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MOET_ERR_CUDA;
   int first = 0;
-  const int codes[4] = {moet_internal_error_requant(), moet_internal_error_route(),
-                        moet_internal_error_moe(), moet_internal_error_moe_tc()};
+  const int codes[5] = {moet_internal_error_requant(), moet_internal_error_route(),
+                        moet_internal_error_moe(), moet_internal_error_moe_tc(), moet_internal_error_moe_pf()};
   for (int c : codes) {
     if (c < 0) return MOET_ERR_CUDA;
     if (first == 0 && c != 0) first = c;

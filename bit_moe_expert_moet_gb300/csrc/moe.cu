@@ -32,6 +32,7 @@
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "moe_pf.cuh"
 #include "moe_tc.cuh"
 
 namespace moet {
@@ -42,7 +43,7 @@ constexpr int kSmemBudget = 96 * 1024;
 constexpr uint32_t kCodeLut = 0xC242BC3Cu;  // f16 high bytes of +1, -1, +3, -3
 
 struct WsLayout {
-  size_t hdr, tok_scale, tok_max, hmax, inv, chunks, h, o, xt, ht, total;
+  size_t hdr, tok_scale, tok_max, hmax, inv, chunks, h, o, xt, ht, pfa, total;
 };
 
 // Largest T routed through the tcgen05 engine (small tokens-per-expert regime).
@@ -67,10 +68,12 @@ inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   L.chunks = off;    off += align256(sizeof(int4) * (size_t)max_chunks(T, E, k, kTcTok));
   L.h = off;         off += align256(sizeof(float) * pairs * I);
   L.o = off;         off += align256(sizeof(float) * pairs * H);
-  L.xt = off; L.ht = off;
+  L.xt = off; L.ht = off; L.pfa = off;
   if (T <= kTcMaxT && tc_supported(H, I)) {
     L.xt = off;      off += align256(tc_terms_bytes(pairs, (size_t)H));
     L.ht = off;      off += align256(tc_terms_bytes(pairs, (size_t)I));
+  } else if (T > kTcMaxT && pf_supported(H, I)) {
+    L.pfa = off;     off += align256(pf_act_bytes(pairs, (size_t)H, (size_t)I) + 4 * 256);
   }
   L.total = off;
   return L;
@@ -536,7 +539,8 @@ extern "C" moet_status moet_moe_forward(int T, int H, int I, int E, int k, const
   float* o = reinterpret_cast<float*>(ws + L.o);
 
   const bool use_tc = T <= kTcMaxT && tc_supported(H, I);
-  const int chunk = use_tc ? kTcTok : kChunk;
+  const bool use_pf = !use_tc && T > kTcMaxT && pf_supported(H, I);
+  const int chunk = use_tc ? kTcTok : use_pf ? kPfTok : kChunk;
   {
     ProfScope ps(MOET_K_PROLOGUE, st);
     prologue_kernel<<<1 + (T + 7) / 8, kThreads, 0, st>>>(T, H, E, k, chunk, x, expert_offsets, perm, hdr,
@@ -546,7 +550,24 @@ extern "C" moet_status moet_moe_forward(int T, int H, int I, int E, int k, const
   MOET_CUDA_TRY(cudaGetLastError());
 
   const int mc = max_chunks(T, E, k, chunk);
-  if (use_tc) {
+  if (use_pf) {
+    PfForwardArgs f{};
+    f.T = T; f.H = H; f.I = I; f.E = E; f.k = k;
+    f.x = x; f.offsets = expert_offsets; f.perm = perm; f.topk_w = topk_w;
+    f.fc1 = fc1; f.fc2 = fc2;
+    f.delta_slot = with_delta ? delta_slot : nullptr;
+    f.n_slots = n_slots; f.dfc1 = dfc1; f.dfc2 = dfc2;
+    f.gate = with_delta ? gate_mask : nullptr;
+    f.hdr = hdr; f.chunks = chunks; f.o = o;
+    const size_t pairs = (size_t)T * k;
+    char* pb = ws + L.pfa;
+    f.xb = reinterpret_cast<uint16_t*>(pb);  pb += align256(pairs * H * sizeof(uint16_t));
+    f.xbg = reinterpret_cast<uint16_t*>(pb); pb += align256(pairs * H * sizeof(uint16_t));
+    f.h = h;
+    f.hg = reinterpret_cast<float*>(pb);
+    moet_status s = pf_forward(f, st);
+    if (s != MOET_OK) return s;
+  } else if (use_tc) {
     TcForwardArgs f{};
     f.T = T; f.H = H; f.I = I; f.E = E; f.k = k;
     f.x = x; f.offsets = expert_offsets; f.perm = perm; f.topk_w = topk_w;

@@ -1,0 +1,580 @@
+// tcgen05 bf16 FC engine for large token counts (prefill, sm_103a).
+//
+// README "Frontier MoE on consumer Blackwell (SM120)", "How it fits -- 2-bit
+// experts at FP4 quality", "The kernels": with many tokens per expert the FC
+// layers are a dense contraction (tensor-bound), not a weight stream.
+//
+// Weights.  A 2-bit weight times its block scale, q * s16 with q in {+-1, +-3}
+// and s16 an e4m3 value, has at most 6 significant bits, so it is exact in
+// bf16 and in tf32: the planes expand to an exact A operand of tcgen05.mma
+// (fp32 accumulation in TMEM); scale_2 is applied in the epilogue.  The NVFP4
+// delta (e2m1 code times an e4m3 scale, also exact) is expanded the same way
+// and accumulates into the same TMEM accumulator against a copy of the inputs
+// whose ungated rows are zero, so it only reaches gated pairs.
+//
+// Precision.  FC1 runs kind::f16 on bf16: x is bf16, so FC1 is exact up to
+// fp32 accumulation.  FC2 runs kind::tf32 on the fp32 h: rounding h to bf16
+// (2^-9) on top of the bf16 output would exceed the layer's max-error budget,
+// while tf32 keeps 10 mantissa bits of h at half the bf16 MMA rate.
+//
+// Layout.  FC1: a 32-bit TMEM column holds two bf16 of one row; column c of a
+// 32-weight group holds weights c and c + 16 (one shift-and-mask extracts the
+// sign and magnitude bits of both, a byte permute with sign replication turns
+// the magnitude bits into half-word masks).  The bucketing gather writes x in
+// the same K order.  FC2: one tf32 weight per column, natural K order, and h
+// in natural order.
+//
+// Pipeline: one persistent CTA per SM (16 warps) over (work item of <= 256
+// pairs x 128-row weight tile) units: warp 0 streams 256-weight chunks of the
+// planes (or delta) and 64-weight steps of the item's activation rows with
+// TMA (one lane per box); warps 8-15 expand each step's weights into a TMEM A
+// stage (two warps per 32-row quarter); warp 1 issues 4 MMAs
+// per step and commits; warp 2 prepares the unit records; warps 4-7 drain the
+// accumulator (FC1: SiLU(gate) * up -> fp32 h; FC2: times the routing weight ->
+// fp32 o).  Every wait is bounded.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cstring>
+
+#include "common.cuh"
+#include "moe_pf.cuh"
+#include "tc_common.cuh"
+
+namespace moet {
+namespace {
+
+constexpr int kPfThreads = 512;           // 16 warps, roles above
+constexpr int kPfConvWarps = 8;
+constexpr int kPC = 256;                  // weights per weight chunk
+// weights per step: 4 MMAs of K = 16 (bf16, FC1) or K = 8 (tf32, FC2); either way one step
+// is 32 TMEM columns of A and 128-byte activation rows
+template <bool FC1> __host__ __device__ constexpr int step_weights() { return FC1 ? 64 : 32; }
+constexpr int kPRing = 3;                 // weight chunks in flight
+constexpr int kBRing = 5;                 // activation steps in flight
+constexpr int kPAst = 4;                  // TMEM A stages
+constexpr int kPMeta = 2;                 // unit records in flight
+constexpr int kPTmemCols = 512;
+constexpr int kPColA = 256;               // D: columns 0..255; A stage s: kPColA + 32 s
+static_assert(kPColA + 32 * kPAst <= kPTmemCols, "TMEM columns");
+static_assert(kPAst <= kBRing, "an A stage is released by the done barrier of its step");
+// weight chunk stage: planes: sign [128 rows][32 B] (SW32) at 0, magnitude at 4096, row scales
+// [128][16 B] at 8192; delta: codes [128][128 B] (SW128) at 0, scales [128][16 B] at 16384
+constexpr int kPChunkBytes = 18432;
+constexpr int kBStepBytes = 32768;        // activation step: [<= 256 rows][128 B] (SW128)
+constexpr int kPBase = 0, kBBase = kPRing * kPChunkBytes;
+constexpr int kPXchg = kBBase + kBRing * kBStepBytes;
+
+struct PfMaps {
+  CUtensorMap sign, mag, q;      // planes u32 [E N, K/32] box {8, 64} SW32; s16 u8 [E N, K/16] box {16, 64}
+  CUtensorMap dcodes, ds4;       // delta u8 [S N, K/2] box {128, 64} SW128; scales box {16, 64}
+  CUtensorMap act, actg;         // activations bf16 [pairs, K] box {64, 64} SW128 (all / gated rows)
+};
+
+struct PfArgs {
+  int T, H, I, k, K, N, tiles;
+  const int32_t* offsets;
+  const int32_t* perm;
+  const float* topk_w;
+  const float* scale_2;
+  const int32_t* delta_slot;
+  int n_slots;
+  const uint8_t* gate;
+  const int* hdr;
+  const int4* chunks;
+  float* h;                      // FC1 output [pairs, I] (and its gated copy)
+  float* hg;
+  float* o;                      // FC2 output
+};
+
+struct PfMeta {
+  int e, pos0, ntok, ncols;
+  int dslot;                     // delta slot when the unit runs the delta pass, else -1
+  int nck;                       // weight chunks (K / 256, doubled with the delta pass)
+  int r0, r1;
+  float sc2;
+  int pad[7];
+  int pair[kPfTok];              // per column (token of the item): pair id t k + j, -1 = none
+  float wts[kPfTok];             // routing weight of the pair
+  uint8_t gated[kPfTok];         // 1 = the pair's token is gated
+};
+static_assert(sizeof(PfMeta) == 64 + 9 * kPfTok, "PfMeta layout");
+
+struct PfSmem {
+  uint64_t pfull[kPRing], pempty[kPRing];
+  uint64_t bfull[kBRing], bdone[kBRing];
+  uint64_t staged[kPAst];
+  uint64_t acc_full, acc_empty;
+  uint64_t meta_full[kPMeta], meta_empty[kPMeta];
+  PfMeta meta[kPMeta];
+  uint32_t tmem_base;
+  int stuck;
+};
+
+constexpr size_t kPfSmemBytes = 1024 + (size_t)kPXchg + 64 * 16 * sizeof(float) + sizeof(PfSmem);
+static_assert(kPfSmemBytes <= 232448, "shared memory over the per-CTA limit");
+
+__device__ __forceinline__ bool pf_stuck(const PfSmem& sm) {
+  return *reinterpret_cast<const volatile int*>(&sm.stuck) != 0;
+}
+
+// kind::f16 instruction descriptor: fp32 D, bf16 A and B, both K-major, M = 128.
+__device__ __forceinline__ uint32_t f16_idesc(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+// kind::tf32 instruction descriptor: fp32 D, tf32 A and B, both K-major, M = 128.
+__device__ __forceinline__ uint32_t tf32_idesc(int n) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+template <bool BF16>
+__device__ __forceinline__ void mma_ta(uint32_t d, uint32_t a_tmem, uint64_t bd, uint32_t idesc, uint32_t acc) {
+  if (BF16)
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d),
+        "r"(a_tmem), "l"(bd), "r"(idesc), "r"(acc));
+  else
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p; }" ::"r"(d),
+        "r"(a_tmem), "l"(bd), "r"(idesc), "r"(acc));
+}
+
+// bf16 bits of an e4m3 value and of three times it (both exact).
+__device__ __forceinline__ uint32_t bf16_bits(float f) { return __float_as_uint(f) >> 16; }
+
+// 32 weights (sign word S, magnitude word M) with block scales s0 (weights 0-15)
+// and s1 (16-31) -> 16 words: word j = bf16 (weight j) | bf16 (weight j + 16) << 16.
+__device__ __forceinline__ void planes_to_bf16(uint32_t S, uint32_t M, uint32_t s0, uint32_t s1, uint32_t out[16]) {
+  const float f0 = e4m3_to_f32(s0), f1 = e4m3_to_f32(s1);
+  const uint32_t a0 = bf16_bits(f0), b0 = bf16_bits(3.0f * f0);
+  const uint32_t a1 = bf16_bits(f1), b1 = bf16_bits(3.0f * f1);
+  const uint32_t one = a0 | (a1 << 16);                    // q = 1 in both halves
+  const uint32_t dif = (a0 ^ b0) | ((a1 ^ b1) << 16);      // q = 1 -> q = 3
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    // bits j and j + 16 moved to 15 and 31, the msb of bytes 1 and 3
+    const uint32_t mm = prmt(M << (15 - j), 0u, 0xBB99u);  // sign-replicated bytes -> half-word masks
+    const uint32_t ss = (S << (15 - j)) & 0x80008000u;
+    out[j] = (one ^ (mm & dif)) ^ ss;
+  }
+}
+
+// bf16 bits of an NVFP4 value: e2m1 code times an e4m3 scale (exact).
+__device__ __forceinline__ uint32_t e2m1_bf16(uint32_t code, float scale) {
+  return bf16_bits(e2m1_mag_value(code & 7u) * scale) | ((code & 8u) << 12);
+}
+
+// 32 delta codes (16 bytes: byte t = codes of weights 2t, 2t+1) with block scales s0, s1.
+__device__ __forceinline__ void delta_to_bf16(uint4 c, uint32_t s0, uint32_t s1, uint32_t out[16]) {
+  const float f0 = e4m3_to_f32(s0), f1 = e4m3_to_f32(s1);
+  const uint32_t lo[2] = {c.x, c.y}, hi[2] = {c.z, c.w};   // weights 0-15 and 16-31
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const uint32_t cl = (lo[j >> 3] >> (4 * (j & 7))) & 15u;
+    const uint32_t ch = (hi[j >> 3] >> (4 * (j & 7))) & 15u;
+    out[j] = e2m1_bf16(cl, f0) | (e2m1_bf16(ch, f1) << 16);
+  }
+}
+
+
+// ---------------------------------------------------------------- gather
+// xb[pos] = x[token of perm[pos]] in the permuted K order; xbg the same for
+// gated pairs, zero for the others.  Grid (pairs, ceil(H / 8 / 128)).
+__global__ void __launch_bounds__(128) pf_gather_kernel(int pairs, int k, int H, const uint16_t* __restrict__ x,
+                                                        const int32_t* __restrict__ perm,
+                                                        const uint8_t* __restrict__ gate, uint16_t* __restrict__ xb,
+                                                        uint16_t* __restrict__ xbg) {
+  const int pos = blockIdx.x;
+  const int t = blockIdx.y * 128 + threadIdx.x;              // 8 outputs: k' = 8 t .. 8 t + 7
+  if (t >= H / 8) return;
+  const int p = __ldg(perm + pos);
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  bool gated = false;
+  if (p >= 0 && p < pairs) {
+    const int tok = p / k;
+    gated = gate != nullptr && __ldg(gate + tok) != 0;
+    // k' = 32 g + 2 c + b holds weight 32 g + c + 16 b; this thread covers c = 4 q .. 4 q + 3
+    const int g = t >> 2, q = t & 3;
+    const uint16_t* row = x + (size_t)tok * H + 32 * g + 4 * q;
+    const uint2 lo = __ldg(reinterpret_cast<const uint2*>(row));
+    const uint2 hi = __ldg(reinterpret_cast<const uint2*>(row + 16));
+    v.x = (lo.x & 0xFFFFu) | (hi.x << 16);
+    v.y = (lo.x >> 16) | (hi.x & 0xFFFF0000u);
+    v.z = (lo.y & 0xFFFFu) | (hi.y << 16);
+    v.w = (lo.y >> 16) | (hi.y & 0xFFFF0000u);
+  } else {
+    record_error(MOET_ERR_DEVICE_INDEX);
+  }
+  reinterpret_cast<uint4*>(xb + (size_t)pos * H)[t] = v;
+  if (xbg != nullptr) reinterpret_cast<uint4*>(xbg + (size_t)pos * H)[t] = gated ? v : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// ---------------------------------------------------------------- FC kernel
+template <bool FC1>
+__global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, const __grid_constant__ PfMaps maps) {
+  extern __shared__ __align__(1024) unsigned char smem_dyn[];
+  unsigned char* base = smem_dyn + ((1024 - (smem_addr(smem_dyn) & 1023)) & 1023);
+  float (*xchg)[16] = reinterpret_cast<float (*)[16]>(base + kPXchg);
+  PfSmem& sm = *reinterpret_cast<PfSmem*>(base + kPXchg + 64 * 16 * sizeof(float));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int total_units = a.hdr[0] * a.tiles;
+  const int nunits = (int)blockIdx.x < total_units ? (total_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  if (nunits == 0) return;
+  const int nkc = a.K / kPC;                   // weight chunks of the main pass
+
+  if (tid == 0) {
+    sm.stuck = 0;
+    for (int s = 0; s < kPRing; ++s) { mbar_init(&sm.pfull[s], 1); mbar_init(&sm.pempty[s], kPfConvWarps); }
+    for (int s = 0; s < kBRing; ++s) { mbar_init(&sm.bfull[s], 1); mbar_init(&sm.bdone[s], 1); }
+    for (int s = 0; s < kPAst; ++s) mbar_init(&sm.staged[s], kPfConvWarps);
+    mbar_init(&sm.acc_full, 1);
+    mbar_init(&sm.acc_empty, 4);
+    for (int s = 0; s < kPMeta; ++s) { mbar_init(&sm.meta_full[s], 1); mbar_init(&sm.meta_empty[s], 4); }
+    asm volatile("fence.mbarrier_init.release.cluster;");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&sm.tmem_base)),
+                 "r"(kPTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;");
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 0) {
+    // ---------------- producer: one lane per TMA box
+    int gc = 0, gs = 0;
+    bool bad = false;
+    for (int j = 0; j < nunits && !bad; ++j) {
+      const int m = j % kPMeta;
+      if (!mbar_wait_warp(&sm.meta_full[m], (j / kPMeta) & 1)) { bad = true; break; }
+      const PfMeta& um = sm.meta[m];
+      const int pos0 = um.pos0, nck = um.nck, dslot = um.dslot;
+      const int nb = (um.ncols + 63) / 64;                 // 64-row activation boxes per step
+      const int w0 = um.e * a.N + um.r0, w1 = um.e * a.N + um.r1;
+      const int d0 = dslot * a.N + um.r0, d1 = dslot * a.N + um.r1;
+      for (int c = 0; c < nck && !bad; ++c, ++gc) {
+        const bool dp = c >= nkc;
+        const int cc = dp ? c - nkc : c;
+        const int ps = gc % kPRing;
+        if (gc >= kPRing && !mbar_wait_warp(&sm.pempty[ps], ((gc / kPRing) - 1) & 1)) { bad = true; break; }
+        unsigned char* pst = base + kPBase + ps * kPChunkBytes;
+        if (lane == 0) mbar_expect_tx(&sm.pfull[ps], dp ? 18432u : 10240u);
+        __syncwarp();
+        if (!dp) {
+          if (lane < 6) {
+            const int hv = lane & 1;
+            const CUtensorMap* map = lane < 2 ? &maps.sign : lane < 4 ? &maps.mag : &maps.q;
+            const int off = lane < 2 ? 2048 * hv : lane < 4 ? 4096 + 2048 * hv : 8192 + 1024 * hv;
+            tma_load_2d(smem_addr(pst + off), map, lane < 4 ? cc * 8 : cc * 16, hv ? w1 : w0, &sm.pfull[ps]);
+          }
+        } else {
+          if (lane < 4) {
+            const int hv = lane & 1;
+            const CUtensorMap* map = lane < 2 ? &maps.dcodes : &maps.ds4;
+            const int off = lane < 2 ? 8192 * hv : 16384 + 1024 * hv;
+            tma_load_2d(smem_addr(pst + off), map, lane < 2 ? cc * 128 : cc * 16, hv ? d1 : d0, &sm.pfull[ps]);
+          }
+        }
+        for (int s = 0; s < kPC / step_weights<FC1>(); ++s, ++gs) {
+          const int bs = gs % kBRing;
+          if (gs >= kBRing && !mbar_wait_warp(&sm.bdone[bs], ((gs / kBRing) - 1) & 1)) { bad = true; break; }
+          unsigned char* bst = base + kBBase + bs * kBStepBytes;
+          if (lane == 0) mbar_expect_tx(&sm.bfull[bs], (uint32_t)nb * 64u * 128u);
+          __syncwarp();
+          if (lane < nb)
+            tma_load_2d(smem_addr(bst + 8192 * lane), dp ? &maps.actg : &maps.act, cc * kPC + s * step_weights<FC1>(),
+                        pos0 + 64 * lane, &sm.bfull[bs]);
+        }
+      }
+    }
+    if (bad && lane == 0) atomicExch(&sm.stuck, 1);
+    if (lane == 0) {
+      // every copy this warp issued has landed before the CTA may exit
+      for (int i = gc > kPRing ? gc - kPRing : 0; i < gc; ++i) mbar_wait(&sm.pfull[i % kPRing], (i / kPRing) & 1);
+      for (int i = gs > kBRing ? gs - kBRing : 0; i < gs; ++i) mbar_wait(&sm.bfull[i % kBRing], (i / kBRing) & 1);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issue
+    if (lane == 0) {
+      int gs = 0, last = -1;
+      bool bad = false;
+      for (int j = 0; j < nunits && !bad; ++j) {
+        const int m = j % kPMeta;
+        if (!mbar_wait(&sm.meta_full[m], (j / kPMeta) & 1)) { bad = true; break; }
+        if (j >= 1 && !mbar_wait(&sm.acc_empty, (j - 1) & 1)) { bad = true; break; }
+        if (pf_stuck(sm)) { bad = true; break; }
+        asm volatile("tcgen05.fence::after_thread_sync;");
+        const int nst = sm.meta[m].nck * (kPC / step_weights<FC1>());
+        const uint32_t idesc = FC1 ? f16_idesc(sm.meta[m].ncols) : tf32_idesc(sm.meta[m].ncols);
+        for (int st = 0; st < nst; ++st, ++gs) {
+          const int as = gs % kPAst, bs = gs % kBRing;
+          if (!mbar_wait(&sm.staged[as], (gs / kPAst) & 1)) { bad = true; break; }
+          if (!mbar_wait(&sm.bfull[bs], (gs / kBRing) & 1)) { bad = true; break; }
+          asm volatile("tcgen05.fence::after_thread_sync;");
+          const uint32_t bsm = smem_addr(base + kBBase + bs * kBStepBytes);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            mma_ta<FC1>(tmem, tmem + kPColA + 32 * as + 8 * i, sw128_desc(bsm + 32 * i), idesc,
+                        (st > 0 || i > 0) ? 1u : 0u);
+          tc_commit(&sm.bdone[bs]);
+          last = gs;
+        }
+        if (bad) break;
+        tc_commit(&sm.acc_full);
+      }
+      if (bad) atomicExch(&sm.stuck, 1);
+      // every MMA this thread issued is complete before TMEM is released
+      if (last >= 0) mbar_wait(&sm.bdone[last % kBRing], (last / kBRing) & 1);
+    }
+  } else if (warp == 2) {
+    // ---------------- scheduler
+    for (int j = 0; j < nunits; ++j) {
+      const int m = j % kPMeta;
+      if (j >= kPMeta && !mbar_wait_warp(&sm.meta_empty[m], ((j / kPMeta) - 1) & 1)) {
+        if (lane == 0) atomicExch(&sm.stuck, 1);
+        break;
+      }
+      if (__any_sync(0xffffffffu, pf_stuck(sm))) break;
+      const int u = (int)blockIdx.x + j * (int)gridDim.x;
+      const int item = u / a.tiles, tile = u - item * a.tiles;
+      const int4 ch = a.chunks[item];
+      const int e = ch.x, ntok = ch.z;
+      const int pos0 = __ldg(a.offsets + e) + ch.y;
+      int dslot = -1;
+      if (a.delta_slot != nullptr && a.gate != nullptr) {
+        dslot = __ldg(a.delta_slot + e);
+        if (dslot >= a.n_slots) {
+          if (lane == 0) record_error(MOET_ERR_DEVICE_INDEX);
+          dslot = -1;
+        }
+      }
+      // per-column table of the item: pair id, routing weight, gate flag
+      PfMeta& um = sm.meta[m];
+      bool gated = false;
+      for (int t = lane; t < kPfTok; t += 32) {
+        int pr = -1;
+        float wv = 0.0f;
+        uint8_t gf = 0;
+        if (t < ntok) {
+          const int p = __ldg(a.perm + pos0 + t);
+          if (p < 0 || p >= a.T * a.k) {
+            record_error(MOET_ERR_DEVICE_INDEX);
+          } else {
+            pr = p;
+            wv = __ldg(a.topk_w + p);
+            if (a.gate != nullptr && __ldg(a.gate + p / a.k)) gf = 1;
+          }
+        }
+        um.pair[t] = pr;
+        um.wts[t] = wv;
+        um.gated[t] = gf;
+        gated = gated || gf != 0;
+      }
+      if (!__any_sync(0xffffffffu, gated)) dslot = -1;
+      if (lane == 0) {
+        um.e = e; um.pos0 = pos0; um.ntok = ntok;
+        um.ncols = ((ntok + 15) / 16) * 16;
+        um.dslot = dslot;
+        um.nck = dslot >= 0 ? 2 * nkc : nkc;
+        um.r0 = FC1 ? tile * 64 : tile * 128;
+        um.r1 = FC1 ? a.I + tile * 64 : tile * 128 + 64;
+        um.sc2 = __ldg(a.scale_2 + e);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.meta_full[m]);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------- epilogue: TMEM lane quarter warp & 3
+    const int trow = 32 * (warp & 3) + lane;
+    const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;
+    for (int j = 0; j < nunits; ++j) {
+      const int m = j % kPMeta;
+      bool ok = mbar_wait_warp(&sm.meta_full[m], (j / kPMeta) & 1);
+      ok = ok && mbar_wait_warp(&sm.acc_full, j & 1);
+      asm volatile("tcgen05.fence::after_thread_sync;");
+      if (epi_any(!ok || pf_stuck(sm))) {
+        if (!ok && lane == 0) atomicExch(&sm.stuck, 1);
+        break;
+      }
+      const PfMeta& um = sm.meta[m];
+      const int ncols = um.ncols, ntok = um.ntok, pos0 = um.pos0;
+      const float sc2 = um.sc2;
+      const int dslot_unit = a.hg != nullptr ? um.dslot : -1;
+      const int wrow = trow < 64 ? um.r0 + trow : um.r1 + trow - 64;
+      for (int c0 = 0; c0 < ncols; c0 += 16) {
+        float v[16];
+        tmem_ld16(tmem + lane_q + c0, v);
+        if (!FC1) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int col = c0 + i;
+            const int p = um.pair[col];
+            if (col < ntok && p >= 0) a.o[(size_t)p * a.H + wrow] = v[i] * sc2 * um.wts[col];
+          }
+        } else {
+          if (trow >= 64) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) xchg[trow - 64][i] = v[i];
+          }
+          asm volatile("bar.sync 1, 128;");
+          if (trow < 64) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int col = c0 + i;
+              if (col < ntok) {
+                const float g = v[i] * sc2, u = xchg[trow][i] * sc2;
+                const float hv = g / (1.0f + expf(-g)) * u;
+                const size_t at = (size_t)(pos0 + col) * a.I + wrow;
+                a.h[at] = hv;
+                // the gated copy feeds FC2's delta pass, which runs for exactly these units
+                if (dslot_unit >= 0) a.hg[at] = um.gated[col] ? hv : 0.0f;
+              }
+            }
+          }
+          asm volatile("bar.sync 1, 128;");
+        }
+      }
+      asm volatile("tcgen05.fence::before_thread_sync;");
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&sm.acc_empty);
+        mbar_arrive(&sm.meta_empty[m]);
+      }
+    }
+  } else if (warp >= 8) {
+    // ---------------- converters: two warps per 32-row quarter; half h fills TMEM
+    // columns 16 h .. 16 h + 15 of each step's A stage for its row
+    const int half = (warp - 8) >> 2;
+    const int trow = 32 * (warp & 3) + lane;
+    const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;
+    int gc = 0, gs = 0;
+    bool bad = false;
+    for (int j = 0; j < nunits && !bad; ++j) {
+      const int m = j % kPMeta;
+      if (!mbar_wait_warp(&sm.meta_full[m], (j / kPMeta) & 1)) { bad = true; break; }
+      if (__any_sync(0xffffffffu, pf_stuck(sm))) { bad = true; break; }
+      const int nck = sm.meta[m].nck;
+      for (int c = 0; c < nck && !bad; ++c, ++gc) {
+        const int ps = gc % kPRing;
+        if (!mbar_wait_warp(&sm.pfull[ps], (gc / kPRing) & 1)) { bad = true; break; }
+        const unsigned char* pst = base + kPBase + ps * kPChunkBytes;
+        const bool dp = c >= nkc;
+        constexpr int kSteps = kPC / step_weights<FC1>();
+        for (int s = 0; s < kSteps; ++s, ++gs) {
+          const int as = gs % kPAst;
+          // the A stage is free once the MMAs of step gs - kPAst are done
+          if (gs >= kPAst && !mbar_wait_warp(&sm.bdone[(gs - kPAst) % kBRing], ((gs - kPAst) / kBRing) & 1)) {
+            bad = true;
+            break;
+          }
+          // the 32-weight group of the chunk this thread expands: FC1 2 s + half (bf16 pairs of
+          // weights c and c + 16), FC2 s (tf32, weights 16 half .. 16 half + 15)
+          const int wi = FC1 ? 2 * s + half : s;
+          const uint32_t sc = *reinterpret_cast<const uint16_t*>(pst + (dp ? 16384 : 8192) + trow * 16 + 2 * wi);
+          const uint32_t s0 = sc & 0xFFu, s1 = sc >> 8;
+          uint32_t av[16];
+          if (!dp) {
+            // 32-byte-swizzled plane rows: 16-byte piece p of row r at p ^ ((r >> 2) & 1)
+            const int wo = trow * 32 + ((((wi >> 2) ^ ((trow >> 2) & 1))) << 4) + 4 * (wi & 3);
+            planes_to_bf16(*reinterpret_cast<const uint32_t*>(pst + wo),
+                           *reinterpret_cast<const uint32_t*>(pst + 4096 + wo), s0, s1, av);
+          } else {
+            // 128-byte-swizzled code rows: piece p of row r at p ^ (r & 7)
+            delta_to_bf16(*reinterpret_cast<const uint4*>(pst + trow * 128 + ((wi ^ (trow & 7)) << 4)), s0, s1, av);
+          }
+          if (!FC1) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) av[j] = half ? (av[j] & 0xFFFF0000u) : (av[j] << 16);
+          }
+          tmem_st16(tmem + lane_q + kPColA + 32 * as + 16 * half, av);
+          asm volatile("tcgen05.wait::st.sync.aligned;");
+          asm volatile("tcgen05.fence::before_thread_sync;");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.staged[as]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.pempty[ps]);
+      }
+    }
+    if (bad && lane == 0) atomicExch(&sm.stuck, 1);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    asm volatile("tcgen05.fence::after_thread_sync;");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kPTmemCols));
+  }
+  if (tid == 0 && pf_stuck(sm)) record_error(MOET_ERR_TIMEOUT);
+}
+
+// ---------------------------------------------------------------- host side
+template <bool FC1>
+moet_status launch_pf(const PfArgs& a, const moet_planes* pl, const moet_nvfp4* dl, const void* act,
+                      const void* actg, int pairs, int E, cudaStream_t st) {
+  PfMaps m;
+  std::memset(&m, 0, sizeof(m));
+  const uint64_t rowsW = (uint64_t)E * a.N, K = (uint64_t)a.K;
+  bool ok = make_map(&m.sign, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, pl->sign, rowsW, K / 32, 8, 64, CU_TENSOR_MAP_SWIZZLE_32B) &&
+            make_map(&m.mag, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, pl->mag, rowsW, K / 32, 8, 64, CU_TENSOR_MAP_SWIZZLE_32B) &&
+            make_map(&m.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pl->s16, rowsW, K / 16, 16, 64, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+            (FC1 ? make_map(&m.act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, act, (uint64_t)pairs, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)
+                 : make_map(&m.act, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, act, (uint64_t)pairs, K, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B));
+  if (ok && a.delta_slot != nullptr) {
+    const uint64_t rowsD = (uint64_t)a.n_slots * a.N;
+    ok = make_map(&m.dcodes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dl->codes, rowsD, K / 2, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_map(&m.ds4, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dl->s4, rowsD, K / 16, 16, 64, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+         (FC1 ? make_map(&m.actg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, actg, (uint64_t)pairs, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)
+              : make_map(&m.actg, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, actg, (uint64_t)pairs, K, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B));
+  }
+  if (!ok) return MOET_ERR_CUDA;
+  const int grid = sm_count();
+  if (grid <= 0) return MOET_ERR_CUDA;
+  auto kern = pf_fc_kernel<FC1>;
+  MOET_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPfSmemBytes));
+  {
+    ProfScope ps(FC1 ? MOET_K_FC1 : MOET_K_FC2, st);
+    kern<<<grid, kPfThreads, kPfSmemBytes, st>>>(a, m);
+  }
+  MOET_CUDA_TRY(cudaGetLastError());
+  return MOET_OK;
+}
+
+}  // namespace
+
+moet_status pf_forward(const PfForwardArgs& f, cudaStream_t st) {
+  const int pairs = f.T * f.k;
+  const bool with_delta = f.delta_slot != nullptr && f.gate != nullptr;
+  {
+    ProfScope ps(MOET_K_TERMS, st);
+    const dim3 grid(pairs, (f.H / 8 + 127) / 128);
+    pf_gather_kernel<<<grid, 128, 0, st>>>(pairs, f.k, f.H, f.x, f.perm, with_delta ? f.gate : nullptr, f.xb,
+                                           with_delta ? f.xbg : nullptr);
+  }
+  MOET_CUDA_TRY(cudaGetLastError());
+  PfArgs a{};
+  a.T = f.T; a.H = f.H; a.I = f.I; a.k = f.k;
+  a.offsets = f.offsets; a.perm = f.perm; a.topk_w = f.topk_w;
+  a.delta_slot = with_delta ? f.delta_slot : nullptr; a.n_slots = f.n_slots;
+  a.gate = with_delta ? f.gate : nullptr;
+  a.hdr = f.hdr; a.chunks = f.chunks;
+  PfArgs a1 = a;
+  a1.K = f.H; a1.N = 2 * f.I; a1.tiles = f.I / 64;
+  a1.scale_2 = f.fc1->scale_2;
+  a1.h = f.h; a1.hg = with_delta ? f.hg : nullptr;
+  moet_status s = launch_pf<true>(a1, f.fc1, f.dfc1, f.xb, f.xbg, pairs, f.E, st);
+  if (s != MOET_OK) return s;
+  PfArgs a2 = a;
+  a2.K = f.I; a2.N = f.H; a2.tiles = f.H / 128;
+  a2.scale_2 = f.fc2->scale_2;
+  a2.o = f.o;
+  return launch_pf<false>(a2, f.fc2, f.dfc2, f.h, f.hg, pairs, f.E, st);
+}
+
+}  // namespace moet
+
+MOET_ERROR_ACCESSOR(moet_internal_error_moe_pf)

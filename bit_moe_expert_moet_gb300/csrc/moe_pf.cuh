@@ -1,0 +1,48 @@
+// Internal interface between the forward's entry point (moe.cu) and the
+// tcgen05 bf16 engine for large token counts (moe_pf.cu).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/moet.h"
+
+namespace moet {
+
+constexpr int kPfTok = 256;   // routed pairs per work item -> MMA N <= 256
+
+// True when the bf16 engine handles this layer shape.
+inline bool pf_supported(int H, int I) { return H % 256 == 0 && I % 256 == 0; }
+
+// Bytes of the engine's extra activation buffers for `pairs` routed pairs: x in
+// bucketed order as bf16 plus its gated copy (rows of ungated pairs zero), and
+// the gated copy of h (fp32; h itself is the forward's h buffer).
+inline size_t pf_act_bytes(size_t pairs, size_t H, size_t I) {
+  return pairs * H * 2 * sizeof(uint16_t) + pairs * I * sizeof(float);
+}
+
+struct PfForwardArgs {
+  int T, H, I, E, k;
+  const uint16_t* x;
+  const int32_t* offsets;
+  const int32_t* perm;
+  const float* topk_w;
+  const moet_planes* fc1;
+  const moet_planes* fc2;
+  const int32_t* delta_slot;   // nullable
+  int n_slots;
+  const moet_nvfp4* dfc1;
+  const moet_nvfp4* dfc2;
+  const uint8_t* gate;         // nullable
+  const int* hdr;              // [0] = number of work items
+  const int4* chunks;          // (expert, first pair, count <= kPfTok)
+  uint16_t* xb;                // [T k, H] bf16, bucketed rows, K permuted within 32-groups
+  uint16_t* xbg;               // same, rows of ungated pairs zero
+  float* h;                    // [T k, I] fp32, FC1 output (bucketed rows, natural order)
+  float* hg;                   // same, rows of ungated pairs zero
+  float* o;                    // [T k, H] pair order
+};
+
+moet_status pf_forward(const PfForwardArgs& a, cudaStream_t st);
+
+}  // namespace moet

@@ -309,10 +309,12 @@ def _full_layer(moet, cfg, dset, rng):
     return ref, gp
 
 
-@pytest.mark.parametrize("name,tokens", [("dsv3_decode_t64", [0, 37]), ("glm_decode", [3])])
+@pytest.mark.parametrize("name,tokens", [("dsv3_decode_t64", [0, 37]), ("glm_decode", [3]), ("dsv3_prefill", None)])
 def test_forward_full_size_sampled(moet, name, tokens):
     cfg = W.CONFIGS[name]
     logits, xb, dset, gate = W.draw_layer_inputs(cfg)
+    if tokens is None:   # prefill-sized batch: one ungated token and two gated ones (delta pass)
+        tokens = [int(np.flatnonzero(gate == 0)[0])] + [int(t) for t in np.flatnonzero(gate == 1)[:2]]
     rng = np.random.default_rng(50)
     ref, gp = _full_layer(moet, cfg, dset, rng)
     yg, err = _run_forward(moet, logits, xb, cfg.k, gp, cfg.E, cfg.H, dset, gate)
