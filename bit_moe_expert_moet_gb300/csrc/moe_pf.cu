@@ -24,10 +24,10 @@
 // the same K order.  FC2: one tf32 weight per column, natural K order, and h
 // in natural order.
 //
-// Pipeline: one persistent CTA per SM (16 warps) over (work item of <= 256
+// Pipeline: one persistent CTA per SM (20 warps) over (work item of <= 256
 // pairs x 128-row weight tile) units: warp 0 streams 256-weight chunks of the
-// planes (or delta) and 64-weight steps of the item's activation rows with
-// TMA (one lane per box); warps 8-15 expand each step's weights into a TMEM A
+// planes (or delta) and warps 3, 16-18 take turns streaming the steps of the
+// item's activation rows, with TMA (one lane per box); warps 8-15 expand each step's weights into a TMEM A
 // stage (two warps per 32-row quarter); warp 1 issues 4 MMAs
 // per step and commits; warp 2 prepares the unit records; warps 4-7 drain the
 // accumulator (FC1: SiLU(gate) * up -> fp32 h; FC2: times the routing weight ->
@@ -44,7 +44,8 @@
 namespace moet {
 namespace {
 
-constexpr int kPfThreads = 512;           // 16 warps, roles above
+constexpr int kPfThreads = 640;           // 20 warps, roles above
+constexpr int kBProd = 4;                 // activation producer warps (3, 16, 17, 18), steps in turn
 constexpr int kPfConvWarps = 8;
 constexpr int kPC = 256;                  // weights per weight chunk
 // weights per step: 4 MMAs of K = 16 (bf16, FC1) or K = 8 (tf32, FC2); either way one step
@@ -58,6 +59,7 @@ constexpr int kPTmemCols = 512;
 constexpr int kPColA = 256;               // D: columns 0..255; A stage s: kPColA + 32 s
 static_assert(kPColA + 32 * kPAst <= kPTmemCols, "TMEM columns");
 static_assert(kPAst <= kBRing, "an A stage is released by the done barrier of its step");
+static_assert(kPAst % 2 == 0, "the MMA thread takes steps in pairs");
 // weight chunk stage: planes: sign [128 rows][32 B] (SW32) at 0, magnitude at 4096, row scales
 // [128][16 B] at 8192; delta: codes [128][128 B] (SW128) at 0, scales [128][16 B] at 16384
 constexpr int kPChunkBytes = 18432;
@@ -245,8 +247,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
   asm volatile("tcgen05.fence::after_thread_sync;");
   const uint32_t tmem = sm.tmem_base;
 
-  if (warp == 0) {
-    // ---------------- producer: one lane per TMA box
+  const int bprod = warp == 3 ? 0 : (warp >= 16 && warp < 16 + kBProd - 1) ? warp - 15 : -1;
+  if (warp == 0 || bprod >= 0) {
+    // ---------------- producers, one lane per TMA box: warp 0 streams the weight chunks,
+    // the activation producers take the 64-row activation steps in turn
     int gc = 0, gs = 0;
     bool bad = false;
     for (int j = 0; j < nunits && !bad; ++j) {
@@ -260,27 +264,31 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
       for (int c = 0; c < nck && !bad; ++c, ++gc) {
         const bool dp = c >= nkc;
         const int cc = dp ? c - nkc : c;
-        const int ps = gc % kPRing;
-        if (gc >= kPRing && !mbar_wait_warp(&sm.pempty[ps], ((gc / kPRing) - 1) & 1)) { bad = true; break; }
-        unsigned char* pst = base + kPBase + ps * kPChunkBytes;
-        if (lane == 0) mbar_expect_tx(&sm.pfull[ps], dp ? 18432u : 10240u);
-        __syncwarp();
-        if (!dp) {
-          if (lane < 6) {
-            const int hv = lane & 1;
-            const CUtensorMap* map = lane < 2 ? &maps.sign : lane < 4 ? &maps.mag : &maps.q;
-            const int off = lane < 2 ? 2048 * hv : lane < 4 ? 4096 + 2048 * hv : 8192 + 1024 * hv;
-            tma_load_2d(smem_addr(pst + off), map, lane < 4 ? cc * 8 : cc * 16, hv ? w1 : w0, &sm.pfull[ps]);
+        if (warp == 0) {
+          const int ps = gc % kPRing;
+          if (gc >= kPRing && !mbar_wait_warp(&sm.pempty[ps], ((gc / kPRing) - 1) & 1)) { bad = true; break; }
+          unsigned char* pst = base + kPBase + ps * kPChunkBytes;
+          if (lane == 0) mbar_expect_tx(&sm.pfull[ps], dp ? 18432u : 10240u);
+          __syncwarp();
+          if (!dp) {
+            if (lane < 6) {
+              const int hv = lane & 1;
+              const CUtensorMap* map = lane < 2 ? &maps.sign : lane < 4 ? &maps.mag : &maps.q;
+              const int off = lane < 2 ? 2048 * hv : lane < 4 ? 4096 + 2048 * hv : 8192 + 1024 * hv;
+              tma_load_2d(smem_addr(pst + off), map, lane < 4 ? cc * 8 : cc * 16, hv ? w1 : w0, &sm.pfull[ps]);
+            }
+          } else {
+            if (lane < 4) {
+              const int hv = lane & 1;
+              const CUtensorMap* map = lane < 2 ? &maps.dcodes : &maps.ds4;
+              const int off = lane < 2 ? 8192 * hv : 16384 + 1024 * hv;
+              tma_load_2d(smem_addr(pst + off), map, lane < 2 ? cc * 128 : cc * 16, hv ? d1 : d0, &sm.pfull[ps]);
+            }
           }
-        } else {
-          if (lane < 4) {
-            const int hv = lane & 1;
-            const CUtensorMap* map = lane < 2 ? &maps.dcodes : &maps.ds4;
-            const int off = lane < 2 ? 8192 * hv : 16384 + 1024 * hv;
-            tma_load_2d(smem_addr(pst + off), map, lane < 2 ? cc * 128 : cc * 16, hv ? d1 : d0, &sm.pfull[ps]);
-          }
+          continue;
         }
         for (int s = 0; s < kPC / step_weights<FC1>(); ++s, ++gs) {
+          if (gs % kBProd != bprod) continue;
           const int bs = gs % kBRing;
           if (gs >= kBRing && !mbar_wait_warp(&sm.bdone[bs], ((gs / kBRing) - 1) & 1)) { bad = true; break; }
           unsigned char* bst = base + kBBase + bs * kBStepBytes;
@@ -295,8 +303,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
     if (bad && lane == 0) atomicExch(&sm.stuck, 1);
     if (lane == 0) {
       // every copy this warp issued has landed before the CTA may exit
-      for (int i = gc > kPRing ? gc - kPRing : 0; i < gc; ++i) mbar_wait(&sm.pfull[i % kPRing], (i / kPRing) & 1);
-      for (int i = gs > kBRing ? gs - kBRing : 0; i < gs; ++i) mbar_wait(&sm.bfull[i % kBRing], (i / kBRing) & 1);
+      if (warp == 0)
+        for (int i = gc > kPRing ? gc - kPRing : 0; i < gc; ++i) mbar_wait(&sm.pfull[i % kPRing], (i / kPRing) & 1);
+      else
+        for (int i = gs > kBRing ? gs - kBRing : 0; i < gs; ++i)
+          if (i % kBProd == bprod) mbar_wait(&sm.bfull[i % kBRing], (i / kBRing) & 1);
     }
   } else if (warp == 1) {
     // ---------------- MMA issue
@@ -311,18 +322,23 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
         asm volatile("tcgen05.fence::after_thread_sync;");
         const int nst = sm.meta[m].nck * (kPC / step_weights<FC1>());
         const uint32_t idesc = FC1 ? f16_idesc(sm.meta[m].ncols) : tf32_idesc(sm.meta[m].ncols);
-        for (int st = 0; st < nst; ++st, ++gs) {
-          const int as = gs % kPAst, bs = gs % kBRing;
-          if (!mbar_wait(&sm.staged[as], (gs / kPAst) & 1)) { bad = true; break; }
-          if (!mbar_wait(&sm.bfull[bs], (gs / kBRing) & 1)) { bad = true; break; }
+        // two steps per iteration: staged of the second step implies the first (every converter
+        // warp arrives for its steps in order), so one wait covers 8 MMAs
+        for (int st = 0; st < nst; st += 2, gs += 2) {
+          if (!mbar_wait(&sm.staged[(gs + 1) % kPAst], ((gs + 1) / kPAst) & 1)) { bad = true; break; }
           asm volatile("tcgen05.fence::after_thread_sync;");
-          const uint32_t bsm = smem_addr(base + kBBase + bs * kBStepBytes);
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            mma_ta<FC1>(tmem, tmem + kPColA + 32 * as + 8 * i, sw128_desc(bsm + 32 * i), idesc,
-                        (st > 0 || i > 0) ? 1u : 0u);
-          tc_commit(&sm.bdone[bs]);
-          last = gs;
+          for (int h = 0; h < 2; ++h) {
+            const int as = (gs + h) % kPAst, bs = (gs + h) % kBRing;
+            const uint32_t bsm = smem_addr(base + kBBase + bs * kBStepBytes);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              mma_ta<FC1>(tmem, tmem + kPColA + 32 * as + 8 * i, sw128_desc(bsm + 32 * i), idesc,
+                          (st > 0 || h > 0 || i > 0) ? 1u : 0u);
+          }
+          tc_commit(&sm.bdone[gs % kBRing]);
+          tc_commit(&sm.bdone[(gs + 1) % kBRing]);
+          last = gs + 1;
         }
         if (bad) break;
         tc_commit(&sm.acc_full);
@@ -446,7 +462,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
         mbar_arrive(&sm.meta_empty[m]);
       }
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 8 && warp < 16) {
     // ---------------- converters: two warps per 32-row quarter; half h fills TMEM
     // columns 16 h .. 16 h + 15 of each step's A stage for its row
     const int half = (warp - 8) >> 2;
@@ -494,6 +510,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
           tmem_st16(tmem + lane_q + kPColA + 32 * as + 16 * half, av);
           asm volatile("tcgen05.wait::st.sync.aligned;");
           asm volatile("tcgen05.fence::before_thread_sync;");
+          // the step is staged only once its activations have landed as well
+          if (!mbar_wait_warp(&sm.bfull[gs % kBRing], (gs / kBRing) & 1)) { bad = true; break; }
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.staged[as]);
         }
