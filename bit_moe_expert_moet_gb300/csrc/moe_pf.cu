@@ -164,23 +164,51 @@ __device__ __forceinline__ void planes_to_bf16(uint32_t S, uint32_t M, uint32_t 
   }
 }
 
-// bf16 bits of an NVFP4 value: e2m1 code times an e4m3 scale (exact).
-__device__ __forceinline__ uint32_t e2m1_bf16(uint32_t code, float scale) {
-  return bf16_bits(e2m1_mag_value(code & 7u) * scale) | ((code & 8u) << 12);
+// e2m1 magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6} as bf16, split into byte tables for prmt
+// (first word: codes 0-3, second: codes 4-7)
+constexpr uint32_t kE2m1LoA = 0xC0800000u, kE2m1LoB = 0xC0804000u;   // low bytes
+constexpr uint32_t kE2m1HiA = 0x3F3F3F00u, kE2m1HiB = 0x40404040u;   // high bytes
+
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
-// 32 delta codes (16 bytes: byte t = codes of weights 2t, 2t+1) with block scales s0, s1.
+// Two e2m1 codes (bits 0-3 and 8-11 of c) times the bf16x2 scales sc -> bf16x2 (exact: a code
+// value has 2 significant bits, an e4m3 scale 4).
+__device__ __forceinline__ uint32_t e2m1x2_bf16(uint32_t c, uint32_t sc) {
+  const uint32_t sel = c & 0x0707u;
+  const uint32_t mag = prmt(kE2m1LoA, kE2m1LoB, sel) | (prmt(kE2m1HiA, kE2m1HiB, sel) << 8);
+  return mul_bf16x2(mag, sc) ^ (((c & 0x0008u) << 12) | ((c & 0x0800u) << 20));
+}
+
+// FC1: 32 delta codes (16 bytes: byte t = codes of weights 2t, 2t+1, low nibble first) with
+// block scales s0 (weights 0-15), s1 (16-31) -> word j = bf16 (weight j) | bf16 (weight j + 16) << 16.
 __device__ __forceinline__ void delta_to_bf16(uint4 c, uint32_t s0, uint32_t s1, uint32_t out[16]) {
-  const float f0 = e4m3_to_f32(s0), f1 = e4m3_to_f32(s1);
-  const uint32_t lo[2] = {c.x, c.y}, hi[2] = {c.z, c.w};   // weights 0-15 and 16-31
+  const uint32_t sc = bf16_bits(e4m3_to_f32(s0)) | (bf16_bits(e4m3_to_f32(s1)) << 16);
+  const uint32_t lo[2] = {c.x, c.y}, hi[2] = {c.z, c.w};
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    const uint32_t cl = (lo[j >> 3] >> (4 * (j & 7))) & 15u;
-    const uint32_t ch = (hi[j >> 3] >> (4 * (j & 7))) & 15u;
-    out[j] = e2m1_bf16(cl, f0) | (e2m1_bf16(ch, f1) << 16);
+    const int sh = 4 * (j & 7);
+    out[j] = e2m1x2_bf16(((lo[j >> 3] >> sh) & 15u) | (((hi[j >> 3] >> sh) & 15u) << 8), sc);
   }
 }
 
+// FC2: the 16 delta codes of one half-group (8 bytes) with its block scale -> fp32 (tf32) bits of
+// its weights, one per word, in K order.
+__device__ __forceinline__ void delta_to_tf32(uint2 c, uint32_t s, uint32_t out[16]) {
+  const uint32_t b = bf16_bits(e4m3_to_f32(s));
+  const uint32_t sc = b | (b << 16);
+  const uint32_t w[2] = {c.x, c.y};
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    const uint32_t byte = (w[t >> 2] >> (8 * (t & 3))) & 0xFFu;
+    const uint32_t v = e2m1x2_bf16((byte & 15u) | ((byte >> 4) << 8), sc);
+    out[2 * t] = v << 16;
+    out[2 * t + 1] = v & 0xFFFF0000u;
+  }
+}
 
 // ---------------------------------------------------------------- gather
 // xb[pos] = x[token of perm[pos]] in the permuted K order; xbg the same for
@@ -219,7 +247,7 @@ template <bool FC1>
 __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, const __grid_constant__ PfMaps maps) {
   extern __shared__ __align__(1024) unsigned char smem_dyn[];
   unsigned char* base = smem_dyn + ((1024 - (smem_addr(smem_dyn) & 1023)) & 1023);
-  float (*xchg)[16] = reinterpret_cast<float (*)[16]>(base + kPXchg);
+  float (*xchg)[64] = reinterpret_cast<float (*)[64]>(base + kPXchg);   // [16 columns][64 rows]
   PfSmem& sm = *reinterpret_cast<PfSmem*>(base + kPXchg + 64 * 16 * sizeof(float));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int total_units = a.hdr[0] * a.tiles;
@@ -433,26 +461,41 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
             if (col < ntok && p >= 0) a.o[(size_t)p * a.H + wrow] = v[i] * sc2 * um.wts[col];
           }
         } else {
-          if (trow >= 64) {
+          // SiLU(gate) * up: the gate rows (quarters 0-1) finish columns c0 .. c0 + 7, the up rows
+          // (quarters 2-3) columns c0 + 8 .. c0 + 15; each side hands the other its half
+          const int r = trow & 63;
+          const bool up = trow >= 64;
+          if (up) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) xchg[trow - 64][i] = v[i];
+            for (int i = 0; i < 8; ++i) xchg[i][r] = v[i];
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) xchg[8 + i][r] = v[8 + i];
           }
-          asm volatile("bar.sync 1, 128;");
-          if (trow < 64) {
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          float g[8], u[8];
+          if (up) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int col = c0 + i;
-              if (col < ntok) {
-                const float g = v[i] * sc2, u = xchg[trow][i] * sc2;
-                const float hv = g / (1.0f + expf(-g)) * u;
-                const size_t at = (size_t)(pos0 + col) * a.I + wrow;
-                a.h[at] = hv;
-                // the gated copy feeds FC2's delta pass, which runs for exactly these units
-                if (dslot_unit >= 0) a.hg[at] = um.gated[col] ? hv : 0.0f;
-              }
+            for (int i = 0; i < 8; ++i) { g[i] = xchg[8 + i][r]; u[i] = v[8 + i]; }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) { g[i] = v[i]; u[i] = xchg[i][r]; }
+          }
+          const int cb = c0 + (up ? 8 : 0);
+          const int hcol = um.r0 + r;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int col = cb + i;
+            if (col < ntok) {
+              const float gv = g[i] * sc2, uv = u[i] * sc2;
+              const float hv = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+              const size_t at = (size_t)(pos0 + col) * a.I + hcol;
+              a.h[at] = hv;
+              // the gated copy feeds FC2's delta pass, which runs for exactly these units
+              if (dslot_unit >= 0) a.hg[at] = um.gated[col] ? hv : 0.0f;
             }
           }
-          asm volatile("bar.sync 1, 128;");
+          asm volatile("bar.sync 1, 128;" ::: "memory");
         }
       }
       asm volatile("tcgen05.fence::before_thread_sync;");
@@ -499,13 +542,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
             const int wo = trow * 32 + ((((wi >> 2) ^ ((trow >> 2) & 1))) << 4) + 4 * (wi & 3);
             planes_to_bf16(*reinterpret_cast<const uint32_t*>(pst + wo),
                            *reinterpret_cast<const uint32_t*>(pst + 4096 + wo), s0, s1, av);
+            if (!FC1) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) av[j] = half ? (av[j] & 0xFFFF0000u) : (av[j] << 16);
+            }
           } else {
             // 128-byte-swizzled code rows: piece p of row r at p ^ (r & 7)
-            delta_to_bf16(*reinterpret_cast<const uint4*>(pst + trow * 128 + ((wi ^ (trow & 7)) << 4)), s0, s1, av);
-          }
-          if (!FC1) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) av[j] = half ? (av[j] & 0xFFFF0000u) : (av[j] << 16);
+            const unsigned char* cp = pst + trow * 128 + ((wi ^ (trow & 7)) << 4);
+            if (FC1)
+              delta_to_bf16(*reinterpret_cast<const uint4*>(cp), s0, s1, av);
+            else
+              delta_to_tf32(*reinterpret_cast<const uint2*>(cp + 8 * half), half ? s1 : s0, av);
           }
           tmem_st16(tmem + lane_q + kPColA + 32 * as + 16 * half, av);
           asm volatile("tcgen05.wait::st.sync.aligned;");
