@@ -53,12 +53,11 @@ constexpr int kPC = 256;                  // weights per weight chunk
 template <bool FC1> __host__ __device__ constexpr int step_weights() { return FC1 ? 64 : 32; }
 constexpr int kPRing = 3;                 // weight chunks in flight
 constexpr int kBRing = 5;                 // activation steps in flight
-constexpr int kPAst = 4;                  // TMEM A stages
+constexpr int kPAst = 8;                  // TMEM A stages (released in pairs)
 constexpr int kPMeta = 2;                 // unit records in flight
 constexpr int kPTmemCols = 512;
 constexpr int kPColA = 256;               // D: columns 0..255; A stage s: kPColA + 32 s
 static_assert(kPColA + 32 * kPAst <= kPTmemCols, "TMEM columns");
-static_assert(kPAst <= kBRing, "an A stage is released by the done barrier of its step");
 static_assert(kPAst % 2 == 0, "the MMA thread takes steps in pairs");
 // weight chunk stage: planes: sign [128 rows][32 B] (SW32) at 0, magnitude at 4096, row scales
 // [128][16 B] at 8192; delta: codes [128][128 B] (SW128) at 0, scales [128][16 B] at 16384
@@ -106,6 +105,7 @@ struct PfSmem {
   uint64_t pfull[kPRing], pempty[kPRing];
   uint64_t bfull[kBRing], bdone[kBRing];
   uint64_t staged[kPAst];
+  uint64_t adone[kPAst / 2];      // MMAs of a pair of steps done: their A stages are free
   uint64_t acc_full, acc_empty;
   uint64_t meta_full[kPMeta], meta_empty[kPMeta];
   PfMeta meta[kPMeta];
@@ -260,6 +260,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
     for (int s = 0; s < kPRing; ++s) { mbar_init(&sm.pfull[s], 1); mbar_init(&sm.pempty[s], kPfConvWarps); }
     for (int s = 0; s < kBRing; ++s) { mbar_init(&sm.bfull[s], 1); mbar_init(&sm.bdone[s], 1); }
     for (int s = 0; s < kPAst; ++s) mbar_init(&sm.staged[s], kPfConvWarps);
+    for (int s = 0; s < kPAst / 2; ++s) mbar_init(&sm.adone[s], 1);
     mbar_init(&sm.acc_full, 1);
     mbar_init(&sm.acc_empty, 4);
     for (int s = 0; s < kPMeta; ++s) { mbar_init(&sm.meta_full[s], 1); mbar_init(&sm.meta_empty[s], 4); }
@@ -351,9 +352,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
         const int nst = sm.meta[m].nck * (kPC / step_weights<FC1>());
         const uint32_t idesc = FC1 ? f16_idesc(sm.meta[m].ncols) : tf32_idesc(sm.meta[m].ncols);
         // two steps per iteration: staged of the second step implies the first (every converter
-        // warp arrives for its steps in order), so one wait covers 8 MMAs
+        // warp arrives for its steps in order); then both steps' activations must have landed
         for (int st = 0; st < nst; st += 2, gs += 2) {
-          if (!mbar_wait(&sm.staged[(gs + 1) % kPAst], ((gs + 1) / kPAst) & 1)) { bad = true; break; }
+          if (!mbar_wait(&sm.staged[(gs + 1) % kPAst], ((gs + 1) / kPAst) & 1) ||
+              !mbar_wait(&sm.bfull[gs % kBRing], (gs / kBRing) & 1) ||
+              !mbar_wait(&sm.bfull[(gs + 1) % kBRing], ((gs + 1) / kBRing) & 1)) {
+            bad = true;
+            break;
+          }
           asm volatile("tcgen05.fence::after_thread_sync;");
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -366,6 +372,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
           }
           tc_commit(&sm.bdone[gs % kBRing]);
           tc_commit(&sm.bdone[(gs + 1) % kBRing]);
+          tc_commit(&sm.adone[(gs >> 1) % (kPAst / 2)]);
           last = gs + 1;
         }
         if (bad) break;
@@ -526,10 +533,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
         constexpr int kSteps = kPC / step_weights<FC1>();
         for (int s = 0; s < kSteps; ++s, ++gs) {
           const int as = gs % kPAst;
-          // the A stage is free once the MMAs of step gs - kPAst are done
-          if (gs >= kPAst && !mbar_wait_warp(&sm.bdone[(gs - kPAst) % kBRing], ((gs - kPAst) / kBRing) & 1)) {
-            bad = true;
-            break;
+          // the A stage is free once the MMAs of the pair that used it last are done
+          if (gs >= kPAst) {
+            const int q = (gs - kPAst) >> 1;
+            if (!mbar_wait_warp(&sm.adone[q % (kPAst / 2)], (q / (kPAst / 2)) & 1)) { bad = true; break; }
           }
           // the 32-weight group of the chunk this thread expands: FC1 2 s + half (bf16 pairs of
           // weights c and c + 16), FC2 s (tf32, weights 16 half .. 16 half + 15)
@@ -557,8 +564,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
           tmem_st16(tmem + lane_q + kPColA + 32 * as + 16 * half, av);
           asm volatile("tcgen05.wait::st.sync.aligned;");
           asm volatile("tcgen05.fence::before_thread_sync;");
-          // the step is staged only once its activations have landed as well
-          if (!mbar_wait_warp(&sm.bfull[gs % kBRing], (gs / kBRing) & 1)) { bad = true; break; }
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.staged[as]);
         }
