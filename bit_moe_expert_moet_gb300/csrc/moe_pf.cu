@@ -26,7 +26,7 @@
 //
 // Pipeline: one persistent CTA per SM (20 warps) over (work item of <= 256
 // pairs x 128-row weight tile) units: warp 0 streams 256-weight chunks of the
-// planes (or delta) and warps 3, 16-18 take turns streaming the steps of the
+// planes (or delta) and warps 3, 16, 18, 19 take turns streaming the steps of the
 // item's activation rows, with TMA (one lane per box); warps 8-15 expand each step's weights into a TMEM A
 // stage (two warps per 32-row quarter); warp 1 issues 4 MMAs
 // per step and commits; warp 2 prepares the unit records; warps 4-7 drain the
@@ -45,7 +45,7 @@ namespace moet {
 namespace {
 
 constexpr int kPfThreads = 640;           // 20 warps, roles above
-constexpr int kBProd = 4;                 // activation producer warps (3, 16, 17, 18), steps in turn
+constexpr int kBProd = 4;                 // activation producer warps (3, 16, 18, 19), steps in turn
 constexpr int kPfConvWarps = 8;
 constexpr int kPC = 256;                  // weights per weight chunk
 // weights per step: 4 MMAs of K = 16 (bf16, FC1) or K = 8 (tf32, FC2); either way one step
@@ -104,7 +104,7 @@ static_assert(sizeof(PfMeta) == 64 + 9 * kPfTok, "PfMeta layout");
 struct PfSmem {
   uint64_t pfull[kPRing], pempty[kPRing];
   uint64_t bfull[kBRing], bdone[kBRing];
-  uint64_t staged[kPAst];
+  uint64_t staged[kPAst / 2];     // both A stages of a pair of steps expanded
   uint64_t adone[kPAst / 2];      // MMAs of a pair of steps done: their A stages are free
   uint64_t acc_full, acc_empty;
   uint64_t meta_full[kPMeta], meta_empty[kPMeta];
@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
     sm.stuck = 0;
     for (int s = 0; s < kPRing; ++s) { mbar_init(&sm.pfull[s], 1); mbar_init(&sm.pempty[s], kPfConvWarps); }
     for (int s = 0; s < kBRing; ++s) { mbar_init(&sm.bfull[s], 1); mbar_init(&sm.bdone[s], 1); }
-    for (int s = 0; s < kPAst; ++s) mbar_init(&sm.staged[s], kPfConvWarps);
+    for (int s = 0; s < kPAst / 2; ++s) mbar_init(&sm.staged[s], kPfConvWarps);
     for (int s = 0; s < kPAst / 2; ++s) mbar_init(&sm.adone[s], 1);
     mbar_init(&sm.acc_full, 1);
     mbar_init(&sm.acc_empty, 4);
@@ -276,7 +276,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
   asm volatile("tcgen05.fence::after_thread_sync;");
   const uint32_t tmem = sm.tmem_base;
 
-  const int bprod = warp == 3 ? 0 : (warp >= 16 && warp < 16 + kBProd - 1) ? warp - 15 : -1;
+  // activation producers 3, 16, 18, 19: none on the MMA thread's sub-partition (warp % 4 == 1)
+  const int bprod = warp == 3 ? 0 : warp == 16 ? 1 : warp == 18 ? 2 : warp == 19 ? 3 : -1;
   if (warp == 0 || bprod >= 0) {
     // ---------------- producers, one lane per TMA box: warp 0 streams the weight chunks,
     // the activation producers take the 64-row activation steps in turn
@@ -351,10 +352,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
         asm volatile("tcgen05.fence::after_thread_sync;");
         const int nst = sm.meta[m].nck * (kPC / step_weights<FC1>());
         const uint32_t idesc = FC1 ? f16_idesc(sm.meta[m].ncols) : tf32_idesc(sm.meta[m].ncols);
-        // two steps per iteration: staged of the second step implies the first (every converter
-        // warp arrives for its steps in order); then both steps' activations must have landed
+        // two steps per iteration: both A stages expanded, both steps' activations landed
         for (int st = 0; st < nst; st += 2, gs += 2) {
-          if (!mbar_wait(&sm.staged[(gs + 1) % kPAst], ((gs + 1) / kPAst) & 1) ||
+          if (!mbar_wait(&sm.staged[(gs >> 1) % (kPAst / 2)], ((gs >> 1) / (kPAst / 2)) & 1) ||
               !mbar_wait(&sm.bfull[gs % kBRing], (gs / kBRing) & 1) ||
               !mbar_wait(&sm.bfull[(gs + 1) % kBRing], ((gs + 1) / kBRing) & 1)) {
             bad = true;
@@ -531,41 +531,44 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
         const unsigned char* pst = base + kPBase + ps * kPChunkBytes;
         const bool dp = c >= nkc;
         constexpr int kSteps = kPC / step_weights<FC1>();
-        for (int s = 0; s < kSteps; ++s, ++gs) {
-          const int as = gs % kPAst;
-          // the A stage is free once the MMAs of the pair that used it last are done
+        // steps in pairs (the MMA thread consumes them in pairs): one TMEM fence and one arrive per pair
+        for (int s = 0; s < kSteps; s += 2, gs += 2) {
+          // the pair's A stages are free once the MMAs of the pair that used them last are done
           if (gs >= kPAst) {
             const int q = (gs - kPAst) >> 1;
             if (!mbar_wait_warp(&sm.adone[q % (kPAst / 2)], (q / (kPAst / 2)) & 1)) { bad = true; break; }
           }
-          // the 32-weight group of the chunk this thread expands: FC1 2 s + half (bf16 pairs of
-          // weights c and c + 16), FC2 s (tf32, weights 16 half .. 16 half + 15)
-          const int wi = FC1 ? 2 * s + half : s;
-          const uint32_t sc = *reinterpret_cast<const uint16_t*>(pst + (dp ? 16384 : 8192) + trow * 16 + 2 * wi);
-          const uint32_t s0 = sc & 0xFFu, s1 = sc >> 8;
-          uint32_t av[16];
-          if (!dp) {
-            // 32-byte-swizzled plane rows: 16-byte piece p of row r at p ^ ((r >> 2) & 1)
-            const int wo = trow * 32 + ((((wi >> 2) ^ ((trow >> 2) & 1))) << 4) + 4 * (wi & 3);
-            planes_to_bf16(*reinterpret_cast<const uint32_t*>(pst + wo),
-                           *reinterpret_cast<const uint32_t*>(pst + 4096 + wo), s0, s1, av);
-            if (!FC1) {
 #pragma unroll
-              for (int j = 0; j < 16; ++j) av[j] = half ? (av[j] & 0xFFFF0000u) : (av[j] << 16);
+          for (int h2 = 0; h2 < 2; ++h2) {
+            // the 32-weight group of the chunk this thread expands: FC1 2 s + half (bf16 pairs of
+            // weights c and c + 16), FC2 s (tf32, weights 16 half .. 16 half + 15)
+            const int wi = FC1 ? 2 * (s + h2) + half : s + h2;
+            const uint32_t sc = *reinterpret_cast<const uint16_t*>(pst + (dp ? 16384 : 8192) + trow * 16 + 2 * wi);
+            const uint32_t s0 = sc & 0xFFu, s1 = sc >> 8;
+            uint32_t av[16];
+            if (!dp) {
+              // 32-byte-swizzled plane rows: 16-byte piece p of row r at p ^ ((r >> 2) & 1)
+              const int wo = trow * 32 + ((((wi >> 2) ^ ((trow >> 2) & 1))) << 4) + 4 * (wi & 3);
+              planes_to_bf16(*reinterpret_cast<const uint32_t*>(pst + wo),
+                             *reinterpret_cast<const uint32_t*>(pst + 4096 + wo), s0, s1, av);
+              if (!FC1) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) av[j] = half ? (av[j] & 0xFFFF0000u) : (av[j] << 16);
+              }
+            } else {
+              // 128-byte-swizzled code rows: piece p of row r at p ^ (r & 7)
+              const unsigned char* cp = pst + trow * 128 + ((wi ^ (trow & 7)) << 4);
+              if (FC1)
+                delta_to_bf16(*reinterpret_cast<const uint4*>(cp), s0, s1, av);
+              else
+                delta_to_tf32(*reinterpret_cast<const uint2*>(cp + 8 * half), half ? s1 : s0, av);
             }
-          } else {
-            // 128-byte-swizzled code rows: piece p of row r at p ^ (r & 7)
-            const unsigned char* cp = pst + trow * 128 + ((wi ^ (trow & 7)) << 4);
-            if (FC1)
-              delta_to_bf16(*reinterpret_cast<const uint4*>(cp), s0, s1, av);
-            else
-              delta_to_tf32(*reinterpret_cast<const uint2*>(cp + 8 * half), half ? s1 : s0, av);
+            tmem_st16(tmem + lane_q + kPColA + 32 * ((gs + h2) % kPAst) + 16 * half, av);
           }
-          tmem_st16(tmem + lane_q + kPColA + 32 * as + 16 * half, av);
           asm volatile("tcgen05.wait::st.sync.aligned;");
           asm volatile("tcgen05.fence::before_thread_sync;");
           __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.staged[as]);
+          if (lane == 0) mbar_arrive(&sm.staged[(gs >> 1) % (kPAst / 2)]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.pempty[ps]);
