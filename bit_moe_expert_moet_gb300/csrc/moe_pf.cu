@@ -195,21 +195,6 @@ __device__ __forceinline__ void delta_to_bf16(uint4 c, uint32_t s0, uint32_t s1,
   }
 }
 
-// FC2: the 16 delta codes of one half-group (8 bytes) with its block scale -> fp32 (tf32) bits of
-// its weights, one per word, in K order.
-__device__ __forceinline__ void delta_to_tf32(uint2 c, uint32_t s, uint32_t out[16]) {
-  const uint32_t b = bf16_bits(e4m3_to_f32(s));
-  const uint32_t sc = b | (b << 16);
-  const uint32_t w[2] = {c.x, c.y};
-#pragma unroll
-  for (int t = 0; t < 8; ++t) {
-    const uint32_t byte = (w[t >> 2] >> (8 * (t & 3))) & 0xFFu;
-    const uint32_t v = e2m1x2_bf16((byte & 15u) | ((byte >> 4) << 8), sc);
-    out[2 * t] = v << 16;
-    out[2 * t + 1] = v & 0xFFFF0000u;
-  }
-}
-
 // ---------------------------------------------------------------- gather
 // xb[pos] = x[token of perm[pos]] in the permuted K order; xbg the same for
 // gated pairs, zero for the others.  Grid (pairs, ceil(H / 8 / 128)).
@@ -538,11 +523,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
             const int q = (gs - kPAst) >> 1;
             if (!mbar_wait_warp(&sm.adone[q % (kPAst / 2)], (q / (kPAst / 2)) & 1)) { bad = true; break; }
           }
+          // FC1: half h expands 32-weight group 2 (s + h2) + h of step s + h2 (bf16 pairs of weights
+          // c and c + 16 per column).  FC2: half h expands all of step s + h (tf32, one weight per
+          // column), so no pair of weights is expanded twice.
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            // the 32-weight group of the chunk this thread expands: FC1 2 s + half (bf16 pairs of
-            // weights c and c + 16), FC2 s (tf32, weights 16 half .. 16 half + 15)
-            const int wi = FC1 ? 2 * (s + h2) + half : s + h2;
+          for (int h2 = 0; h2 < (FC1 ? 2 : 1); ++h2) {
+            const int wi = FC1 ? 2 * (s + h2) + half : s + half;
             const uint32_t sc = *reinterpret_cast<const uint16_t*>(pst + (dp ? 16384 : 8192) + trow * 16 + 2 * wi);
             const uint32_t s0 = sc & 0xFFu, s1 = sc >> 8;
             uint32_t av[16];
@@ -551,19 +537,21 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
               const int wo = trow * 32 + ((((wi >> 2) ^ ((trow >> 2) & 1))) << 4) + 4 * (wi & 3);
               planes_to_bf16(*reinterpret_cast<const uint32_t*>(pst + wo),
                              *reinterpret_cast<const uint32_t*>(pst + 4096 + wo), s0, s1, av);
-              if (!FC1) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) av[j] = half ? (av[j] & 0xFFFF0000u) : (av[j] << 16);
-              }
             } else {
               // 128-byte-swizzled code rows: piece p of row r at p ^ (r & 7)
-              const unsigned char* cp = pst + trow * 128 + ((wi ^ (trow & 7)) << 4);
-              if (FC1)
-                delta_to_bf16(*reinterpret_cast<const uint4*>(cp), s0, s1, av);
-              else
-                delta_to_tf32(*reinterpret_cast<const uint2*>(cp + 8 * half), half ? s1 : s0, av);
+              delta_to_bf16(*reinterpret_cast<const uint4*>(pst + trow * 128 + ((wi ^ (trow & 7)) << 4)), s0, s1, av);
             }
-            tmem_st16(tmem + lane_q + kPColA + 32 * ((gs + h2) % kPAst) + 16 * half, av);
+            if (FC1) {
+              tmem_st16(tmem + lane_q + kPColA + 32 * ((gs + h2) % kPAst) + 16 * half, av);
+            } else {
+              // word j holds weights j and j + 16: tf32 columns j and j + 16
+              uint32_t lo[16], hi[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) { lo[j] = av[j] << 16; hi[j] = av[j] & 0xFFFF0000u; }
+              const uint32_t col = tmem + lane_q + kPColA + 32 * ((gs + half) % kPAst);
+              tmem_st16(col, lo);
+              tmem_st16(col + 16, hi);
+            }
           }
           asm volatile("tcgen05.wait::st.sync.aligned;");
           asm volatile("tcgen05.fence::before_thread_sync;");
