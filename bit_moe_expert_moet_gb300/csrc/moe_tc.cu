@@ -10,10 +10,10 @@
 // {+-0.5, +-1.5}, and s16 is exactly a ue4m3 block-16 scale.  So the planes
 // become an exact NVFP4 A operand: each thread expands one weight row of the
 // 128-row tile (sign and magnitude words -> e2m1 nibbles s|0|m|1) with a
-// handful of integer ops per 8 weights, stores it to shared memory in the
-// 128-byte-swizzled K-major layout, and writes the row scales to TMEM; the
-// tensor core applies the block scale.  The factor 2 of the halved levels is
-// applied in the epilogue.
+// handful of integer ops per 8 weights and stores it to TMEM (the A operand of
+// tcgen05.mma may live there), with the row scales beside it; the tensor core
+// applies the block scale.  The factor 2 of the halved levels is applied in the
+// epilogue.
 //
 // Activations.  Each activation row (bf16 token for FC1, fp32 h for FC2) is
 // expanded into kTcTerms NVFP4 terms r = sum_t g_t * e2m1 * ue4m3, each term
@@ -28,18 +28,18 @@
 // against a naturally ordered copy of the terms ("cnat") and accumulates in
 // a second TMEM region.
 //
-// Pipeline: a persistent CTA per SM (16 warps, warp-specialised, no CTA-wide
-// barrier in the loop) walks (work item, 128-row weight tile) units.  One
-// thread streams each unit's K chunks into a ring of raw shared-memory stages
-// with TMA (sign and magnitude planes, row scales, the item's activation-term
-// rows and their scales); converter warps expand the planes into a ring of
-// swizzled A stages and write the scale factors to TMEM; one thread issues the
-// MMAs (K = 64 each) and commits them to the stage's "done" barrier and, at
-// the end of a unit, to one of two TMEM accumulator buffers that the epilogue
-// warps drain while the next unit accumulates.  A scheduler warp prepares
-// each unit's record (pairs, routing weights, gate flags, term scales) ahead
-// of use.  Every wait is bounded; a stuck CTA records an error, waits for its
-// copies and MMAs in flight and releases TMEM.
+// Pipeline: a persistent CTA per SM (24 warps, warp-specialised, no CTA-wide
+// barrier in the loop) walks (work item, 128-row weight tile) units.  Two
+// producer warps stream each unit's K chunks into a ring of raw shared-memory
+// stages with TMA, one lane per box (sign and magnitude planes, row scales, the
+// item's activation-term rows and their scales); 16 converter warps expand the
+// planes into TMEM A stages and write the scale factors to TMEM; one thread
+// issues the MMAs (K = 64 each) and commits them to the stage's "done" barrier
+// and, at the end of a unit, to one of two TMEM accumulator buffers that the
+// epilogue warps drain while the next unit accumulates.  A scheduler warp
+// prepares each unit's record (pairs, routing weights, gate flags, term scales)
+// ahead of use.  Every wait is bounded; a stuck CTA records an error, waits for
+// its copies and MMAs in flight and releases TMEM.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
