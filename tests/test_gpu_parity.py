@@ -239,10 +239,10 @@ def test_forward_tiny_layer(moet, gate_mode):
     check_y(yg, yo)
 
 
-@pytest.mark.parametrize("T", [1, 9, 33, 100, 300, 600])
+@pytest.mark.parametrize("T", [1, 9, 33, 100, 300, 512, 513, 600])
 def test_forward_mid_size(moet, T):
     """Several row tiles, K chunks, N-tiles and work items (T=300 gives > 64 pairs per
-    expert; T <= 512 runs the tcgen05 engine, T=600 the mma.sync engine)."""
+    expert; T <= 512 runs the block-scaled decode engine, T > 512 the bf16 prefill engine)."""
     H, I, E, k = 1024, 256, 16, 4
     rng = np.random.default_rng(30 + T)
     dset = np.array([1, 4, 5, 11], dtype=np.int32)
@@ -256,6 +256,40 @@ def test_forward_mid_size(moet, T):
     # no delta arguments at all
     yg2, _ = _run_forward(moet, logits, xb, k, gp, E, H)
     check_y(yg2, _oracle_forward(logits, xb, k, ref))
+
+
+@pytest.mark.parametrize("gate_mode", ["draw", "all", "none"])
+def test_forward_prefill_ragged_items(moet, gate_mode):
+    """Prefill engine with experts of more than 256 pairs: items split at 256 with a ragged
+    tail (T=1100, E=8, k=2: about 275 pairs per expert), every token checked; the delta pass
+    with some, all or no gated tokens."""
+    H, I, E, k, T = 512, 256, 8, 2, 1100
+    rng = np.random.default_rng(60)
+    dset = np.array([0, 3, 6], dtype=np.int32)
+    ref, gp = _make_layer(moet, H, I, E, dset, rng=rng)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    xb = W.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    gate = {"draw": (rng.random(T) < 0.3), "all": np.ones(T, bool), "none": np.zeros(T, bool)}[gate_mode]
+    gate = gate.astype(np.uint8)
+    yg, err = _run_forward(moet, logits, xb, k, gp, E, H, dset, gate)
+    assert err == 0
+    check_y(yg, _oracle_forward(logits, xb, k, ref, dset, gate, E))
+
+
+@pytest.mark.parametrize("T", [100, 700])
+def test_forward_mma_sync_engine(moet, T):
+    """Shapes the tcgen05 engines do not take (I = 384, not a multiple of 256) run the
+    mma.sync engine at any token count."""
+    H, I, E, k = 1024, 384, 16, 4
+    rng = np.random.default_rng(70 + T)
+    dset = np.array([2, 9], dtype=np.int32)
+    ref, gp = _make_layer(moet, H, I, E, dset, rng=rng)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    xb = W.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    gate = (rng.random(T) < 0.5).astype(np.uint8)
+    yg, err = _run_forward(moet, logits, xb, k, gp, E, H, dset, gate)
+    assert err == 0
+    check_y(yg, _oracle_forward(logits, xb, k, ref, dset, gate, E))
 
 
 def test_forward_is_deterministic(moet):
