@@ -98,12 +98,26 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(
   if (blockIdx.x == 0) {
     if (warp != 0) return;
     bool ok = __ldg(offsets) == 0 && __ldg(offsets + E) == T * k;
+    // all of this lane's offsets first (independent loads, one memory latency), then the scan
+    constexpr int kMaxPerLane = 1024 / 32;
+    int lo[kMaxPerLane + 1];
+#pragma unroll
+    for (int i = 0; i <= kMaxPerLane; ++i) {
+      const int e = 32 * i + lane;
+      lo[i] = e <= E ? __ldg(offsets + e) : 0;
+    }
     int running = 0;
-    for (int c0 = 0; c0 < E; c0 += 32) {
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) {
+      const int c0 = 32 * i;
+      if (c0 >= E) break;
       const int e = c0 + lane;
+      // offsets[e + 1] of this lane is offsets[e'] of lane + 1 (or of lane 0 in the next group)
+      const int up = __shfl_down_sync(0xffffffffu, lo[i], 1);
+      const int nx = __shfl_sync(0xffffffffu, lo[i + 1], 0);
       int n = 0;
       if (e < E) {
-        n = __ldg(offsets + e + 1) - __ldg(offsets + e);
+        n = (lane == 31 ? nx : up) - lo[i];
         if (n < 0) { ok = false; n = 0; }
       }
       const int nch = (n + chunk - 1) / chunk;
