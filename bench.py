@@ -589,6 +589,31 @@ def run_ours(args, rank, world, local):
             del l3
             torch.cuda.empty_cache()
         extras["decode_sweep"] = sweep
+
+        # expert cache: the headline layer through the slot table with every 10th expert not
+        # resident (their pairs contribute zero and are counted); the planes stay where they are
+        slot_np = np.arange(cfg.E, dtype=np.int32)
+        slot_np[::10] = -1
+        slot_t = torch.from_numpy(slot_np).to(dev)
+        miss = torch.zeros(1, dtype=torch.int32, device=dev)
+        kwp = {}
+        if layer.use_delta:
+            kwp = dict(delta_slot=layer.slot, dfc1=layer.pools[1], dfc2=layer.pools[2], gate_mask=layer.gate)
+
+        def pooled_step():
+            moet.route_topk(layer.logits, cfg.k, layer.idx, layer.w, layer.off, layer.perm)
+            moet.moe_forward_pooled(layer.x, layer.idx, layer.w, layer.off, layer.perm, slot_t, layer.planes[1],
+                                    layer.planes[2], layer.y, layer.ws, miss_count=miss, **kwp)
+
+        gp_ = capture_graph(torch, pooled_step)
+        miss.zero_()
+        tp = time_steps(torch, gp_.replay, args.steps, args.warmup, flush)
+        med = statistics.median(tp)
+        n_replays = args.steps + args.warmup
+        extras["pooled"] = {"workload": cfg.name, "resident_experts": int((slot_np >= 0).sum()),
+                            "missed_pairs_per_step": int(miss.item()) / n_replays,
+                            "tokens_per_s": cfg.T / (med * 1e-3), "ms_per_step_median": med}
+        del gp_
         extras["requant"] = time_requant(moet, torch, dev)
         extras["requant"]["frac_of_hbm_peak"] = extras["requant"]["gbs"] / peak
 

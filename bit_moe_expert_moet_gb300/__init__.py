@@ -11,6 +11,8 @@ Entry points (same names as the C ABI without the ``moet_`` prefix):
   requant_2bit     NVFP4 -> 2-bit sign/magnitude planes + s16 (+ delta)
   route_topk       logits -> top-k ids/weights, expert offsets, permutation
   moe_forward      the MoE layer y = sum_j w_j FFN_e(x) on the 2-bit planes
+  moe_forward_pooled  the same over a pool of resident experts (slot table,
+                   non-resident experts contribute zero and are counted)
 """
 from ._lib import (  # noqa: F401
     MoetError,
@@ -28,6 +30,7 @@ from ._lib import (  # noqa: F401
     route_topk,
     forward_workspace_size,
     moe_forward,
+    moe_forward_pooled,
     moe_forward_static,
     FORWARD_STATIC_SCRATCH_BYTES,
 )

@@ -58,6 +58,11 @@ lib.moet_moe_forward.argtypes = [_i, _i, _i, _i, _i, _p, _p, _p, _p, _p,
                                  ctypes.POINTER(_Planes), ctypes.POINTER(_Planes),
                                  _p, _i, ctypes.POINTER(_Nvfp4), ctypes.POINTER(_Nvfp4),
                                  _p, _p, _p, _sz, _p]
+lib.moet_moe_forward_pooled.restype = _i
+lib.moet_moe_forward_pooled.argtypes = [_i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _i,
+                                        ctypes.POINTER(_Planes), ctypes.POINTER(_Planes),
+                                        _p, _i, ctypes.POINTER(_Nvfp4), ctypes.POINTER(_Nvfp4),
+                                        _p, _p, _p, _p, _p, _sz, _p]
 
 
 class MoetError(RuntimeError):
@@ -195,6 +200,46 @@ def moe_forward(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
         _ptr(delta_slot, torch.int32, "delta_slot"), n_slots,
         ctypes.byref(d1) if d1 is not None else None, ctypes.byref(d2) if d2 is not None else None,
         _ptr(gate_mask, torch.uint8, "gate_mask"), _ptr(y, None, "y"),
+        _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def moe_forward_pooled(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
+                       expert_offsets: torch.Tensor, perm: torch.Tensor, expert_slot: torch.Tensor,
+                       fc1: Planes, fc2: Planes, y: torch.Tensor, workspace: torch.Tensor,
+                       delta_slot: Optional[torch.Tensor] = None, dfc1: Optional[DeltaPool] = None,
+                       dfc2: Optional[DeltaPool] = None, gate_mask: Optional[torch.Tensor] = None,
+                       miss_count: Optional[torch.Tensor] = None, miss_mask: Optional[torch.Tensor] = None,
+                       stream=None):
+    """moe_forward over a pool of resident experts: fc1/fc2 hold n_pool slots, expert e lives in
+    slot expert_slot[e] (-1 = not resident: contributes zero, counted in miss_count (u32 [1]) and
+    flagged in miss_mask (u8 [E]))."""
+    T, H = x.shape
+    E = expert_slot.shape[0]
+    n_pool = fc1.scale_2.shape[0]
+    I = fc2.sign.shape[2] * 32
+    k = topk_idx.shape[1]
+    if x.dtype != torch.bfloat16 or y.dtype != torch.bfloat16:
+        raise TypeError("x and y must be bfloat16")
+    if miss_count is not None and (miss_count.dtype != torch.int32 or miss_count.numel() < 1):
+        raise TypeError("miss_count must be an int32 tensor of at least one element (the u32 counter)")
+    c1, c2 = fc1._c("fc1"), fc2._c("fc2")
+    n_slots = 0
+    d1 = d2 = None
+    if delta_slot is not None:
+        if dfc1 is None or dfc2 is None or gate_mask is None:
+            raise ValueError("delta_slot needs dfc1, dfc2 and gate_mask")
+        n_slots = dfc1.codes.shape[0]
+        d1, d2 = dfc1._c("dfc1"), dfc2._c("dfc2")
+    _check("moet_moe_forward_pooled", lib.moet_moe_forward_pooled(
+        T, H, I, E, k, _ptr(x, None, "x"), _ptr(topk_idx, torch.int32, "topk_idx"),
+        _ptr(topk_w, torch.float32, "topk_w"), _ptr(expert_offsets, torch.int32, "expert_offsets"),
+        _ptr(perm, torch.int32, "perm"), _ptr(expert_slot, torch.int32, "expert_slot"), n_pool,
+        ctypes.byref(c1), ctypes.byref(c2),
+        _ptr(delta_slot, torch.int32, "delta_slot"), n_slots,
+        ctypes.byref(d1) if d1 is not None else None, ctypes.byref(d2) if d2 is not None else None,
+        _ptr(gate_mask, torch.uint8, "gate_mask"), _ptr(miss_count, None, "miss_count"),
+        _ptr(miss_mask, torch.uint8, "miss_mask"), _ptr(y, None, "y"),
         _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
         _stream(stream)))
 

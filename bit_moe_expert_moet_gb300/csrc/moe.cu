@@ -43,7 +43,7 @@ constexpr int kSmemBudget = 96 * 1024;
 constexpr uint32_t kCodeLut = 0xC242BC3Cu;  // f16 high bytes of +1, -1, +3, -3
 
 struct WsLayout {
-  size_t hdr, tok_scale, tok_max, hmax, inv, chunks, h, o, xt, ht, pfa, total;
+  size_t hdr, tok_scale, tok_max, hmax, inv, pvalid, chunks, h, o, xt, ht, pfa, total;
 };
 
 // Largest T routed through the tcgen05 engine (small tokens-per-expert regime).
@@ -65,6 +65,7 @@ inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   L.tok_max = off;   off += align256(sizeof(float) * T);
   L.hmax = off;      off += align256(sizeof(unsigned) * pairs);
   L.inv = off;       off += align256(sizeof(int32_t) * pairs);
+  L.pvalid = off;    off += align256(pairs);
   L.chunks = off;    off += align256(sizeof(int4) * (size_t)max_chunks(T, E, k, kTcTok));
   L.h = off;         off += align256(sizeof(float) * pairs * I);
   L.o = off;         off += align256(sizeof(float) * pairs * H);
@@ -90,10 +91,16 @@ __device__ __forceinline__ float pow2_scale_for(float amax) {
 }
 
 // ---------------------------------------------------------------- prologue
+// With an expert slot table (pooled forward), experts that are not resident get no work items,
+// their routed pairs are counted (miss_count, miss_mask) and marked invalid for the combine, and
+// each work item carries the expert's pool slot (.w) for the plane and scale_2 addressing; without
+// one, .w is the expert id.
 __global__ void __launch_bounds__(kThreads) prologue_kernel(
     int T, int H, int E, int k, int chunk, const uint16_t* __restrict__ x, const int32_t* __restrict__ offsets,
     const int32_t* __restrict__ perm, int* __restrict__ hdr, float* __restrict__ tok_scale,
-    float* __restrict__ tok_max, unsigned* __restrict__ hmax, int32_t* __restrict__ inv, int4* __restrict__ chunks) {
+    float* __restrict__ tok_max, unsigned* __restrict__ hmax, int32_t* __restrict__ inv, int4* __restrict__ chunks,
+    const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ expert_slot, int n_pool,
+    unsigned* __restrict__ miss_count, uint8_t* __restrict__ miss_mask, uint8_t* __restrict__ pvalid) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (blockIdx.x == 0) {
     if (warp != 0) return;
@@ -115,12 +122,20 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(
       // offsets[e + 1] of this lane is offsets[e'] of lane + 1 (or of lane 0 in the next group)
       const int up = __shfl_down_sync(0xffffffffu, lo[i], 1);
       const int nx = __shfl_sync(0xffffffffu, lo[i + 1], 0);
-      int n = 0;
+      int n = 0, pslot = e;
       if (e < E) {
         n = (lane == 31 ? nx : up) - lo[i];
         if (n < 0) { ok = false; n = 0; }
+        if (expert_slot != nullptr) {
+          pslot = __ldg(expert_slot + e);
+          if (pslot >= n_pool) { record_error(MOET_ERR_DEVICE_INDEX); pslot = -1; }
+          if (pslot < 0 && n > 0) {
+            if (miss_count != nullptr) atomicAdd(miss_count, (unsigned)n);
+            if (miss_mask != nullptr) miss_mask[e] = 1;
+          }
+        }
       }
-      const int nch = (n + chunk - 1) / chunk;
+      const int nch = pslot >= 0 ? (n + chunk - 1) / chunk : 0;
       int incl = nch;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -130,7 +145,7 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(
       const int first = running + incl - nch;
       for (int c = 0; c < nch; ++c) {
         const int cnt = min(chunk, n - c * chunk);
-        chunks[first + c] = make_int4(e, c * chunk, cnt, 0);
+        chunks[first + c] = make_int4(e, c * chunk, cnt, pslot);
       }
       running += __shfl_sync(0xffffffffu, incl, 31);
     }
@@ -148,6 +163,13 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(
   const int nthreads = (gridDim.x - 1) * kThreads;
   for (int i = (blockIdx.x - 1) * kThreads + tid; i < T * k; i += nthreads) {
     hmax[i] = 0u;
+    if (pvalid != nullptr) {
+      // pair i (= t k + j) counts in the combine only if its expert is resident
+      const int e = __ldg(topk_idx + i);
+      int sl = -1;
+      if (e >= 0 && e < E) sl = __ldg(expert_slot + e);
+      pvalid[i] = (sl >= 0 && sl < n_pool) ? 1 : 0;
+    }
     if (inv != nullptr) {
       const int p = __ldg(perm + i);
       if (p >= 0 && p < T * k) inv[p] = i;
@@ -211,6 +233,7 @@ __global__ void __launch_bounds__(kThreads, 2) fc_kernel(const FcArgs a) {
   if ((int)blockIdx.y >= a.hdr[0]) return;
   const int4 ch = a.chunks[blockIdx.y];
   const int e = ch.x, count = ch.z;
+  const size_t pe = (size_t)ch.w;                        // pool slot of the expert's planes
   const int pos0 = __ldg(a.offsets + e) + ch.y;
   const int K = a.K;
   const int pitch = a.ks + 16;                           // halves per staged row
@@ -265,12 +288,12 @@ __global__ void __launch_bounds__(kThreads, 2) fc_kernel(const FcArgs a) {
     row_u = r0 + g + 8;
   }
   const size_t wpr = (size_t)K / 32, bpr = (size_t)K / 16;
-  const uint32_t* Sg = a.sign + ((size_t)e * a.N + row_g) * wpr;
-  const uint32_t* Mg = a.mag + ((size_t)e * a.N + row_g) * wpr;
-  const uint32_t* Su = a.sign + ((size_t)e * a.N + row_u) * wpr;
-  const uint32_t* Mu = a.mag + ((size_t)e * a.N + row_u) * wpr;
-  const uint8_t* Qg = a.s16 + ((size_t)e * a.N + row_g) * bpr;
-  const uint8_t* Qu = a.s16 + ((size_t)e * a.N + row_u) * bpr;
+  const uint32_t* Sg = a.sign + (pe * a.N + row_g) * wpr;
+  const uint32_t* Mg = a.mag + (pe * a.N + row_g) * wpr;
+  const uint32_t* Su = a.sign + (pe * a.N + row_u) * wpr;
+  const uint32_t* Mu = a.mag + (pe * a.N + row_u) * wpr;
+  const uint8_t* Qg = a.s16 + (pe * a.N + row_g) * bpr;
+  const uint8_t* Qu = a.s16 + (pe * a.N + row_u) * bpr;
   const uint8_t* Dg = nullptr; const uint8_t* Du = nullptr;
   const uint8_t* DQg = nullptr; const uint8_t* DQu = nullptr;
   if (do_delta) {
@@ -423,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 2) fc_kernel(const FcArgs a) {
   }
 
   // ---- epilogue
-  const float sc2 = __ldg(a.scale_2 + e);
+  const float sc2 = __ldg(a.scale_2 + pe);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -453,6 +476,7 @@ __global__ void __launch_bounds__(kThreads, 2) fc_kernel(const FcArgs a) {
 // ---------------------------------------------------------------- combine
 __global__ void __launch_bounds__(kThreads) combine_kernel(int T, int H, int k, const int* __restrict__ hdr,
                                                            const float* __restrict__ o,
+                                                           const uint8_t* __restrict__ pvalid,
                                                            uint16_t* __restrict__ y) {
   const long long n4 = (long long)T * H / 4;
   const bool ok = hdr[1] != 0;
@@ -462,6 +486,8 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(int T, int H, int k, 
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
     if (ok) {
       for (int j = 0; j < k; ++j) {
+        // a pair of a non-resident expert (pooled forward) contributes zero; its o row is never written
+        if (pvalid != nullptr && __ldg(pvalid + (size_t)t * k + j) == 0) continue;
         const float4 v = *reinterpret_cast<const float4*>(o + ((size_t)t * k + j) * H + r);
         s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
       }
@@ -512,13 +538,15 @@ extern "C" size_t moet_forward_workspace_size(int T, int H, int I, int E, int k)
   return ws_layout(T, H, I, E, k).total;
 }
 
-extern "C" moet_status moet_moe_forward(int T, int H, int I, int E, int k, const uint16_t* x,
-                                        const int32_t* topk_idx, const float* topk_w,
-                                        const int32_t* expert_offsets, const int32_t* perm,
-                                        const moet_planes* fc1, const moet_planes* fc2,
-                                        const int32_t* delta_slot, int n_slots, const moet_nvfp4* dfc1,
-                                        const moet_nvfp4* dfc2, const uint8_t* gate_mask, uint16_t* y,
-                                        void* workspace, size_t ws_bytes, moet_stream stream) {
+// The forward behind moet_moe_forward (expert_slot == null: the planes hold all E experts) and
+// moet_moe_forward_pooled (the planes hold n_pool slots, expert e in slot expert_slot[e]).
+static moet_status forward_impl(int T, int H, int I, int E, int k, const uint16_t* x, const int32_t* topk_idx,
+                                const float* topk_w, const int32_t* expert_offsets, const int32_t* perm,
+                                const int32_t* expert_slot, int n_pool, const moet_planes* fc1,
+                                const moet_planes* fc2, const int32_t* delta_slot, int n_slots,
+                                const moet_nvfp4* dfc1, const moet_nvfp4* dfc2, const uint8_t* gate_mask,
+                                unsigned* miss_count, uint8_t* miss_mask, uint16_t* y, void* workspace,
+                                size_t ws_bytes, moet_stream stream) {
   if (T < 1 || H < 128 || I < 128 || H % 128 || I % 128 || E < 1 || E > 1024 || k < 1 || k > 16 ||
       k > E)
     return MOET_ERR_SHAPE;
@@ -551,6 +579,8 @@ extern "C" moet_status moet_moe_forward(int T, int H, int I, int E, int k, const
   int4* chunks = reinterpret_cast<int4*>(ws + L.chunks);
   float* h = reinterpret_cast<float*>(ws + L.h);
   float* o = reinterpret_cast<float*>(ws + L.o);
+  uint8_t* pvalid = expert_slot != nullptr ? reinterpret_cast<uint8_t*>(ws + L.pvalid) : nullptr;
+  const int n_planes = expert_slot != nullptr ? n_pool : E;     // experts (or slots) the planes hold
 
   const bool use_tc = T <= kTcMaxT && tc_supported(H, I);
   const bool use_pf = !use_tc && T > kTcMaxT && pf_supported(H, I);
@@ -559,14 +589,15 @@ extern "C" moet_status moet_moe_forward(int T, int H, int I, int E, int k, const
     ProfScope ps(MOET_K_PROLOGUE, st);
     prologue_kernel<<<1 + (T + 7) / 8, kThreads, 0, st>>>(T, H, E, k, chunk, x, expert_offsets, perm, hdr,
                                                            tok_scale, tok_max, hmax, use_tc ? inv : nullptr,
-                                                           chunks);
+                                                           chunks, topk_idx, expert_slot, n_pool, miss_count,
+                                                           miss_mask, pvalid);
   }
   MOET_CUDA_TRY(cudaGetLastError());
 
   const int mc = max_chunks(T, E, k, chunk);
   if (use_pf) {
     PfForwardArgs f{};
-    f.T = T; f.H = H; f.I = I; f.E = E; f.k = k;
+    f.T = T; f.H = H; f.I = I; f.E = n_planes; f.k = k;   // E: experts the planes hold (tensor maps)
     f.x = x; f.offsets = expert_offsets; f.perm = perm; f.topk_w = topk_w;
     f.fc1 = fc1; f.fc2 = fc2;
     f.delta_slot = with_delta ? delta_slot : nullptr;
@@ -583,7 +614,7 @@ extern "C" moet_status moet_moe_forward(int T, int H, int I, int E, int k, const
     if (s != MOET_OK) return s;
   } else if (use_tc) {
     TcForwardArgs f{};
-    f.T = T; f.H = H; f.I = I; f.E = E; f.k = k;
+    f.T = T; f.H = H; f.I = I; f.E = n_planes; f.k = k;   // E: experts the planes hold (tensor maps)
     f.x = x; f.offsets = expert_offsets; f.perm = perm; f.topk_w = topk_w;
     f.fc1 = fc1; f.fc2 = fc2;
     f.delta_slot = with_delta ? delta_slot : nullptr;
@@ -607,7 +638,7 @@ extern "C" moet_status moet_moe_forward(int T, int H, int I, int E, int k, const
   const int maxn = T < kChunk ? T : kChunk;
   const int nt = maxn <= 8 ? 1 : maxn <= 16 ? 2 : maxn <= 32 ? 4 : 8;
   FcArgs a{};
-  a.T = T; a.H = H; a.I = I; a.E = E; a.k = k;
+  a.T = T; a.H = H; a.I = I; a.E = n_planes; a.k = k;
   a.x = x; a.h_in = h; a.offsets = expert_offsets; a.perm = perm; a.topk_w = topk_w;
   a.delta_slot = with_delta ? delta_slot : nullptr;
   a.gate = with_delta ? gate_mask : nullptr;
@@ -636,8 +667,36 @@ extern "C" moet_status moet_moe_forward(int T, int H, int I, int E, int k, const
   if (gc > 152 * 8) gc = 152 * 8;
   {
     ProfScope ps(MOET_K_COMBINE, st);
-    combine_kernel<<<gc, kThreads, 0, st>>>(T, H, k, hdr, o, y);
+    combine_kernel<<<gc, kThreads, 0, st>>>(T, H, k, hdr, o, pvalid, y);
   }
   MOET_CUDA_TRY(cudaGetLastError());
   return MOET_OK;
+}
+
+extern "C" moet_status moet_moe_forward(int T, int H, int I, int E, int k, const uint16_t* x,
+                                        const int32_t* topk_idx, const float* topk_w,
+                                        const int32_t* expert_offsets, const int32_t* perm,
+                                        const moet_planes* fc1, const moet_planes* fc2,
+                                        const int32_t* delta_slot, int n_slots, const moet_nvfp4* dfc1,
+                                        const moet_nvfp4* dfc2, const uint8_t* gate_mask, uint16_t* y,
+                                        void* workspace, size_t ws_bytes, moet_stream stream) {
+  return forward_impl(T, H, I, E, k, x, topk_idx, topk_w, expert_offsets, perm, nullptr, E, fc1, fc2, delta_slot,
+                      n_slots, dfc1, dfc2, gate_mask, nullptr, nullptr, y, workspace, ws_bytes, stream);
+}
+
+extern "C" moet_status moet_moe_forward_pooled(int T, int H, int I, int E, int k, const uint16_t* x,
+                                               const int32_t* topk_idx, const float* topk_w,
+                                               const int32_t* expert_offsets, const int32_t* perm,
+                                               const int32_t* expert_slot, int n_pool,
+                                               const moet_planes* fc1, const moet_planes* fc2,
+                                               const int32_t* delta_slot, int n_slots, const moet_nvfp4* dfc1,
+                                               const moet_nvfp4* dfc2, const uint8_t* gate_mask,
+                                               uint32_t* miss_count, uint8_t* miss_mask, uint16_t* y,
+                                               void* workspace, size_t ws_bytes, moet_stream stream) {
+  if (!expert_slot) return MOET_ERR_INVALID_ARG;
+  if (n_pool < 1) return MOET_ERR_SHAPE;
+  if ((uintptr_t)expert_slot & 3) return MOET_ERR_ALIGN;
+  return forward_impl(T, H, I, E, k, x, topk_idx, topk_w, expert_offsets, perm, expert_slot, n_pool, fc1, fc2,
+                      delta_slot, n_slots, dfc1, dfc2, gate_mask, miss_count, miss_mask, y, workspace, ws_bytes,
+                      stream);
 }

@@ -15,7 +15,8 @@
 // Precision.  FC1 runs kind::f16 on bf16: x is bf16, so FC1 is exact up to
 // fp32 accumulation.  FC2 runs kind::tf32 on the fp32 h: rounding h to bf16
 // (2^-9) on top of the bf16 output would exceed the layer's max-error budget,
-// while tf32 keeps 10 mantissa bits of h at half the bf16 MMA rate.
+// while tf32 keeps 10 mantissa bits of h at half the bf16 MMA rate (FC1's epilogue rounds h to
+// the nearest tf32, so the tensor core's truncation to tf32 adds no bias).
 //
 // Layout.  FC1: a 32-bit TMEM column holds two bf16 of one row; column c of a
 // 32-weight group holds weights c and c + 16 (one shift-and-mask extracts the
@@ -89,7 +90,7 @@ struct PfArgs {
 };
 
 struct PfMeta {
-  int e, pos0, ntok, ncols;
+  int e, pos0, ntok, ncols;      // e: the planes' expert (pool slot) index
   int dslot;                     // delta slot when the unit runs the delta pass, else -1
   int nck;                       // weight chunks (K / 256, doubled with the delta pass)
   int r0, r1;
@@ -142,6 +143,13 @@ __device__ __forceinline__ void mma_ta(uint32_t d, uint32_t a_tmem, uint64_t bd,
         "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
         "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p; }" ::"r"(d),
         "r"(a_tmem), "l"(bd), "r"(idesc), "r"(acc));
+}
+
+// fp32 value rounded to the nearest tf32 (10 explicit mantissa bits; ties away from zero).
+__device__ __forceinline__ float tf32_rna(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
 }
 
 // bf16 bits of an e4m3 value and of three times it (both exact).
@@ -380,6 +388,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
       const int item = u / a.tiles, tile = u - item * a.tiles;
       const int4 ch = a.chunks[item];
       const int e = ch.x, ntok = ch.z;
+      const int pe = ch.w;                 // pool slot of the expert's planes and scale_2
       const int pos0 = __ldg(a.offsets + e) + ch.y;
       int dslot = -1;
       if (a.delta_slot != nullptr && a.gate != nullptr) {
@@ -413,13 +422,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
       }
       if (!__any_sync(0xffffffffu, gated)) dslot = -1;
       if (lane == 0) {
-        um.e = e; um.pos0 = pos0; um.ntok = ntok;
+        um.e = pe; um.pos0 = pos0; um.ntok = ntok;
         um.ncols = ((ntok + 15) / 16) * 16;
         um.dslot = dslot;
         um.nck = dslot >= 0 ? 2 * nkc : nkc;
         um.r0 = FC1 ? tile * 64 : tile * 128;
         um.r1 = FC1 ? a.I + tile * 64 : tile * 128 + 64;
-        um.sc2 = __ldg(a.scale_2 + e);
+        um.sc2 = __ldg(a.scale_2 + pe);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.meta_full[m]);
@@ -480,7 +489,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
             const int col = cb + i;
             if (col < ntok) {
               const float gv = g[i] * sc2, uv = u[i] * sc2;
-              const float hv = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+              // h goes to FC2's tf32 MMA, which keeps the top 19 bits of each input: round it to
+              // nearest tf32 here so that FC2 sees an unbiased value, not a truncated one
+              const float hv = tf32_rna(__fdividef(gv, 1.0f + __expf(-gv)) * uv);
               const size_t at = (size_t)(pos0 + col) * a.I + hcol;
               a.h[at] = hv;
               // the gated copy feeds FC2's delta pass, which runs for exactly these units

@@ -35,7 +35,7 @@ struct PfForwardArgs {
   const moet_nvfp4* dfc2;
   const uint8_t* gate;         // nullable
   const int* hdr;              // [0] = number of work items
-  const int4* chunks;          // (expert, first pair, count <= kPfTok)
+  const int4* chunks;          // (expert, first pair, count <= kPfTok, pool slot of the planes)
   uint16_t* xb;                // [T k, H] bf16, bucketed rows, K permuted within 32-groups
   uint16_t* xbg;               // same, rows of ungated pairs zero
   float* h;                    // [T k, I] fp32, FC1 output (bucketed rows, natural order)

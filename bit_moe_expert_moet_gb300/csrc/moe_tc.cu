@@ -242,7 +242,7 @@ struct FcTcArgs {
 
 // One unit of work = (work item, 128-row weight tile), written by the scheduler warp.
 struct UnitMeta {
-  int e, pos0, ntok, ncols;
+  int e, pos0, ntok, ncols;      // e: the planes' expert (pool slot) index
   int dslot;                     // delta slot when the unit runs the delta pass, else -1
   int nch;                       // stages: ceil(K/512) plane stages (+ K/256 delta stages)
   int r0, r1;                    // first weight rows of the tile's two 64-row halves
@@ -471,6 +471,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
       const int item = u / a.tiles, tile = u - item * a.tiles;
       const int4 ch = a.chunks[item];
       const int e = ch.x, ntok = ch.z;
+      const int pe = ch.w;                 // pool slot of the expert's planes and scale_2
       const int pos0 = __ldg(a.offsets + e) + ch.y;
       int dslot = -1;
       if (a.delta_slot != nullptr && a.gate != nullptr) {
@@ -502,13 +503,13 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
         um.gsc[col] = tk < ntok && ptk >= 0 ? __ldg(a.gsc + (size_t)(pos0 + tk) * kTcTerms + col % kTcTerms) : 0.0f;
       }
       if (lane == 0) {
-        um.e = e; um.pos0 = pos0; um.ntok = ntok;
+        um.e = pe; um.pos0 = pos0; um.ntok = ntok;
         um.ncols = ((kTcTerms * ntok + 15) / 16) * 16;
         um.dslot = dslot;
         um.nch = dslot >= 0 ? nps + a.K / kKD : nps;
         um.r0 = FC1 ? tile * 64 : tile * 128;
         um.r1 = FC1 ? a.I + tile * 64 : tile * 128 + 64;
-        um.sc2 = __ldg(a.scale_2 + e);
+        um.sc2 = __ldg(a.scale_2 + pe);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.meta_full[m]);

@@ -40,7 +40,7 @@ struct TcForwardArgs {
   const moet_nvfp4* dfc2;
   const uint8_t* gate;         // nullable
   const int* hdr;              // [0] = number of work items
-  const int4* chunks;          // (expert, first pair, count <= kTcTok)
+  const int4* chunks;          // (expert, first pair, count <= kTcTok, pool slot of the planes)
   float* h;                    // [T k, I] bucketed
   float* o;                    // [T k, H] pair order
   const float* tokmax;         // [T] max |x_t| (written by the prologue)

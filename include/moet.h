@@ -159,6 +159,39 @@ moet_status moet_moe_forward(int T, int H, int I, int E, int k, const uint16_t* 
                              void* workspace, size_t ws_bytes, moet_stream stream);
 
 /* ------------------------------------------------------------------------
+ * moet_moe_forward_pooled -- moet_moe_forward over a device-resident pool of
+ * experts, for layers whose 2-bit planes do not all fit on the GPU.
+ * README "Frontier MoE on consumer Blackwell (SM120)", "When the model doesn't
+ * fit at all -- the GPU as an expert cache": the GPU holds a cache of hot
+ * experts addressed through a slot table read inside the (graph-captured)
+ * forward; a routed expert that is not resident contributes zero to y and is
+ * counted, so the caller can fetch every missing expert, update the table
+ * and replay the step -- which then equals a fully resident forward bit for
+ * bit (an expert's arithmetic does not depend on its pool slot).
+ *   expert_slot [E] i32: pool slot of expert e, or -1 (not resident); a slot
+ *     >= n_pool is a device index error and the expert counts as missing.
+ *   fc1/fc2: planes of the n_pool pool slots ([n_pool, 2I, H/32] ... and
+ *     scale_2 [n_pool]); all other arguments as for moet_moe_forward (the
+ *     delta table stays indexed by expert id).
+ *   miss_count: if non-NULL, one u32 to which the number of routed (token,
+ *     expert) pairs whose expert is not resident is added (atomically; the
+ *     caller resets it).  miss_mask: if non-NULL, u8 [E]; entry e is set to 1
+ *     when expert e was routed and is not resident (never cleared here).
+ *   Workspace: moet_forward_workspace_size(T, H, I, E, k), as for
+ *     moet_moe_forward.
+ * With every routed expert resident the result equals moet_moe_forward's on
+ * the same weights bit for bit.  */
+moet_status moet_moe_forward_pooled(int T, int H, int I, int E, int k, const uint16_t* x,
+                                    const int32_t* topk_idx, const float* topk_w,
+                                    const int32_t* expert_offsets, const int32_t* perm,
+                                    const int32_t* expert_slot, int n_pool,
+                                    const moet_planes* fc1, const moet_planes* fc2,
+                                    const int32_t* delta_slot, int n_slots, const moet_nvfp4* dfc1,
+                                    const moet_nvfp4* dfc2, const uint8_t* gate_mask,
+                                    uint32_t* miss_count, uint8_t* miss_mask, uint16_t* y,
+                                    void* workspace, size_t ws_bytes, moet_stream stream);
+
+/* ------------------------------------------------------------------------
  * moet_moe_forward_static -- moet_moe_forward for callers that cannot
  * allocate device memory (a plug-in given only its input and output buffers,
  * code inside a runtime whose device allocator belongs to someone else, a C

@@ -54,12 +54,18 @@ def ffn(x: np.ndarray, w1: np.ndarray, w2: np.ndarray) -> np.ndarray:
 
 
 def moe_forward(x, idx, w, fc1, fc2, delta_slot=None, dfc1=None, dfc2=None, gate=None,
-                tokens=None):
+                tokens=None, resident=None):
     """y [T, H] fp64.  ``x`` holds fp64 activation values (exact bf16 values).
 
     ``tokens`` optionally restricts the computation to a subset of token ids
     (rows of the returned array outside the subset are zero); used to check
     sampled outputs of full-size layers.
+
+    ``resident`` optionally marks which experts are resident on the GPU (bool
+    [E]); a pair routed to an expert that is not contributes zero (README
+    "Frontier MoE on consumer Blackwell (SM120)", "When the model doesn't fit at
+    all -- the GPU as an expert cache": the missing expert's contribution is
+    zeroed and counted, the routing weights are left as they are).
     """
     x = np.asarray(x, dtype=np.float64)
     T, H = x.shape
@@ -71,6 +77,8 @@ def moe_forward(x, idx, w, fc1, fc2, delta_slot=None, dfc1=None, dfc2=None, gate
     for t in tok_set:
         for j in range(k):
             e = int(idx[t, j])
+            if resident is not None and not resident[e]:
+                continue
             wd = bool(use_delta and gate[t] and delta_slot[e] >= 0)
             pairs.setdefault((e, wd), []).append((t, j))
     for (e, wd), plist in sorted(pairs.items()):

@@ -177,3 +177,29 @@ def test_forward_k1_is_one_mlp_and_delta_moves_toward_nvfp4():
     g, u = x @ n1[:I].T, x @ n1[I:].T
     yn = (g / (1 + np.exp(-g)) * u) @ n2.T
     assert np.linalg.norm(yd - yn) < 0.2 * np.linalg.norm(y - yn)
+
+
+def test_forward_missing_experts_contribute_zero():
+    """README "When the model doesn't fit at all": a routed expert that is not resident
+    contributes zero (routing weights untouched).  Pinned against the full forward minus a
+    textbook SwiGLU MLP (numpy matmuls on the dequantised weights) for every missing pair."""
+    cfg, x, idx, w, fc, dfc, slot, gate, _ = _tiny_layer()
+    I = cfg.I
+    routed = sorted(set(int(e) for e in idx.ravel()))
+    missing = set(routed[::2])
+    resident = np.array([e not in missing for e in range(cfg.E)])
+    y_full = moe.moe_forward(x, idx, w, fc[1], fc[2])
+    y_res = moe.moe_forward(x, idx, w, fc[1], fc[2], resident=resident)
+    expect = np.zeros_like(y_full)
+    for t in range(cfg.T):
+        for j in range(cfg.k):
+            e = int(idx[t, j])
+            if e not in missing:
+                continue
+            a1 = requant.dequant_2bit(fc[1]["sign"][e], fc[1]["mag"][e], fc[1]["s16"][e], fc[1]["scale_2"][e])
+            a2 = requant.dequant_2bit(fc[2]["sign"][e], fc[2]["mag"][e], fc[2]["s16"][e], fc[2]["scale_2"][e])
+            g, u = a1[:I] @ x[t], a1[I:] @ x[t]
+            expect[t] += w[t, j] * (a2 @ (g / (1 + np.exp(-g)) * u))
+    assert missing and np.allclose(y_full - y_res, expect, rtol=1e-10, atol=1e-13)
+    assert np.array_equal(moe.moe_forward(x, idx, w, fc[1], fc[2], resident=np.ones(cfg.E, bool)), y_full)
+    assert not np.any(moe.moe_forward(x, idx, w, fc[1], fc[2], resident=np.zeros(cfg.E, bool)))
