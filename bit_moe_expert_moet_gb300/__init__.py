@@ -13,6 +13,7 @@ Entry points (same names as the C ABI without the ``moet_`` prefix):
   moe_forward      the MoE layer y = sum_j w_j FFN_e(x) on the 2-bit planes
   moe_forward_pooled  the same over a pool of resident experts (slot table,
                    non-resident experts contribute zero and are counted)
+  gate_from_confidence  the confidence gate: gate mask and the experts to promote
 """
 from ._lib import (  # noqa: F401
     MoetError,
@@ -31,6 +32,7 @@ from ._lib import (  # noqa: F401
     forward_workspace_size,
     moe_forward,
     moe_forward_pooled,
+    gate_from_confidence,
     moe_forward_static,
     FORWARD_STATIC_SCRATCH_BYTES,
 )

@@ -58,6 +58,8 @@ lib.moet_moe_forward.argtypes = [_i, _i, _i, _i, _i, _p, _p, _p, _p, _p,
                                  ctypes.POINTER(_Planes), ctypes.POINTER(_Planes),
                                  _p, _i, ctypes.POINTER(_Nvfp4), ctypes.POINTER(_Nvfp4),
                                  _p, _p, _p, _sz, _p]
+lib.moet_gate_from_confidence.restype = _i
+lib.moet_gate_from_confidence.argtypes = [_i, _i, _i, _p, ctypes.c_float, _p, _p, _p, _p, _p, _p]
 lib.moet_moe_forward_pooled.restype = _i
 lib.moet_moe_forward_pooled.argtypes = [_i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _i,
                                         ctypes.POINTER(_Planes), ctypes.POINTER(_Planes),
@@ -202,6 +204,24 @@ def moe_forward(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
         _ptr(gate_mask, torch.uint8, "gate_mask"), _ptr(y, None, "y"),
         _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+
+
+def gate_from_confidence(conf: torch.Tensor, tau: float, topk_idx: torch.Tensor, gate_mask: torch.Tensor,
+                         delta_slot: Optional[torch.Tensor] = None, need_mask: Optional[torch.Tensor] = None,
+                         counts: Optional[torch.Tensor] = None, n_experts: Optional[int] = None, stream=None):
+    """gate_mask[t] = conf[t] < tau (u8); need_mask[e] = 1 for experts a gated token routes to that
+    have no delta slot; counts (int32 [2]) += (gated tokens, such pairs)."""
+    T, k = topk_idx.shape
+    E = n_experts if n_experts is not None else (delta_slot.shape[0] if delta_slot is not None else
+                                                 (need_mask.shape[0] if need_mask is not None else None))
+    if E is None:
+        raise ValueError("n_experts is needed without delta_slot or need_mask")
+    if counts is not None and (counts.dtype != torch.int32 or counts.numel() < 2):
+        raise TypeError("counts must be an int32 tensor of at least two elements (u32 counters)")
+    _check("moet_gate_from_confidence", lib.moet_gate_from_confidence(
+        T, E, k, _ptr(conf, torch.float32, "conf"), float(tau), _ptr(topk_idx, torch.int32, "topk_idx"),
+        _ptr(delta_slot, torch.int32, "delta_slot"), _ptr(gate_mask, torch.uint8, "gate_mask"),
+        _ptr(need_mask, torch.uint8, "need_mask"), _ptr(counts, None, "counts"), _stream(stream)))
 
 
 def moe_forward_pooled(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,

@@ -195,11 +195,61 @@ static moet_status launch_route(int T, int E, int k, const float* logits, int32_
   return MOET_OK;
 }
 
+// ---------------------------------------------------------------- confidence gate
+// One thread per (token, slot j) pair: the gate of its token, and for gated tokens whether its
+// expert lacks a delta slot.  Thread j = 0 of a token writes the gate and counts it.
+__global__ void __launch_bounds__(256) gate_kernel(int T, int E, int k, const float* __restrict__ conf, float tau,
+                                                   const int32_t* __restrict__ topk_idx,
+                                                   const int32_t* __restrict__ delta_slot,
+                                                   uint8_t* __restrict__ gate_mask, uint8_t* __restrict__ need_mask,
+                                                   unsigned* __restrict__ counts) {
+  const long long p = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (p >= (long long)T * k) return;
+  const int t = (int)(p / k), j = (int)(p - (long long)t * k);
+  const bool gated = __ldg(conf + t) < tau;                 // false for NaN
+  if (j == 0) {
+    gate_mask[t] = gated ? 1 : 0;
+    if (gated && counts != nullptr) atomicAdd(counts, 1u);
+  }
+  if (!gated) return;
+  const int e = __ldg(topk_idx + p);
+  if (e < 0 || e >= E) {
+    record_error(MOET_ERR_DEVICE_INDEX);
+    return;
+  }
+  const bool cached = delta_slot != nullptr && __ldg(delta_slot + e) >= 0;
+  if (!cached) {
+    if (need_mask != nullptr) need_mask[e] = 1;
+    if (counts != nullptr) atomicAdd(counts + 1, 1u);
+  }
+}
+
 }  // namespace moet
 
 using namespace moet;
 
 MOET_ERROR_ACCESSOR(moet_internal_error_route)
+
+extern "C" moet_status moet_gate_from_confidence(int T, int E, int k, const float* conf, float tau,
+                                                 const int32_t* topk_idx, const int32_t* delta_slot,
+                                                 uint8_t* gate_mask, uint8_t* need_mask, uint32_t* counts,
+                                                 moet_stream stream) {
+  if (T < 1 || E < 1 || E > 1024 || k < 1 || k > 16 || k > E) return MOET_ERR_SHAPE;
+  if ((long long)T * k > (1LL << 30)) return MOET_ERR_UNSUPPORTED;
+  if (!conf || !topk_idx || !gate_mask) return MOET_ERR_INVALID_ARG;
+  if (((uintptr_t)conf & 3) || ((uintptr_t)topk_idx & 3) || ((uintptr_t)delta_slot & 3) ||
+      ((uintptr_t)counts & 3))
+    return MOET_ERR_ALIGN;
+  cudaStream_t st = (cudaStream_t)stream;
+  const long long n = (long long)T * k;
+  {
+    ProfScope ps(MOET_K_ROUTE, st);
+    gate_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(T, E, k, conf, tau, topk_idx, delta_slot, gate_mask,
+                                                             need_mask, counts);
+  }
+  MOET_CUDA_TRY(cudaGetLastError());
+  return MOET_OK;
+}
 
 extern "C" moet_status moet_route_topk(int T, int E, int k, const float* logits, int32_t* topk_idx,
                                        float* topk_w, int32_t* expert_offsets, int32_t* perm,

@@ -117,6 +117,31 @@ moet_status moet_route_topk(int T, int E, int k, const float* logits, int32_t* t
                             moet_stream stream);
 
 /* ------------------------------------------------------------------------
+ * moet_gate_from_confidence -- the confidence gate's producer.
+ * README "Frontier MoE on consumer Blackwell (SM120)", "How it fits" (the FP4
+ * tier): a confidence gate re-runs low-confidence steps at FP4 -- it promotes
+ * the step's routed experts into the delta cache, replays the step once and
+ * decides again.  The pages do not define the confidence; here it is one
+ * float per token supplied by the caller (e.g. the probability of the token
+ * the previous step sampled), and the gate of token t is conf[t] < tau
+ * (strict; a NaN confidence never gates).
+ *   1 <= T, 1 <= E <= 1024, 1 <= k <= min(16, E).
+ *   conf [T] fp32 (read); topk_idx [T, k] i32 (read, as from moet_route_topk);
+ *   delta_slot [E] i32 (read; NULL = no expert is cached).
+ *   gate_mask [T] u8 (written: 1 = gated).
+ *   need_mask [E] u8 (nullable; entry e set to 1 when a gated token routes to
+ *     e and e has no delta slot -- the experts to promote before the replay;
+ *     never cleared here).
+ *   counts: nullable u32 [2]; counts[0] += gated tokens, counts[1] += (gated
+ *     token, expert) pairs whose expert has no delta slot (atomic; the caller
+ *     resets them).
+ * An expert id outside [0, E) is a device index error; its pair is skipped. */
+moet_status moet_gate_from_confidence(int T, int E, int k, const float* conf, float tau,
+                                      const int32_t* topk_idx, const int32_t* delta_slot,
+                                      uint8_t* gate_mask, uint8_t* need_mask, uint32_t* counts,
+                                      moet_stream stream);
+
+/* ------------------------------------------------------------------------
  * moet_moe_forward -- the MoE expert layer on 2-bit planes with the delta.
  * README "How it fits" bullet 2: y_t = sum_j w_tj FFN_{e_tj}(x_t), with
  * FFN_e(x) = W2_e (SiLU(Wg_e x) * (Wu_e x)) and SiLU(z) = z / (1 + e^-z).

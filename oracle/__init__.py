@@ -26,4 +26,4 @@ Every function here is pinned by a ``-m "not gpu"`` test in ``tests/`` to
 something other than itself (brute force, closed forms, invariants or a
 hand-worked example); the one exception is stated in ``moe.py``.
 """
-from . import formats, nvfp4, requant, route, moe  # noqa: F401
+from . import formats, nvfp4, requant, route, moe, gate  # noqa: F401

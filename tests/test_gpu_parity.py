@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import workloads as W
-from oracle import moe as omoe, nvfp4 as onv, requant as orq, route as oroute
+from oracle import gate as ogate, moe as omoe, nvfp4 as onv, requant as orq, route as oroute
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -388,6 +388,72 @@ def test_forward_pooled_slot_out_of_range_sets_device_flag(moet):
     moet.moe_forward_pooled(x, idx, w, off, perm, dev(slot), pp[1], pp[2], y, ws)
     assert moet.last_device_error() == 8                        # MOET_ERR_DEVICE_INDEX
     assert torch.isfinite(y.float()).all()
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 256, 8), (64, 256, 8), (300, 16, 4)])
+def test_gate_from_confidence_bit_exact(moet, T, E, k):
+    rng = np.random.default_rng(100 + T)
+    conf = rng.random(T).astype(np.float32)
+    conf[::7] = np.float32(0.6)                              # exactly tau: not gated
+    conf[1::11] = np.nan
+    conf[2::13] = -np.inf
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    slot = np.full(E, -1, np.int32)
+    cached = rng.permutation(E)[: E // 3]
+    slot[cached] = np.arange(len(cached), dtype=np.int32)
+    gate = torch.zeros(T, dtype=torch.uint8, device=DEV)
+    need = torch.zeros(E, dtype=torch.uint8, device=DEV)
+    counts = torch.zeros(2, dtype=torch.int32, device=DEV)
+    moet.gate_from_confidence(dev(conf), 0.6, dev(idx), gate, delta_slot=dev(slot), need_mask=need, counts=counts)
+    assert moet.last_device_error() == 0
+    g, nd, ng, npairs = ogate.gate_from_confidence(conf, 0.6, idx, slot)
+    assert np.array_equal(host(gate), g)
+    assert np.array_equal(host(need).astype(bool), nd)
+    assert host(counts).tolist() == [ng, npairs]
+
+
+def test_gate_replay_promotes_and_decides_again(moet):
+    """The gate's replay: gate from confidence, promote every expert it asks for into the delta
+    cache (their delta codes are already in the pool; the slot table is updated), replay the
+    forward; the result equals the oracle with those slots, and a second decision asks for
+    nothing."""
+    H, I, E, k, T = 1024, 256, 16, 4, 33
+    rng = np.random.default_rng(110)
+    # every expert's delta in pool slot e; at first only a few experts hold a slot
+    ref, gp = _make_layer(moet, H, I, E, np.arange(E, dtype=np.int32), rng=rng)
+    slot = np.full(E, -1, np.int32)
+    slot[[2, 7, 11]] = [2, 7, 11]
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    xb = W.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    conf = rng.random(T).astype(np.float32)
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    off = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    perm = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    moet.route_topk(dev(logits), k, idx, w, off, perm)
+    gate = torch.zeros(T, dtype=torch.uint8, device=DEV)
+    need = torch.zeros(E, dtype=torch.uint8, device=DEV)
+    counts = torch.zeros(2, dtype=torch.int32, device=DEV)
+    moet.gate_from_confidence(dev(conf), 0.6, idx, gate, delta_slot=dev(slot), need_mask=need, counts=counts)
+    # the oracle decides on its own routing; the GPU's decision must match it bit for bit
+    oi, _ = oroute.route_topk(logits, k)
+    gate_o, need_o, _, npairs_o = ogate.gate_from_confidence(conf, 0.6, oi, slot)
+    assert np.array_equal(host(gate), gate_o) and np.array_equal(host(need).astype(bool), need_o)
+    assert need_o.any() and host(counts)[1] == npairs_o
+    slot2 = slot.copy()
+    slot2[need_o] = np.flatnonzero(need_o).astype(np.int32)            # promote
+    x = dev(xb.view(np.int16)).view(torch.bfloat16)
+    ws = torch.empty(moet.forward_workspace_size(T, H, I, E, k), dtype=torch.uint8, device=DEV)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    moet.moe_forward(x, idx, w, off, perm, gp[1], gp[2], y, ws, delta_slot=dev(slot2), dfc1=gp[1, "d"],
+                     dfc2=gp[2, "d"], gate_mask=gate)
+    assert moet.last_device_error() == 0
+    yo = _oracle_forward(logits, xb, k, ref, np.arange(E, dtype=np.int32), gate_o, E, slot=slot2)
+    check_y(y.float().cpu().numpy(), yo)
+    # decide again with the promoted table: nothing left to promote
+    need.zero_(); counts.zero_()
+    moet.gate_from_confidence(dev(conf), 0.6, idx, gate, delta_slot=dev(slot2), need_mask=need, counts=counts)
+    assert not host(need).any() and host(counts)[1] == 0
 
 
 def test_forward_is_deterministic(moet):

@@ -203,3 +203,19 @@ def test_forward_missing_experts_contribute_zero():
     assert missing and np.allclose(y_full - y_res, expect, rtol=1e-10, atol=1e-13)
     assert np.array_equal(moe.moe_forward(x, idx, w, fc[1], fc[2], resident=np.ones(cfg.E, bool)), y_full)
     assert not np.any(moe.moe_forward(x, idx, w, fc[1], fc[2], resident=np.zeros(cfg.E, bool)))
+
+
+def test_gate_from_confidence_worked_example():
+    """The gate: conf < tau strictly, NaN never gated; experts to promote = routed by a gated token
+    and without a delta slot (each pair counted)."""
+    from oracle import gate as ogate
+    conf = np.array([0.9, 0.59, 0.6, np.nan, -np.inf, 0.2], dtype=np.float32)
+    idx = np.array([[0, 1], [1, 2], [3, 0], [2, 3], [0, 3], [2, 1]], dtype=np.int32)
+    slot = np.array([-1, 0, -1, 1], dtype=np.int32)        # experts 1 and 3 cached
+    gate, need, n_gated, n_pairs = ogate.gate_from_confidence(conf, 0.6, idx, slot)
+    assert gate.tolist() == [0, 1, 0, 0, 1, 1]              # 0.6 is not below 0.6; NaN never
+    # gated tokens 1 (experts 1, 2), 4 (0, 3), 5 (2, 1): uncached 2, 0, 2
+    assert need.tolist() == [True, False, True, False]
+    assert (n_gated, n_pairs) == (3, 3)
+    g2, need2, _, n2 = ogate.gate_from_confidence(conf, 0.6, idx, None)   # nothing cached
+    assert g2.tolist() == gate.tolist() and need2.tolist() == [True, True, True, True] and n2 == 6
