@@ -456,6 +456,42 @@ def test_gate_replay_promotes_and_decides_again(moet):
     assert not host(need).any() and host(counts)[1] == 0
 
 
+@pytest.mark.parametrize("T", [300, 600])
+def test_forward_all_tokens_on_the_same_experts(moet, T):
+    """Degenerate routing: every token picks the same k experts (a logit bias), so each of them
+    gets T pairs split into many work items with a ragged last one (16-pair items in the decode
+    engine at T=300, 256-pair items in the prefill engine at T=600); the other experts get none."""
+    H, I, E, k = 512, 256, 16, 4
+    rng = np.random.default_rng(120 + T)
+    dset = np.array([3, 9], dtype=np.int32)
+    ref, gp = _make_layer(moet, H, I, E, dset, rng=rng)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    logits[:, [3, 5, 9, 12]] += 50.0
+    xb = W.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    gate = (rng.random(T) < 0.4).astype(np.uint8)
+    yg, err = _run_forward(moet, logits, xb, k, gp, E, H, dset, gate)
+    assert err == 0
+    check_y(yg, _oracle_forward(logits, xb, k, ref, dset, gate, E))
+
+
+def test_forward_max_experts_and_k(moet):
+    """E = 1024 experts and k = 16 (the interface's maxima) on random planes: most routed experts
+    get a single pair, each token sums 16 pairs."""
+    H, I, E, k, T = 256, 256, 1024, 16, 5
+    rng = np.random.default_rng(130)
+    ref, gp = {}, {}
+    for f, (N, K) in ((1, (2 * I, H)), (2, (H, I))):
+        pl = _random_planes(rng, E, N, K)
+        ref[f] = pl
+        gp[f] = moet.Planes(dev(pl["sign"].view(np.int32)), dev(pl["mag"].view(np.int32)), dev(pl["s16"]),
+                            dev(pl["scale_2"]))
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    xb = W.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    yg, err = _run_forward(moet, logits, xb, k, gp, E, H)
+    assert err == 0
+    check_y(yg, _oracle_forward(logits, xb, k, ref))
+
+
 def test_forward_is_deterministic(moet):
     H, I, E, k, T = 1024, 256, 16, 4, 100
     rng = np.random.default_rng(40)
