@@ -381,6 +381,36 @@ def capture_graph(torch, fn):
     return g
 
 
+def time_requant_fp8(moet, torch, dev, steps=3, n_mat=16):
+    """moet_requant_fp8_2bit over n_mat FP8 block-quant matrices of the DeepSeek-V3 FC1 shape
+    [2I, H] = [4096, 7168] (random codes, the NaN codes excluded; random 128x128 block scales),
+    with the delta.  Per weight 1 B in, 0.3125 + 0.5625 B out."""
+    N, K = 4096, 7168
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    codes = torch.randint(0, 256, (n_mat, N, K), dtype=torch.uint8, device=dev, generator=g)
+    codes[(codes & 0x7F) == 0x7F] ^= 1
+    bs = torch.rand((n_mat, N // 128, K // 128), device=dev, generator=g) * 0.02 + 0.001
+    sc2 = torch.empty(n_mat, dtype=torch.float32, device=dev)
+    sign = torch.empty((n_mat, N, K // 32), dtype=torch.int32, device=dev)
+    mag = torch.empty_like(sign)
+    s16 = torch.empty((n_mat, N, K // 16), dtype=torch.uint8, device=dev)
+    dcodes = torch.empty((n_mat, N, K // 2), dtype=torch.uint8, device=dev)
+    ds4 = torch.empty_like(s16)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def run():
+        moet.requant_fp8_2bit(codes, bs, sc2, sign, mag, s16, dcodes, ds4)
+
+    ts = time_steps(torch, run, steps, 1, flush)
+    ms = statistics.median(ts)
+    weights = n_mat * N * K
+    moved = weights * (1 + 0.3125 + 0.5625)
+    return {"matrices": n_mat, "shape": [N, K], "weights": weights, "ms_per_pass": ms,
+            "gweights_per_s": weights / (ms * 1e-3) / 1e9, "gbs": moved / (ms * 1e-3) / 1e9,
+            "bound": "fp64 ALU (exact ratio rounding in fp64)"}
+
+
 def time_requant(moet, torch, dev, steps=3):
     """moet_requant_2bit over the full NVFP4 expert set of the 1T-class layer (768 matrices)."""
     cfg = W.CONFIGS["kimi_layer"]
@@ -615,6 +645,7 @@ def run_ours(args, rank, world, local):
                             "tokens_per_s": cfg.T / (med * 1e-3), "ms_per_step_median": med}
         del gp_
         extras["requant"] = time_requant(moet, torch, dev)
+        extras["requant_fp8"] = time_requant_fp8(moet, torch, dev)
         extras["requant"]["frac_of_hbm_peak"] = extras["requant"]["gbs"] / peak
 
     cpu = None

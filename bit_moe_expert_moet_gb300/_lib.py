@@ -58,6 +58,8 @@ lib.moet_moe_forward.argtypes = [_i, _i, _i, _i, _i, _p, _p, _p, _p, _p,
                                  ctypes.POINTER(_Planes), ctypes.POINTER(_Planes),
                                  _p, _i, ctypes.POINTER(_Nvfp4), ctypes.POINTER(_Nvfp4),
                                  _p, _p, _p, _sz, _p]
+lib.moet_requant_fp8_2bit.restype = _i
+lib.moet_requant_fp8_2bit.argtypes = [_i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p]
 lib.moet_gate_from_confidence.restype = _i
 lib.moet_gate_from_confidence.argtypes = [_i, _i, _i, _p, ctypes.c_float, _p, _p, _p, _p, _p, _p]
 lib.moet_moe_forward_pooled.restype = _i
@@ -203,6 +205,19 @@ def moe_forward(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
         ctypes.byref(d1) if d1 is not None else None, ctypes.byref(d2) if d2 is not None else None,
         _ptr(gate_mask, torch.uint8, "gate_mask"), _ptr(y, None, "y"),
         _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def requant_fp8_2bit(codes: torch.Tensor, bscale: torch.Tensor, scale_2: torch.Tensor, sign: torch.Tensor,
+                     mag: torch.Tensor, s16: torch.Tensor, dcodes: Optional[torch.Tensor] = None,
+                     ds4: Optional[torch.Tensor] = None, stream=None):
+    """FP8 block-quant codes u8 [M, N, K] with fp32 128x128 block scales [M, ceil(N/128), ceil(K/128)]
+    -> scale_2 fp32 [M], planes and s16 (+ delta codes/scales), all written."""
+    M, N, K = codes.shape
+    _check("moet_requant_fp8_2bit", lib.moet_requant_fp8_2bit(
+        M, N, K, _ptr(codes, torch.uint8, "codes"), _ptr(bscale, torch.float32, "bscale"),
+        _ptr(scale_2, torch.float32, "scale_2"), _ptr(sign, torch.int32, "sign"), _ptr(mag, torch.int32, "mag"),
+        _ptr(s16, torch.uint8, "s16"), _ptr(dcodes, torch.uint8, "dcodes"), _ptr(ds4, torch.uint8, "ds4"),
         _stream(stream)))
 
 

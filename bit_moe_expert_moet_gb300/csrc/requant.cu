@@ -253,6 +253,181 @@ using namespace moet;
 
 MOET_ERROR_ACCESSOR(moet_internal_error_requant)
 
+// ---------------------------------------------------------------- FP8 block-quant input
+// README "How it fits -- 2-bit experts at FP4 quality", last paragraph: FP8 block-quant
+// checkpoints (an e4m3 code per weight, one fp32 scale per 128 x 128 block) are requantised to
+// the same planes.  W = e4m3(code) * block scale is exact in fp64 (4 + 24 significant bits), so
+// the rule is the NVFP4 one applied to W with scale_2 = fp32(fp64(amax) / 1344): every ratio is
+// rounded once by exact fp64 comparisons (all products of the short significands involved fit in
+// fp64's 53 bits), no quotient is rounded and reused.
+constexpr int kFp8Block = 128;
+
+// e4m3 satfinite RNE of a / d for a >= 0, d > 0, both exact in fp64 with d * (two neighbouring
+// e4m3 values) exact: a guess from the rounded quotient, corrected against the doubled midpoints.
+__device__ __forceinline__ uint32_t e4m3_rne_ratio_dd(double a, double d) {
+  if (!(a > 0.0)) return 0u;                          // zero (also for an all-zero matrix, d = 0)
+  uint32_t c = f32_to_e4m3_rn((float)(a / d));
+  const double a2 = 2.0 * a;
+  if (c < 126u) {
+    const double m2 = d * ((double)e4m3_to_f32(c) + (double)e4m3_to_f32(c + 1));
+    if (a2 > m2 || (a2 == m2 && (c & 1u))) c += 1;
+  }
+  if (c > 0u) {
+    const double m2 = d * ((double)e4m3_to_f32(c - 1) + (double)e4m3_to_f32(c));
+    if (a2 < m2 || (a2 == m2 && (c & 1u))) c -= 1;
+  }
+  return c;
+}
+
+// e2m1 magnitude code of RNE(a / s), saturating, ties to even, by exact comparison with the
+// seven midpoints scaled by s (fp64).
+__device__ __forceinline__ uint32_t e2m1_rne_mag_d(double a, double s) {
+  uint32_t c = 0;
+  c += (a > 0.25 * s);
+  c += (a >= 0.75 * s);
+  c += (a > 1.25 * s);
+  c += (a >= 1.75 * s);
+  c += (a > 2.5 * s);
+  c += (a >= 3.5 * s);
+  c += (a > 5.0 * s);
+  return c;
+}
+
+__device__ __forceinline__ double fp8_bscale(const float* bscale, int n, int k, int nbk) {
+  return (double)__ldg(bscale + (size_t)(n / kFp8Block) * nbk + k / kFp8Block);
+}
+
+// One CTA per matrix: amax over |W| in fp64 (the e4m3 magnitude order is the code order, so
+// each 16-code chunk contributes its largest code once), then scale_2 = fp32(fp64(amax) / 1344).
+__global__ void __launch_bounds__(1024) fp8_scale2_kernel(int N, int K, const uint8_t* __restrict__ codes,
+                                                          const float* __restrict__ bscale,
+                                                          float* __restrict__ scale_2) {
+  const int m = blockIdx.x;
+  const int nbn = (N + kFp8Block - 1) / kFp8Block, nbk = (K + kFp8Block - 1) / kFp8Block;
+  const uint8_t* cm = codes + (size_t)m * N * K;
+  const float* bm = bscale + (size_t)m * nbn * nbk;
+  const long long chunks = (long long)N * K / 16;
+  double mx = 0.0;
+  for (long long i = threadIdx.x; i < chunks; i += blockDim.x) {
+    const uint4 c = __ldg(reinterpret_cast<const uint4*>(cm) + i);
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    uint32_t top = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) top = max(top, (w[q] >> (8 * b)) & 0x7Fu);
+    const long long e0 = i * 16;
+    const int n = (int)(e0 / K), k = (int)(e0 - (long long)n * K);
+    mx = fmax(mx, (double)e4m3_to_f32(top) * fp8_bscale(bm, n, k, nbk));
+  }
+  __shared__ double red[32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    mx = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (threadIdx.x == 0) scale_2[m] = __double2float_rn(__ddiv_rn(mx, 1344.0));
+  }
+}
+
+// One thread per 32-weight group of a row: 32 codes in, one sign and one magnitude word, two s16
+// bytes (and 16 delta code bytes + two delta scale bytes) out.
+__global__ void __launch_bounds__(256) requant_fp8_kernel(
+    int M, int N, int K, const uint8_t* __restrict__ codes, const float* __restrict__ bscale,
+    const float* __restrict__ scale_2, uint32_t* __restrict__ sign_out, uint32_t* __restrict__ mag_out,
+    uint16_t* __restrict__ s16_out, uint4* __restrict__ dcodes_out, uint16_t* __restrict__ ds4_out) {
+  const long long gpm = (long long)N * (K / 32);
+  const long long n_groups = (long long)M * gpm;
+  const int nbn = (N + kFp8Block - 1) / kFp8Block, nbk = (K + kFp8Block - 1) / kFp8Block;
+  for (long long gi = (long long)blockIdx.x * blockDim.x + threadIdx.x; gi < n_groups;
+       gi += (long long)gridDim.x * blockDim.x) {
+    const int m = (int)(gi / gpm);
+    const long long r = gi - (long long)m * gpm;
+    const int n = (int)(r / (K / 32)), k0 = (int)(r - (long long)n * (K / 32)) * 32;
+    const double s2 = (double)__ldg(scale_2 + m);
+    const double bs = fp8_bscale(bscale + (size_t)m * nbn * nbk, n, k0, nbk);
+    const uint4* src = reinterpret_cast<const uint4*>(codes + ((size_t)m * N + n) * K + k0);
+    const uint4 c0 = __ldg(src), c1 = __ldg(src + 1);
+    const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    uint32_t sign = 0, mag = 0, s16pair = 0, ds4pair = 0;
+    uint32_t dwords[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      double wv[16];
+      double bmax = 0.0;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t c = (words[4 * b + (j >> 2)] >> (8 * (j & 3))) & 0xFFu;
+        const double a = (double)e4m3_to_f32(c & 0x7Fu) * bs;          // exact
+        wv[j] = (c & 0x80u) ? -a : a;
+        bmax = fmax(bmax, a);
+        sign |= (c >> 7) << (16 * b + j);
+      }
+      const uint32_t s16 = e4m3_rne_ratio_dd(bmax, 3.0 * s2);
+      const double lvl = (double)e4m3_to_f32(s16) * s2;                 // s16 scale_2, exact
+      s16pair |= s16 << (8 * b);
+      double d[16];
+      double dmax = 0.0;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t mg = fabs(wv[j]) >= 2.0 * lvl;
+        mag |= mg << (16 * b + j);
+        const double q = (mg ? 3.0 : 1.0) * lvl;
+        d[j] = wv[j] - (((sign >> (16 * b + j)) & 1u) ? -q : q);          // exact
+        dmax = fmax(dmax, fabs(d[j]));
+      }
+      if (dcodes_out != nullptr) {
+        const uint32_t ds4 = e4m3_rne_ratio_dd(dmax, 6.0 * s2);
+        const double step = (double)e4m3_to_f32(ds4) * s2;
+        ds4pair |= ds4 << (8 * b);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const uint32_t dm = step > 0.0 ? e2m1_rne_mag_d(fabs(d[j]), step) : 0u;
+          const uint32_t code = dm | ((d[j] < 0.0 && dm != 0u) ? 8u : 0u);
+          dwords[2 * b + (j >> 3)] |= code << (4 * (j & 7));
+        }
+      }
+    }
+    sign_out[gi] = sign;
+    mag_out[gi] = mag;
+    s16_out[gi] = (uint16_t)s16pair;
+    if (dcodes_out != nullptr) {
+      dcodes_out[gi] = make_uint4(dwords[0], dwords[1], dwords[2], dwords[3]);
+      ds4_out[gi] = (uint16_t)ds4pair;
+    }
+  }
+}
+
+extern "C" moet_status moet_requant_fp8_2bit(int M, int N, int K, const uint8_t* codes, const float* bscale,
+                                             float* scale_2, uint32_t* sign, uint32_t* mag, uint8_t* s16,
+                                             uint8_t* dcodes, uint8_t* ds4, moet_stream stream) {
+  if (M < 1 || N < 1 || K < 32 || K % 32 != 0) return MOET_ERR_SHAPE;
+  if (!codes || !bscale || !scale_2 || !sign || !mag || !s16) return MOET_ERR_INVALID_ARG;
+  if ((dcodes == nullptr) != (ds4 == nullptr)) return MOET_ERR_INVALID_ARG;
+  if (((uintptr_t)codes & 15) || ((uintptr_t)bscale & 3) || ((uintptr_t)scale_2 & 3) ||
+      ((uintptr_t)sign & 3) || ((uintptr_t)mag & 3) || ((uintptr_t)s16 & 1))
+    return MOET_ERR_ALIGN;
+  if (dcodes && (((uintptr_t)dcodes & 15) || ((uintptr_t)ds4 & 1))) return MOET_ERR_ALIGN;
+  if (M > 65535) return MOET_ERR_UNSUPPORTED;
+  cudaStream_t st = (cudaStream_t)stream;
+  const long long n_groups = (long long)M * N * (K / 32);
+  {
+    ProfScope ps(MOET_K_REQUANT, st);
+    fp8_scale2_kernel<<<M, 1024, 0, st>>>(N, K, codes, bscale, scale_2);
+  }
+  MOET_CUDA_TRY(cudaGetLastError());
+  {
+    ProfScope ps(MOET_K_REQUANT, st);
+    requant_fp8_kernel<<<grid_for(n_groups, 256), 256, 0, st>>>(M, N, K, codes, bscale, scale_2, sign, mag,
+                                                                 (uint16_t*)s16, (uint4*)dcodes, (uint16_t*)ds4);
+  }
+  MOET_CUDA_TRY(cudaGetLastError());
+  return MOET_OK;
+}
+
 extern "C" moet_status moet_requant_2bit(int M, int N, int K, const uint8_t* codes,
                                          const uint8_t* s4, uint32_t* sign, uint32_t* mag,
                                          uint8_t* s16, uint8_t* dcodes, uint8_t* ds4,

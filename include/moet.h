@@ -102,6 +102,29 @@ moet_status moet_requant_2bit(int M, int N, int K, const uint8_t* codes, const u
                               uint8_t* dcodes, uint8_t* ds4, moet_stream stream);
 
 /* ------------------------------------------------------------------------
+ * moet_requant_fp8_2bit -- FP8 block-quant weights -> 2-bit planes (+ delta).
+ * README "How it fits -- 2-bit experts at FP4 quality", last paragraph: FP8
+ * block-quant checkpoints are requantised to the sign-symmetric codebook at
+ * load like the NVFP4 ones.  A matrix holds an e4m3 code per weight and one
+ * fp32 scale per 128 x 128 block: W = e4m3(code) * bscale (exact in fp64).
+ * The pages give no formula for this input; this library applies the NVFP4
+ * rule of moet_requant_2bit to W with a per-matrix
+ *   scale_2 = fp32(fp64(amax |W|) / 1344)      (1344 = 3 * 448),
+ * so the largest block's s16 lands at 448:
+ *   s16 = e4m3 satfinite RNE(max_b |W| / (3 scale_2)); sign = the code's sign
+ *   bit; mag = |W| >= 2 s16 scale_2; the delta is the NVFP4 residual of
+ *   W - q s16 scale_2 on the same scale_2 (scale e4m3 RNE(max|d| / (6 scale_2)),
+ *   codes e2m1 RNE, zero as +0).  Every ratio is rounded once, exactly (fp64).
+ *   M >= 1 matrices of [N, K], K % 32 == 0.  codes [M, N, K] u8 (16 B aligned;
+ *   the NaN codes 0x7F/0xFF are not valid weights); bscale [M, ceil(N/128),
+ *   ceil(K/128)] fp32 (read).  scale_2 [M] fp32, sign/mag [M, N, K/32] u32,
+ *   s16 [M, N, K/16] u8 (written); dcodes [M, N, K/2] / ds4 [M, N, K/16]
+ *   (both NULL = no delta).  Outputs are bit-exact. */
+moet_status moet_requant_fp8_2bit(int M, int N, int K, const uint8_t* codes, const float* bscale,
+                                  float* scale_2, uint32_t* sign, uint32_t* mag, uint8_t* s16,
+                                  uint8_t* dcodes, uint8_t* ds4, moet_stream stream);
+
+/* ------------------------------------------------------------------------
  * moet_route_topk -- router top-k, renormalised softmax, bucketing by expert.
  * Per token: the k largest logits (ties -> lower expert id; NaN below -inf),
  * ordered by decreasing logit; w_j = exp(l_j - l_max) / sum over the k.

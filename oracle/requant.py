@@ -94,3 +94,77 @@ def dequant_2bit_units(sign: np.ndarray, mag: np.ndarray, s16: np.ndarray) -> np
 
 def dequant_2bit(sign, mag, s16, scale_2) -> np.ndarray:
     return dequant_2bit_units(sign, mag, s16) * np.float64(scale_2)
+
+
+# ---------------------------------------------------------------- FP8 block-quant input
+FP8_BLOCK = 128          # DeepSeek-style block quantisation: one fp32 scale per 128 x 128 block
+S16_TOP = 3 * 448        # scale_2 = amax / 1344: the largest block's s16 lands at 448
+
+
+def fp8_dequantize(codes: np.ndarray, bscale: np.ndarray) -> np.ndarray:
+    """[N, K] e4m3 codes with fp32 block scales [ceil(N/128), ceil(K/128)] -> exact fp64 weights
+    (an e4m3 value has 4 significant bits, an fp32 scale 24: the product is exact in fp64)."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    N, K = codes.shape
+    bs = np.asarray(bscale, dtype=np.float32).astype(np.float64)
+    rep = np.repeat(np.repeat(bs, FP8_BLOCK, axis=0)[:N], FP8_BLOCK, axis=1)[:, :K]
+    return e4m3_decode(codes) * rep
+
+
+def fp8_scale_2(codes: np.ndarray, bscale: np.ndarray) -> np.float32:
+    """Per-matrix scale_2 for an FP8 block-quant matrix: fp32(fp64(amax) / 1344), i.e. the fp64
+    quotient rounded to nearest, then to the nearest fp32 (the two roundings define it)."""
+    amax = float(np.abs(fp8_dequantize(codes, bscale)).max())
+    return np.float32(np.float64(amax) / np.float64(S16_TOP))
+
+
+def requant_fp8_2bit(codes: np.ndarray, bscale: np.ndarray, want_delta: bool = True):
+    """One [N, K] FP8 block-quant matrix -> scale_2, 2-bit planes (+ NVFP4 delta).
+    The e4m3 NaN codes (0x7F, 0xFF) are not valid weights.
+
+    README "Frontier MoE on consumer Blackwell (SM120)", §"How it fits -- 2-bit experts at FP4
+    quality", last paragraph: FP8 block-quant checkpoints are requantised to the sign-symmetric
+    codebook at load, as the NVFP4 ones are.  The pages give no formula for this input; the
+    reading here is the NVFP4 rule applied to the exact FP8 weights W with a per-matrix
+    scale_2 = amax / (3 * 448) (see fp8_scale_2):
+
+      s16[b]  = e4m3 satfinite RNE( max_b |W| / (3 scale_2) )
+      sign_k  = sign bit of the e4m3 code (so -0 maps to the negative side)
+      mag_k   = |W_k| >= 2 s16[b] scale_2
+      d_k     = W_k - q_k s16[b] scale_2                    (exact in fp64)
+      ds4[b]  = e4m3 satfinite RNE( max_b |d| / (6 scale_2) )
+      dcode_k = sign(d_k) | e2m1 satfinite RNE( |d_k| / (ds4[b] scale_2) ), zero as +0.
+
+    Every ratio is rounded once by exact comparison (formats._rne_ratio): all products of
+    the short significands involved are exact in fp64.
+    """
+    codes = np.asarray(codes, dtype=np.uint8)
+    N, K = codes.shape
+    assert K % 32 == 0
+    sc2 = fp8_scale_2(codes, bscale)
+    s2 = np.float64(sc2)
+    w = fp8_dequantize(codes, bscale)
+    aw = np.abs(w)
+    bmax = aw.reshape(N, K // 16, 16).max(axis=2)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        s16 = np.where(bmax > 0, e4m3_rne_ratio(bmax, 3.0 * s2), 0)   # a zero block (or matrix): 0
+    lvl = np.repeat(E4M3_POS[s16.astype(np.int64)], 16, axis=1) * s2      # s16 scale_2, exact
+    sign = (codes >> 7).astype(np.uint8)
+    mag = (aw >= 2.0 * lvl).astype(np.uint8)
+    out = dict(scale_2=sc2, sign=pack_bits(sign), mag=pack_bits(mag), s16=s16.astype(np.uint8))
+    if want_delta:
+        w2 = np.where(sign == 1, -1.0, 1.0) * np.where(mag == 1, 3.0, 1.0) * lvl
+        d = w - w2
+        ad = np.abs(d)
+        dmax = ad.reshape(N, K // 16, 16).max(axis=2)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            ds4 = np.where(dmax > 0, e4m3_rne_ratio(dmax, 6.0 * s2), 0)
+        step = np.repeat(E4M3_POS[ds4.astype(np.int64)], 16, axis=1) * s2
+        dmag = np.zeros((N, K), dtype=np.uint8)
+        nz = step > 0
+        dmag[nz] = e2m1_rne_ratio(ad[nz], step[nz])
+        dsign = ((d < 0) & (dmag > 0)).astype(np.uint8)
+        dcode = (dsign << 3) | dmag
+        out["dcodes"] = (dcode[:, 0::2] | (dcode[:, 1::2] << 4)).astype(np.uint8)
+        out["ds4"] = ds4.astype(np.uint8)
+    return out

@@ -133,6 +133,40 @@ def test_requant_exhaustive_scale_and_max_code(moet):
     _check_requant(_gpu_requant(moet, codes, s4), codes, s4)
 
 
+@pytest.mark.parametrize("M,N,K", [(3, 200, 96), (1, 128, 2048), (2, 7, 32)])
+def test_requant_fp8_bit_exact(moet, M, N, K):
+    """FP8 block-quant -> scale_2, planes, s16 and delta, bit-exact against the oracle; N and K
+    not multiples of the 128 x 128 scale blocks, signed zeros, +-448 and subnormals included,
+    and an all-zero matrix."""
+    rng = np.random.default_rng(140 + N + K)
+    codes = rng.integers(0, 256, (M, N, K), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] ^= 1
+    codes[0, 0, :5] = [0x00, 0x80, 0x7E, 0xFE, 0x01]
+    if M > 1:
+        codes[-1] = 0                                       # an all-zero matrix
+    bs = (rng.random((M, (N + 127) // 128, (K + 127) // 128)) * 0.02 + 0.001).astype(np.float32)
+    g = dict(scale_2=torch.empty(M, dtype=torch.float32, device=DEV),
+             sign=torch.empty((M, N, K // 32), dtype=torch.int32, device=DEV),
+             mag=torch.empty((M, N, K // 32), dtype=torch.int32, device=DEV),
+             s16=torch.empty((M, N, K // 16), dtype=torch.uint8, device=DEV),
+             dcodes=torch.empty((M, N, K // 2), dtype=torch.uint8, device=DEV),
+             ds4=torch.empty((M, N, K // 16), dtype=torch.uint8, device=DEV))
+    moet.requant_fp8_2bit(dev(codes), dev(bs), g["scale_2"], g["sign"], g["mag"], g["s16"], g["dcodes"], g["ds4"])
+    torch.cuda.synchronize()
+    for m in range(M):
+        o = orq.requant_fp8_2bit(codes[m], bs[m])
+        assert host(g["scale_2"])[m] == o["scale_2"]
+        assert np.array_equal(host(g["sign"])[m].view(np.uint32), o["sign"])
+        assert np.array_equal(host(g["mag"])[m].view(np.uint32), o["mag"])
+        for key in ("s16", "dcodes", "ds4"):
+            assert np.array_equal(host(g[key])[m], o[key]), key
+    # without the delta outputs: the same planes
+    sign2 = torch.empty_like(g["sign"]); mag2 = torch.empty_like(g["mag"]); s162 = torch.empty_like(g["s16"])
+    sc2 = torch.empty_like(g["scale_2"])
+    moet.requant_fp8_2bit(dev(codes), dev(bs), sc2, sign2, mag2, s162)
+    assert torch.equal(sign2, g["sign"]) and torch.equal(mag2, g["mag"]) and torch.equal(s162, g["s16"])
+
+
 def test_requant_without_delta_matches_planes(moet):
     rng = np.random.default_rng(23)
     codes, s4 = _random_nvfp4(rng, 2, 32, 256)

@@ -197,3 +197,83 @@ def test_requant_realistic_weights_roundtrip():
     relf = np.linalg.norm(v - w2 - dq) / np.linalg.norm(v)
     assert 0.2 < rel2 < 0.6          # 2-bit alone is coarse
     assert relf < 0.1 * rel2         # the FP4 residual recovers >90% of it
+
+
+# ---------------------------------------------------------------- FP8 block-quant input
+def _random_fp8(rng, N, K, nbs_scale=1.0):
+    codes = rng.integers(0, 256, (N, K), dtype=np.uint8)
+    nan = (codes & 0x7F) == 0x7F
+    codes[nan] ^= 1                                       # the NaN codes are not weights
+    codes[0, :5] = [0x00, 0x80, 0x7E, 0xFE, 0x01]          # +0, -0, +-448, smallest subnormal
+    bs = (rng.random(((N + 127) // 128, (K + 127) // 128)) * 0.02 + 0.001).astype(np.float32) * np.float32(nbs_scale)
+    return codes, bs
+
+
+def test_fp8_requant_matches_exact_fractions():
+    """Every integer output of the fp64 FP8 requant against the same rule evaluated in exact
+    rational arithmetic (Fraction), weight by weight."""
+    rng = np.random.default_rng(21)
+    codes, bs = _random_fp8(rng, 3, 64)
+    bs[:] = rng.choice(np.array([0.0078125, 0.3, 1.7e-3], np.float32), size=bs.shape)
+    out = requant.requant_fp8_2bit(codes, bs)
+    s2 = Fraction(float(out["scale_2"]))
+    N, K = codes.shape
+    sign = requant.unpack_bits(out["sign"]); mag = requant.unpack_bits(out["mag"])
+    dc = np.zeros((N, K), np.uint8)
+    dc[:, 0::2] = out["dcodes"] & 15; dc[:, 1::2] = out["dcodes"] >> 4
+    for n in range(N):
+        wf = [F.E4M3_VALUE_FRAC[int(c) & 0x7F] * Fraction(float(bs[n // 128, k // 128])) * (-1 if c & 0x80 else 1)
+              for k, c in enumerate(codes[n])]
+        for b in range(K // 16):
+            blk = wf[16 * b:16 * b + 16]
+            s16 = F.e4m3_rne_fraction(max(abs(x) for x in blk) / (3 * s2))
+            assert out["s16"][n, b] == s16
+            lvl = F.E4M3_VALUE_FRAC[s16] * s2
+            d = []
+            for j, x in enumerate(blk):
+                k = 16 * b + j
+                assert sign[n, k] == (codes[n, k] >> 7)
+                m = abs(x) >= 2 * lvl
+                assert mag[n, k] == m
+                q = (3 if m else 1) * lvl * (-1 if sign[n, k] else 1)
+                d.append(x - q)
+            dmax = max(abs(x) for x in d)
+            ds4 = F.e4m3_rne_fraction(dmax / (6 * s2)) if dmax else 0
+            assert out["ds4"][n, b] == ds4
+            step = F.E4M3_VALUE_FRAC[ds4] * s2
+            for j, x in enumerate(d):
+                mg = F.e2m1_rne_fraction(abs(x) / step) if step else 0
+                code = mg | (8 if (x < 0 and mg) else 0)
+                assert dc[n, 16 * b + j] == code
+
+
+def test_fp8_requant_scale_and_sign_invariance():
+    """Doubling every block scale doubles scale_2 exactly and changes no plane, scale or delta
+    code; negating every weight flips the sign plane and the delta signs only."""
+    rng = np.random.default_rng(22)
+    codes, bs = _random_fp8(rng, 200, 96)
+    a = requant.requant_fp8_2bit(codes, bs)
+    b = requant.requant_fp8_2bit(codes, bs * np.float32(2))
+    assert np.float32(b["scale_2"]) == np.float32(2) * np.float32(a["scale_2"])
+    for key in ("sign", "mag", "s16", "dcodes", "ds4"):
+        assert np.array_equal(a[key], b[key]), key
+    c = requant.requant_fp8_2bit(codes ^ np.uint8(0x80), bs)
+    assert np.array_equal(c["sign"], ~a["sign"]) and np.array_equal(c["mag"], a["mag"])
+    assert np.array_equal(c["s16"], a["s16"]) and np.array_equal(c["ds4"], a["ds4"])
+    flip = np.zeros_like(a["dcodes"])
+    lo, hi = a["dcodes"] & 15, a["dcodes"] >> 4
+    flip |= np.where((lo & 7) != 0, 8, 0).astype(np.uint8)
+    flip |= np.where((hi & 7) != 0, 0x80, 0).astype(np.uint8)
+    assert np.array_equal(c["dcodes"], a["dcodes"] ^ flip)
+
+
+def test_fp8_requant_top_block_and_zero_matrix():
+    rng = np.random.default_rng(23)
+    codes, bs = _random_fp8(rng, 4, 64)
+    out = requant.requant_fp8_2bit(codes, bs)
+    w = requant.fp8_dequantize(codes, bs)
+    top = np.unravel_index(np.argmax(np.abs(w)), w.shape)
+    assert out["s16"][top[0], top[1] // 16] == 126                  # the largest block: s16 = 448
+    z = requant.requant_fp8_2bit(np.zeros((2, 32), np.uint8), np.ones((1, 1), np.float32))
+    assert z["scale_2"] == 0 and not z["s16"].any() and not z["ds4"].any() and not z["dcodes"].any()
+    assert (z["mag"] == 0xFFFFFFFF).all()                             # |q| = 3 on a zero scale
