@@ -411,6 +411,35 @@ def time_requant_fp8(moet, torch, dev, steps=3, n_mat=16):
             "bound": "fp64 ALU (exact ratio rounding in fp64)"}
 
 
+def time_requant_mxfp4(moet, torch, dev, steps=3, n_mat=16):
+    """moet_requant_mxfp4_2bit over n_mat MXFP4 matrices of the DeepSeek-V3 FC1 shape
+    [2I, H] = [4096, 7168] (random codes, random E8M0 exponents 2^-10 .. 2^-4), with the delta.
+    Per weight 0.5 + 1/32 B in, 0.3125 + 0.5625 B out."""
+    N, K = 4096, 7168
+    g = torch.Generator(device=dev)
+    g.manual_seed(8)
+    codes = torch.randint(0, 256, (n_mat, N, K // 2), dtype=torch.uint8, device=dev, generator=g)
+    e8m0 = torch.randint(117, 124, (n_mat, N, K // 32), dtype=torch.uint8, device=dev, generator=g)
+    sc2 = torch.empty(n_mat, dtype=torch.float32, device=dev)
+    sign = torch.empty((n_mat, N, K // 32), dtype=torch.int32, device=dev)
+    mag = torch.empty_like(sign)
+    s16 = torch.empty((n_mat, N, K // 16), dtype=torch.uint8, device=dev)
+    dcodes = torch.empty((n_mat, N, K // 2), dtype=torch.uint8, device=dev)
+    ds4 = torch.empty_like(s16)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def run():
+        moet.requant_mxfp4_2bit(codes, e8m0, sc2, sign, mag, s16, dcodes, ds4)
+
+    ts = time_steps(torch, run, steps, 1, flush)
+    ms = statistics.median(ts)
+    weights = n_mat * N * K
+    moved = weights * (0.5 + 1 / 32 + 0.3125 + 0.5625)
+    return {"matrices": n_mat, "shape": [N, K], "weights": weights, "ms_per_pass": ms,
+            "gweights_per_s": weights / (ms * 1e-3) / 1e9, "gbs": moved / (ms * 1e-3) / 1e9,
+            "bound": "fp64 ALU (exact ratio rounding in fp64)"}
+
+
 def time_requant(moet, torch, dev, steps=3):
     """moet_requant_2bit over the full NVFP4 expert set of the 1T-class layer (768 matrices)."""
     cfg = W.CONFIGS["kimi_layer"]
@@ -646,6 +675,7 @@ def run_ours(args, rank, world, local):
         del gp_
         extras["requant"] = time_requant(moet, torch, dev)
         extras["requant_fp8"] = time_requant_fp8(moet, torch, dev)
+        extras["requant_mxfp4"] = time_requant_mxfp4(moet, torch, dev)
         extras["requant"]["frac_of_hbm_peak"] = extras["requant"]["gbs"] / peak
 
     cpu = None

@@ -10,6 +10,7 @@ Entry points (same names as the C ABI without the ``moet_`` prefix):
   quantize_nvfp4   fp32 weights -> NVFP4 (codes, s4, scale_2)
   requant_2bit     NVFP4 -> 2-bit sign/magnitude planes + s16 (+ delta)
   requant_fp8_2bit FP8 block-quant -> scale_2, planes + s16 (+ delta)
+  requant_mxfp4_2bit  MXFP4 (FP4 experts) -> scale_2, planes + s16 (+ delta)
   route_topk       logits -> top-k ids/weights, expert offsets, permutation
   moe_forward      the MoE layer y = sum_j w_j FFN_e(x) on the 2-bit planes
   moe_forward_pooled  the same over a pool of resident experts (slot table,
@@ -30,6 +31,7 @@ from ._lib import (  # noqa: F401
     quantize_nvfp4,
     requant_2bit,
     requant_fp8_2bit,
+    requant_mxfp4_2bit,
     route_topk,
     forward_workspace_size,
     moe_forward,

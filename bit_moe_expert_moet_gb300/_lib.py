@@ -60,6 +60,8 @@ lib.moet_moe_forward.argtypes = [_i, _i, _i, _i, _i, _p, _p, _p, _p, _p,
                                  _p, _p, _p, _sz, _p]
 lib.moet_requant_fp8_2bit.restype = _i
 lib.moet_requant_fp8_2bit.argtypes = [_i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p]
+lib.moet_requant_mxfp4_2bit.restype = _i
+lib.moet_requant_mxfp4_2bit.argtypes = [_i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p]
 lib.moet_gate_from_confidence.restype = _i
 lib.moet_gate_from_confidence.argtypes = [_i, _i, _i, _p, ctypes.c_float, _p, _p, _p, _p, _p, _p]
 lib.moet_moe_forward_pooled.restype = _i
@@ -216,6 +218,19 @@ def requant_fp8_2bit(codes: torch.Tensor, bscale: torch.Tensor, scale_2: torch.T
     M, N, K = codes.shape
     _check("moet_requant_fp8_2bit", lib.moet_requant_fp8_2bit(
         M, N, K, _ptr(codes, torch.uint8, "codes"), _ptr(bscale, torch.float32, "bscale"),
+        _ptr(scale_2, torch.float32, "scale_2"), _ptr(sign, torch.int32, "sign"), _ptr(mag, torch.int32, "mag"),
+        _ptr(s16, torch.uint8, "s16"), _ptr(dcodes, torch.uint8, "dcodes"), _ptr(ds4, torch.uint8, "ds4"),
+        _stream(stream)))
+
+
+def requant_mxfp4_2bit(codes: torch.Tensor, e8m0: torch.Tensor, scale_2: torch.Tensor, sign: torch.Tensor,
+                       mag: torch.Tensor, s16: torch.Tensor, dcodes: Optional[torch.Tensor] = None,
+                       ds4: Optional[torch.Tensor] = None, stream=None):
+    """MXFP4 codes u8 [M, N, K/2] with E8M0 scales u8 [M, N, K/32] -> scale_2 fp32 [M], planes and
+    s16 (+ delta codes/scales), all written."""
+    M, N, K2 = codes.shape
+    _check("moet_requant_mxfp4_2bit", lib.moet_requant_mxfp4_2bit(
+        M, N, 2 * K2, _ptr(codes, torch.uint8, "codes"), _ptr(e8m0, torch.uint8, "e8m0"),
         _ptr(scale_2, torch.float32, "scale_2"), _ptr(sign, torch.int32, "sign"), _ptr(mag, torch.int32, "mag"),
         _ptr(s16, torch.uint8, "s16"), _ptr(dcodes, torch.uint8, "dcodes"), _ptr(ds4, torch.uint8, "ds4"),
         _stream(stream)))

@@ -83,30 +83,41 @@ __global__ void __launch_bounds__(256) requant_2bit_kernel(
 // or above a threshold code.  Both s16 and that threshold depend only on
 // (largest code, s4); every CTA tabulates them once in shared memory with the
 // exact rounding above, and the per-weight work is integer arithmetic on
-// eight nibbles at a time.
-__device__ __forceinline__ uint32_t gather_nibble_bit3(uint32_t x) {
-  // bit 3 of nibble i -> bit i (i = 0..7)
-  uint32_t t = (x >> 3) & 0x11111111u;
-  t = (t | (t >> 3)) & 0x03030303u;
-  t = (t | (t >> 6)) & 0x000F000Fu;
-  return (t | (t >> 12)) & 0xFFu;
+// eight nibbles at a time.  The kernel is bound by integer issue, so the bit
+// gathers run as multiplies (the FMA pipe) and byte permutes.
+
+// Bit 3 of each nibble of t (t = x & 0x88888888) gathered by one multiply: the
+// partial products of t * 0x249 (shifts 0, 3, 6, 9) put nibbles 0-3's bits at
+// bits 12-15 and nibbles 4-7's at bits 28-31, and every other partial product
+// lands on a bit of its own, so no carry reaches those eight.
+__device__ __forceinline__ uint32_t gather_bit3(uint32_t t) { return t * 0x249u; }
+
+// The 32 gathered bits of four words (gather_bit3 results r0..r3) in word order.
+__device__ __forceinline__ uint32_t assemble_bits(uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+  const uint32_t p01 = __byte_perm(r0, r1, 0x7351), p23 = __byte_perm(r2, r3, 0x7351);
+  const uint32_t a = __byte_perm(p01, p23, 0x5410);   // bytes 1 of r0..r3: nibbles 0-3
+  const uint32_t b = __byte_perm(p01, p23, 0x7632);   // bytes 3 of r0..r3: nibbles 4-7
+  return ((a >> 4) & 0x0F0F0F0Fu) | (b & 0xF0F0F0F0u);
 }
 
-__device__ __forceinline__ uint32_t max_mag_code(uint32_t w0, uint32_t w1) {
-  uint32_t m = __vmaxu4(__vmaxu4(w0 & 0x07070707u, (w0 >> 4) & 0x07070707u),
-                        __vmaxu4(w1 & 0x07070707u, (w1 >> 4) & 0x07070707u));
-  m = __vmaxu4(m, m >> 16);
-  m = __vmaxu4(m, m >> 8);
-  return m & 0xFFu;
+// Largest magnitude code (nibble & 7) among the 16 nibbles of (w0, w1), given
+// o = w | 0x88888888: its bit 2 is an OR of bit 2, then bits 1 and 0 test
+// "some nibble >= t" with a per-nibble subtraction (8 + m - t keeps bit 3 iff
+// m >= t, and never borrows across a nibble).
+__device__ __forceinline__ uint32_t max_mag_code(uint32_t w0, uint32_t w1, uint32_t o0, uint32_t o1) {
+  uint32_t t = ((w0 | w1) & 0x44444444u) ? 4u : 0u;
+  uint32_t T = (t + 2u) * 0x11111111u;
+  if (((o0 - T) | (o1 - T)) & 0x88888888u) t += 2u;
+  T = (t + 1u) * 0x11111111u;
+  if (((o0 - T) | (o1 - T)) & 0x88888888u) t += 1u;
+  return t;
 }
 
-// mag bits (|q| = 3) of the 8 nibbles of w, given the block's threshold code
-__device__ __forceinline__ uint32_t mag_bits(uint32_t w, uint32_t add) {
-  return gather_nibble_bit3(((w & 0x77777777u) + add) & 0x88888888u);
-}
+constexpr int kGroupsPerIter = 4;
 
-constexpr int kGroupsPerIter = 2;
-
+// Thread t of a CTA handles groups base + u * blockDim + t (u < kGroupsPerIter), so every load
+// and store instruction of a warp covers consecutive groups; all loads of an iteration are issued
+// before its first use.
 __global__ void __launch_bounds__(256) requant_planes_kernel(
     long long n_groups, const uint4* __restrict__ codes, const uint16_t* __restrict__ s4,
     uint32_t* __restrict__ sign_out, uint32_t* __restrict__ mag_out, uint16_t* __restrict__ s16_out) {
@@ -123,34 +134,39 @@ __global__ void __launch_bounds__(256) requant_planes_kernel(
     lut[i] = (uint16_t)(s16 | (thr << 8));
   }
   __syncthreads();
-  const long long stride = (long long)gridDim.x * blockDim.x * kGroupsPerIter;
-  for (long long g0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * kGroupsPerIter; g0 < n_groups;
-       g0 += stride) {
+  const long long span = (long long)blockDim.x * kGroupsPerIter;
+  for (long long base = (long long)blockIdx.x * span; base < n_groups; base += (long long)gridDim.x * span) {
     uint4 cw[kGroupsPerIter];
     uint32_t sc[kGroupsPerIter];
 #pragma unroll
     for (int u = 0; u < kGroupsPerIter; ++u) {
-      if (g0 + u < n_groups) {
-        cw[u] = __ldg(codes + g0 + u);
-        sc[u] = __ldg(s4 + g0 + u);
+      const long long gi = base + (long long)u * blockDim.x + threadIdx.x;
+      if (gi < n_groups) {
+        cw[u] = __ldg(codes + gi);
+        sc[u] = __ldg(s4 + gi);
       }
     }
 #pragma unroll
     for (int u = 0; u < kGroupsPerIter; ++u) {
-      if (g0 + u >= n_groups) break;
+      const long long gi = base + (long long)u * blockDim.x + threadIdx.x;
+      if (gi >= n_groups) break;
       const uint32_t w[4] = {cw[u].x, cw[u].y, cw[u].z, cw[u].w};
-      uint32_t sign = 0, mag = 0, s16pair = 0;
+      uint32_t o[4], mr[4], s16pair = 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) o[q] = w[q] | 0x88888888u;
 #pragma unroll
       for (int b = 0; b < 2; ++b) {
-        const uint32_t e = lut[((sc[u] >> (8 * b)) & 0x7Fu) * 8 + max_mag_code(w[2 * b], w[2 * b + 1])];
+        const uint32_t mc = max_mag_code(w[2 * b], w[2 * b + 1], o[2 * b], o[2 * b + 1]);
+        const uint32_t e = lut[((sc[u] >> (8 * b)) & 0x7Fu) * 8 + mc];
         s16pair |= (e & 0xFFu) << (8 * b);
-        const uint32_t add = (8u - (e >> 8)) * 0x11111111u;
-        sign |= (gather_nibble_bit3(w[2 * b]) | (gather_nibble_bit3(w[2 * b + 1]) << 8)) << (16 * b);
-        mag |= (mag_bits(w[2 * b], add) | (mag_bits(w[2 * b + 1], add) << 8)) << (16 * b);
+        const uint32_t T = (e >> 8) * 0x11111111u;   // |q| = 3 iff magnitude code >= threshold
+        mr[2 * b] = gather_bit3((o[2 * b] - T) & 0x88888888u);
+        mr[2 * b + 1] = gather_bit3((o[2 * b + 1] - T) & 0x88888888u);
       }
-      sign_out[g0 + u] = sign;
-      mag_out[g0 + u] = mag;
-      s16_out[g0 + u] = (uint16_t)s16pair;
+      sign_out[gi] = assemble_bits(gather_bit3(w[0] & 0x88888888u), gather_bit3(w[1] & 0x88888888u),
+                                   gather_bit3(w[2] & 0x88888888u), gather_bit3(w[3] & 0x88888888u));
+      mag_out[gi] = assemble_bits(mr[0], mr[1], mr[2], mr[3]);
+      s16_out[gi] = (uint16_t)s16pair;
     }
   }
 }
@@ -239,9 +255,19 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_kernel(
   }
 }
 
-static int grid_for(long long n, int block) {
-  long long g = (n + block - 1) / block;
-  const long long cap = 152LL * 16;  // grid-stride beyond 16 CTAs per SM
+// Grid of a grid-stride streaming kernel: at most as many CTAs as can be resident at once (the
+// occupancy calculator's CTAs per SM x the SM count), so the work splits evenly over one wave
+// instead of leaving a partial wave as a tail.
+template <typename Kern>
+static int resident_grid(Kern kernel, int block, long long n_threads) {
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    sms = 152;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, block, 0) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  long long g = (n_threads + block - 1) / block;
+  const long long cap = (long long)sms * per_sm;
   if (g > cap) g = cap;
   if (g < 1) g = 1;
   return (int)g;
@@ -333,6 +359,45 @@ __global__ void __launch_bounds__(1024) fp8_scale2_kernel(int N, int K, const ui
   }
 }
 
+// The NVFP4 rule on one block of 16 exact weights (fp64) with their sign bits (bit j = weight j)
+// and the matrix's scale_2: the block's s16 and magnitude bits and, when `delta` is set, its 16
+// delta codes (two words, low nibble first) and delta scale.
+struct Block16 {
+  uint32_t mag, s16, dlo, dhi, ds4;
+};
+
+__device__ __forceinline__ Block16 exact_rule_16(const double (&wv)[16], uint32_t sbits, double s2,
+                                                 bool delta) {
+  Block16 r = {0u, 0u, 0u, 0u, 0u};
+  double bmax = 0.0;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) bmax = fmax(bmax, fabs(wv[j]));
+  r.s16 = e4m3_rne_ratio_dd(bmax, 3.0 * s2);
+  const double lvl = (double)e4m3_to_f32(r.s16) * s2;                   // s16 scale_2, exact
+  double d[16];
+  double dmax = 0.0;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const uint32_t mg = fabs(wv[j]) >= 2.0 * lvl;
+    r.mag |= mg << j;
+    const double q = (mg ? 3.0 : 1.0) * lvl;
+    d[j] = wv[j] - (((sbits >> j) & 1u) ? -q : q);                      // exact
+    dmax = fmax(dmax, fabs(d[j]));
+  }
+  if (delta) {
+    r.ds4 = e4m3_rne_ratio_dd(dmax, 6.0 * s2);
+    const double step = (double)e4m3_to_f32(r.ds4) * s2;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t dm = step > 0.0 ? e2m1_rne_mag_d(fabs(d[j]), step) : 0u;
+      const uint32_t code = dm | ((d[j] < 0.0 && dm != 0u) ? 8u : 0u);
+      if (j < 8) r.dlo |= code << (4 * j);
+      else r.dhi |= code << (4 * (j - 8));
+    }
+  }
+  return r;
+}
+
 // One thread per 32-weight group of a row: 32 codes in, one sign and one magnitude word, two s16
 // bytes (and 16 delta code bytes + two delta scale bytes) out.
 __global__ void __launch_bounds__(256) requant_fp8_kernel(
@@ -342,6 +407,7 @@ __global__ void __launch_bounds__(256) requant_fp8_kernel(
   const long long gpm = (long long)N * (K / 32);
   const long long n_groups = (long long)M * gpm;
   const int nbn = (N + kFp8Block - 1) / kFp8Block, nbk = (K + kFp8Block - 1) / kFp8Block;
+  const bool delta = dcodes_out != nullptr;
   for (long long gi = (long long)blockIdx.x * blockDim.x + threadIdx.x; gi < n_groups;
        gi += (long long)gridDim.x * blockDim.x) {
     const int m = (int)(gi / gpm);
@@ -357,48 +423,143 @@ __global__ void __launch_bounds__(256) requant_fp8_kernel(
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
       double wv[16];
-      double bmax = 0.0;
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const uint32_t c = (words[4 * b + (j >> 2)] >> (8 * (j & 3))) & 0xFFu;
         const double a = (double)e4m3_to_f32(c & 0x7Fu) * bs;          // exact
         wv[j] = (c & 0x80u) ? -a : a;
-        bmax = fmax(bmax, a);
         sign |= (c >> 7) << (16 * b + j);
       }
-      const uint32_t s16 = e4m3_rne_ratio_dd(bmax, 3.0 * s2);
-      const double lvl = (double)e4m3_to_f32(s16) * s2;                 // s16 scale_2, exact
-      s16pair |= s16 << (8 * b);
-      double d[16];
-      double dmax = 0.0;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const uint32_t mg = fabs(wv[j]) >= 2.0 * lvl;
-        mag |= mg << (16 * b + j);
-        const double q = (mg ? 3.0 : 1.0) * lvl;
-        d[j] = wv[j] - (((sign >> (16 * b + j)) & 1u) ? -q : q);          // exact
-        dmax = fmax(dmax, fabs(d[j]));
-      }
-      if (dcodes_out != nullptr) {
-        const uint32_t ds4 = e4m3_rne_ratio_dd(dmax, 6.0 * s2);
-        const double step = (double)e4m3_to_f32(ds4) * s2;
-        ds4pair |= ds4 << (8 * b);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const uint32_t dm = step > 0.0 ? e2m1_rne_mag_d(fabs(d[j]), step) : 0u;
-          const uint32_t code = dm | ((d[j] < 0.0 && dm != 0u) ? 8u : 0u);
-          dwords[2 * b + (j >> 3)] |= code << (4 * (j & 7));
-        }
-      }
+      const Block16 o = exact_rule_16(wv, sign >> (16 * b), s2, delta);
+      mag |= o.mag << (16 * b);
+      s16pair |= o.s16 << (8 * b);
+      ds4pair |= o.ds4 << (8 * b);
+      dwords[2 * b] = o.dlo;
+      dwords[2 * b + 1] = o.dhi;
     }
     sign_out[gi] = sign;
     mag_out[gi] = mag;
     s16_out[gi] = (uint16_t)s16pair;
-    if (dcodes_out != nullptr) {
+    if (delta) {
       dcodes_out[gi] = make_uint4(dwords[0], dwords[1], dwords[2], dwords[3]);
       ds4_out[gi] = (uint16_t)ds4pair;
     }
   }
+}
+
+// ---------------------------------------------------------------- MXFP4 (FP4 experts) input
+// README "How it fits -- 2-bit experts at FP4 quality", last paragraph: checkpoints with FP4
+// experts load by a code remap.  Read as OCP MXFP4 -- an e2m1 code per weight (two per byte, low
+// nibble = even k) and one E8M0 scale 2^(e - 127) per 32 weights along K -- remapped by the same
+// rule as the FP8 input: W = e2m1(code) 2^(e - 127) is exact in fp64 and scale_2 =
+// fp32(fp64(amax) / 1344).
+
+// 2^(e - 127) as an fp64, built from its exponent field (e in 0..254 gives a normal fp64).
+__device__ __forceinline__ double e8m0_value(uint32_t e) {
+  return __longlong_as_double((long long)(e + (1023 - 127)) << 52);
+}
+
+// One CTA per matrix: amax over |W| in fp64 (each 32-weight group contributes its largest
+// magnitude code once, e2m1 magnitudes being ordered like their codes).
+__global__ void __launch_bounds__(1024) mxfp4_scale2_kernel(int N, int K, const uint8_t* __restrict__ codes,
+                                                            const uint8_t* __restrict__ e8m0,
+                                                            float* __restrict__ scale_2) {
+  const int m = blockIdx.x;
+  const long long groups = (long long)N * (K / 32);
+  const uint4* cm = reinterpret_cast<const uint4*>(codes) + (size_t)m * groups;
+  const uint8_t* em = e8m0 + (size_t)m * groups;
+  double mx = 0.0;
+  for (long long i = threadIdx.x; i < groups; i += blockDim.x) {
+    const uint4 c = __ldg(cm + i);
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    uint32_t top = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int b = 0; b < 8; ++b) top = max(top, (w[q] >> (4 * b)) & 7u);
+    mx = fmax(mx, (double)e2m1_mag_value(top) * e8m0_value(__ldg(em + i)));
+  }
+  __shared__ double red[32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    mx = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (threadIdx.x == 0) scale_2[m] = __double2float_rn(__ddiv_rn(mx, 1344.0));
+  }
+}
+
+// One thread per 32-weight group (16 code bytes and one exponent byte in, like the FP8 kernel out).
+__global__ void __launch_bounds__(256) requant_mxfp4_kernel(
+    int M, long long gpm, const uint4* __restrict__ codes, const uint8_t* __restrict__ e8m0,
+    const float* __restrict__ scale_2, uint32_t* __restrict__ sign_out, uint32_t* __restrict__ mag_out,
+    uint16_t* __restrict__ s16_out, uint4* __restrict__ dcodes_out, uint16_t* __restrict__ ds4_out) {
+  const long long n_groups = (long long)M * gpm;
+  const bool delta = dcodes_out != nullptr;
+  for (long long gi = (long long)blockIdx.x * blockDim.x + threadIdx.x; gi < n_groups;
+       gi += (long long)gridDim.x * blockDim.x) {
+    const double s2 = (double)__ldg(scale_2 + gi / gpm);
+    const double p2 = e8m0_value(__ldg(e8m0 + gi));
+    const uint4 cw = __ldg(codes + gi);
+    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+    uint32_t sign = 0, mag = 0, s16pair = 0, ds4pair = 0;
+    uint32_t dwords[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      double wv[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t c = (words[2 * b + (j >> 3)] >> (4 * (j & 7))) & 0xFu;
+        const double a = (double)e2m1_mag_value(c & 7u) * p2;             // exact
+        wv[j] = (c & 8u) ? -a : a;
+        sign |= (c >> 3) << (16 * b + j);
+      }
+      const Block16 o = exact_rule_16(wv, sign >> (16 * b), s2, delta);
+      mag |= o.mag << (16 * b);
+      s16pair |= o.s16 << (8 * b);
+      ds4pair |= o.ds4 << (8 * b);
+      dwords[2 * b] = o.dlo;
+      dwords[2 * b + 1] = o.dhi;
+    }
+    sign_out[gi] = sign;
+    mag_out[gi] = mag;
+    s16_out[gi] = (uint16_t)s16pair;
+    if (delta) {
+      dcodes_out[gi] = make_uint4(dwords[0], dwords[1], dwords[2], dwords[3]);
+      ds4_out[gi] = (uint16_t)ds4pair;
+    }
+  }
+}
+
+extern "C" moet_status moet_requant_mxfp4_2bit(int M, int N, int K, const uint8_t* codes, const uint8_t* e8m0,
+                                               float* scale_2, uint32_t* sign, uint32_t* mag, uint8_t* s16,
+                                               uint8_t* dcodes, uint8_t* ds4, moet_stream stream) {
+  if (M < 1 || N < 1 || K < 32 || K % 32 != 0) return MOET_ERR_SHAPE;
+  if (!codes || !e8m0 || !scale_2 || !sign || !mag || !s16) return MOET_ERR_INVALID_ARG;
+  if ((dcodes == nullptr) != (ds4 == nullptr)) return MOET_ERR_INVALID_ARG;
+  if (((uintptr_t)codes & 15) || ((uintptr_t)scale_2 & 3) || ((uintptr_t)sign & 3) ||
+      ((uintptr_t)mag & 3) || ((uintptr_t)s16 & 1))
+    return MOET_ERR_ALIGN;
+  if (dcodes && (((uintptr_t)dcodes & 15) || ((uintptr_t)ds4 & 1))) return MOET_ERR_ALIGN;
+  if (M > 65535) return MOET_ERR_UNSUPPORTED;
+  cudaStream_t st = (cudaStream_t)stream;
+  const long long gpm = (long long)N * (K / 32);
+  {
+    ProfScope ps(MOET_K_REQUANT, st);
+    mxfp4_scale2_kernel<<<M, 1024, 0, st>>>(N, K, codes, e8m0, scale_2);
+  }
+  MOET_CUDA_TRY(cudaGetLastError());
+  {
+    ProfScope ps(MOET_K_REQUANT, st);
+    const int g = resident_grid(requant_mxfp4_kernel, 256, gpm * M);
+    requant_mxfp4_kernel<<<g, 256, 0, st>>>(M, gpm, (const uint4*)codes, e8m0, scale_2, sign, mag, (uint16_t*)s16,
+                                            (uint4*)dcodes, (uint16_t*)ds4);
+  }
+  MOET_CUDA_TRY(cudaGetLastError());
+  return MOET_OK;
 }
 
 extern "C" moet_status moet_requant_fp8_2bit(int M, int N, int K, const uint8_t* codes, const float* bscale,
@@ -421,8 +582,9 @@ extern "C" moet_status moet_requant_fp8_2bit(int M, int N, int K, const uint8_t*
   MOET_CUDA_TRY(cudaGetLastError());
   {
     ProfScope ps(MOET_K_REQUANT, st);
-    requant_fp8_kernel<<<grid_for(n_groups, 256), 256, 0, st>>>(M, N, K, codes, bscale, scale_2, sign, mag,
-                                                                 (uint16_t*)s16, (uint4*)dcodes, (uint16_t*)ds4);
+    const int g = resident_grid(requant_fp8_kernel, 256, n_groups);
+    requant_fp8_kernel<<<g, 256, 0, st>>>(M, N, K, codes, bscale, scale_2, sign, mag, (uint16_t*)s16,
+                                          (uint4*)dcodes, (uint16_t*)ds4);
   }
   MOET_CUDA_TRY(cudaGetLastError());
   return MOET_OK;
@@ -444,12 +606,12 @@ extern "C" moet_status moet_requant_2bit(int M, int N, int K, const uint8_t* cod
   {
     ProfScope ps(MOET_K_REQUANT, (cudaStream_t)stream);
     if (dcodes == nullptr) {
-      long long g = (n_groups + 256LL * kGroupsPerIter - 1) / (256LL * kGroupsPerIter);
-      if (g > 152LL * 8) g = 152LL * 8;
-      requant_planes_kernel<<<(int)g, 256, 0, (cudaStream_t)stream>>>(
+      const int g = resident_grid(requant_planes_kernel, 256, (n_groups + kGroupsPerIter - 1) / kGroupsPerIter);
+      requant_planes_kernel<<<g, 256, 0, (cudaStream_t)stream>>>(
           n_groups, (const uint4*)codes, (const uint16_t*)s4, sign, mag, (uint16_t*)s16);
     } else {
-      requant_2bit_kernel<<<grid_for(n_groups, 256), 256, 0, (cudaStream_t)stream>>>(
+      const int g = resident_grid(requant_2bit_kernel, 256, n_groups);
+      requant_2bit_kernel<<<g, 256, 0, (cudaStream_t)stream>>>(
           n_groups, (const uint4*)codes, (const uint16_t*)s4, sign, mag, (uint16_t*)s16,
           (uint4*)dcodes, (uint16_t*)ds4);
     }
@@ -485,7 +647,8 @@ extern "C" moet_status moet_quantize_nvfp4(int M, int N, int K, const float* w, 
   const long long n_groups = gpm * M;
   {
     ProfScope ps(MOET_K_QUANTIZE, st);
-    quantize_nvfp4_kernel<<<grid_for(n_groups, 256), 256, 0, st>>>(
+    const int g = resident_grid(quantize_nvfp4_kernel, 256, n_groups);
+    quantize_nvfp4_kernel<<<g, 256, 0, st>>>(
         n_groups, gpm, (const float4*)w, scale_2, (uint4*)codes, (uint16_t*)s4);
   }
   MOET_CUDA_TRY(cudaGetLastError());

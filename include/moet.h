@@ -125,6 +125,26 @@ moet_status moet_requant_fp8_2bit(int M, int N, int K, const uint8_t* codes, con
                                   uint8_t* dcodes, uint8_t* ds4, moet_stream stream);
 
 /* ------------------------------------------------------------------------
+ * moet_requant_mxfp4_2bit -- FP4-expert (MXFP4) weights -> 2-bit planes (+ delta).
+ * README "How it fits -- 2-bit experts at FP4 quality", last paragraph:
+ * checkpoints whose experts are FP4 (DeepSeek-V4-Flash) load by a code remap.
+ * The pages name no format; this library reads it as OCP MXFP4: an e2m1 code
+ * per weight and one E8M0 scale 2^(e - 127) per 32 weights along K, so
+ * W = e2m1(code) * 2^(e - 127), exact in fp64.  The remap is the rule of
+ * moet_requant_fp8_2bit applied to W: scale_2 = fp32(fp64(amax |W|) / 1344),
+ * s16 = e4m3 satfinite RNE(max_b |W| / (3 scale_2)), sign = the code's sign
+ * bit, mag = |W| >= 2 s16 scale_2, and the NVFP4 delta of W - q s16 scale_2.
+ *   M >= 1 matrices of [N, K], K % 32 == 0.  codes [M, N, K/2] u8, low nibble =
+ *   even k (16 B aligned); e8m0 [M, N, K/32] u8 (read; 0xFF = NaN is not a
+ *   valid scale: the outputs of its group are unspecified, nothing faults).
+ *   scale_2 [M] fp32, sign/mag [M, N, K/32] u32, s16 [M, N, K/16] u8 (written);
+ *   dcodes [M, N, K/2] / ds4 [M, N, K/16] (both NULL = no delta).  Outputs are
+ *   bit-exact. */
+moet_status moet_requant_mxfp4_2bit(int M, int N, int K, const uint8_t* codes, const uint8_t* e8m0,
+                                    float* scale_2, uint32_t* sign, uint32_t* mag, uint8_t* s16,
+                                    uint8_t* dcodes, uint8_t* ds4, moet_stream stream);
+
+/* ------------------------------------------------------------------------
  * moet_route_topk -- router top-k, renormalised softmax, bucketing by expert.
  * Per token: the k largest logits (ties -> lower expert id; NaN below -inf),
  * ordered by decreasing logit; w_j = exp(l_j - l_max) / sum over the k.

@@ -30,7 +30,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .formats import E4M3_POS, e2m1_rne_ratio, e4m3_rne_ratio, e4m3_decode
+from .formats import E4M3_POS, e2m1_decode, e2m1_rne_ratio, e4m3_rne_ratio, e4m3_decode
 from .nvfp4 import dequantize_units, unpack_codes
 
 
@@ -126,30 +126,37 @@ def requant_fp8_2bit(codes: np.ndarray, bscale: np.ndarray, want_delta: bool = T
     quality", last paragraph: FP8 block-quant checkpoints are requantised to the sign-symmetric
     codebook at load, as the NVFP4 ones are.  The pages give no formula for this input; the
     reading here is the NVFP4 rule applied to the exact FP8 weights W with a per-matrix
-    scale_2 = amax / (3 * 448) (see fp8_scale_2):
+    scale_2 = amax / (3 * 448) (see fp8_scale_2 and requant_exact_2bit).
+    """
+    codes = np.asarray(codes, dtype=np.uint8)
+    return requant_exact_2bit(fp8_dequantize(codes, bscale), (codes >> 7).astype(np.uint8), want_delta)
 
+
+def requant_exact_2bit(w: np.ndarray, sign: np.ndarray, want_delta: bool = True):
+    """The NVFP4 rule applied to exact weights W [N, K] (fp64) with their sign bits [N, K]:
+
+      scale_2 = fp32( fp64(max |W|) / 1344 )                 (the largest block's s16 is 448)
       s16[b]  = e4m3 satfinite RNE( max_b |W| / (3 scale_2) )
-      sign_k  = sign bit of the e4m3 code (so -0 maps to the negative side)
+      sign_k  = the input's sign bit (so -0 maps to the negative side)
       mag_k   = |W_k| >= 2 s16[b] scale_2
       d_k     = W_k - q_k s16[b] scale_2                    (exact in fp64)
       ds4[b]  = e4m3 satfinite RNE( max_b |d| / (6 scale_2) )
       dcode_k = sign(d_k) | e2m1 satfinite RNE( |d_k| / (ds4[b] scale_2) ), zero as +0.
 
     Every ratio is rounded once by exact comparison (formats._rne_ratio): all products of
-    the short significands involved are exact in fp64.
+    the short significands involved are exact in fp64.  A zero block (or matrix) gets s16 = 0.
     """
-    codes = np.asarray(codes, dtype=np.uint8)
-    N, K = codes.shape
+    w = np.asarray(w, dtype=np.float64)
+    sign = np.asarray(sign, dtype=np.uint8)
+    N, K = w.shape
     assert K % 32 == 0
-    sc2 = fp8_scale_2(codes, bscale)
-    s2 = np.float64(sc2)
-    w = fp8_dequantize(codes, bscale)
     aw = np.abs(w)
+    sc2 = np.float32(np.float64(aw.max()) / np.float64(S16_TOP))
+    s2 = np.float64(sc2)
     bmax = aw.reshape(N, K // 16, 16).max(axis=2)
     with np.errstate(divide="ignore", invalid="ignore"):
         s16 = np.where(bmax > 0, e4m3_rne_ratio(bmax, 3.0 * s2), 0)   # a zero block (or matrix): 0
     lvl = np.repeat(E4M3_POS[s16.astype(np.int64)], 16, axis=1) * s2      # s16 scale_2, exact
-    sign = (codes >> 7).astype(np.uint8)
     mag = (aw >= 2.0 * lvl).astype(np.uint8)
     out = dict(scale_2=sc2, sign=pack_bits(sign), mag=pack_bits(mag), s16=s16.astype(np.uint8))
     if want_delta:
@@ -168,3 +175,34 @@ def requant_fp8_2bit(codes: np.ndarray, bscale: np.ndarray, want_delta: bool = T
         out["dcodes"] = (dcode[:, 0::2] | (dcode[:, 1::2] << 4)).astype(np.uint8)
         out["ds4"] = ds4.astype(np.uint8)
     return out
+
+
+# ---------------------------------------------------------------- MXFP4 (FP4 experts) input
+MX_BLOCK = 32            # OCP microscaling: one E8M0 scale per 32 consecutive weights along K
+E8M0_BIAS = 127
+
+
+def mxfp4_dequantize(codes: np.ndarray, e8m0: np.ndarray) -> np.ndarray:
+    """[N, K/2] e2m1 codes (low nibble = even k) with E8M0 scales [N, K/32] -> exact fp64
+    weights W = e2m1(code) * 2^(e - 127).  The E8M0 NaN code 0xFF is not a valid scale."""
+    e8m0 = np.asarray(e8m0, dtype=np.uint8)
+    assert not (e8m0 == 0xFF).any(), "E8M0 0xFF (NaN) is not a weight scale"
+    v = e2m1_decode(unpack_codes(codes))
+    return v * np.repeat(np.ldexp(1.0, e8m0.astype(np.int64) - E8M0_BIAS), MX_BLOCK, axis=1)
+
+
+def requant_mxfp4_2bit(codes: np.ndarray, e8m0: np.ndarray, want_delta: bool = True):
+    """One [N, K] MXFP4 matrix -> scale_2, 2-bit planes (+ NVFP4 delta).
+
+    README "Frontier MoE on consumer Blackwell (SM120)", §"How it fits -- 2-bit experts at FP4
+    quality", last paragraph: checkpoints with FP4 experts (DeepSeek-V4-Flash) load by a code
+    remap.  The pages name no format and no formula.  Readings: the FP4 experts are OCP MXFP4
+    (an e2m1 code per weight, one power-of-two E8M0 scale per 32 weights along K), and the remap
+    is the same rule as the FP8 input -- the NVFP4 rule on the exact weights with
+    scale_2 = amax / 1344 (requant_exact_2bit).  The sign plane is the e2m1 sign bit; the
+    magnitude plane depends only on each code, its block's largest code and exponent, and
+    scale_2: it is a remap of the codes.
+    """
+    codes = np.asarray(codes, dtype=np.uint8)
+    sign = (unpack_codes(codes) >> 3).astype(np.uint8)
+    return requant_exact_2bit(mxfp4_dequantize(codes, e8m0), sign, want_delta)

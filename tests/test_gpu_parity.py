@@ -107,19 +107,24 @@ def _random_nvfp4(rng, M, N, K):
 
 def _check_requant(got, codes, s4):
     for m in range(codes.shape[0]):
-        ref = orq.requant_2bit(codes[m], s4[m])
+        ref = orq.requant_2bit(codes[m], s4[m], want_delta="dcodes" in got)
         for key in ("sign", "mag", "s16", "dcodes", "ds4"):
-            assert np.array_equal(ref[key], got[key][m]), (m, key)
+            if key in got:
+                assert np.array_equal(ref[key], got[key][m]), (m, key)
 
 
-def test_requant_bit_exact_random(moet):
+@pytest.mark.parametrize("delta", [True, False], ids=["with_delta", "planes_only"])
+def test_requant_bit_exact_random(moet, delta):
     rng = np.random.default_rng(21)
     codes, s4 = _random_nvfp4(rng, 3, 64, 512)
-    _check_requant(_gpu_requant(moet, codes, s4), codes, s4)
+    _check_requant(_gpu_requant(moet, codes, s4, delta), codes, s4)
 
 
-def test_requant_exhaustive_scale_and_max_code(moet):
-    """Every (s4, max code) pair, including all s16 ties in the e4m3 subnormal range."""
+@pytest.mark.parametrize("delta", [True, False], ids=["with_delta", "planes_only"])
+def test_requant_exhaustive_scale_and_max_code(moet, delta):
+    """Every (s4, max code) pair, including all s16 ties in the e4m3 subnormal range; the
+    planes-only kernel (a table per (s4, max code) and integer bit gathers) and the delta kernel
+    (the rule weight by weight) both."""
     rows = []
     rng = np.random.default_rng(22)
     for s in range(127):
@@ -130,7 +135,26 @@ def test_requant_exhaustive_scale_and_max_code(moet):
             rows.append((c, s))
     codes = np.stack([(c[0::2] | (c[1::2] << 4)).astype(np.uint8) for c, _ in rows])[None]
     s4 = np.array([[s, (s * 7 + 3) % 127] for _, s in rows], dtype=np.uint8)[None]
-    _check_requant(_gpu_requant(moet, codes, s4), codes, s4)
+    _check_requant(_gpu_requant(moet, codes, s4, delta), codes, s4)
+
+
+def test_requant_planes_large_ragged(moet):
+    """A pass of many grid-stride iterations with a ragged tail (3 x 4099 rows x 7168): the
+    planes-only kernel equals the delta kernel's planes everywhere, and sampled rows equal the
+    oracle (the rule is local to a row)."""
+    rng = np.random.default_rng(24)
+    M, N, K = 3, 4099, 7168
+    codes = rng.integers(0, 256, (M, N, K // 2), dtype=np.uint8)
+    s4 = rng.integers(0, 127, (M, N, K // 16), dtype=np.uint8)
+    a = _gpu_requant(moet, codes, s4, delta=True)
+    b = _gpu_requant(moet, codes, s4, delta=False)
+    for key in ("sign", "mag", "s16"):
+        assert np.array_equal(a[key], b[key]), key
+    for m in range(M):
+        rows = np.unique(np.r_[0, N - 1, rng.integers(0, N, 6)])
+        ref = orq.requant_2bit(codes[m, rows], s4[m, rows], want_delta=False)
+        for key in ("sign", "mag", "s16"):
+            assert np.array_equal(ref[key], b[key][m, rows]), (m, key)
 
 
 @pytest.mark.parametrize("M,N,K", [(3, 200, 96), (1, 128, 2048), (2, 7, 32)])
@@ -164,6 +188,41 @@ def test_requant_fp8_bit_exact(moet, M, N, K):
     sign2 = torch.empty_like(g["sign"]); mag2 = torch.empty_like(g["mag"]); s162 = torch.empty_like(g["s16"])
     sc2 = torch.empty_like(g["scale_2"])
     moet.requant_fp8_2bit(dev(codes), dev(bs), sc2, sign2, mag2, s162)
+    assert torch.equal(sign2, g["sign"]) and torch.equal(mag2, g["mag"]) and torch.equal(s162, g["s16"])
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 200, 96), (1, 128, 2048), (2, 7, 32)])
+def test_requant_mxfp4_bit_exact(moet, M, N, K):
+    """MXFP4 (e2m1 codes, E8M0 scale per 32 along K) -> scale_2, planes, s16 and delta, bit-exact
+    against the oracle; signed zeros, +-6, the extreme exponents 2^-127 and 2^127 in one matrix
+    and an all-zero matrix included."""
+    rng = np.random.default_rng(150 + N + K)
+    codes = rng.integers(0, 256, (M, N, K // 2), dtype=np.uint8)
+    codes[0, 0, :2] = [0x80, 0x7F]
+    e8m0 = rng.integers(100, 150, (M, N, K // 32)).astype(np.uint8)
+    e8m0[0, 0, 0] = 0
+    e8m0[0, -1, -1] = 254
+    if M > 1:
+        codes[-1] = 0                                       # an all-zero matrix
+    g = dict(scale_2=torch.empty(M, dtype=torch.float32, device=DEV),
+             sign=torch.empty((M, N, K // 32), dtype=torch.int32, device=DEV),
+             mag=torch.empty((M, N, K // 32), dtype=torch.int32, device=DEV),
+             s16=torch.empty((M, N, K // 16), dtype=torch.uint8, device=DEV),
+             dcodes=torch.empty((M, N, K // 2), dtype=torch.uint8, device=DEV),
+             ds4=torch.empty((M, N, K // 16), dtype=torch.uint8, device=DEV))
+    moet.requant_mxfp4_2bit(dev(codes), dev(e8m0), g["scale_2"], g["sign"], g["mag"], g["s16"], g["dcodes"],
+                            g["ds4"])
+    torch.cuda.synchronize()
+    for m in range(M):
+        o = orq.requant_mxfp4_2bit(codes[m], e8m0[m])
+        assert host(g["scale_2"])[m] == o["scale_2"]
+        assert np.array_equal(host(g["sign"])[m].view(np.uint32), o["sign"])
+        assert np.array_equal(host(g["mag"])[m].view(np.uint32), o["mag"])
+        for key in ("s16", "dcodes", "ds4"):
+            assert np.array_equal(host(g[key])[m], o[key]), key
+    sign2 = torch.empty_like(g["sign"]); mag2 = torch.empty_like(g["mag"]); s162 = torch.empty_like(g["s16"])
+    sc2 = torch.empty_like(g["scale_2"])
+    moet.requant_mxfp4_2bit(dev(codes), dev(e8m0), sc2, sign2, mag2, s162)
     assert torch.equal(sign2, g["sign"]) and torch.equal(mag2, g["mag"]) and torch.equal(s162, g["s16"])
 
 

@@ -277,3 +277,110 @@ def test_fp8_requant_top_block_and_zero_matrix():
     z = requant.requant_fp8_2bit(np.zeros((2, 32), np.uint8), np.ones((1, 1), np.float32))
     assert z["scale_2"] == 0 and not z["s16"].any() and not z["ds4"].any() and not z["dcodes"].any()
     assert (z["mag"] == 0xFFFFFFFF).all()                             # |q| = 3 on a zero scale
+
+
+# ---------------------------------------------------------------- MXFP4 (FP4 experts) input
+def _random_mxfp4(rng, N, K, lo=110, hi=140):
+    codes = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    codes[0, :2] = [0x80, 0x7F]                            # (+0, -0), (-6, +6)
+    e8m0 = rng.integers(lo, hi, (N, K // 32)).astype(np.uint8)
+    return codes, e8m0
+
+
+def test_mxfp4_requant_matches_exact_fractions():
+    """Every integer output of the fp64 MXFP4 requant against the same rule on weights decoded
+    in exact rational arithmetic (Fraction) from the codes and E8M0 exponents, weight by weight;
+    exponents span the whole E8M0 range except NaN."""
+    rng = np.random.default_rng(31)
+    codes, e8m0 = _random_mxfp4(rng, 3, 64)
+    e8m0[0] = [0, 254]                                     # 2^-127 and 2^127
+    e8m0[1] = [127, 126]
+    e8m0[2] = [1, 3]
+    for rows in ([0], [1, 2]):
+        c, e = codes[rows], e8m0[rows]
+        out = requant.requant_mxfp4_2bit(c, e)
+        N, K = c.shape[0], c.shape[1] * 2
+        nib = np.zeros((N, K), np.uint8)
+        nib[:, 0::2] = c & 15; nib[:, 1::2] = c >> 4
+        wf = [[F.E2M1_MAG_FRAC[int(x) & 7] * Fraction(2) ** (int(e[n, k // 32]) - 127) * (-1 if x & 8 else 1)
+               for k, x in enumerate(nib[n])] for n in range(N)]
+        amax = max(abs(x) for r in wf for x in r)
+        assert Fraction(float(out["scale_2"])) == Fraction(float(np.float32(float(amax / 1344))))
+        s2 = Fraction(float(out["scale_2"]))
+        sign = requant.unpack_bits(out["sign"]); mag = requant.unpack_bits(out["mag"])
+        dc = np.zeros((N, K), np.uint8)
+        dc[:, 0::2] = out["dcodes"] & 15; dc[:, 1::2] = out["dcodes"] >> 4
+        for n in range(N):
+            for b in range(K // 16):
+                blk = wf[n][16 * b:16 * b + 16]
+                bm = max(abs(x) for x in blk)
+                s16 = F.e4m3_rne_fraction(bm / (3 * s2)) if bm else 0
+                assert out["s16"][n, b] == s16
+                lvl = F.E4M3_VALUE_FRAC[s16] * s2
+                d = []
+                for j, x in enumerate(blk):
+                    k = 16 * b + j
+                    assert sign[n, k] == (nib[n, k] >> 3)
+                    m = abs(x) >= 2 * lvl
+                    assert mag[n, k] == m
+                    d.append(x - (3 if m else 1) * lvl * (-1 if sign[n, k] else 1))
+                dmax = max(abs(x) for x in d)
+                ds4 = F.e4m3_rne_fraction(dmax / (6 * s2)) if dmax else 0
+                assert out["ds4"][n, b] == ds4
+                step = F.E4M3_VALUE_FRAC[ds4] * s2
+                for j, x in enumerate(d):
+                    mg = F.e2m1_rne_fraction(abs(x) / step) if step else 0
+                    assert dc[n, 16 * b + j] == (mg | (8 if (x < 0 and mg) else 0))
+
+
+def test_mxfp4_requant_equals_fp8_on_the_same_weights():
+    """An MXFP4 matrix whose weights are all e4m3 values (exponents 2^-6 .. 2^6) and the FP8
+    block-quant matrix holding the same weights (block scale 1) give the same scale_2, planes,
+    s16 and delta: both inputs go through one rule on the exact weights."""
+    rng = np.random.default_rng(32)
+    N, K = 130, 96
+    codes, e8m0 = _random_mxfp4(rng, N, K, lo=121, hi=134)
+    w = requant.mxfp4_dequantize(codes, e8m0)
+    e4 = F.e4m3_decode(np.arange(256, dtype=np.uint8))
+    lut = {}
+    for c in range(256):
+        if (c & 0x7F) != 0x7F:
+            lut.setdefault((float(abs(e4[c])), c >> 7), c)
+    nib = np.zeros((N, K), np.uint8)
+    nib[:, 0::2] = codes & 15; nib[:, 1::2] = codes >> 4
+    f8 = np.array([[lut[(float(abs(w[n, k])), int(nib[n, k] >> 3))] for k in range(K)] for n in range(N)], np.uint8)
+    a = requant.requant_mxfp4_2bit(codes, e8m0)
+    b = requant.requant_fp8_2bit(f8, np.ones((2, 1), np.float32))
+    assert a["scale_2"] == b["scale_2"]
+    for key in ("sign", "mag", "s16", "dcodes", "ds4"):
+        assert np.array_equal(a[key], b[key]), key
+
+
+def test_mxfp4_requant_scale_and_sign_invariance():
+    """Adding 1 to every exponent doubles scale_2 exactly and changes nothing else; flipping
+    every code's sign bit flips the sign plane and the delta signs only."""
+    rng = np.random.default_rng(33)
+    codes, e8m0 = _random_mxfp4(rng, 200, 96)
+    a = requant.requant_mxfp4_2bit(codes, e8m0)
+    b = requant.requant_mxfp4_2bit(codes, e8m0 + np.uint8(1))
+    assert np.float32(b["scale_2"]) == np.float32(2) * np.float32(a["scale_2"])
+    for key in ("sign", "mag", "s16", "dcodes", "ds4"):
+        assert np.array_equal(a[key], b[key]), key
+    c = requant.requant_mxfp4_2bit(codes ^ np.uint8(0x88), e8m0)
+    assert np.array_equal(c["sign"], ~a["sign"]) and np.array_equal(c["mag"], a["mag"])
+    assert np.array_equal(c["s16"], a["s16"]) and np.array_equal(c["ds4"], a["ds4"])
+    lo, hi = a["dcodes"] & 15, a["dcodes"] >> 4
+    flip = np.where((lo & 7) != 0, 8, 0).astype(np.uint8) | np.where((hi & 7) != 0, 0x80, 0).astype(np.uint8)
+    assert np.array_equal(c["dcodes"], a["dcodes"] ^ flip)
+
+
+def test_mxfp4_requant_top_block_and_zero_matrix():
+    rng = np.random.default_rng(34)
+    codes, e8m0 = _random_mxfp4(rng, 4, 64)
+    out = requant.requant_mxfp4_2bit(codes, e8m0)
+    w = requant.mxfp4_dequantize(codes, e8m0)
+    top = np.unravel_index(np.argmax(np.abs(w)), w.shape)
+    assert out["s16"][top[0], top[1] // 16] == 126                  # the largest block: s16 = 448
+    z = requant.requant_mxfp4_2bit(np.zeros((2, 16), np.uint8), np.full((2, 1), 127, np.uint8))
+    assert z["scale_2"] == 0 and not z["s16"].any() and not z["ds4"].any() and not z["dcodes"].any()
+    assert (z["mag"] == 0xFFFFFFFF).all()
