@@ -42,6 +42,7 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 PREFILL_MIN_T = 512          # the library runs its bf16 prefill engine above this many tokens
 L2_FLUSH_BYTES = 512 << 20
+EXTRAS = ("sweep", "pooled", "requant", "requant_fp8", "requant_mxfp4")
 
 
 def parse():
@@ -55,7 +56,16 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--experts", type=int, default=0,
                     help="override E (smaller layer for profiler captures; not a bench line)")
-    return ap.parse_args()
+    ap.add_argument("--extras", default=",".join(EXTRAS),
+                    help="comma list of the extra measurements to run (default: all of " + ",".join(EXTRAS) + ")")
+    ap.add_argument("--requant-experts", type=int, default=0,
+                    help="requant over this many experts of the 1T-class layer instead of all (profiler captures)")
+    args = ap.parse_args()
+    args.extras = {e for e in args.extras.split(",") if e}
+    unknown = args.extras - set(EXTRAS)
+    if unknown:
+        ap.error(f"unknown extras {sorted(unknown)}")
+    return args
 
 
 def workload(args):
@@ -440,12 +450,13 @@ def time_requant_mxfp4(moet, torch, dev, steps=3, n_mat=16):
             "bound": "fp64 ALU (exact ratio rounding in fp64)"}
 
 
-def time_requant(moet, torch, dev, steps=3):
-    """moet_requant_2bit over the full NVFP4 expert set of the 1T-class layer (768 matrices)."""
+def time_requant(moet, torch, dev, steps=3, n_experts=0):
+    """moet_requant_2bit over the full NVFP4 expert set of the 1T-class layer (768 matrices), or over
+    its first n_experts experts."""
     cfg = W.CONFIGS["kimi_layer"]
     gen = torch.Generator(device=dev)
     gen.manual_seed(99)
-    E, H, I = cfg.E, cfg.H, cfg.I
+    E, H, I = (n_experts or cfg.E), cfg.H, cfg.I
     results = {}
     bufs = {}
     for f, (N, K) in ((1, (2 * I, H)), (2, (H, I))):
@@ -453,8 +464,9 @@ def time_requant(moet, torch, dev, steps=3):
         s4 = torch.empty((E, N, K // 16), dtype=torch.uint8, device=dev)
         sc2 = torch.empty(E, dtype=torch.float32, device=dev)
         for e0 in range(0, E, 16):
-            w = gen_weight_chunk(torch, gen, cfg.dist, (16, N, K), dev)
-            moet.quantize_nvfp4(w, codes[e0:e0 + 16], s4[e0:e0 + 16], sc2[e0:e0 + 16])
+            e1 = min(E, e0 + 16)
+            w = gen_weight_chunk(torch, gen, cfg.dist, (e1 - e0, N, K), dev)
+            moet.quantize_nvfp4(w, codes[e0:e1], s4[e0:e1], sc2[e0:e1])
             del w
         sign = torch.empty((E, N, K // 32), dtype=torch.int32, device=dev)
         mag = torch.empty_like(sign)
@@ -627,7 +639,7 @@ def run_ours(args, rank, world, local):
                     "fc1_launch_ms": f2, "experts_touched": l2.n_used, "delta_experts_touched": l2.n_delta,
                     "kernel_ms_per_launch": {k: v[2] / max(v[1], 1) for k, v in p2.items() if v[0]}}
 
-        for name in ("dsv3_decode_t1", "dsv3_decode_t8", "dsv3_prefill"):
+        for name in (("dsv3_decode_t1", "dsv3_decode_t8", "dsv3_prefill") if "sweep" in args.extras else ()):
             c2 = W.CONFIGS[name]
             if name == cfg.name or (c2.H, c2.I, c2.E) != (cfg.H, cfg.I, cfg.E):
                 continue
@@ -641,42 +653,47 @@ def run_ours(args, rank, world, local):
                 r["frac_of_fp8_peak"] = r["tflops"] / (2.0 * tpk)
             sweep[name] = r
             del l2
-        for name in ("glm_decode", "kimi_layer"):
+        for name in (("glm_decode", "kimi_layer") if "sweep" in args.extras else ()):
             c3 = W.CONFIGS[name]
             l3 = Layer(moet, torch, c3, dev)
             sweep[name] = timed(l3, args.steps, args.warmup)
             del l3
             torch.cuda.empty_cache()
-        extras["decode_sweep"] = sweep
+        if sweep:
+            extras["decode_sweep"] = sweep
 
-        # expert cache: the headline layer through the slot table with every 10th expert not
-        # resident (their pairs contribute zero and are counted); the planes stay where they are
-        slot_np = np.arange(cfg.E, dtype=np.int32)
-        slot_np[::10] = -1
-        slot_t = torch.from_numpy(slot_np).to(dev)
-        miss = torch.zeros(1, dtype=torch.int32, device=dev)
-        kwp = {}
-        if layer.use_delta:
-            kwp = dict(delta_slot=layer.slot, dfc1=layer.pools[1], dfc2=layer.pools[2], gate_mask=layer.gate)
+        if "pooled" in args.extras:
+            # expert cache: the headline layer through the slot table with every 10th expert not
+            # resident (their pairs contribute zero and are counted); the planes stay where they are
+            slot_np = np.arange(cfg.E, dtype=np.int32)
+            slot_np[::10] = -1
+            slot_t = torch.from_numpy(slot_np).to(dev)
+            miss = torch.zeros(1, dtype=torch.int32, device=dev)
+            kwp = {}
+            if layer.use_delta:
+                kwp = dict(delta_slot=layer.slot, dfc1=layer.pools[1], dfc2=layer.pools[2], gate_mask=layer.gate)
 
-        def pooled_step():
-            moet.route_topk(layer.logits, cfg.k, layer.idx, layer.w, layer.off, layer.perm)
-            moet.moe_forward_pooled(layer.x, layer.idx, layer.w, layer.off, layer.perm, slot_t, layer.planes[1],
-                                    layer.planes[2], layer.y, layer.ws, miss_count=miss, **kwp)
+            def pooled_step():
+                moet.route_topk(layer.logits, cfg.k, layer.idx, layer.w, layer.off, layer.perm)
+                moet.moe_forward_pooled(layer.x, layer.idx, layer.w, layer.off, layer.perm, slot_t, layer.planes[1],
+                                        layer.planes[2], layer.y, layer.ws, miss_count=miss, **kwp)
 
-        gp_ = capture_graph(torch, pooled_step)
-        miss.zero_()
-        tp = time_steps(torch, gp_.replay, args.steps, args.warmup, flush)
-        med = statistics.median(tp)
-        n_replays = args.steps + args.warmup
-        extras["pooled"] = {"workload": cfg.name, "resident_experts": int((slot_np >= 0).sum()),
-                            "missed_pairs_per_step": int(miss.item()) / n_replays,
-                            "tokens_per_s": cfg.T / (med * 1e-3), "ms_per_step_median": med}
-        del gp_
-        extras["requant"] = time_requant(moet, torch, dev)
-        extras["requant_fp8"] = time_requant_fp8(moet, torch, dev)
-        extras["requant_mxfp4"] = time_requant_mxfp4(moet, torch, dev)
-        extras["requant"]["frac_of_hbm_peak"] = extras["requant"]["gbs"] / peak
+            gp_ = capture_graph(torch, pooled_step)
+            miss.zero_()
+            tp = time_steps(torch, gp_.replay, args.steps, args.warmup, flush)
+            med = statistics.median(tp)
+            n_replays = args.steps + args.warmup
+            extras["pooled"] = {"workload": cfg.name, "resident_experts": int((slot_np >= 0).sum()),
+                                "missed_pairs_per_step": int(miss.item()) / n_replays,
+                                "tokens_per_s": cfg.T / (med * 1e-3), "ms_per_step_median": med}
+            del gp_
+        if "requant" in args.extras:
+            extras["requant"] = time_requant(moet, torch, dev, n_experts=args.requant_experts)
+            extras["requant"]["frac_of_hbm_peak"] = extras["requant"]["gbs"] / peak
+        if "requant_fp8" in args.extras:
+            extras["requant_fp8"] = time_requant_fp8(moet, torch, dev)
+        if "requant_mxfp4" in args.extras:
+            extras["requant_mxfp4"] = time_requant_mxfp4(moet, torch, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
