@@ -42,7 +42,7 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 PREFILL_MIN_T = 512          # the library runs its bf16 prefill engine above this many tokens
 L2_FLUSH_BYTES = 512 << 20
-EXTRAS = ("sweep", "pooled", "requant", "requant_fp8", "requant_mxfp4")
+EXTRAS = ("sweep", "pooled", "requant", "requant_fp8", "requant_mxfp4", "sign_bias")
 
 
 def parse():
@@ -450,6 +450,36 @@ def time_requant_mxfp4(moet, torch, dev, steps=3, n_mat=16):
             "bound": "fp64 ALU (exact ratio rounding in fp64)"}
 
 
+def time_sign_bias_probe(moet, torch, dev, steps=3, n_mat=16):
+    """moet_sign_bias_probe over n_mat fp32 matrices of the DeepSeek-V3 FC1 shape [4096, 7168]
+    (Student-t(4) weights, std 0.02) for the naive int2 codebook and the two symmetric ones: the
+    time per pass and the per-matrix bias and rel-RMS (mean, and the share of negative biases)."""
+    N, K = 4096, 7168
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    w = gen_weight_chunk(torch, g, "t4", (n_mat, N, K), dev)
+    rows = torch.empty((n_mat, N, 4), dtype=torch.float64, device=dev)
+    sums = torch.empty((n_mat, 4), dtype=torch.float64, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    out = {"matrices": n_mat, "shape": [N, K], "weights": n_mat * N * K,
+           "bound": "alu (fp32 search over 969 assignments per 16 weights)"}
+    for name, levels in (("int2", (-2, -1, 0, 1)), ("sym13", (-3, -1, 1, 3)), ("sym14", (-4, -1, 1, 4))):
+        ts = time_steps(torch, lambda: moet.sign_bias_probe(w, levels, rows, sums), steps, 1, flush)
+        s = sums.cpu().numpy()
+        n = N * K
+        rms = np.sqrt(s[:, 1] / n)
+        bias = s[:, 2] / n / rms
+        rel = np.sqrt(s[:, 3] / s[:, 1])
+        out[name] = {"levels": list(levels), "ms_per_pass": statistics.median(ts),
+                     "gweights_per_s": n_mat * n / (statistics.median(ts) * 1e-3) / 1e9,
+                     "bias_mean": float(bias.mean()), "bias_negative_share": float((bias < 0).mean()),
+                     "rel_rms_mean": float(rel.mean())}
+    out["bias_ratio_int2_over_sym13"] = abs(out["int2"]["bias_mean"]) / max(abs(out["sym13"]["bias_mean"]), 1e-300)
+    del w, rows, flush
+    torch.cuda.empty_cache()
+    return out
+
+
 def time_requant(moet, torch, dev, steps=3, n_experts=0):
     """moet_requant_2bit over the full NVFP4 expert set of the 1T-class layer (768 matrices), or over
     its first n_experts experts."""
@@ -694,6 +724,8 @@ def run_ours(args, rank, world, local):
             extras["requant_fp8"] = time_requant_fp8(moet, torch, dev)
         if "requant_mxfp4" in args.extras:
             extras["requant_mxfp4"] = time_requant_mxfp4(moet, torch, dev)
+        if "sign_bias" in args.extras:
+            extras["sign_bias"] = time_sign_bias_probe(moet, torch, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

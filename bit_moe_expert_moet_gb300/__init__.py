@@ -11,6 +11,7 @@ Entry points (same names as the C ABI without the ``moet_`` prefix):
   requant_2bit     NVFP4 -> 2-bit sign/magnitude planes + s16 (+ delta)
   requant_fp8_2bit FP8 block-quant -> scale_2, planes + s16 (+ delta)
   requant_mxfp4_2bit  MXFP4 (FP4 experts) -> scale_2, planes + s16 (+ delta)
+  sign_bias_probe  bias and L2 error of per-block optimal fits to a 4-level codebook
   route_topk       logits -> top-k ids/weights, expert offsets, permutation
   moe_forward      the MoE layer y = sum_j w_j FFN_e(x) on the 2-bit planes
   moe_forward_pooled  the same over a pool of resident experts (slot table,
@@ -32,6 +33,7 @@ from ._lib import (  # noqa: F401
     requant_2bit,
     requant_fp8_2bit,
     requant_mxfp4_2bit,
+    sign_bias_probe,
     route_topk,
     forward_workspace_size,
     moe_forward,

@@ -61,6 +61,8 @@ lib.moet_moe_forward.argtypes = [_i, _i, _i, _i, _i, _p, _p, _p, _p, _p,
 lib.moet_requant_fp8_2bit.restype = _i
 lib.moet_requant_fp8_2bit.argtypes = [_i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p]
 lib.moet_requant_mxfp4_2bit.restype = _i
+lib.moet_sign_bias_probe.restype = _i
+lib.moet_sign_bias_probe.argtypes = [_i, _i, _i, _p, ctypes.POINTER(ctypes.c_int32), _p, _p, _p]
 lib.moet_requant_mxfp4_2bit.argtypes = [_i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p]
 lib.moet_gate_from_confidence.restype = _i
 lib.moet_gate_from_confidence.argtypes = [_i, _i, _i, _p, ctypes.c_float, _p, _p, _p, _p, _p, _p]
@@ -103,7 +105,7 @@ def _ptr(t: Optional[torch.Tensor], dtype=None, name: str = "") -> Optional[int]
     return t.data_ptr()
 
 
-KERNEL_KINDS = ("requant", "quantize", "route", "prologue", "fc1", "fc2", "combine", "terms")
+KERNEL_KINDS = ("requant", "quantize", "route", "prologue", "fc1", "fc2", "combine", "terms", "probe")
 
 
 def profile_enable(on: bool = True):
@@ -234,6 +236,16 @@ def requant_mxfp4_2bit(codes: torch.Tensor, e8m0: torch.Tensor, scale_2: torch.T
         _ptr(scale_2, torch.float32, "scale_2"), _ptr(sign, torch.int32, "sign"), _ptr(mag, torch.int32, "mag"),
         _ptr(s16, torch.uint8, "s16"), _ptr(dcodes, torch.uint8, "dcodes"), _ptr(ds4, torch.uint8, "ds4"),
         _stream(stream)))
+
+
+def sign_bias_probe(w: torch.Tensor, levels, row_sums: torch.Tensor, sums: torch.Tensor, stream=None):
+    """fp32 weights [M, N, K] and 4 ascending integer levels -> per-row fp64 sums [M, N, 4] and
+    per-matrix sums [M, 4] of W, W^2, Q - W and (Q - W)^2 for the per-block L2-optimal fit."""
+    M, N, K = w.shape
+    lv = (ctypes.c_int32 * 4)(*[int(v) for v in levels])
+    _check("moet_sign_bias_probe", lib.moet_sign_bias_probe(
+        M, N, K, _ptr(w, torch.float32, "w"), lv, _ptr(row_sums, torch.float64, "row_sums"),
+        _ptr(sums, torch.float64, "sums"), _stream(stream)))
 
 
 def gate_from_confidence(conf: torch.Tensor, tau: float, topk_idx: torch.Tensor, gate_mask: torch.Tensor,

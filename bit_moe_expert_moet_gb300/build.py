@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoet.so")
-SOURCES = ["requant.cu", "route.cu", "moe.cu", "moe_tc.cu", "moe_pf.cu", "api.cu", "forward_static.cu"]
+SOURCES = ["requant.cu", "route.cu", "moe.cu", "moe_tc.cu", "moe_pf.cu", "api.cu", "forward_static.cu", "signbias.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

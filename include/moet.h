@@ -145,6 +145,24 @@ moet_status moet_requant_mxfp4_2bit(int M, int N, int K, const uint8_t* codes, c
                                     uint8_t* dcodes, uint8_t* ds4, moet_stream stream);
 
 /* ------------------------------------------------------------------------
+ * moet_sign_bias_probe -- bias and L2 error of per-block optimal 2-bit fits.
+ * README "How it fits -- 2-bit experts at FP4 quality", bullet 1 (the
+ * sign-bias finding): the L2-optimal fit of a naive 2-bit codebook drops one
+ * sign's tail and biases every tensor; a sign-symmetric codebook at the same
+ * L2 error does not.  For a codebook of 4 integer levels L, each block of 16
+ * weights along K gets the scale s > 0 that minimises
+ * sum (w - s L[nearest(w / s)])^2 (exactly: the best of the 969 monotone
+ * assignments of the sorted block, chosen in fp32 with a fixed operation
+ * order, its sums evaluated in fp64); Q is that fit (0 when no s > 0 fits).
+ *   M >= 1 matrices of [N, K] fp32, K % 16 == 0: w (device, 16 B aligned,
+ *   read; NaN/inf weights give unspecified sums).  levels: HOST int32[4],
+ *   strictly ascending, each in [-64, 64].  row_sums [M, N, 4] and sums [M, 4]
+ *   fp64 (device, written): per row and per matrix (rows summed in order)
+ *   sum W, sum W^2, sum (Q - W), sum (Q - W)^2. */
+moet_status moet_sign_bias_probe(int M, int N, int K, const float* w, const int32_t* levels,
+                                 double* row_sums, double* sums, moet_stream stream);
+
+/* ------------------------------------------------------------------------
  * moet_route_topk -- router top-k, renormalised softmax, bucketing by expert.
  * Per token: the k largest logits (ties -> lower expert id; NaN below -inf),
  * ordered by decreasing logit; w_j = exp(l_j - l_max) / sum over the k.
@@ -308,7 +326,8 @@ typedef enum {
   MOET_K_FC2 = 5,
   MOET_K_COMBINE = 6,
   MOET_K_TERMS = 7, /* activation -> NVFP4 term expansion of the tensor-core path */
-  MOET_KERNEL_KINDS = 8
+  MOET_K_PROBE = 8, /* moet_sign_bias_probe */
+  MOET_KERNEL_KINDS = 9
 } moet_kernel_kind;
 
 moet_status moet_profile_enable(int on);

@@ -21,9 +21,11 @@ Modules
   requant  NVFP4 -> 2-bit sign/magnitude planes, and the NVFP4 delta
   route    router top-k, renormalised softmax, bucketing permutation
   moe      the MoE forward (FC1 gate|up, SiLU*mul, FC2, weighted combine)
+  gate     the confidence gate and the experts it promotes
+  signbias the sign-bias probe (per-block L2-optimal fits to a 4-level codebook)
 
 Every function here is pinned by a ``-m "not gpu"`` test in ``tests/`` to
 something other than itself (brute force, closed forms, invariants or a
 hand-worked example); the one exception is stated in ``moe.py``.
 """
-from . import formats, nvfp4, requant, route, moe, gate  # noqa: F401
+from . import formats, nvfp4, requant, route, moe, gate, signbias  # noqa: F401

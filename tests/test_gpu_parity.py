@@ -649,3 +649,70 @@ def test_forward_full_size_sampled(moet, name, tokens):
     assert np.all(np.isfinite(yg))
     yo = _oracle_forward(logits, xb, cfg.k, ref, dset, gate, cfg.E, tokens=tokens)
     check_y(yg[tokens], yo[tokens])
+
+
+# ---------------------------------------------------------------- sign-bias probe
+PROBE_CODEBOOKS = [(-2, -1, 0, 1), (-3, -1, 1, 3), (-4, -1, 1, 4)]
+
+
+def _gpu_probe(moet, w, levels):
+    M, N, K = w.shape
+    rows = torch.empty((M, N, 4), dtype=torch.float64, device=DEV)
+    sums = torch.empty((M, 4), dtype=torch.float64, device=DEV)
+    moet.sign_bias_probe(dev(w), levels, rows, sums)
+    torch.cuda.synchronize()
+    return host(rows), host(sums)
+
+
+@pytest.mark.parametrize("levels", PROBE_CODEBOOKS)
+def test_sign_bias_probe_matches_oracle(moet, levels):
+    """Per-row and per-matrix sums against the oracle: ragged rows (33 blocks, so lanes hold
+    unequal counts), zero blocks, one-signed blocks, repeated values and exact grid fits.  The
+    assignment search runs in the same fp32 order on both sides, so only fp64 summation order
+    differs."""
+    from oracle import signbias as osb
+    rng = np.random.default_rng(160)
+    M, N, K = 3, 37, 528
+    w = (rng.standard_t(4, (M, N, K)) * 0.02).astype(np.float32)
+    w[0, 0, :16] = 0
+    w[0, 1, :16] = np.abs(w[0, 1, :16])
+    w[0, 2, 16:32] = -np.abs(w[0, 2, 16:32])
+    w[1, 3, :16] = 0.01
+    w[1, 4, :16] = np.float32(0.25) * np.asarray(levels, np.float32)[np.arange(16) % 4]
+    w[2] *= np.float32(1e-3)
+    rows, sums = _gpu_probe(moet, w, levels)
+    for m in range(M):
+        ref = osb.probe(w[m], levels)
+        scale = np.abs(ref).max()
+        assert np.allclose(rows[m], ref, rtol=1e-12, atol=1e-13 * scale), m
+        assert np.allclose(sums[m], ref.sum(0), rtol=1e-12, atol=1e-12 * scale), m
+        assert np.array_equal(sums[m], np.cumsum(rows[m], axis=0)[-1])       # rows summed in order
+
+
+def test_sign_bias_probe_full_size_sampled_rows(moet):
+    """DeepSeek-V3 FC1-sized matrices [4096, 7168]: sampled rows equal the oracle; the naive
+    codebook's bias is negative on every matrix and the symmetric codebook's far smaller."""
+    from oracle import signbias as osb
+    rng = np.random.default_rng(161)
+    M, N, K = 2, 4096, 7168
+    w = (rng.standard_t(4, (M, N, K)) * (0.02 / np.sqrt(2))).astype(np.float32)
+    stats = {}
+    for levels in ((-2, -1, 0, 1), (-3, -1, 1, 3)):
+        rows, sums = _gpu_probe(moet, w, levels)
+        for m in range(M):
+            sel = np.unique(np.r_[0, N - 1, rng.integers(0, N, 6)])
+            ref = osb.probe(w[m, sel], levels)
+            assert np.allclose(rows[m, sel], ref, rtol=1e-12, atol=1e-13 * np.abs(ref).max())
+        stats[levels] = [osb.statistics(sums[m], N * K) for m in range(M)]
+    assert all(s["bias"] < -0.01 for s in stats[(-2, -1, 0, 1)])
+    for a, b in zip(stats[(-3, -1, 1, 3)], stats[(-2, -1, 0, 1)]):
+        assert abs(a["bias"]) * 10 < abs(b["bias"])
+
+
+def test_sign_bias_probe_rejects_bad_levels(moet):
+    w = torch.zeros((1, 2, 32), dtype=torch.float32, device=DEV)
+    rows = torch.empty((1, 2, 4), dtype=torch.float64, device=DEV)
+    sums = torch.empty((1, 4), dtype=torch.float64, device=DEV)
+    for bad in ((-1, -1, 0, 1), (3, 1, -1, -3), (-100, -1, 1, 100)):
+        with pytest.raises(moet.MoetError):
+            moet.sign_bias_probe(w, bad, rows, sums)
