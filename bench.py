@@ -743,7 +743,7 @@ def run_ours(args, rank, world, local):
                     "peak_source": tpk_kind, "unit": "TFLOP/s", "frac": tach / tpk, "traffic": None,
                     "algorithmic_flops_per_launch": layer.flops_fc1, "launch_ms": fc1_ms,
                     "frac_of_fp8_peak": tach / (2.0 * tpk)}   # fp8 dense = 2x bf16 (nominal ratio)
-        dtype = "bf16 (FC1) / tf32 (FC2) mma on exactly expanded 2-bit weights, fp32 accumulate"
+        dtype = "bf16 (FC1) / fp16 with per-row power-of-two scaling of h (FC2) mma on exactly expanded 2-bit weights, fp32 accumulate"
     else:
         roofline = {"bound": "hbm", "kernel": "fc_tc_kernel<FC1>", "achieved": achieved, "peak": peak,
                     "peak_source": peak_kind, "unit": "GB/s", "frac": achieved / peak,

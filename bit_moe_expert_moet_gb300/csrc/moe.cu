@@ -74,7 +74,7 @@ inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
     L.xt = off;      off += align256(tc_terms_bytes(pairs, (size_t)H));
     L.ht = off;      off += align256(tc_terms_bytes(pairs, (size_t)I));
   } else if (T > kTcMaxT && pf_supported(H, I)) {
-    L.pfa = off;     off += align256(pf_act_bytes(pairs, (size_t)H, (size_t)I) + 4 * 256);
+    L.pfa = off;     off += align256(pf_act_bytes(pairs, (size_t)H, (size_t)I) + 5 * 256);
   }
   L.total = off;
   return L;
@@ -609,7 +609,9 @@ static moet_status forward_impl(int T, int H, int I, int E, int k, const uint16_
     f.xb = reinterpret_cast<uint16_t*>(pb);  pb += align256(pairs * H * sizeof(uint16_t));
     f.xbg = reinterpret_cast<uint16_t*>(pb); pb += align256(pairs * H * sizeof(uint16_t));
     f.h = h;
-    f.hg = reinterpret_cast<float*>(pb);
+    f.h16 = reinterpret_cast<uint16_t*>(pb);  pb += align256(pairs * I * sizeof(uint16_t));
+    f.hg16 = reinterpret_cast<uint16_t*>(pb); pb += align256(pairs * I * sizeof(uint16_t));
+    f.hscale = reinterpret_cast<float*>(pb);
     moet_status s = pf_forward(f, st);
     if (s != MOET_OK) return s;
   } else if (use_tc) {

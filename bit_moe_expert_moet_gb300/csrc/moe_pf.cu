@@ -5,25 +5,26 @@
 // layers are a dense contraction (tensor-bound), not a weight stream.
 //
 // Weights.  A 2-bit weight times its block scale, q * s16 with q in {+-1, +-3}
-// and s16 an e4m3 value, has at most 6 significant bits, so it is exact in
-// bf16 and in tf32: the planes expand to an exact A operand of tcgen05.mma
-// (fp32 accumulation in TMEM); scale_2 is applied in the epilogue.  The NVFP4
-// delta (e2m1 code times an e4m3 scale, also exact) is expanded the same way
-// and accumulates into the same TMEM accumulator against a copy of the inputs
-// whose ungated rows are zero, so it only reaches gated pairs.
+// and s16 an e4m3 value (2^-9 .. 1344 in magnitude), has at most 6 significant
+// bits, so it is exact in bf16 and in fp16: the planes expand to an exact A
+// operand of tcgen05.mma kind::f16 (fp32 accumulation in TMEM); scale_2 is
+// applied in the epilogue.  The NVFP4 delta (e2m1 code times an e4m3 scale,
+// 2^-10 .. 2688, also exact in both) is expanded the same way and accumulates
+// into the same TMEM accumulator against a copy of the inputs whose ungated
+// rows are zero, so it only reaches gated pairs.
 //
-// Precision.  FC1 runs kind::f16 on bf16: x is bf16, so FC1 is exact up to
-// fp32 accumulation.  FC2 runs kind::tf32 on the fp32 h: rounding h to bf16
-// (2^-9) on top of the bf16 output would exceed the layer's max-error budget,
-// while tf32 keeps 10 mantissa bits of h at half the bf16 MMA rate (FC1's epilogue rounds h to
-// the nearest tf32, so the tensor core's truncation to tf32 adds no bias).
+// Precision.  FC1 runs on bf16 (x is bf16, so FC1 is exact up to fp32
+// accumulation).  FC2 runs on fp16: rounding h to bf16 (8 significant bits) on
+// top of the bf16 output would exceed the layer's max-error budget, fp16 keeps
+// 11.  pf_h16_kernel scales each fp32 h row by a power of two that puts its
+// maximum in [2^14, 2^15) (no overflow, and everything above 2^-28 of the
+// maximum stays normal) and rounds it to fp16; FC2's epilogue undoes the scale.
 //
-// Layout.  FC1: a 32-bit TMEM column holds two bf16 of one row; column c of a
-// 32-weight group holds weights c and c + 16 (one shift-and-mask extracts the
-// sign and magnitude bits of both, a byte permute with sign replication turns
-// the magnitude bits into half-word masks).  The bucketing gather writes x in
-// the same K order.  FC2: one tf32 weight per column, natural K order, and h
-// in natural order.
+// Layout.  A 32-bit TMEM column holds two 16-bit values of one row; column c
+// of a 32-weight group holds weights c and c + 16 (one shift-and-mask extracts
+// the sign and magnitude bits of both, a byte permute with sign replication
+// turns the magnitude bits into half-word masks).  The bucketing gather (x)
+// and pf_h16_kernel (h) write the activations in the same K order.
 //
 // Pipeline: one persistent CTA per SM (20 warps) over (work item of <= 256
 // pairs x 128-row weight tile) units: warp 0 streams 256-weight chunks of the
@@ -31,10 +32,11 @@
 // item's activation rows, with TMA (one lane per box); warps 8-15 expand each step's weights into a TMEM A
 // stage (two warps per 32-row quarter); warp 1 issues 4 MMAs
 // per step and commits; warp 2 prepares the unit records; warps 4-7 drain the
-// accumulator (FC1: SiLU(gate) * up -> fp32 h; FC2: times the routing weight ->
-// fp32 o).  Every wait is bounded.
+// accumulator (FC1: SiLU(gate) * up -> fp32 h; FC2: times the routing weight and
+// the row's h scale -> fp32 o).  Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <cstring>
 
@@ -49,9 +51,8 @@ constexpr int kPfThreads = 640;           // 20 warps, roles above
 constexpr int kBProd = 4;                 // activation producer warps (3, 16, 18, 19), steps in turn
 constexpr int kPfConvWarps = 8;
 constexpr int kPC = 256;                  // weights per weight chunk
-// weights per step: 4 MMAs of K = 16 (bf16, FC1) or K = 8 (tf32, FC2); either way one step
-// is 32 TMEM columns of A and 128-byte activation rows
-template <bool FC1> __host__ __device__ constexpr int step_weights() { return FC1 ? 64 : 32; }
+// weights per step: 4 MMAs of K = 16, i.e. 32 TMEM columns of A and 128-byte activation rows
+constexpr int kStepWeights = 64;
 constexpr int kPRing = 3;                 // weight chunks in flight
 constexpr int kBRing = 5;                 // activation steps in flight
 constexpr int kPAst = 8;                  // TMEM A stages (released in pairs)
@@ -70,7 +71,7 @@ constexpr int kPXchg = kBBase + kBRing * kBStepBytes;
 struct PfMaps {
   CUtensorMap sign, mag, q;      // planes u32 [E N, K/32] box {8, 64} SW32; s16 u8 [E N, K/16] box {16, 64}
   CUtensorMap dcodes, ds4;       // delta u8 [S N, K/2] box {128, 64} SW128; scales box {16, 64}
-  CUtensorMap act, actg;         // activations bf16 [pairs, K] box {64, 64} SW128 (all / gated rows)
+  CUtensorMap act, actg;         // activations bf16 (FC1) / fp16 (FC2) [pairs, K] box {64, 64} SW128 (all / gated rows)
 };
 
 struct PfArgs {
@@ -84,8 +85,8 @@ struct PfArgs {
   const uint8_t* gate;
   const int* hdr;
   const int4* chunks;
-  float* h;                      // FC1 output [pairs, I] (and its gated copy)
-  float* hg;
+  float* h;                      // FC1 output [pairs, I]
+  const float* hscale;           // FC2: per bucketed row, the power of two that undoes the fp16 scaling of h
   float* o;                      // FC2 output
 };
 
@@ -121,46 +122,35 @@ __device__ __forceinline__ bool pf_stuck(const PfSmem& sm) {
   return *reinterpret_cast<const volatile int*>(&sm.stuck) != 0;
 }
 
-// kind::f16 instruction descriptor: fp32 D, bf16 A and B, both K-major, M = 128.
+// kind::f16 instruction descriptor: fp32 D, A and B both bf16 (BF = true) or both fp16, both
+// K-major, M = 128.  The two operands always share the type.
+template <bool BF>
 __device__ __forceinline__ uint32_t f16_idesc(int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+  const uint32_t t = BF ? 1u : 0u;
+  return (1u << 4) | (t << 7) | (t << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 }
 
-// kind::tf32 instruction descriptor: fp32 D, tf32 A and B, both K-major, M = 128.
-__device__ __forceinline__ uint32_t tf32_idesc(int n) {
-  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
-}
-
-template <bool BF16>
 __device__ __forceinline__ void mma_ta(uint32_t d, uint32_t a_tmem, uint64_t bd, uint32_t idesc, uint32_t acc) {
-  if (BF16)
-    asm volatile(
-        "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d),
-        "r"(a_tmem), "l"(bd), "r"(idesc), "r"(acc));
-  else
-    asm volatile(
-        "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p; }" ::"r"(d),
-        "r"(a_tmem), "l"(bd), "r"(idesc), "r"(acc));
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d),
+      "r"(a_tmem), "l"(bd), "r"(idesc), "r"(acc));
 }
 
-// fp32 value rounded to the nearest tf32 (10 explicit mantissa bits; ties away from zero).
-__device__ __forceinline__ float tf32_rna(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return __uint_as_float(r);
+// 16-bit float bits (bf16 if BF, else fp16) of a value that is exact in that format.
+template <bool BF>
+__device__ __forceinline__ uint32_t h16_bits(float f) {
+  return BF ? (__float_as_uint(f) >> 16) : (uint32_t)__half_as_ushort(__float2half_rn(f));
 }
-
-// bf16 bits of an e4m3 value and of three times it (both exact).
-__device__ __forceinline__ uint32_t bf16_bits(float f) { return __float_as_uint(f) >> 16; }
 
 // 32 weights (sign word S, magnitude word M) with block scales s0 (weights 0-15)
-// and s1 (16-31) -> 16 words: word j = bf16 (weight j) | bf16 (weight j + 16) << 16.
-__device__ __forceinline__ void planes_to_bf16(uint32_t S, uint32_t M, uint32_t s0, uint32_t s1, uint32_t out[16]) {
+// and s1 (16-31) -> 16 words: word j = bits (weight j) | bits (weight j + 16) << 16,
+// bf16 (BF) or fp16 (both have the sign in bit 15 of a half).
+template <bool BF>
+__device__ __forceinline__ void planes_to_16(uint32_t S, uint32_t M, uint32_t s0, uint32_t s1, uint32_t out[16]) {
   const float f0 = e4m3_to_f32(s0), f1 = e4m3_to_f32(s1);
-  const uint32_t a0 = bf16_bits(f0), b0 = bf16_bits(3.0f * f0);
-  const uint32_t a1 = bf16_bits(f1), b1 = bf16_bits(3.0f * f1);
+  const uint32_t a0 = h16_bits<BF>(f0), b0 = h16_bits<BF>(3.0f * f0);
+  const uint32_t a1 = h16_bits<BF>(f1), b1 = h16_bits<BF>(3.0f * f1);
   const uint32_t one = a0 | (a1 << 16);                    // q = 1 in both halves
   const uint32_t dif = (a0 ^ b0) | ((a1 ^ b1) << 16);      // q = 1 -> q = 3
 #pragma unroll
@@ -172,34 +162,42 @@ __device__ __forceinline__ void planes_to_bf16(uint32_t S, uint32_t M, uint32_t 
   }
 }
 
-// e2m1 magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6} as bf16, split into byte tables for prmt
-// (first word: codes 0-3, second: codes 4-7)
-constexpr uint32_t kE2m1LoA = 0xC0800000u, kE2m1LoB = 0xC0804000u;   // low bytes
-constexpr uint32_t kE2m1HiA = 0x3F3F3F00u, kE2m1HiB = 0x40404040u;   // high bytes
+// e2m1 magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6} as bf16 and as fp16, split into byte tables for prmt
+// (first word: codes 0-3, second: codes 4-7); the fp16 values have zero low bytes
+constexpr uint32_t kE2m1LoA = 0xC0800000u, kE2m1LoB = 0xC0804000u;   // bf16 low bytes
+constexpr uint32_t kE2m1HiA = 0x3F3F3F00u, kE2m1HiB = 0x40404040u;   // bf16 high bytes
+constexpr uint32_t kE2m1F16A = 0x3E3C3800u, kE2m1F16B = 0x46444240u; // fp16 high bytes
 
-__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+template <bool BF>
+__device__ __forceinline__ uint32_t mul_16x2(uint32_t a, uint32_t b) {
   uint32_t d;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  if (BF)
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  else
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
 
-// Two e2m1 codes (bits 0-3 and 8-11 of c) times the bf16x2 scales sc -> bf16x2 (exact: a code
-// value has 2 significant bits, an e4m3 scale 4).
-__device__ __forceinline__ uint32_t e2m1x2_bf16(uint32_t c, uint32_t sc) {
+// Two e2m1 codes (bits 0-3 and 8-11 of c) times the 16x2 scales sc -> 16x2 (exact: a code
+// value has 2 significant bits, an e4m3 scale 4, and the products stay in the normal range).
+template <bool BF>
+__device__ __forceinline__ uint32_t e2m1x2_16(uint32_t c, uint32_t sc) {
   const uint32_t sel = c & 0x0707u;
-  const uint32_t mag = prmt(kE2m1LoA, kE2m1LoB, sel) | (prmt(kE2m1HiA, kE2m1HiB, sel) << 8);
-  return mul_bf16x2(mag, sc) ^ (((c & 0x0008u) << 12) | ((c & 0x0800u) << 20));
+  const uint32_t mag = BF ? (prmt(kE2m1LoA, kE2m1LoB, sel) | (prmt(kE2m1HiA, kE2m1HiB, sel) << 8))
+                          : (prmt(kE2m1F16A, kE2m1F16B, sel) << 8);
+  return mul_16x2<BF>(mag, sc) ^ (((c & 0x0008u) << 12) | ((c & 0x0800u) << 20));
 }
 
-// FC1: 32 delta codes (16 bytes: byte t = codes of weights 2t, 2t+1, low nibble first) with
-// block scales s0 (weights 0-15), s1 (16-31) -> word j = bf16 (weight j) | bf16 (weight j + 16) << 16.
-__device__ __forceinline__ void delta_to_bf16(uint4 c, uint32_t s0, uint32_t s1, uint32_t out[16]) {
-  const uint32_t sc = bf16_bits(e4m3_to_f32(s0)) | (bf16_bits(e4m3_to_f32(s1)) << 16);
+// 32 delta codes (16 bytes: byte t = codes of weights 2t, 2t+1, low nibble first) with block
+// scales s0 (weights 0-15), s1 (16-31) -> word j = bits (weight j) | bits (weight j + 16) << 16.
+template <bool BF>
+__device__ __forceinline__ void delta_to_16(uint4 c, uint32_t s0, uint32_t s1, uint32_t out[16]) {
+  const uint32_t sc = h16_bits<BF>(e4m3_to_f32(s0)) | (h16_bits<BF>(e4m3_to_f32(s1)) << 16);
   const uint32_t lo[2] = {c.x, c.y}, hi[2] = {c.z, c.w};
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const int sh = 4 * (j & 7);
-    out[j] = e2m1x2_bf16(((lo[j >> 3] >> sh) & 15u) | (((hi[j >> 3] >> sh) & 15u) << 8), sc);
+    out[j] = e2m1x2_16<BF>(((lo[j >> 3] >> sh) & 15u) | (((hi[j >> 3] >> sh) & 15u) << 8), sc);
   }
 }
 
@@ -233,6 +231,62 @@ __global__ void __launch_bounds__(128) pf_gather_kernel(int pairs, int k, int H,
   }
   reinterpret_cast<uint4*>(xb + (size_t)pos * H)[t] = v;
   if (xbg != nullptr) reinterpret_cast<uint4*>(xbg + (size_t)pos * H)[t] = gated ? v : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// FC1's fp32 h (bucketed rows, natural K order) -> FC2's fp16 operand in the permuted K order
+// (as xb), each row times the power of two 2^-e that puts its max |h| in [2^14, 2^15), and
+// hscale[pos] = 2^e; hg16 the same for gated pairs, zero for the others.  One CTA per row.
+__global__ void __launch_bounds__(256) pf_h16_kernel(int pairs, int k, int I, const float* __restrict__ h,
+                                                     const int32_t* __restrict__ perm,
+                                                     const uint8_t* __restrict__ gate, uint16_t* __restrict__ h16,
+                                                     uint16_t* __restrict__ hg16, float* __restrict__ hscale) {
+  const int pos = blockIdx.x;
+  const float* row = h + (size_t)pos * I;
+  __shared__ float red[8];
+  float mx = 0.0f;
+  for (int c = threadIdx.x; c < I / 4; c += blockDim.x) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(row) + c);
+    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  mx = red[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) mx = fmaxf(mx, red[w]);
+  // 2^-e with max * 2^-e in [2^14, 2^15): e = (exponent of max) - 15; a zero or non-finite
+  // maximum keeps the row as it is
+  int e = 0;
+  if (mx > 0.0f && mx <= 3.0e38f) {
+    frexpf(mx, &e);                                        // mx = f 2^e, f in [0.5, 1)
+    e = e - 15 < -112 ? -112 : e - 15;                     // 2^-e stays finite in fp32
+  }
+  const float down = ldexpf(1.0f, -e);
+  const int p = __ldg(perm + pos);
+  bool gated = false;
+  if (p >= 0 && p < pairs) {
+    gated = gate != nullptr && __ldg(gate + p / k) != 0;
+  } else if (threadIdx.x == 0) {
+    record_error(MOET_ERR_DEVICE_INDEX);
+  }
+  if (threadIdx.x == 0) hscale[pos] = ldexpf(1.0f, e);
+  // 8 outputs per thread: k' = 8 t .. 8 t + 7 of the permuted order, where k' = 32 g + 2 c + b
+  // holds element 32 g + c + 16 b
+  for (int t = threadIdx.x; t < I / 8; t += blockDim.x) {
+    const int g = t >> 2, q = t & 3;
+    const float4 lo = __ldg(reinterpret_cast<const float4*>(row + 32 * g + 4 * q));
+    const float4 hi = __ldg(reinterpret_cast<const float4*>(row + 32 * g + 16 + 4 * q));
+    const float a[4] = {lo.x, lo.y, lo.z, lo.w}, b[4] = {hi.x, hi.y, hi.z, hi.w};
+    uint32_t wv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      wv[i] = (uint32_t)__half_as_ushort(__float2half_rn(a[i] * down)) |
+              ((uint32_t)__half_as_ushort(__float2half_rn(b[i] * down)) << 16);
+    const uint4 v = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    reinterpret_cast<uint4*>(h16 + (size_t)pos * I)[t] = v;
+    if (hg16 != nullptr) reinterpret_cast<uint4*>(hg16 + (size_t)pos * I)[t] = gated ? v : make_uint4(0u, 0u, 0u, 0u);
+  }
 }
 
 // ---------------------------------------------------------------- FC kernel
@@ -310,7 +364,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
           }
           continue;
         }
-        for (int s = 0; s < kPC / step_weights<FC1>(); ++s, ++gs) {
+        for (int s = 0; s < kPC / kStepWeights; ++s, ++gs) {
           if (gs % kBProd != bprod) continue;
           const int bs = gs % kBRing;
           if (gs >= kBRing && !mbar_wait_warp(&sm.bdone[bs], ((gs / kBRing) - 1) & 1)) { bad = true; break; }
@@ -318,7 +372,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
           if (lane == 0) mbar_expect_tx(&sm.bfull[bs], (uint32_t)nb * 64u * 128u);
           __syncwarp();
           if (lane < nb)
-            tma_load_2d(smem_addr(bst + 8192 * lane), dp ? &maps.actg : &maps.act, cc * kPC + s * step_weights<FC1>(),
+            tma_load_2d(smem_addr(bst + 8192 * lane), dp ? &maps.actg : &maps.act, cc * kPC + s * kStepWeights,
                         pos0 + 64 * lane, &sm.bfull[bs]);
         }
       }
@@ -343,8 +397,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
         if (j >= 1 && !mbar_wait(&sm.acc_empty, (j - 1) & 1)) { bad = true; break; }
         if (pf_stuck(sm)) { bad = true; break; }
         asm volatile("tcgen05.fence::after_thread_sync;");
-        const int nst = sm.meta[m].nck * (kPC / step_weights<FC1>());
-        const uint32_t idesc = FC1 ? f16_idesc(sm.meta[m].ncols) : tf32_idesc(sm.meta[m].ncols);
+        const int nst = sm.meta[m].nck * (kPC / kStepWeights);
+        const uint32_t idesc = f16_idesc<FC1>(sm.meta[m].ncols);   // FC1 bf16, FC2 fp16
         // two steps per iteration: both A stages expanded, both steps' activations landed
         for (int st = 0; st < nst; st += 2, gs += 2) {
           if (!mbar_wait(&sm.staged[(gs >> 1) % (kPAst / 2)], ((gs >> 1) / (kPAst / 2)) & 1) ||
@@ -360,7 +414,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
             const uint32_t bsm = smem_addr(base + kBBase + bs * kBStepBytes);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-              mma_ta<FC1>(tmem, tmem + kPColA + 32 * as + 8 * i, sw128_desc(bsm + 32 * i), idesc,
+              mma_ta(tmem, tmem + kPColA + 32 * as + 8 * i, sw128_desc(bsm + 32 * i), idesc,
                           (st > 0 || h > 0 || i > 0) ? 1u : 0u);
           }
           tc_commit(&sm.bdone[gs % kBRing]);
@@ -449,7 +503,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
       const PfMeta& um = sm.meta[m];
       const int ncols = um.ncols, ntok = um.ntok, pos0 = um.pos0;
       const float sc2 = um.sc2;
-      const int dslot_unit = a.hg != nullptr ? um.dslot : -1;
       const int wrow = trow < 64 ? um.r0 + trow : um.r1 + trow - 64;
       for (int c0 = 0; c0 < ncols; c0 += 16) {
         float v[16];
@@ -459,7 +512,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
           for (int i = 0; i < 16; ++i) {
             const int col = c0 + i;
             const int p = um.pair[col];
-            if (col < ntok && p >= 0) a.o[(size_t)p * a.H + wrow] = v[i] * sc2 * um.wts[col];
+            if (col < ntok && p >= 0)
+              a.o[(size_t)p * a.H + wrow] = v[i] * sc2 * um.wts[col] * __ldg(a.hscale + pos0 + col);
           }
         } else {
           // SiLU(gate) * up: the gate rows (quarters 0-1) finish columns c0 .. c0 + 7, the up rows
@@ -489,13 +543,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
             const int col = cb + i;
             if (col < ntok) {
               const float gv = g[i] * sc2, uv = u[i] * sc2;
-              // h goes to FC2's tf32 MMA, which keeps the top 19 bits of each input: round it to
-              // nearest tf32 here so that FC2 sees an unbiased value, not a truncated one
-              const float hv = tf32_rna(__fdividef(gv, 1.0f + __expf(-gv)) * uv);
-              const size_t at = (size_t)(pos0 + col) * a.I + hcol;
-              a.h[at] = hv;
-              // the gated copy feeds FC2's delta pass, which runs for exactly these units
-              if (dslot_unit >= 0) a.hg[at] = um.gated[col] ? hv : 0.0f;
+              a.h[(size_t)(pos0 + col) * a.I + hcol] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
             }
           }
           asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -526,7 +574,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
         if (!mbar_wait_warp(&sm.pfull[ps], (gc / kPRing) & 1)) { bad = true; break; }
         const unsigned char* pst = base + kPBase + ps * kPChunkBytes;
         const bool dp = c >= nkc;
-        constexpr int kSteps = kPC / step_weights<FC1>();
+        constexpr int kSteps = kPC / kStepWeights;
         // steps in pairs (the MMA thread consumes them in pairs): one TMEM fence and one arrive per pair
         for (int s = 0; s < kSteps; s += 2, gs += 2) {
           // the pair's A stages are free once the MMAs of the pair that used them last are done
@@ -534,35 +582,25 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
             const int q = (gs - kPAst) >> 1;
             if (!mbar_wait_warp(&sm.adone[q % (kPAst / 2)], (q / (kPAst / 2)) & 1)) { bad = true; break; }
           }
-          // FC1: half h expands 32-weight group 2 (s + h2) + h of step s + h2 (bf16 pairs of weights
-          // c and c + 16 per column).  FC2: half h expands all of step s + h (tf32, one weight per
-          // column), so no pair of weights is expanded twice.
+          // half h expands 32-weight group 2 (s + h2) + h of step s + h2 (16-bit pairs of weights
+          // c and c + 16 per column)
 #pragma unroll
-          for (int h2 = 0; h2 < (FC1 ? 2 : 1); ++h2) {
-            const int wi = FC1 ? 2 * (s + h2) + half : s + half;
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int wi = 2 * (s + h2) + half;
             const uint32_t sc = *reinterpret_cast<const uint16_t*>(pst + (dp ? 16384 : 8192) + trow * 16 + 2 * wi);
             const uint32_t s0 = sc & 0xFFu, s1 = sc >> 8;
             uint32_t av[16];
             if (!dp) {
               // 32-byte-swizzled plane rows: 16-byte piece p of row r at p ^ ((r >> 2) & 1)
               const int wo = trow * 32 + ((((wi >> 2) ^ ((trow >> 2) & 1))) << 4) + 4 * (wi & 3);
-              planes_to_bf16(*reinterpret_cast<const uint32_t*>(pst + wo),
-                             *reinterpret_cast<const uint32_t*>(pst + 4096 + wo), s0, s1, av);
+              planes_to_16<FC1>(*reinterpret_cast<const uint32_t*>(pst + wo),
+                                *reinterpret_cast<const uint32_t*>(pst + 4096 + wo), s0, s1, av);
             } else {
               // 128-byte-swizzled code rows: piece p of row r at p ^ (r & 7)
-              delta_to_bf16(*reinterpret_cast<const uint4*>(pst + trow * 128 + ((wi ^ (trow & 7)) << 4)), s0, s1, av);
+              delta_to_16<FC1>(*reinterpret_cast<const uint4*>(pst + trow * 128 + ((wi ^ (trow & 7)) << 4)), s0, s1,
+                               av);
             }
-            if (FC1) {
-              tmem_st16(tmem + lane_q + kPColA + 32 * ((gs + h2) % kPAst) + 16 * half, av);
-            } else {
-              // word j holds weights j and j + 16: tf32 columns j and j + 16
-              uint32_t lo[16], hi[16];
-#pragma unroll
-              for (int j = 0; j < 16; ++j) { lo[j] = av[j] << 16; hi[j] = av[j] & 0xFFFF0000u; }
-              const uint32_t col = tmem + lane_q + kPColA + 32 * ((gs + half) % kPAst);
-              tmem_st16(col, lo);
-              tmem_st16(col + 16, hi);
-            }
+            tmem_st16(tmem + lane_q + kPColA + 32 * ((gs + h2) % kPAst) + 16 * half, av);
           }
           asm volatile("tcgen05.wait::st.sync.aligned;");
           asm volatile("tcgen05.fence::before_thread_sync;");
@@ -594,14 +632,14 @@ moet_status launch_pf(const PfArgs& a, const moet_planes* pl, const moet_nvfp4* 
   bool ok = make_map(&m.sign, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, pl->sign, rowsW, K / 32, 8, 64, CU_TENSOR_MAP_SWIZZLE_32B) &&
             make_map(&m.mag, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, pl->mag, rowsW, K / 32, 8, 64, CU_TENSOR_MAP_SWIZZLE_32B) &&
             make_map(&m.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pl->s16, rowsW, K / 16, 16, 64, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-            (FC1 ? make_map(&m.act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, act, (uint64_t)pairs, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)
-                 : make_map(&m.act, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, act, (uint64_t)pairs, K, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B));
+            make_map(&m.act, FC1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, act,
+                     (uint64_t)pairs, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
   if (ok && a.delta_slot != nullptr) {
     const uint64_t rowsD = (uint64_t)a.n_slots * a.N;
     ok = make_map(&m.dcodes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dl->codes, rowsD, K / 2, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
          make_map(&m.ds4, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dl->s4, rowsD, K / 16, 16, 64, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-         (FC1 ? make_map(&m.actg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, actg, (uint64_t)pairs, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)
-              : make_map(&m.actg, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, actg, (uint64_t)pairs, K, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B));
+         make_map(&m.actg, FC1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, actg,
+                  (uint64_t)pairs, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   if (!ok) return MOET_ERR_CUDA;
   const int grid = sm_count();
@@ -637,14 +675,21 @@ moet_status pf_forward(const PfForwardArgs& f, cudaStream_t st) {
   PfArgs a1 = a;
   a1.K = f.H; a1.N = 2 * f.I; a1.tiles = f.I / 64;
   a1.scale_2 = f.fc1->scale_2;
-  a1.h = f.h; a1.hg = with_delta ? f.hg : nullptr;
+  a1.h = f.h;
   moet_status s = launch_pf<true>(a1, f.fc1, f.dfc1, f.xb, f.xbg, pairs, f.E, st);
   if (s != MOET_OK) return s;
+  {
+    ProfScope ps(MOET_K_TERMS, st);
+    pf_h16_kernel<<<pairs, 256, 0, st>>>(pairs, f.k, f.I, f.h, f.perm, with_delta ? f.gate : nullptr, f.h16,
+                                         with_delta ? f.hg16 : nullptr, f.hscale);
+  }
+  MOET_CUDA_TRY(cudaGetLastError());
   PfArgs a2 = a;
   a2.K = f.I; a2.N = f.H; a2.tiles = f.H / 128;
   a2.scale_2 = f.fc2->scale_2;
+  a2.hscale = f.hscale;
   a2.o = f.o;
-  return launch_pf<false>(a2, f.fc2, f.dfc2, f.h, f.hg, pairs, f.E, st);
+  return launch_pf<false>(a2, f.fc2, f.dfc2, f.h16, f.hg16, pairs, f.E, st);
 }
 
 }  // namespace moet

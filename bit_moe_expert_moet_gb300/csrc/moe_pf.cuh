@@ -15,10 +15,11 @@ constexpr int kPfTok = 256;   // routed pairs per work item -> MMA N <= 256
 inline bool pf_supported(int H, int I) { return H % 256 == 0 && I % 256 == 0; }
 
 // Bytes of the engine's extra activation buffers for `pairs` routed pairs: x in
-// bucketed order as bf16 plus its gated copy (rows of ungated pairs zero), and
-// the gated copy of h (fp32; h itself is the forward's h buffer).
+// bucketed order as bf16 plus its gated copy (rows of ungated pairs zero), h as
+// scaled fp16 plus its gated copy, and the per-row scales of h (FC1 writes fp32
+// h into the forward's h buffer).
 inline size_t pf_act_bytes(size_t pairs, size_t H, size_t I) {
-  return pairs * H * 2 * sizeof(uint16_t) + pairs * I * sizeof(float);
+  return pairs * H * 2 * sizeof(uint16_t) + pairs * I * 2 * sizeof(uint16_t) + pairs * sizeof(float);
 }
 
 struct PfForwardArgs {
@@ -39,7 +40,9 @@ struct PfForwardArgs {
   uint16_t* xb;                // [T k, H] bf16, bucketed rows, K permuted within 32-groups
   uint16_t* xbg;               // same, rows of ungated pairs zero
   float* h;                    // [T k, I] fp32, FC1 output (bucketed rows, natural order)
-  float* hg;                   // same, rows of ungated pairs zero
+  uint16_t* h16;               // [T k, I] fp16, h times 2^-e per row, K permuted within 32-groups
+  uint16_t* hg16;              // same, rows of ungated pairs zero
+  float* hscale;               // [T k] 2^e per bucketed row
   float* o;                    // [T k, H] pair order
 };
 
