@@ -363,6 +363,33 @@ def test_forward_mid_size(moet, T):
     check_y(yg2, _oracle_forward(logits, xb, k, ref))
 
 
+@pytest.mark.parametrize("T", [64, 600])
+def test_forward_extreme_token_magnitudes(moet, T):
+    """Tokens scaled by 1e-12 and 1e+12 and an all-zero token, each group held to the layer
+    tolerance on its own (a global check would not see a tiny token): the activation scaling of
+    both engines -- per-token NVFP4 term scales (T = 64) and the per-row power-of-two scaling of
+    h into fp16 (T = 600) -- must follow the magnitude."""
+    H, I, E, k = 1024, 256, 16, 4
+    rng = np.random.default_rng(70 + T)
+    dset = np.array([2, 7, 9], dtype=np.int32)
+    ref, gp = _make_layer(moet, H, I, E, dset, rng=rng)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    x = rng.standard_normal((T, H)).astype(np.float32)
+    tiny, huge, zero = np.arange(0, 5), np.arange(5, 10), 10
+    x[tiny] *= np.float32(1e-12)
+    x[huge] *= np.float32(1e12)
+    x[zero] = 0.0
+    xb = W.f32_to_bf16_bits(x)
+    gate = (rng.random(T) < 0.5).astype(np.uint8)
+    yg, err = _run_forward(moet, logits, xb, k, gp, E, H, dset, gate)
+    assert err == 0
+    yo = _oracle_forward(logits, xb, k, ref, dset, gate, E)
+    yg = np.asarray(yg, np.float64)
+    for rows in (tiny, huge, np.arange(11, T)):
+        check_y(yg[rows], yo[rows])
+    assert not yg[zero].any() and not yo[zero].any()
+
+
 @pytest.mark.parametrize("gate_mode", ["draw", "all", "none"])
 def test_forward_prefill_ragged_items(moet, gate_mode):
     """Prefill engine with experts of more than 256 pairs: items split at 256 with a ragged
