@@ -289,10 +289,11 @@ MOET_ERROR_ACCESSOR(moet_internal_error_requant)
 constexpr int kFp8Block = 128;
 
 // e4m3 satfinite RNE of a / d for a >= 0, d > 0, both exact in fp64 with d * (two neighbouring
-// e4m3 values) exact: a guess from the rounded quotient, corrected against the doubled midpoints.
-__device__ __forceinline__ uint32_t e4m3_rne_ratio_dd(double a, double d) {
+// e4m3 values) exact: a guess from a * inv_d (inv_d ~ 1 / d; the guess is within one code, the
+// quotient itself is never used), corrected against the doubled midpoints.
+__device__ __forceinline__ uint32_t e4m3_rne_ratio_dd(double a, double d, double inv_d) {
   if (!(a > 0.0)) return 0u;                          // zero (also for an all-zero matrix, d = 0)
-  uint32_t c = f32_to_e4m3_rn((float)(a / d));
+  uint32_t c = f32_to_e4m3_rn((float)(a * inv_d));
   const double a2 = 2.0 * a;
   if (c < 126u) {
     const double m2 = d * ((double)e4m3_to_f32(c) + (double)e4m3_to_f32(c + 1));
@@ -359,6 +360,21 @@ __global__ void __launch_bounds__(1024) fp8_scale2_kernel(int N, int K, const ui
   }
 }
 
+// A matrix's scale_2 with the two divisors of the rule and guesses of their inverses.
+struct Scale2 {
+  double s2, d3, d6, i3, i6;
+};
+
+__device__ __forceinline__ Scale2 make_scale2(float sc2) {
+  Scale2 c;
+  c.s2 = (double)sc2;
+  c.d3 = 3.0 * c.s2;                                  // exact: 26 significant bits
+  c.d6 = 6.0 * c.s2;
+  c.i3 = 1.0 / c.d3;                                  // inf for a zero matrix, never used there
+  c.i6 = 1.0 / c.d6;
+  return c;
+}
+
 // The NVFP4 rule on one block of 16 exact weights (fp64) with their sign bits (bit j = weight j)
 // and the matrix's scale_2: the block's s16 and magnitude bits and, when `delta` is set, its 16
 // delta codes (two words, low nibble first) and delta scale.
@@ -366,13 +382,14 @@ struct Block16 {
   uint32_t mag, s16, dlo, dhi, ds4;
 };
 
-__device__ __forceinline__ Block16 exact_rule_16(const double (&wv)[16], uint32_t sbits, double s2,
+__device__ __forceinline__ Block16 exact_rule_16(const double (&wv)[16], uint32_t sbits, const Scale2& sc,
                                                  bool delta) {
+  const double s2 = sc.s2;
   Block16 r = {0u, 0u, 0u, 0u, 0u};
   double bmax = 0.0;
 #pragma unroll
   for (int j = 0; j < 16; ++j) bmax = fmax(bmax, fabs(wv[j]));
-  r.s16 = e4m3_rne_ratio_dd(bmax, 3.0 * s2);
+  r.s16 = e4m3_rne_ratio_dd(bmax, sc.d3, sc.i3);
   const double lvl = (double)e4m3_to_f32(r.s16) * s2;                   // s16 scale_2, exact
   double d[16];
   double dmax = 0.0;
@@ -385,7 +402,7 @@ __device__ __forceinline__ Block16 exact_rule_16(const double (&wv)[16], uint32_
     dmax = fmax(dmax, fabs(d[j]));
   }
   if (delta) {
-    r.ds4 = e4m3_rne_ratio_dd(dmax, 6.0 * s2);
+    r.ds4 = e4m3_rne_ratio_dd(dmax, sc.d6, sc.i6);
     const double step = (double)e4m3_to_f32(r.ds4) * s2;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
@@ -408,12 +425,17 @@ __global__ void __launch_bounds__(256) requant_fp8_kernel(
   const long long n_groups = (long long)M * gpm;
   const int nbn = (N + kFp8Block - 1) / kFp8Block, nbk = (K + kFp8Block - 1) / kFp8Block;
   const bool delta = dcodes_out != nullptr;
+  int m_sc = -1;
+  Scale2 sc;
   for (long long gi = (long long)blockIdx.x * blockDim.x + threadIdx.x; gi < n_groups;
        gi += (long long)gridDim.x * blockDim.x) {
     const int m = (int)(gi / gpm);
     const long long r = gi - (long long)m * gpm;
     const int n = (int)(r / (K / 32)), k0 = (int)(r - (long long)n * (K / 32)) * 32;
-    const double s2 = (double)__ldg(scale_2 + m);
+    if (m != m_sc) {
+      sc = make_scale2(__ldg(scale_2 + m));
+      m_sc = m;
+    }
     const double bs = fp8_bscale(bscale + (size_t)m * nbn * nbk, n, k0, nbk);
     const uint4* src = reinterpret_cast<const uint4*>(codes + ((size_t)m * N + n) * K + k0);
     const uint4 c0 = __ldg(src), c1 = __ldg(src + 1);
@@ -430,7 +452,7 @@ __global__ void __launch_bounds__(256) requant_fp8_kernel(
         wv[j] = (c & 0x80u) ? -a : a;
         sign |= (c >> 7) << (16 * b + j);
       }
-      const Block16 o = exact_rule_16(wv, sign >> (16 * b), s2, delta);
+      const Block16 o = exact_rule_16(wv, sign >> (16 * b), sc, delta);
       mag |= o.mag << (16 * b);
       s16pair |= o.s16 << (8 * b);
       ds4pair |= o.ds4 << (8 * b);
@@ -492,43 +514,118 @@ __global__ void __launch_bounds__(1024) mxfp4_scale2_kernel(int N, int K, const 
   }
 }
 
-// One thread per 32-weight group (16 code bytes and one exponent byte in, like the FP8 kernel out).
+// e2m1 magnitude code of RNE(a / s) like e2m1_rne_mag_d, by bisection over the same seven
+// thresholds (t[i] = midpoint i times s, with its own comparison: > for even i, >= for odd i).
+__device__ __forceinline__ uint32_t e2m1_rne_mag_bisect(double a, const double (&t)[7]) {
+  uint32_t c = a >= t[3] ? 4u : 0u;
+  c += (c ? a >= t[5] : a >= t[1]) ? 2u : 0u;
+  const double u = c == 0u ? t[0] : c == 2u ? t[2] : c == 4u ? t[4] : t[6];
+  return c + (a > u ? 1u : 0u);
+}
+
+// Bit v of the result: some nibble of the 16 in (a, b) has magnitude code v.  A nibble of
+// x = (w & 7 per nibble) ^ v is zero exactly where the code is v; the borrow test
+// (x - 0x1..1) & ~x & 0x8..8 is nonzero iff some nibble of x is zero.
+__device__ __forceinline__ uint32_t codes_present(uint32_t a, uint32_t b) {
+  const uint32_t ma = a & 0x77777777u, mb = b & 0x77777777u;
+  uint32_t pres = 0;
+#pragma unroll
+  for (uint32_t v = 0; v < 8; ++v) {
+    const uint32_t xa = ma ^ (v * 0x11111111u), xb = mb ^ (v * 0x11111111u);
+    const uint32_t z = ((xa - 0x11111111u) & ~xa) | ((xb - 0x11111111u) & ~xb);
+    pres |= ((z & 0x88888888u) != 0u ? 1u : 0u) << v;
+  }
+  return pres;
+}
+
+// Delta codes of the 8 nibbles of w from per-code tables: byte c of (tlo, thi) is the delta code
+// of a positive weight with magnitude code c, byte c of (flo, fhi) is 8 when that code is nonzero
+// (a negative weight flips it).  Even and odd nibbles go through one byte permute each.
+__device__ __forceinline__ uint32_t delta_from_tables(uint32_t w, uint32_t tlo, uint32_t thi, uint32_t flo,
+                                                      uint32_t fhi) {
+  const uint32_t ce = w & 0x07070707u, co = (w >> 4) & 0x07070707u;   // codes of nibbles 0,2,4,6 / 1,3,5,7
+  const uint32_t se = (ce | (ce >> 4)) & 0x00FF00FFu, so = (co | (co >> 4)) & 0x00FF00FFu;
+  const uint32_t sel_e = (se | (se >> 8)) & 0xFFFFu, sel_o = (so | (so >> 8)) & 0xFFFFu;
+  const uint32_t de = prmt(tlo, thi, sel_e) ^ (prmt(flo, fhi, sel_e) & (w & 0x08080808u));
+  const uint32_t dd = prmt(tlo, thi, sel_o) ^ (prmt(flo, fhi, sel_o) & ((w >> 4) & 0x08080808u));
+  return de | (dd << 4);
+}
+
+// One thread per 32-weight group (16 code bytes and one exponent byte in, like the FP8 kernel
+// out).  All 32 weights share p2 = 2^(e - 127), so within a 16-block every decision of the rule is
+// a function of the 3-bit magnitude code: the fp64 work runs once per block over the 8 codes (s16
+// from the largest code present, the |q| = 3 threshold code, the delta scale from the codes
+// present, the 8 delta codes), and the 16 weights take integer operations only.
 __global__ void __launch_bounds__(256) requant_mxfp4_kernel(
     int M, long long gpm, const uint4* __restrict__ codes, const uint8_t* __restrict__ e8m0,
     const float* __restrict__ scale_2, uint32_t* __restrict__ sign_out, uint32_t* __restrict__ mag_out,
     uint16_t* __restrict__ s16_out, uint4* __restrict__ dcodes_out, uint16_t* __restrict__ ds4_out) {
   const long long n_groups = (long long)M * gpm;
   const bool delta = dcodes_out != nullptr;
+  int m_sc = -1;
+  Scale2 sc;
   for (long long gi = (long long)blockIdx.x * blockDim.x + threadIdx.x; gi < n_groups;
        gi += (long long)gridDim.x * blockDim.x) {
-    const double s2 = (double)__ldg(scale_2 + gi / gpm);
+    const int m = (int)(gi / gpm);
+    if (m != m_sc) {
+      sc = make_scale2(__ldg(scale_2 + m));
+      m_sc = m;
+    }
     const double p2 = e8m0_value(__ldg(e8m0 + gi));
     const uint4 cw = __ldg(codes + gi);
-    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-    uint32_t sign = 0, mag = 0, s16pair = 0, ds4pair = 0;
-    uint32_t dwords[4] = {0, 0, 0, 0};
+    const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+    double wv[8];                                                        // e2m1 value of code c times p2
+#pragma unroll
+    for (int c = 0; c < 8; ++c) wv[c] = (double)e2m1_mag_value((uint32_t)c) * p2;   // exact
+    uint32_t mr[4], s16pair = 0, ds4pair = 0, dw[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
-      double wv[16];
+      const uint32_t wa = w[2 * b], wb = w[2 * b + 1];
+      const uint32_t pres = codes_present(wa, wb);
+      const uint32_t cmax = 31u - (uint32_t)__clz(pres);                 // pres != 0: 16 codes
+      double bmax = 0.0;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const uint32_t c = (words[2 * b + (j >> 3)] >> (4 * (j & 7))) & 0xFu;
-        const double a = (double)e2m1_mag_value(c & 7u) * p2;             // exact
-        wv[j] = (c & 8u) ? -a : a;
-        sign |= (c >> 3) << (16 * b + j);
+      for (int c = 0; c < 8; ++c) bmax = (uint32_t)c == cmax ? wv[c] : bmax;
+      const uint32_t s16 = e4m3_rne_ratio_dd(bmax, sc.d3, sc.i3);
+      const double lvl = (double)e4m3_to_f32(s16) * sc.s2;              // exact
+      uint32_t thr = 0;                                                  // |q| = 3 iff code >= thr
+#pragma unroll
+      for (int c = 0; c < 8; ++c) thr += wv[c] < 2.0 * lvl ? 1u : 0u;
+      s16pair |= s16 << (8 * b);
+      const uint32_t T = thr * 0x11111111u;
+      mr[2 * b] = gather_bit3(((wa | 0x88888888u) - T) & 0x88888888u);
+      mr[2 * b + 1] = gather_bit3(((wb | 0x88888888u) - T) & 0x88888888u);
+      if (delta) {
+        double d[8], dmax = 0.0;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          d[c] = wv[c] - ((uint32_t)c >= thr ? 3.0 : 1.0) * lvl;         // exact
+          if ((pres >> c) & 1u) dmax = fmax(dmax, fabs(d[c]));
+        }
+        const uint32_t ds4 = e4m3_rne_ratio_dd(dmax, sc.d6, sc.i6);
+        const double step = (double)e4m3_to_f32(ds4) * sc.s2;
+        const double t[7] = {0.25 * step, 0.75 * step, 1.25 * step, 1.75 * step, 2.5 * step, 3.5 * step,
+                             5.0 * step};
+        uint32_t tlo = 0, thi = 0, flo = 0, fhi = 0;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t dm = step > 0.0 ? e2m1_rne_mag_bisect(fabs(d[c]), t) : 0u;
+          const uint32_t e = dm | ((d[c] < 0.0 && dm != 0u) ? 8u : 0u);  // for a positive weight
+          const uint32_t f = dm != 0u ? 8u : 0u;
+          if (c < 4) { tlo |= e << (8 * c); flo |= f << (8 * c); }
+          else { thi |= e << (8 * (c - 4)); fhi |= f << (8 * (c - 4)); }
+        }
+        ds4pair |= ds4 << (8 * b);
+        dw[2 * b] = delta_from_tables(wa, tlo, thi, flo, fhi);
+        dw[2 * b + 1] = delta_from_tables(wb, tlo, thi, flo, fhi);
       }
-      const Block16 o = exact_rule_16(wv, sign >> (16 * b), s2, delta);
-      mag |= o.mag << (16 * b);
-      s16pair |= o.s16 << (8 * b);
-      ds4pair |= o.ds4 << (8 * b);
-      dwords[2 * b] = o.dlo;
-      dwords[2 * b + 1] = o.dhi;
     }
-    sign_out[gi] = sign;
-    mag_out[gi] = mag;
+    sign_out[gi] = assemble_bits(gather_bit3(w[0] & 0x88888888u), gather_bit3(w[1] & 0x88888888u),
+                                 gather_bit3(w[2] & 0x88888888u), gather_bit3(w[3] & 0x88888888u));
+    mag_out[gi] = assemble_bits(mr[0], mr[1], mr[2], mr[3]);
     s16_out[gi] = (uint16_t)s16pair;
     if (delta) {
-      dcodes_out[gi] = make_uint4(dwords[0], dwords[1], dwords[2], dwords[3]);
+      dcodes_out[gi] = make_uint4(dw[0], dw[1], dw[2], dw[3]);
       ds4_out[gi] = (uint16_t)ds4pair;
     }
   }
