@@ -306,18 +306,20 @@ __device__ __forceinline__ uint32_t e4m3_rne_ratio_dd(double a, double d, double
   return c;
 }
 
-// e2m1 magnitude code of RNE(a / s), saturating, ties to even, by exact comparison with the
-// seven midpoints scaled by s (fp64).
-__device__ __forceinline__ uint32_t e2m1_rne_mag_d(double a, double s) {
-  uint32_t c = 0;
-  c += (a > 0.25 * s);
-  c += (a >= 0.75 * s);
-  c += (a > 1.25 * s);
-  c += (a >= 1.75 * s);
-  c += (a > 2.5 * s);
-  c += (a >= 3.5 * s);
-  c += (a > 5.0 * s);
-  return c;
+// e2m1 magnitude code of RNE(a / s), saturating, ties to even, by exact comparison with the seven
+// midpoints of the e2m1 grid scaled by s, t[i] = {0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5}[i] * s
+// (exact in fp64): the code is the number of thresholds a passes, > for even i and >= for odd i
+// (ties to the even code), found by bisection.
+__device__ __forceinline__ uint32_t e2m1_rne_mag_bisect(double a, const double (&t)[7]) {
+  uint32_t c = a >= t[3] ? 4u : 0u;
+  c += (c ? a >= t[5] : a >= t[1]) ? 2u : 0u;
+  const double u = c == 0u ? t[0] : c == 2u ? t[2] : c == 4u ? t[4] : t[6];
+  return c + (a > u ? 1u : 0u);
+}
+
+__device__ __forceinline__ void e2m1_thresholds(double step, double (&t)[7]) {
+  t[0] = 0.25 * step; t[1] = 0.75 * step; t[2] = 1.25 * step; t[3] = 1.75 * step;
+  t[4] = 2.5 * step; t[5] = 3.5 * step; t[6] = 5.0 * step;
 }
 
 __device__ __forceinline__ double fp8_bscale(const float* bscale, int n, int k, int nbk) {
@@ -404,9 +406,11 @@ __device__ __forceinline__ Block16 exact_rule_16(const double (&wv)[16], uint32_
   if (delta) {
     r.ds4 = e4m3_rne_ratio_dd(dmax, sc.d6, sc.i6);
     const double step = (double)e4m3_to_f32(r.ds4) * s2;
+    double t[7];
+    e2m1_thresholds(step, t);
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      const uint32_t dm = step > 0.0 ? e2m1_rne_mag_d(fabs(d[j]), step) : 0u;
+      const uint32_t dm = step > 0.0 ? e2m1_rne_mag_bisect(fabs(d[j]), t) : 0u;
       const uint32_t code = dm | ((d[j] < 0.0 && dm != 0u) ? 8u : 0u);
       if (j < 8) r.dlo |= code << (4 * j);
       else r.dhi |= code << (4 * (j - 8));
@@ -514,15 +518,6 @@ __global__ void __launch_bounds__(1024) mxfp4_scale2_kernel(int N, int K, const 
   }
 }
 
-// e2m1 magnitude code of RNE(a / s) like e2m1_rne_mag_d, by bisection over the same seven
-// thresholds (t[i] = midpoint i times s, with its own comparison: > for even i, >= for odd i).
-__device__ __forceinline__ uint32_t e2m1_rne_mag_bisect(double a, const double (&t)[7]) {
-  uint32_t c = a >= t[3] ? 4u : 0u;
-  c += (c ? a >= t[5] : a >= t[1]) ? 2u : 0u;
-  const double u = c == 0u ? t[0] : c == 2u ? t[2] : c == 4u ? t[4] : t[6];
-  return c + (a > u ? 1u : 0u);
-}
-
 // Bit v of the result: some nibble of the 16 in (a, b) has magnitude code v.  A nibble of
 // x = (w & 7 per nibble) ^ v is zero exactly where the code is v; the borrow test
 // (x - 0x1..1) & ~x & 0x8..8 is nonzero iff some nibble of x is zero.
@@ -604,8 +599,8 @@ __global__ void __launch_bounds__(256) requant_mxfp4_kernel(
         }
         const uint32_t ds4 = e4m3_rne_ratio_dd(dmax, sc.d6, sc.i6);
         const double step = (double)e4m3_to_f32(ds4) * sc.s2;
-        const double t[7] = {0.25 * step, 0.75 * step, 1.25 * step, 1.75 * step, 2.5 * step, 3.5 * step,
-                             5.0 * step};
+        double t[7];
+        e2m1_thresholds(step, t);
         uint32_t tlo = 0, thi = 0, flo = 0, fhi = 0;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
