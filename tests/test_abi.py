@@ -61,6 +61,37 @@ def test_host_side_rejections(lib):
     assert lib.moet_moe_forward(1, 128, 128, 8, 2, *fwd_null) == 1                         # nulls
 
 
+def test_host_side_rejections_of_the_load_time_and_cache_calls(lib):
+    """FP8 / MXFP4 requant, the sign-bias probe, the confidence gate and the pooled forward reject
+    bad shapes, null pointers, misaligned buffers and bad codebooks before any CUDA call."""
+    p = ctypes.c_void_p(256)                                                              # aligned dummy
+    q = ctypes.c_void_p(258)                                                              # misaligned
+    for fn in (lib.moet_requant_fp8_2bit, lib.moet_requant_mxfp4_2bit):
+        assert fn(0, 4, 64, p, p, p, p, p, p, None, None, None) == 2                      # M < 1
+        assert fn(1, 4, 48, p, p, p, p, p, p, None, None, None) == 2                      # K % 32
+        assert fn(1, 4, 64, None, p, p, p, p, p, None, None, None) == 1                   # null codes
+        assert fn(1, 4, 64, p, p, p, p, p, p, p, None, None) == 1                         # half a delta
+        assert fn(1, 4, 64, q, p, p, p, p, p, None, None, None) == 3                      # codes not 16 B
+    lv = lambda *v: (ctypes.c_int32 * 4)(*v)
+    probe = lib.moet_sign_bias_probe
+    assert probe(1, 4, 40, p, lv(-2, -1, 0, 1), p, p, None) == 2                          # K % 16
+    assert probe(1, 4, 64, None, lv(-2, -1, 0, 1), p, p, None) == 1                       # null weights
+    assert probe(1, 4, 64, p, lv(-1, -1, 0, 1), p, p, None) == 1                          # not ascending
+    assert probe(1, 4, 64, p, lv(-65, -1, 1, 3), p, p, None) == 1                         # out of range
+    assert probe(1, 4, 64, q, lv(-2, -1, 0, 1), p, p, None) == 3                          # w not 16 B
+    gate = lib.moet_gate_from_confidence
+    assert gate(4, 8, 9, p, 0.6, p, None, p, None, None, None) == 2                       # k > E
+    assert gate(4, 2048, 2, p, 0.6, p, None, p, None, None, None) == 2                    # E > 1024
+    assert gate(4, 8, 2, None, 0.6, p, None, p, None, None, None) == 1                    # null conf
+    assert gate(4, 8, 2, ctypes.c_void_p(257), 0.6, p, None, p, None, None, None) == 3    # conf not 4 B
+    pooled = lib.moet_moe_forward_pooled
+    # fc1, fc2, delta_slot, n_slots, dfc1, dfc2, gate_mask, miss_count, miss_mask, y, workspace, bytes, stream
+    tail = [None, None, None, 0, None, None, None, None, None, None, None, 0, None]
+    assert pooled(1, 128, 128, 8, 2, p, p, p, p, p, None, 4, *tail) == 1                  # null slot table
+    assert pooled(1, 128, 128, 8, 2, p, p, p, p, p, p, 0, *tail) == 2                     # empty pool
+    assert pooled(1, 128, 128, 8, 2, p, p, p, p, p, ctypes.c_void_p(258), 4, *tail) == 3  # slot table not 4 B
+
+
 def test_workspace_size_is_monotone(lib):
     ws = lib.moet_forward_workspace_size
     a = ws(1, 7168, 2048, 256, 8)
