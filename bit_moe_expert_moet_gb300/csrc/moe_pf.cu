@@ -55,12 +55,14 @@ constexpr int kPC = 256;                  // weights per weight chunk
 constexpr int kStepWeights = 64;
 constexpr int kPRing = 3;                 // weight chunks in flight
 constexpr int kBRing = 5;                 // activation steps in flight
-constexpr int kPAst = 8;                  // TMEM A stages (released in pairs)
+constexpr int kPAst = 8;                  // TMEM A stages
+constexpr int kGrp = 4;                   // steps per converter hand-off (one weight chunk)
+constexpr int kNGrp = kPAst / kGrp;       // hand-off groups of A stages in flight
 constexpr int kPMeta = 2;                 // unit records in flight
 constexpr int kPTmemCols = 512;
 constexpr int kPColA = 256;               // D: columns 0..255; A stage s: kPColA + 32 s
 static_assert(kPColA + 32 * kPAst <= kPTmemCols, "TMEM columns");
-static_assert(kPAst % 2 == 0, "the MMA thread takes steps in pairs");
+static_assert(kPAst % kGrp == 0 && (kPC / 64) % kGrp == 0, "hand-off groups tile the A ring and the chunks");
 // weight chunk stage: planes: sign [128 rows][32 B] (SW32) at 0, magnitude at 4096, row scales
 // [128][16 B] at 8192; delta: codes [128][128 B] (SW128) at 0, scales [128][16 B] at 16384
 constexpr int kPChunkBytes = 18432;
@@ -106,8 +108,8 @@ static_assert(sizeof(PfMeta) == 64 + 9 * kPfTok, "PfMeta layout");
 struct PfSmem {
   uint64_t pfull[kPRing], pempty[kPRing];
   uint64_t bfull[kBRing], bdone[kBRing];
-  uint64_t staged[kPAst / 2];     // both A stages of a pair of steps expanded
-  uint64_t adone[kPAst / 2];      // MMAs of a pair of steps done: their A stages are free
+  uint64_t staged[kNGrp];         // the A stages of a group of steps expanded
+  uint64_t adone[kNGrp];          // MMAs of a group of steps done: their A stages are free
   uint64_t acc_full, acc_empty;
   uint64_t meta_full[kPMeta], meta_empty[kPMeta];
   PfMeta meta[kPMeta];
@@ -306,8 +308,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
     sm.stuck = 0;
     for (int s = 0; s < kPRing; ++s) { mbar_init(&sm.pfull[s], 1); mbar_init(&sm.pempty[s], kPfConvWarps); }
     for (int s = 0; s < kBRing; ++s) { mbar_init(&sm.bfull[s], 1); mbar_init(&sm.bdone[s], 1); }
-    for (int s = 0; s < kPAst / 2; ++s) mbar_init(&sm.staged[s], kPfConvWarps);
-    for (int s = 0; s < kPAst / 2; ++s) mbar_init(&sm.adone[s], 1);
+    for (int s = 0; s < kNGrp; ++s) mbar_init(&sm.staged[s], kPfConvWarps);
+    for (int s = 0; s < kNGrp; ++s) mbar_init(&sm.adone[s], 1);
     mbar_init(&sm.acc_full, 1);
     mbar_init(&sm.acc_empty, 4);
     for (int s = 0; s < kPMeta; ++s) { mbar_init(&sm.meta_full[s], 1); mbar_init(&sm.meta_empty[s], 4); }
@@ -399,28 +401,33 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
         asm volatile("tcgen05.fence::after_thread_sync;");
         const int nst = sm.meta[m].nck * (kPC / kStepWeights);
         const uint32_t idesc = f16_idesc<FC1>(sm.meta[m].ncols);   // FC1 bf16, FC2 fp16
-        // two steps per iteration: both A stages expanded, both steps' activations landed
-        for (int st = 0; st < nst; st += 2, gs += 2) {
-          if (!mbar_wait(&sm.staged[(gs >> 1) % (kPAst / 2)], ((gs >> 1) / (kPAst / 2)) & 1) ||
-              !mbar_wait(&sm.bfull[gs % kBRing], (gs / kBRing) & 1) ||
-              !mbar_wait(&sm.bfull[(gs + 1) % kBRing], ((gs + 1) / kBRing) & 1)) {
+        // a group of kGrp steps per iteration: its A stages expanded (one wait), then each
+        // step's activations (one wait per step: the activation ring is shallower than a group
+        // plus the next)
+        for (int st = 0; st < nst && !bad; st += kGrp, gs += kGrp) {
+          const int grp = gs / kGrp;
+          if (!mbar_wait(&sm.staged[grp % kNGrp], (grp / kNGrp) & 1)) {
             bad = true;
             break;
           }
-          asm volatile("tcgen05.fence::after_thread_sync;");
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
+          for (int h = 0; h < kGrp; ++h) {
             const int as = (gs + h) % kPAst, bs = (gs + h) % kBRing;
+            if (!mbar_wait(&sm.bfull[bs], ((gs + h) / kBRing) & 1)) {
+              bad = true;
+              break;
+            }
+            asm volatile("tcgen05.fence::after_thread_sync;");
             const uint32_t bsm = smem_addr(base + kBBase + bs * kBStepBytes);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               mma_ta(tmem, tmem + kPColA + 32 * as + 8 * i, sw128_desc(bsm + 32 * i), idesc,
-                          (st > 0 || h > 0 || i > 0) ? 1u : 0u);
+                     (st > 0 || h > 0 || i > 0) ? 1u : 0u);
+            tc_commit(&sm.bdone[bs]);
+            last = gs + h;
           }
-          tc_commit(&sm.bdone[gs % kBRing]);
-          tc_commit(&sm.bdone[(gs + 1) % kBRing]);
-          tc_commit(&sm.adone[(gs >> 1) % (kPAst / 2)]);
-          last = gs + 1;
+          if (bad) break;
+          tc_commit(&sm.adone[grp % kNGrp]);
         }
         if (bad) break;
         tc_commit(&sm.acc_full);
@@ -575,17 +582,19 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
         const unsigned char* pst = base + kPBase + ps * kPChunkBytes;
         const bool dp = c >= nkc;
         constexpr int kSteps = kPC / kStepWeights;
-        // steps in pairs (the MMA thread consumes them in pairs): one TMEM fence and one arrive per pair
-        for (int s = 0; s < kSteps; s += 2, gs += 2) {
-          // the pair's A stages are free once the MMAs of the pair that used them last are done
-          if (gs >= kPAst) {
-            const int q = (gs - kPAst) >> 1;
-            if (!mbar_wait_warp(&sm.adone[q % (kPAst / 2)], (q / (kPAst / 2)) & 1)) { bad = true; break; }
+        // steps in groups of kGrp (the MMA thread consumes them so): one TMEM fence and one arrive
+        // per group
+        for (int s = 0; s < kSteps; s += kGrp, gs += kGrp) {
+          const int grp = gs / kGrp;
+          // the group's A stages are free once the MMAs of the group that used them last are done
+          if (grp >= kNGrp) {
+            const int q = grp - kNGrp;
+            if (!mbar_wait_warp(&sm.adone[q % kNGrp], (q / kNGrp) & 1)) { bad = true; break; }
           }
           // half h expands 32-weight group 2 (s + h2) + h of step s + h2 (16-bit pairs of weights
           // c and c + 16 per column)
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
+          for (int h2 = 0; h2 < kGrp; ++h2) {
             const int wi = 2 * (s + h2) + half;
             const uint32_t sc = *reinterpret_cast<const uint16_t*>(pst + (dp ? 16384 : 8192) + trow * 16 + 2 * wi);
             const uint32_t s0 = sc & 0xFFu, s1 = sc >> 8;
@@ -605,7 +614,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
           asm volatile("tcgen05.wait::st.sync.aligned;");
           asm volatile("tcgen05.fence::before_thread_sync;");
           __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.staged[(gs >> 1) % (kPAst / 2)]);
+          if (lane == 0) mbar_arrive(&sm.staged[grp % kNGrp]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.pempty[ps]);
