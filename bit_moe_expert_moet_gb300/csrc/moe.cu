@@ -474,10 +474,11 @@ __global__ void __launch_bounds__(kThreads, 2) fc_kernel(const FcArgs a) {
 }
 
 // ---------------------------------------------------------------- combine
-__global__ void __launch_bounds__(kThreads) combine_kernel(int T, int H, int k, const int* __restrict__ hdr,
-                                                           const float* __restrict__ o,
-                                                           const uint8_t* __restrict__ pvalid,
-                                                           uint16_t* __restrict__ y) {
+constexpr int kCombineBatch = 8;                // partial rows in flight per thread
+constexpr int kCombineCtasPerSm = 4;            // guaranteed by the launch bounds: one full wave
+__global__ void __launch_bounds__(kThreads, kCombineCtasPerSm)
+    combine_kernel(int T, int H, int k, const int* __restrict__ hdr, const float* __restrict__ o,
+                   const uint8_t* __restrict__ pvalid, uint16_t* __restrict__ y) {
   const long long n4 = (long long)T * H / 4;
   const bool ok = hdr[1] != 0;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
@@ -485,11 +486,21 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(int T, int H, int k, 
     const long long t = (i * 4) / H, r = (i * 4) % H;
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
     if (ok) {
-      for (int j = 0; j < k; ++j) {
-        // a pair of a non-resident expert (pooled forward) contributes zero; its o row is never written
-        if (pvalid != nullptr && __ldg(pvalid + (size_t)t * k + j) == 0) continue;
-        const float4 v = *reinterpret_cast<const float4*>(o + ((size_t)t * k + j) * H + r);
-        s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+      // the partial rows are loaded kCombineBatch at a time before their adds (the loads
+      // overlap), then summed in pair order; a pair of a non-resident expert (pooled forward) is
+      // skipped: its o row is never written
+      for (int j0 = 0; j0 < k; j0 += kCombineBatch) {
+        float4 v[kCombineBatch];
+        bool use[kCombineBatch];
+#pragma unroll
+        for (int u = 0; u < kCombineBatch; ++u) {
+          const int j = j0 + u;
+          use[u] = j < k && (pvalid == nullptr || __ldg(pvalid + (size_t)t * k + j) != 0);
+          if (use[u]) v[u] = __ldg(reinterpret_cast<const float4*>(o + ((size_t)t * k + j) * H + r));
+        }
+#pragma unroll
+        for (int u = 0; u < kCombineBatch; ++u)
+          if (use[u]) { s.x += v[u].x; s.y += v[u].y; s.z += v[u].z; s.w += v[u].w; }
       }
     }
     const __nv_bfloat162 lo = __floats2bfloat162_rn(s.x, s.y), hi = __floats2bfloat162_rn(s.z, s.w);
@@ -665,8 +676,13 @@ static moet_status forward_impl(int T, int H, int I, int E, int k, const uint16_
   }
 
   long long n4 = (long long)T * H / 4;
-  int gc = (int)((n4 + kThreads - 1) / kThreads);
-  if (gc > 152 * 8) gc = 152 * 8;
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    sms = 152;
+  long long gcl = (n4 + kThreads - 1) / kThreads;
+  if (gcl > (long long)sms * kCombineCtasPerSm) gcl = (long long)sms * kCombineCtasPerSm;
+  const int gc = (int)gcl;
   {
     ProfScope ps(MOET_K_COMBINE, st);
     combine_kernel<<<gc, kThreads, 0, st>>>(T, H, k, hdr, o, pvalid, y);
