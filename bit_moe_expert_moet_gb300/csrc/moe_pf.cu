@@ -204,21 +204,36 @@ __device__ __forceinline__ void delta_to_16(uint4 c, uint32_t s0, uint32_t s1, u
 }
 
 // ---------------------------------------------------------------- gather
+// Whether the delta pass can read the gated-copy row of pair p: its expert holds a delta slot.
+// Rows of the other pairs are never read, so the gated copies skip them.
+__device__ __forceinline__ bool pair_in_delta_pass(int p, const int32_t* __restrict__ topk_idx, int n_experts,
+                                                   const int32_t* __restrict__ delta_slot, int n_slots) {
+  const int e = __ldg(topk_idx + p);
+  if (e < 0 || e >= n_experts) return false;
+  const int ds = __ldg(delta_slot + e);
+  return ds >= 0 && ds < n_slots;
+}
+
 // xb[pos] = x[token of perm[pos]] in the permuted K order; xbg the same for
-// gated pairs, zero for the others.  Grid (pairs, ceil(H / 8 / 128)).
+// gated pairs, zero for the others (written for the delta pass's pairs only:
+// xbg == null or delta_slot == null writes none).  Grid (pairs, ceil(H / 8 / 128)).
 __global__ void __launch_bounds__(128) pf_gather_kernel(int pairs, int k, int H, const uint16_t* __restrict__ x,
                                                         const int32_t* __restrict__ perm,
-                                                        const uint8_t* __restrict__ gate, uint16_t* __restrict__ xb,
-                                                        uint16_t* __restrict__ xbg) {
+                                                        const uint8_t* __restrict__ gate,
+                                                        const int32_t* __restrict__ topk_idx, int n_experts,
+                                                        const int32_t* __restrict__ delta_slot, int n_slots,
+                                                        uint16_t* __restrict__ xb, uint16_t* __restrict__ xbg) {
   const int pos = blockIdx.x;
   const int t = blockIdx.y * 128 + threadIdx.x;              // 8 outputs: k' = 8 t .. 8 t + 7
   if (t >= H / 8) return;
   const int p = __ldg(perm + pos);
   uint4 v = make_uint4(0u, 0u, 0u, 0u);
-  bool gated = false;
+  bool gated = false, in_delta = false;
   if (p >= 0 && p < pairs) {
     const int tok = p / k;
     gated = gate != nullptr && __ldg(gate + tok) != 0;
+    in_delta = xbg != nullptr && delta_slot != nullptr &&
+               pair_in_delta_pass(p, topk_idx, n_experts, delta_slot, n_slots);
     // k' = 32 g + 2 c + b holds weight 32 g + c + 16 b; this thread covers c = 4 q .. 4 q + 3
     const int g = t >> 2, q = t & 3;
     const uint16_t* row = x + (size_t)tok * H + 32 * g + 4 * q;
@@ -232,16 +247,20 @@ __global__ void __launch_bounds__(128) pf_gather_kernel(int pairs, int k, int H,
     record_error(MOET_ERR_DEVICE_INDEX);
   }
   reinterpret_cast<uint4*>(xb + (size_t)pos * H)[t] = v;
-  if (xbg != nullptr) reinterpret_cast<uint4*>(xbg + (size_t)pos * H)[t] = gated ? v : make_uint4(0u, 0u, 0u, 0u);
+  if (in_delta) reinterpret_cast<uint4*>(xbg + (size_t)pos * H)[t] = gated ? v : make_uint4(0u, 0u, 0u, 0u);
 }
 
 // FC1's fp32 h (bucketed rows, natural K order) -> FC2's fp16 operand in the permuted K order
 // (as xb), each row times the power of two 2^-e that puts its max |h| in [2^14, 2^15), and
-// hscale[pos] = 2^e; hg16 the same for gated pairs, zero for the others.  One CTA per row.
+// hscale[pos] = 2^e; hg16 the same for gated pairs, zero for the others (for the delta pass's
+// pairs only, as xbg).  One CTA per row.
 __global__ void __launch_bounds__(256) pf_h16_kernel(int pairs, int k, int I, const float* __restrict__ h,
                                                      const int32_t* __restrict__ perm,
-                                                     const uint8_t* __restrict__ gate, uint16_t* __restrict__ h16,
-                                                     uint16_t* __restrict__ hg16, float* __restrict__ hscale) {
+                                                     const uint8_t* __restrict__ gate,
+                                                     const int32_t* __restrict__ topk_idx, int n_experts,
+                                                     const int32_t* __restrict__ delta_slot, int n_slots,
+                                                     uint16_t* __restrict__ h16, uint16_t* __restrict__ hg16,
+                                                     float* __restrict__ hscale) {
   const int pos = blockIdx.x;
   const float* row = h + (size_t)pos * I;
   __shared__ float red[8];
@@ -266,9 +285,11 @@ __global__ void __launch_bounds__(256) pf_h16_kernel(int pairs, int k, int I, co
   }
   const float down = ldexpf(1.0f, -e);
   const int p = __ldg(perm + pos);
-  bool gated = false;
+  bool gated = false, in_delta = false;
   if (p >= 0 && p < pairs) {
     gated = gate != nullptr && __ldg(gate + p / k) != 0;
+    in_delta = hg16 != nullptr && delta_slot != nullptr &&
+               pair_in_delta_pass(p, topk_idx, n_experts, delta_slot, n_slots);
   } else if (threadIdx.x == 0) {
     record_error(MOET_ERR_DEVICE_INDEX);
   }
@@ -287,7 +308,7 @@ __global__ void __launch_bounds__(256) pf_h16_kernel(int pairs, int k, int I, co
               ((uint32_t)__half_as_ushort(__float2half_rn(b[i] * down)) << 16);
     const uint4 v = make_uint4(wv[0], wv[1], wv[2], wv[3]);
     reinterpret_cast<uint4*>(h16 + (size_t)pos * I)[t] = v;
-    if (hg16 != nullptr) reinterpret_cast<uint4*>(hg16 + (size_t)pos * I)[t] = gated ? v : make_uint4(0u, 0u, 0u, 0u);
+    if (in_delta) reinterpret_cast<uint4*>(hg16 + (size_t)pos * I)[t] = gated ? v : make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
@@ -671,7 +692,8 @@ moet_status pf_forward(const PfForwardArgs& f, cudaStream_t st) {
   {
     ProfScope ps(MOET_K_TERMS, st);
     const dim3 grid(pairs, (f.H / 8 + 127) / 128);
-    pf_gather_kernel<<<grid, 128, 0, st>>>(pairs, f.k, f.H, f.x, f.perm, with_delta ? f.gate : nullptr, f.xb,
+    pf_gather_kernel<<<grid, 128, 0, st>>>(pairs, f.k, f.H, f.x, f.perm, with_delta ? f.gate : nullptr, f.topk_idx,
+                                           f.n_experts, with_delta ? f.delta_slot : nullptr, f.n_slots, f.xb,
                                            with_delta ? f.xbg : nullptr);
   }
   MOET_CUDA_TRY(cudaGetLastError());
@@ -689,7 +711,8 @@ moet_status pf_forward(const PfForwardArgs& f, cudaStream_t st) {
   if (s != MOET_OK) return s;
   {
     ProfScope ps(MOET_K_TERMS, st);
-    pf_h16_kernel<<<pairs, 256, 0, st>>>(pairs, f.k, f.I, f.h, f.perm, with_delta ? f.gate : nullptr, f.h16,
+    pf_h16_kernel<<<pairs, 256, 0, st>>>(pairs, f.k, f.I, f.h, f.perm, with_delta ? f.gate : nullptr, f.topk_idx,
+                                         f.n_experts, with_delta ? f.delta_slot : nullptr, f.n_slots, f.h16,
                                          with_delta ? f.hg16 : nullptr, f.hscale);
   }
   MOET_CUDA_TRY(cudaGetLastError());
