@@ -25,7 +25,8 @@ Modules
   signbias the sign-bias probe (per-block L2-optimal fits to a 4-level codebook)
 
 Every function here is pinned by a ``-m "not gpu"`` test in ``tests/`` to
-something other than itself (brute force, closed forms, invariants or a
-hand-worked example); the one exception is stated in ``moe.py``.
+something other than itself (brute force, closed forms, invariants, exact
+rational arithmetic or a hand-worked example).  Agreement with the pages' own
+outputs is unpinned: the pages print no tensors or layer outputs.
 """
 from . import formats, nvfp4, requant, route, moe, gate, signbias  # noqa: F401
