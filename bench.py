@@ -13,7 +13,12 @@ from the same steps launched call by call with the library's event profiler.
 The end-to-end number replays a graph of the step plus the host copies of its
 inputs (pinned) and its output.  The load-time requantisation is timed
 separately over the full NVFP4 expert set of the 1T-class layer (768
-matrices) and reported under "requant".
+matrices) and reported under "requant".  Other extras on the same line: the
+T=1 / T=8 / prefill / GLM worst-case / 1T-class layers ("decode_sweep"), the
+forward through the expert-cache slot table ("pooled"), the FP8 and MXFP4
+requantisations and the sign-bias probe over 16 FC1-shaped matrices
+("requant_fp8", "requant_mxfp4", "sign_bias"); --extras picks a subset and
+--requant-experts shrinks the requant set (profiler captures).
 
 Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle
 instead, on a bounded sample of the same workload.
