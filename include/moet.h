@@ -290,7 +290,7 @@ moet_status moet_moe_forward_pooled(int T, int H, int I, int E, int k, const uin
  *  - Returns MOET_ERR_WORKSPACE, enqueueing nothing, when the layer needs
  *    more scratch than that (moet_forward_workspace_size(T,H,I,E,k) >
  *    MOET_FORWARD_STATIC_SCRATCH_BYTES); e.g. H=7168, I=2048, E=256, k=8 fits
- *    up to T=21 tokens.
+ *    up to T=13 tokens.
  *  - The first call on a device (with that device current) looks the array's
  *    device address up with cudaGetSymbolAddress; make it before any stream
  *    capture.

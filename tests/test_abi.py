@@ -92,6 +92,18 @@ def test_host_side_rejections_of_the_load_time_and_cache_calls(lib):
     assert pooled(1, 128, 128, 8, 2, p, p, p, p, p, ctypes.c_void_p(258), 4, *tail) == 3  # slot table not 4 B
 
 
+def test_static_forward_rejects_layers_larger_than_its_scratch(lib):
+    """moet_moe_forward_static checks the layer against its fixed 8 MiB scratch before any CUDA
+    call: the DeepSeek-V3 decode layer fits up to T = 13 tokens (as the header states) and is
+    rejected beyond."""
+    import bit_moe_expert_moet_gb300 as m
+    ws = lib.moet_forward_workspace_size
+    assert ws(13, 7168, 2048, 256, 8) <= m.FORWARD_STATIC_SCRATCH_BYTES < ws(14, 7168, 2048, 256, 8)
+    nulls = [None] * 5 + [None, None, None, 0, None, None, None, None, None]
+    assert lib.moet_moe_forward_static(14, 7168, 2048, 256, 8, *nulls) == 5               # WORKSPACE
+    assert lib.moet_moe_forward_static(0, 7168, 2048, 256, 8, *nulls) == 2                # SHAPE
+
+
 def test_workspace_size_is_monotone(lib):
     ws = lib.moet_forward_workspace_size
     a = ws(1, 7168, 2048, 256, 8)
