@@ -50,7 +50,7 @@ typedef enum {
   MOET_ERR_INVALID_ARG = 1, /* null pointer where one is required, bad enum/size      */
   MOET_ERR_SHAPE = 2,       /* a dimension violates the stated divisibility or range  */
   MOET_ERR_ALIGN = 3,       /* a pointer is not aligned as the entry point requires   */
-  MOET_ERR_UNSUPPORTED = 4, /* shape valid in principle but not handled by this build */
+  MOET_ERR_UNSUPPORTED = 4, /* shape valid in principle but not handled by the library  */
   MOET_ERR_WORKSPACE = 5,   /* workspace missing or smaller than the size query       */
   MOET_ERR_CUDA = 6,        /* a CUDA runtime call or kernel launch failed            */
   MOET_ERR_TIMEOUT = 7,     /* a bounded device wait expired (device flag)            */
