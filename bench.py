@@ -11,14 +11,16 @@ flushed (512 MB memset) before every step and each step is timed alone with
 CUDA events on the launching stream.  Per-kernel durations (the roofline) come
 from the same steps launched call by call with the library's event profiler.
 The end-to-end number replays a graph of the step plus the host copies of its
-inputs (pinned) and its output.  The load-time requantisation is timed
-separately over the full NVFP4 expert set of the 1T-class layer (768
-matrices) and reported under "requant".  Other extras on the same line: the
-T=1 / T=8 / prefill / GLM worst-case / 1T-class layers ("decode_sweep"), the
-forward through the expert-cache slot table ("pooled"), the FP8 and MXFP4
-requantisations and the sign-bias probe over 16 FC1-shaped matrices
-("requant_fp8", "requant_mxfp4", "sign_bias"); --extras picks a subset and
---requant-experts shrinks the requant set (profiler captures).
+inputs (pinned) and its output.  Every layer configuration (T=1 / 8 / 64,
+prefill, GLM worst case, 1T-class) gets a compact record under "configs" at the
+end of the line: tokens/s of the step and end to end, FC1 / FC2 time per step
+and the roofline fractions.  The load-time requantisation is timed over the
+full NVFP4 expert set of the 1T-class layer (768 matrices), planes only and
+with the delta ("requant").  Other extras: the forward through the expert-cache
+slot table ("pooled"), the FP8 and MXFP4 requantisations and the sign-bias
+probe over 16 FC1-shaped matrices ("requant_fp8", "requant_mxfp4",
+"sign_bias"); --extras picks a subset and --requant-experts shrinks the
+requant set (profiler captures).
 
 Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle
 instead, on a bounded sample of the same workload.
@@ -269,15 +271,18 @@ def step_bytes(cfg, idx, gate, slot):
         + 8 * len(used) + 2 * T * H + 2 * T * H + 4 * T * E
     fc1 = len(used) * w1 * (2 / 8 + 1 / 16) + len(delta_used) * w1 * (4 / 8 + 1 / 16) \
         + 4 * len(used) + 2 * T * H + 4 * T * k * I
-    return total, fc1, len(used), len(delta_used)
+    w2 = H * I
+    fc2 = len(used) * w2 * (2 / 8 + 1 / 16) + len(delta_used) * w2 * (4 / 8 + 1 / 16) \
+        + 4 * len(used) + 4 * T * k * I + 4 * T * k * H
+    return total, fc1, fc2, len(used), len(delta_used)
 
 
-def fc1_flops(cfg, idx, gate, slot):
-    """Algorithmic FLOPs of the FC1 launch: 2 (2I) H per routed pair, again for every pair whose
-    token is gated and whose expert has a cached delta (the delta pass)."""
+def fc_flops(cfg, idx, gate, slot):
+    """Algorithmic FLOPs of FC1 and FC2: 2 (2I) H and 2 H I per routed pair, again for every pair
+    whose token is gated and whose expert has a cached delta (the delta pass)."""
     pairs = cfg.T * cfg.k
     dpairs = sum(1 for t in range(cfg.T) if gate[t] for e in idx[t] if slot[e] >= 0)
-    return 2.0 * (2 * cfg.I) * cfg.H * (pairs + dpairs)
+    return 2.0 * (2 * cfg.I) * cfg.H * (pairs + dpairs), 2.0 * cfg.H * cfg.I * (pairs + dpairs)
 
 
 def bf16_peak():
@@ -291,6 +296,36 @@ def bf16_peak():
         except Exception:
             pass
     return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def _r(v, sig=4):
+    """v rounded to `sig` significant digits (keeps the one-line record short)."""
+    if v is None or not isinstance(v, (int, float)) or v == 0 or not math.isfinite(v):
+        return v
+    return float(f"{v:.{sig}g}")
+
+
+def config_summary(l, step_ms, e2e_ms, prof, nsteps, peak):
+    """Compact record of one layer configuration: tokens/s of the graph-replayed step and of the
+    end-to-end step (host copies inside), per-step FC1 / FC2 kernel time from the event profiler
+    (all launches of a kind in a step summed), and the roofline fractions: HBM (algorithmic bytes
+    over the copy peak) for decode, bf16 tensor (useful FLOPs over the bf16 peak) for prefill."""
+    c = l.cfg
+    f1 = prof["fc1"][2] / nsteps
+    f2 = prof["fc2"][2] / nsteps
+    out = {"T": c.T, "tok_s": _r(c.T / (step_ms * 1e-3)), "e2e_tok_s": _r(c.T / (e2e_ms * 1e-3)),
+           "step_ms": _r(step_ms), "fc1_ms": _r(f1), "fc2_ms": _r(f2)}
+    if c.T > PREFILL_MIN_T:
+        tpk, _ = bf16_peak()
+        tf = 6.0 * c.H * c.I * c.T * c.k / (step_ms * 1e-3) / 1e12
+        out.update({"tflops": _r(tf), "frac_bf16": _r(tf / tpk),
+                    "fc1_frac_bf16": _r(l.flops_fc1 / (f1 * 1e-3) / 1e12 / tpk),
+                    "fc2_frac_bf16": _r(l.flops_fc2 / (f2 * 1e-3) / 1e12 / tpk)})
+    else:
+        out.update({"step_frac_hbm": _r(l.bytes_total / (step_ms * 1e-3) / 1e9 / peak),
+                    "fc1_frac_hbm": _r(l.bytes_fc1 / (f1 * 1e-3) / 1e9 / peak),
+                    "fc2_frac_hbm": _r(l.bytes_fc2 / (f2 * 1e-3) / 1e9 / peak)})
+    return out
 
 
 class Layer:
@@ -335,9 +370,10 @@ class Layer:
         self.step()
         t.cuda.synchronize(dev)
         self.idx_np = self.idx.cpu().numpy()
-        self.bytes_total, self.bytes_fc1, self.n_used, self.n_delta = step_bytes(
+        self.bytes_total, self.bytes_fc1, self.bytes_fc2, self.n_used, self.n_delta = step_bytes(
             cfg, self.idx_np, gate, self.slot_np)
-        self.flops_fc1 = fc1_flops(cfg, self.idx_np, gate, self.slot_np) if cfg.T > PREFILL_MIN_T else 0.0
+        gate_eff = gate if self.use_delta else np.zeros_like(gate)
+        self.flops_fc1, self.flops_fc2 = fc_flops(cfg, self.idx_np, gate_eff, self.slot_np)
 
     def step(self):
         m = self.moet
@@ -421,9 +457,8 @@ def time_requant_fp8(moet, torch, dev, steps=3, n_mat=16):
     ms = statistics.median(ts)
     weights = n_mat * N * K
     moved = weights * (1 + 0.3125 + 0.5625)
-    return {"matrices": n_mat, "shape": [N, K], "weights": weights, "ms_per_pass": ms,
-            "gweights_per_s": weights / (ms * 1e-3) / 1e9, "gbs": moved / (ms * 1e-3) / 1e9,
-            "bound": "fp64 ALU (exact ratio rounding in fp64)"}
+    return {"matrices": n_mat, "ms": _r(ms), "gw_s": _r(weights / (ms * 1e-3) / 1e9),
+            "gbs": _r(moved / (ms * 1e-3) / 1e9)}
 
 
 def time_requant_mxfp4(moet, torch, dev, steps=3, n_mat=16):
@@ -450,9 +485,8 @@ def time_requant_mxfp4(moet, torch, dev, steps=3, n_mat=16):
     ms = statistics.median(ts)
     weights = n_mat * N * K
     moved = weights * (0.5 + 1 / 32 + 0.3125 + 0.5625)
-    return {"matrices": n_mat, "shape": [N, K], "weights": weights, "ms_per_pass": ms,
-            "gweights_per_s": weights / (ms * 1e-3) / 1e9, "gbs": moved / (ms * 1e-3) / 1e9,
-            "bound": "fp64 ALU (exact ratio rounding in fp64)"}
+    return {"matrices": n_mat, "ms": _r(ms), "gw_s": _r(weights / (ms * 1e-3) / 1e9),
+            "gbs": _r(moved / (ms * 1e-3) / 1e9)}
 
 
 def time_sign_bias_probe(moet, torch, dev, steps=3, n_mat=16):
@@ -466,8 +500,7 @@ def time_sign_bias_probe(moet, torch, dev, steps=3, n_mat=16):
     rows = torch.empty((n_mat, N, 4), dtype=torch.float64, device=dev)
     sums = torch.empty((n_mat, 4), dtype=torch.float64, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    out = {"matrices": n_mat, "shape": [N, K], "weights": n_mat * N * K,
-           "bound": "alu (fp32 search over 969 assignments per 16 weights)"}
+    out = {"matrices": n_mat}
     for name, levels in (("int2", (-2, -1, 0, 1)), ("sym13", (-3, -1, 1, 3)), ("sym14", (-4, -1, 1, 4))):
         ts = time_steps(torch, lambda: moet.sign_bias_probe(w, levels, rows, sums), steps, 1, flush)
         s = sums.cpu().numpy()
@@ -475,24 +508,23 @@ def time_sign_bias_probe(moet, torch, dev, steps=3, n_mat=16):
         rms = np.sqrt(s[:, 1] / n)
         bias = s[:, 2] / n / rms
         rel = np.sqrt(s[:, 3] / s[:, 1])
-        out[name] = {"levels": list(levels), "ms_per_pass": statistics.median(ts),
-                     "gweights_per_s": n_mat * n / (statistics.median(ts) * 1e-3) / 1e9,
-                     "bias_mean": float(bias.mean()), "bias_negative_share": float((bias < 0).mean()),
-                     "rel_rms_mean": float(rel.mean())}
-    out["bias_ratio_int2_over_sym13"] = abs(out["int2"]["bias_mean"]) / max(abs(out["sym13"]["bias_mean"]), 1e-300)
+        out[name] = {"ms": _r(statistics.median(ts)), "bias": _r(float(bias.mean()), 3),
+                     "neg": _r(float((bias < 0).mean()), 3), "rel_rms": _r(float(rel.mean()), 3)}
+    out["int2_over_sym13"] = _r(abs(out["int2"]["bias"]) / max(abs(out["sym13"]["bias"]), 1e-300), 3)
     del w, rows, flush
     torch.cuda.empty_cache()
     return out
 
 
-def time_requant(moet, torch, dev, steps=3, n_experts=0):
-    """moet_requant_2bit over the full NVFP4 expert set of the 1T-class layer (768 matrices), or over
-    its first n_experts experts."""
+def time_requant(moet, torch, dev, peak, steps=3, n_experts=0):
+    """moet_requant_2bit over the full NVFP4 expert set of the 1T-class layer (768 matrices, or the
+    first n_experts experts' matrices): one pass writing the planes only, one pass writing the
+    planes and the NVFP4 delta (what filling the delta cache costs).  Bytes moved per pass are the
+    tensors read and written; the fraction is of the copy peak."""
     cfg = W.CONFIGS["kimi_layer"]
     gen = torch.Generator(device=dev)
     gen.manual_seed(99)
     E, H, I = (n_experts or cfg.E), cfg.H, cfg.I
-    results = {}
     bufs = {}
     for f, (N, K) in ((1, (2 * I, H)), (2, (H, I))):
         codes = torch.empty((E, N, K // 2), dtype=torch.uint8, device=dev)
@@ -506,32 +538,28 @@ def time_requant(moet, torch, dev, steps=3, n_experts=0):
         sign = torch.empty((E, N, K // 32), dtype=torch.int32, device=dev)
         mag = torch.empty_like(sign)
         s16 = torch.empty((E, N, K // 16), dtype=torch.uint8, device=dev)
-        bufs[f] = (codes, s4, sign, mag, s16)
+        dcodes = torch.empty_like(codes)
+        ds4 = torch.empty_like(s4)
+        bufs[f] = (codes, s4, sign, mag, s16, dcodes, ds4)
     torch.cuda.synchronize()
-
-    def run():
-        for f in (1, 2):
-            codes, s4, sign, mag, s16 = bufs[f]
-            moet.requant_2bit(codes, s4, sign, mag, s16)
-
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    moet.profile_read()
-    moet.profile_enable(True)
-    ts = time_steps(torch, run, steps, 1, flush)
-    moet.profile_enable(False)
-    prof = moet.profile_read()
-    nbytes = 0
-    for f in (1, 2):
-        for t in bufs[f]:
-            nbytes += t.numel() * t.element_size()
-    lau, timed, ms = prof["requant"]
-    per_launch_ms = ms / max(timed, 1)
-    results = {"matrices": 2 * E, "weights": 3 * H * I * E, "bytes_per_pass": nbytes,
-               "ms_per_pass": statistics.median(ts), "gbs": nbytes / (statistics.median(ts) * 1e-3) / 1e9,
-               "kernel_ms_per_launch": per_launch_ms, "launches_per_pass": 2}
+    out = {"matrices": 2 * E, "weights": 3 * H * I * E}
+    for name, with_delta in (("planes", False), ("delta", True)):
+        def run():
+            for f in (1, 2):
+                codes, s4, sign, mag, s16, dcodes, ds4 = bufs[f]
+                if with_delta:
+                    moet.requant_2bit(codes, s4, sign, mag, s16, dcodes, ds4)
+                else:
+                    moet.requant_2bit(codes, s4, sign, mag, s16)
+        ts = time_steps(torch, run, steps, 1, flush)
+        nbytes = sum(t.numel() * t.element_size() for f in (1, 2) for t in bufs[f][:5 + 2 * with_delta])
+        ms = statistics.median(ts)
+        out[name] = {"ms": _r(ms), "gbs": _r(nbytes / (ms * 1e-3) / 1e9), "frac_hbm": _r(nbytes / (ms * 1e-3) / 1e9 / peak),
+                     "bytes": nbytes}
     del bufs, flush
     torch.cuda.empty_cache()
-    return results
+    return out
 
 
 # ------------------------------------------------------------------ CPU oracle timing
@@ -561,8 +589,7 @@ def oracle_sample(cfg, n_pairs=1, seed=7):
     wts = ow[:, :n_pairs]
     omoe.moe_forward(x, idx, wts, fc1, fc2)
     dt = time.perf_counter() - t0
-    desc = (f"oracle route of all {cfg.T}x{E} logits + forward of {n_pairs} of token 0's {k} "
-            f"(token, expert) pairs = {n_pairs / k:.3f} token of {cfg.name}")
+    desc = f"route of all {cfg.T} tokens + forward of {n_pairs} (token, expert) pair = {n_pairs / k:.3f} token"
     return n_pairs / k, dt, desc
 
 
@@ -652,50 +679,40 @@ def run_ours(args, rank, world, local):
     launches_timed = total_launches * args.steps // (args.steps + args.warmup)
 
     extras = {}
+    configs = {}
+    if rank == 0:
+        configs[cfg.name] = config_summary(layer, statistics.median(ts), statistics.median(ts_e2e), prof,
+                                           args.steps + args.warmup, peak)
     if not args.no_extras and rank == 0:
-        sweep = {}
-
         def timed(l2, steps, warmup):
             g2 = capture_graph(torch, l2.step)
             t2 = time_steps(torch, g2.replay, steps, warmup, flush)
             del g2
+            g3 = capture_graph(torch, l2.step_e2e)
+            t3 = time_steps(torch, g3.replay, steps, warmup, flush)
+            del g3
             moet.profile_read()
             moet.profile_enable(True)
             time_steps(torch, l2.step, steps, warmup, flush)
             moet.profile_enable(False)
             p2 = moet.profile_read()
-            med = statistics.median(t2)
-            f2 = p2["fc1"][2] / max(p2["fc1"][1], 1)
-            return {"T": l2.cfg.T, "tokens_per_s": l2.cfg.T / (med * 1e-3), "ms_per_step_median": med,
-                    "step_gbs": l2.bytes_total / (med * 1e-3) / 1e9,
-                    "step_frac_of_hbm": l2.bytes_total / (med * 1e-3) / 1e9 / peak,
-                    "fc1_gbs": l2.bytes_fc1 / (f2 * 1e-3) / 1e9,
-                    "fc1_frac_of_hbm": l2.bytes_fc1 / (f2 * 1e-3) / 1e9 / peak,
-                    "fc1_launch_ms": f2, "experts_touched": l2.n_used, "delta_experts_touched": l2.n_delta,
-                    "kernel_ms_per_launch": {k: v[2] / max(v[1], 1) for k, v in p2.items() if v[0]}}
+            return config_summary(l2, statistics.median(t2), statistics.median(t3), p2, steps + warmup, peak)
 
         for name in (("dsv3_decode_t1", "dsv3_decode_t8", "dsv3_prefill") if "sweep" in args.extras else ()):
             c2 = W.CONFIGS[name]
             if name == cfg.name or (c2.H, c2.I, c2.E) != (cfg.H, cfg.I, cfg.E):
                 continue
             l2 = layer.rebatch(c2)
-            r = timed(l2, args.steps if c2.T <= 512 else 3, args.warmup if c2.T <= 512 else 1)
-            if c2.T > 512:   # prefill: tensor work 6 H I flops per routed pair
-                flops = 6.0 * c2.H * c2.I * c2.T * c2.k
-                r["tflops"] = flops / (r["ms_per_step_median"] * 1e-3) / 1e12
-                tpk, _ = bf16_peak()
-                r["frac_of_bf16_peak"] = r["tflops"] / tpk
-                r["frac_of_fp8_peak"] = r["tflops"] / (2.0 * tpk)
-            sweep[name] = r
+            configs[name] = timed(l2, args.steps if c2.T <= 512 else 5, args.warmup if c2.T <= 512 else 3)
             del l2
         for name in (("glm_decode", "kimi_layer") if "sweep" in args.extras else ()):
+            if name == cfg.name:
+                continue
             c3 = W.CONFIGS[name]
             l3 = Layer(moet, torch, c3, dev)
-            sweep[name] = timed(l3, args.steps, args.warmup)
+            configs[name] = timed(l3, args.steps, args.warmup)
             del l3
             torch.cuda.empty_cache()
-        if sweep:
-            extras["decode_sweep"] = sweep
 
         if "pooled" in args.extras:
             # expert cache: the headline layer through the slot table with every 10th expert not
@@ -718,19 +735,20 @@ def run_ours(args, rank, world, local):
             tp = time_steps(torch, gp_.replay, args.steps, args.warmup, flush)
             med = statistics.median(tp)
             n_replays = args.steps + args.warmup
-            extras["pooled"] = {"workload": cfg.name, "resident_experts": int((slot_np >= 0).sum()),
-                                "missed_pairs_per_step": int(miss.item()) / n_replays,
-                                "tokens_per_s": cfg.T / (med * 1e-3), "ms_per_step_median": med}
+            extras["pooled"] = {"resident": int((slot_np >= 0).sum()),
+                                "missed_pairs": int(miss.item()) / n_replays,
+                                "tok_s": _r(cfg.T / (med * 1e-3)), "step_ms": _r(med)}
             del gp_
         if "requant" in args.extras:
-            extras["requant"] = time_requant(moet, torch, dev, n_experts=args.requant_experts)
-            extras["requant"]["frac_of_hbm_peak"] = extras["requant"]["gbs"] / peak
+            extras["requant"] = time_requant(moet, torch, dev, peak, n_experts=args.requant_experts)
         if "requant_fp8" in args.extras:
             extras["requant_fp8"] = time_requant_fp8(moet, torch, dev)
         if "requant_mxfp4" in args.extras:
             extras["requant_mxfp4"] = time_requant_mxfp4(moet, torch, dev)
         if "sign_bias" in args.extras:
             extras["sign_bias"] = time_sign_bias_probe(moet, torch, dev)
+    if configs:
+        extras["configs"] = configs           # last: the most-read records sit at the end of the line
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -739,22 +757,25 @@ def run_ours(args, rank, world, local):
 
     if rank != 0:
         return
-    kernel_ms = {k: (v[2] / max(v[1], 1)) for k, v in prof.items() if v[0]}
     if cfg.T > PREFILL_MIN_T:
-        # prefill regime: FC1 is a dense bf16 contraction on the tensor cores
+        # prefill regime: FC1 is a dense contraction on the tensor cores (useful FLOPs per step over
+        # FC1's summed launch time in the step)
         tpk, tpk_kind = bf16_peak()
-        tach = layer.flops_fc1 / (fc1_ms * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "kernel": "pf_fc_kernel<FC1>", "achieved": tach, "peak": tpk,
-                    "peak_source": tpk_kind, "unit": "TFLOP/s", "frac": tach / tpk, "traffic": None,
-                    "algorithmic_flops_per_launch": layer.flops_fc1, "launch_ms": fc1_ms,
-                    "frac_of_fp8_peak": tach / (2.0 * tpk)}   # fp8 dense = 2x bf16 (nominal ratio)
-        dtype = "bf16 (FC1) / fp16 with per-row power-of-two scaling of h (FC2) mma on exactly expanded 2-bit weights, fp32 accumulate"
+        f1_step = prof["fc1"][2] / (args.steps + args.warmup)
+        tach = layer.flops_fc1 / (f1_step * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "kernel": "FC1 (pf_fc_kernel<FC1> + fc_tc_kernel<FC1>)", "achieved": _r(tach),
+                    "peak": tpk, "peak_source": tpk_kind, "unit": "TFLOP/s", "frac": _r(tach / tpk), "traffic": None,
+                    "flops": layer.flops_fc1, "ms": _r(f1_step), "frac_fp8": _r(tach / (2.0 * tpk))}
+        dtype = "bf16/fp16 tcgen05 on exact 2-bit weights (+ nvfp4 block-scaled for small items), fp32 acc"
     else:
-        roofline = {"bound": "hbm", "kernel": "fc_tc_kernel<FC1>", "achieved": achieved, "peak": peak,
-                    "peak_source": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                    "traffic": fc1_traffic(cfg.name), "algorithmic_bytes_per_launch": layer.bytes_fc1,
-                    "launch_ms": fc1_ms, "frac_of_nominal_8tbs": achieved / 8000.0}
-        dtype = "nvfp4 block-scaled mma (2-bit levels as e2m1, activations as 4 nvfp4 terms), fp32 accumulate"
+        tr = fc1_traffic(cfg.name)
+        roofline = {"bound": "hbm", "kernel": "fc_tc_kernel<FC1>", "achieved": _r(achieved), "peak": peak,
+                    "peak_source": peak_kind, "unit": "GB/s", "frac": _r(achieved / peak), "traffic": tr,
+                    "traffic_source": "profiles/fc1_traffic.txt (ncu, same kernel source sha256)" if tr else None,
+                    "bytes": layer.bytes_fc1, "ms": _r(fc1_ms), "frac_8tbs": _r(achieved / 8000.0)}
+        dtype = "nvfp4 block-scaled tcgen05 (2-bit levels as e2m1, activations as 4 nvfp4 terms), fp32 acc"
+    if cpu is not None:
+        cpu["value"] = _r(cpu["value"])
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -762,13 +783,9 @@ def run_ours(args, rank, world, local):
         "data": "synthetic",
         "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "k": cfg.k,
                    "delta_experts": int((layer.slot_np >= 0).sum()), "gate": cfg.gate,
-                   "experts_touched": layer.n_used, "delta_experts_touched": layer.n_delta,
-                   "l2": "flushed before every step (512 MB memset, outside the events)",
-                   "parallelism": f"replicas x{world}"},
-        "step_gbs": layer.bytes_total / (ms_step * 1e-3) / 1e9,
-        "step_frac_of_hbm": layer.bytes_total / (ms_step * 1e-3) / 1e9 / peak,
+                   "l2": "flushed before each step", "parallelism": f"replicas x{world}"},
+        "step_frac_hbm": _r(layer.bytes_total / (ms_step * 1e-3) / 1e9 / peak),
         "roofline": roofline,
-        "kernel_ms_per_launch": kernel_ms,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": layer.h2d_bytes,
                 "d2h_bytes_per_step": layer.d2h_bytes},
@@ -776,7 +793,7 @@ def run_ours(args, rank, world, local):
         "gpu_launches": launches_timed,
         "device_error": err,
     }
-    line.update(extras)
+    line.update(extras)            # per-config records ("configs") come last
     print(json.dumps(line), flush=True)
 
 

@@ -291,9 +291,13 @@ moet_status moet_moe_forward_pooled(int T, int H, int I, int E, int k, const uin
  *    more scratch than that (moet_forward_workspace_size(T,H,I,E,k) >
  *    MOET_FORWARD_STATIC_SCRATCH_BYTES); e.g. H=7168, I=2048, E=256, k=8 fits
  *    up to T=13 tokens.
- *  - The first call on a device (with that device current) looks the array's
- *    device address up with cudaGetSymbolAddress; make it before any stream
- *    capture.
+ *  - A call made while `stream` is not being captured looks the array's
+ *    device address up (cudaGetSymbolAddress, on the current device), so a
+ *    device reset that reloads the library's module is picked up by the next
+ *    such call.  A call made during stream capture reuses the address found by
+ *    the last call outside capture on that device and returns
+ *    MOET_ERR_UNSUPPORTED if there was none: make the first call on a device
+ *    before any stream capture.
  *  - Every call uses the same array and leaves its contents behind; calls
  *    that overlap on the GPU race on it, so the caller must serialise them.
  *    No scratch contents need to start at zero. */

@@ -19,18 +19,21 @@ among the monotone assignments of the sorted block: c1 smallest weights -> L0, t
 -> L1, c3 - c2 -> L2, the rest -> L3, for 0 <= c1 <= c2 <= c3 <= 16 (969 candidates).  For one
 assignment the best scale is s = Nc / Dc with Nc = sum a_i w_i and Dc = sum a_i^2, leaving the
 error sum w^2 - Nc^2 / Dc, so the best candidate maximises Nc^2 / Dc among those with Nc > 0
-(s > 0); if none has Nc > 0 the block quantises to 0.
+(s > 0); if none has Nc > 0 the block quantises to 0.  Where several candidates reach the same
+maximum exactly, the first in the order c1, then c2, then c3 ascending is taken.
 
-Decision precision.  The argmax decides an integer (the assignment), so it is taken in fp32 with
-one fixed operation order, which the GPU kernel follows too:
-  P[0] = 0, P[j + 1] = fl(P[j] + w_sorted[j])                      (fp32 prefix sums)
-  N = fl(fl(fl(fl(A P[c1]) + fl(B P[c2])) + fl(C P[c3])) + fl(Dl P[16]))
-      with A = L0 - L1, B = L1 - L2, C = L2 - L3, Dl = L3          (integers)
-  D = (L0^2 - L1^2) c1 + (L1^2 - L2^2) c2 + (L2^2 - L3^2) c3 + 16 L3^2  (exact)
-  candidates in the order c1, then c2, then c3 ascending; one replaces the best when N > 0 and
-  fl(fl(N N) Dbest) > fl(NNbest D)                               (first maximum wins)
-The chosen block's sums are then evaluated in fp64: Nc and sum a_i from the counts and the fp64
-sums of the four groups, s = Nc / Dc, bias = s sum a - sum w, error = sum w^2 - Nc^2 / Dc.
+Decision arithmetic.  The argmax decides an integer (the assignment), so it is taken exactly:
+the block's fp32 weights are integers times one power of two, 2^E, so every prefix sum P and
+every Nc = (L0 - L1) P[c1] + (L1 - L2) P[c2] + (L2 - L3) P[c3] + L3 P[16] is an exact integer
+times 2^E (int64 when the block's magnitudes span at most 24 binades, Python integers
+otherwise), and Dc is an integer.  Scores are ranked in fp64 and every candidate within a
+relative 1e-9 of the top fp64 score is compared exactly, Nc_a^2 Dc_b against Nc_b^2 Dc_a in
+integers.  The chosen block's sums are then evaluated in fp64: Nc and sum a_i from the counts
+and the fp64 sums of the four groups, s = Nc / Dc, bias = s sum a - sum w, error = sum w^2 -
+Nc^2 / Dc.  Each block also reports its decision margin (the relative gap between the best score
+and the best score of a candidate with a different, exactly smaller score) and its Nc, so that
+an implementation that ranks the candidates in lower precision can be held to the exact choice
+wherever the margin exceeds its rounding error.
 """
 from __future__ import annotations
 
@@ -47,30 +50,174 @@ def _candidates(B: int):
     return [(c1, c2, c3) for c1 in range(B + 1) for c2 in range(c1, B + 1) for c3 in range(c2, B + 1)]
 
 
-def best_assignment(ws: np.ndarray, levels) -> tuple:
-    """The search on one sorted block ws (fp32, ascending): (c1, c2, c3) of the best candidate, or
-    None when no candidate has N > 0."""
+_CAND_CACHE = {}
+
+
+def _cand_arrays(B: int):
+    if B not in _CAND_CACHE:
+        c = np.array(_candidates(B), dtype=np.int64)
+        _CAND_CACHE[B] = (c[:, 0], c[:, 1], c[:, 2])
+    return _CAND_CACHE[B]
+
+
+def _block_integers(ws: np.ndarray):
+    """Sorted fp32 blocks [nb, B] -> (n [nb, B] integers as Python-int object array or int64, E [nb])
+    with ws = n * 2^E exactly; int64 where every block spans at most 24 binades."""
     ws = np.asarray(ws, dtype=np.float32)
-    B = ws.shape[0]
+    a = np.abs(ws.astype(np.float64))
+    nz = a > 0
+    big = np.where(nz, a, 0.0).max(axis=1)
+    small = np.where(nz, a, np.inf).min(axis=1)
+    e_small = np.where(np.isfinite(small), np.floor(np.log2(np.where(np.isfinite(small), small, 1.0))), 0.0)
+    e_big = np.where(big > 0, np.floor(np.log2(np.where(big > 0, big, 1.0))), 0.0)
+    E = np.maximum(e_small - 23, -149).astype(np.int64)            # ulp exponent of the smallest |w|
+    spread = (e_big - e_small).astype(np.int64)
+    n = ws.astype(np.float64) * np.ldexp(1.0, -E)[:, None]          # exact integers (fp64 holds 2^53)
+    ok = spread <= 24
+    return n, E, ok
+
+
+def _exact_int(x) -> int:
+    return int(x)
+
+
+def _decide(n_rows, levels):
+    """Exact argmax over the candidates for integer blocks n_rows [m, B] (Python ints or int64 in
+    float64 storage).  Returns (cut [m, 3] (-1 = none), margin [m], nbest [m] float)."""
+    m, B = n_rows.shape
     L0, L1, L2, L3 = (int(v) for v in levels)
-    f32 = np.float32
-    P = [f32(0)]
-    for j in range(B):
-        P.append(f32(P[-1] + ws[j]))
-    A, Bc, C, Dl = f32(L0 - L1), f32(L1 - L2), f32(L2 - L3), f32(L3)
-    best, nn_best, d_best = None, f32(0), f32(1)
-    for c1, c2, c3 in _candidates(B):
-        n = f32(f32(f32(f32(A * P[c1]) + f32(Bc * P[c2])) + f32(C * P[c3])) + f32(Dl * P[B]))
-        d = f32((L0 * L0 - L1 * L1) * c1 + (L1 * L1 - L2 * L2) * c2 + (L2 * L2 - L3 * L3) * c3 + B * L3 * L3)
-        if n > 0:
-            nn = f32(n * n)
-            if f32(nn * d_best) > f32(nn_best * d):
-                best, nn_best, d_best = (c1, c2, c3), nn, d
-    return best
+    c1, c2, c3 = _cand_arrays(B)
+    D = ((L0 * L0 - L1 * L1) * c1 + (L1 * L1 - L2 * L2) * c2 + (L2 * L2 - L3 * L3) * c3
+         + B * L3 * L3).astype(np.int64)
+    A, Bc, C = L0 - L1, L1 - L2, L2 - L3
+    cut = np.full((m, 3), -1, dtype=np.int64)
+    margin = np.zeros(m)
+    nbest = np.zeros(m)
+    for r in range(m):
+        P = [0]
+        for j in range(B):
+            P.append(P[-1] + _exact_int(n_rows[r, j]))
+        Pa = np.array(P, dtype=object)
+        N = A * Pa[c1] + Bc * Pa[c2] + C * Pa[c3] + L3 * Pa[B]          # exact (Python ints)
+        Nf = N.astype(np.float64)
+        pos = Nf > 0
+        if not pos.any():
+            continue
+        with np.errstate(divide="ignore", invalid="ignore"):
+            score = np.where(pos, Nf * Nf / D, -1.0)
+        top = score.max()
+        near = np.flatnonzero(score >= top * (1.0 - 1e-9))
+        best = int(near[0])
+        for i in near[1:]:                                             # exact: N_i^2 D_b > N_b^2 D_i
+            i = int(i)
+            if N[i] * N[i] * int(D[best]) > N[best] * N[best] * int(D[i]):
+                best = i
+        # the best score of any other candidate (an exact tie gives margin 0)
+        others = np.delete(score, best)
+        second = others.max() if others.size else -1.0
+        margin[r] = (score[best] - second) / score[best] if second > 0 else 1.0
+        cut[r] = (c1[best], c2[best], c3[best])
+        nbest[r] = float(N[best])
+    return cut, margin, nbest
+
+
+def _decide_fast(n, levels):
+    """Vectorised twin of _decide for int64-range blocks: exact integer N in int64, fp64 ranking,
+    exact comparison (Python ints) of the candidates that come within 1e-9 of the top."""
+    nb, B = n.shape
+    L0, L1, L2, L3 = (int(v) for v in levels)
+    c1, c2, c3 = _cand_arrays(B)
+    D = ((L0 * L0 - L1 * L1) * c1 + (L1 * L1 - L2 * L2) * c2 + (L2 * L2 - L3 * L3) * c3
+         + B * L3 * L3).astype(np.int64)
+    ni = n.astype(np.int64)
+    P = np.zeros((nb, B + 1), dtype=np.int64)
+    P[:, 1:] = np.cumsum(ni, axis=1)
+    N = (L0 - L1) * P[:, c1] + (L1 - L2) * P[:, c2] + (L2 - L3) * P[:, c3] + L3 * P[:, B:B + 1]   # [nb, 969]
+    Nf = N.astype(np.float64)
+    pos = Nf > 0
+    with np.errstate(divide="ignore", invalid="ignore"):
+        score = np.where(pos, Nf * Nf / D[None, :], -1.0)
+    top = score.max(axis=1)
+    cut = np.full((nb, 3), -1, dtype=np.int64)
+    margin = np.zeros(nb)
+    nbest = np.zeros(nb)
+    has = top > 0
+    near = score >= (top * (1.0 - 1e-9))[:, None]
+    first = np.argmax(near, axis=1)
+    multi = near.sum(axis=1) > 1
+    best = first.copy()
+    for r in np.flatnonzero(multi & has):
+        cand = np.flatnonzero(near[r])
+        b = int(cand[0])
+        for i in cand[1:]:
+            i = int(i)
+            if int(N[r, i]) ** 2 * int(D[b]) > int(N[r, b]) ** 2 * int(D[i]):
+                b = i
+        best[r] = b
+    sb_ = score[np.arange(nb), best]
+    # the best score of any other candidate (an exact tie gives margin 0)
+    rest = score.copy()
+    rest[np.arange(nb), best] = -1.0
+    second = rest.max(axis=1)
+    margin = np.where(has, np.where(second > 0, (sb_ - second) / np.where(sb_ > 0, sb_, 1.0), 1.0), 0.0)
+    cut[has] = np.stack([c1[best], c2[best], c3[best]], axis=1)[has]
+    nbest[has] = Nf[np.arange(nb), best][has]
+    return cut, margin, nbest
+
+
+def probe_blocks(w: np.ndarray, levels, block: int = BLOCK):
+    """One [N, K] matrix -> (per-block sums [N, K/block, 4] (sum W, sum W^2, sum (Q - W),
+    sum (Q - W)^2), decision margin [N, K/block], Nc of the choice in units of 2^E times 2^E
+    (fp64) [N, K/block], sum |W| [N, K/block])."""
+    w = np.asarray(w, dtype=np.float32)
+    N, K = w.shape
+    assert K % block == 0
+    ws = np.sort(w.reshape(-1, block), axis=1)
+    nb = ws.shape[0]
+    L0, L1, L2, L3 = (int(v) for v in levels)
+    n, E, ok = _block_integers(ws)
+    cut = np.full((nb, 3), -1, dtype=np.int64)
+    margin = np.zeros(nb)
+    nbest = np.zeros(nb)
+    if ok.any():
+        c, mg, nbv = _decide_fast(n[ok], levels)
+        cut[ok], margin[ok], nbest[ok] = c, mg, nbv
+    if (~ok).any():
+        from fractions import Fraction
+        rows = np.flatnonzero(~ok)
+        for r in rows:                     # wide blocks: exact Python integers
+            ints = np.array([int(Fraction(float(x)) / Fraction(2) ** int(E[r])) for x in ws[r]], dtype=object)
+            c, mg, nbv = _decide(ints[None, :], levels)
+            cut[r], margin[r], nbest[r] = c[0], mg[0], nbv[0]
+    wd = ws.astype(np.float64)
+    sw, sw2 = wd.sum(axis=1), (wd * wd).sum(axis=1)
+    idx = np.arange(block)[None, :]
+    a = np.where(idx < cut[:, 0:1], L0, np.where(idx < cut[:, 1:2], L1,
+                                                 np.where(idx < cut[:, 2:3], L2, L3))).astype(np.float64)
+    nc, dc = (a * wd).sum(axis=1), (a * a).sum(axis=1)
+    found = cut[:, 0] >= 0
+    with np.errstate(divide="ignore", invalid="ignore"):
+        bias = np.where(found, nc / dc * a.sum(axis=1) - sw, -sw)
+        err = np.where(found, sw2 - nc * nc / dc, sw2)
+    per_block = np.stack([sw, sw2, bias, err], axis=1).reshape(N, K // block, 4)
+    return (per_block, margin.reshape(N, K // block), (nbest * np.ldexp(1.0, E)).reshape(N, K // block),
+            np.abs(wd).sum(axis=1).reshape(N, K // block))
+
+
+def best_assignment(ws: np.ndarray, levels):
+    """(c1, c2, c3) of the exact best candidate for one sorted fp32 block, or None when no
+    candidate has Nc > 0."""
+    ws = np.sort(np.asarray(ws, dtype=np.float32))
+    from fractions import Fraction
+    den = max(Fraction(float(x)).denominator for x in ws)      # a power of two: x den is an integer
+    ints = np.array([int(Fraction(float(x)) * den) for x in ws], dtype=object)
+    cut, _, _ = _decide(ints[None, :], levels)
+    return None if cut[0, 0] < 0 else tuple(int(v) for v in cut[0])
 
 
 def block_sums(w: np.ndarray, levels) -> tuple:
-    """(sum w, sum w^2, bias sum (Q - w), error sum (Q - w)^2) of one block, fp64."""
+    """(sum w, sum w^2, bias sum (Q - w), error sum (Q - w)^2) of one block, fp64 (the exact choice
+    made with Python integers throughout)."""
     w = np.asarray(w, dtype=np.float32)
     B = w.shape[0]
     ws = np.sort(w)
@@ -89,45 +236,8 @@ def block_sums(w: np.ndarray, levels) -> tuple:
 
 
 def probe(w: np.ndarray, levels, block: int = BLOCK) -> np.ndarray:
-    """One [N, K] matrix -> [N, 4] per-row sums (sum W, sum W^2, sum (Q - W), sum (Q - W)^2).
-    The same search as best_assignment / block_sums, run on all blocks at once (every fp32
-    operation is the same elementwise operation on arrays)."""
-    w = np.asarray(w, dtype=np.float32)
-    N, K = w.shape
-    assert K % block == 0
-    ws = np.sort(w.reshape(-1, block), axis=1)
-    nb = ws.shape[0]
-    L0, L1, L2, L3 = (int(v) for v in levels)
-    f32 = np.float32
-    P = np.zeros((nb, block + 1), dtype=np.float32)
-    for j in range(block):
-        P[:, j + 1] = P[:, j] + ws[:, j]
-    A, Bc, C, Dl = f32(L0 - L1), f32(L1 - L2), f32(L2 - L3), f32(L3)
-    tail = Dl * P[:, block]
-    cut = np.full((nb, 3), -1, dtype=np.int64)
-    nn_best = np.zeros(nb, dtype=np.float32)
-    d_best = np.ones(nb, dtype=np.float32)
-    for c1, c2, c3 in _candidates(block):
-        n = ((A * P[:, c1] + Bc * P[:, c2]) + C * P[:, c3]) + tail
-        d = f32((L0 * L0 - L1 * L1) * c1 + (L1 * L1 - L2 * L2) * c2 + (L2 * L2 - L3 * L3) * c3
-                + block * L3 * L3)
-        nn = n * n
-        upd = (n > 0) & (nn * d_best > nn_best * d)
-        cut[upd] = (c1, c2, c3)
-        nn_best[upd] = nn[upd]
-        d_best[upd] = d
-    wd = ws.astype(np.float64)
-    sw, sw2 = wd.sum(axis=1), (wd * wd).sum(axis=1)
-    idx = np.arange(block)[None, :]
-    a = np.where(idx < cut[:, 0:1], L0, np.where(idx < cut[:, 1:2], L1,
-                                                 np.where(idx < cut[:, 2:3], L2, L3))).astype(np.float64)
-    nc, dc = (a * wd).sum(axis=1), (a * a).sum(axis=1)
-    found = cut[:, 0] >= 0
-    with np.errstate(divide="ignore", invalid="ignore"):
-        bias = np.where(found, nc / dc * a.sum(axis=1) - sw, -sw)
-        err = np.where(found, sw2 - nc * nc / dc, sw2)
-    per_block = np.stack([sw, sw2, bias, err], axis=1)
-    return per_block.reshape(N, K // block, 4).sum(axis=1)
+    """One [N, K] matrix -> [N, 4] per-row sums (sum W, sum W^2, sum (Q - W), sum (Q - W)^2)."""
+    return probe_blocks(w, levels, block)[0].sum(axis=1)
 
 
 def statistics(sums: np.ndarray, n_weights: int) -> dict:

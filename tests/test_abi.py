@@ -112,3 +112,12 @@ def test_workspace_size_is_monotone(lib):
     assert ws(0, 7168, 2048, 256, 8) == 0
     # fp32 h [T k, I] and o [T k, H] dominate
     assert b >= 64 * 8 * (7168 + 2048) * 4
+
+
+def test_static_scratch_size_matches_header(lib):
+    """The binding's copy of the fixed scratch size of moet_moe_forward_static is the header's."""
+    from bit_moe_expert_moet_gb300 import _lib
+    with open(os.path.join(ROOT, "include", "moet.h")) as f:
+        m = re.search(r"#define\s+MOET_FORWARD_STATIC_SCRATCH_BYTES\s+\(\(size_t\)(\d+)\s*<<\s*(\d+)\)", f.read())
+    assert m is not None
+    assert _lib.FORWARD_STATIC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))

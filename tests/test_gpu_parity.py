@@ -2,7 +2,8 @@
 
 Integer outputs (NVFP4 codes/scales, planes, s16, delta, top-k ids, offsets,
 permutation) must match bit for bit; routing weights within 1e-6; the layer
-output within relative Frobenius 5e-3 and max-abs 2e-2 rms(y*).
+output within relative Frobenius 5e-3 and max-abs 2e-2 rms(y*) (the bound and
+when the bf16 rounding of the exact output is taken out of it: ``_parity``).
 """
 import numpy as np
 import pytest
@@ -10,10 +11,10 @@ import torch
 
 import workloads as W
 from oracle import gate as ogate, moe as omoe, nvfp4 as onv, requant as orq, route as oroute
+from _parity import check_y
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
-REL_FROB, MAX_ABS = 5e-3, 2e-2
 
 
 @pytest.fixture(scope="module")
@@ -30,26 +31,6 @@ def dev(a):
 
 def host(t):
     return t.cpu().numpy()
-
-
-def _bf16_half_ulp(v):
-    """Half a bf16 ulp at |v| (8 significant bits): the rounding any bf16 output carries."""
-    _, e = np.frexp(np.abs(v))
-    return np.where(v != 0, np.ldexp(1.0, e - 9), 0.0)
-
-
-def check_y(yg, yo):
-    """The layer tolerance: relative Frobenius error <= 5e-3 and max-abs error <= 2e-2 rms(y*).
-    The max-abs budget is for the computation; the final rounding to the bf16 output format
-    (at most half a bf16 ulp of y*, the same for any exact implementation) is taken out of it,
-    which matters only for outputs whose largest elements are many rms (e.g. with experts that
-    contribute zero)."""
-    yg = np.asarray(yg, np.float64)
-    rel = np.linalg.norm(yg - yo) / np.linalg.norm(yo)
-    over = np.maximum(np.abs(yg - yo) - _bf16_half_ulp(yo), 0.0)
-    mx = over.max() / np.sqrt(np.mean(yo ** 2))
-    assert rel <= REL_FROB and mx <= MAX_ABS, (rel, mx)
-    return rel, mx
 
 
 # ------------------------------------------------------------------ quantiser / requant
@@ -648,34 +629,101 @@ def _random_planes(rng, E, N, K):
     return dict(sign=sign, mag=mag, s16=s16, scale_2=sc2)
 
 
-def _full_layer(moet, cfg, dset, rng):
-    ref, gp = {}, {}
+# Full-size layers: the planes of every expert come from the seeded generators in `workloads`
+# (drawn on the host, one (expert, FC) matrix at a time, and uploaded); the oracle regenerates
+# the planes of the experts the sampled tokens route to, in spawn-started worker processes
+# (`_oracle_shard`), one shard of experts each.
+FULL_SEED = 50
+FULL_CASES = {
+    # name: (config, sampled tokens or a rule, gate override)
+    "dsv3_decode_t1": ("dsv3_decode_t1", "all", None),
+    "dsv3_decode_t1_gated": ("dsv3_decode_t1", "all", "all"),
+    "dsv3_decode_t8": ("dsv3_decode_t8", "all", None),
+    "dsv3_decode_t64": ("dsv3_decode_t64", "mix", None),
+    "glm_decode": ("glm_decode", "all", None),
+    "kimi_layer": ("kimi_layer", "spread", None),
+    "dsv3_prefill": ("dsv3_prefill", "mix", None),
+}
+
+
+def _full_layer_gpu(moet, cfg, n_slots):
+    """GPU planes [E, ...] and delta pool [n_slots, ...] drawn by the shared generators."""
+    heavy = cfg.dist == "student_t4"
+    gp = {}
     for f, (N, K) in ((1, (2 * cfg.I, cfg.H)), (2, (cfg.H, cfg.I))):
-        p = _random_planes(rng, cfg.E, N, K)
-        ref[f] = p
-        gp[f] = moet.Planes(dev(p["sign"].view(np.int32)), dev(p["mag"].view(np.int32)), dev(p["s16"]),
-                            dev(p["scale_2"]))
-        S = max(len(dset), 1)
-        d = dict(codes=rng.integers(0, 256, (S, N, K // 2), dtype=np.uint8),
-                 s4=rng.integers(16, 41, (S, N, K // 16), dtype=np.uint8))
-        ref[f, "d"] = d
-        gp[f, "d"] = moet.DeltaPool(dev(d["codes"]), dev(d["s4"]))
-    return ref, gp
+        sign = torch.empty((cfg.E, N, K // 32), dtype=torch.int32, device=DEV)
+        mag = torch.empty_like(sign)
+        s16 = torch.empty((cfg.E, N, K // 16), dtype=torch.uint8, device=DEV)
+        for e in range(cfg.E):
+            sg, mg, sc = W.draw_plane_matrix(FULL_SEED, e, f, N, K, heavy)
+            sign[e].copy_(torch.from_numpy(sg.view(np.int32)))
+            mag[e].copy_(torch.from_numpy(mg.view(np.int32)))
+            s16[e].copy_(torch.from_numpy(sc))
+        gp[f] = moet.Planes(sign, mag, s16, dev(W.draw_plane_scale2(FULL_SEED, f, cfg.E, K)))
+        S = max(n_slots, 1)
+        codes = torch.zeros((S, N, K // 2), dtype=torch.uint8, device=DEV)
+        s4 = torch.zeros((S, N, K // 16), dtype=torch.uint8, device=DEV)
+        for s_ in range(n_slots):
+            dc, ds = W.draw_delta_matrix(FULL_SEED, s_, f, N, K)
+            codes[s_].copy_(torch.from_numpy(dc))
+            s4[s_].copy_(torch.from_numpy(ds))
+        gp[f, "d"] = moet.DeltaPool(codes, s4)
+    return gp
 
 
-@pytest.mark.parametrize("name,tokens", [("dsv3_decode_t64", [0, 37]), ("glm_decode", [3]), ("dsv3_prefill", None)])
-def test_forward_full_size_sampled(moet, name, tokens):
-    cfg = W.CONFIGS[name]
+def _sample_tokens(rule, T, gate):
+    if rule == "all":
+        return list(range(T))
+    if rule == "spread":
+        return sorted({int(t) for t in np.linspace(0, T - 1, 8).round()})
+    # "mix": four gated and four ungated tokens (as many as the batch has)
+    g = [int(t) for t in np.flatnonzero(gate != 0)]
+    u = [int(t) for t in np.flatnonzero(gate == 0)]
+    pick = g[:: max(1, len(g) // 4)][:4] + u[:: max(1, len(u) // 4)][:4]
+    return sorted(set(pick))
+
+
+def _oracle_full(cfg, logits, xb, gate, slot, tokens):
+    """Oracle y for the sampled tokens, the experts split over spawn workers."""
+    import multiprocessing as mp
+    import os
+    import _oracle_shard
+    oi, ow = oroute.route_topk(logits, cfg.k)
+    x = W.bf16_bits_to_f32(xb[tokens]).astype(np.float64)
+    idx, wts = oi[tokens], ow[tokens]
+    g = gate[tokens] if slot is not None else None
+    experts = np.unique(idx)
+    n = max(1, min(8, os.cpu_count() or 1, len(experts)))
+    shards = [sh for sh in np.array_split(experts, n) if len(sh)]
+    jobs = [(FULL_SEED, cfg.H, cfg.I, cfg.E, cfg.dist == "student_t4", x, idx, wts, g, slot, sh) for sh in shards]
+    with mp.get_context("spawn").Pool(len(jobs)) as pool:
+        parts = pool.map(_oracle_shard.shard_forward, jobs)
+    return np.sum(parts, axis=0)
+
+
+@pytest.mark.parametrize("case", list(FULL_CASES))
+def test_forward_full_size_sampled(moet, case):
+    """Every layer configuration at full size, the whole batch through the library, sampled
+    tokens against the oracle: all tokens at T = 1 and 8 (GLM: every token gated), four gated and
+    four ungated tokens at T = 64 and in the prefill batch, eight tokens spread over the 1T-class
+    layer's 256.  Planes with block scales over the whole e4m3 range (subnormal and zero blocks
+    included), wider still for the Student-t layers."""
+    cname, rule, gate_override = FULL_CASES[case]
+    cfg = W.CONFIGS[cname]
     logits, xb, dset, gate = W.draw_layer_inputs(cfg)
-    if tokens is None:   # prefill-sized batch: one ungated token and two gated ones (delta pass)
-        tokens = [int(np.flatnonzero(gate == 0)[0])] + [int(t) for t in np.flatnonzero(gate == 1)[:2]]
-    rng = np.random.default_rng(50)
-    ref, gp = _full_layer(moet, cfg, dset, rng)
-    yg, err = _run_forward(moet, logits, xb, cfg.k, gp, cfg.E, cfg.H, dset, gate)
+    if gate_override == "all":
+        gate = np.ones(cfg.T, np.uint8)
+    with_delta = len(dset) > 0 and cfg.gate != "none"
+    gp = _full_layer_gpu(moet, cfg, len(dset) if with_delta else 0)
+    yg, err = _run_forward(moet, logits, xb, cfg.k, gp, cfg.E, cfg.H, dset if with_delta else None, gate)
     assert err == 0
     assert np.all(np.isfinite(yg))
-    yo = _oracle_forward(logits, xb, cfg.k, ref, dset, gate, cfg.E, tokens=tokens)
-    check_y(yg[tokens], yo[tokens])
+    tokens = _sample_tokens(rule, cfg.T, gate)
+    slot = W.delta_slot_table(cfg.E, dset) if with_delta else None
+    yo = _oracle_full(cfg, logits, xb, gate, slot, tokens)
+    check_y(yg[tokens], yo, label=f"full-size {case} tokens={len(tokens)}")
+    del gp
+    torch.cuda.empty_cache()
 
 
 # ---------------------------------------------------------------- sign-bias probe

@@ -1,6 +1,7 @@
 """Pins of the sign-bias probe oracle (oracle/signbias.py) against definitions it does not use:
-exhaustive assignments, a direct scan over scales with nearest-level rounding, exact fits,
-scale and sign symmetries, and the pages' qualitative finding on synthetic weights."""
+exhaustive assignments compared exactly in rational arithmetic, a direct scan over scales with
+nearest-level rounding, exact fits, scale and sign symmetries, and the pages' qualitative
+finding on synthetic weights."""
 import itertools
 
 import numpy as np
@@ -18,25 +19,65 @@ def _nearest_error(w, levels, s):
     return float(((q - w) ** 2).sum()), float((q - w).sum())
 
 
+def _exact_error(w, a):
+    """sum w^2 - (sum a w)^2 / sum a^2 in exact rationals (w fp32, a integer levels)."""
+    from fractions import Fraction
+    wf = [Fraction(float(x)) for x in w]
+    nc = sum(int(ai) * wi for ai, wi in zip(a, wf))
+    dc = sum(int(ai) * int(ai) for ai in a)
+    sw2 = sum(x * x for x in wf)
+    return sw2 - nc * nc / dc if (dc > 0 and nc > 0) else sw2
+
+
+def _chosen_levels(ws, levels):
+    cand = sb.best_assignment(ws, levels)
+    if cand is None:
+        return None
+    cuts = (0,) + cand + (len(ws),)
+    return [levels[j] for j in range(4) for _ in range(cuts[j + 1] - cuts[j])]
+
+
 @pytest.mark.parametrize("levels", CODEBOOKS)
 def test_search_equals_exhaustive_assignments(levels):
-    """On blocks of 6 weights the monotone search finds the minimum of sum w^2 - Nc^2/Dc over all
-    4^6 assignments with Nc > 0 (or 0 when none has), i.e. the L2 optimum over every
-    (assignment, scale > 0) pair."""
+    """On blocks of 6 weights the exact monotone search reaches the minimum of
+    sum w^2 - Nc^2/Dc over all 4^6 assignments with Nc > 0 (sum w^2 when none has) exactly, in
+    rational arithmetic: the L2 optimum over every (assignment, scale > 0) pair.  Blocks include
+    one-signed ones and blocks spanning 60 binades (the exact path beyond int64)."""
     rng = np.random.default_rng(41)
-    combos = np.array(list(itertools.product(range(4), repeat=6)))
-    L = np.asarray(levels, dtype=np.float64)
-    for _ in range(40):
+    combos = list(itertools.product(range(4), repeat=6))
+    for it in range(40):
         w = rng.standard_normal(6).astype(np.float32)
         if rng.random() < 0.3:
             w = np.abs(w) * (1 if rng.random() < 0.5 else -1)            # one-signed blocks
-        wd = w.astype(np.float64)
-        a = L[combos]
-        nc, dc = a @ wd, (a * a).sum(1)
-        ok = (nc > 0) & (dc > 0)
-        best = min((wd * wd).sum(), ((wd * wd).sum() - nc[ok] ** 2 / dc[ok]).min() if ok.any() else np.inf)
-        got = sb.block_sums(w, levels)[3]
-        assert got == pytest.approx(best, rel=1e-6, abs=1e-12)
+        if it % 7 == 3:
+            w[:2] *= np.float32(1e-18)                                     # wide magnitude span
+        ws = np.sort(w)
+        best = min(_exact_error(ws, [levels[c] for c in combo]) for combo in combos)
+        a = _chosen_levels(ws, levels)
+        got = _exact_error(ws, a) if a is not None else _exact_error(ws, [0] * 6)
+        assert got == best, (it, float(got), float(best))
+
+
+@pytest.mark.parametrize("levels", CODEBOOKS)
+def test_vectorised_choice_equals_exact_scalar_choice(levels):
+    """The vectorised search (int64 integers, fp64 ranking, exact comparison of near-top
+    candidates) takes the same assignment as the scalar one in Python integers throughout, on
+    blocks of 16 with repeated values, exact ties and one-signed blocks; an exact tie reports
+    margin 0."""
+    rng = np.random.default_rng(47)
+    w = (rng.standard_t(4, (6, 64)) * 0.02).astype(np.float32)
+    w[0, :16] = np.float32(0.01)                                           # all equal
+    w[1, 16:32] = np.abs(w[1, 16:32])
+    w[2, :16] = np.repeat(w[2, :4], 4)
+    w[3, :16] = np.float32(0.25) * np.asarray(levels, np.float32)[np.arange(16) % 4]
+    per_block, margin, _, _ = sb.probe_blocks(w, levels)
+    for n in range(w.shape[0]):
+        for b in range(4):
+            ref = sb.block_sums(w[n, 16 * b:16 * b + 16], levels)
+            assert np.allclose(per_block[n, b], ref, rtol=1e-13, atol=1e-18), (n, b)
+    # two distinct weights, 8 each: the cut between them can sit at two places with equal scores
+    # for {-1, 1}-symmetric pairs of levels -> at least one exact tie somewhere in such blocks
+    assert (margin >= 0).all() and (margin <= 1).all()
 
 
 @pytest.mark.parametrize("levels", CODEBOOKS)

@@ -4,9 +4,15 @@ Such callers (a plug-in handed only its input and output buffers, code running
 inside a runtime whose device allocator belongs to someone else) cannot provide
 the forward's workspace.  The static entry point uses a fixed scratch array in
 the library's device image instead.  Checked here through the C ABI against the
-workspace entry point on the same inputs, for two calls in a row (the second
-call finds the first call's leftovers in the shared scratch), plus the size
-rejection.  This file is collected last on purpose.
+workspace entry point on the same inputs, bit for bit (both run the same
+deterministic kernels): before each checked call the shared scratch is filled
+by a static call on unrelated data (another token count, top-k, routing, and
+the delta table with a gate mask), so a kernel that read a scratch word before
+writing it would see the leftovers; each check runs twice in a row, with and
+without the delta.  The decode engine's shape (I = 256) and the mma.sync
+engine's (I = 384) both fit the fixed scratch.  Plus the size rejection (the
+binding's copy of the size is checked against the header on the CPU, in test_abi).  This
+file is collected last on purpose.
 """
 import ctypes
 
@@ -15,11 +21,10 @@ import pytest
 import torch
 
 import workloads as W
-from oracle import nvfp4 as onv, requant as orq
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
-REL_FROB, MAX_ABS = 5e-3, 2e-2
+H, E, SEED = 1024, 16, 77
 
 
 @pytest.fixture(scope="module")
@@ -34,61 +39,81 @@ def _dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
 
 
-def _layer(moet, H, I, E, rng):
-    planes = {}
+def _layer(moet, I, dset):
+    """Planes of E experts and a delta pool of len(dset) slots from the seeded generators."""
+    planes, pools = {}, {}
     for f, (N, K) in ((1, (2 * I, H)), (2, (H, I))):
-        w = (rng.standard_normal((E, N, K)) * 0.02).astype(np.float32)
-        q = [onv.quantize(w[e]) for e in range(E)]
-        rq = [orq.requant_2bit(a[0], a[1], want_delta=False) for a in q]
-        planes[f] = moet.Planes(_dev(np.stack([r["sign"] for r in rq]).view(np.int32)),
-                                _dev(np.stack([r["mag"] for r in rq]).view(np.int32)),
-                                _dev(np.stack([r["s16"] for r in rq])),
-                                _dev(np.array([a[2] for a in q], np.float32)))
-    return planes
+        p = [W.draw_plane_matrix(SEED + I, e, f, N, K) for e in range(E)]
+        planes[f] = moet.Planes(_dev(np.stack([a[0] for a in p]).view(np.int32)),
+                                _dev(np.stack([a[1] for a in p]).view(np.int32)),
+                                _dev(np.stack([a[2] for a in p])),
+                                _dev(W.draw_plane_scale2(SEED + I, f, E, K)))
+        d = [W.draw_delta_matrix(SEED + I, s, f, N, K) for s in range(len(dset))]
+        pools[f] = moet.DeltaPool(_dev(np.stack([a[0] for a in d])), _dev(np.stack([a[1] for a in d])))
+    return planes, pools
 
 
-def _close(a, b):
-    a = a.astype(np.float64)
-    b = b.astype(np.float64)
-    rel = np.linalg.norm(a - b) / np.linalg.norm(b)
-    mx = np.abs(a - b).max() / np.sqrt(np.mean(b ** 2))
-    return rel <= REL_FROB and mx <= MAX_ABS, (rel, mx)
+class _Batch:
+    """One routed batch of T tokens (top-k on device) with a gate mask."""
+
+    def __init__(self, moet, rng, T, k):
+        self.T, self.k = T, k
+        self.x = _dev(W.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32)).view(np.int16)).view(
+            torch.bfloat16)
+        self.idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+        self.w = torch.empty((T, k), dtype=torch.float32, device=DEV)
+        self.off = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+        self.perm = torch.empty(T * k, dtype=torch.int32, device=DEV)
+        moet.route_topk(_dev(rng.standard_normal((T, E)).astype(np.float32)), k, self.idx, self.w, self.off,
+                        self.perm)
+        self.gate = _dev((rng.random(T) < 0.5).astype(np.uint8))
+
+    def args(self):
+        return self.x, self.idx, self.w, self.off, self.perm
 
 
-def test_static_scratch_forward_matches_workspace_forward(moet):
-    H, I, E, k, T = 1024, 256, 16, 4, 9
-    rng = np.random.default_rng(77)
-    planes = _layer(moet, H, I, E, rng)
-    logits = _dev(rng.standard_normal((T, E)).astype(np.float32))
-    x = _dev(W.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32)).view(np.int16)).view(torch.bfloat16)
-    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
-    w = torch.empty((T, k), dtype=torch.float32, device=DEV)
-    off = torch.empty(E + 1, dtype=torch.int32, device=DEV)
-    perm = torch.empty(T * k, dtype=torch.int32, device=DEV)
-    moet.route_topk(logits, k, idx, w, off, perm)
-    y_ref = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
-    ws = torch.empty(moet.forward_workspace_size(T, H, I, E, k), dtype=torch.uint8, device=DEV)
-    moet.moe_forward(x, idx, w, off, perm, planes[1], planes[2], y_ref, ws)
-    ref = y_ref.float().cpu().numpy()
-    outs = []
-    for _ in range(2):
-        y = torch.full((T, H), float("nan"), dtype=torch.bfloat16, device=DEV)
-        moet.moe_forward_static(x, idx, w, off, perm, planes[1], planes[2], y)
-        torch.cuda.synchronize()
-        outs.append(y.float().cpu().numpy())
+@pytest.mark.parametrize("I", [256, 384], ids=["decode_engine", "mma_sync_engine"])
+def test_static_scratch_forward_equals_workspace_forward(moet, I):
+    rng = np.random.default_rng(SEED + I)
+    dset = np.array([1, 4, 9, 12], dtype=np.int32)
+    planes, pools = _layer(moet, I, dset)
+    slot = _dev(W.delta_slot_table(E, dset))
+    dkw = dict(delta_slot=slot, dfc1=pools[1], dfc2=pools[2])
+    main = _Batch(moet, rng, 9, 4)
+    other = [_Batch(moet, rng, 5, 2), _Batch(moet, rng, 13, 6)]
+
+    refs = {}
+    for with_delta in (True, False):
+        y = torch.empty((main.T, H), dtype=torch.bfloat16, device=DEV)
+        ws = torch.empty(moet.forward_workspace_size(main.T, H, I, E, main.k), dtype=torch.uint8, device=DEV)
+        kw = dict(dkw, gate_mask=main.gate) if with_delta else {}
+        moet.moe_forward(*main.args(), planes[1], planes[2], y, ws, **kw)
+        refs[with_delta] = y
+    torch.cuda.synchronize()
     assert moet.last_device_error() == 0
-    for o in outs:
-        ok, err = _close(o, ref)
-        assert ok, err
+
+    for n, with_delta in enumerate((True, False, True)):
+        # unrelated data first: the scratch now holds another batch's headers, work items,
+        # activation terms, h and o
+        ob = other[n % 2]
+        junk = torch.empty((ob.T, H), dtype=torch.bfloat16, device=DEV)
+        moet.moe_forward_static(*ob.args(), planes[1], planes[2], junk, **dict(dkw, gate_mask=ob.gate))
+        for _ in range(2):                        # two calls in a row
+            y = torch.full((main.T, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+            kw = dict(dkw, gate_mask=main.gate) if with_delta else {}
+            moet.moe_forward_static(*main.args(), planes[1], planes[2], y, **kw)
+            torch.cuda.synchronize()
+            assert torch.equal(y, refs[with_delta]), (I, with_delta)
+    assert moet.last_device_error() == 0
 
 
 def test_static_scratch_forward_rejects_oversized_layers(moet):
     lib = moet.lib
-    T, H, I, E, k = 64, 7168, 2048, 256, 8                # needs far more than the fixed scratch
-    assert moet.forward_workspace_size(T, H, I, E, k) > moet.FORWARD_STATIC_SCRATCH_BYTES
+    T, H_, I, E_, k = 64, 7168, 2048, 256, 8                # needs far more than the fixed scratch
+    assert moet.forward_workspace_size(T, H_, I, E_, k) > moet.FORWARD_STATIC_SCRATCH_BYTES
     dummy = torch.zeros(16, dtype=torch.uint8, device=DEV)
     p = ctypes.c_void_p(dummy.data_ptr())
     planes = moet._lib._Planes(p, p, p, p)
-    status = lib.moet_moe_forward_static(T, H, I, E, k, p, p, p, p, p, ctypes.byref(planes),
+    status = lib.moet_moe_forward_static(T, H_, I, E_, k, p, p, p, p, p, ctypes.byref(planes),
                                          ctypes.byref(planes), None, 0, None, None, None, p, None)
     assert moet.status_string(status) == "MOET_ERR_WORKSPACE"

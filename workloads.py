@@ -34,7 +34,8 @@ import math
 import numpy as np
 
 __all__ = ["LayerConfig", "CONFIGS", "draw_logits", "draw_x_bf16", "draw_weight",
-           "draw_delta_set", "draw_gate", "bf16_bits_to_f32", "f32_to_bf16_bits"]
+           "draw_delta_set", "draw_gate", "bf16_bits_to_f32", "f32_to_bf16_bits",
+           "draw_plane_matrix", "draw_plane_scale2", "draw_delta_matrix"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -154,3 +155,54 @@ def delta_slot_table(E: int, dset: np.ndarray) -> np.ndarray:
     slot = np.full(E, -1, dtype=np.int32)
     slot[dset] = np.arange(len(dset), dtype=np.int32)
     return slot
+
+
+# ---------------------------------------------------------------- random plane sets
+# Any sign and magnitude bits with any e4m3 block scales form a valid 2-bit
+# expert matrix, so the full-size parity checks draw the planes directly (the
+# oracle's own requantisation of 17 G weights would take hours on a CPU).  Each
+# part of each (expert, FC) matrix has its own stream, so any one part can be
+# regenerated alone: default_rng([seed, 2000 + e, fc, part]).
+
+def draw_plane_matrix(seed: int, expert: int, fc: int, N: int, K: int, heavy: bool = False):
+    """(sign [N, K/32] u32, mag [N, K/32] u32, s16 [N, K/16] u8) of one expert matrix.
+
+    Bits are uniform.  Block-scale codes (e4m3fn) are a mixture over the whole
+    finite range: 90 % in the upper band a requantised layer mostly holds
+    (codes 96..126, i.e. 32..448; with ``heavy`` 72..126, i.e. 4..448, a
+    Student-t-like spread of block maxima), 5 % small normal codes below that
+    band, 4 % subnormal codes 1..7 and 1 % zero blocks."""
+    def g(part):
+        return np.random.default_rng([seed, 2000 + expert, fc, part])
+    sign = g(0).integers(0, 2 ** 32, (N, K // 32), dtype=np.uint32)
+    mag = g(1).integers(0, 2 ** 32, (N, K // 32), dtype=np.uint32)
+    r = g(2)
+    nb = (N, K // 16)
+    lo = 72 if heavy else 96
+    s16 = r.integers(lo, 127, nb, dtype=np.uint8)
+    u = r.random(nb)
+    small = r.integers(8, lo, nb, dtype=np.uint8)
+    sub = r.integers(1, 8, nb, dtype=np.uint8)
+    s16 = np.where(u < 0.05, small, s16)
+    s16 = np.where((u >= 0.05) & (u < 0.09), sub, s16)
+    s16 = np.where((u >= 0.09) & (u < 0.10), np.uint8(0), s16).astype(np.uint8)
+    return sign, mag, s16
+
+
+def draw_plane_scale2(seed: int, fc: int, E: int, K: int) -> np.ndarray:
+    """Per-expert fp32 scale_2 [E] for draw_plane_matrix planes: uniform in
+    [0.5, 1.5] / (450 sqrt(K)) (450 is about the rms of q s16 for the upper band),
+    so that a unit-variance activation row gives O(1) outputs."""
+    r = np.random.default_rng([seed, 3000, fc])
+    return (r.uniform(0.5, 1.5, E) / (450.0 * math.sqrt(K))).astype(np.float32)
+
+
+def draw_delta_matrix(seed: int, slot: int, fc: int, N: int, K: int):
+    """(codes [N, K/2] u8, s4 [N, K/16] u8) of one delta-pool slot: uniform code
+    bytes; scale codes 64..110 (0.125..224, the range of a residual's block
+    maxima over 6) with 2 % zero blocks."""
+    r = np.random.default_rng([seed, 4000 + slot, fc])
+    codes = r.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    s4 = r.integers(64, 111, (N, K // 16), dtype=np.uint8)
+    s4[r.random(s4.shape) < 0.02] = 0
+    return codes, s4
