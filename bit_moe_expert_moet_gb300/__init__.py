@@ -17,6 +17,8 @@ Entry points (same names as the C ABI without the ``moet_`` prefix):
   moe_forward_pooled  the same over a pool of resident experts (slot table,
                    non-resident experts contribute zero and are counted)
   gate_from_confidence  the confidence gate: gate mask and the experts to promote
+  moe_forward_static    moe_forward with its scratch in the library image (no workspace)
+  debug_wait_expiry     test control of the engines' bounded waits
 """
 from ._lib import (  # noqa: F401
     MoetError,
@@ -28,6 +30,7 @@ from ._lib import (  # noqa: F401
     last_device_error,
     profile_enable,
     profile_read,
+    debug_wait_expiry,
     KERNEL_KINDS,
     quantize_nvfp4,
     requant_2bit,

@@ -49,6 +49,8 @@ lib.moet_moe_forward_static.argtypes = [_i, _i, _i, _i, _i, _p, _p, _p, _p, _p,
                                         _p, _i, ctypes.POINTER(_Nvfp4), ctypes.POINTER(_Nvfp4),
                                         _p, _p, _p]
 FORWARD_STATIC_SCRATCH_BYTES = 8 << 20
+lib.moet_debug_wait_expiry.restype = _i
+lib.moet_debug_wait_expiry.argtypes = [_i, _i]
 lib.moet_profile_enable.restype = _i
 lib.moet_profile_enable.argtypes = [_i]
 lib.moet_profile_read.restype = _i
@@ -106,6 +108,13 @@ def _ptr(t: Optional[torch.Tensor], dtype=None, name: str = "") -> Optional[int]
 
 
 KERNEL_KINDS = ("requant", "quantize", "route", "prologue", "fc1", "fc2", "combine", "terms", "probe")
+
+
+def debug_wait_expiry(polls: int = 0, withhold: bool = False):
+    """Test control of the tcgen05 engines' bounded waits (moet_debug_wait_expiry): polls > 0
+    lowers the poll bound, withhold makes CTA 0 of each engine launch skip its first unit record
+    so that the waits on it run out.  debug_wait_expiry() restores the defaults."""
+    _check("moet_debug_wait_expiry", lib.moet_debug_wait_expiry(int(polls), 1 if withhold else 0))
 
 
 def profile_enable(on: bool = True):

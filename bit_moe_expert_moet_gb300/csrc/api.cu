@@ -91,6 +91,16 @@ extern "C" __attribute__((visibility("hidden"))) int moet_internal_error_route(v
 extern "C" __attribute__((visibility("hidden"))) int moet_internal_error_moe(void);
 extern "C" __attribute__((visibility("hidden"))) int moet_internal_error_moe_tc(void);
 extern "C" __attribute__((visibility("hidden"))) int moet_internal_error_moe_pf(void);
+extern "C" __attribute__((visibility("hidden"))) int moet_internal_debug_waits_moe_tc(int, int);
+extern "C" __attribute__((visibility("hidden"))) int moet_internal_debug_waits_moe_pf(int, int);
+
+extern "C" moet_status moet_debug_wait_expiry(int polls, int withhold) {
+  if (polls < 0 || (withhold != 0 && withhold != 1)) return MOET_ERR_INVALID_ARG;
+  if (moet_internal_debug_waits_moe_tc(polls, withhold) != 0 ||
+      moet_internal_debug_waits_moe_pf(polls, withhold) != 0)
+    return MOET_ERR_CUDA;
+  return MOET_OK;
+}
 
 extern "C" const char* moet_status_string(moet_status s) {
   switch (s) {

@@ -43,17 +43,34 @@ constexpr int kSmemBudget = 96 * 1024;
 constexpr uint32_t kCodeLut = 0xC242BC3Cu;  // f16 high bytes of +1, -1, +3, -3
 
 struct WsLayout {
-  size_t hdr, tok_scale, tok_max, hmax, inv, pvalid, chunks, h, o, xt, ht, pfa, total;
+  size_t hdr, tok_scale, tok_max, hmax, inv, pvalid, chunks, chunks_s, h, o, xt, ht, pfa, total;
 };
 
 // Largest T routed through the tcgen05 engine (small tokens-per-expert regime).
 constexpr int kTcMaxT = 512;
+
+// Prefill regime (T > kTcMaxT): an expert routed at most this many pairs is a weight stream with
+// few tokens, where the bf16 engine's 128-row tiles would cost as much as for 256 pairs; its pairs
+// go through the block-scaled decode engine in items of kTcTok instead (a second work list).
+constexpr int kPfSmallMax = 64;
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 __host__ __device__ inline int max_chunks(int T, int E, int k, int chunk) {
   const long long pairs = (long long)T * k;
   return (int)((pairs < E ? pairs : E) + (pairs + chunk - 1) / chunk);
+}
+
+// Capacity of the prefill regime's second work list: items of <= kTcTok pairs of experts with at
+// most kPfSmallMax pairs.
+inline int pf_small_items(int T, int E, int k) {
+  const long long a = max_chunks(T, E, k, kTcTok);
+  const long long b = (long long)E * ((kPfSmallMax + kTcTok - 1) / kTcTok);
+  return (int)(a < b ? a : b);
+}
+
+inline bool pf_hybrid(int T, int H, int I) {
+  return T > kTcMaxT && pf_supported(H, I) && tc_supported(H, I) && kPfSmallMax > 0;
 }
 
 inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
@@ -69,12 +86,18 @@ inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   L.chunks = off;    off += align256(sizeof(int4) * (size_t)max_chunks(T, E, k, kTcTok));
   L.h = off;         off += align256(sizeof(float) * pairs * I);
   L.o = off;         off += align256(sizeof(float) * pairs * H);
-  L.xt = off; L.ht = off; L.pfa = off;
+  L.xt = off; L.ht = off; L.pfa = off; L.chunks_s = off;
   if (T <= kTcMaxT && tc_supported(H, I)) {
     L.xt = off;      off += align256(tc_terms_bytes(pairs, (size_t)H));
     L.ht = off;      off += align256(tc_terms_bytes(pairs, (size_t)I));
   } else if (T > kTcMaxT && pf_supported(H, I)) {
     L.pfa = off;     off += align256(pf_act_bytes(pairs, (size_t)H, (size_t)I) + 5 * 256);
+    if (pf_hybrid(T, H, I)) {
+      const size_t items = (size_t)pf_small_items(T, E, k), rows = items * kTcTok;
+      L.chunks_s = off; off += align256(sizeof(int4) * items);
+      L.xt = off;       off += align256(tc_terms_bytes(rows, (size_t)H));
+      L.ht = off;       off += align256(tc_terms_bytes(rows, (size_t)I));
+    }
   }
   L.total = off;
   return L;
@@ -96,7 +119,8 @@ __device__ __forceinline__ float pow2_scale_for(float amax) {
 // each work item carries the expert's pool slot (.w) for the plane and scale_2 addressing; without
 // one, .w is the expert id.
 __global__ void __launch_bounds__(kThreads) prologue_kernel(
-    int T, int H, int E, int k, int chunk, const uint16_t* __restrict__ x, const int32_t* __restrict__ offsets,
+    int T, int H, int E, int k, int chunk, int chunk_small, int small_max, int4* __restrict__ chunks_small,
+    const uint16_t* __restrict__ x, const int32_t* __restrict__ offsets,
     const int32_t* __restrict__ perm, int* __restrict__ hdr, float* __restrict__ tok_scale,
     float* __restrict__ tok_max, unsigned* __restrict__ hmax, int32_t* __restrict__ inv, int4* __restrict__ chunks,
     const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ expert_slot, int n_pool,
@@ -113,7 +137,7 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(
       const int e = 32 * i + lane;
       lo[i] = e <= E ? __ldg(offsets + e) : 0;
     }
-    int running = 0;
+    int running = 0, running_s = 0;
 #pragma unroll
     for (int i = 0; i < kMaxPerLane; ++i) {
       const int c0 = 32 * i;
@@ -135,25 +159,36 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(
           }
         }
       }
-      const int nch = pslot >= 0 ? (n + chunk - 1) / chunk : 0;
-      int incl = nch;
+      // an expert with at most small_max pairs goes to the second list (items of chunk_small)
+      const bool small = small_max > 0 && n <= small_max;
+      const int nch = pslot >= 0 && !small ? (n + chunk - 1) / chunk : 0;
+      const int nchs = pslot >= 0 && small ? (n + chunk_small - 1) / chunk_small : 0;
+      int incl = nch, incl_s = nchs;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
+        const int ys = __shfl_up_sync(0xffffffffu, incl_s, o);
+        if (lane >= o) { incl += y; incl_s += ys; }
       }
       const int first = running + incl - nch;
       for (int c = 0; c < nch; ++c) {
         const int cnt = min(chunk, n - c * chunk);
         chunks[first + c] = make_int4(e, c * chunk, cnt, pslot);
       }
+      const int first_s = running_s + incl_s - nchs;
+      for (int c = 0; c < nchs; ++c) {
+        const int cnt = min(chunk_small, n - c * chunk_small);
+        chunks_small[first_s + c] = make_int4(e, c * chunk_small, cnt, pslot);
+      }
       running += __shfl_sync(0xffffffffu, incl, 31);
+      running_s += __shfl_sync(0xffffffffu, incl_s, 31);
     }
     ok = __all_sync(0xffffffffu, ok);
     if (lane == 0) {
       if (!ok) record_error(MOET_ERR_DEVICE_INDEX);
       hdr[0] = ok ? running : 0;
       hdr[1] = ok ? 1 : 0;
+      hdr[2] = ok ? running_s : 0;
     }
     return;
   }
@@ -595,10 +630,13 @@ static moet_status forward_impl(int T, int H, int I, int E, int k, const uint16_
 
   const bool use_tc = T <= kTcMaxT && tc_supported(H, I);
   const bool use_pf = !use_tc && T > kTcMaxT && pf_supported(H, I);
+  const bool hybrid = use_pf && pf_hybrid(T, H, I);
   const int chunk = use_tc ? kTcTok : use_pf ? kPfTok : kChunk;
+  int4* chunks_s = hybrid ? reinterpret_cast<int4*>(ws + L.chunks_s) : nullptr;
   {
     ProfScope ps(MOET_K_PROLOGUE, st);
-    prologue_kernel<<<1 + (T + 7) / 8, kThreads, 0, st>>>(T, H, E, k, chunk, x, expert_offsets, perm, hdr,
+    prologue_kernel<<<1 + (T + 7) / 8, kThreads, 0, st>>>(T, H, E, k, chunk, kTcTok, hybrid ? kPfSmallMax : 0,
+                                                           chunks_s, x, expert_offsets, perm, hdr,
                                                            tok_scale, tok_max, hmax, use_tc ? inv : nullptr,
                                                            chunks, topk_idx, expert_slot, n_pool, miss_count,
                                                            miss_mask, pvalid);
@@ -606,6 +644,34 @@ static moet_status forward_impl(int T, int H, int I, int E, int k, const uint16_
   MOET_CUDA_TRY(cudaGetLastError());
 
   const int mc = max_chunks(T, E, k, chunk);
+  // the block-scaled decode engine's part: every item of the decode regime, or the prefill
+  // regime's second list (experts with few pairs), with term rows per item slot
+  auto carve = [](char* base, size_t rows, size_t K, uint8_t** cperm, uint8_t** cnat, uint8_t** sf, float** g) {
+    size_t off = 0;
+    *cperm = reinterpret_cast<uint8_t*>(base + off); off += align256(rows * kTcTerms * (K / 2));
+    *cnat = reinterpret_cast<uint8_t*>(base + off);  off += align256(rows * kTcTerms * (K / 2));
+    *sf = reinterpret_cast<uint8_t*>(base + off);    off += align256(rows * kTcTerms * (K / 16));
+    *g = reinterpret_cast<float*>(base + off);
+  };
+  auto tc_args = [&](bool items) {
+    TcForwardArgs f{};
+    f.T = T; f.H = H; f.I = I; f.E = n_planes; f.k = k;   // E: experts the planes hold (tensor maps)
+    f.x = x; f.offsets = expert_offsets; f.perm = perm; f.topk_w = topk_w;
+    f.fc1 = fc1; f.fc2 = fc2;
+    f.delta_slot = with_delta ? delta_slot : nullptr;
+    f.n_slots = n_slots; f.dfc1 = dfc1; f.dfc2 = dfc2;
+    f.gate = with_delta ? gate_mask : nullptr;
+    f.hdr = items ? hdr + 2 : hdr;
+    f.chunks = items ? chunks_s : chunks;
+    f.h = h; f.o = o; f.max_items = items ? pf_small_items(T, E, k) : mc;
+    f.tokmax = tok_max; f.hmax = hmax; f.inv = inv;
+    f.item_rows = items ? 1 : 0;
+    const size_t rows = items ? (size_t)pf_small_items(T, E, k) * kTcTok : (size_t)T * k;
+    f.act_rows = (int)rows;
+    carve(ws + L.xt, rows, (size_t)H, &f.buf.x_cperm, &f.buf.x_cnat, &f.buf.x_sf, &f.buf.x_g);
+    carve(ws + L.ht, rows, (size_t)I, &f.buf.h_cperm, &f.buf.h_cnat, &f.buf.h_sf, &f.buf.h_g);
+    return f;
+  };
   if (use_pf) {
     PfForwardArgs f{};
     f.T = T; f.H = H; f.I = I; f.E = n_planes; f.k = k;   // E: experts the planes hold (tensor maps)
@@ -624,29 +690,24 @@ static moet_status forward_impl(int T, int H, int I, int E, int k, const uint16_
     f.h16 = reinterpret_cast<uint16_t*>(pb);  pb += align256(pairs * I * sizeof(uint16_t));
     f.hg16 = reinterpret_cast<uint16_t*>(pb); pb += align256(pairs * I * sizeof(uint16_t));
     f.hscale = reinterpret_cast<float*>(pb);
-    moet_status s = pf_forward(f, st);
-    if (s != MOET_OK) return s;
+    // FC1 of both lists (they write disjoint bucketed rows of h), then FC2 of both (disjoint
+    // pairs of o); each engine's FC2 reads only its own rows of h
+    if (hybrid) {
+      const TcForwardArgs g = tc_args(true);
+      moet_status s = tc_forward_fc1(g, st);
+      if (s != MOET_OK) return s;
+      s = pf_forward_fc1(f, st);
+      if (s != MOET_OK) return s;
+      s = tc_forward_fc2(g, st);
+      if (s != MOET_OK) return s;
+      s = pf_forward_fc2(f, st);
+      if (s != MOET_OK) return s;
+    } else {
+      moet_status s = pf_forward(f, st);
+      if (s != MOET_OK) return s;
+    }
   } else if (use_tc) {
-    TcForwardArgs f{};
-    f.T = T; f.H = H; f.I = I; f.E = n_planes; f.k = k;   // E: experts the planes hold (tensor maps)
-    f.x = x; f.offsets = expert_offsets; f.perm = perm; f.topk_w = topk_w;
-    f.fc1 = fc1; f.fc2 = fc2;
-    f.delta_slot = with_delta ? delta_slot : nullptr;
-    f.n_slots = n_slots; f.dfc1 = dfc1; f.dfc2 = dfc2;
-    f.gate = with_delta ? gate_mask : nullptr;
-    f.hdr = hdr; f.chunks = chunks; f.h = h; f.o = o; f.max_items = mc;
-    f.tokmax = tok_max; f.hmax = hmax; f.inv = inv;
-    const size_t pairs = (size_t)T * k;
-    auto carve = [](char* base, size_t rows, size_t K, uint8_t** cperm, uint8_t** cnat, uint8_t** sf, float** g) {
-      size_t off = 0;
-      *cperm = reinterpret_cast<uint8_t*>(base + off); off += align256(rows * kTcTerms * (K / 2));
-      *cnat = reinterpret_cast<uint8_t*>(base + off);  off += align256(rows * kTcTerms * (K / 2));
-      *sf = reinterpret_cast<uint8_t*>(base + off);    off += align256(rows * kTcTerms * (K / 16));
-      *g = reinterpret_cast<float*>(base + off);
-    };
-    carve(ws + L.xt, pairs, (size_t)H, &f.buf.x_cperm, &f.buf.x_cnat, &f.buf.x_sf, &f.buf.x_g);
-    carve(ws + L.ht, pairs, (size_t)I, &f.buf.h_cperm, &f.buf.h_cnat, &f.buf.h_sf, &f.buf.h_g);
-    moet_status s = tc_forward(f, st);
+    moet_status s = tc_forward(tc_args(false), st);
     if (s != MOET_OK) return s;
   } else {
   const int maxn = T < kChunk ? T : kChunk;

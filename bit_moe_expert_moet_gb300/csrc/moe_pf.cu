@@ -320,6 +320,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
   float (*xchg)[64] = reinterpret_cast<float (*)[64]>(base + kPXchg);   // [16 columns][64 rows]
   PfSmem& sm = *reinterpret_cast<PfSmem*>(base + kPXchg + 64 * 16 * sizeof(float));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int wl = wait_limit();
   const int total_units = a.hdr[0] * a.tiles;
   const int nunits = (int)blockIdx.x < total_units ? (total_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
   if (nunits == 0) return;
@@ -355,7 +356,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
     bool bad = false;
     for (int j = 0; j < nunits && !bad; ++j) {
       const int m = j % kPMeta;
-      if (!mbar_wait_warp(&sm.meta_full[m], (j / kPMeta) & 1)) { bad = true; break; }
+      if (!mbar_wait_warp(&sm.meta_full[m], (j / kPMeta) & 1, wl)) { bad = true; break; }
       const PfMeta& um = sm.meta[m];
       const int pos0 = um.pos0, nck = um.nck, dslot = um.dslot;
       const int nb = (um.ncols + 63) / 64;                 // 64-row activation boxes per step
@@ -366,7 +367,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
         const int cc = dp ? c - nkc : c;
         if (warp == 0) {
           const int ps = gc % kPRing;
-          if (gc >= kPRing && !mbar_wait_warp(&sm.pempty[ps], ((gc / kPRing) - 1) & 1)) { bad = true; break; }
+          if (gc >= kPRing && !mbar_wait_warp(&sm.pempty[ps], ((gc / kPRing) - 1) & 1, wl)) { bad = true; break; }
           unsigned char* pst = base + kPBase + ps * kPChunkBytes;
           if (lane == 0) mbar_expect_tx(&sm.pfull[ps], dp ? 18432u : 10240u);
           __syncwarp();
@@ -390,7 +391,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
         for (int s = 0; s < kPC / kStepWeights; ++s, ++gs) {
           if (gs % kBProd != bprod) continue;
           const int bs = gs % kBRing;
-          if (gs >= kBRing && !mbar_wait_warp(&sm.bdone[bs], ((gs / kBRing) - 1) & 1)) { bad = true; break; }
+          if (gs >= kBRing && !mbar_wait_warp(&sm.bdone[bs], ((gs / kBRing) - 1) & 1, wl)) { bad = true; break; }
           unsigned char* bst = base + kBBase + bs * kBStepBytes;
           if (lane == 0) mbar_expect_tx(&sm.bfull[bs], (uint32_t)nb * 64u * 128u);
           __syncwarp();
@@ -404,10 +405,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
     if (lane == 0) {
       // every copy this warp issued has landed before the CTA may exit
       if (warp == 0)
-        for (int i = gc > kPRing ? gc - kPRing : 0; i < gc; ++i) mbar_wait(&sm.pfull[i % kPRing], (i / kPRing) & 1);
+        for (int i = gc > kPRing ? gc - kPRing : 0; i < gc; ++i) mbar_wait(&sm.pfull[i % kPRing], (i / kPRing) & 1, wl);
       else
         for (int i = gs > kBRing ? gs - kBRing : 0; i < gs; ++i)
-          if (i % kBProd == bprod) mbar_wait(&sm.bfull[i % kBRing], (i / kBRing) & 1);
+          if (i % kBProd == bprod) mbar_wait(&sm.bfull[i % kBRing], (i / kBRing) & 1, wl);
     }
   } else if (warp == 1) {
     // ---------------- MMA issue
@@ -416,8 +417,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
       bool bad = false;
       for (int j = 0; j < nunits && !bad; ++j) {
         const int m = j % kPMeta;
-        if (!mbar_wait(&sm.meta_full[m], (j / kPMeta) & 1)) { bad = true; break; }
-        if (j >= 1 && !mbar_wait(&sm.acc_empty, (j - 1) & 1)) { bad = true; break; }
+        if (!mbar_wait(&sm.meta_full[m], (j / kPMeta) & 1, wl)) { bad = true; break; }
+        if (j >= 1 && !mbar_wait(&sm.acc_empty, (j - 1) & 1, wl)) { bad = true; break; }
         if (pf_stuck(sm)) { bad = true; break; }
         asm volatile("tcgen05.fence::after_thread_sync;");
         const int nst = sm.meta[m].nck * (kPC / kStepWeights);
@@ -427,14 +428,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
         // plus the next)
         for (int st = 0; st < nst && !bad; st += kGrp, gs += kGrp) {
           const int grp = gs / kGrp;
-          if (!mbar_wait(&sm.staged[grp % kNGrp], (grp / kNGrp) & 1)) {
+          if (!mbar_wait(&sm.staged[grp % kNGrp], (grp / kNGrp) & 1, wl)) {
             bad = true;
             break;
           }
 #pragma unroll
           for (int h = 0; h < kGrp; ++h) {
             const int as = (gs + h) % kPAst, bs = (gs + h) % kBRing;
-            if (!mbar_wait(&sm.bfull[bs], ((gs + h) / kBRing) & 1)) {
+            if (!mbar_wait(&sm.bfull[bs], ((gs + h) / kBRing) & 1, wl)) {
               bad = true;
               break;
             }
@@ -455,13 +456,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
       }
       if (bad) atomicExch(&sm.stuck, 1);
       // every MMA this thread issued is complete before TMEM is released
-      if (last >= 0) mbar_wait(&sm.bdone[last % kBRing], (last / kBRing) & 1);
+      if (last >= 0) mbar_wait(&sm.bdone[last % kBRing], (last / kBRing) & 1, wl);
     }
   } else if (warp == 2) {
     // ---------------- scheduler
     for (int j = 0; j < nunits; ++j) {
       const int m = j % kPMeta;
-      if (j >= kPMeta && !mbar_wait_warp(&sm.meta_empty[m], ((j / kPMeta) - 1) & 1)) {
+      if (j >= kPMeta && !mbar_wait_warp(&sm.meta_empty[m], ((j / kPMeta) - 1) & 1, wl)) {
         if (lane == 0) atomicExch(&sm.stuck, 1);
         break;
       }
@@ -513,7 +514,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
         um.sc2 = __ldg(a.scale_2 + pe);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.meta_full[m]);
+      // (a test can make CTA 0 withhold its first record: every wait on it then runs out)
+      const bool withhold = blockIdx.x == 0 && j == 0 && *reinterpret_cast<volatile int*>(&g_dbg_withhold) != 0;
+      if (lane == 0 && !withhold) mbar_arrive(&sm.meta_full[m]);
     }
   } else if (warp >= 4 && warp < 8) {
     // ---------------- epilogue: TMEM lane quarter warp & 3
@@ -521,8 +524,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
     const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;
     for (int j = 0; j < nunits; ++j) {
       const int m = j % kPMeta;
-      bool ok = mbar_wait_warp(&sm.meta_full[m], (j / kPMeta) & 1);
-      ok = ok && mbar_wait_warp(&sm.acc_full, j & 1);
+      bool ok = mbar_wait_warp(&sm.meta_full[m], (j / kPMeta) & 1, wl);
+      ok = ok && mbar_wait_warp(&sm.acc_full, j & 1, wl);
       asm volatile("tcgen05.fence::after_thread_sync;");
       if (epi_any(!ok || pf_stuck(sm))) {
         if (!ok && lane == 0) atomicExch(&sm.stuck, 1);
@@ -594,12 +597,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
     bool bad = false;
     for (int j = 0; j < nunits && !bad; ++j) {
       const int m = j % kPMeta;
-      if (!mbar_wait_warp(&sm.meta_full[m], (j / kPMeta) & 1)) { bad = true; break; }
+      if (!mbar_wait_warp(&sm.meta_full[m], (j / kPMeta) & 1, wl)) { bad = true; break; }
       if (__any_sync(0xffffffffu, pf_stuck(sm))) { bad = true; break; }
       const int nck = sm.meta[m].nck;
       for (int c = 0; c < nck && !bad; ++c, ++gc) {
         const int ps = gc % kPRing;
-        if (!mbar_wait_warp(&sm.pfull[ps], (gc / kPRing) & 1)) { bad = true; break; }
+        if (!mbar_wait_warp(&sm.pfull[ps], (gc / kPRing) & 1, wl)) { bad = true; break; }
         const unsigned char* pst = base + kPBase + ps * kPChunkBytes;
         const bool dp = c >= nkc;
         constexpr int kSteps = kPC / kStepWeights;
@@ -610,7 +613,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
           // the group's A stages are free once the MMAs of the group that used them last are done
           if (grp >= kNGrp) {
             const int q = grp - kNGrp;
-            if (!mbar_wait_warp(&sm.adone[q % kNGrp], (q / kNGrp) & 1)) { bad = true; break; }
+            if (!mbar_wait_warp(&sm.adone[q % kNGrp], (q / kNGrp) & 1, wl)) { bad = true; break; }
           }
           // half h expands 32-weight group 2 (s + h2) + h of step s + h2 (16-bit pairs of weights
           // c and c + 16 per column)
@@ -686,7 +689,20 @@ moet_status launch_pf(const PfArgs& a, const moet_planes* pl, const moet_nvfp4* 
 
 }  // namespace
 
-moet_status pf_forward(const PfForwardArgs& f, cudaStream_t st) {
+namespace {
+PfArgs pf_common(const PfForwardArgs& f) {
+  const bool with_delta = f.delta_slot != nullptr && f.gate != nullptr;
+  PfArgs a{};
+  a.T = f.T; a.H = f.H; a.I = f.I; a.k = f.k;
+  a.offsets = f.offsets; a.perm = f.perm; a.topk_w = f.topk_w;
+  a.delta_slot = with_delta ? f.delta_slot : nullptr; a.n_slots = f.n_slots;
+  a.gate = with_delta ? f.gate : nullptr;
+  a.hdr = f.hdr; a.chunks = f.chunks;
+  return a;
+}
+}  // namespace
+
+moet_status pf_forward_fc1(const PfForwardArgs& f, cudaStream_t st) {
   const int pairs = f.T * f.k;
   const bool with_delta = f.delta_slot != nullptr && f.gate != nullptr;
   {
@@ -697,18 +713,16 @@ moet_status pf_forward(const PfForwardArgs& f, cudaStream_t st) {
                                            with_delta ? f.xbg : nullptr);
   }
   MOET_CUDA_TRY(cudaGetLastError());
-  PfArgs a{};
-  a.T = f.T; a.H = f.H; a.I = f.I; a.k = f.k;
-  a.offsets = f.offsets; a.perm = f.perm; a.topk_w = f.topk_w;
-  a.delta_slot = with_delta ? f.delta_slot : nullptr; a.n_slots = f.n_slots;
-  a.gate = with_delta ? f.gate : nullptr;
-  a.hdr = f.hdr; a.chunks = f.chunks;
-  PfArgs a1 = a;
+  PfArgs a1 = pf_common(f);
   a1.K = f.H; a1.N = 2 * f.I; a1.tiles = f.I / 64;
   a1.scale_2 = f.fc1->scale_2;
   a1.h = f.h;
-  moet_status s = launch_pf<true>(a1, f.fc1, f.dfc1, f.xb, f.xbg, pairs, f.E, st);
-  if (s != MOET_OK) return s;
+  return launch_pf<true>(a1, f.fc1, f.dfc1, f.xb, f.xbg, pairs, f.E, st);
+}
+
+moet_status pf_forward_fc2(const PfForwardArgs& f, cudaStream_t st) {
+  const int pairs = f.T * f.k;
+  const bool with_delta = f.delta_slot != nullptr && f.gate != nullptr;
   {
     ProfScope ps(MOET_K_TERMS, st);
     pf_h16_kernel<<<pairs, 256, 0, st>>>(pairs, f.k, f.I, f.h, f.perm, with_delta ? f.gate : nullptr, f.topk_idx,
@@ -716,7 +730,7 @@ moet_status pf_forward(const PfForwardArgs& f, cudaStream_t st) {
                                          with_delta ? f.hg16 : nullptr, f.hscale);
   }
   MOET_CUDA_TRY(cudaGetLastError());
-  PfArgs a2 = a;
+  PfArgs a2 = pf_common(f);
   a2.K = f.I; a2.N = f.H; a2.tiles = f.H / 128;
   a2.scale_2 = f.fc2->scale_2;
   a2.hscale = f.hscale;
@@ -724,6 +738,13 @@ moet_status pf_forward(const PfForwardArgs& f, cudaStream_t st) {
   return launch_pf<false>(a2, f.fc2, f.dfc2, f.h16, f.hg16, pairs, f.E, st);
 }
 
+moet_status pf_forward(const PfForwardArgs& f, cudaStream_t st) {
+  const moet_status s = pf_forward_fc1(f, st);
+  if (s != MOET_OK) return s;
+  return pf_forward_fc2(f, st);
+}
+
 }  // namespace moet
 
 MOET_ERROR_ACCESSOR(moet_internal_error_moe_pf)
+MOET_DEBUG_WAITS_SETTER(moet_internal_debug_waits_moe_pf)

@@ -48,6 +48,10 @@ struct PfForwardArgs {
   float* o;                    // [T k, H] pair order
 };
 
+// FC1 (the gather of x, then the FC kernel) and FC2 (h to scaled fp16, then the FC kernel);
+// pf_forward runs both.
+moet_status pf_forward_fc1(const PfForwardArgs& a, cudaStream_t st);
+moet_status pf_forward_fc2(const PfForwardArgs& a, cudaStream_t st);
 moet_status pf_forward(const PfForwardArgs& a, cudaStream_t st);
 
 }  // namespace moet

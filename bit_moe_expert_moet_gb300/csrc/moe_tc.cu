@@ -130,47 +130,11 @@ __device__ __forceinline__ uint4 planes_to_e2m1(uint32_t S, uint32_t M) {
 // position); FC2 expands each bucketed pair row in place (inv = null, ncopy = 1).
 constexpr int kTermThreads = 128;
 
-template <bool BF16_IN>
-__global__ void __launch_bounds__(kTermThreads) act_terms_kernel(int K, const void* __restrict__ src,
-                                                                const int32_t* __restrict__ inv, int ncopy,
-                                                                int out_rows, const float* __restrict__ rowmax,
-                                                                uint8_t* __restrict__ cperm, uint8_t* __restrict__ cnat,
-                                                                uint8_t* __restrict__ sfb, float* __restrict__ gsc) {
-  const int row = blockIdx.x, tid = threadIdx.x;
-  const size_t srow = (size_t)row;
-  const float m = __ldg(rowmax + srow);
-  const float g0 = m / (6.0f * 448.0f);
-  // output rows of this source row (out of range entries are skipped)
-  auto out_row = [&](int cp) -> int {
-    const int r = inv ? __ldg(inv + (size_t)row * ncopy + cp) : row;
-    return r >= 0 && r < out_rows ? r : -1;
-  };
-  if (blockIdx.y == 0 && tid < kTcTerms) {
-    for (int cp = 0; cp < ncopy; ++cp) {
-      const int orow = out_row(cp);
-      if (orow >= 0) gsc[(size_t)orow * kTcTerms + tid] = ldexpf(g0, -2 * tid);
-    }
-  }
-  const int b = blockIdx.y * kTermThreads + tid;            // 16-element block of the row
-  if (b >= K / 16) return;
-  float r[16];
-  if (BF16_IN) {
-    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) + srow * K + 16 * b);
-    const uint4 u0 = __ldg(p), u1 = __ldg(p + 1);
-    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      r[2 * i] = __uint_as_float(w[i] << 16);
-      r[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-  } else {
-    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(src) + srow * K + 16 * b);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 v = p[i];
-      r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
-    }
-  }
+// The kTcTerms NVFP4 terms of one 16-element block r (the residual is updated in place) under the
+// row's first term scale g0: per term the codes in natural order (nat) and in the expansion's
+// order (per), two words each, and the ue4m3 block scale.
+__device__ __forceinline__ void block_terms(float (&r)[16], float g0, uint32_t (&nat)[kTcTerms][2],
+                                            uint32_t (&per)[kTcTerms][2], uint32_t (&sfo)[kTcTerms]) {
 #pragma unroll
   for (int t = 0; t < kTcTerms; ++t) {
     const float g = ldexpf(g0, -2 * t);
@@ -197,20 +161,132 @@ __global__ void __launch_bounds__(kTermThreads) act_terms_kernel(int K, const vo
     }
     // natural order: byte i holds elements 2i, 2i+1; permuted order: position p = 4 r + n
     // holds element r + 4 n
-    uint32_t nat[2] = {0u, 0u}, per[2] = {0u, 0u};
+    nat[t][0] = nat[t][1] = per[t][0] = per[t][1] = 0u;
 #pragma unroll
     for (int p = 0; p < 16; ++p) {
-      nat[p >> 3] |= code[p] << (4 * (p & 7));
-      per[p >> 3] |= code[(p >> 2) + 4 * (p & 3)] << (4 * (p & 7));
+      nat[t][p >> 3] |= code[p] << (4 * (p & 7));
+      per[t][p >> 3] |= code[(p >> 2) + 4 * (p & 3)] << (4 * (p & 7));
     }
+    sfo[t] = sf;
+  }
+}
+
+// The 16 source elements of block b of a row: bf16 (FC1 input x) or fp32 (FC2 input h).
+template <bool BF16_IN>
+__device__ __forceinline__ void load_block(const void* __restrict__ src, size_t srow, int K, int b, float (&r)[16]) {
+  if (BF16_IN) {
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) + srow * K + 16 * b);
+    const uint4 u0 = __ldg(p), u1 = __ldg(p + 1);
+    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      r[2 * i] = __uint_as_float(w[i] << 16);
+      r[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(src) + srow * K + 16 * b);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 v = p[i];
+      r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
+    }
+  }
+}
+
+__device__ __forceinline__ void store_block_terms(int K, int b, size_t orow, const uint32_t (&nat)[kTcTerms][2],
+                                                  const uint32_t (&per)[kTcTerms][2],
+                                                  const uint32_t (&sfo)[kTcTerms], uint8_t* __restrict__ cperm,
+                                                  uint8_t* __restrict__ cnat, uint8_t* __restrict__ sfb) {
+#pragma unroll
+  for (int t = 0; t < kTcTerms; ++t) {
+    const size_t term_row = orow * kTcTerms + t;
+    *reinterpret_cast<uint2*>(cnat + term_row * (K / 2) + 8 * b) = make_uint2(nat[t][0], nat[t][1]);
+    *reinterpret_cast<uint2*>(cperm + term_row * (K / 2) + 8 * b) = make_uint2(per[t][0], per[t][1]);
+    sfb[term_row * (K / 16) + b] = (uint8_t)sfo[t];
+  }
+}
+
+// Grid (source rows, ceil(K / 16 / 128)), 128 threads: one thread expands one 16-element block
+// into kTcTerms NVFP4 terms.  Term t has the fp32 scale g_t = m / (6 * 448) / 4^t, m = the row
+// maximum (given: per token for FC1, per pair from FC1's epilogue for FC2), and a ue4m3 scale per
+// block chosen from the block's current residual, so each term quantises what the previous ones
+// left (a block's residual shrinks at least ~6x per term while g_t shrinks 4x, keeping the block
+// scales in the normal e4m3 range).  Outputs per (output row, term): codes in permuted and natural
+// K order (8 bytes each per block), one ue4m3 scale per block, and g_t.  FC1 expands each token
+// once and writes it to the bucketed rows of its k pairs (inv = pair -> bucketed position); FC2
+// expands each bucketed pair row in place (inv = null, ncopy = 1).
+template <bool BF16_IN>
+__global__ void __launch_bounds__(kTermThreads) act_terms_kernel(int K, const void* __restrict__ src,
+                                                                const int32_t* __restrict__ inv, int ncopy,
+                                                                int out_rows, const float* __restrict__ rowmax,
+                                                                uint8_t* __restrict__ cperm, uint8_t* __restrict__ cnat,
+                                                                uint8_t* __restrict__ sfb, float* __restrict__ gsc) {
+  const int row = blockIdx.x, tid = threadIdx.x;
+  const size_t srow = (size_t)row;
+  const float m = __ldg(rowmax + srow);
+  const float g0 = m / (6.0f * 448.0f);
+  // output rows of this source row (out of range entries are skipped)
+  auto out_row = [&](int cp) -> int {
+    const int r = inv ? __ldg(inv + (size_t)row * ncopy + cp) : row;
+    return r >= 0 && r < out_rows ? r : -1;
+  };
+  if (blockIdx.y == 0 && tid < kTcTerms) {
     for (int cp = 0; cp < ncopy; ++cp) {
       const int orow = out_row(cp);
-      if (orow < 0) continue;
-      const size_t term_row = (size_t)orow * kTcTerms + t;
-      *reinterpret_cast<uint2*>(cnat + term_row * (K / 2) + 8 * b) = make_uint2(nat[0], nat[1]);
-      *reinterpret_cast<uint2*>(cperm + term_row * (K / 2) + 8 * b) = make_uint2(per[0], per[1]);
-      sfb[term_row * (K / 16) + b] = (uint8_t)sf;
+      if (orow >= 0) gsc[(size_t)orow * kTcTerms + tid] = ldexpf(g0, -2 * tid);
     }
+  }
+  const int b = blockIdx.y * kTermThreads + tid;            // 16-element block of the row
+  if (b >= K / 16) return;
+  float r[16];
+  load_block<BF16_IN>(src, srow, K, b, r);
+  uint32_t nat[kTcTerms][2], per[kTcTerms][2], sfo[kTcTerms];
+  block_terms(r, g0, nat, per, sfo);
+  for (int cp = 0; cp < ncopy; ++cp) {
+    const int orow = out_row(cp);
+    if (orow >= 0) store_block_terms(K, b, (size_t)orow, nat, per, sfo, cperm, cnat, sfb);
+  }
+}
+
+// The same expansion for the term rows of a work-item list (the prefill regime's experts with few
+// pairs): term row j belongs to slot j % kTcTok of item j / kTcTok, i.e. to the pair at bucketed
+// position offsets[e] + first + j % kTcTok (rows past the item's count are not written).  The
+// source row is the pair's token (FC1, bf16 x, row maximum per token) or the pair's bucketed
+// position (FC2, fp32 h, row maximum per pair).  Grid-stride over (row, 16-element block).
+template <bool BF16_IN>
+__global__ void __launch_bounds__(256) act_terms_items_kernel(int K, const void* __restrict__ src,
+                                                             const int* __restrict__ n_items,
+                                                             const int4* __restrict__ chunks,
+                                                             const int32_t* __restrict__ offsets,
+                                                             const int32_t* __restrict__ perm, int k, int pairs,
+                                                             const float* __restrict__ rowmax,
+                                                             uint8_t* __restrict__ cperm, uint8_t* __restrict__ cnat,
+                                                             uint8_t* __restrict__ sfb, float* __restrict__ gsc) {
+  const int nb = K / 16;
+  const long long total = (long long)__ldg(n_items) * kTcTok * nb;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int row = (int)(idx / nb), b = (int)(idx - (long long)row * nb);
+    const int4 ch = __ldg(chunks + row / kTcTok);
+    const int slot = row % kTcTok;
+    if (slot >= ch.z) continue;
+    const int pos = __ldg(offsets + ch.x) + ch.y + slot;
+    const int p = pos >= 0 && pos < pairs ? __ldg(perm + pos) : -1;
+    if (p < 0 || p >= pairs) {
+      record_error(MOET_ERR_DEVICE_INDEX);
+      continue;
+    }
+    const size_t srow = BF16_IN ? (size_t)(p / k) : (size_t)pos;
+    const float g0 = __ldg(rowmax + srow) / (6.0f * 448.0f);
+    if (b == 0) {
+#pragma unroll
+      for (int t = 0; t < kTcTerms; ++t) gsc[(size_t)row * kTcTerms + t] = ldexpf(g0, -2 * t);
+    }
+    float r[16];
+    load_block<BF16_IN>(src, srow, K, b, r);
+    uint32_t nat[kTcTerms][2], per[kTcTerms][2], sfo[kTcTerms];
+    block_terms(r, g0, nat, per, sfo);
+    store_block_terms(K, b, (size_t)row, nat, per, sfo, cperm, cnat, sfb);
   }
 }
 
@@ -238,6 +314,8 @@ struct FcTcArgs {
   const float* gsc;
   float* out;
   unsigned* hmax;                // FC1: max |h| per bucketed pair (fp32 bits), for the FC2 terms
+  int item_rows;                 // 1: activation-term rows at item * kTcTok (act_terms_items_kernel),
+                                 // 0: at the pair's bucketed position
 };
 
 // One unit of work = (work item, 128-row weight tile), written by the scheduler warp.
@@ -247,7 +325,8 @@ struct UnitMeta {
   int nch;                       // stages: ceil(K/512) plane stages (+ K/256 delta stages)
   int r0, r1;                    // first weight rows of the tile's two 64-row halves
   float sc2;                     // the expert's scale_2
-  int pad[7];
+  int crow0;                     // first activation-term source row of the item
+  int pad[6];
   int pair[kTcTok];              // pair id t k + j per token column (-1 = none)
   float wts[kTcTok];             // routing weight per token column
   float gate_f[kTcTok];          // 1 = the delta counts for this column
@@ -307,6 +386,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
   UnitMeta* meta = reinterpret_cast<UnitMeta*>(base + kRaw * kRawBytes + kXchgBytes);
   TcSmem& sm = *reinterpret_cast<TcSmem*>(meta + kMeta);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int wl = wait_limit();
   const int total_units = a.hdr[0] * a.tiles;
   const int nunits = (int)blockIdx.x < total_units ? (total_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
   if (nunits == 0) return;
@@ -338,17 +418,17 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
     bool bad = false;
     for (int j = 0; j < nunits && !bad; ++j) {
       const int m = j % kMeta;
-      if (!mbar_wait_warp(&sm.meta_full[m], (j / kMeta) & 1)) { bad = true; break; }
+      if (!mbar_wait_warp(&sm.meta_full[m], (j / kMeta) & 1, wl)) { bad = true; break; }
       const UnitMeta& um = meta[m];
-      const int pos0 = um.pos0, nch = um.nch, dslot = um.dslot;
+      const int nch = um.nch, dslot = um.dslot;
       const int nbox = um.ncols / 16;
       const int y0 = (dslot >= 0 ? dslot : um.e) * a.N;      // delta rows only used by delta stages
       const int w0 = um.e * a.N + um.r0, w1 = um.e * a.N + um.r1;
-      const int trow0 = pos0 * kTcTerms;                    // first activation-term row of the item
+      const int trow0 = um.crow0 * kTcTerms;                // first activation-term row of the item
       for (int c = 0; c < nch; ++c, ++g) {
         if ((g & 1) != pw) continue;
         const int rs = g % kRaw, ru = g / kRaw;
-        if (ru > 0 && !mbar_wait_warp(&sm.done[rs], (ru - 1) & 1)) { bad = true; break; }
+        if (ru > 0 && !mbar_wait_warp(&sm.done[rs], (ru - 1) & 1, wl)) { bad = true; break; }
         unsigned char* st = raw + rs * kRawBytes;
         uint64_t* fb = &sm.full[rs];
         const bool dp = c >= nps;
@@ -411,7 +491,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
     // every copy this warp issued has landed before the CTA may exit
     if (lane == 0)
       for (int i = g > kRaw ? g - kRaw : 0; i < g; ++i)
-        if ((i & 1) == pw) mbar_wait(&sm.full[i % kRaw], (i / kRaw) & 1);
+        if ((i & 1) == pw) mbar_wait(&sm.full[i % kRaw], (i / kRaw) & 1, wl);
   } else if (warp == 1) {
     // ---------------- MMA issue
     if (lane == 0) {
@@ -419,8 +499,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
       bool bad = false;
       for (int j = 0; j < nunits && !bad; ++j) {
         const int m = j % kMeta, ab = j & 1;
-        if (!mbar_wait(&sm.meta_full[m], (j / kMeta) & 1)) { bad = true; break; }
-        if (j >= 2 && !mbar_wait(&sm.acc_empty[ab], ((j >> 1) - 1) & 1)) { bad = true; break; }
+        if (!mbar_wait(&sm.meta_full[m], (j / kMeta) & 1, wl)) { bad = true; break; }
+        if (j >= 2 && !mbar_wait(&sm.acc_empty[ab], ((j >> 1) - 1) & 1, wl)) { bad = true; break; }
         if (is_stuck(sm)) { bad = true; break; }
         asm volatile("tcgen05.fence::after_thread_sync;");
         const int nch = meta[m].nch;
@@ -428,7 +508,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
         const uint32_t dcol = tmem + 128 * ab;
         for (int c = 0; c < nch; ++c, ++g) {
           const int as = g % kAst, au = g / kAst, rs = g % kRaw;
-          if (!mbar_wait(&sm.staged[as], au & 1)) { bad = true; break; }
+          if (!mbar_wait(&sm.staged[as], au & 1, wl)) { bad = true; break; }
           asm volatile("tcgen05.fence::after_thread_sync;");
           const uint32_t rsm = smem_addr(raw + rs * kRawBytes);
           const uint32_t sfa = tmem + kColSFA + 32 * as, sfb = tmem + kColSFB + 32 * as;
@@ -456,13 +536,13 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
       }
       if (bad) set_stuck(sm);
       // every MMA this thread issued is complete before TMEM is released
-      if (last >= 0) mbar_wait(&sm.done[last % kRaw], (last / kRaw) & 1);
+      if (last >= 0) mbar_wait(&sm.done[last % kRaw], (last / kRaw) & 1, wl);
     }
   } else if (warp == 2) {
     // ---------------- scheduler
     for (int j = 0; j < nunits; ++j) {
       const int m = j % kMeta;
-      if (j >= kMeta && !mbar_wait_warp(&sm.meta_empty[m], ((j / kMeta) - 1) & 1)) {
+      if (j >= kMeta && !mbar_wait_warp(&sm.meta_empty[m], ((j / kMeta) - 1) & 1, wl)) {
         if (lane == 0) set_stuck(sm);
         break;
       }
@@ -473,6 +553,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
       const int e = ch.x, ntok = ch.z;
       const int pe = ch.w;                 // pool slot of the expert's planes and scale_2
       const int pos0 = __ldg(a.offsets + e) + ch.y;
+      const int crow0 = a.item_rows ? item * kTcTok : pos0;
       int dslot = -1;
       if (a.delta_slot != nullptr && a.gate != nullptr) {
         dslot = __ldg(a.delta_slot + e);
@@ -500,10 +581,10 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
       for (int h2 = 0; h2 < 2; ++h2) {
         const int col = lane + 32 * h2, tk = col / kTcTerms;
         const int ptk = __shfl_sync(0xffffffffu, pr, tk);
-        um.gsc[col] = tk < ntok && ptk >= 0 ? __ldg(a.gsc + (size_t)(pos0 + tk) * kTcTerms + col % kTcTerms) : 0.0f;
+        um.gsc[col] = tk < ntok && ptk >= 0 ? __ldg(a.gsc + (size_t)(crow0 + tk) * kTcTerms + col % kTcTerms) : 0.0f;
       }
       if (lane == 0) {
-        um.e = pe; um.pos0 = pos0; um.ntok = ntok;
+        um.e = pe; um.pos0 = pos0; um.ntok = ntok; um.crow0 = crow0;
         um.ncols = ((kTcTerms * ntok + 15) / 16) * 16;
         um.dslot = dslot;
         um.nch = dslot >= 0 ? nps + a.K / kKD : nps;
@@ -512,7 +593,9 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
         um.sc2 = __ldg(a.scale_2 + pe);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.meta_full[m]);
+      // (a test can make CTA 0 withhold its first record: every wait on it then runs out)
+      const bool withhold = blockIdx.x == 0 && j == 0 && *reinterpret_cast<volatile int*>(&g_dbg_withhold) != 0;
+      if (lane == 0 && !withhold) mbar_arrive(&sm.meta_full[m]);
     }
   } else if (warp >= 4 && warp < 8) {
     // ---------------- epilogue: TMEM lane quarter warp & 3
@@ -520,8 +603,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
     const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;
     for (int j = 0; j < nunits; ++j) {
       const int m = j % kMeta, ab = j & 1;
-      bool ok = mbar_wait_warp(&sm.meta_full[m], (j / kMeta) & 1);
-      ok = ok && mbar_wait_warp(&sm.acc_full[ab], (j >> 1) & 1);
+      bool ok = mbar_wait_warp(&sm.meta_full[m], (j / kMeta) & 1, wl);
+      ok = ok && mbar_wait_warp(&sm.acc_full[ab], (j >> 1) & 1, wl);
       asm volatile("tcgen05.fence::after_thread_sync;");
       if (epi_any(!ok || is_stuck(sm))) {
         if (!ok && lane == 0) set_stuck(sm);
@@ -609,14 +692,14 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
     bool bad = false;
     for (int j = 0; j < nunits && !bad; ++j) {
       const int m = j % kMeta;
-      if (!mbar_wait_warp(&sm.meta_full[m], (j / kMeta) & 1)) { bad = true; break; }
+      if (!mbar_wait_warp(&sm.meta_full[m], (j / kMeta) & 1, wl)) { bad = true; break; }
       if (__any_sync(0xffffffffu, is_stuck(sm))) { bad = true; break; }
       const int nch = meta[m].nch, ncols = meta[m].ncols;
       for (int c = 0; c < nch; ++c, ++g) {
         const int rs = g % kRaw, ru = g / kRaw, as = g % kAst;
-        if (!mbar_wait_warp(&sm.full[rs], ru & 1)) { bad = true; break; }
+        if (!mbar_wait_warp(&sm.full[rs], ru & 1, wl)) { bad = true; break; }
         // the A stage is free once the MMAs of stage g - kAst are done
-        if (g >= kAst && !mbar_wait_warp(&sm.done[(g - kAst) % kRaw], ((g - kAst) / kRaw) & 1)) { bad = true; break; }
+        if (g >= kAst && !mbar_wait_warp(&sm.done[(g - kAst) % kRaw], ((g - kAst) / kRaw) & 1, wl)) { bad = true; break; }
         const bool dp = c >= nps;
         const int nsub = dp ? 1 : min(2, (a.K - kKC * c) / kKD);
         if (grp < nsub) {
@@ -708,48 +791,85 @@ moet_status launch_fc_tc(const FcTcArgs& a, const moet_planes* pl, const moet_nv
 
 }  // namespace
 
-moet_status tc_forward(const TcForwardArgs& f, cudaStream_t st) {
-  const int pairs = f.T * f.k;
-  // FC1 input terms: each token once, written to the bucketed rows of its k pairs so that a
-  // work item's term rows are consecutive
-  {
-    ProfScope ps(MOET_K_TERMS, st);
-    const dim3 grid(f.T, (f.H / 16 + kTermThreads - 1) / kTermThreads);
-    act_terms_kernel<true><<<grid, kTermThreads, 0, st>>>(f.H, f.x, f.inv, f.k, pairs, f.tokmax, f.buf.x_cperm,
-                                                          f.buf.x_cnat, f.buf.x_sf, f.buf.x_g);
-  }
-  MOET_CUDA_TRY(cudaGetLastError());
+namespace {
+FcTcArgs common_args(const TcForwardArgs& f) {
   FcTcArgs a{};
   a.T = f.T; a.H = f.H; a.I = f.I; a.k = f.k;
   a.offsets = f.offsets; a.perm = f.perm; a.topk_w = f.topk_w;
   a.delta_slot = f.delta_slot; a.n_slots = f.n_slots; a.gate = f.gate;
   a.hdr = f.hdr; a.chunks = f.chunks;
-  FcTcArgs a1 = a;
+  a.item_rows = f.item_rows;
+  return a;
+}
+
+// Grid of the item-mode terms kernel: resident CTAs over all SMs.
+int items_grid() {
+  const int sms = sm_count();
+  return (sms > 0 ? sms : 152) * 8;
+}
+}  // namespace
+
+moet_status tc_forward_fc1(const TcForwardArgs& f, cudaStream_t st) {
+  const int pairs = f.T * f.k;
+  {
+    ProfScope ps(MOET_K_TERMS, st);
+    if (f.item_rows) {
+      // FC1 input terms of the items' pairs, at item * kTcTok + slot
+      act_terms_items_kernel<true><<<items_grid(), 256, 0, st>>>(f.H, f.x, f.hdr, f.chunks, f.offsets, f.perm, f.k,
+                                                                 pairs, f.tokmax, f.buf.x_cperm, f.buf.x_cnat,
+                                                                 f.buf.x_sf, f.buf.x_g);
+    } else {
+      // each token once, written to the bucketed rows of its k pairs so that a work item's term
+      // rows are consecutive
+      const dim3 grid(f.T, (f.H / 16 + kTermThreads - 1) / kTermThreads);
+      act_terms_kernel<true><<<grid, kTermThreads, 0, st>>>(f.H, f.x, f.inv, f.k, pairs, f.tokmax, f.buf.x_cperm,
+                                                            f.buf.x_cnat, f.buf.x_sf, f.buf.x_g);
+    }
+  }
+  MOET_CUDA_TRY(cudaGetLastError());
+  FcTcArgs a1 = common_args(f);
   a1.K = f.H; a1.N = 2 * f.I;
   a1.scale_2 = f.fc1->scale_2;
   a1.gsc = f.buf.x_g;
   a1.out = f.h;
   a1.hmax = f.hmax;
-  moet_status s = launch_fc_tc<true>(a1, f.fc1, f.dfc1, f.buf.x_cperm, f.buf.x_cnat, f.buf.x_sf, pairs, f.E,
-                                     f.I / 64, st);
-  if (s != MOET_OK) return s;
-  // FC2 input terms: one row per bucketed pair (h rows are in bucketed order)
+  return launch_fc_tc<true>(a1, f.fc1, f.dfc1, f.buf.x_cperm, f.buf.x_cnat, f.buf.x_sf, f.act_rows, f.E, f.I / 64,
+                            st);
+}
+
+moet_status tc_forward_fc2(const TcForwardArgs& f, cudaStream_t st) {
+  const int pairs = f.T * f.k;
   {
     ProfScope ps(MOET_K_TERMS, st);
-    const dim3 grid(pairs, (f.I / 16 + kTermThreads - 1) / kTermThreads);
-    act_terms_kernel<false><<<grid, kTermThreads, 0, st>>>(f.I, f.h, nullptr, 1, pairs,
-                                                           reinterpret_cast<const float*>(f.hmax), f.buf.h_cperm,
-                                                           f.buf.h_cnat, f.buf.h_sf, f.buf.h_g);
+    if (f.item_rows) {
+      act_terms_items_kernel<false><<<items_grid(), 256, 0, st>>>(f.I, f.h, f.hdr, f.chunks, f.offsets, f.perm, f.k,
+                                                                  pairs, reinterpret_cast<const float*>(f.hmax),
+                                                                  f.buf.h_cperm, f.buf.h_cnat, f.buf.h_sf, f.buf.h_g);
+    } else {
+      // one row per bucketed pair (h rows are in bucketed order)
+      const dim3 grid(pairs, (f.I / 16 + kTermThreads - 1) / kTermThreads);
+      act_terms_kernel<false><<<grid, kTermThreads, 0, st>>>(f.I, f.h, nullptr, 1, pairs,
+                                                             reinterpret_cast<const float*>(f.hmax), f.buf.h_cperm,
+                                                             f.buf.h_cnat, f.buf.h_sf, f.buf.h_g);
+    }
   }
   MOET_CUDA_TRY(cudaGetLastError());
-  FcTcArgs a2 = a;
+  FcTcArgs a2 = common_args(f);
   a2.K = f.I; a2.N = f.H;
   a2.scale_2 = f.fc2->scale_2;
   a2.gsc = f.buf.h_g;
   a2.out = f.o;
-  return launch_fc_tc<false>(a2, f.fc2, f.dfc2, f.buf.h_cperm, f.buf.h_cnat, f.buf.h_sf, pairs, f.E, f.H / 128, st);
+  return launch_fc_tc<false>(a2, f.fc2, f.dfc2, f.buf.h_cperm, f.buf.h_cnat, f.buf.h_sf, f.act_rows, f.E, f.H / 128,
+                             st);
+}
+
+moet_status tc_forward(const TcForwardArgs& f, cudaStream_t st) {
+  const moet_status s = tc_forward_fc1(f, st);
+  if (s != MOET_OK) return s;
+  return tc_forward_fc2(f, st);
 }
 
 }  // namespace moet
 
 MOET_ERROR_ACCESSOR(moet_internal_error_moe_tc)
+MOET_DEBUG_WAITS_SETTER(moet_internal_debug_waits_moe_tc)

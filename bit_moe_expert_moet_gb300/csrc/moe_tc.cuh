@@ -41,6 +41,10 @@ struct TcForwardArgs {
   const uint8_t* gate;         // nullable
   const int* hdr;              // [0] = number of work items
   const int4* chunks;          // (expert, first pair, count <= kTcTok, pool slot of the planes)
+  int item_rows;               // 1: activation-term rows at item * kTcTok + slot (act_rows =
+                               //    kTcTok x the item-list capacity); 0: at the pair's bucketed
+                               //    position (act_rows = T k)
+  int act_rows;                // activation-term source rows the term buffers hold
   float* h;                    // [T k, I] bucketed
   float* o;                    // [T k, H] pair order
   const float* tokmax;         // [T] max |x_t| (written by the prologue)
@@ -50,6 +54,9 @@ struct TcForwardArgs {
   int max_items;
 };
 
+// FC1 (its input terms, then the FC kernel) and FC2 (the same); tc_forward runs both.
+moet_status tc_forward_fc1(const TcForwardArgs& a, cudaStream_t st);
+moet_status tc_forward_fc2(const TcForwardArgs& a, cudaStream_t st);
 moet_status tc_forward(const TcForwardArgs& a, cudaStream_t st);
 
 }  // namespace moet

@@ -13,69 +13,6 @@
 
 namespace moet {
 
-// ---------------------------------------------------------------- requant
-__global__ void __launch_bounds__(256) requant_2bit_kernel(
-    long long n_groups, const uint4* __restrict__ codes, const uint16_t* __restrict__ s4,
-    uint32_t* __restrict__ sign_out, uint32_t* __restrict__ mag_out,
-    uint16_t* __restrict__ s16_out, uint4* __restrict__ dcodes_out,
-    uint16_t* __restrict__ ds4_out) {
-  long long gi = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (; gi < n_groups; gi += stride) {
-    const uint4 cw = __ldg(codes + gi);
-    const uint32_t sc = __ldg(s4 + gi);
-    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-    uint32_t sign = 0, mag = 0, s16pair = 0, ds4pair = 0;
-    uint32_t dwords[4] = {0, 0, 0, 0};
-#pragma unroll
-    for (int b = 0; b < 2; ++b) {  // two blocks of 16 per 32-weight group
-      const float s4f = e4m3_to_f32((sc >> (8 * b)) & 0xFFu);
-      float v[16];
-      float bmax = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const uint32_t c = (words[2 * b + (j >> 3)] >> (4 * (j & 7))) & 0xFu;
-        const float a = e2m1_mag_value(c & 7u) * s4f;  // exact
-        v[j] = (c & 8u) ? -a : a;
-        bmax = fmaxf(bmax, a);
-        sign |= (c >> 3) << (16 * b + j);
-      }
-      const uint32_t s16 = e4m3_rne_ratio_small(bmax, 3.0f);
-      const float s16f = e4m3_to_f32(s16);
-      s16pair |= s16 << (8 * b);
-      float d[16];
-      float dmax = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const uint32_t m = fabsf(v[j]) >= 2.0f * s16f;
-        mag |= m << (16 * b + j);
-        const float q = (m ? 3.0f : 1.0f) * s16f;
-        const float w2 = ((sign >> (16 * b + j)) & 1u) ? -q : q;
-        d[j] = v[j] - w2;  // exact in fp32 (short dyadics of nearby magnitude)
-        dmax = fmaxf(dmax, fabsf(d[j]));
-      }
-      if (dcodes_out != nullptr) {
-        const uint32_t ds4 = e4m3_rne_ratio_small(dmax, 6.0f);
-        const float dsf = e4m3_to_f32(ds4);
-        ds4pair |= ds4 << (8 * b);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const uint32_t dm = dsf > 0.0f ? e2m1_rne_mag(fabsf(d[j]), dsf) : 0u;
-          const uint32_t code = dm | ((d[j] < 0.0f && dm != 0u) ? 8u : 0u);
-          dwords[2 * b + (j >> 3)] |= code << (4 * (j & 7));
-        }
-      }
-    }
-    sign_out[gi] = sign;
-    mag_out[gi] = mag;
-    s16_out[gi] = (uint16_t)s16pair;
-    if (dcodes_out != nullptr) {
-      dcodes_out[gi] = make_uint4(dwords[0], dwords[1], dwords[2], dwords[3]);
-      ds4_out[gi] = (uint16_t)ds4pair;
-    }
-  }
-}
-
 // ---------------------------------------------------------------- requant, planes only
 // Fast path without the delta.  All 16 weights of a block share s4, so
 // v = e2m1(code) * s4 is monotone in the magnitude code: max|v| is the value of
@@ -626,6 +563,108 @@ __global__ void __launch_bounds__(256) requant_mxfp4_kernel(
   }
 }
 
+// ---------------------------------------------------------------- NVFP4 -> planes + delta by tables
+// All 16 weights of an NVFP4 block share s4, so every decision of the rule inside a block --
+// s16 (from the largest magnitude code), the |q| = 3 threshold code, the delta scale (from the
+// largest |d| over the magnitude codes present) and the delta code of each magnitude code -- is a
+// function of (s4, the set of magnitude codes present).  requant_delta_lut_kernel evaluates the
+// rule once per such pair into g_requant_lut, in fp32, exactly: v = e2m1 x s4 and q s16 are short
+// dyadics a few binades apart, so d = v - q s16 is exact, and both e4m3 roundings and the e2m1
+// rounding compare doubled midpoints exactly; requant_delta_kernel then gives each weight its planes and delta code with
+// integer operations (presence by borrow tests, bit gathers by multiplies, codes by byte
+// permutes).  The table is rebuilt by every call (32 K entries, a few microseconds), so nothing
+// depends on state left by an earlier call.
+//   entry (s4 & 0x7F) * 256 + present:  x, y = delta code bytes of magnitude codes 0-3 / 4-7
+//   for a positive weight;  z = s16 | ds4 << 8 | threshold code << 16
+constexpr int kLutEntries = 128 * 256;
+static __device__ uint4 g_requant_lut[kLutEntries];
+
+__global__ void __launch_bounds__(256) requant_delta_lut_kernel() {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= kLutEntries) return;
+  const uint32_t sc = (uint32_t)i >> 8, pres = (uint32_t)i & 0xFFu;
+  if (pres == 0u) {                       // never looked up: a block always holds some code
+    g_requant_lut[i] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  const float s4f = e4m3_to_f32(sc);
+  const uint32_t mc = 31u - (uint32_t)__clz(pres);
+  const uint32_t s16 = e4m3_rne_ratio_small(e2m1_mag_value(mc) * s4f, 3.0f);
+  const float s16f = e4m3_to_f32(s16);
+  uint32_t thr = 0;
+#pragma unroll
+  for (uint32_t c = 0; c < 8; ++c) thr += (e2m1_mag_value(c) * s4f < 2.0f * s16f) ? 1u : 0u;
+  float d[8];
+  float dmax = 0.0f;
+#pragma unroll
+  for (uint32_t c = 0; c < 8; ++c) {
+    const float q = (c >= thr ? 3.0f : 1.0f) * s16f;
+    d[c] = e2m1_mag_value(c) * s4f - q;                      // exact (short dyadics)
+    if ((pres >> c) & 1u) dmax = fmaxf(dmax, fabsf(d[c]));
+  }
+  const uint32_t ds4 = e4m3_rne_ratio_small(dmax, 6.0f);
+  const float dsf = e4m3_to_f32(ds4);
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (uint32_t c = 0; c < 8; ++c) {
+    const uint32_t dm = dsf > 0.0f ? e2m1_rne_mag(fabsf(d[c]), dsf) : 0u;
+    const uint32_t code = dm | ((d[c] < 0.0f && dm != 0u) ? 8u : 0u);
+    if (c < 4) lo |= code << (8 * c);
+    else hi |= code << (8 * (c - 4));
+  }
+  g_requant_lut[i] = make_uint4(lo, hi, s16 | (ds4 << 8) | (thr << 16), 0u);
+}
+
+// Thread t of a CTA handles groups base + u * blockDim + t (u < kGroupsPerIter), as the planes-only
+// kernel; per 16-block one table entry.
+__global__ void __launch_bounds__(256) requant_delta_kernel(
+    long long n_groups, const uint4* __restrict__ codes, const uint16_t* __restrict__ s4,
+    uint32_t* __restrict__ sign_out, uint32_t* __restrict__ mag_out, uint16_t* __restrict__ s16_out,
+    uint4* __restrict__ dcodes_out, uint16_t* __restrict__ ds4_out) {
+  const long long span = (long long)blockDim.x * kGroupsPerIter;
+  for (long long base = (long long)blockIdx.x * span; base < n_groups; base += (long long)gridDim.x * span) {
+    uint4 cw[kGroupsPerIter];
+    uint32_t sc[kGroupsPerIter];
+#pragma unroll
+    for (int u = 0; u < kGroupsPerIter; ++u) {
+      const long long gi = base + (long long)u * blockDim.x + threadIdx.x;
+      if (gi < n_groups) {
+        cw[u] = __ldg(codes + gi);
+        sc[u] = __ldg(s4 + gi);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kGroupsPerIter; ++u) {
+      const long long gi = base + (long long)u * blockDim.x + threadIdx.x;
+      if (gi >= n_groups) break;
+      const uint32_t w[4] = {cw[u].x, cw[u].y, cw[u].z, cw[u].w};
+      uint32_t mr[4], dw[4], s16pair = 0, ds4pair = 0;
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        const uint32_t wa = w[2 * b], wb = w[2 * b + 1];
+        const uint32_t pres = codes_present(wa, wb);
+        const uint4 e = g_requant_lut[(((sc[u] >> (8 * b)) & 0x7Fu) << 8) | pres];
+        s16pair |= (e.z & 0xFFu) << (8 * b);
+        ds4pair |= ((e.z >> 8) & 0xFFu) << (8 * b);
+        const uint32_t T = (e.z >> 16) * 0x11111111u;             // |q| = 3 iff magnitude code >= threshold
+        mr[2 * b] = gather_bit3(((wa | 0x88888888u) - T) & 0x88888888u);
+        mr[2 * b + 1] = gather_bit3(((wb | 0x88888888u) - T) & 0x88888888u);
+        // byte c of (flo, fhi) = 8 when magnitude code c has a nonzero delta magnitude
+        const uint32_t flo = ((e.x & 0x07070707u) + 0x07070707u) & 0x08080808u;
+        const uint32_t fhi = ((e.y & 0x07070707u) + 0x07070707u) & 0x08080808u;
+        dw[2 * b] = delta_from_tables(wa, e.x, e.y, flo, fhi);
+        dw[2 * b + 1] = delta_from_tables(wb, e.x, e.y, flo, fhi);
+      }
+      sign_out[gi] = assemble_bits(gather_bit3(w[0] & 0x88888888u), gather_bit3(w[1] & 0x88888888u),
+                                   gather_bit3(w[2] & 0x88888888u), gather_bit3(w[3] & 0x88888888u));
+      mag_out[gi] = assemble_bits(mr[0], mr[1], mr[2], mr[3]);
+      s16_out[gi] = (uint16_t)s16pair;
+      dcodes_out[gi] = make_uint4(dw[0], dw[1], dw[2], dw[3]);
+      ds4_out[gi] = (uint16_t)ds4pair;
+    }
+  }
+}
+
 extern "C" moet_status moet_requant_mxfp4_2bit(int M, int N, int K, const uint8_t* codes, const uint8_t* e8m0,
                                                float* scale_2, uint32_t* sign, uint32_t* mag, uint8_t* s16,
                                                uint8_t* dcodes, uint8_t* ds4, moet_stream stream) {
@@ -702,8 +741,9 @@ extern "C" moet_status moet_requant_2bit(int M, int N, int K, const uint8_t* cod
       requant_planes_kernel<<<g, 256, 0, (cudaStream_t)stream>>>(
           n_groups, (const uint4*)codes, (const uint16_t*)s4, sign, mag, (uint16_t*)s16);
     } else {
-      const int g = resident_grid(requant_2bit_kernel, 256, n_groups);
-      requant_2bit_kernel<<<g, 256, 0, (cudaStream_t)stream>>>(
+      requant_delta_lut_kernel<<<kLutEntries / 256, 256, 0, (cudaStream_t)stream>>>();
+      const int g = resident_grid(requant_delta_kernel, 256, (n_groups + kGroupsPerIter - 1) / kGroupsPerIter);
+      requant_delta_kernel<<<g, 256, 0, (cudaStream_t)stream>>>(
           n_groups, (const uint4*)codes, (const uint16_t*)s4, sign, mag, (uint16_t*)s16,
           (uint4*)dcodes, (uint16_t*)ds4);
     }

@@ -12,6 +12,16 @@ namespace moet {
 namespace {
 
 constexpr int kWaitLimit = 1 << 20;           // polls before a wait is declared stuck
+// Test control of the engines' waits (moet_debug_wait_expiry): a shorter poll limit and a
+// request that CTA 0 withhold its first unit record, so that every wait on that record runs out.
+// Off (0) unless a test sets it; it can only shorten the waits.
+static __device__ int g_dbg_wait_limit = 0;
+static __device__ int g_dbg_withhold = 0;
+
+__device__ __forceinline__ int wait_limit() {
+  const int v = *reinterpret_cast<volatile int*>(&g_dbg_wait_limit);
+  return v > 0 && v < kWaitLimit ? v : kWaitLimit;
+}
 constexpr uint32_t kSuspendNs = 2000;         // suspend-time hint of one poll (the warp sleeps
                                               // until the phase completes or the hint expires)
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -32,10 +42,11 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
 }
 
-// Bounded wait for the mbarrier phase with the given parity; false if it gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Bounded wait for the mbarrier phase with the given parity; false if it gave up after `limit`
+// polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int limit) {
   const uint32_t a = smem_addr(bar);
-  for (int it = 0; it < kWaitLimit; ++it) {
+  for (int it = 0; it < limit; ++it) {
     uint32_t done;
     asm volatile(
         "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
@@ -86,9 +97,9 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 }
 
 // Warp-uniform bounded wait: true once every lane has seen the phase complete.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int limit) {
   const uint32_t a = smem_addr(bar);
-  for (int it = 0; it < kWaitLimit; ++it) {
+  for (int it = 0; it < limit; ++it) {
     uint32_t done;
     asm volatile(
         "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
@@ -157,3 +168,12 @@ int sm_count() {
 
 }  // namespace
 }  // namespace moet
+
+// Defines `int name(int polls, int withhold)`: sets this unit's wait controls (blocking copies).
+// Returns -1 if a copy fails.
+#define MOET_DEBUG_WAITS_SETTER(name)                                                           \
+  extern "C" __attribute__((visibility("hidden"))) int name(int polls, int withhold) {          \
+    if (cudaMemcpyToSymbol(moet::g_dbg_wait_limit, &polls, sizeof(int)) != cudaSuccess) return -1; \
+    if (cudaMemcpyToSymbol(moet::g_dbg_withhold, &withhold, sizeof(int)) != cudaSuccess) return -1; \
+    return 0;                                                                                    \
+  }

@@ -312,6 +312,28 @@ moet_status moet_moe_forward_static(int T, int H, int I, int E, int k, const uin
                                     moet_stream stream);
 
 /* ------------------------------------------------------------------------
+ * moet_debug_wait_expiry -- test control of the forward engines' bounded waits.
+ * The two tcgen05 engines (the block-scaled decode engine and the bf16 prefill
+ * engine behind moet_moe_forward) hand work between warps through mbarriers;
+ * every wait polls at most 2^20 times (each poll suspended for at most about
+ * 2 us).  A wait that runs out marks the CTA stuck: every warp role leaves
+ * its loop, the copy and MMA issuers wait (bounded) for what they have in
+ * flight, TMEM is released, and MOET_ERR_TIMEOUT is recorded for
+ * moet_last_device_error; the outputs of that launch are unspecified, the
+ * context stays usable.  This control lets a test drive that path:
+ *   polls     > 0 lowers the poll bound of every wait to `polls` (a value at
+ *             or above the default leaves it unchanged); 0 restores it.
+ *   withhold  1 makes CTA 0 of every engine launch skip publishing its first
+ *             unit record, so that every wait on that record runs out;
+ *             0 (the default) publishes every record.
+ * The setting holds for later launches until changed.  Returns
+ * MOET_ERR_INVALID_ARG for polls < 0 or withhold not 0/1, MOET_ERR_CUDA if
+ * the setting cannot be copied to the current device.  Blocking; not for use
+ * during stream capture.  Not a part of the layer computation: the pages
+ * describe no such control. */
+moet_status moet_debug_wait_expiry(int polls, int withhold);
+
+/* ------------------------------------------------------------------------
  * Kernel timing (tracing aid, off by default).  While enabled, the library
  * records a CUDA event before and after each of its kernel launches on the
  * launching stream (so timings are on-device and per launch; leave it off

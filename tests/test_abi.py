@@ -121,3 +121,8 @@ def test_static_scratch_size_matches_header(lib):
         m = re.search(r"#define\s+MOET_FORWARD_STATIC_SCRATCH_BYTES\s+\(\(size_t\)(\d+)\s*<<\s*(\d+)\)", f.read())
     assert m is not None
     assert _lib.FORWARD_STATIC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+
+
+def test_debug_wait_expiry_rejects_bad_arguments(lib):
+    assert lib.moet_debug_wait_expiry(-1, 0) == 1          # INVALID_ARG, nothing copied
+    assert lib.moet_debug_wait_expiry(0, 2) == 1
