@@ -52,7 +52,7 @@ constexpr int kTcMaxT = 512;
 // Prefill regime (T > kTcMaxT): an expert routed at most this many pairs is a weight stream with
 // few tokens, where the bf16 engine's 128-row tiles would cost as much as for 256 pairs; its pairs
 // go through the block-scaled decode engine in items of kTcTok instead (a second work list).
-constexpr int kPfSmallMax = 64;
+constexpr int kPfSmallMax = 32;
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 

@@ -147,7 +147,11 @@ __device__ __forceinline__ uint32_t h16_bits(float f) {
 
 // 32 weights (sign word S, magnitude word M) with block scales s0 (weights 0-15)
 // and s1 (16-31) -> 16 words: word j = bits (weight j) | bits (weight j + 16) << 16,
-// bf16 (BF) or fp16 (both have the sign in bit 15 of a half).
+// bf16 (BF) or fp16 (both have the sign in bit 15 of a half).  One shift of a plane word by
+// 7 - j puts bits j, j + 8, j + 16, j + 24 at the most significant bits of its four bytes, which
+// serves words j (bytes 0, 2) and j + 8 (bytes 1, 3): a sign-replicating byte permute turns the
+// magnitude bits into half-word masks, and the sign bits sit at bits 15 and 31 already for word
+// j + 8 (for word j after one more byte shift, taken once from S << 8).
 template <bool BF>
 __device__ __forceinline__ void planes_to_16(uint32_t S, uint32_t M, uint32_t s0, uint32_t s1, uint32_t out[16]) {
   const float f0 = e4m3_to_f32(s0), f1 = e4m3_to_f32(s1);
@@ -155,12 +159,14 @@ __device__ __forceinline__ void planes_to_16(uint32_t S, uint32_t M, uint32_t s0
   const uint32_t a1 = h16_bits<BF>(f1), b1 = h16_bits<BF>(3.0f * f1);
   const uint32_t one = a0 | (a1 << 16);                    // q = 1 in both halves
   const uint32_t dif = (a0 ^ b0) | ((a1 ^ b1) << 16);      // q = 1 -> q = 3
+  const uint32_t S8 = S << 8;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    // bits j and j + 16 moved to 15 and 31, the msb of bytes 1 and 3
-    const uint32_t mm = prmt(M << (15 - j), 0u, 0xBB99u);  // sign-replicated bytes -> half-word masks
-    const uint32_t ss = (S << (15 - j)) & 0x80008000u;
-    out[j] = (one ^ (mm & dif)) ^ ss;
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t mj = M << (7 - j), sj = S << (7 - j), s8j = S8 << (7 - j);
+    const uint32_t mlo = prmt(mj, 0u, 0xAA88u);            // bits j, j + 16 -> half-word masks
+    const uint32_t mhi = prmt(mj, 0u, 0xBB99u);            // bits j + 8, j + 24
+    out[j] = (one ^ (mlo & dif)) | (s8j & 0x80008000u);
+    out[j + 8] = (one ^ (mhi & dif)) | (sj & 0x80008000u);
   }
 }
 
