@@ -26,14 +26,15 @@
 // turns the magnitude bits into half-word masks).  The bucketing gather (x)
 // and pf_h16_kernel (h) write the activations in the same K order.
 //
-// Pipeline: one persistent CTA per SM (20 warps) over (work item of <= 256
+// Pipeline: one persistent CTA per SM (24 warps) over (work item of <= 256
 // pairs x 128-row weight tile) units: warp 0 streams 256-weight chunks of the
 // planes (or delta) and warps 3, 16, 18, 19 take turns streaming the steps of the
 // item's activation rows, with TMA (one lane per box); warps 8-15 expand each step's weights into a TMEM A
 // stage (two warps per 32-row quarter); warp 1 issues 4 MMAs
-// per step and commits; warp 2 prepares the unit records; warps 4-7 drain the
-// accumulator (FC1: SiLU(gate) * up -> fp32 h; FC2: times the routing weight and
-// the row's h scale -> fp32 o).  Every wait is bounded.
+// per step and commits; warp 2 prepares the unit records; warps 4-7 and 20-23 (two per
+// lane quarter, alternate 16-column chunks) drain the accumulator (FC1: SiLU(gate) * up ->
+// fp32 h; FC2: times the routing weight, scale_2 and the row's h scale -> fp32 o).  Every wait
+// is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -47,7 +48,8 @@
 namespace moet {
 namespace {
 
-constexpr int kPfThreads = 640;           // 20 warps, roles above
+constexpr int kPfThreads = 768;           // 24 warps, roles above
+constexpr int kPfEpiWarps = 8;            // epilogue warps: two per TMEM lane quarter (4-7, 20-23)
 constexpr int kBProd = 4;                 // activation producer warps (3, 16, 18, 19), steps in turn
 constexpr int kPfConvWarps = 8;
 constexpr int kPC = 256;                  // weights per weight chunk
@@ -68,7 +70,7 @@ static_assert(kPAst % kGrp == 0 && (kPC / 64) % kGrp == 0, "hand-off groups tile
 constexpr int kPChunkBytes = 18432;
 constexpr int kBStepBytes = 32768;        // activation step: [<= 256 rows][128 B] (SW128)
 constexpr int kPBase = 0, kBBase = kPRing * kPChunkBytes;
-constexpr int kPXchg = kBBase + kBRing * kBStepBytes;
+constexpr int kPMisc = kBBase + kBRing * kBStepBytes;      // barriers and unit records
 
 struct PfMaps {
   CUtensorMap sign, mag, q;      // planes u32 [E N, K/32] box {8, 64} SW32; s16 u8 [E N, K/16] box {16, 64}
@@ -100,7 +102,7 @@ struct PfMeta {
   float sc2;
   int pad[7];
   int pair[kPfTok];              // per column (token of the item): pair id t k + j, -1 = none
-  float wts[kPfTok];             // routing weight of the pair
+  float wts[kPfTok];             // FC2: routing weight x scale_2 x h scale of the pair
   uint8_t gated[kPfTok];         // 1 = the pair's token is gated
 };
 static_assert(sizeof(PfMeta) == 64 + 9 * kPfTok, "PfMeta layout");
@@ -117,7 +119,7 @@ struct PfSmem {
   int stuck;
 };
 
-constexpr size_t kPfSmemBytes = 1024 + (size_t)kPXchg + 64 * 16 * sizeof(float) + sizeof(PfSmem);
+constexpr size_t kPfSmemBytes = 1024 + (size_t)kPMisc + sizeof(PfSmem);
 static_assert(kPfSmemBytes <= 232448, "shared memory over the per-CTA limit");
 
 __device__ __forceinline__ bool pf_stuck(const PfSmem& sm) {
@@ -130,6 +132,15 @@ template <bool BF>
 __device__ __forceinline__ uint32_t f16_idesc(int n) {
   const uint32_t t = BF ? 1u : 0u;
   return (1u << 4) | (t << 7) | (t << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+// Row of the weight chunk (gate rows 0-63, up rows 64-127 for FC1; output rows for FC2) held by
+// TMEM lane t.  FC1 interleaves them per lane quarter: lanes 0-15 of quarter q hold gate rows
+// 16 q .. 16 q + 15 and lanes 16-31 the matching up rows, so that every gate value meets its up
+// value in the same warp (one shuffle, no shared memory) in the epilogue.
+template <bool FC1>
+__device__ __forceinline__ int tile_row(int t) {
+  return FC1 ? ((t & 16) ? 64 : 0) + 16 * (t >> 5) + (t & 15) : t;
 }
 
 __device__ __forceinline__ void mma_ta(uint32_t d, uint32_t a_tmem, uint64_t bd, uint32_t idesc, uint32_t acc) {
@@ -323,8 +334,7 @@ template <bool FC1>
 __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, const __grid_constant__ PfMaps maps) {
   extern __shared__ __align__(1024) unsigned char smem_dyn[];
   unsigned char* base = smem_dyn + ((1024 - (smem_addr(smem_dyn) & 1023)) & 1023);
-  float (*xchg)[64] = reinterpret_cast<float (*)[64]>(base + kPXchg);   // [16 columns][64 rows]
-  PfSmem& sm = *reinterpret_cast<PfSmem*>(base + kPXchg + 64 * 16 * sizeof(float));
+  PfSmem& sm = *reinterpret_cast<PfSmem*>(base + kPMisc);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wl = wait_limit();
   const int total_units = a.hdr[0] * a.tiles;
@@ -339,8 +349,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
     for (int s = 0; s < kNGrp; ++s) mbar_init(&sm.staged[s], kPfConvWarps);
     for (int s = 0; s < kNGrp; ++s) mbar_init(&sm.adone[s], 1);
     mbar_init(&sm.acc_full, 1);
-    mbar_init(&sm.acc_empty, 4);
-    for (int s = 0; s < kPMeta; ++s) { mbar_init(&sm.meta_full[s], 1); mbar_init(&sm.meta_empty[s], 4); }
+    mbar_init(&sm.acc_empty, kPfEpiWarps);
+    for (int s = 0; s < kPMeta; ++s) { mbar_init(&sm.meta_full[s], 1); mbar_init(&sm.meta_empty[s], kPfEpiWarps); }
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
   if (warp == 1) {
@@ -487,8 +497,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
           dslot = -1;
         }
       }
-      // per-column table of the item: pair id, routing weight, gate flag
+      // per-column table of the item: pair id, FC2's output factor (routing weight x scale_2 x the
+      // row's h scale), gate flag
       PfMeta& um = sm.meta[m];
+      const float sc2 = __ldg(a.scale_2 + pe);
       bool gated = false;
       for (int t = lane; t < kPfTok; t += 32) {
         int pr = -1;
@@ -500,7 +512,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
             record_error(MOET_ERR_DEVICE_INDEX);
           } else {
             pr = p;
-            wv = __ldg(a.topk_w + p);
+            if (!FC1) wv = __ldg(a.topk_w + p) * sc2 * __ldg(a.hscale + pos0 + t);
             if (a.gate != nullptr && __ldg(a.gate + p / a.k)) gf = 1;
           }
         }
@@ -517,73 +529,60 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
         um.nck = dslot >= 0 ? 2 * nkc : nkc;
         um.r0 = FC1 ? tile * 64 : tile * 128;
         um.r1 = FC1 ? a.I + tile * 64 : tile * 128 + 64;
-        um.sc2 = __ldg(a.scale_2 + pe);
+        um.sc2 = sc2;
       }
       __syncwarp();
       // (a test can make CTA 0 withhold its first record: every wait on it then runs out)
       const bool withhold = blockIdx.x == 0 && j == 0 && *reinterpret_cast<volatile int*>(&g_dbg_withhold) != 0;
       if (lane == 0 && !withhold) mbar_arrive(&sm.meta_full[m]);
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ---------------- epilogue: TMEM lane quarter warp & 3
+  } else if ((warp >= 4 && warp < 8) || warp >= 20) {
+    // ---------------- epilogue: TMEM lane quarter warp & 3; the two warps of a quarter take
+    // alternate 16-column chunks
+    const int ehalf = warp >= 20 ? 1 : 0;
     const int trow = 32 * (warp & 3) + lane;
     const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;
+    const bool lo = lane < 16;                     // FC1: this lane holds a gate row, lane ^ 16 its up row
     for (int j = 0; j < nunits; ++j) {
       const int m = j % kPMeta;
       bool ok = mbar_wait_warp(&sm.meta_full[m], (j / kPMeta) & 1, wl);
       ok = ok && mbar_wait_warp(&sm.acc_full, j & 1, wl);
       asm volatile("tcgen05.fence::after_thread_sync;");
-      if (epi_any(!ok || pf_stuck(sm))) {
+      if (epi_any<32 * kPfEpiWarps>(!ok || pf_stuck(sm))) {
         if (!ok && lane == 0) atomicExch(&sm.stuck, 1);
         break;
       }
       const PfMeta& um = sm.meta[m];
       const int ncols = um.ncols, ntok = um.ntok, pos0 = um.pos0;
       const float sc2 = um.sc2;
-      const int wrow = trow < 64 ? um.r0 + trow : um.r1 + trow - 64;
-      for (int c0 = 0; c0 < ncols; c0 += 16) {
+      for (int c0 = 16 * ehalf; c0 < ncols; c0 += 32) {
         float v[16];
         tmem_ld16(tmem + lane_q + c0, v);
         if (!FC1) {
+          // output row trow; per column the routing weight x scale_2 x the row's h scale
+          const int wrow = um.r0 + trow;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int col = c0 + i;
             const int p = um.pair[col];
-            if (col < ntok && p >= 0)
-              a.o[(size_t)p * a.H + wrow] = v[i] * sc2 * um.wts[col] * __ldg(a.hscale + pos0 + col);
+            if (col < ntok && p >= 0) a.o[(size_t)p * a.H + wrow] = v[i] * um.wts[col];
           }
         } else {
-          // SiLU(gate) * up: the gate rows (quarters 0-1) finish columns c0 .. c0 + 7, the up rows
-          // (quarters 2-3) columns c0 + 8 .. c0 + 15; each side hands the other its half
-          const int r = trow & 63;
-          const bool up = trow >= 64;
-          if (up) {
+          // SiLU(gate) * up: the gate lane finishes columns c0 .. c0 + 7, the up lane c0 + 8 .. c0 + 15;
+          // each hands the other the half it needs
+          float r[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) xchg[i][r] = v[i];
-          } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) xchg[8 + i][r] = v[8 + i];
-          }
-          asm volatile("bar.sync 1, 128;" ::: "memory");
-          float g[8], u[8];
-          if (up) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) { g[i] = xchg[8 + i][r]; u[i] = v[8 + i]; }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) { g[i] = v[i]; u[i] = xchg[i][r]; }
-          }
-          const int cb = c0 + (up ? 8 : 0);
-          const int hcol = um.r0 + r;
+          for (int i = 0; i < 8; ++i) r[i] = __shfl_xor_sync(0xffffffffu, lo ? v[8 + i] : v[i], 16);
+          const int cb = c0 + (lo ? 0 : 8);
+          const int hcol = um.r0 + 16 * (warp & 3) + (lane & 15);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int col = cb + i;
             if (col < ntok) {
-              const float gv = g[i] * sc2, uv = u[i] * sc2;
+              const float gv = (lo ? v[i] : r[i]) * sc2, uv = (lo ? r[i] : v[8 + i]) * sc2;
               a.h[(size_t)(pos0 + col) * a.I + hcol] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
             }
           }
-          asm volatile("bar.sync 1, 128;" ::: "memory");
         }
       }
       asm volatile("tcgen05.fence::before_thread_sync;");
@@ -598,6 +597,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
     // columns 16 h .. 16 h + 15 of each step's A stage for its row
     const int half = (warp - 8) >> 2;
     const int trow = 32 * (warp & 3) + lane;
+    const int srow = tile_row<FC1>(trow);              // the weight row this TMEM lane holds
     const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;
     int gc = 0, gs = 0;
     bool bad = false;
@@ -626,17 +626,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
 #pragma unroll
           for (int h2 = 0; h2 < kGrp; ++h2) {
             const int wi = 2 * (s + h2) + half;
-            const uint32_t sc = *reinterpret_cast<const uint16_t*>(pst + (dp ? 16384 : 8192) + trow * 16 + 2 * wi);
+            const uint32_t sc = *reinterpret_cast<const uint16_t*>(pst + (dp ? 16384 : 8192) + srow * 16 + 2 * wi);
             const uint32_t s0 = sc & 0xFFu, s1 = sc >> 8;
             uint32_t av[16];
             if (!dp) {
               // 32-byte-swizzled plane rows: 16-byte piece p of row r at p ^ ((r >> 2) & 1)
-              const int wo = trow * 32 + ((((wi >> 2) ^ ((trow >> 2) & 1))) << 4) + 4 * (wi & 3);
+              const int wo = srow * 32 + ((((wi >> 2) ^ ((srow >> 2) & 1))) << 4) + 4 * (wi & 3);
               planes_to_16<FC1>(*reinterpret_cast<const uint32_t*>(pst + wo),
                                 *reinterpret_cast<const uint32_t*>(pst + 4096 + wo), s0, s1, av);
             } else {
               // 128-byte-swizzled code rows: piece p of row r at p ^ (r & 7)
-              delta_to_16<FC1>(*reinterpret_cast<const uint4*>(pst + trow * 128 + ((wi ^ (trow & 7)) << 4)), s0, s1,
+              delta_to_16<FC1>(*reinterpret_cast<const uint4*>(pst + srow * 128 + ((wi ^ (srow & 7)) << 4)), s0, s1,
                                av);
             }
             tmem_st16(tmem + lane_q + kPColA + 32 * ((gs + h2) % kPAst) + 16 * half, av);

@@ -111,13 +111,14 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, i
   return false;
 }
 
-// OR of `flag` over the 128 epilogue threads (named barrier 1); every epilogue
+// OR of `flag` over the NT epilogue threads (named barrier 1); every epilogue
 // thread gets the same answer, so their later barriers stay matched.
+template <int NT = 128>
 __device__ __forceinline__ bool epi_any(bool flag) {
   uint32_t out;
-  asm volatile("{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.or.pred q, 1, 128, p; selp.u32 %0, 1, 0, q; }"
+  asm volatile("{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.or.pred q, 1, %2, p; selp.u32 %0, 1, 0, q; }"
                : "=r"(out)
-               : "r"(flag ? 1u : 0u));
+               : "r"(flag ? 1u : 0u), "n"(NT));
   return out != 0u;
 }
 
