@@ -3,7 +3,7 @@
 // Routing step of the MoE layer (README "Frontier MoE on consumer Blackwell
 // (SM120)", "How it fits"; the airanks page's DeepSeek-V4.1 table, row "MoE at
 // decode", counts seven launches from router to FC1 in stock vLLM -- here it is
-// one launch for up to 16 tokens and two beyond).
+// one launch for up to 16 tokens, two beyond, three above 4096 pairs).
 //
 // Top-k: one warp per token; each lane holds ceil(E/32) logits in registers
 // and a 64-bit key (order-preserving logit bits, then the complement of the
@@ -166,6 +166,85 @@ __global__ void __launch_bounds__(1024) bucket_kernel(int T, int E, int k, const
   }
 }
 
+// ---------------------------------------------------------------- bucketing of large batches
+// Beyond kBucketMultiPairs pairs the single CTA's chunk loop dominates the routing step (66 us at
+// T = 4096, k = 8), so the work is split over one CTA per 1024-pair chunk without any scratch
+// buffer: bucket_offsets_kernel (one CTA) counts all pairs per expert and writes the exclusive
+// scan to offsets; bucket_scatter_kernel's CTA c counts per expert the pairs before its chunk
+// (re-reading those ids from L2), adds them to the offsets, and scatters its own chunk stably
+// with the same warp-rank scheme as bucket_kernel.  The permutation is the same as bucket_kernel's.
+constexpr int kBucketMultiPairs = 4096;
+
+__global__ void __launch_bounds__(1024) bucket_offsets_kernel(int n, int E, const int32_t* __restrict__ topk_idx,
+                                                               int32_t* __restrict__ offsets) {
+  __shared__ int counts[1024];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < E; i += 1024) counts[i] = 0;
+  __syncthreads();
+  for (int p = tid; p < n; p += 1024) {
+    const int e = __ldg(topk_idx + p);
+    if (e < 0 || e >= E) {
+      record_error(MOET_ERR_DEVICE_INDEX);
+      continue;
+    }
+    atomicAdd(counts + e, 1);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int running = 0;
+    for (int c0 = 0; c0 < E; c0 += 32) {
+      const int e = c0 + lane;
+      const int v = e < E ? counts[e] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (e < E) offsets[e] = running + incl - v;
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) offsets[E] = running;
+  }
+}
+
+__global__ void __launch_bounds__(1024) bucket_scatter_kernel(int n, int E, const int32_t* __restrict__ topk_idx,
+                                                               const int32_t* __restrict__ offsets,
+                                                               int32_t* __restrict__ perm) {
+  extern __shared__ int smem[];
+  int* base = smem;                                   // [E]
+  unsigned char* wc = (unsigned char*)(smem + E);     // [32][E]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c0 = blockIdx.x * 1024;
+  for (int i = tid; i < E; i += 1024) base[i] = 0;
+  for (int i = tid; i < 32 * E; i += 1024) wc[i] = 0;
+  __syncthreads();
+  // pairs of each expert before this chunk (ids out of range are recorded by bucket_offsets_kernel)
+  for (int p = tid; p < c0; p += 1024) {
+    const int e = __ldg(topk_idx + p);
+    if (e >= 0 && e < E) atomicAdd(base + e, 1);
+  }
+  __syncthreads();
+  for (int i = tid; i < E; i += 1024) base[i] += __ldg(offsets + i);
+  const int p = c0 + tid;
+  int e = -1;
+  if (p < n) {
+    e = __ldg(topk_idx + p);
+    if (e < 0 || e >= E) e = -1;
+  }
+  const unsigned lt_mask = (1u << lane) - 1u;
+  const unsigned peers = __match_any_sync(0xffffffffu, e);
+  const int rank = __popc(peers & lt_mask);
+  const int cnt = __popc(peers);
+  if (e >= 0 && rank == 0) wc[warp * E + e] = (unsigned char)cnt;
+  __syncthreads();
+  if (e >= 0) {
+    int pre = 0;
+    for (int w = 0; w < warp; ++w) pre += wc[w * E + e];
+    perm[base[e] + pre + rank] = p;
+  }
+}
+
 // Largest T routed by the single-CTA fused kernel: beyond it the top-k work
 // (about k warp-wide arg-max rounds per token) is spread over one warp per
 // token on many SMs, and one CTA buckets the result (at T = 64, E = 256, k = 8
@@ -181,6 +260,23 @@ static moet_status launch_route(int T, int E, int k, const float* logits, int32_
     if (smem > 48 * 1024) MOET_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     ProfScope ps(MOET_K_ROUTE, st);
     kern<<<1, 1024, smem, st>>>(T, E, k, logits, idx, w, offsets, perm);
+  } else if ((long long)T * k > kBucketMultiPairs) {
+    {
+      ProfScope ps(MOET_K_ROUTE, st);
+      topk_kernel<VPL><<<(T + 7) / 8, 256, 0, st>>>(T, E, k, logits, idx, w);
+    }
+    MOET_CUDA_TRY(cudaGetLastError());
+    const int n = T * k;
+    {
+      ProfScope ps(MOET_K_ROUTE, st);
+      bucket_offsets_kernel<<<1, 1024, 0, st>>>(n, E, idx, offsets);
+    }
+    MOET_CUDA_TRY(cudaGetLastError());
+    const size_t ssmem = (size_t)E * 4 + (size_t)E * 32;
+    if (ssmem > 48 * 1024)
+      MOET_CUDA_TRY(cudaFuncSetAttribute(bucket_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem));
+    ProfScope ps(MOET_K_ROUTE, st);
+    bucket_scatter_kernel<<<(n + 1023) / 1024, 1024, ssmem, st>>>(n, E, idx, offsets, perm);
   } else {
     {
       ProfScope ps(MOET_K_ROUTE, st);

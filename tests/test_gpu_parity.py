@@ -228,7 +228,8 @@ def _gpu_route(moet, logits, k):
 
 
 @pytest.mark.parametrize("T,E,k", [(1, 256, 8), (4, 8, 2), (37, 64, 6), (64, 256, 8), (512, 384, 8),
-                                   (513, 256, 8), (4096, 256, 8), (256, 1024, 16), (100, 16, 1), (9, 33, 5)])
+                                   (513, 256, 8), (4096, 256, 8), (256, 1024, 16), (100, 16, 1), (9, 33, 5),
+                                   (700, 64, 7), (3000, 1024, 16)])
 def test_route_bit_exact(moet, T, E, k):
     rng = np.random.default_rng(T * 1000 + E)
     logits = rng.standard_normal((T, E)).astype(np.float32)
