@@ -657,6 +657,7 @@ static moet_status forward_impl(int T, int H, int I, int E, int k, const uint16_
     TcForwardArgs f{};
     f.T = T; f.H = H; f.I = I; f.E = n_planes; f.k = k;   // E: experts the planes hold (tensor maps)
     f.x = x; f.offsets = expert_offsets; f.perm = perm; f.topk_w = topk_w;
+    f.topk_idx = topk_idx; f.n_experts = E;
     f.fc1 = fc1; f.fc2 = fc2;
     f.delta_slot = with_delta ? delta_slot : nullptr;
     f.n_slots = n_slots; f.dfc1 = dfc1; f.dfc2 = dfc2;

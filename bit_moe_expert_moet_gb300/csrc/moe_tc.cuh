@@ -32,6 +32,8 @@ struct TcForwardArgs {
   const int32_t* offsets;
   const int32_t* perm;
   const float* topk_w;
+  const int32_t* topk_idx;     // expert of each pair
+  int n_experts;               // experts the ids range over (delta_slot entries)
   const moet_planes* fc1;
   const moet_planes* fc2;
   const int32_t* delta_slot;   // nullable
