@@ -114,12 +114,18 @@ moet_status moet_requant_2bit(int M, int N, int K, const uint8_t* codes, const u
  *   s16 = e4m3 satfinite RNE(max_b |W| / (3 scale_2)); sign = the code's sign
  *   bit; mag = |W| >= 2 s16 scale_2; the delta is the NVFP4 residual of
  *   W - q s16 scale_2 on the same scale_2 (scale e4m3 RNE(max|d| / (6 scale_2)),
- *   codes e2m1 RNE, zero as +0).  Every ratio is rounded once, exactly (fp64).
+ *   codes e2m1 RNE, zero as +0).  Every ratio is rounded once, exactly: the
+ *   kernels hold each number as an integer times a power of two and decide by
+ *   integer comparisons.
  *   M >= 1 matrices of [N, K], K % 32 == 0.  codes [M, N, K] u8 (16 B aligned;
  *   the NaN codes 0x7F/0xFF are not valid weights); bscale [M, ceil(N/128),
- *   ceil(K/128)] fp32 (read).  scale_2 [M] fp32, sign/mag [M, N, K/32] u32,
- *   s16 [M, N, K/16] u8 (written); dcodes [M, N, K/2] / ds4 [M, N, K/16]
- *   (both NULL = no delta).  Outputs are bit-exact. */
+ *   ceil(K/128)] fp32, finite and >= 0 (read; for another value the outputs of
+ *   that block and the matrix's scale_2 are unspecified, nothing faults).
+ *   scale_2 [M] fp32, sign/mag [M, N, K/32] u32, s16 [M, N, K/16] u8
+ *   (written; the first words of each matrix's sign plane also serve as
+ *   scratch for the amax pass before the planes are written); dcodes
+ *   [M, N, K/2] / ds4 [M, N, K/16] (both NULL = no delta).  Outputs are
+ *   bit-exact. */
 moet_status moet_requant_fp8_2bit(int M, int N, int K, const uint8_t* codes, const float* bscale,
                                   float* scale_2, uint32_t* sign, uint32_t* mag, uint8_t* s16,
                                   uint8_t* dcodes, uint8_t* ds4, moet_stream stream);
@@ -137,9 +143,10 @@ moet_status moet_requant_fp8_2bit(int M, int N, int K, const uint8_t* codes, con
  *   M >= 1 matrices of [N, K], K % 32 == 0.  codes [M, N, K/2] u8, low nibble =
  *   even k (16 B aligned); e8m0 [M, N, K/32] u8 (read; 0xFF = NaN is not a
  *   valid scale: the outputs of its group are unspecified, nothing faults).
- *   scale_2 [M] fp32, sign/mag [M, N, K/32] u32, s16 [M, N, K/16] u8 (written);
- *   dcodes [M, N, K/2] / ds4 [M, N, K/16] (both NULL = no delta).  Outputs are
- *   bit-exact. */
+ *   scale_2 [M] fp32, sign/mag [M, N, K/32] u32, s16 [M, N, K/16] u8 (written;
+ *   the sign plane also serves as scratch for the amax pass, as in
+ *   moet_requant_fp8_2bit); dcodes [M, N, K/2] / ds4 [M, N, K/16] (both NULL =
+ *   no delta).  Outputs are bit-exact (integer arithmetic, as above). */
 moet_status moet_requant_mxfp4_2bit(int M, int N, int K, const uint8_t* codes, const uint8_t* e8m0,
                                     float* scale_2, uint32_t* sign, uint32_t* mag, uint8_t* s16,
                                     uint8_t* dcodes, uint8_t* ds4, moet_stream stream);

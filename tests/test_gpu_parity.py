@@ -138,18 +138,28 @@ def test_requant_planes_large_ragged(moet):
             assert np.array_equal(ref[key], b[key][m, rows]), (m, key)
 
 
-@pytest.mark.parametrize("M,N,K", [(3, 200, 96), (1, 128, 2048), (2, 7, 32)])
-def test_requant_fp8_bit_exact(moet, M, N, K):
+@pytest.mark.parametrize("M,N,K,wide", [(3, 200, 96, False), (1, 128, 2048, False), (2, 7, 32, False),
+                                         (2, 300, 640, True), (5, 64, 8192, True)])
+def test_requant_fp8_bit_exact(moet, M, N, K, wide):
     """FP8 block-quant -> scale_2, planes, s16 and delta, bit-exact against the oracle; N and K
     not multiples of the 128 x 128 scale blocks, signed zeros, +-448 and subnormals included,
-    and an all-zero matrix."""
+    and an all-zero matrix.  The wide cases spread the block scales over 2^-120 .. 2^20 (an fp32
+    subnormal and a zero scale among them), so most blocks sit far below the matrix's largest
+    and get a zero or subnormal s16; the amax pass then runs on many CTAs per matrix."""
     rng = np.random.default_rng(140 + N + K)
     codes = rng.integers(0, 256, (M, N, K), dtype=np.uint8)
     codes[(codes & 0x7F) == 0x7F] ^= 1
     codes[0, 0, :5] = [0x00, 0x80, 0x7E, 0xFE, 0x01]
     if M > 1:
         codes[-1] = 0                                       # an all-zero matrix
-    bs = (rng.random((M, (N + 127) // 128, (K + 127) // 128)) * 0.02 + 0.001).astype(np.float32)
+    shape = (M, (N + 127) // 128, (K + 127) // 128)
+    if wide:
+        bs = np.ldexp(rng.random(shape) + 0.5, rng.integers(-120, 21, shape)).astype(np.float32)
+        bs[0, 0, 0] = np.float32(3e-43)
+        bs[0, -1, -1] = 0.0
+        codes[0, :16, 128:144] = codes[0, 0, 128]           # sixteen equal codes in a row of a block
+    else:
+        bs = (rng.random(shape) * 0.02 + 0.001).astype(np.float32)
     g = dict(scale_2=torch.empty(M, dtype=torch.float32, device=DEV),
              sign=torch.empty((M, N, K // 32), dtype=torch.int32, device=DEV),
              mag=torch.empty((M, N, K // 32), dtype=torch.int32, device=DEV),
@@ -172,15 +182,16 @@ def test_requant_fp8_bit_exact(moet, M, N, K):
     assert torch.equal(sign2, g["sign"]) and torch.equal(mag2, g["mag"]) and torch.equal(s162, g["s16"])
 
 
-@pytest.mark.parametrize("M,N,K", [(3, 200, 96), (1, 128, 2048), (2, 7, 32)])
-def test_requant_mxfp4_bit_exact(moet, M, N, K):
+@pytest.mark.parametrize("M,N,K,lo,hi", [(3, 200, 96, 100, 150), (1, 128, 2048, 100, 150), (2, 7, 32, 100, 150),
+                                         (4, 300, 512, 0, 255)])
+def test_requant_mxfp4_bit_exact(moet, M, N, K, lo, hi):
     """MXFP4 (e2m1 codes, E8M0 scale per 32 along K) -> scale_2, planes, s16 and delta, bit-exact
     against the oracle; signed zeros, +-6, the extreme exponents 2^-127 and 2^127 in one matrix
-    and an all-zero matrix included."""
+    and an all-zero matrix included; the last case draws exponents over the whole E8M0 range."""
     rng = np.random.default_rng(150 + N + K)
     codes = rng.integers(0, 256, (M, N, K // 2), dtype=np.uint8)
     codes[0, 0, :2] = [0x80, 0x7F]
-    e8m0 = rng.integers(100, 150, (M, N, K // 32)).astype(np.uint8)
+    e8m0 = rng.integers(lo, hi, (M, N, K // 32)).astype(np.uint8)
     e8m0[0, 0, 0] = 0
     e8m0[0, -1, -1] = 254
     if M > 1:

@@ -209,12 +209,30 @@ def _random_fp8(rng, N, K, nbs_scale=1.0):
     return codes, bs
 
 
-def test_fp8_requant_matches_exact_fractions():
+def _fp8_wide_scales(rng):
+    """Three rows of 384 codes under three block scales each, the scales spread over 2^-120 ..
+    2^20 with one fp32 subnormal and one zero: blocks far below the matrix's largest (s16 = 0 or
+    a subnormal s16) next to the top block."""
+    codes, _ = _random_fp8(rng, 3, 384)
+    codes[2, 256:272] = codes[2, 256]                        # sixteen equal codes
+    bs = np.array([[np.ldexp(1.37, 20), np.ldexp(1.9, -7), np.float32(3e-43)]], np.float32)
+    bs2 = np.array([[np.ldexp(1.1, -120), 0.0, np.ldexp(1.61, 13)]], np.float32)
+    return codes, bs, bs2
+
+
+@pytest.mark.parametrize("case", ["narrow", "wide_a", "wide_b"])
+def test_fp8_requant_matches_exact_fractions(case):
     """Every integer output of the fp64 FP8 requant against the same rule evaluated in exact
-    rational arithmetic (Fraction), weight by weight."""
+    rational arithmetic (Fraction), weight by weight; block scales of one magnitude, then spread
+    over 140 binades (the exactness of the fp64 residual and every fp64 comparison is claimed for
+    any scales, so it is pinned there too)."""
     rng = np.random.default_rng(21)
-    codes, bs = _random_fp8(rng, 3, 64)
-    bs[:] = rng.choice(np.array([0.0078125, 0.3, 1.7e-3], np.float32), size=bs.shape)
+    if case == "narrow":
+        codes, bs = _random_fp8(rng, 3, 64)
+        bs[:] = rng.choice(np.array([0.0078125, 0.3, 1.7e-3], np.float32), size=bs.shape)
+    else:
+        codes, bs_a, bs_b = _fp8_wide_scales(rng)
+        bs = bs_a if case == "wide_a" else bs_b
     out = requant.requant_fp8_2bit(codes, bs)
     s2 = Fraction(float(out["scale_2"]))
     N, K = codes.shape
