@@ -143,10 +143,12 @@ __device__ __forceinline__ int tile_row(int t) {
   return FC1 ? ((t & 16) ? 64 : 0) + 16 * (t >> 5) + (t & 15) : t;
 }
 
-__device__ __forceinline__ void mma_ta(uint32_t d, uint32_t a_tmem, uint64_t bd, uint32_t idesc, uint32_t acc) {
+// kind::f16 MMA with A in TMEM, issued by one elected lane of a converged warp (warp-uniform
+// operands stay in uniform registers).
+__device__ __forceinline__ void mma_ta_elect(uint32_t d, uint32_t a_tmem, uint64_t bd, uint32_t idesc, uint32_t acc) {
   asm volatile(
-      "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d),
+      "{ .reg .pred p, e; setp.ne.b32 p, %4, 0; elect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d),
       "r"(a_tmem), "l"(bd), "r"(idesc), "r"(acc));
 }
 
@@ -427,53 +429,55 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
           if (i % kBProd == bprod) mbar_wait(&sm.bfull[i % kBRing], (i / kBRing) & 1, wl);
     }
   } else if (warp == 1) {
-    // ---------------- MMA issue
-    if (lane == 0) {
-      int gs = 0, last = -1;
-      bool bad = false;
-      for (int j = 0; j < nunits && !bad; ++j) {
-        const int m = j % kPMeta;
-        if (!mbar_wait(&sm.meta_full[m], (j / kPMeta) & 1, wl)) { bad = true; break; }
-        if (j >= 1 && !mbar_wait(&sm.acc_empty, (j - 1) & 1, wl)) { bad = true; break; }
-        if (pf_stuck(sm)) { bad = true; break; }
-        asm volatile("tcgen05.fence::after_thread_sync;");
-        const int nst = sm.meta[m].nck * (kPC / kStepWeights);
-        const uint32_t idesc = f16_idesc<FC1>(sm.meta[m].ncols);   // FC1 bf16, FC2 fp16
-        // a group of kGrp steps per iteration: its A stages expanded (one wait), then each
-        // step's activations (one wait per step: the activation ring is shallower than a group
-        // plus the next)
-        for (int st = 0; st < nst && !bad; st += kGrp, gs += kGrp) {
-          const int grp = gs / kGrp;
-          if (!mbar_wait(&sm.staged[grp % kNGrp], (grp / kNGrp) & 1, wl)) {
+    // ---------------- MMA issue.  The whole warp walks the loop, so every operand stays
+    // warp-uniform (uniform registers); one elected lane issues each MMA and commit.  An
+    // activation stage's descriptor is the ring's base descriptor plus the stage's offset / 16.
+    int gs = 0, last = -1;
+    bool bad = false;
+    const uint64_t b_desc = sw128_desc(smem_addr(base + kBBase));
+    for (int j = 0; j < nunits && !bad; ++j) {
+      const int m = j % kPMeta;
+      if (!mbar_wait_warp(&sm.meta_full[m], (j / kPMeta) & 1, wl)) { bad = true; break; }
+      if (j >= 1 && !mbar_wait_warp(&sm.acc_empty, (j - 1) & 1, wl)) { bad = true; break; }
+      if (__any_sync(0xffffffffu, pf_stuck(sm))) { bad = true; break; }
+      asm volatile("tcgen05.fence::after_thread_sync;");
+      const int nst = sm.meta[m].nck * (kPC / kStepWeights);
+      const uint32_t idesc = f16_idesc<FC1>(sm.meta[m].ncols);   // FC1 bf16, FC2 fp16
+      // a group of kGrp steps per iteration: its A stages expanded (one wait), then each
+      // step's activations (one wait per step: the activation ring is shallower than a group
+      // plus the next)
+      for (int st = 0; st < nst && !bad; st += kGrp, gs += kGrp) {
+        const int grp = gs / kGrp;
+        if (!mbar_wait_warp(&sm.staged[grp % kNGrp], (grp / kNGrp) & 1, wl)) {
+          bad = true;
+          break;
+        }
+#pragma unroll
+        for (int h = 0; h < kGrp; ++h) {
+          const int as = (gs + h) % kPAst, bs = (gs + h) % kBRing;
+          if (!mbar_wait_warp(&sm.bfull[bs], ((gs + h) / kBRing) & 1, wl)) {
             bad = true;
             break;
           }
+          asm volatile("tcgen05.fence::after_thread_sync;");
+          const uint64_t bd = b_desc + (uint64_t)((bs * kBStepBytes) >> 4);
 #pragma unroll
-          for (int h = 0; h < kGrp; ++h) {
-            const int as = (gs + h) % kPAst, bs = (gs + h) % kBRing;
-            if (!mbar_wait(&sm.bfull[bs], ((gs + h) / kBRing) & 1, wl)) {
-              bad = true;
-              break;
-            }
-            asm volatile("tcgen05.fence::after_thread_sync;");
-            const uint32_t bsm = smem_addr(base + kBBase + bs * kBStepBytes);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              mma_ta(tmem, tmem + kPColA + 32 * as + 8 * i, sw128_desc(bsm + 32 * i), idesc,
-                     (st > 0 || h > 0 || i > 0) ? 1u : 0u);
-            tc_commit(&sm.bdone[bs]);
-            last = gs + h;
-          }
-          if (bad) break;
-          tc_commit(&sm.adone[grp % kNGrp]);
+          for (int i = 0; i < 4; ++i)
+            mma_ta_elect(tmem, tmem + kPColA + 32 * as + 8 * i, bd + (uint64_t)((32 * i) >> 4), idesc,
+                         (st > 0 || h > 0 || i > 0) ? 1u : 0u);
+          tc_commit_elect(&sm.bdone[bs]);
+          last = gs + h;
         }
         if (bad) break;
-        tc_commit(&sm.acc_full);
+        tc_commit_elect(&sm.adone[grp % kNGrp]);
       }
-      if (bad) atomicExch(&sm.stuck, 1);
-      // every MMA this thread issued is complete before TMEM is released
-      if (last >= 0) mbar_wait(&sm.bdone[last % kBRing], (last / kBRing) & 1, wl);
+      if (bad) break;
+      tc_commit_elect(&sm.acc_full);
     }
+    if (bad && lane == 0) atomicExch(&sm.stuck, 1);
+    // every MMA this warp issued is complete before TMEM is released
+    if (last >= 0 && lane == 0) mbar_wait(&sm.bdone[last % kBRing], (last / kBRing) & 1, wl);
+    __syncwarp();
   } else if (warp == 2) {
     // ---------------- scheduler
     for (int j = 0; j < nunits; ++j) {

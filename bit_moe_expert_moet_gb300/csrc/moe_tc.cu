@@ -81,20 +81,22 @@ __device__ __forceinline__ uint32_t mxf4_idesc(int n) {
   return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 }
 
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t sfa,
-                                       uint32_t sfb, uint32_t acc) {
+// The block-scaled MMA (A and B from shared memory), issued by one elected lane of a converged
+// warp: the operands are warp-uniform, so they stay in uniform registers.
+__device__ __forceinline__ void tc_mma_elect(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t sfa,
+                                             uint32_t sfb, uint32_t acc) {
   asm volatile(
-      "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p; }"
+      "{ .reg .pred p, e; setp.ne.b32 p, %6, 0; elect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p; }"
       ::"r"(d), "l"(ad), "l"(bd), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc));
 }
 
 // Same MMA with the A operand in TMEM (row = lane, K along the columns, 8 e2m1 per column).
-__device__ __forceinline__ void tc_mma_ta(uint32_t d, uint32_t a_tmem, uint64_t bd, uint32_t idesc, uint32_t sfa,
-                                          uint32_t sfb, uint32_t acc) {
+__device__ __forceinline__ void tc_mma_ta_elect(uint32_t d, uint32_t a_tmem, uint64_t bd, uint32_t idesc,
+                                                uint32_t sfa, uint32_t sfb, uint32_t acc) {
   asm volatile(
-      "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], [%1], %2, %3, [%4], [%5], p; }"
+      "{ .reg .pred p, e; setp.ne.b32 p, %6, 0; elect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], [%1], %2, %3, [%4], [%5], p; }"
       ::"r"(d), "r"(a_tmem), "l"(bd), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc));
 }
 
@@ -643,51 +645,58 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
       for (int i = g > kRaw ? g - kRaw : 0; i < g; ++i)
         if ((i & 1) == pw) mbar_wait(&sm.full[i % kRaw], (i / kRaw) & 1, wl);
   } else if (warp == 1) {
-    // ---------------- MMA issue
-    if (lane == 0) {
-      int g = 0, last = -1;
-      bool bad = false;
-      for (int j = 0; j < nunits && !bad; ++j) {
-        const int m = j % kMeta, ab = j & 1;
-        if (!mbar_wait(&sm.meta_full[m], (j / kMeta) & 1, wl)) { bad = true; break; }
-        if (j >= 2 && !mbar_wait(&sm.acc_empty[ab], ((j >> 1) - 1) & 1, wl)) { bad = true; break; }
-        if (is_stuck(sm)) { bad = true; break; }
+    // ---------------- MMA issue.  The whole warp walks the loop, so every operand (descriptors,
+    // TMEM addresses, loop state) is warp-uniform and stays in the uniform datapath; one elected
+    // lane issues each MMA and commit.  A stage's shared-memory descriptors are its base
+    // descriptor plus constant offsets (byte offset / 16 in the address field, which cannot
+    // carry: shared addresses stay below 256 KB).
+    int g = 0, last = -1;
+    bool bad = false;
+    const uint64_t raw_desc = sw128_desc(smem_addr(raw));
+    for (int j = 0; j < nunits && !bad; ++j) {
+      const int m = j % kMeta, ab = j & 1;
+      if (!mbar_wait_warp(&sm.meta_full[m], (j / kMeta) & 1, wl)) { bad = true; break; }
+      if (j >= 2 && !mbar_wait_warp(&sm.acc_empty[ab], ((j >> 1) - 1) & 1, wl)) { bad = true; break; }
+      if (__any_sync(0xffffffffu, is_stuck(sm))) { bad = true; break; }
+      asm volatile("tcgen05.fence::after_thread_sync;");
+      const int nch = meta[m].nch;
+      const uint32_t idesc = mxf4_idesc(meta[m].ncols);
+      const uint32_t dcol = tmem + 128 * ab;
+      for (int c = 0; c < nch; ++c, ++g) {
+        const int as = g % kAst, au = g / kAst, rs = g % kRaw;
+        if (!mbar_wait_warp(&sm.staged[as], au & 1, wl)) { bad = true; break; }
         asm volatile("tcgen05.fence::after_thread_sync;");
-        const int nch = meta[m].nch;
-        const uint32_t idesc = mxf4_idesc(meta[m].ncols);
-        const uint32_t dcol = tmem + 128 * ab;
-        for (int c = 0; c < nch; ++c, ++g) {
-          const int as = g % kAst, au = g / kAst, rs = g % kRaw;
-          if (!mbar_wait(&sm.staged[as], au & 1, wl)) { bad = true; break; }
-          asm volatile("tcgen05.fence::after_thread_sync;");
-          const uint32_t rsm = smem_addr(raw + rs * kRawBytes);
-          const uint32_t sfa = tmem + kColSFA + 32 * as, sfb = tmem + kColSFB + 32 * as;
-          if (c < nps) {
-            const int nsub = min(2, (a.K - kKC * c) / kKD);
-            const uint32_t ata = tmem + kColA + 64 * as;
-            for (int h = 0; h < nsub; ++h) {
+        const uint64_t rd = raw_desc + (uint64_t)((rs * kRawBytes) >> 4);
+        const uint32_t sfa = tmem + kColSFA + 32 * as, sfb = tmem + kColSFB + 32 * as;
+        if (c < nps) {
+          const int nsub = min(2, (a.K - kKC * c) / kKD);
+          const uint32_t ata = tmem + kColA + 64 * as;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (h < nsub) {
 #pragma unroll
               for (int i = 0; i < 4; ++i)
-                tc_mma_ta(dcol, ata + 32 * h + 8 * i, sw128_desc(rsm + kRB + 8192 * h + 32 * i), idesc,
-                          sfa + 16 * h + 4 * i, sfb + 16 * h + 4 * i, (c > 0 || h > 0 || i > 0) ? 1u : 0u);
+                tc_mma_ta_elect(dcol, ata + 32 * h + 8 * i, rd + (uint64_t)((kRB + 8192 * h + 32 * i) >> 4), idesc,
+                                sfa + 16 * h + 4 * i, sfb + 16 * h + 4 * i, (c > 0 || h > 0 || i > 0) ? 1u : 0u);
             }
-          } else {
-            const int dc = c - nps;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              tc_mma(dcol + 64, sw128_desc(rsm + 32 * i), sw128_desc(rsm + kRB + 32 * i), idesc, sfa + 4 * i,
-                     sfb + 4 * i, (dc > 0 || i > 0) ? 1u : 0u);
           }
-          tc_commit(&sm.done[rs]);
-          last = g;
+        } else {
+          const int dc = c - nps;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            tc_mma_elect(dcol + 64, rd + (uint64_t)((32 * i) >> 4), rd + (uint64_t)((kRB + 32 * i) >> 4), idesc,
+                         sfa + 4 * i, sfb + 4 * i, (dc > 0 || i > 0) ? 1u : 0u);
         }
-        if (bad) break;
-        tc_commit(&sm.acc_full[ab]);
+        tc_commit_elect(&sm.done[rs]);
+        last = g;
       }
-      if (bad) set_stuck(sm);
-      // every MMA this thread issued is complete before TMEM is released
-      if (last >= 0) mbar_wait(&sm.done[last % kRaw], (last / kRaw) & 1, wl);
+      if (bad) break;
+      tc_commit_elect(&sm.acc_full[ab]);
     }
+    if (bad && lane == 0) set_stuck(sm);
+    // every MMA this warp issued is complete before TMEM is released
+    if (last >= 0 && lane == 0) mbar_wait(&sm.done[last % kRaw], (last / kRaw) & 1, wl);
+    __syncwarp();
   } else if (warp == 2) {
     // ---------------- scheduler
     for (int j = 0; j < nunits; ++j) {
