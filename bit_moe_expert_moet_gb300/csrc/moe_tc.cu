@@ -28,13 +28,13 @@
 // against a naturally ordered copy of the terms ("cnat") and accumulates in
 // a second TMEM region.
 //
-// Pipeline: a persistent CTA per SM (24 warps, warp-specialised, no CTA-wide
+// Pipeline: a persistent CTA per SM (16 warps, warp-specialised, no CTA-wide
 // barrier in the loop) walks (work item, 128-row weight tile) units.  Two
 // producer warps stream each unit's K chunks into a ring of raw shared-memory
 // stages with TMA, one lane per box (sign and magnitude planes, row scales, the
-// item's activation-term rows and their scales); 16 converter warps expand the
-// planes into TMEM A stages and write the scale factors to TMEM; one thread
-// issues the MMAs (K = 64 each) and commits them to the stage's "done" barrier
+// item's activation-term rows and their scales); 8 converter warps expand the
+// planes into TMEM A stages and write the scale factors to TMEM; the MMA warp
+// issues the MMAs (K = 64 each, one elected lane) and commits them to the stage's "done" barrier
 // and, at the end of a unit, to one of two TMEM accumulator buffers that the
 // epilogue warps drain while the next unit accumulates.  A scheduler warp
 // prepares each unit's record (pairs, routing weights, gate flags, term scales)
@@ -52,9 +52,9 @@
 namespace moet {
 namespace {
 
-constexpr int kWsThreads = 768;              // 24 warps, roles in fc_tc_kernel
+constexpr int kWsThreads = 512;              // 16 warps, roles in fc_tc_kernel
 constexpr int kConvGroups = 2;                // converter groups, one per MMA sub-step of a stage
-constexpr int kConvWarps = 8;                 // per group: two warps per 32-row quarter
+constexpr int kConvWarps = 4;                 // per group: one warp per 32-row quarter
 constexpr int kRaw = 5;                       // raw TMA stages in flight
 constexpr int kAst = 2;                       // expanded-A stages (in TMEM)
 constexpr int kMeta = 4;                      // unit records in flight
@@ -513,13 +513,13 @@ __device__ __forceinline__ void set_stuck(TcSmem& sm) { atomicExch(&sm.stuck, 1)
 // + j gridDim.x of the (work item x weight tile) grid.  Warp roles:
 //   0, 3   producers, alternate stages: each TMA box of a stage is issued by
 //          its own lane (one instruction), into a ring of kRaw raw stages
-//   1      TMEM owner; one thread issues the MMAs and their commits
+//   1      TMEM owner; issues the MMAs and their commits (warp-uniform, one elected lane)
 //   2      scheduler: per unit, the item's pairs, weights, gate flags and term
 //          scales into a ring of kMeta unit records
 //   4-7    epilogue (TMEM lane quarters 0-3): term sums, SiLU * up / routing
 //          weight, stores; the accumulators are double-buffered in TMEM so the
 //          next unit's MMAs run while the epilogue reads this one's
-//   8-23   converters in two groups of eight warps (two per 32-row quarter);
+//   8-15   converters in two groups of four warps (one per 32-row quarter);
 //          group h takes sub-step h of every stage: planes -> e2m1 A operand
 //          and scale factors, both stored straight into TMEM (each thread owns
 //          the TMEM lane of its weight row), so the expanded A never touches
@@ -838,15 +838,15 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
     }
   } else if (warp >= 8) {
     // ---------------- converters: group grp expands sub-step grp (256 weights) of
-    // every plane stage (group 0 handles the delta stages); in a group, two warps
-    // per 32-row quarter; half h expands weight words 4h..4h+3 of the sub-step;
-    // half 0 writes the row scales to TMEM, half 1 the activation-term scales
-    const int grp = (warp - 8) >> 3;
-    const int half = ((warp - 8) >> 2) & 1;
+    // every plane stage (group 0 handles the delta stages); in a group, one warp per
+    // 32-row quarter, each thread one row: its 8 plane words -> 32 TMEM columns, then
+    // the sub-step's row scales and activation-term scales
+    const int grp = (warp - 8) >> 2;
     const int trow = 32 * (warp & 3) + lane;
     const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;
     // 64-byte-swizzled plane rows: 16-byte piece p of row r sits at piece p ^ ((r >> 1) & 3)
-    const int praw = trow * 64 + (((2 * grp + half) ^ ((trow >> 1) & 3)) << 4);
+    const int praw0 = trow * 64 + (((2 * grp) ^ ((trow >> 1) & 3)) << 4);
+    const int praw1 = trow * 64 + (((2 * grp + 1) ^ ((trow >> 1) & 3)) << 4);
     int g = 0;
     bool bad = false;
     for (int j = 0; j < nunits && !bad; ++j) {
@@ -864,34 +864,42 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
         if (grp < nsub) {
           const unsigned char* st = raw + rs * kRawBytes;
           if (!dp) {
-            // this thread's 128 weights of the row -> 16 TMEM columns of its lane (K order)
-            const uint4 sw = *reinterpret_cast<const uint4*>(st + kRSign + praw);
-            const uint4 mw = *reinterpret_cast<const uint4*>(st + kRMag + praw);
-            uint32_t av[16];
-            const uint4 e0 = planes_to_e2m1(sw.x, mw.x), e1 = planes_to_e2m1(sw.y, mw.y);
-            const uint4 e2 = planes_to_e2m1(sw.z, mw.z), e3 = planes_to_e2m1(sw.w, mw.w);
-            av[0] = e0.x; av[1] = e0.y; av[2] = e0.z; av[3] = e0.w;
-            av[4] = e1.x; av[5] = e1.y; av[6] = e1.z; av[7] = e1.w;
-            av[8] = e2.x; av[9] = e2.y; av[10] = e2.z; av[11] = e2.w;
-            av[12] = e3.x; av[13] = e3.y; av[14] = e3.z; av[15] = e3.w;
-            tmem_st16(tmem + lane_q + kColA + 64 * as + 32 * grp + 16 * half, av);
-          }
-          // scale factors to TMEM, replicated layout: rows lane + 32 j -> columns 4 i + j
-          uint32_t v[16];
+            // this thread's 256 weights of the row -> 32 TMEM columns of its lane (K order)
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            const int n = lane + 32 * jj;
-            uint4 q = make_uint4(0u, 0u, 0u, 0u);
-            if (half == 0) {
-              // plane row scales: 32-byte-swizzled rows, piece h of row n at h ^ ((n >> 2) & 1)
-              const int off = dp ? kRDS + n * 16 : kRQ + n * 32 + ((grp ^ ((n >> 2) & 1)) << 4);
-              q = *reinterpret_cast<const uint4*>(st + off);
-            } else if (n < ncols) {
-              q = *reinterpret_cast<const uint4*>(st + kRSF + (dp ? n * 16 : n * 32 + 16 * grp));
+            for (int hh = 0; hh < 2; ++hh) {
+              const int pr = hh ? praw1 : praw0;
+              const uint4 sw = *reinterpret_cast<const uint4*>(st + kRSign + pr);
+              const uint4 mw = *reinterpret_cast<const uint4*>(st + kRMag + pr);
+              uint32_t av[16];
+              const uint4 e0 = planes_to_e2m1(sw.x, mw.x), e1 = planes_to_e2m1(sw.y, mw.y);
+              const uint4 e2 = planes_to_e2m1(sw.z, mw.z), e3 = planes_to_e2m1(sw.w, mw.w);
+              av[0] = e0.x; av[1] = e0.y; av[2] = e0.z; av[3] = e0.w;
+              av[4] = e1.x; av[5] = e1.y; av[6] = e1.z; av[7] = e1.w;
+              av[8] = e2.x; av[9] = e2.y; av[10] = e2.z; av[11] = e2.w;
+              av[12] = e3.x; av[13] = e3.y; av[14] = e3.z; av[15] = e3.w;
+              tmem_st16(tmem + lane_q + kColA + 64 * as + 32 * grp + 16 * hh, av);
             }
-            v[0 * 4 + jj] = q.x; v[1 * 4 + jj] = q.y; v[2 * 4 + jj] = q.z; v[3 * 4 + jj] = q.w;
           }
-          tmem_st16(tmem + lane_q + (half ? kColSFB : kColSFA) + 32 * as + 16 * grp, v);
+          // scale factors to TMEM, replicated layout: rows lane + 32 j -> columns 4 i + j; the row
+          // scales (A) and the activation-term scales (B) of this sub-step
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t v[16];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const int n = lane + 32 * jj;
+              uint4 q = make_uint4(0u, 0u, 0u, 0u);
+              if (half == 0) {
+                // plane row scales: 32-byte-swizzled rows, piece h of row n at h ^ ((n >> 2) & 1)
+                const int off = dp ? kRDS + n * 16 : kRQ + n * 32 + ((grp ^ ((n >> 2) & 1)) << 4);
+                q = *reinterpret_cast<const uint4*>(st + off);
+              } else if (n < ncols) {
+                q = *reinterpret_cast<const uint4*>(st + kRSF + (dp ? n * 16 : n * 32 + 16 * grp));
+              }
+              v[0 * 4 + jj] = q.x; v[1 * 4 + jj] = q.y; v[2 * 4 + jj] = q.z; v[3 * 4 + jj] = q.w;
+            }
+            tmem_st16(tmem + lane_q + (half ? kColSFB : kColSFA) + 32 * as + 16 * grp, v);
+          }
           asm volatile("tcgen05.wait::st.sync.aligned;");
           asm volatile("tcgen05.fence::before_thread_sync;");
         }
