@@ -43,7 +43,7 @@ constexpr int kSmemBudget = 96 * 1024;
 constexpr uint32_t kCodeLut = 0xC242BC3Cu;  // f16 high bytes of +1, -1, +3, -3
 
 struct WsLayout {
-  size_t hdr, tok_scale, tok_max, hmax, inv, pvalid, chunks, chunks_s, h, o, xt, ht, pfa, total;
+  size_t hdr, tok_scale, tok_max, hmax, inv, pvalid, chunks, chunks_s, h, o, xt, ht, pfa, perm2, total;
 };
 
 // Largest T routed through the tcgen05 engine (small tokens-per-expert regime).
@@ -86,12 +86,13 @@ inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   L.chunks = off;    off += align256(sizeof(int4) * (size_t)max_chunks(T, E, k, kTcTok));
   L.h = off;         off += align256(sizeof(float) * pairs * I);
   L.o = off;         off += align256(sizeof(float) * pairs * H);
-  L.xt = off; L.ht = off; L.pfa = off; L.chunks_s = off;
+  L.xt = off; L.ht = off; L.pfa = off; L.chunks_s = off; L.perm2 = off;
   if (T <= kTcMaxT && tc_supported(H, I)) {
     L.xt = off;      off += align256(tc_terms_bytes(pairs, (size_t)H));
     L.ht = off;      off += align256(tc_terms_bytes(pairs, (size_t)I));
   } else if (T > kTcMaxT && pf_supported(H, I)) {
     L.pfa = off;     off += align256(pf_act_bytes(pairs, (size_t)H, (size_t)I) + 5 * 256);
+    L.perm2 = off;   off += align256(sizeof(int32_t) * pairs);
     if (pf_hybrid(T, H, I)) {
       const size_t items = (size_t)pf_small_items(T, E, k), rows = items * kTcTok;
       L.chunks_s = off; off += align256(sizeof(int4) * items);
@@ -101,6 +102,44 @@ inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   }
   L.total = off;
   return L;
+}
+
+// Prefill regime with the delta: the engines walk the pairs in a private order, the bucketed
+// order with each cached expert's pairs stably split into its gated pairs first, then the rest.
+// A work item is a run of consecutive pairs of one expert, so only the items that reach into
+// the gated run make the delta pass, and within an item the gated pairs are the leading
+// columns.  Every pair's result depends only on its own column, so the layer's output is the
+// same as in the bucketed order.  One warp per expert; a pair id out of range counts as
+// ungated (the engines report it).
+__global__ void __launch_bounds__(kThreads) gated_first_kernel(int E, int k, int n_pairs,
+                                                               const int32_t* __restrict__ offsets,
+                                                               const int32_t* __restrict__ perm,
+                                                               const int32_t* __restrict__ delta_slot,
+                                                               const uint8_t* __restrict__ gate,
+                                                               int32_t* __restrict__ perm2) {
+  const int e = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (e >= E) return;
+  const int off = __ldg(offsets + e), n = __ldg(offsets + e + 1) - off;
+  if (n <= 0 || off < 0 || off + n > n_pairs) return;
+  const bool cached = __ldg(delta_slot + e) >= 0;
+  const uint32_t below = (1u << lane) - 1u;
+  auto is_gated = [&](int p) { return cached && p >= 0 && p < n_pairs && __ldg(gate + p / k) != 0; };
+  int G = 0;
+  for (int c = 0; c < n; c += 32) {
+    const int i = c + lane;
+    const bool g = i < n && is_gated(__ldg(perm + off + i));
+    G += __popc(__ballot_sync(0xffffffffu, g));
+  }
+  int gi = 0, ui = G;
+  for (int c = 0; c < n; c += 32) {
+    const int i = c + lane;
+    const int p = i < n ? __ldg(perm + off + i) : -1;
+    const bool g = i < n && is_gated(p);
+    const uint32_t mg = __ballot_sync(0xffffffffu, g), mu = __ballot_sync(0xffffffffu, i < n && !g);
+    if (i < n) perm2[off + (g ? gi + __popc(mg & below) : ui + __popc(mu & below))] = p;
+    gi += __popc(mg);
+    ui += __popc(mu);
+  }
 }
 
 // power-of-two multiplier that brings max|row| into [2^14, 2^15)
@@ -674,9 +713,21 @@ static moet_status forward_impl(int T, int H, int I, int E, int k, const uint16_
     return f;
   };
   if (use_pf) {
+    // with the delta, the engines walk each cached expert's pairs gated first
+    const int32_t* eperm = perm;
+    if (with_delta) {
+      int32_t* perm2 = reinterpret_cast<int32_t*>(ws + L.perm2);
+      {
+        ProfScope ps(MOET_K_PROLOGUE, st);
+        gated_first_kernel<<<(E + kThreads / 32 - 1) / (kThreads / 32), kThreads, 0, st>>>(
+            E, k, T * k, expert_offsets, perm, delta_slot, gate_mask, perm2);
+      }
+      MOET_CUDA_TRY(cudaGetLastError());
+      eperm = perm2;
+    }
     PfForwardArgs f{};
     f.T = T; f.H = H; f.I = I; f.E = n_planes; f.k = k;   // E: experts the planes hold (tensor maps)
-    f.x = x; f.offsets = expert_offsets; f.perm = perm; f.topk_w = topk_w;
+    f.x = x; f.offsets = expert_offsets; f.perm = eperm; f.topk_w = topk_w;
     f.topk_idx = topk_idx; f.n_experts = E;
     f.fc1 = fc1; f.fc2 = fc2;
     f.delta_slot = with_delta ? delta_slot : nullptr;
@@ -694,7 +745,8 @@ static moet_status forward_impl(int T, int H, int I, int E, int k, const uint16_
     // FC1 of both lists (they write disjoint bucketed rows of h), then FC2 of both (disjoint
     // pairs of o); each engine's FC2 reads only its own rows of h
     if (hybrid) {
-      const TcForwardArgs g = tc_args(true);
+      TcForwardArgs g = tc_args(true);
+      g.perm = eperm;
       moet_status s = tc_forward_fc1(g, st);
       if (s != MOET_OK) return s;
       s = pf_forward_fc1(f, st);

@@ -100,7 +100,8 @@ struct PfMeta {
   int nck;                       // weight chunks (K / 256, doubled with the delta pass)
   int r0, r1;
   float sc2;
-  int pad[7];
+  int ncols_d;                   // delta pass: columns up to the last gated one (multiple of 16)
+  int pad[6];
   int pair[kPfTok];              // per column (token of the item): pair id t k + j, -1 = none
   float wts[kPfTok];             // FC2: routing weight x scale_2 x h scale of the pair
   uint8_t gated[kPfTok];         // 1 = the pair's token is gated
@@ -378,6 +379,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
       const PfMeta& um = sm.meta[m];
       const int pos0 = um.pos0, nck = um.nck, dslot = um.dslot;
       const int nb = (um.ncols + 63) / 64;                 // 64-row activation boxes per step
+      const int nbd = (um.ncols_d + 63) / 64;              // ... of a delta step
       const int w0 = um.e * a.N + um.r0, w1 = um.e * a.N + um.r1;
       const int d0 = dslot * a.N + um.r0, d1 = dslot * a.N + um.r1;
       for (int c = 0; c < nck && !bad; ++c, ++gc) {
@@ -411,9 +413,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
           const int bs = gs % kBRing;
           if (gs >= kBRing && !mbar_wait_warp(&sm.bdone[bs], ((gs / kBRing) - 1) & 1, wl)) { bad = true; break; }
           unsigned char* bst = base + kBBase + bs * kBStepBytes;
-          if (lane == 0) mbar_expect_tx(&sm.bfull[bs], (uint32_t)nb * 64u * 128u);
+          const int nbs = dp ? nbd : nb;
+          if (lane == 0) mbar_expect_tx(&sm.bfull[bs], (uint32_t)nbs * 64u * 128u);
           __syncwarp();
-          if (lane < nb)
+          if (lane < nbs)
             tma_load_2d(smem_addr(bst + 8192 * lane), dp ? &maps.actg : &maps.act, cc * kPC + s * kStepWeights,
                         pos0 + 64 * lane, &sm.bfull[bs]);
         }
@@ -443,6 +446,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
       asm volatile("tcgen05.fence::after_thread_sync;");
       const int nst = sm.meta[m].nck * (kPC / kStepWeights);
       const uint32_t idesc = f16_idesc<FC1>(sm.meta[m].ncols);   // FC1 bf16, FC2 fp16
+      const uint32_t idesc_d = f16_idesc<FC1>(sm.meta[m].ncols_d);   // the delta pass's steps
       // a group of kGrp steps per iteration: its A stages expanded (one wait), then each
       // step's activations (one wait per step: the activation ring is shallower than a group
       // plus the next)
@@ -463,7 +467,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
           const uint64_t bd = b_desc + (uint64_t)((bs * kBStepBytes) >> 4);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            mma_ta_elect(tmem, tmem + kPColA + 32 * as + 8 * i, bd + (uint64_t)((32 * i) >> 4), idesc,
+            mma_ta_elect(tmem, tmem + kPColA + 32 * as + 8 * i, bd + (uint64_t)((32 * i) >> 4),
+                         st >= nkc * (kPC / kStepWeights) ? idesc_d : idesc,
                          (st > 0 || h > 0 || i > 0) ? 1u : 0u);
           tc_commit_elect(&sm.bdone[bs]);
           last = gs + h;
@@ -506,6 +511,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
       PfMeta& um = sm.meta[m];
       const float sc2 = __ldg(a.scale_2 + pe);
       bool gated = false;
+      int last_g = -1;
       for (int t = lane; t < kPfTok; t += 32) {
         int pr = -1;
         float wv = 0.0f;
@@ -524,11 +530,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
         um.wts[t] = wv;
         um.gated[t] = gf;
         gated = gated || gf != 0;
+        if (gf) last_g = t;
       }
       if (!__any_sync(0xffffffffu, gated)) dslot = -1;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) last_g = max(last_g, __shfl_xor_sync(0xffffffffu, last_g, o));
       if (lane == 0) {
         um.e = pe; um.pos0 = pos0; um.ntok = ntok;
         um.ncols = ((ntok + 15) / 16) * 16;
+        um.ncols_d = ((last_g + 1 + 15) / 16) * 16;   // the delta reaches only gated columns
         um.dslot = dslot;
         um.nck = dslot >= 0 ? 2 * nkc : nkc;
         um.r0 = FC1 ? tile * 64 : tile * 128;
