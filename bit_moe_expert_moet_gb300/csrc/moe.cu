@@ -109,36 +109,76 @@ inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
 // A work item is a run of consecutive pairs of one expert, so only the items that reach into
 // the gated run make the delta pass, and within an item the gated pairs are the leading
 // columns.  Every pair's result depends only on its own column, so the layer's output is the
-// same as in the bucketed order.  One warp per expert; a pair id out of range counts as
-// ungated (the engines report it).
-__global__ void __launch_bounds__(kThreads) gated_first_kernel(int E, int k, int n_pairs,
-                                                               const int32_t* __restrict__ offsets,
+// same as in the bucketed order.  One CTA per expert: the gated count first (all loads in
+// flight), then 1024-pair chunks, four consecutive pairs per thread, placed by a block-wide
+// exclusive scan.  A pair id out of range counts as ungated (the engines report it).
+constexpr int kGfPer = 4;                       // pairs per thread per chunk
+
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  int base = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) {
+    const int t = warp_tot[w];
+    base += w < warp ? t : 0;
+    all += t;
+  }
+  __syncthreads();                               // warp_tot is reused by the next call
+  *total = all;
+  return base + incl - v;
+}
+
+__global__ void __launch_bounds__(kThreads) gated_first_kernel(int k, int n_pairs, const int32_t* __restrict__ offsets,
                                                                const int32_t* __restrict__ perm,
                                                                const int32_t* __restrict__ delta_slot,
                                                                const uint8_t* __restrict__ gate,
                                                                int32_t* __restrict__ perm2) {
-  const int e = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (e >= E) return;
+  __shared__ int warp_tot[kThreads / 32];
+  const int e = blockIdx.x, tid = threadIdx.x;
   const int off = __ldg(offsets + e), n = __ldg(offsets + e + 1) - off;
   if (n <= 0 || off < 0 || off + n > n_pairs) return;
-  const bool cached = __ldg(delta_slot + e) >= 0;
-  const uint32_t below = (1u << lane) - 1u;
-  auto is_gated = [&](int p) { return cached && p >= 0 && p < n_pairs && __ldg(gate + p / k) != 0; };
-  int G = 0;
-  for (int c = 0; c < n; c += 32) {
-    const int i = c + lane;
-    const bool g = i < n && is_gated(__ldg(perm + off + i));
-    G += __popc(__ballot_sync(0xffffffffu, g));
+  if (__ldg(delta_slot + e) < 0) {
+    for (int i = tid; i < n; i += kThreads) perm2[off + i] = __ldg(perm + off + i);
+    return;
   }
-  int gi = 0, ui = G;
-  for (int c = 0; c < n; c += 32) {
-    const int i = c + lane;
-    const int p = i < n ? __ldg(perm + off + i) : -1;
-    const bool g = i < n && is_gated(p);
-    const uint32_t mg = __ballot_sync(0xffffffffu, g), mu = __ballot_sync(0xffffffffu, i < n && !g);
-    if (i < n) perm2[off + (g ? gi + __popc(mg & below) : ui + __popc(mu & below))] = p;
-    gi += __popc(mg);
-    ui += __popc(mu);
+  auto is_gated = [&](int p) { return p >= 0 && p < n_pairs && __ldg(gate + p / k) != 0; };
+  int mine = 0;
+  for (int i = tid; i < n; i += kThreads) mine += is_gated(__ldg(perm + off + i)) ? 1 : 0;
+  int G = 0;
+  (void)block_exclusive_scan(mine, warp_tot, &G);
+  int gi = 0, ui = G;                            // next gated / ungated destination
+  for (int c = 0; c < n; c += kThreads * kGfPer) {
+    int p[kGfPer];
+    bool g[kGfPer];
+    int ng = 0, nu = 0;
+#pragma unroll
+    for (int q = 0; q < kGfPer; ++q) {
+      const int i = c + tid * kGfPer + q;
+      p[q] = i < n ? __ldg(perm + off + i) : -1;
+      g[q] = i < n && is_gated(p[q]);
+      ng += g[q] ? 1 : 0;
+      nu += (i < n && !g[q]) ? 1 : 0;
+    }
+    int tg = 0, tu = 0;
+    int pg = block_exclusive_scan(ng, warp_tot, &tg);
+    int pu = block_exclusive_scan(nu, warp_tot, &tu);
+#pragma unroll
+    for (int q = 0; q < kGfPer; ++q) {
+      const int i = c + tid * kGfPer + q;
+      if (i >= n) break;
+      if (g[q]) perm2[off + gi + pg++] = p[q];
+      else perm2[off + ui + pu++] = p[q];
+    }
+    gi += tg;
+    ui += tu;
   }
 }
 
@@ -719,8 +759,7 @@ static moet_status forward_impl(int T, int H, int I, int E, int k, const uint16_
       int32_t* perm2 = reinterpret_cast<int32_t*>(ws + L.perm2);
       {
         ProfScope ps(MOET_K_PROLOGUE, st);
-        gated_first_kernel<<<(E + kThreads / 32 - 1) / (kThreads / 32), kThreads, 0, st>>>(
-            E, k, T * k, expert_offsets, perm, delta_slot, gate_mask, perm2);
+        gated_first_kernel<<<E, kThreads, 0, st>>>(k, T * k, expert_offsets, perm, delta_slot, gate_mask, perm2);
       }
       MOET_CUDA_TRY(cudaGetLastError());
       eperm = perm2;
