@@ -236,38 +236,49 @@ __device__ __forceinline__ bool pair_in_delta_pass(int p, const int32_t* __restr
 
 // xb[pos] = x[token of perm[pos]] in the permuted K order; xbg the same for
 // gated pairs, zero for the others (written for the delta pass's pairs only:
-// xbg == null or delta_slot == null writes none).  Grid (pairs, ceil(H / 8 / 128)).
-__global__ void __launch_bounds__(128) pf_gather_kernel(int pairs, int k, int H, const uint16_t* __restrict__ x,
+// xbg == null or delta_slot == null writes none).  One CTA per row; a thread takes two
+// neighbouring 8-element outputs at a time (16-byte loads of both halves of their 32-group).
+constexpr int kGatherThreads = 224;
+__global__ void __launch_bounds__(kGatherThreads) pf_gather_kernel(int pairs, int k, int H, const uint16_t* __restrict__ x,
                                                         const int32_t* __restrict__ perm,
                                                         const uint8_t* __restrict__ gate,
                                                         const int32_t* __restrict__ topk_idx, int n_experts,
                                                         const int32_t* __restrict__ delta_slot, int n_slots,
                                                         uint16_t* __restrict__ xb, uint16_t* __restrict__ xbg) {
   const int pos = blockIdx.x;
-  const int t = blockIdx.y * 128 + threadIdx.x;              // 8 outputs: k' = 8 t .. 8 t + 7
-  if (t >= H / 8) return;
   const int p = __ldg(perm + pos);
-  uint4 v = make_uint4(0u, 0u, 0u, 0u);
-  bool gated = false, in_delta = false;
-  if (p >= 0 && p < pairs) {
-    const int tok = p / k;
-    gated = gate != nullptr && __ldg(gate + tok) != 0;
+  bool gated = false, in_delta = false, ok = p >= 0 && p < pairs;
+  if (ok) {
+    gated = gate != nullptr && __ldg(gate + p / k) != 0;
     in_delta = xbg != nullptr && delta_slot != nullptr &&
                pair_in_delta_pass(p, topk_idx, n_experts, delta_slot, n_slots);
-    // k' = 32 g + 2 c + b holds weight 32 g + c + 16 b; this thread covers c = 4 q .. 4 q + 3
-    const int g = t >> 2, q = t & 3;
-    const uint16_t* row = x + (size_t)tok * H + 32 * g + 4 * q;
-    const uint2 lo = __ldg(reinterpret_cast<const uint2*>(row));
-    const uint2 hi = __ldg(reinterpret_cast<const uint2*>(row + 16));
-    v.x = (lo.x & 0xFFFFu) | (hi.x << 16);
-    v.y = (lo.x >> 16) | (hi.x & 0xFFFF0000u);
-    v.z = (lo.y & 0xFFFFu) | (hi.y << 16);
-    v.w = (lo.y >> 16) | (hi.y & 0xFFFF0000u);
-  } else {
+  } else if (threadIdx.x == 0) {
     record_error(MOET_ERR_DEVICE_INDEX);
   }
-  reinterpret_cast<uint4*>(xb + (size_t)pos * H)[t] = v;
-  if (in_delta) reinterpret_cast<uint4*>(xbg + (size_t)pos * H)[t] = gated ? v : make_uint4(0u, 0u, 0u, 0u);
+  const uint16_t* xr = x + (size_t)(ok ? p / k : 0) * H;
+  uint4* out = reinterpret_cast<uint4*>(xb + (size_t)pos * H);
+  uint4* outg = reinterpret_cast<uint4*>(xbg + (size_t)pos * H);
+  // outputs t and t + 1 (t even): k' = 32 g + 2 c + b holds weight 32 g + c + 16 b, and the pair
+  // covers c = 8 r .. 8 r + 7 (t = 4 g + 2 r)
+  for (int tt = threadIdx.x; tt < H / 16; tt += kGatherThreads) {
+    const int g = tt >> 1, r = tt & 1;
+    uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+    if (ok) {
+      lo = __ldg(reinterpret_cast<const uint4*>(xr + 32 * g + 8 * r));
+      hi = __ldg(reinterpret_cast<const uint4*>(xr + 32 * g + 16 + 8 * r));
+    }
+    const uint4 v0 = make_uint4((lo.x & 0xFFFFu) | (hi.x << 16), (lo.x >> 16) | (hi.x & 0xFFFF0000u),
+                                (lo.y & 0xFFFFu) | (hi.y << 16), (lo.y >> 16) | (hi.y & 0xFFFF0000u));
+    const uint4 v1 = make_uint4((lo.z & 0xFFFFu) | (hi.z << 16), (lo.z >> 16) | (hi.z & 0xFFFF0000u),
+                                (lo.w & 0xFFFFu) | (hi.w << 16), (lo.w >> 16) | (hi.w & 0xFFFF0000u));
+    out[2 * tt] = v0;
+    out[2 * tt + 1] = v1;
+    if (in_delta) {
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      outg[2 * tt] = gated ? v0 : z;
+      outg[2 * tt + 1] = gated ? v1 : z;
+    }
+  }
 }
 
 // FC1's fp32 h (bucketed rows, natural K order) -> FC2's fp16 operand in the permuted K order
@@ -316,19 +327,28 @@ __global__ void __launch_bounds__(256) pf_h16_kernel(int pairs, int k, int I, co
   if (threadIdx.x == 0) hscale[pos] = ldexpf(1.0f, e);
   // 8 outputs per thread: k' = 8 t .. 8 t + 7 of the permuted order, where k' = 32 g + 2 c + b
   // holds element 32 g + c + 16 b
-  for (int t = threadIdx.x; t < I / 8; t += blockDim.x) {
-    const int g = t >> 2, q = t & 3;
-    const float4 lo = __ldg(reinterpret_cast<const float4*>(row + 32 * g + 4 * q));
-    const float4 hi = __ldg(reinterpret_cast<const float4*>(row + 32 * g + 16 + 4 * q));
-    const float a[4] = {lo.x, lo.y, lo.z, lo.w}, b[4] = {hi.x, hi.y, hi.z, hi.w};
-    uint32_t wv[4];
+  // two neighbouring outputs (t, t + 1, t even) per iteration: c = 8 r .. 8 r + 7 of group g
+  for (int tt = threadIdx.x; tt < I / 16; tt += blockDim.x) {
+    const int g = tt >> 1, r = tt & 1;
+    const float4* src = reinterpret_cast<const float4*>(row + 32 * g + 8 * r);
+    const float4 l0 = __ldg(src), l1 = __ldg(src + 1), h0 = __ldg(src + 4), h1 = __ldg(src + 5);
+    const float a[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+    const float b[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    uint32_t wv[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 8; ++i)
       wv[i] = (uint32_t)__half_as_ushort(__float2half_rn(a[i] * down)) |
               ((uint32_t)__half_as_ushort(__float2half_rn(b[i] * down)) << 16);
-    const uint4 v = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-    reinterpret_cast<uint4*>(h16 + (size_t)pos * I)[t] = v;
-    if (in_delta) reinterpret_cast<uint4*>(hg16 + (size_t)pos * I)[t] = gated ? v : make_uint4(0u, 0u, 0u, 0u);
+    const uint4 v0 = make_uint4(wv[0], wv[1], wv[2], wv[3]), v1 = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+    uint4* out = reinterpret_cast<uint4*>(h16 + (size_t)pos * I);
+    out[2 * tt] = v0;
+    out[2 * tt + 1] = v1;
+    if (in_delta) {
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      uint4* outg = reinterpret_cast<uint4*>(hg16 + (size_t)pos * I);
+      outg[2 * tt] = gated ? v0 : z;
+      outg[2 * tt + 1] = gated ? v1 : z;
+    }
   }
 }
 
@@ -727,8 +747,7 @@ moet_status pf_forward_fc1(const PfForwardArgs& f, cudaStream_t st) {
   const bool with_delta = f.delta_slot != nullptr && f.gate != nullptr;
   {
     ProfScope ps(MOET_K_TERMS, st);
-    const dim3 grid(pairs, (f.H / 8 + 127) / 128);
-    pf_gather_kernel<<<grid, 128, 0, st>>>(pairs, f.k, f.H, f.x, f.perm, with_delta ? f.gate : nullptr, f.topk_idx,
+    pf_gather_kernel<<<pairs, kGatherThreads, 0, st>>>(pairs, f.k, f.H, f.x, f.perm, with_delta ? f.gate : nullptr, f.topk_idx,
                                            f.n_experts, with_delta ? f.delta_slot : nullptr, f.n_slots, f.xb,
                                            with_delta ? f.xbg : nullptr);
   }
