@@ -421,6 +421,45 @@ def test_forward_prefill_two_lists(moet, gate_mode):
     check_y(yg, _oracle_forward(logits, xb, k, ref, dset, gate, E))
 
 
+@pytest.mark.parametrize("T", [64, 700], ids=["decode_engine", "prefill_engines"])
+def test_forward_pair_order_within_experts_leaves_y_unchanged(moet, T):
+    """Any order of the pairs inside each expert's bucket gives the same y bit for bit: every
+    pair's result depends only on its own column (the prefill regime relies on this when it
+    walks each cached expert's gated pairs first).  Skewed routing over 64 experts with delta
+    experts and a gate mask; the bucketing permutation is shuffled within every expert's range."""
+    H, I, E, k = 1024, 256, 64, 4
+    rng = np.random.default_rng(230 + T)
+    dset = np.array([0, 1, 5, 17, 40, 63], dtype=np.int32)
+    ref, gp = _make_layer(moet, H, I, E, dset, rng=rng)
+    bias = np.log(np.arange(1, E + 1, dtype=np.float64) ** -1.1)[rng.permutation(E)]
+    logits = (rng.standard_normal((T, E)) + bias).astype(np.float32)
+    xb = W.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    gate = (rng.random(T) < 0.3).astype(np.uint8)
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    off = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    perm = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    moet.route_topk(dev(logits), k, idx, w, off, perm)
+    x = dev(xb.view(np.int16)).view(torch.bfloat16)
+    ws = torch.empty(moet.forward_workspace_size(T, H, I, E, k), dtype=torch.uint8, device=DEV)
+    dkw = dict(delta_slot=dev(W.delta_slot_table(E, dset)), dfc1=gp[1, "d"], dfc2=gp[2, "d"], gate_mask=dev(gate))
+    ys = []
+    offs, pm = off.cpu().numpy(), perm.cpu().numpy()
+    for shuffle in (False, True):
+        pr = pm.copy()
+        if shuffle:
+            for e in range(E):
+                seg = pr[offs[e]:offs[e + 1]]
+                pr[offs[e]:offs[e + 1]] = seg[rng.permutation(len(seg))]
+            assert not np.array_equal(pr, pm)
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+        moet.moe_forward(x, idx, w, off, dev(pr), gp[1], gp[2], y, ws, **dkw)
+        ys.append(y)
+    torch.cuda.synchronize()
+    assert moet.last_device_error() == 0
+    assert torch.equal(ys[0], ys[1])
+
+
 @pytest.mark.parametrize("T", [100, 700])
 def test_forward_mma_sync_engine(moet, T):
     """Shapes the tcgen05 engines do not take (I = 384, not a multiple of 256) run the
