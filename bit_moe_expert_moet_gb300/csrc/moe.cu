@@ -77,7 +77,7 @@ inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   WsLayout L;
   const size_t pairs = (size_t)T * k;
   size_t off = 0;
-  L.hdr = off;       off += align256(16);
+  L.hdr = off;       off += align256(32);              // [0..2] item counts, ok; [4..5] unit counters
   L.tok_scale = off; off += align256(sizeof(float) * T);
   L.tok_max = off;   off += align256(sizeof(float) * T);
   L.hmax = off;      off += align256(sizeof(unsigned) * pairs);
@@ -203,7 +203,8 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(
     const int32_t* __restrict__ perm, int* __restrict__ hdr, float* __restrict__ tok_scale,
     float* __restrict__ tok_max, unsigned* __restrict__ hmax, int32_t* __restrict__ inv, int4* __restrict__ chunks,
     const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ expert_slot, int n_pool,
-    unsigned* __restrict__ miss_count, uint8_t* __restrict__ miss_mask, uint8_t* __restrict__ pvalid) {
+    unsigned* __restrict__ miss_count, uint8_t* __restrict__ miss_mask, uint8_t* __restrict__ pvalid,
+    const int32_t* __restrict__ delta_slot) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (blockIdx.x == 0) {
     if (warp != 0) return;
@@ -217,11 +218,19 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(
       lo[i] = e <= E ? __ldg(offsets + e) : 0;
     }
     int running = 0, running_s = 0;
+    // Two passes over the experts when a delta table is given and the batch has at least 8 tokens:
+    // the items of experts with a delta slot first (their units may carry the delta pass, three
+    // times the stages of a plain unit, and the decode engine hands units out in list order), then
+    // the others.  (Below 8 tokens the second pass, serial in this warp, costs more than the
+    // balancing saves.)
+    const int passes = delta_slot != nullptr && T >= 8 ? 2 : 1;
+    for (int pass = 0; pass < passes; ++pass)
 #pragma unroll
     for (int i = 0; i < kMaxPerLane; ++i) {
       const int c0 = 32 * i;
       if (c0 >= E) break;
       const int e = c0 + lane;
+      const bool take = passes == 1 || (e < E && __ldg(delta_slot + e) >= 0) == (pass == 0);
       // offsets[e + 1] of this lane is offsets[e'] of lane + 1 (or of lane 0 in the next group)
       const int up = __shfl_down_sync(0xffffffffu, lo[i], 1);
       const int nx = __shfl_sync(0xffffffffu, lo[i + 1], 0);
@@ -232,7 +241,7 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(
         if (expert_slot != nullptr) {
           pslot = __ldg(expert_slot + e);
           if (pslot >= n_pool) { record_error(MOET_ERR_DEVICE_INDEX); pslot = -1; }
-          if (pslot < 0 && n > 0) {
+          if (pslot < 0 && n > 0 && pass == 0) {
             if (miss_count != nullptr) atomicAdd(miss_count, (unsigned)n);
             if (miss_mask != nullptr) miss_mask[e] = 1;
           }
@@ -240,8 +249,8 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(
       }
       // an expert with at most small_max pairs goes to the second list (items of chunk_small)
       const bool small = small_max > 0 && n <= small_max;
-      const int nch = pslot >= 0 && !small ? (n + chunk - 1) / chunk : 0;
-      const int nchs = pslot >= 0 && small ? (n + chunk_small - 1) / chunk_small : 0;
+      const int nch = take && pslot >= 0 && !small ? (n + chunk - 1) / chunk : 0;
+      const int nchs = take && pslot >= 0 && small ? (n + chunk_small - 1) / chunk_small : 0;
       int incl = nch, incl_s = nchs;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -268,6 +277,8 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(
       hdr[0] = ok ? running : 0;
       hdr[1] = ok ? 1 : 0;
       hdr[2] = ok ? running_s : 0;
+      hdr[4] = 0;                                        // the decode engine's unit counters (FC1, FC2)
+      hdr[5] = 0;
     }
     return;
   }
@@ -718,7 +729,7 @@ static moet_status forward_impl(int T, int H, int I, int E, int k, const uint16_
                                                            chunks_s, x, expert_offsets, perm, hdr,
                                                            tok_scale, tok_max, hmax, use_tc ? inv : nullptr,
                                                            chunks, topk_idx, expert_slot, n_pool, miss_count,
-                                                           miss_mask, pvalid);
+                                                           miss_mask, pvalid, with_delta ? delta_slot : nullptr);
   }
   MOET_CUDA_TRY(cudaGetLastError());
 
@@ -742,6 +753,7 @@ static moet_status forward_impl(int T, int H, int I, int E, int k, const uint16_
     f.n_slots = n_slots; f.dfc1 = dfc1; f.dfc2 = dfc2;
     f.gate = with_delta ? gate_mask : nullptr;
     f.hdr = items ? hdr + 2 : hdr;
+    f.work = hdr + 4;
     f.chunks = items ? chunks_s : chunks;
     f.h = h; f.o = o; f.max_items = items ? pf_small_items(T, E, k) : mc;
     f.tokmax = tok_max; f.hmax = hmax; f.inv = inv;

@@ -462,6 +462,7 @@ struct FcTcArgs {
   int n_slots;
   const uint8_t* gate;
   const int* hdr;
+  int* work;                     // units handed out so far (one counter per launch, zeroed beforehand)
   const int4* chunks;
   const float* gsc;
   float* out;
@@ -539,9 +540,11 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
   TcSmem& sm = *reinterpret_cast<TcSmem*>(meta + kMeta);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wl = wait_limit();
+  // Units are handed out one at a time from a global counter (the scheduler warp takes the next
+  // one when a record slot is free), so CTAs that draw units with a delta pass (three times the
+  // stages) take fewer; items of delta experts come first in the item list.  The record after a
+  // CTA's last unit has nch = -1 and ends every role's loop.
   const int total_units = a.hdr[0] * a.tiles;
-  const int nunits = (int)blockIdx.x < total_units ? (total_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-  if (nunits == 0) return;
   const int nps = (a.K + kKC - 1) / kKC;        // plane stages per unit
 
   if (tid == 0) {
@@ -568,10 +571,11 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
     const int pw = warp == 0 ? 0 : 1;
     int g = 0;
     bool bad = false;
-    for (int j = 0; j < nunits && !bad; ++j) {
+    for (int j = 0; !bad; ++j) {
       const int m = j % kMeta;
       if (!mbar_wait_warp(&sm.meta_full[m], (j / kMeta) & 1, wl)) { bad = true; break; }
       const UnitMeta& um = meta[m];
+      if (um.nch < 0) break;                                  // no more units
       const int nch = um.nch, dslot = um.dslot;
       const int nbox = um.ncols / 16;
       const int y0 = (dslot >= 0 ? dslot : um.e) * a.N;      // delta rows only used by delta stages
@@ -653,9 +657,10 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
     int g = 0, last = -1;
     bool bad = false;
     const uint64_t raw_desc = sw128_desc(smem_addr(raw));
-    for (int j = 0; j < nunits && !bad; ++j) {
+    for (int j = 0; !bad; ++j) {
       const int m = j % kMeta, ab = j & 1;
       if (!mbar_wait_warp(&sm.meta_full[m], (j / kMeta) & 1, wl)) { bad = true; break; }
+      if (meta[m].nch < 0) break;                            // no more units
       if (j >= 2 && !mbar_wait_warp(&sm.acc_empty[ab], ((j >> 1) - 1) & 1, wl)) { bad = true; break; }
       if (__any_sync(0xffffffffu, is_stuck(sm))) { bad = true; break; }
       asm volatile("tcgen05.fence::after_thread_sync;");
@@ -699,14 +704,24 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
     __syncwarp();
   } else if (warp == 2) {
     // ---------------- scheduler
-    for (int j = 0; j < nunits; ++j) {
+    for (int j = 0;; ++j) {
       const int m = j % kMeta;
       if (j >= kMeta && !mbar_wait_warp(&sm.meta_empty[m], ((j / kMeta) - 1) & 1, wl)) {
         if (lane == 0) set_stuck(sm);
         break;
       }
       if (__any_sync(0xffffffffu, is_stuck(sm))) break;
-      const int u = (int)blockIdx.x + j * (int)gridDim.x;
+      int u = 0;
+      if (lane == 0) u = atomicAdd(a.work, 1);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      // (a test can make CTA 0 withhold its first record: every wait on it then runs out)
+      const bool withhold = blockIdx.x == 0 && j == 0 && *reinterpret_cast<volatile int*>(&g_dbg_withhold) != 0;
+      if (u >= total_units) {
+        if (lane == 0) meta[m].nch = -1;                     // the end record
+        __syncwarp();
+        if (lane == 0 && !withhold) mbar_arrive(&sm.meta_full[m]);
+        break;
+      }
       const int item = u / a.tiles, tile = u - item * a.tiles;
       const int4 ch = a.chunks[item];
       const int e = ch.x, ntok = ch.z;
@@ -752,17 +767,16 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
         um.sc2 = __ldg(a.scale_2 + pe);
       }
       __syncwarp();
-      // (a test can make CTA 0 withhold its first record: every wait on it then runs out)
-      const bool withhold = blockIdx.x == 0 && j == 0 && *reinterpret_cast<volatile int*>(&g_dbg_withhold) != 0;
       if (lane == 0 && !withhold) mbar_arrive(&sm.meta_full[m]);
     }
   } else if (warp >= 4 && warp < 8) {
     // ---------------- epilogue: TMEM lane quarter warp & 3
     const int trow = 32 * (warp & 3) + lane;
     const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;
-    for (int j = 0; j < nunits; ++j) {
+    for (int j = 0;; ++j) {
       const int m = j % kMeta, ab = j & 1;
       bool ok = mbar_wait_warp(&sm.meta_full[m], (j / kMeta) & 1, wl);
+      if (ok && meta[m].nch < 0) break;                      // no more units (same for all four warps)
       ok = ok && mbar_wait_warp(&sm.acc_full[ab], (j >> 1) & 1, wl);
       asm volatile("tcgen05.fence::after_thread_sync;");
       if (epi_any(!ok || is_stuck(sm))) {
@@ -849,9 +863,10 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
     const int praw1 = trow * 64 + (((2 * grp + 1) ^ ((trow >> 1) & 3)) << 4);
     int g = 0;
     bool bad = false;
-    for (int j = 0; j < nunits && !bad; ++j) {
+    for (int j = 0; !bad; ++j) {
       const int m = j % kMeta;
       if (!mbar_wait_warp(&sm.meta_full[m], (j / kMeta) & 1, wl)) { bad = true; break; }
+      if (meta[m].nch < 0) break;                            // no more units
       if (__any_sync(0xffffffffu, is_stuck(sm))) { bad = true; break; }
       const int nch = meta[m].nch, ncols = meta[m].ncols;
       for (int c = 0; c < nch; ++c, ++g) {
@@ -1013,6 +1028,7 @@ moet_status tc_forward_fc1(const TcForwardArgs& f, cudaStream_t st) {
   }
   MOET_CUDA_TRY(cudaGetLastError());
   FcTcArgs a1 = common_args(f);
+  a1.work = f.work;
   a1.K = f.H; a1.N = 2 * f.I;
   a1.scale_2 = f.fc1->scale_2;
   a1.gsc = f.buf.x_g;
@@ -1050,6 +1066,7 @@ moet_status tc_forward_fc2(const TcForwardArgs& f, cudaStream_t st) {
   }
   MOET_CUDA_TRY(cudaGetLastError());
   FcTcArgs a2 = common_args(f);
+  a2.work = f.work + 1;
   a2.K = f.I; a2.N = f.H;
   a2.scale_2 = f.fc2->scale_2;
   a2.gsc = f.buf.h_g;

@@ -42,6 +42,7 @@ struct TcForwardArgs {
   const moet_nvfp4* dfc2;
   const uint8_t* gate;         // nullable
   const int* hdr;              // [0] = number of work items
+  int* work;                   // [0] FC1, [1] FC2: units handed out so far (zeroed by the prologue)
   const int4* chunks;          // (expert, first pair, count <= kTcTok, pool slot of the planes)
   int item_rows;               // 1: activation-term rows at item * kTcTok + slot (act_rows =
                                //    kTcTok x the item-list capacity); 0: at the pair's bucketed
