@@ -77,7 +77,7 @@ inline WsLayout ws_layout(int T, int H, int I, int E, int k) {
   WsLayout L;
   const size_t pairs = (size_t)T * k;
   size_t off = 0;
-  L.hdr = off;       off += align256(32);              // [0..2] item counts, ok; [4..5] unit counters
+  L.hdr = off;       off += align256(32);              // [0..2] item counts, ok; [4..7] unit counters
   L.tok_scale = off; off += align256(sizeof(float) * T);
   L.tok_max = off;   off += align256(sizeof(float) * T);
   L.hmax = off;      off += align256(sizeof(unsigned) * pairs);
@@ -279,6 +279,8 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(
       hdr[2] = ok ? running_s : 0;
       hdr[4] = 0;                                        // the decode engine's unit counters (FC1, FC2)
       hdr[5] = 0;
+      hdr[6] = 0;                                        // the bf16 engine's (FC1, FC2)
+      hdr[7] = 0;
     }
     return;
   }
@@ -785,6 +787,7 @@ static moet_status forward_impl(int T, int H, int I, int E, int k, const uint16_
     f.n_slots = n_slots; f.dfc1 = dfc1; f.dfc2 = dfc2;
     f.gate = with_delta ? gate_mask : nullptr;
     f.hdr = hdr; f.chunks = chunks; f.o = o;
+    f.work = hdr + 6;
     const size_t pairs = (size_t)T * k;
     char* pb = ws + L.pfa;
     f.xb = reinterpret_cast<uint16_t*>(pb);  pb += align256(pairs * H * sizeof(uint16_t));

@@ -88,6 +88,7 @@ struct PfArgs {
   int n_slots;
   const uint8_t* gate;
   const int* hdr;
+  int* work;                     // units handed out so far (one counter per launch, zeroed beforehand)
   const int4* chunks;
   float* h;                      // FC1 output [pairs, I]
   const float* hscale;           // FC2: per bucketed row, the power of two that undoes the fp16 scaling of h
@@ -360,9 +361,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
   PfSmem& sm = *reinterpret_cast<PfSmem*>(base + kPMisc);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wl = wait_limit();
+  // Units are handed out one at a time from a global counter (the scheduler warp takes the next
+  // one when a record slot is free), so the uneven units (partial items, delta passes) spread over
+  // the CTAs; the record after a CTA's last unit has nck = -1 and ends every role's loop.
   const int total_units = a.hdr[0] * a.tiles;
-  const int nunits = (int)blockIdx.x < total_units ? (total_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-  if (nunits == 0) return;
   const int nkc = a.K / kPC;                   // weight chunks of the main pass
 
   if (tid == 0) {
@@ -393,10 +395,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
     // the activation producers take the 64-row activation steps in turn
     int gc = 0, gs = 0;
     bool bad = false;
-    for (int j = 0; j < nunits && !bad; ++j) {
+    for (int j = 0; !bad; ++j) {
       const int m = j % kPMeta;
       if (!mbar_wait_warp(&sm.meta_full[m], (j / kPMeta) & 1, wl)) { bad = true; break; }
       const PfMeta& um = sm.meta[m];
+      if (um.nck < 0) break;                                 // no more units
       const int pos0 = um.pos0, nck = um.nck, dslot = um.dslot;
       const int nb = (um.ncols + 63) / 64;                 // 64-row activation boxes per step
       const int nbd = (um.ncols_d + 63) / 64;              // ... of a delta step
@@ -458,9 +461,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
     int gs = 0, last = -1;
     bool bad = false;
     const uint64_t b_desc = sw128_desc(smem_addr(base + kBBase));
-    for (int j = 0; j < nunits && !bad; ++j) {
+    for (int j = 0; !bad; ++j) {
       const int m = j % kPMeta;
       if (!mbar_wait_warp(&sm.meta_full[m], (j / kPMeta) & 1, wl)) { bad = true; break; }
+      if (sm.meta[m].nck < 0) break;                         // no more units
       if (j >= 1 && !mbar_wait_warp(&sm.acc_empty, (j - 1) & 1, wl)) { bad = true; break; }
       if (__any_sync(0xffffffffu, pf_stuck(sm))) { bad = true; break; }
       asm volatile("tcgen05.fence::after_thread_sync;");
@@ -505,14 +509,24 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
     __syncwarp();
   } else if (warp == 2) {
     // ---------------- scheduler
-    for (int j = 0; j < nunits; ++j) {
+    for (int j = 0;; ++j) {
       const int m = j % kPMeta;
       if (j >= kPMeta && !mbar_wait_warp(&sm.meta_empty[m], ((j / kPMeta) - 1) & 1, wl)) {
         if (lane == 0) atomicExch(&sm.stuck, 1);
         break;
       }
       if (__any_sync(0xffffffffu, pf_stuck(sm))) break;
-      const int u = (int)blockIdx.x + j * (int)gridDim.x;
+      int u = 0;
+      if (lane == 0) u = atomicAdd(a.work, 1);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      // (a test can make CTA 0 withhold its first record: every wait on it then runs out)
+      const bool withhold = blockIdx.x == 0 && j == 0 && *reinterpret_cast<volatile int*>(&g_dbg_withhold) != 0;
+      if (u >= total_units) {
+        if (lane == 0) sm.meta[m].nck = -1;                  // the end record
+        __syncwarp();
+        if (lane == 0 && !withhold) mbar_arrive(&sm.meta_full[m]);
+        break;
+      }
       const int item = u / a.tiles, tile = u - item * a.tiles;
       const int4 ch = a.chunks[item];
       const int e = ch.x, ntok = ch.z;
@@ -566,8 +580,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
         um.sc2 = sc2;
       }
       __syncwarp();
-      // (a test can make CTA 0 withhold its first record: every wait on it then runs out)
-      const bool withhold = blockIdx.x == 0 && j == 0 && *reinterpret_cast<volatile int*>(&g_dbg_withhold) != 0;
       if (lane == 0 && !withhold) mbar_arrive(&sm.meta_full[m]);
     }
   } else if ((warp >= 4 && warp < 8) || warp >= 20) {
@@ -577,9 +589,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
     const int trow = 32 * (warp & 3) + lane;
     const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;
     const bool lo = lane < 16;                     // FC1: this lane holds a gate row, lane ^ 16 its up row
-    for (int j = 0; j < nunits; ++j) {
+    for (int j = 0;; ++j) {
       const int m = j % kPMeta;
       bool ok = mbar_wait_warp(&sm.meta_full[m], (j / kPMeta) & 1, wl);
+      if (ok && sm.meta[m].nck < 0) break;                   // no more units (same for all eight warps)
       ok = ok && mbar_wait_warp(&sm.acc_full, j & 1, wl);
       asm volatile("tcgen05.fence::after_thread_sync;");
       if (epi_any<32 * kPfEpiWarps>(!ok || pf_stuck(sm))) {
@@ -635,9 +648,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
     const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;
     int gc = 0, gs = 0;
     bool bad = false;
-    for (int j = 0; j < nunits && !bad; ++j) {
+    for (int j = 0; !bad; ++j) {
       const int m = j % kPMeta;
       if (!mbar_wait_warp(&sm.meta_full[m], (j / kPMeta) & 1, wl)) { bad = true; break; }
+      if (sm.meta[m].nck < 0) break;                         // no more units
       if (__any_sync(0xffffffffu, pf_stuck(sm))) { bad = true; break; }
       const int nck = sm.meta[m].nck;
       for (int c = 0; c < nck && !bad; ++c, ++gc) {
@@ -753,6 +767,7 @@ moet_status pf_forward_fc1(const PfForwardArgs& f, cudaStream_t st) {
   }
   MOET_CUDA_TRY(cudaGetLastError());
   PfArgs a1 = pf_common(f);
+  a1.work = f.work;
   a1.K = f.H; a1.N = 2 * f.I; a1.tiles = f.I / 64;
   a1.scale_2 = f.fc1->scale_2;
   a1.h = f.h;
@@ -770,6 +785,7 @@ moet_status pf_forward_fc2(const PfForwardArgs& f, cudaStream_t st) {
   }
   MOET_CUDA_TRY(cudaGetLastError());
   PfArgs a2 = pf_common(f);
+  a2.work = f.work + 1;
   a2.K = f.I; a2.N = f.H; a2.tiles = f.H / 128;
   a2.scale_2 = f.fc2->scale_2;
   a2.hscale = f.hscale;

@@ -38,6 +38,7 @@ struct PfForwardArgs {
   const moet_nvfp4* dfc2;
   const uint8_t* gate;         // nullable
   const int* hdr;              // [0] = number of work items
+  int* work;                   // [0] FC1, [1] FC2: units handed out so far (zeroed by the prologue)
   const int4* chunks;          // (expert, first pair, count <= kPfTok, pool slot of the planes)
   uint16_t* xb;                // [T k, H] bf16, bucketed rows, K permuted within 32-groups
   uint16_t* xbg;               // same, rows of ungated pairs zero
