@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(
     float* __restrict__ tok_max, unsigned* __restrict__ hmax, int32_t* __restrict__ inv, int4* __restrict__ chunks,
     const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ expert_slot, int n_pool,
     unsigned* __restrict__ miss_count, uint8_t* __restrict__ miss_mask, uint8_t* __restrict__ pvalid,
-    const int32_t* __restrict__ delta_slot) {
+    const int32_t* __restrict__ delta_slot, int rowmax_mode) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (blockIdx.x == 0) {
     if (warp != 0) return;
@@ -303,6 +303,18 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(
     }
   }
   if (gw >= T) return;
+  // The per-token max |x| (and its power-of-two scale) feeds the decode and mma.sync engines'
+  // input quantisation: every token (rowmax_mode 1), none (0: the bf16 engine alone), or in the
+  // prefill regime's split only tokens with a pair in the small-expert list (2).
+  if (rowmax_mode == 0) return;
+  if (rowmax_mode == 2) {
+    bool small = false;
+    if (lane < k) {
+      const int e = __ldg(topk_idx + (size_t)gw * k + lane);
+      small = e >= 0 && e < E && __ldg(offsets + e + 1) - __ldg(offsets + e) <= small_max;
+    }
+    if (!__any_sync(0xffffffffu, small)) return;
+  }
   const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)gw * H);
   float m = 0.0f;
   for (int i = lane; i < H / 8; i += 32) {
@@ -731,7 +743,8 @@ static moet_status forward_impl(int T, int H, int I, int E, int k, const uint16_
                                                            chunks_s, x, expert_offsets, perm, hdr,
                                                            tok_scale, tok_max, hmax, use_tc ? inv : nullptr,
                                                            chunks, topk_idx, expert_slot, n_pool, miss_count,
-                                                           miss_mask, pvalid, with_delta ? delta_slot : nullptr);
+                                                           miss_mask, pvalid, with_delta ? delta_slot : nullptr,
+                                                           hybrid ? 2 : use_pf ? 0 : 1);
   }
   MOET_CUDA_TRY(cudaGetLastError());
 
