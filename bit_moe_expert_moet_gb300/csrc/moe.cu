@@ -207,76 +207,90 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(
     const int32_t* __restrict__ delta_slot, int rowmax_mode) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (blockIdx.x == 0) {
-    if (warp != 0) return;
-    bool ok = __ldg(offsets) == 0 && __ldg(offsets + E) == T * k;
-    // all of this lane's offsets first (independent loads, one memory latency), then the scan
-    constexpr int kMaxPerLane = 1024 / 32;
-    int lo[kMaxPerLane + 1];
+    // The work items (lists chunks and chunks_small), built by the block's warps: warp w takes the
+    // 32-expert groups w, w + 8, ...  With a delta table the items of experts with a delta slot
+    // come first in each list (their units may carry the delta pass, three times the stages of a
+    // plain unit, and the engines hand units out in list order), then the others; within each
+    // class, expert order.  Per expert four item counts (list x class), scanned inside each group
+    // by warp shuffles and across groups in shared memory.
+    constexpr int kGroups = 1024 / 32;                  // E <= 1024
+    constexpr int kPerWarp = kGroups / (kThreads / 32);
+    __shared__ int gpre[kGroups][4];                    // per group: items of (list, class), then their prefix
+    __shared__ int tot[4];
+    __shared__ int okf;
+    if (tid == 0) okf = __ldg(offsets) == 0 && __ldg(offsets + E) == T * k;
+    __syncthreads();                                    // okf set before any warp may clear it
+    const bool split = delta_slot != nullptr;
+    const int ngroups = (E + 31) / 32;
+    int nv[kPerWarp], pv[kPerWarp], cnt[kPerWarp][4], excl[kPerWarp][4];
 #pragma unroll
-    for (int i = 0; i <= kMaxPerLane; ++i) {
-      const int e = 32 * i + lane;
-      lo[i] = e <= E ? __ldg(offsets + e) : 0;
-    }
-    int running = 0, running_s = 0;
-    // Two passes over the experts when a delta table is given and the batch has at least 8 tokens:
-    // the items of experts with a delta slot first (their units may carry the delta pass, three
-    // times the stages of a plain unit, and the decode engine hands units out in list order), then
-    // the others.  (Below 8 tokens the second pass, serial in this warp, costs more than the
-    // balancing saves.)
-    const int passes = delta_slot != nullptr && T >= 8 ? 2 : 1;
-    for (int pass = 0; pass < passes; ++pass)
-#pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
-      const int c0 = 32 * i;
-      if (c0 >= E) break;
-      const int e = c0 + lane;
-      const bool take = passes == 1 || (e < E && __ldg(delta_slot + e) >= 0) == (pass == 0);
-      // offsets[e + 1] of this lane is offsets[e'] of lane + 1 (or of lane 0 in the next group)
-      const int up = __shfl_down_sync(0xffffffffu, lo[i], 1);
-      const int nx = __shfl_sync(0xffffffffu, lo[i + 1], 0);
+    for (int r = 0; r < kPerWarp; ++r) {
+      const int g = warp + r * (kThreads / 32), e = 32 * g + lane;
       int n = 0, pslot = e;
-      if (e < E) {
-        n = (lane == 31 ? nx : up) - lo[i];
-        if (n < 0) { ok = false; n = 0; }
+      bool heavy = true;
+      if (g < ngroups && e < E) {
+        n = __ldg(offsets + e + 1) - __ldg(offsets + e);
+        if (n < 0) { okf = 0; n = 0; }
         if (expert_slot != nullptr) {
           pslot = __ldg(expert_slot + e);
           if (pslot >= n_pool) { record_error(MOET_ERR_DEVICE_INDEX); pslot = -1; }
-          if (pslot < 0 && n > 0 && pass == 0) {
+          if (pslot < 0 && n > 0) {
             if (miss_count != nullptr) atomicAdd(miss_count, (unsigned)n);
             if (miss_mask != nullptr) miss_mask[e] = 1;
           }
         }
+        heavy = !split || __ldg(delta_slot + e) >= 0;
       }
       // an expert with at most small_max pairs goes to the second list (items of chunk_small)
       const bool small = small_max > 0 && n <= small_max;
-      const int nch = take && pslot >= 0 && !small ? (n + chunk - 1) / chunk : 0;
-      const int nchs = take && pslot >= 0 && small ? (n + chunk_small - 1) / chunk_small : 0;
-      int incl = nch, incl_s = nchs;
+      const int nch = g < ngroups && e < E && pslot >= 0 && !small ? (n + chunk - 1) / chunk : 0;
+      const int nchs = g < ngroups && e < E && pslot >= 0 && small ? (n + chunk_small - 1) / chunk_small : 0;
+      nv[r] = n;
+      pv[r] = pslot;
+      cnt[r][0] = heavy ? nch : 0;   cnt[r][1] = heavy ? 0 : nch;      // list 0 (chunks): heavy, light
+      cnt[r][2] = heavy ? nchs : 0;  cnt[r][3] = heavy ? 0 : nchs;     // list 1 (chunks_small)
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        const int ys = __shfl_up_sync(0xffffffffu, incl_s, o);
-        if (lane >= o) { incl += y; incl_s += ys; }
+      for (int q = 0; q < 4; ++q) {
+        int incl = cnt[r][q];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        excl[r][q] = incl - cnt[r][q];
+        if (lane == 31 && g < ngroups) gpre[g][q] = incl;
       }
-      const int first = running + incl - nch;
-      for (int c = 0; c < nch; ++c) {
-        const int cnt = min(chunk, n - c * chunk);
-        chunks[first + c] = make_int4(e, c * chunk, cnt, pslot);
-      }
-      const int first_s = running_s + incl_s - nchs;
-      for (int c = 0; c < nchs; ++c) {
-        const int cnt = min(chunk_small, n - c * chunk_small);
-        chunks_small[first_s + c] = make_int4(e, c * chunk_small, cnt, pslot);
-      }
-      running += __shfl_sync(0xffffffffu, incl, 31);
-      running_s += __shfl_sync(0xffffffffu, incl_s, 31);
     }
-    ok = __all_sync(0xffffffffu, ok);
-    if (lane == 0) {
+    __syncthreads();
+    if (tid < 4) {
+      int running = 0;
+      for (int g = 0; g < ngroups; ++g) {
+        const int v = gpre[g][tid];
+        gpre[g][tid] = running;
+        running += v;
+      }
+      tot[tid] = running;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < kPerWarp; ++r) {
+      const int g = warp + r * (kThreads / 32), e = 32 * g + lane;
+      if (g >= ngroups || e >= E) continue;
+      const int n = nv[r], pslot = pv[r];
+      const int nch = cnt[r][0] + cnt[r][1], nchs = cnt[r][2] + cnt[r][3];
+      const int first = cnt[r][0] > 0 ? gpre[g][0] + excl[r][0] : tot[0] + gpre[g][1] + excl[r][1];
+      for (int c = 0; c < nch; ++c) chunks[first + c] = make_int4(e, c * chunk, min(chunk, n - c * chunk), pslot);
+      const int first_s = cnt[r][2] > 0 ? gpre[g][2] + excl[r][2] : tot[2] + gpre[g][3] + excl[r][3];
+      for (int c = 0; c < nchs; ++c)
+        chunks_small[first_s + c] = make_int4(e, c * chunk_small, min(chunk_small, n - c * chunk_small), pslot);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      const bool ok = okf != 0;
       if (!ok) record_error(MOET_ERR_DEVICE_INDEX);
-      hdr[0] = ok ? running : 0;
+      hdr[0] = ok ? tot[0] + tot[1] : 0;
       hdr[1] = ok ? 1 : 0;
-      hdr[2] = ok ? running_s : 0;
+      hdr[2] = ok ? tot[2] + tot[3] : 0;
       hdr[4] = 0;                                        // the decode engine's unit counters (FC1, FC2)
       hdr[5] = 0;
       hdr[6] = 0;                                        // the bf16 engine's (FC1, FC2)
