@@ -285,8 +285,12 @@ __global__ void __launch_bounds__(kGatherThreads) pf_gather_kernel(int pairs, in
 // FC1's fp32 h (bucketed rows, natural K order) -> FC2's fp16 operand in the permuted K order
 // (as xb), each row times the power of two 2^-e that puts its max |h| in [2^14, 2^15), and
 // hscale[pos] = 2^e; hg16 the same for gated pairs, zero for the others (for the delta pass's
-// pairs only, as xbg).  One CTA per row.
-__global__ void __launch_bounds__(256) pf_h16_kernel(int pairs, int k, int I, const float* __restrict__ h,
+// pairs only, as xbg).  One CTA per row; a thread holds J pairs of neighbouring 8-element outputs
+// (both halves of their 32-group, 64 bytes of h each) in registers, so h is read once: the row's
+// max |h| comes from those registers, then the same registers are scaled and stored.
+constexpr int kH16MaxThreads = 256;
+template <int J>
+__global__ void __launch_bounds__(kH16MaxThreads) pf_h16_kernel(int pairs, int k, int I, const float* __restrict__ h,
                                                      const int32_t* __restrict__ perm,
                                                      const uint8_t* __restrict__ gate,
                                                      const int32_t* __restrict__ topk_idx, int n_experts,
@@ -295,19 +299,32 @@ __global__ void __launch_bounds__(256) pf_h16_kernel(int pairs, int k, int I, co
                                                      float* __restrict__ hscale) {
   const int pos = blockIdx.x;
   const float* row = h + (size_t)pos * I;
-  __shared__ float red[8];
+  const int ntt = I / 16;
+  __shared__ float red[kH16MaxThreads / 32];
+  // output pair tt covers k' = 16 tt .. 16 tt + 15 of the permuted order, where k' = 32 g + 2 c + b
+  // holds element 32 g + c + 16 b: c = 8 r .. 8 r + 7 of group g (tt = 2 g + r)
+  float4 v[J][4];
   float mx = 0.0f;
-  for (int c = threadIdx.x; c < I / 4; c += blockDim.x) {
-    const float4 v = __ldg(reinterpret_cast<const float4*>(row) + c);
-    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int tt = threadIdx.x + j * blockDim.x;
+    if (tt < ntt) {
+      const float4* src = reinterpret_cast<const float4*>(row + 32 * (tt >> 1) + 8 * (tt & 1));
+      v[j][0] = __ldg(src);
+      v[j][1] = __ldg(src + 1);
+      v[j][2] = __ldg(src + 4);
+      v[j][3] = __ldg(src + 5);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[j][q].x), fabsf(v[j][q].y)), fmaxf(fabsf(v[j][q].z), fabsf(v[j][q].w))));
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
   __syncthreads();
   mx = red[0];
-#pragma unroll
-  for (int w = 1; w < 8; ++w) mx = fmaxf(mx, red[w]);
+  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) mx = fmaxf(mx, red[w]);
   // 2^-e with max * 2^-e in [2^14, 2^15): e = (exponent of max) - 15; a zero or non-finite
   // maximum keeps the row as it is
   int e = 0;
@@ -326,27 +343,24 @@ __global__ void __launch_bounds__(256) pf_h16_kernel(int pairs, int k, int I, co
     record_error(MOET_ERR_DEVICE_INDEX);
   }
   if (threadIdx.x == 0) hscale[pos] = ldexpf(1.0f, e);
-  // 8 outputs per thread: k' = 8 t .. 8 t + 7 of the permuted order, where k' = 32 g + 2 c + b
-  // holds element 32 g + c + 16 b
-  // two neighbouring outputs (t, t + 1, t even) per iteration: c = 8 r .. 8 r + 7 of group g
-  for (int tt = threadIdx.x; tt < I / 16; tt += blockDim.x) {
-    const int g = tt >> 1, r = tt & 1;
-    const float4* src = reinterpret_cast<const float4*>(row + 32 * g + 8 * r);
-    const float4 l0 = __ldg(src), l1 = __ldg(src + 1), h0 = __ldg(src + 4), h1 = __ldg(src + 5);
-    const float a[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
-    const float b[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+  uint4* out = reinterpret_cast<uint4*>(h16 + (size_t)pos * I);
+  uint4* outg = reinterpret_cast<uint4*>(hg16 + (size_t)pos * I);
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int tt = threadIdx.x + j * blockDim.x;
+    if (tt >= ntt) continue;
+    const float a[8] = {v[j][0].x, v[j][0].y, v[j][0].z, v[j][0].w, v[j][1].x, v[j][1].y, v[j][1].z, v[j][1].w};
+    const float b[8] = {v[j][2].x, v[j][2].y, v[j][2].z, v[j][2].w, v[j][3].x, v[j][3].y, v[j][3].z, v[j][3].w};
     uint32_t wv[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
       wv[i] = (uint32_t)__half_as_ushort(__float2half_rn(a[i] * down)) |
               ((uint32_t)__half_as_ushort(__float2half_rn(b[i] * down)) << 16);
     const uint4 v0 = make_uint4(wv[0], wv[1], wv[2], wv[3]), v1 = make_uint4(wv[4], wv[5], wv[6], wv[7]);
-    uint4* out = reinterpret_cast<uint4*>(h16 + (size_t)pos * I);
     out[2 * tt] = v0;
     out[2 * tt + 1] = v1;
     if (in_delta) {
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-      uint4* outg = reinterpret_cast<uint4*>(hg16 + (size_t)pos * I);
       outg[2 * tt] = gated ? v0 : z;
       outg[2 * tt + 1] = gated ? v1 : z;
     }
@@ -779,9 +793,15 @@ moet_status pf_forward_fc2(const PfForwardArgs& f, cudaStream_t st) {
   const bool with_delta = f.delta_slot != nullptr && f.gate != nullptr;
   {
     ProfScope ps(MOET_K_TERMS, st);
-    pf_h16_kernel<<<pairs, 256, 0, st>>>(pairs, f.k, f.I, f.h, f.perm, with_delta ? f.gate : nullptr, f.topk_idx,
-                                         f.n_experts, with_delta ? f.delta_slot : nullptr, f.n_slots, f.h16,
-                                         with_delta ? f.hg16 : nullptr, f.hscale);
+    // J output pairs per thread, the fewest that fit the row in kH16MaxThreads threads
+    // (pf_supported caps I at 4 * 16 * kH16MaxThreads)
+    const int ntt = f.I / 16;
+    const int J = ntt <= kH16MaxThreads ? 1 : ntt <= 2 * kH16MaxThreads ? 2 : 4;
+    const int threads = ((ntt + J - 1) / J + 31) / 32 * 32;
+    auto kern = J == 1 ? pf_h16_kernel<1> : J == 2 ? pf_h16_kernel<2> : pf_h16_kernel<4>;
+    kern<<<pairs, threads, 0, st>>>(pairs, f.k, f.I, f.h, f.perm, with_delta ? f.gate : nullptr, f.topk_idx,
+                                    f.n_experts, with_delta ? f.delta_slot : nullptr, f.n_slots, f.h16,
+                                    with_delta ? f.hg16 : nullptr, f.hscale);
   }
   MOET_CUDA_TRY(cudaGetLastError());
   PfArgs a2 = pf_common(f);

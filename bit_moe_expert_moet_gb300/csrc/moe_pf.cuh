@@ -12,7 +12,8 @@ namespace moet {
 constexpr int kPfTok = 256;   // routed pairs per work item -> MMA N <= 256
 
 // True when the bf16 engine handles this layer shape.
-inline bool pf_supported(int H, int I) { return H % 256 == 0 && I % 256 == 0; }
+// I <= 16384: the h -> fp16 kernel holds a row of h in at most 256 threads' registers.
+inline bool pf_supported(int H, int I) { return H % 256 == 0 && I % 256 == 0 && I <= 16384; }
 
 // Bytes of the engine's extra activation buffers for `pairs` routed pairs: x in
 // bucketed order as bf16 plus its gated copy (rows of ungated pairs zero), h as

@@ -135,9 +135,33 @@ constexpr int kTermThreads = 128;
 // per block) instead of one thread per block: latency- rather than throughput-bound.
 constexpr long long kCoopTermBlocks = 16384;
 
+// Two e2m1 codes (sign | 3-bit magnitude) by one hardware conversion, round to nearest even with
+// saturation at +-6: hi in bits 4-7, lo in bits 0-3.
+__device__ __forceinline__ uint32_t e2m1x2_rn(float hi, float lo) {
+  uint32_t r;
+  asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// The values of the two e2m1 codes in bits 0-3 (lo) and 4-7 (hi) of c.
+__device__ __forceinline__ void e2m1x2_values(uint32_t c, float& lo, float& hi) {
+  asm("{ .reg .b8 t; .reg .b16 l, h; .reg .b32 d; cvt.u8.u32 t, %2; cvt.rn.f16x2.e2m1x2 d, t;"
+      " mov.b32 {l, h}, d; cvt.f32.f16 %0, l; cvt.f32.f16 %1, h; }"
+      : "=f"(lo), "=f"(hi) : "r"(c));
+}
+
+// Exchange of the nibbles at the positions in m with those d nibbles above them.
+__device__ __forceinline__ uint64_t nibble_swap(uint64_t x, int d, uint64_t m) {
+  const uint64_t t = ((x >> (4 * d)) ^ x) & m;
+  return x ^ t ^ (t << (4 * d));
+}
+
 // The kTcTerms NVFP4 terms of one 16-element block r (the residual is updated in place) under the
 // row's first term scale g0: per term the codes in natural order (nat) and in the expansion's
-// order (per), two words each, and the ue4m3 block scale.
+// order (per), two words each, and the ue4m3 block scale.  A term's codes are RNE(r_i / sc) in
+// e2m1 (one conversion per two elements, ratios rounded to fp32 first; an exact tie may go
+// either way, which only changes what the next term quantises) and its residual is
+// r_i - value_i * sc in one fused multiply-add.
 __device__ __forceinline__ void block_terms(float (&r)[16], float g0, uint32_t (&nat)[kTcTerms][2],
                                             uint32_t (&per)[kTcTerms][2], uint32_t (&sfo)[kTcTerms]) {
 #pragma unroll
@@ -152,26 +176,27 @@ __device__ __forceinline__ void block_terms(float (&r)[16], float g0, uint32_t (
       sf = f32_to_e4m3_rn(bm / (6.0f * g));
       sc = e4m3_to_f32(sf) * g;
     }
-    uint32_t code[16];
+    const float inv = sc > 0.0f ? 1.0f / sc : 0.0f;     // sc = 0: every code 0, r unchanged
+    // natural order: nibble i holds element i
+    uint64_t n = 0;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      code[i] = 0;
-      if (sc > 0.0f) {
-        const uint32_t mg = e2m1_rne_mag(fabsf(r[i]), sc);
-        const bool neg = r[i] < 0.0f && mg != 0u;
-        const float q = e2m1_mag_value(mg) * sc;
-        r[i] -= neg ? -q : q;
-        code[i] = mg | (neg ? 8u : 0u);
-      }
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t c = e2m1x2_rn(r[2 * i + 1] * inv, r[2 * i] * inv);
+      float v0, v1;
+      e2m1x2_values(c, v0, v1);
+      r[2 * i] = fmaf(-v0, sc, r[2 * i]);
+      r[2 * i + 1] = fmaf(-v1, sc, r[2 * i + 1]);
+      n |= (uint64_t)c << (8 * i);
     }
-    // natural order: byte i holds elements 2i, 2i+1; permuted order: position p = 4 r + n
-    // holds element r + 4 n
-    nat[t][0] = nat[t][1] = per[t][0] = per[t][1] = 0u;
-#pragma unroll
-    for (int p = 0; p < 16; ++p) {
-      nat[t][p >> 3] |= code[p] << (4 * (p & 7));
-      per[t][p >> 3] |= code[(p >> 2) + 4 * (p & 3)] << (4 * (p & 7));
-    }
+    // expansion order: position p = 4 a + b holds element a + 4 b, the transpose of the 4 x 4
+    // nibble matrix (row a = nibbles 4 a .. 4 a + 3) by two exchanges: the off-diagonal 2 x 2
+    // blocks (nibbles 2, 3, 6, 7 <-> 8, 9, 12, 13), then inside each 2 x 2 block
+    uint64_t q = nibble_swap(n, 6, 0x00000000FF00FF00ull);
+    q = nibble_swap(q, 3, 0x0000F0F00000F0F0ull);
+    nat[t][0] = (uint32_t)n;
+    nat[t][1] = (uint32_t)(n >> 32);
+    per[t][0] = (uint32_t)q;
+    per[t][1] = (uint32_t)(q >> 32);
     sfo[t] = sf;
   }
 }

@@ -401,6 +401,24 @@ def test_forward_prefill_ragged_items(moet, gate_mode):
     check_y(yg, _oracle_forward(logits, xb, k, ref, dset, gate, E))
 
 
+@pytest.mark.parametrize("I", [4352, 12288], ids=["two_per_thread", "four_per_thread"])
+def test_forward_prefill_wide_intermediate(moet, I):
+    """Prefill engine with an intermediate size whose h row spans more than 256 threads' output
+    pairs (I / 16 = 272: two per thread, the last thread's second pair past the row; I / 16 = 768:
+    four per thread; about 300 pairs per expert, so items split at 256): the h -> fp16 step holds a row of h in registers, takes its max |h| there and
+    writes the permuted fp16 row and its gated copy from the same registers.  Every token checked."""
+    H, E, k, T = 256, 4, 2, 600
+    rng = np.random.default_rng(200 + I)
+    dset = np.array([1, 3], dtype=np.int32)
+    ref, gp = _make_layer(moet, H, I, E, dset, rng=rng)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    xb = W.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    gate = (rng.random(T) < 0.3).astype(np.uint8)
+    yg, err = _run_forward(moet, logits, xb, k, gp, E, H, dset, gate)
+    assert err == 0
+    check_y(yg, _oracle_forward(logits, xb, k, ref, dset, gate, E))
+
+
 @pytest.mark.parametrize("gate_mode", ["draw", "all"])
 def test_forward_prefill_two_lists(moet, gate_mode):
     """Prefill regime with skewed routing (a Zipf logit bias over 64 experts): hot experts (more
