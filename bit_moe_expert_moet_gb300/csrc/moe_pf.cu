@@ -616,32 +616,48 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
       const PfMeta& um = sm.meta[m];
       const int ncols = um.ncols, ntok = um.ntok, pos0 = um.pos0;
       const float sc2 = um.sc2;
-      for (int c0 = 16 * ehalf; c0 < ncols; c0 += 32) {
-        float v[16];
-        tmem_ld16(tmem + lane_q + c0, v);
-        if (!FC1) {
-          // output row trow; per column the routing weight x scale_2 x the row's h scale
-          const int wrow = um.r0 + trow;
+      // two of this warp's 16-column chunks (c0 and c0 + 32) per TMEM wait
+      for (int c0 = 16 * ehalf; c0 < ncols; c0 += 64) {
+        const bool two = c0 + 32 < ncols;                    // the same for the whole warp
+        float v2[2][16];
+        tmem_ld16_pair(tmem + lane_q + c0, two, v2[0], v2[1]);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int col = c0 + i;
-            const int p = um.pair[col];
-            if (col < ntok && p >= 0) a.o[(size_t)p * a.H + wrow] = v[i] * um.wts[col];
-          }
-        } else {
-          // SiLU(gate) * up: the gate lane finishes columns c0 .. c0 + 7, the up lane c0 + 8 .. c0 + 15;
-          // each hands the other the half it needs
-          float r[8];
+        for (int hh = 0; hh < 2; ++hh) {
+          if (hh == 1 && !two) break;
+          const int cc = c0 + 32 * hh;
+          const float* v = v2[hh];
+          if (!FC1) {
+            // output row trow; per column the routing weight x scale_2 x the row's h scale
+            float* orow = a.o + um.r0 + trow;
+            const int4* pp = reinterpret_cast<const int4*>(um.pair + cc);
+            const float4* wp = reinterpret_cast<const float4*>(um.wts + cc);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) r[i] = __shfl_xor_sync(0xffffffffu, lo ? v[8 + i] : v[i], 16);
-          const int cb = c0 + (lo ? 0 : 8);
-          const int hcol = um.r0 + 16 * (warp & 3) + (lane & 15);
+            for (int q = 0; q < 4; ++q) {
+              const int4 p4 = pp[q];
+              const float4 w4 = wp[q];
+              const int pq[4] = {p4.x, p4.y, p4.z, p4.w};
+              const float wq[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int col = cb + i;
-            if (col < ntok) {
-              const float gv = (lo ? v[i] : r[i]) * sc2, uv = (lo ? r[i] : v[8 + i]) * sc2;
-              a.h[(size_t)(pos0 + col) * a.I + hcol] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+              for (int t = 0; t < 4; ++t) {
+                const int col = cc + 4 * q + t;
+                if (col < ntok && pq[t] >= 0) orow[(size_t)pq[t] * a.H] = v[4 * q + t] * wq[t];
+              }
+            }
+          } else {
+            // SiLU(gate) * up: the gate lane finishes columns cc .. cc + 7, the up lane cc + 8 ..
+            // cc + 15; each hands the other the half it needs
+            float r[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) r[i] = __shfl_xor_sync(0xffffffffu, lo ? v[8 + i] : v[i], 16);
+            const int cb = cc + (lo ? 0 : 8);
+            const int hcol = um.r0 + 16 * (warp & 3) + (lane & 15);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int col = cb + i;
+              if (col < ntok) {
+                const float gv = (lo ? v[i] : r[i]) * sc2, uv = (lo ? r[i] : v[8 + i]) * sc2;
+                a.h[(size_t)(pos0 + col) * a.I + hcol] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+              }
             }
           }
         }

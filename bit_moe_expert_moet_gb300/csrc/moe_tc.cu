@@ -131,9 +131,6 @@ __device__ __forceinline__ uint4 planes_to_e2m1(uint32_t S, uint32_t M) {
 // writes it to the bucketed rows of its k pairs (inv = pair -> bucketed
 // position); FC2 expands each bucketed pair row in place (inv = null, ncopy = 1).
 constexpr int kTermThreads = 128;
-// Launches of at most this many 16-element blocks use the cooperative expansion (one half-warp
-// per block) instead of one thread per block: latency- rather than throughput-bound.
-constexpr long long kCoopTermBlocks = 16384;
 
 // Two e2m1 codes (sign | 3-bit magnitude) by one hardware conversion, round to nearest even with
 // saturation at +-6: hi in bits 4-7, lo in bits 0-3.
@@ -262,6 +259,28 @@ struct NatRows {
 // K order (8 bytes each per block), one ue4m3 scale per block, and g_t.  FC1 expands each token
 // once and writes it to the bucketed rows of its k pairs (inv = pair -> bucketed position); FC2
 // expands each bucketed pair row in place (inv = null, ncopy = 1; perm gives the row's pair).
+// The output rows of source row `row` (ncopy <= 32 of them) and whether each needs the
+// natural-order copy, looked up once per warp: lane cp holds copy cp's output row (-1: skipped,
+// out of range) and its flag, so the lookups of all copies are in flight together.  The row's
+// pair is token row x k + copy (FC1, inv given) or the bucketed row's pair (FC2, inv null).
+struct CopyInfo {
+  int orow;
+  bool want;
+};
+__device__ __forceinline__ CopyInfo copy_info(int row, int lane, const int32_t* __restrict__ inv, int ncopy,
+                                              int out_rows, const int32_t* __restrict__ perm, const NatRows& nr) {
+  CopyInfo ci{-1, false};
+  if (lane < ncopy) {
+    const int r = inv ? __ldg(inv + (size_t)row * ncopy + lane) : row;
+    if (r >= 0 && r < out_rows) {
+      ci.orow = r;
+      const int p = inv ? row * ncopy + lane : __ldg(perm + row);
+      ci.want = p >= 0 && p < out_rows && nr.want(p);
+    }
+  }
+  return ci;
+}
+
 template <bool BF16_IN>
 __global__ void __launch_bounds__(kTermThreads) act_terms_kernel(int K, const void* __restrict__ src,
                                                                 const int32_t* __restrict__ inv, int ncopy,
@@ -269,34 +288,35 @@ __global__ void __launch_bounds__(kTermThreads) act_terms_kernel(int K, const vo
                                                                 uint8_t* __restrict__ cperm, uint8_t* __restrict__ cnat,
                                                                 uint8_t* __restrict__ sfb, float* __restrict__ gsc,
                                                                 const int32_t* __restrict__ perm, NatRows nr) {
-  const int row = blockIdx.x, tid = threadIdx.x;
+  const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
   const size_t srow = (size_t)row;
   const float m = __ldg(rowmax + srow);
   const float g0 = m / (6.0f * 448.0f);
-  // output rows of this source row (out of range entries are skipped)
-  auto out_row = [&](int cp) -> int {
-    const int r = inv ? __ldg(inv + (size_t)row * ncopy + cp) : row;
-    return r >= 0 && r < out_rows ? r : -1;
-  };
-  if (blockIdx.y == 0 && tid < kTcTerms) {
+  const CopyInfo ci = copy_info(row, lane, inv, ncopy, out_rows, perm, nr);
+  const int b = blockIdx.y * kTermThreads + tid;            // 16-element block of the row
+  const bool active = b < K / 16;
+  if (blockIdx.y == 0 && tid < 32) {
     for (int cp = 0; cp < ncopy; ++cp) {
-      const int orow = out_row(cp);
-      if (orow >= 0) gsc[(size_t)orow * kTcTerms + tid] = ldexpf(g0, -2 * tid);
+      const int orow = __shfl_sync(0xffffffffu, ci.orow, cp);
+      if (orow >= 0 && lane < kTcTerms) gsc[(size_t)orow * kTcTerms + lane] = ldexpf(g0, -2 * lane);
     }
   }
-  const int b = blockIdx.y * kTermThreads + tid;            // 16-element block of the row
-  if (b >= K / 16) return;
+  if (__all_sync(0xffffffffu, !active)) return;            // the whole warp is past the row's end
+  // every lane of the warp stays (the copies' rows come from lanes 0 .. ncopy - 1); lanes past
+  // the row's end expand zeros and store nothing
   float r[16];
-  load_block<BF16_IN>(src, srow, K, b, r);
+  if (active) {
+    load_block<BF16_IN>(src, srow, K, b, r);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) r[i] = 0.0f;
+  }
   uint32_t nat[kTcTerms][2], per[kTcTerms][2], sfo[kTcTerms];
   block_terms(r, g0, nat, per, sfo);
   for (int cp = 0; cp < ncopy; ++cp) {
-    const int orow = out_row(cp);
-    if (orow < 0) continue;
-    // the row's pair: token row x k + copy (FC1), or the bucketed row's pair (FC2)
-    const int p = inv ? row * ncopy + cp : __ldg(perm + row);
-    const bool want_nat = p >= 0 && p < out_rows && nr.want(p);
-    store_block_terms(K, b, (size_t)orow, nat, per, sfo, cperm, cnat, sfb, want_nat);
+    const int orow = __shfl_sync(0xffffffffu, ci.orow, cp);
+    const bool want = __shfl_sync(0xffffffffu, ci.want ? 1 : 0, cp) != 0;
+    if (orow >= 0 && active) store_block_terms(K, b, (size_t)orow, nat, per, sfo, cperm, cnat, sfb, want);
   }
 }
 
@@ -340,130 +360,6 @@ __global__ void __launch_bounds__(256) act_terms_items_kernel(int K, const void*
     uint32_t nat[kTcTerms][2], per[kTcTerms][2], sfo[kTcTerms];
     block_terms(r, g0, nat, per, sfo);
     store_block_terms(K, b, (size_t)row, nat, per, sfo, cperm, cnat, sfb, nr.want(p));
-  }
-}
-
-// Cooperative expansion: the 16 lanes of a half-warp hold the 16 elements of one block (lane
-// e = lane & 15 holds element e).  Per term t, under the scale g = g0 / 4^t: the block maximum m
-// of the current residuals (four xor-shuffles inside the half), the ue4m3 block scale
-// sf = RNE(m / (6 g)) and sc = sf g, and per element the e2m1 code of RNE(|r| / sc) (ties to
-// even, saturating) with r's sign unless the magnitude is zero; the element's residual r then
-// loses the code's value times sc.  The 4-bit codes are packed by OR-reductions -- natural order:
-// word e >> 3, nibble e & 7 (lanes differing in bits 0-2 of e); expansion order: position
-// 4 (e & 3) + (e >> 2), i.e. word (e & 3) >> 1, nibble 4 (e & 1) + (e >> 2) (lanes differing in
-// bits 0, 2, 3 of e).  Afterwards every lane holds natural word e >> 3 and expansion word
-// (e & 3) >> 1 of each term, and the term's block scale.  Every lane of the warp takes part.
-__device__ __forceinline__ void coop_terms(float r, float g0, int e, uint32_t (&natw)[kTcTerms],
-                                           uint32_t (&perw)[kTcTerms], uint32_t (&sfo)[kTcTerms]) {
-#pragma unroll
-  for (int t = 0; t < kTcTerms; ++t) {
-    const float g = ldexpf(g0, -2 * t);
-    float bm = fabsf(r);
-    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
-    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
-    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
-    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
-    uint32_t sf = 0;
-    float sc = 0.0f;
-    if (g > 0.0f) {
-      sf = f32_to_e4m3_rn(bm / (6.0f * g));
-      sc = e4m3_to_f32(sf) * g;
-    }
-    uint32_t code = 0;
-    if (sc > 0.0f) {
-      const uint32_t mg = e2m1_rne_mag(fabsf(r), sc);
-      const bool neg = r < 0.0f && mg != 0u;
-      const float q = e2m1_mag_value(mg) * sc;
-      r -= neg ? -q : q;
-      code = mg | (neg ? 8u : 0u);
-    }
-    uint32_t vn = code << (4 * (e & 7));
-    vn |= __shfl_xor_sync(0xffffffffu, vn, 1);
-    vn |= __shfl_xor_sync(0xffffffffu, vn, 2);
-    vn |= __shfl_xor_sync(0xffffffffu, vn, 4);
-    uint32_t vp = code << (4 * (4 * (e & 1) + (e >> 2)));
-    vp |= __shfl_xor_sync(0xffffffffu, vp, 1);
-    vp |= __shfl_xor_sync(0xffffffffu, vp, 4);
-    vp |= __shfl_xor_sync(0xffffffffu, vp, 8);
-    natw[t] = vn;
-    perw[t] = vp;
-    sfo[t] = sf;
-  }
-}
-
-// One element of block b of a row: bf16 (FC1 input x) or fp32 (FC2 input h).
-template <bool BF16_IN>
-__device__ __forceinline__ float load_elem(const void* __restrict__ src, size_t srow, int K, int b, int e) {
-  if (BF16_IN)
-    return __uint_as_float((uint32_t)__ldg(static_cast<const uint16_t*>(src) + srow * K + 16 * b + e) << 16);
-  return __ldg(static_cast<const float*>(src) + srow * K + 16 * b + e);
-}
-
-// The writes of one block's terms to output row orow, shared among the half's lanes: lane e = 0
-// writes natural word 0, expansion word 0 and the block scales, lane 8 natural word 1, lane 2
-// expansion word 1.
-__device__ __forceinline__ void coop_store(int K, int b, size_t orow, int e, const uint32_t (&natw)[kTcTerms],
-                                           const uint32_t (&perw)[kTcTerms], const uint32_t (&sfo)[kTcTerms],
-                                           uint8_t* __restrict__ cperm, uint8_t* __restrict__ cnat,
-                                           uint8_t* __restrict__ sfb, bool want_nat) {
-  if (e != 0 && e != 2 && e != 8) return;
-#pragma unroll
-  for (int t = 0; t < kTcTerms; ++t) {
-    const size_t term_row = orow * kTcTerms + t;
-    uint32_t* cn = reinterpret_cast<uint32_t*>(cnat + term_row * (K / 2) + 8 * b);
-    uint32_t* cq = reinterpret_cast<uint32_t*>(cperm + term_row * (K / 2) + 8 * b);
-    if (e == 0) {
-      if (want_nat) cn[0] = natw[t];
-      cq[0] = perw[t];
-      sfb[term_row * (K / 16) + b] = (uint8_t)sfo[t];
-    } else if (e == 8) {
-      if (want_nat) cn[1] = natw[t];
-    } else {
-      cq[1] = perw[t];
-    }
-  }
-}
-
-// act_terms_kernel with one half-warp per block (coop_terms): grid (source rows,
-// ceil(K / 16 / 8)), the same outputs.  For launches with few blocks (small batches), where the
-// serial expansion's per-thread latency dominates (T = 1: 31 -> 21 us for the two launches of a
-// step); with many blocks it executes twice the instructions and is slower (T = 64: 35 -> 62 us).
-template <bool BF16_IN>
-__global__ void __launch_bounds__(kTermThreads) act_terms_coop_kernel(int K, const void* __restrict__ src,
-                                                                const int32_t* __restrict__ inv, int ncopy,
-                                                                int out_rows, const float* __restrict__ rowmax,
-                                                                uint8_t* __restrict__ cperm, uint8_t* __restrict__ cnat,
-                                                                uint8_t* __restrict__ sfb, float* __restrict__ gsc,
-                                                                const int32_t* __restrict__ perm, NatRows nr) {
-  const int row = blockIdx.x, tid = threadIdx.x;
-  const size_t srow = (size_t)row;
-  const float m = __ldg(rowmax + srow);
-  const float g0 = m / (6.0f * 448.0f);
-  // output rows of this source row (out of range entries are skipped)
-  auto out_row = [&](int cp) -> int {
-    const int r = inv ? __ldg(inv + (size_t)row * ncopy + cp) : row;
-    return r >= 0 && r < out_rows ? r : -1;
-  };
-  if (blockIdx.y == 0 && tid < kTcTerms) {
-    for (int cp = 0; cp < ncopy; ++cp) {
-      const int orow = out_row(cp);
-      if (orow >= 0) gsc[(size_t)orow * kTcTerms + tid] = ldexpf(g0, -2 * tid);
-    }
-  }
-  const int e = tid & 15;
-  const int b = blockIdx.y * (kTermThreads / 16) + (tid >> 4);     // 16-element block of the row
-  const bool active = b < K / 16;
-  const float r = active ? load_elem<BF16_IN>(src, srow, K, b, e) : 0.0f;
-  uint32_t natw[kTcTerms], perw[kTcTerms], sfo[kTcTerms];
-  coop_terms(r, g0, e, natw, perw, sfo);
-  if (!active) return;
-  for (int cp = 0; cp < ncopy; ++cp) {
-    const int orow = out_row(cp);
-    if (orow < 0) continue;
-    // the row's pair: token row x k + copy (FC1), or the bucketed row's pair (FC2)
-    const int p = inv ? row * ncopy + cp : __ldg(perm + row);
-    const bool want_nat = p >= 0 && p < out_rows && nr.want(p);
-    coop_store(K, b, (size_t)orow, e, natw, perw, sfo, cperm, cnat, sfb, want_nat);
   }
 }
 
@@ -1038,17 +934,9 @@ moet_status tc_forward_fc1(const TcForwardArgs& f, cudaStream_t st) {
     } else {
       // each token once, written to the bucketed rows of its k pairs so that a work item's term
       // rows are consecutive
-      if ((long long)f.T * (f.H / 16) <= kCoopTermBlocks) {
-        const dim3 grid(f.T, (f.H / 16 + kTermThreads / 16 - 1) / (kTermThreads / 16));
-        act_terms_coop_kernel<true><<<grid, kTermThreads, 0, st>>>(f.H, f.x, f.inv, f.k, pairs, f.tokmax,
-                                                                   f.buf.x_cperm, f.buf.x_cnat, f.buf.x_sf, f.buf.x_g,
-                                                                   f.perm, nat_rows(f));
-      } else {
-        const dim3 grid(f.T, (f.H / 16 + kTermThreads - 1) / kTermThreads);
-        act_terms_kernel<true><<<grid, kTermThreads, 0, st>>>(f.H, f.x, f.inv, f.k, pairs, f.tokmax, f.buf.x_cperm,
-                                                              f.buf.x_cnat, f.buf.x_sf, f.buf.x_g, f.perm,
-                                                              nat_rows(f));
-      }
+      const dim3 grid(f.T, (f.H / 16 + kTermThreads - 1) / kTermThreads);
+      act_terms_kernel<true><<<grid, kTermThreads, 0, st>>>(f.H, f.x, f.inv, f.k, pairs, f.tokmax, f.buf.x_cperm,
+                                                            f.buf.x_cnat, f.buf.x_sf, f.buf.x_g, f.perm, nat_rows(f));
     }
   }
   MOET_CUDA_TRY(cudaGetLastError());
@@ -1074,19 +962,10 @@ moet_status tc_forward_fc2(const TcForwardArgs& f, cudaStream_t st) {
                                                                   nat_rows(f));
     } else {
       // one row per bucketed pair (h rows are in bucketed order)
-      if ((long long)pairs * (f.I / 16) <= kCoopTermBlocks) {
-        const dim3 grid(pairs, (f.I / 16 + kTermThreads / 16 - 1) / (kTermThreads / 16));
-        act_terms_coop_kernel<false><<<grid, kTermThreads, 0, st>>>(f.I, f.h, nullptr, 1, pairs,
-                                                                    reinterpret_cast<const float*>(f.hmax),
-                                                                    f.buf.h_cperm, f.buf.h_cnat, f.buf.h_sf,
-                                                                    f.buf.h_g, f.perm, nat_rows(f));
-      } else {
-        const dim3 grid(pairs, (f.I / 16 + kTermThreads - 1) / kTermThreads);
-        act_terms_kernel<false><<<grid, kTermThreads, 0, st>>>(f.I, f.h, nullptr, 1, pairs,
-                                                               reinterpret_cast<const float*>(f.hmax), f.buf.h_cperm,
-                                                               f.buf.h_cnat, f.buf.h_sf, f.buf.h_g, f.perm,
-                                                               nat_rows(f));
-      }
+      const dim3 grid(pairs, (f.I / 16 + kTermThreads - 1) / kTermThreads);
+      act_terms_kernel<false><<<grid, kTermThreads, 0, st>>>(f.I, f.h, nullptr, 1, pairs,
+                                                             reinterpret_cast<const float*>(f.hmax), f.buf.h_cperm,
+                                                             f.buf.h_cnat, f.buf.h_sf, f.buf.h_g, f.perm, nat_rows(f));
     }
   }
   MOET_CUDA_TRY(cudaGetLastError());
