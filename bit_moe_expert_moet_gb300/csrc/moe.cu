@@ -141,6 +141,8 @@ __global__ void __launch_bounds__(kThreads) gated_first_kernel(int k, int n_pair
                                                                const int32_t* __restrict__ delta_slot,
                                                                const uint8_t* __restrict__ gate,
                                                                int32_t* __restrict__ perm2) {
+  pdl_wait();                                  // the previous kernel is complete
+  pdl_trigger();
   __shared__ int warp_tot[kThreads / 32];
   const int e = blockIdx.x, tid = threadIdx.x;
   const int off = __ldg(offsets + e), n = __ldg(offsets + e + 1) - off;
@@ -205,6 +207,8 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(
     const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ expert_slot, int n_pool,
     unsigned* __restrict__ miss_count, uint8_t* __restrict__ miss_mask, uint8_t* __restrict__ pvalid,
     const int32_t* __restrict__ delta_slot, int rowmax_mode) {
+  pdl_wait();                                  // the previous kernel is complete
+  pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (blockIdx.x == 0) {
     // The work items (lists chunks and chunks_small), built by the block's warps: warp w takes the
@@ -380,6 +384,8 @@ struct FcArgs {
 
 template <bool FC1, int NT>
 __global__ void __launch_bounds__(kThreads, 2) fc_kernel(const FcArgs a) {
+  pdl_wait();                                  // the previous kernel is complete
+  pdl_trigger();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
@@ -632,6 +638,8 @@ constexpr int kCombineCtasPerSm = 4;            // guaranteed by the launch boun
 __global__ void __launch_bounds__(kThreads, kCombineCtasPerSm)
     combine_kernel(int T, int H, int k, const int* __restrict__ hdr, const float* __restrict__ o,
                    const uint8_t* __restrict__ pvalid, uint16_t* __restrict__ y) {
+  pdl_wait();                                  // the previous kernel is complete
+  pdl_trigger();
   const long long n4 = (long long)T * H / 4;
   const bool ok = hdr[1] != 0;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
@@ -671,7 +679,7 @@ static moet_status launch_fc(const FcArgs& a, int row_tiles, int grid_y, cudaStr
   MOET_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   {
     ProfScope ps(FC1 ? MOET_K_FC1 : MOET_K_FC2, st);
-    kern<<<dim3(row_tiles, grid_y), kThreads, smem, st>>>(a);
+    MOET_CUDA_TRY(pdl_launch(false, kern, dim3(dim3(row_tiles, grid_y)), dim3(kThreads), smem, st, a));
   }
   MOET_CUDA_TRY(cudaGetLastError());
   return MOET_OK;
@@ -753,12 +761,12 @@ static moet_status forward_impl(int T, int H, int I, int E, int k, const uint16_
   int4* chunks_s = hybrid ? reinterpret_cast<int4*>(ws + L.chunks_s) : nullptr;
   {
     ProfScope ps(MOET_K_PROLOGUE, st);
-    prologue_kernel<<<1 + (T + 7) / 8, kThreads, 0, st>>>(T, H, E, k, chunk, kTcTok, hybrid ? kPfSmallMax : 0,
+    MOET_CUDA_TRY(pdl_launch(use_tc, prologue_kernel, dim3(1 + (T + 7) / 8), dim3(kThreads), 0, st, T, H, E, k, chunk, kTcTok, hybrid ? kPfSmallMax : 0,
                                                            chunks_s, x, expert_offsets, perm, hdr,
                                                            tok_scale, tok_max, hmax, use_tc ? inv : nullptr,
                                                            chunks, topk_idx, expert_slot, n_pool, miss_count,
                                                            miss_mask, pvalid, with_delta ? delta_slot : nullptr,
-                                                           hybrid ? 2 : use_pf ? 0 : 1);
+                                                           hybrid ? 2 : use_pf ? 0 : 1));
   }
   MOET_CUDA_TRY(cudaGetLastError());
 
@@ -800,7 +808,7 @@ static moet_status forward_impl(int T, int H, int I, int E, int k, const uint16_
       int32_t* perm2 = reinterpret_cast<int32_t*>(ws + L.perm2);
       {
         ProfScope ps(MOET_K_PROLOGUE, st);
-        gated_first_kernel<<<E, kThreads, 0, st>>>(k, T * k, expert_offsets, perm, delta_slot, gate_mask, perm2);
+        MOET_CUDA_TRY(pdl_launch(false, gated_first_kernel, dim3(E), dim3(kThreads), 0, st, k, T * k, expert_offsets, perm, delta_slot, gate_mask, perm2));
       }
       MOET_CUDA_TRY(cudaGetLastError());
       eperm = perm2;
@@ -881,7 +889,7 @@ static moet_status forward_impl(int T, int H, int I, int E, int k, const uint16_
   const int gc = (int)gcl;
   {
     ProfScope ps(MOET_K_COMBINE, st);
-    combine_kernel<<<gc, kThreads, 0, st>>>(T, H, k, hdr, o, pvalid, y);
+    MOET_CUDA_TRY(pdl_launch(use_tc, combine_kernel, dim3(gc), dim3(kThreads), 0, st, T, H, k, hdr, o, pvalid, y));
   }
   MOET_CUDA_TRY(cudaGetLastError());
   return MOET_OK;

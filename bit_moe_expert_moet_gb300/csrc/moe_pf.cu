@@ -246,6 +246,8 @@ __global__ void __launch_bounds__(kGatherThreads) pf_gather_kernel(int pairs, in
                                                         const int32_t* __restrict__ topk_idx, int n_experts,
                                                         const int32_t* __restrict__ delta_slot, int n_slots,
                                                         uint16_t* __restrict__ xb, uint16_t* __restrict__ xbg) {
+  pdl_wait();                                  // the previous kernel is complete
+  pdl_trigger();
   const int pos = blockIdx.x;
   const int p = __ldg(perm + pos);
   bool gated = false, in_delta = false, ok = p >= 0 && p < pairs;
@@ -297,6 +299,8 @@ __global__ void __launch_bounds__(kH16MaxThreads) pf_h16_kernel(int pairs, int k
                                                      const int32_t* __restrict__ delta_slot, int n_slots,
                                                      uint16_t* __restrict__ h16, uint16_t* __restrict__ hg16,
                                                      float* __restrict__ hscale) {
+  pdl_wait();                                  // the previous kernel is complete
+  pdl_trigger();
   const int pos = blockIdx.x;
   const float* row = h + (size_t)pos * I;
   const int ntt = I / 16;
@@ -378,7 +382,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
   // Units are handed out one at a time from a global counter (the scheduler warp takes the next
   // one when a record slot is free), so the uneven units (partial items, delta passes) spread over
   // the CTAs; the record after a CTA's last unit has nck = -1 and ends every role's loop.
-  const int total_units = a.hdr[0] * a.tiles;
   const int nkc = a.K / kPC;                   // weight chunks of the main pass
 
   if (tid == 0) {
@@ -401,6 +404,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_fc_kernel(const PfArgs a, co
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;");
   const uint32_t tmem = sm.tmem_base;
+  // set-up above overlaps the previous kernel; its outputs are read from here on
+  pdl_wait();
+  pdl_trigger();
+  const int total_units = a.hdr[0] * a.tiles;
 
   // activation producers 3, 16, 18, 19: none on the MMA thread's sub-partition (warp % 4 == 1)
   const int bprod = warp == 3 ? 0 : warp == 16 ? 1 : warp == 18 ? 2 : warp == 19 ? 3 : -1;
@@ -765,7 +772,7 @@ moet_status launch_pf(const PfArgs& a, const moet_planes* pl, const moet_nvfp4* 
   MOET_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPfSmemBytes));
   {
     ProfScope ps(FC1 ? MOET_K_FC1 : MOET_K_FC2, st);
-    kern<<<grid, kPfThreads, kPfSmemBytes, st>>>(a, m);
+    MOET_CUDA_TRY(pdl_launch(false, kern, dim3(grid), dim3(kPfThreads), kPfSmemBytes, st, a, m));
   }
   MOET_CUDA_TRY(cudaGetLastError());
   return MOET_OK;
@@ -791,9 +798,9 @@ moet_status pf_forward_fc1(const PfForwardArgs& f, cudaStream_t st) {
   const bool with_delta = f.delta_slot != nullptr && f.gate != nullptr;
   {
     ProfScope ps(MOET_K_TERMS, st);
-    pf_gather_kernel<<<pairs, kGatherThreads, 0, st>>>(pairs, f.k, f.H, f.x, f.perm, with_delta ? f.gate : nullptr, f.topk_idx,
+    MOET_CUDA_TRY(pdl_launch(false, pf_gather_kernel, dim3(pairs), dim3(kGatherThreads), 0, st, pairs, f.k, f.H, f.x, f.perm, with_delta ? f.gate : nullptr, f.topk_idx,
                                            f.n_experts, with_delta ? f.delta_slot : nullptr, f.n_slots, f.xb,
-                                           with_delta ? f.xbg : nullptr);
+                                           with_delta ? f.xbg : nullptr));
   }
   MOET_CUDA_TRY(cudaGetLastError());
   PfArgs a1 = pf_common(f);
@@ -815,9 +822,9 @@ moet_status pf_forward_fc2(const PfForwardArgs& f, cudaStream_t st) {
     const int J = ntt <= kH16MaxThreads ? 1 : ntt <= 2 * kH16MaxThreads ? 2 : 4;
     const int threads = ((ntt + J - 1) / J + 31) / 32 * 32;
     auto kern = J == 1 ? pf_h16_kernel<1> : J == 2 ? pf_h16_kernel<2> : pf_h16_kernel<4>;
-    kern<<<pairs, threads, 0, st>>>(pairs, f.k, f.I, f.h, f.perm, with_delta ? f.gate : nullptr, f.topk_idx,
+    MOET_CUDA_TRY(pdl_launch(false, kern, dim3(pairs), dim3(threads), 0, st, pairs, f.k, f.I, f.h, f.perm, with_delta ? f.gate : nullptr, f.topk_idx,
                                     f.n_experts, with_delta ? f.delta_slot : nullptr, f.n_slots, f.h16,
-                                    with_delta ? f.hg16 : nullptr, f.hscale);
+                                    with_delta ? f.hg16 : nullptr, f.hscale));
   }
   MOET_CUDA_TRY(cudaGetLastError());
   PfArgs a2 = pf_common(f);

@@ -288,6 +288,8 @@ __global__ void __launch_bounds__(kTermThreads) act_terms_kernel(int K, const vo
                                                                 uint8_t* __restrict__ cperm, uint8_t* __restrict__ cnat,
                                                                 uint8_t* __restrict__ sfb, float* __restrict__ gsc,
                                                                 const int32_t* __restrict__ perm, NatRows nr) {
+  pdl_wait();                                  // the previous kernel is complete
+  pdl_trigger();
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
   const size_t srow = (size_t)row;
   const float m = __ldg(rowmax + srow);
@@ -335,6 +337,8 @@ __global__ void __launch_bounds__(256) act_terms_items_kernel(int K, const void*
                                                              uint8_t* __restrict__ cperm, uint8_t* __restrict__ cnat,
                                                              uint8_t* __restrict__ sfb, float* __restrict__ gsc,
                                                              NatRows nr) {
+  pdl_wait();                                  // the previous kernel is complete
+  pdl_trigger();
   const int nb = K / 16;
   const long long total = (long long)__ldg(n_items) * kTcTok * nb;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -465,7 +469,6 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
   // one when a record slot is free), so CTAs that draw units with a delta pass (three times the
   // stages) take fewer; items of delta experts come first in the item list.  The record after a
   // CTA's last unit has nch = -1 and ends every role's loop.
-  const int total_units = a.hdr[0] * a.tiles;
   const int nps = (a.K + kKC - 1) / kKC;        // plane stages per unit
 
   if (tid == 0) {
@@ -485,6 +488,10 @@ __global__ void __launch_bounds__(kWsThreads, 1) fc_tc_kernel(const FcTcArgs a, 
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;");
   const uint32_t tmem = sm.tmem_base;
+  // set-up above overlaps the previous kernel; its outputs are read from here on
+  pdl_wait();
+  pdl_trigger();
+  const int total_units = a.hdr[0] * a.tiles;
 
   if (warp == 0 || warp == 3) {
     // ---------------- producers: warp pw takes the stages g with g % 2 == pw; the
@@ -886,7 +893,7 @@ moet_status launch_fc_tc(const FcTcArgs& a, const moet_planes* pl, const moet_nv
   MOET_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes));
   {
     ProfScope ps(FC1 ? MOET_K_FC1 : MOET_K_FC2, st);
-    kern<<<grid, kWsThreads, kSmemBytes, st>>>(ab, m);
+    MOET_CUDA_TRY(pdl_launch(a.item_rows == 0, kern, dim3(grid), dim3(kWsThreads), kSmemBytes, st, ab, m));
   }
   MOET_CUDA_TRY(cudaGetLastError());
   return MOET_OK;
@@ -928,15 +935,15 @@ moet_status tc_forward_fc1(const TcForwardArgs& f, cudaStream_t st) {
     ProfScope ps(MOET_K_TERMS, st);
     if (f.item_rows) {
       // FC1 input terms of the items' pairs, at item * kTcTok + slot
-      act_terms_items_kernel<true><<<items_grid(), 256, 0, st>>>(f.H, f.x, f.hdr, f.chunks, f.offsets, f.perm, f.k,
+      MOET_CUDA_TRY(pdl_launch(false, act_terms_items_kernel<true>, dim3(items_grid()), dim3(256), 0, st, f.H, f.x, f.hdr, f.chunks, f.offsets, f.perm, f.k,
                                                                  pairs, f.tokmax, f.buf.x_cperm, f.buf.x_cnat,
-                                                                 f.buf.x_sf, f.buf.x_g, nat_rows(f));
+                                                                 f.buf.x_sf, f.buf.x_g, nat_rows(f)));
     } else {
       // each token once, written to the bucketed rows of its k pairs so that a work item's term
       // rows are consecutive
       const dim3 grid(f.T, (f.H / 16 + kTermThreads - 1) / kTermThreads);
-      act_terms_kernel<true><<<grid, kTermThreads, 0, st>>>(f.H, f.x, f.inv, f.k, pairs, f.tokmax, f.buf.x_cperm,
-                                                            f.buf.x_cnat, f.buf.x_sf, f.buf.x_g, f.perm, nat_rows(f));
+      MOET_CUDA_TRY(pdl_launch(true, act_terms_kernel<true>, dim3(grid), dim3(kTermThreads), 0, st, f.H, f.x, f.inv, f.k, pairs, f.tokmax, f.buf.x_cperm,
+                                                            f.buf.x_cnat, f.buf.x_sf, f.buf.x_g, f.perm, nat_rows(f)));
     }
   }
   MOET_CUDA_TRY(cudaGetLastError());
@@ -956,16 +963,16 @@ moet_status tc_forward_fc2(const TcForwardArgs& f, cudaStream_t st) {
   {
     ProfScope ps(MOET_K_TERMS, st);
     if (f.item_rows) {
-      act_terms_items_kernel<false><<<items_grid(), 256, 0, st>>>(f.I, f.h, f.hdr, f.chunks, f.offsets, f.perm, f.k,
+      MOET_CUDA_TRY(pdl_launch(false, act_terms_items_kernel<false>, dim3(items_grid()), dim3(256), 0, st, f.I, f.h, f.hdr, f.chunks, f.offsets, f.perm, f.k,
                                                                   pairs, reinterpret_cast<const float*>(f.hmax),
                                                                   f.buf.h_cperm, f.buf.h_cnat, f.buf.h_sf, f.buf.h_g,
-                                                                  nat_rows(f));
+                                                                  nat_rows(f)));
     } else {
       // one row per bucketed pair (h rows are in bucketed order)
       const dim3 grid(pairs, (f.I / 16 + kTermThreads - 1) / kTermThreads);
-      act_terms_kernel<false><<<grid, kTermThreads, 0, st>>>(f.I, f.h, nullptr, 1, pairs,
+      MOET_CUDA_TRY(pdl_launch(true, act_terms_kernel<false>, dim3(grid), dim3(kTermThreads), 0, st, f.I, f.h, nullptr, 1, pairs,
                                                              reinterpret_cast<const float*>(f.hmax), f.buf.h_cperm,
-                                                             f.buf.h_cnat, f.buf.h_sf, f.buf.h_g, f.perm, nat_rows(f));
+                                                             f.buf.h_cnat, f.buf.h_sf, f.buf.h_g, f.perm, nat_rows(f)));
     }
   }
   MOET_CUDA_TRY(cudaGetLastError());

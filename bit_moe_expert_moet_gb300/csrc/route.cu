@@ -84,6 +84,8 @@ template <int VPL>
 __global__ void __launch_bounds__(256) topk_kernel(int T, int E, int k, const float* __restrict__ logits,
                                                    int32_t* __restrict__ topk_idx,
                                                    float* __restrict__ topk_w) {
+  pdl_wait();                                  // the previous kernel is complete
+  pdl_trigger();
   const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   if (t < T) topk_one_token<VPL>(t, E, k, logits, topk_idx, topk_w);
 }
@@ -96,6 +98,8 @@ __global__ void __launch_bounds__(1024) bucket_kernel(int T, int E, int k, const
                                                       float* __restrict__ topk_w,
                                                       int32_t* __restrict__ offsets,
                                                       int32_t* __restrict__ perm) {
+  pdl_wait();                                  // the previous kernel is complete
+  pdl_trigger();
   extern __shared__ int smem[];
   int* counts = smem;                               // [E]
   int* base = smem + E;                             // [E]
@@ -177,6 +181,8 @@ constexpr int kBucketMultiPairs = 4096;
 
 __global__ void __launch_bounds__(1024) bucket_offsets_kernel(int n, int E, const int32_t* __restrict__ topk_idx,
                                                                int32_t* __restrict__ offsets) {
+  pdl_wait();                                  // the previous kernel is complete
+  pdl_trigger();
   __shared__ int counts[1024];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int i = tid; i < E; i += 1024) counts[i] = 0;
@@ -211,6 +217,8 @@ __global__ void __launch_bounds__(1024) bucket_offsets_kernel(int n, int E, cons
 __global__ void __launch_bounds__(1024) bucket_scatter_kernel(int n, int E, const int32_t* __restrict__ topk_idx,
                                                                const int32_t* __restrict__ offsets,
                                                                int32_t* __restrict__ perm) {
+  pdl_wait();                                  // the previous kernel is complete
+  pdl_trigger();
   extern __shared__ int smem[];
   int* base = smem;                                   // [E]
   unsigned char* wc = (unsigned char*)(smem + E);     // [32][E]
@@ -259,34 +267,34 @@ static moet_status launch_route(int T, int E, int k, const float* logits, int32_
     auto kern = bucket_kernel<VPL, true>;
     if (smem > 48 * 1024) MOET_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     ProfScope ps(MOET_K_ROUTE, st);
-    kern<<<1, 1024, smem, st>>>(T, E, k, logits, idx, w, offsets, perm);
+    MOET_CUDA_TRY(pdl_launch(true, kern, dim3(1), dim3(1024), smem, st, T, E, k, logits, idx, w, offsets, perm));
   } else if ((long long)T * k > kBucketMultiPairs) {
     {
       ProfScope ps(MOET_K_ROUTE, st);
-      topk_kernel<VPL><<<(T + 7) / 8, 256, 0, st>>>(T, E, k, logits, idx, w);
+      MOET_CUDA_TRY(pdl_launch(false, topk_kernel<VPL>, dim3((T + 7) / 8), dim3(256), 0, st, T, E, k, logits, idx, w));
     }
     MOET_CUDA_TRY(cudaGetLastError());
     const int n = T * k;
     {
       ProfScope ps(MOET_K_ROUTE, st);
-      bucket_offsets_kernel<<<1, 1024, 0, st>>>(n, E, idx, offsets);
+      MOET_CUDA_TRY(pdl_launch(false, bucket_offsets_kernel, dim3(1), dim3(1024), 0, st, n, E, idx, offsets));
     }
     MOET_CUDA_TRY(cudaGetLastError());
     const size_t ssmem = (size_t)E * 4 + (size_t)E * 32;
     if (ssmem > 48 * 1024)
       MOET_CUDA_TRY(cudaFuncSetAttribute(bucket_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem));
     ProfScope ps(MOET_K_ROUTE, st);
-    bucket_scatter_kernel<<<(n + 1023) / 1024, 1024, ssmem, st>>>(n, E, idx, offsets, perm);
+    MOET_CUDA_TRY(pdl_launch(false, bucket_scatter_kernel, dim3((n + 1023) / 1024), dim3(1024), ssmem, st, n, E, idx, offsets, perm));
   } else {
     {
       ProfScope ps(MOET_K_ROUTE, st);
-      topk_kernel<VPL><<<(T + 7) / 8, 256, 0, st>>>(T, E, k, logits, idx, w);
+      MOET_CUDA_TRY(pdl_launch(true, topk_kernel<VPL>, dim3((T + 7) / 8), dim3(256), 0, st, T, E, k, logits, idx, w));
     }
     MOET_CUDA_TRY(cudaGetLastError());
     auto kern = bucket_kernel<VPL, false>;
     if (smem > 48 * 1024) MOET_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     ProfScope ps(MOET_K_ROUTE, st);
-    kern<<<1, 1024, smem, st>>>(T, E, k, logits, idx, w, offsets, perm);
+    MOET_CUDA_TRY(pdl_launch(true, kern, dim3(1), dim3(1024), smem, st, T, E, k, logits, idx, w, offsets, perm));
   }
   MOET_CUDA_TRY(cudaGetLastError());
   return MOET_OK;
