@@ -16,8 +16,9 @@
  *  - Every call is asynchronous on `stream` and returns after enqueueing.
  *    Host-side argument checks run first and nothing is enqueued when one
  *    fails.  No entry point synchronises, except moet_last_device_error.
- *    Stream order holds as usual: some kernels (routing and the forward of
- *    up to 512 tokens) are launched with programmatic stream serialization,
+ *    Stream order holds as usual: some kernels (routing of up to 4096 pairs,
+ *    the forward's block-scaled engine for up to 512 tokens) are launched
+ *    with programmatic stream serialization,
  *    so they may be scheduled while the previous kernel on `stream` still
  *    runs, but each waits for that kernel's completion before its first
  *    access to global memory.
