@@ -240,8 +240,11 @@ def _gpu_route(moet, logits, k):
 
 @pytest.mark.parametrize("T,E,k", [(1, 256, 8), (4, 8, 2), (37, 64, 6), (64, 256, 8), (512, 384, 8),
                                    (513, 256, 8), (4096, 256, 8), (256, 1024, 16), (100, 16, 1), (9, 33, 5),
-                                   (700, 64, 7), (3000, 1024, 16)])
+                                   (700, 64, 7), (3000, 1024, 16), (16, 1024, 16), (15, 100, 15), (16, 7, 7)])
 def test_route_bit_exact(moet, T, E, k):
+    """Every routing path: up to 16 tokens in one CTA with the counting bucketing (at its 256-pair
+    limit, with a pair count that needs padding, and with every expert chosen by every token),
+    the two-kernel path up to 4096 pairs, the multi-CTA path beyond."""
     rng = np.random.default_rng(T * 1000 + E)
     logits = rng.standard_normal((T, E)).astype(np.float32)
     logits[:, 1] = logits[:, 2]                   # ties -> lower id
